@@ -1,0 +1,161 @@
+"""fp64 CPU oracle for diagonal-decay gated linear attention (test infrastructure).
+
+Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` use this package.  The CUDA library never imports, links or
+calls it, and it shares no code with the library.
+
+* ``gla_fwd`` / ``gla_bwd`` wrap the plain C token recurrence and its
+  brute-force adjoint in ``oracle.c`` (fp64, pthreads).
+* ``chunked.py`` holds the segmented/chunked fp64 form written from the ZeCO
+  pages, used only to pin the recurrence against the pages' decomposition.
+
+Parity status: every function here is pinned by the ``-m "not gpu"`` tests
+(hand-worked cases, the alpha=1 causal-attention special case, a closed form,
+the chunked form, central finite differences, and the dlog_alpha identity),
+and planted mistakes in copies of oracle.c are each caught by those pins.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_SO = os.path.join(_BUILD, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c with gcc into oracle/_build/liboracle.so (portable flags)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < os.path.getmtime(_SRC):
+        tmp = _SO + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-fPIC", "-shared", "-std=c11", "-fno-fast-math", "-pthread", _SRC,
+               "-o", tmp, "-lm"]
+        subprocess.check_call(cmd)
+        os.replace(tmp, _SO)
+    return _SO
+
+
+def configure(lib):
+    """Declare the argument types of a loaded oracle library and return it."""
+    i64, dp, ip = ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p
+    lib.oracle_gla_fwd.argtypes = [i64] * 5 + [dp] * 5 + [i64, ip, dp, dp, ctypes.c_int]
+    lib.oracle_gla_fwd.restype = ctypes.c_int
+    lib.oracle_gla_bwd.argtypes = ([i64] * 5 + [dp] * 7 + [i64, ip, dp, dp, dp, dp] +
+                                   [i64, ip, dp, ctypes.c_int])
+    lib.oracle_gla_bwd.restype = ctypes.c_int
+    return lib
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            _lib = configure(ctypes.CDLL(build()))
+    return _lib
+
+
+def default_threads() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+def _f64(x):
+    if x is None:
+        return None
+    if hasattr(x, "detach"):  # torch tensor
+        x = x.detach().to("cpu").double().numpy()
+    return np.ascontiguousarray(x, dtype=np.float64)
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _idx(ix):
+    if ix is None:
+        return None
+    return np.ascontiguousarray(np.asarray(ix, dtype=np.int64))
+
+
+def gla_fwd(q, k, v, log_alpha, S0=None, cols=None, nthreads=None):
+    """Token-recurrence forward in fp64.
+
+    Returns ``(o, S_final)`` with ``o`` [B,H,T,ncols] and ``S_final``
+    [B,H,dk,ncols]; ``cols`` selects d_v columns (None: all).
+    """
+    q, k, v, g, S0 = _f64(q), _f64(k), _f64(v), _f64(log_alpha), _f64(S0)
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    assert k.shape == q.shape == g.shape and v.shape == (B, H, T, dv)
+    if S0 is not None:
+        assert S0.shape == (B, H, dk, dv)
+    cols = _idx(cols)
+    nc = dv if cols is None else len(cols)
+    o = np.zeros((B, H, T, nc))
+    sf = np.zeros((B, H, dk, nc))
+    rc = _load().oracle_gla_fwd(B, H, T, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(S0),
+                                nc, _ptr(cols), _ptr(o), _ptr(sf),
+                                nthreads or default_threads())
+    if rc != 0:
+        raise RuntimeError(f"oracle_gla_fwd failed ({rc})")
+    return o, sf
+
+
+def gla_bwd(q, k, v, log_alpha, S0, do, dS_final, rows=None, cols=None, nthreads=None,
+            want_rows=True, want_cols=True):
+    """Brute-force adjoint in fp64.
+
+    Returns a dict: ``dq``, ``dk``, ``dlog_alpha`` [B,H,T,nrows], ``dS0``
+    [B,H,nrows,dv] for the selected d_k rows, and ``dv`` [B,H,T,ncols] for the
+    selected d_v columns (None: all rows / all columns).
+    """
+    q, k, v, g = _f64(q), _f64(k), _f64(v), _f64(log_alpha)
+    S0, do, dSf = _f64(S0), _f64(do), _f64(dS_final)
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    rows, cols = _idx(rows), _idx(cols)
+    nr = (dk if rows is None else len(rows)) if want_rows else 0
+    nc = (dv if cols is None else len(cols)) if want_cols else 0
+    dq = np.zeros((B, H, T, nr))
+    dk_ = np.zeros((B, H, T, nr))
+    dg = np.zeros((B, H, T, nr))
+    dS0 = np.zeros((B, H, nr, dv))
+    dv_ = np.zeros((B, H, T, nc))
+    rc = _load().oracle_gla_bwd(B, H, T, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(S0),
+                                _ptr(do), _ptr(dSf), nr, _ptr(rows), _ptr(dq), _ptr(dk_),
+                                _ptr(dg), _ptr(dS0), nc, _ptr(cols), _ptr(dv_),
+                                nthreads or default_threads())
+    if rc != 0:
+        raise RuntimeError(f"oracle_gla_bwd failed ({rc})")
+    return dict(dq=dq, dk=dk_, dlog_alpha=dg, dS0=dS0, dv=dv_)
+
+
+def boundary_states(q, k, v, log_alpha, S0, P, nthreads=None):
+    """States entering each segment: S_in[p] = state after token p*L-1 (S_in[0] = S0).
+
+    Returns [B,H,P+1,dk,dv]; S_in[P] is S_final.  Computed with the plain
+    recurrence on prefixes, so it is independent of any chunked evaluation.
+    """
+    q, k, v, g, S0 = _f64(q), _f64(k), _f64(v), _f64(log_alpha), _f64(S0)
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    L = T // P
+    out = np.zeros((B, H, P + 1, dk, dv))
+    out[:, :, 0] = 0.0 if S0 is None else S0
+    S = S0
+    for p in range(P):
+        sl = slice(p * L, (p + 1) * L)
+        _, S = gla_fwd(q[:, :, sl], k[:, :, sl], v[:, :, sl], g[:, :, sl], S,
+                       nthreads=nthreads)
+        out[:, :, p + 1] = S
+    return out
