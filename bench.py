@@ -1,0 +1,449 @@
+"""Throughput of segmented GLA forward+backward on one GB300 (per rank).
+
+Workload (default): the 1M-token, 64-segment forward+backward --
+B=1, H=4, T=1,048,576, P=64 (L=16,384), C=64, K=8, d_k=256, d_v=512, bf16 I/O,
+fp32 accumulation, synthetic inputs from workloads.py.  One step is one
+zeco_gla_fwd plus one zeco_gla_bwd over the whole batch (every kernel of the
+path).  Inputs (14 GiB) are far larger than the 126 MB L2, so no L2 flush is
+needed between steps.
+
+Timing: W untimed warm-up steps, then K timed steps bracketed by a barrier and
+torch.cuda.synchronize() on both sides, CUDA events on the library's stream,
+maximum over ranks.  N > 1 (torchrun) runs N independent replicas, one per GPU
+(weak scaling; the path has no cross-GPU exchange in this build).
+
+`--impl reference` times the fp64 CPU oracle instead, on a bounded sample of
+the same workload, on this host's cores.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "GLA fwd+bwd tokens/sec on 1 GB300 and % of roofline (1M tok, P=64)"
+
+# Algorithmic HBM bytes per token per head (bf16, d_k=256, d_v=512), per kernel.
+# Inputs read once and outputs written once; segment states counted per token
+# as state_bytes / L.  The ZeCO operator total (fwd 5632 + bwd 8192 B per
+# token-head, plus segment states) is the roofline denominator of the step.
+E = 2  # bytes per bf16 element
+
+
+def kernel_bytes_per_token(dk, dv, L, e=E):
+    st = dk * dv * 4 / L  # one fp32 state per segment, per token
+    return {
+        # pass 1: read k, v, g; write one local state per segment
+        "chunk_state": e * (2 * dk + dv) + st,
+        "seg_scan_fwd": 2 * st,
+        # pass 2: read q, k, v, g and S_in[p]; write o
+        "fwd_out": e * (3 * dk + 2 * dv) + st,
+        # bwd pre-pass: read q, do, g; write one adjoint state per segment
+        "dstate_local": e * (2 * dk + dv) + st,
+        "seg_scan_rev": 3 * st,
+        # dv: read q, k, g, do and D[p+1]; write dv
+        "bwd_dv": e * (3 * dk + 2 * dv) + st,
+        # dq, dk, dg: read q, k, v, g, do, S_in[p], D[p+1]; write dq, dk, dg
+        "bwd_dqk": e * (3 * dk + 2 * dv) + e * 3 * dk + 2 * st,
+    }
+
+
+def zeco_operator_bytes_per_token(dk, dv, L, e=E):
+    """ZeCO two-pass algorithmic bytes per token-head (fwd + bwd + segment states)."""
+    fwd = e * (5 * dk + 3 * dv)
+    bwd = e * (8 * dk + 4 * dv)
+    states = (16 + 20) * dk * dv / L
+    return fwd + bwd + states
+
+
+def zeco_operator_flops_per_token(dk, dv, C):
+    fwd = 2 * C * (dk + dv) + 6 * dk * dv
+    bwd = 2 * C * (3 * dk + 2 * dv) + 12 * dk * dv
+    return fwd + bwd
+
+
+def canonical_kernel(name):
+    for key in ("chunk_state", "seg_scan_fwd", "fwd_out", "dstate_local", "seg_scan_rev",
+                "bwd_dv", "bwd_dqk"):
+        if key in name:
+            return key
+    return name
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "sm_max_mhz": 2070.0}, "fallback"
+
+
+# ------------------------------------------------------------ clocks sampler
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.t:
+            self.t.join(timeout=2)
+        sm, smax, reasons, power = [], None, set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        sm.sort()
+        med = sm[len(sm) // 2] if sm else None
+        return {"sm_mhz": med, "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(power) if power else None}
+
+
+# ------------------------------------------------------------- distributed
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(elapsed_s_max: float, tokens_per_rank_step: int, steps: int, world: int):
+    """Whole-job throughput: tokens processed by all ranks / the slowest rank's time."""
+    total = tokens_per_rank_step * steps * world
+    return total / elapsed_s_max, elapsed_s_max * 1e3 / steps
+
+
+# ------------------------------------------------------------- CPU oracle leg
+
+
+def cpu_oracle_sample(w, sample_tokens, nthreads=None):
+    """Time the fp64 oracle (fwd + full bwd) on the first `sample_tokens` tokens of
+    every head of batch 0.  Returns tokens/s in the workload's unit and details."""
+    import oracle
+    x = workloads.make_inputs(w.replace(T=sample_tokens, P=1, B=1), device="cpu")
+    nt = nthreads or oracle.default_threads()
+    t0 = time.perf_counter()
+    oracle.gla_fwd(x["q"], x["k"], x["v"], x["log_alpha"], x["S0"], nthreads=nt)
+    oracle.gla_bwd(x["q"], x["k"], x["v"], x["log_alpha"], x["S0"], x["do"], x["dS_final"],
+                   nthreads=nt)
+    dt = time.perf_counter() - t0
+    # all H heads of the sample were processed: the sample covers sample_tokens tokens
+    return sample_tokens / dt, dt, nt
+
+
+# ---------------------------------------------------------------- main
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return 0
+    w = workloads.BY_NAME[args.workload]
+    sample = args.ref_sample_tokens
+    vals = []
+    nt = None
+    for _ in range(args.warmup):
+        pass  # the oracle has no warm-up state worth timing
+    t_all = 0.0
+    for _ in range(args.steps):
+        v, dt, nt = cpu_oracle_sample(w, sample)
+        vals.append(v)
+        t_all += dt
+    value = sum(vals) / len(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * w.tokens / value, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "dk": w.dk, "dv": w.dv,
+                   "P": w.P, "K": w.K, "C": w.C},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": nt, "kind": "oracle",
+                         "sample": f"batch 0, all {w.H} heads, first {sample} tokens, fp64 "
+                                   f"recurrence fwd + brute-force adjoint bwd, per step"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default=workloads.LONG_FWDBWD.name)
+    ap.add_argument("--path", default="auto", choices=["auto", "simt", "tc"])
+    ap.add_argument("--e2e-steps", type=int, default=2)
+    ap.add_argument("--cpu-sample-tokens", type=int, default=16384)
+    ap.add_argument("--ref-sample-tokens", type=int, default=4096)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl != "reference":
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        rc = run_reference(args, world, rank)
+        return rc
+
+    import chunked_state_scan_gb300 as z
+    z.load_library()
+    w = workloads.BY_NAME[args.workload]
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.Stream(device=dev)
+    x = workloads.make_inputs(w, device=dev)
+    shape = z.make_shape(w.B, w.H, w.T, w.dk, w.dv, w.P, w.K, w.C, w.dtype, args.path)
+    path = z.resolve_path(shape)
+    # outputs and buffers, allocated once (the library itself never allocates)
+    o = torch.empty_like(x["v"])
+    S_final = torch.empty_like(x["S0"])
+    saved = torch.empty(z.saved_bytes(shape), dtype=torch.uint8, device=dev)
+    ws = torch.empty(max(z.workspace_bytes(shape, True), 16), dtype=torch.uint8, device=dev)
+    grads = dict(dq=torch.empty_like(x["q"]), dk=torch.empty_like(x["k"]),
+                 dv=torch.empty_like(x["v"]), dlog_alpha=torch.empty_like(x["log_alpha"]),
+                 dS0=torch.empty_like(x["S0"]))
+
+    def step(xx):
+        z.zeco_gla_fwd(xx["q"], xx["k"], xx["v"], xx["log_alpha"], xx["S0"], P=w.P, K=w.K,
+                       C=w.C, path=args.path, o=o, S_final=S_final, saved=saved, stream=stream)
+        if w.bwd:
+            z.zeco_gla_bwd(xx["q"], xx["k"], xx["v"], xx["log_alpha"], saved, xx["do"],
+                           xx["dS_final"], P=w.P, K=w.K, C=w.C, path=args.path, grads=grads,
+                           workspace=ws, stream=stream)
+
+    torch.cuda.synchronize(dev)
+    for _ in range(args.warmup):
+        step(x)
+    torch.cuda.synchronize(dev)
+
+    # ---- per-kernel durations (library-recorded events on the same stream)
+    lib = z.load_library()
+    n_ev = 16
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
+    with torch.cuda.stream(stream):
+        for e in evs:
+            e.record(stream)  # materialise the handles
+    torch.cuda.synchronize(dev)
+    handles = (ctypes.c_void_p * n_ev)(*[e.cuda_event for e in evs])
+    per_kernel = {}
+    prof_steps = 2
+    for _ in range(prof_steps):
+        lib.zeco_set_profile_events.argtypes = [ctypes.c_void_p, ctypes.c_int]
+        lib.zeco_set_profile_events(ctypes.cast(handles, ctypes.c_void_p), n_ev)
+        step(x)
+        n = lib.zeco_profile_event_count()
+        names = []
+        lib.zeco_profile_kernel_name.restype = ctypes.c_char_p
+        for i in range(n):
+            names.append(lib.zeco_profile_kernel_name(i).decode())
+        lib.zeco_set_profile_events(None, 0)
+        torch.cuda.synchronize(dev)
+        for i in range(1, n):
+            per_kernel.setdefault(names[i], []).append(evs[i - 1].elapsed_time(evs[i]))
+    # event 0 is recorded before the forward's first kernel; the backward's first
+    # kernel is timed from the forward's last kernel (same stream, back to back)
+    kern_ms = {k: sum(v) / len(v) for k, v in per_kernel.items()}
+    launches_per_step = len(kern_ms)
+
+    # ---- timed region
+    clocks = ClockSampler(torch.cuda.current_device() if world == 1 else local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step(x)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clk = clocks.stop()
+    elapsed = e0.elapsed_time(e1) / 1e3
+    elapsed_max = max_over_ranks(elapsed, world)
+    value, ms_step = aggregate(elapsed_max, w.tokens, args.steps, world)
+
+    # ---- roofline of the dominant kernel and of the whole step
+    peaks, peak_kind = load_peaks()
+    hbm_peak = float(peaks["hbm_gbs"])
+    bh = w.B * w.H
+    kb = kernel_bytes_per_token(w.dk, w.dv, w.L)
+    dom = max(kern_ms, key=kern_ms.get)
+    dom_key = canonical_kernel(dom)
+    dom_bytes = kb.get(dom_key, 0.0) * w.T * bh
+    dom_gbs = dom_bytes / (kern_ms[dom] * 1e-3) / 1e9
+    op_bytes = zeco_operator_bytes_per_token(w.dk, w.dv, w.L) * w.T * bh
+    op_flops = zeco_operator_flops_per_token(w.dk, w.dv, w.C) * w.T * bh
+    t_roof = max(op_bytes / (hbm_peak * 1e9), op_flops / (float(peaks["bf16_tflops"]) * 1e12))
+    step_s = ms_step * 1e-3
+    traffic = None
+    tr_path = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tr_path):
+        try:
+            with open(tr_path) as f:
+                tr = json.load(f)
+            ent = tr.get(f"{path}:{dom}")
+            if ent:
+                traffic = ent
+        except (OSError, ValueError):
+            traffic = None
+    scan_ms = sum(v for k, v in kern_ms.items() if "seg_scan" in k)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic (seeded; shapes and distributions of the GLA-1B layer workload)",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "dk": w.dk, "dv": w.dv,
+                   "P": w.P, "K": w.K, "C": w.C, "path": path,
+                   "l2": "no flush: inputs 14 GiB >> 126 MB L2",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": dom_gbs, "peak": hbm_peak,
+                     "unit": "GB/s", "frac": dom_gbs / hbm_peak, "traffic": traffic,
+                     "peak_source": f"{peak_kind} hbm_gbs",
+                     "algorithmic_bytes_per_launch": dom_bytes},
+        "operator_roofline": {"bytes": op_bytes, "flops": op_flops, "t_roof_ms": t_roof * 1e3,
+                              "frac": t_roof / step_s,
+                              "note": "ZeCO two-pass algorithmic bytes/flops per step vs "
+                                      f"{peak_kind} peaks"},
+        "kernels_ms": kern_ms, "scan_share": scan_ms / sum(kern_ms.values()),
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+    }
+
+    # ---- end to end through the public API with host buffers
+    if not args.no_e2e and w.bwd:
+        names_in = ["q", "k", "v", "log_alpha", "do", "dS_final", "S0"]
+        host_in = {n: x[n].cpu().pin_memory() for n in names_in}
+        outs = [o, S_final] + [grads[n] for n in ("dq", "dk", "dv", "dlog_alpha", "dS0")]
+        host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+        dev_in = {n: torch.empty_like(x[n]) for n in names_in}
+        del x
+        bi = sum(t.numel() * t.element_size() for t in host_in.values())
+        bo = sum(t.numel() * t.element_size() for t in host_out)
+
+        def e2e_step():
+            with torch.cuda.stream(stream):
+                for n in names_in:
+                    dev_in[n].copy_(host_in[n], non_blocking=True)
+                step(dev_in)
+                for h, t in zip(host_out, outs):
+                    h.copy_(t, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        t0 = time.perf_counter()
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        t1 = time.perf_counter()
+        barrier(world)
+        el = max_over_ranks(t1 - t0, world)
+        ev, _ = aggregate(el, w.tokens, args.e2e_steps, world)
+        line["e2e"] = {"value": ev, "unit": "tokens/s", "h2d_bytes_per_step": bi,
+                       "d2h_bytes_per_step": bo, "steps": args.e2e_steps}
+
+    # ---- CPU baseline (rank 0 only, N = 1 only)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, dt, nt = cpu_oracle_sample(w, args.cpu_sample_tokens)
+        line["cpu_baseline"] = {
+            "value": v, "unit": "tokens/s", "cores": nt, "kind": "oracle",
+            "sample": f"batch 0, all {w.H} heads, first {args.cpu_sample_tokens} tokens: fp64 "
+                      f"token recurrence fwd + brute-force adjoint bwd ({dt:.1f} s)"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,160 @@
+"""Segmented (ZeCO-style) gated linear attention on one GB300 -- Python binding.
+
+This module only marshals arguments: it allocates outputs with PyTorch on the
+current CUDA device and calls the C ABI of libzeco_gla.so (declared in
+include/zeco_gla.h) on the current stream.  Every step of the computation runs
+in the library's CUDA kernels.  There is no CPU or PyTorch fallback: if the
+library is not built, or no GPU is present, the calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libzeco_gla.so")
+
+ZECO_OK, ZECO_ERR_ARG, ZECO_ERR_UNSUPPORTED, ZECO_ERR_WORKSPACE, ZECO_ERR_CUDA = 0, -1, -2, -3, -4
+ZECO_F32, ZECO_BF16 = 0, 1
+PATH_AUTO, PATH_SIMT, PATH_TC = 0, 1, 2
+_PATHS = {"auto": PATH_AUTO, "simt": PATH_SIMT, "tc": PATH_TC}
+
+EXPORTED = ["zeco_gla_saved_bytes", "zeco_gla_workspace_bytes", "zeco_gla_fwd", "zeco_gla_bwd",
+            "zeco_strerror", "zeco_gla_resolve_path"]
+
+
+class ZecoShape(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int64), ("H", ctypes.c_int64), ("T", ctypes.c_int64),
+                ("dk", ctypes.c_int64), ("dv", ctypes.c_int64), ("P", ctypes.c_int32),
+                ("K", ctypes.c_int32), ("C", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("path", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+class ZecoError(RuntimeError):
+    def __init__(self, code, msg):
+        super().__init__(f"{msg} (code {code})")
+        self.code = code
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load_library(path: str = LIB_PATH):
+    """Load libzeco_gla.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    f"CUDA library not built: {path} is missing "
+                    "(run `python -c 'import __graft_entry__ as g; g.build()'`)")
+            lib = ctypes.CDLL(path)
+            vp, sz, sp = ctypes.c_void_p, ctypes.c_size_t, ctypes.POINTER(ZecoShape)
+            lib.zeco_gla_saved_bytes.argtypes = [sp]
+            lib.zeco_gla_saved_bytes.restype = sz
+            lib.zeco_gla_workspace_bytes.argtypes = [sp, ctypes.c_int]
+            lib.zeco_gla_workspace_bytes.restype = sz
+            lib.zeco_gla_fwd.argtypes = [sp] + [vp] * 8 + [vp, sz, vp]
+            lib.zeco_gla_fwd.restype = ctypes.c_int
+            lib.zeco_gla_bwd.argtypes = [sp] + [vp] * 12 + [vp, sz, vp]
+            lib.zeco_gla_bwd.restype = ctypes.c_int
+            lib.zeco_strerror.argtypes = [ctypes.c_int]
+            lib.zeco_strerror.restype = ctypes.c_char_p
+            lib.zeco_gla_resolve_path.argtypes = [sp]
+            lib.zeco_gla_resolve_path.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def make_shape(B, H, T, dk, dv, P, K, C, dtype, path="auto") -> ZecoShape:
+    if isinstance(dtype, torch.dtype):
+        dt = ZECO_BF16 if dtype == torch.bfloat16 else ZECO_F32
+    else:
+        dt = ZECO_BF16 if dtype in ("bf16", ZECO_BF16) else ZECO_F32
+    return ZecoShape(B, H, T, dk, dv, P, K, C, dt, _PATHS.get(path, path), 0)
+
+
+def _check(rc):
+    if rc != ZECO_OK:
+        raise ZecoError(rc, load_library().zeco_strerror(rc).decode())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_ptr(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def saved_bytes(shape: ZecoShape) -> int:
+    return load_library().zeco_gla_saved_bytes(ctypes.byref(shape))
+
+
+def workspace_bytes(shape: ZecoShape, bwd: bool) -> int:
+    return load_library().zeco_gla_workspace_bytes(ctypes.byref(shape), int(bwd))
+
+
+def resolve_path(shape: ZecoShape) -> str:
+    rc = load_library().zeco_gla_resolve_path(ctypes.byref(shape))
+    if rc < 0:
+        _check(rc)
+    return {PATH_SIMT: "simt", PATH_TC: "tc"}[rc]
+
+
+def _shape_of(q, v, P, K, C, path):
+    B, H, T, dk = q.shape
+    return make_shape(B, H, T, dk, v.shape[-1], P, K, C, q.dtype, path)
+
+
+def zeco_gla_fwd(q, k, v, log_alpha, S0=None, *, P, K, C, path="auto", o=None, S_final=None,
+                 saved=None, stream=None, want_S_final=True):
+    """Forward through the C ABI.  Returns (o, S_final or None, saved).
+
+    q, k, log_alpha: [B,H,T,dk]; v: [B,H,T,dv] (fp32 or bf16, CUDA, contiguous);
+    S0: [B,H,dk,dv] fp32 or None (zeros).  ``saved`` must be passed to the backward.
+    """
+    shape = _shape_of(q, v, P, K, C, path)
+    dev = q.device
+    if o is None:
+        o = torch.empty(v.shape, dtype=v.dtype, device=dev)
+    if want_S_final and S_final is None:
+        S_final = torch.empty(q.shape[0], q.shape[1], q.shape[-1], v.shape[-1],
+                              dtype=torch.float32, device=dev)
+    if saved is None:
+        saved = torch.empty(max(saved_bytes(shape), 16), dtype=torch.uint8, device=dev)
+    nws = workspace_bytes(shape, False)
+    ws = torch.empty(nws, dtype=torch.uint8, device=dev) if nws else None
+    rc = load_library().zeco_gla_fwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v),
+                                     _ptr(log_alpha), _ptr(S0), _ptr(o), _ptr(S_final),
+                                     _ptr(saved), _ptr(ws), nws, _stream_ptr(stream))
+    _check(rc)
+    return o, S_final, saved
+
+
+def zeco_gla_bwd(q, k, v, log_alpha, saved, do, dS_final=None, *, P, K, C, path="auto",
+                 grads=None, workspace=None, stream=None, want_dS0=True):
+    """Backward through the C ABI.  Returns dict(dq, dk, dv, dlog_alpha, dS0)."""
+    shape = _shape_of(q, v, P, K, C, path)
+    dev = q.device
+    if grads is None:
+        grads = dict(dq=torch.empty_like(q), dk=torch.empty_like(k), dv=torch.empty_like(v),
+                     dlog_alpha=torch.empty_like(log_alpha))
+        if want_dS0:
+            grads["dS0"] = torch.empty(q.shape[0], q.shape[1], q.shape[-1], v.shape[-1],
+                                       dtype=torch.float32, device=dev)
+    nws = workspace_bytes(shape, True)
+    if workspace is None:
+        workspace = torch.empty(max(nws, 16), dtype=torch.uint8, device=dev)
+    rc = load_library().zeco_gla_bwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v),
+                                     _ptr(log_alpha), _ptr(saved), _ptr(do), _ptr(dS_final),
+                                     _ptr(grads["dq"]), _ptr(grads["dk"]), _ptr(grads["dv"]),
+                                     _ptr(grads["dlog_alpha"]), _ptr(grads.get("dS0")),
+                                     _ptr(workspace), workspace.numel(), _stream_ptr(stream))
+    _check(rc)
+    return grads

@@ -1,0 +1,190 @@
+// api.cu -- the C ABI: argument checks, buffer layout, and the launch sequence.
+#include <stdint.h>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace {
+
+using zeco::Dims;
+
+// Per-thread profiling state (zeco_set_profile_events).
+constexpr int kMaxProf = 256;
+struct ProfState {
+  void* const* events = nullptr;
+  int cap = 0;
+  int count = 0;
+  const char* names[kMaxProf] = {};
+};
+thread_local ProfState g_prof;
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+// Shape checks.  Returns ZECO_OK and fills d, or an error code.
+int check_shape(const zeco_shape* s, Dims* d) {
+  if (!s) return ZECO_ERR_ARG;
+  if (s->B < 1 || s->H < 1 || s->T < 1 || s->dk < 1 || s->dv < 1 || s->P < 1 || s->K < 1 ||
+      s->C < 1)
+    return ZECO_ERR_ARG;
+  if (s->dtype != ZECO_F32 && s->dtype != ZECO_BF16) return ZECO_ERR_ARG;
+  if (s->path < ZECO_PATH_AUTO || s->path > ZECO_PATH_TC) return ZECO_ERR_ARG;
+  if (s->T % s->P != 0 || s->dk % s->K != 0) return ZECO_ERR_ARG;
+  const int64_t L = s->T / s->P;
+  if (L % s->C != 0) return ZECO_ERR_ARG;
+  if (s->C != 16 && s->C != 32 && s->C != 64 && s->C != 128) return ZECO_ERR_UNSUPPORTED;
+  if (s->dk % 16 != 0 || s->dk > 256) return ZECO_ERR_UNSUPPORTED;
+  if (s->dv % 32 != 0 || s->dv > 512) return ZECO_ERR_UNSUPPORTED;
+  if (s->B * s->H * s->P > 65535LL) return ZECO_ERR_UNSUPPORTED;  // grid y/z limit
+  d->B = s->B;
+  d->H = s->H;
+  d->T = s->T;
+  d->dk = s->dk;
+  d->dv = s->dv;
+  d->P = s->P;
+  d->K = s->K;
+  d->C = s->C;
+  d->L = L;
+  d->bf16 = s->dtype == ZECO_BF16;
+  return ZECO_OK;
+}
+
+int resolve(const zeco_shape* s, const Dims& d) {
+  const bool tc = zeco::tc_supported(d);
+  if (s->path == ZECO_PATH_TC) return tc ? (int)ZECO_PATH_TC : (int)ZECO_ERR_UNSUPPORTED;
+  if (s->path == ZECO_PATH_AUTO && tc) return ZECO_PATH_TC;
+  // SIMT: shared memory must fit one CTA
+  if (zeco::simt_smem_bytes(d) > 227 * 1024) return ZECO_ERR_UNSUPPORTED;
+  return ZECO_PATH_SIMT;
+}
+
+}  // namespace
+
+namespace zeco {
+
+void prof_begin(cudaStream_t st) {
+  if (!g_prof.events || g_prof.count >= g_prof.cap) return;
+  if (g_prof.count == 0) {
+    cudaEventRecord((cudaEvent_t)g_prof.events[0], st);
+    g_prof.names[0] = "begin";
+    g_prof.count = 1;
+  }
+}
+
+void prof_mark(const char* kernel, cudaStream_t st) {
+  if (!g_prof.events || g_prof.count >= g_prof.cap || g_prof.count >= kMaxProf) return;
+  cudaEventRecord((cudaEvent_t)g_prof.events[g_prof.count], st);
+  g_prof.names[g_prof.count] = kernel;
+  ++g_prof.count;
+}
+
+}  // namespace zeco
+
+extern "C" {
+
+int zeco_set_profile_events(void* const* events, int n) {
+  g_prof.events = (n > 0) ? events : nullptr;
+  g_prof.cap = (n > 0 && events) ? (n < kMaxProf ? n : kMaxProf) : 0;
+  g_prof.count = 0;
+  return ZECO_OK;
+}
+
+int zeco_profile_event_count(void) { return g_prof.count; }
+
+const char* zeco_profile_kernel_name(int i) {
+  return (i >= 0 && i < g_prof.count) ? g_prof.names[i] : nullptr;
+}
+
+size_t zeco_gla_saved_bytes(const zeco_shape* shape) {
+  Dims d;
+  if (check_shape(shape, &d) != ZECO_OK) return 0;
+  return zeco::saved_layout(d).total;
+}
+
+size_t zeco_gla_workspace_bytes(const zeco_shape* shape, int bwd) {
+  Dims d;
+  if (check_shape(shape, &d) != ZECO_OK) return 0;
+  return bwd ? zeco::bwd_ws_layout(d).total : 0;
+}
+
+int zeco_gla_resolve_path(const zeco_shape* shape) {
+  Dims d;
+  const int rc = check_shape(shape, &d);
+  if (rc != ZECO_OK) return rc;
+  return resolve(shape, d);
+}
+
+int zeco_gla_fwd(const zeco_shape* shape, const void* q, const void* k, const void* v,
+                 const void* log_alpha, const float* S0, void* o, float* S_final, void* saved,
+                 void* workspace, size_t ws_bytes, zeco_stream_t stream) {
+  (void)workspace;
+  (void)ws_bytes;
+  Dims d;
+  int rc = check_shape(shape, &d);
+  if (rc != ZECO_OK) return rc;
+  const void* req[] = {q, k, v, log_alpha, o, saved};
+  for (const void* p : req)
+    if (!p || !aligned16(p)) return ZECO_ERR_ARG;
+  if ((S0 && !aligned16(S0)) || (S_final && !aligned16(S_final))) return ZECO_ERR_ARG;
+  const int path = resolve(shape, d);
+  if (path < 0) return path;
+  const zeco::SavedLayout sl = zeco::saved_layout(d);
+  float* S_in = (float*)((char*)saved + sl.S_in_off);
+  float* gamma = (float*)((char*)saved + sl.gamma_off);
+  cudaStream_t st = (cudaStream_t)stream;
+  zeco::prof_begin(st);
+  cudaError_t e = path == ZECO_PATH_TC
+                      ? zeco::tc_forward(d, q, k, v, log_alpha, S0, o, S_final, S_in, gamma, st)
+                      : zeco::simt_forward(d, q, k, v, log_alpha, S0, o, S_final, S_in, gamma,
+                                           st);
+  return e == cudaSuccess ? ZECO_OK : ZECO_ERR_CUDA;
+}
+
+int zeco_gla_bwd(const zeco_shape* shape, const void* q, const void* k, const void* v,
+                 const void* log_alpha, const void* saved, const void* d_o,
+                 const float* dS_final, void* dq, void* dk, void* dv, void* dlog_alpha,
+                 float* dS0, void* workspace, size_t ws_bytes, zeco_stream_t stream) {
+  Dims d;
+  int rc = check_shape(shape, &d);
+  if (rc != ZECO_OK) return rc;
+  const void* req[] = {q, k, v, log_alpha, saved, d_o, dq, dk, dv, dlog_alpha, workspace};
+  for (const void* p : req)
+    if (!p || !aligned16(p)) return ZECO_ERR_ARG;
+  if ((dS_final && !aligned16(dS_final)) || (dS0 && !aligned16(dS0))) return ZECO_ERR_ARG;
+  const int path = resolve(shape, d);
+  if (path < 0) return path;
+  const zeco::BwdWsLayout wl = zeco::bwd_ws_layout(d);
+  if (ws_bytes < wl.total) return ZECO_ERR_WORKSPACE;
+  const zeco::SavedLayout sl = zeco::saved_layout(d);
+  const float* S_in = (const float*)((const char*)saved + sl.S_in_off);
+  const float* gamma = (const float*)((const char*)saved + sl.gamma_off);
+  float* D = (float*)((char*)workspace + wl.D_off);
+  float* carry = (float*)((char*)workspace + wl.carry_off);
+  cudaStream_t st = (cudaStream_t)stream;
+  zeco::prof_begin(st);
+  cudaError_t e =
+      path == ZECO_PATH_TC
+          ? zeco::tc_backward(d, q, k, v, log_alpha, S_in, gamma, d_o, dS_final, dq, dk, dv,
+                              dlog_alpha, dS0, D, carry, st)
+          : zeco::simt_backward(d, q, k, v, log_alpha, S_in, gamma, d_o, dS_final, dq, dk, dv,
+                                dlog_alpha, dS0, D, carry, st);
+  return e == cudaSuccess ? ZECO_OK : ZECO_ERR_CUDA;
+}
+
+const char* zeco_strerror(int code) {
+  switch (code) {
+    case ZECO_OK:
+      return "success";
+    case ZECO_ERR_ARG:
+      return "invalid argument (null or misaligned pointer, or inconsistent shape)";
+    case ZECO_ERR_UNSUPPORTED:
+      return "shape outside the supported set";
+    case ZECO_ERR_WORKSPACE:
+      return "workspace too small";
+    case ZECO_ERR_CUDA:
+      return "CUDA kernel launch failed";
+    default:
+      return "unknown error code";
+  }
+}
+
+}  // extern "C"

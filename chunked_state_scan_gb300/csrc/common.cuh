@@ -1,0 +1,80 @@
+// common.cuh -- shared definitions of the CUDA library (internal).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/zeco_gla.h"
+
+namespace zeco {
+
+// Problem description handed from the C ABI to the kernel launchers.
+struct Dims {
+  int64_t B, H, T, dk, dv;
+  int P, K, C;
+  int64_t L;  // tokens per segment
+  bool bf16;
+};
+
+// Byte layout of the `saved` buffer and the backward workspace.
+struct SavedLayout {
+  size_t S_in_off, gamma_off, total;
+};
+struct BwdWsLayout {
+  size_t D_off, carry_off, total;
+};
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+inline SavedLayout saved_layout(const Dims& d) {
+  SavedLayout s;
+  const size_t bh = (size_t)d.B * d.H;
+  s.S_in_off = 0;
+  s.gamma_off = align_up(bh * (d.P + 1) * d.dk * d.dv * sizeof(float), 256);
+  s.total = align_up(s.gamma_off + bh * d.P * d.dk * sizeof(float), 256);
+  return s;
+}
+
+inline BwdWsLayout bwd_ws_layout(const Dims& d) {
+  BwdWsLayout w;
+  const size_t bh = (size_t)d.B * d.H;
+  w.D_off = 0;
+  w.carry_off = align_up(bh * (d.P + 1) * d.dk * d.dv * sizeof(float), 256);
+  w.total = align_up(w.carry_off + bh * d.P * d.dk * sizeof(float), 256);
+  return w;
+}
+
+// ------------------------------------------------------------ element I/O
+
+template <typename T>
+__device__ __forceinline__ float ld(const T* p);
+template <>
+__device__ __forceinline__ float ld<float>(const float* p) { return *p; }
+template <>
+__device__ __forceinline__ float ld<__nv_bfloat16>(const __nv_bfloat16* p) {
+  return __bfloat162float(*p);
+}
+
+template <typename T>
+__device__ __forceinline__ void st(T* p, float x);
+template <>
+__device__ __forceinline__ void st<float>(float* p, float x) { *p = x; }
+template <>
+__device__ __forceinline__ void st<__nv_bfloat16>(__nv_bfloat16* p, float x) {
+  *p = __float2bfloat16_rn(x);
+}
+
+// ------------------------------------------------------- launch bookkeeping
+
+// Per-kernel timing marks (see zeco_set_profile_events); no-ops when off.
+void prof_begin(cudaStream_t st);
+void prof_mark(const char* kernel, cudaStream_t st);
+
+// Sets the dynamic shared-memory limit of a kernel once per process.
+template <typename F>
+inline cudaError_t allow_smem(F* kernel, int bytes) {
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
+}  // namespace zeco

@@ -1,0 +1,38 @@
+// launch.h -- internal kernel launchers (not part of the C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace zeco {
+
+// ---- segment scans (scan.cu) ------------------------------------------
+cudaError_t launch_seg_scan_fwd(const Dims& d, float* S_in, const float* gamma, const float* S0,
+                                float* S_final, cudaStream_t st);
+cudaError_t launch_seg_scan_rev(const Dims& d, float* D, const float* S_in, const float* gamma,
+                                const float* dS_final, float* dS0, float* carry,
+                                cudaStream_t st);
+
+// ---- fp32 SIMT path (simt.cu) -----------------------------------------
+// Shared memory the SIMT kernels need for this shape (bytes, max over kernels).
+size_t simt_smem_bytes(const Dims& d);
+cudaError_t simt_forward(const Dims& d, const void* q, const void* k, const void* v,
+                         const void* g, const float* S0, void* o, float* S_final, float* S_in,
+                         float* gamma, cudaStream_t st);
+cudaError_t simt_backward(const Dims& d, const void* q, const void* k, const void* v,
+                          const void* g, const float* S_in, const float* gamma, const void* d_o,
+                          const float* dS_final, void* dq, void* dk, void* dv, void* dg,
+                          float* dS0, float* D, float* carry, cudaStream_t st);
+
+// ---- tcgen05 tensor-core path (tc_*.cu) --------------------------------
+bool tc_supported(const Dims& d);
+cudaError_t tc_forward(const Dims& d, const void* q, const void* k, const void* v,
+                       const void* g, const float* S0, void* o, float* S_final, float* S_in,
+                       float* gamma, cudaStream_t st);
+cudaError_t tc_backward(const Dims& d, const void* q, const void* k, const void* v,
+                        const void* g, const float* S_in, const float* gamma, const void* d_o,
+                        const float* dS_final, void* dq, void* dk, void* dv, void* dg,
+                        float* dS0, float* D, float* carry, cudaStream_t st);
+
+}  // namespace zeco

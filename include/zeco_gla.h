@@ -1,0 +1,162 @@
+/*
+ * zeco_gla.h -- C ABI of the segmented (ZeCO-style) gated linear attention
+ * operator for one NVIDIA GB300 (sm_103a).
+ *
+ * The operator (diagonal-decay GLA; ZeCO: Zero-Communication Overhead Sequence
+ * Parallelism for Linear Attention, Approach and Limitations):
+ *
+ *     S_t = diag(alpha_t) S_{t-1} + k_t^T v_t,   alpha_t = exp(log_alpha_t),
+ *     o_t = q_t S_t,                             S_{-1} = S0,  S_final = S_{T-1},
+ *
+ * with S in R^{dk x dv} per (batch, head) and the decay acting on the d_k rows
+ * (Pith review of ZeCO, "What carries the argument": the All-Scan update scales
+ * the state by the cumulative decay broadcast along d_v).
+ *
+ * It is evaluated the ZeCO way (Pith review of ZeCO, referee major comment 3:
+ * the two-pass schedule of Algorithm 1; assumptions: Appendix A.1 linear
+ * decomposition):
+ *   1. the sequence is cut into P segments of L = T/P tokens; every segment
+ *      computes its local state from zero (chunks of C tokens) and its
+ *      cumulative decay gamma_p = prod_{t in p} alpha_t;
+ *   2. a segment scan -- the All-Scan update S_in[p+1] = (gamma_p^T 1) .* S_in[p]
+ *      + S_loc[p], run independently on K contiguous blocks of d_k rows
+ *      (Pith review of ZeCO, "What carries the argument") -- gives every
+ *      segment its incoming global state; the accumulated state is what is
+ *      carried on (the pages' Algorithm 2 forwards the local state in one
+ *      branch, which the review's major comment 4 identifies as a bug);
+ *   3. every segment recomputes its chunks from S_in[p] and writes o (intra-
+ *      chunk decay-masked attention plus the inter-chunk state term).
+ * The backward keeps S_in from the forward, so it needs no forward re-scan
+ * (Pith review of ZeCO, assumptions: Appendix A.4); the adjoint state runs a
+ * reverse segment scan (the dKV pass of Linear Attention Sequence Parallelism,
+ * summary).  P, K and C change the grouping only: results equal the token
+ * recurrence up to rounding.
+ *
+ * Conventions (all entry points):
+ *   - Tensors are contiguous, row-major: q, k, log_alpha [B,H,T,dk];
+ *     v, o, d_o [B,H,T,dv]; gradients have the shape of their input.  They are
+ *     in the I/O dtype (shape->dtype).  S0, S_final, dS_final, dS0 are fp32
+ *     [B,H,dk,dv].  Arithmetic is fp32 throughout (bf16 inputs are widened;
+ *     bf16 tensor-core products accumulate in fp32).
+ *   - Every pointer is DEVICE memory owned by the caller and must be 16-byte
+ *     aligned.  The library never allocates, never frees, never synchronises
+ *     and never prints.  Work is enqueued on `stream` (NULL: the legacy default
+ *     stream) and is asynchronous; outputs are valid once the stream reaches
+ *     that point.  Calls that share `saved` or `workspace` must be ordered.
+ *   - Return value: ZECO_OK (0) or a negative ZECO_ERR_* code; nothing is
+ *     enqueued when argument checks fail.  ZECO_ERR_CUDA means a launch failed
+ *     (the CUDA error is left for cudaGetLastError of the caller's choosing).
+ *   - Supported shapes: B, H, T, P >= 1, T % P == 0, C in {16, 32, 64, 128}
+ *     with (T/P) % C == 0, dk % K == 0, dk a multiple of 16 in [16, 256], dv a
+ *     multiple of 32 in [32, 512].  The chunked form factors the decay inside a
+ *     chunk as exp(b_t) * exp(-b_s); this is exact in fp32 as long as the sum
+ *     of log_alpha over any chunk stays above -80 (for every d_k row).
+ */
+#ifndef ZECO_GLA_H
+#define ZECO_GLA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t, spelled without the CUDA headers. */
+struct CUstream_st;
+typedef struct CUstream_st *zeco_stream_t;
+
+enum {
+    ZECO_OK = 0,
+    ZECO_ERR_ARG = -1,         /* null / misaligned pointer or invalid shape value */
+    ZECO_ERR_UNSUPPORTED = -2, /* valid shape outside the supported set above */
+    ZECO_ERR_WORKSPACE = -3,   /* ws_bytes smaller than zeco_gla_workspace_bytes() */
+    ZECO_ERR_CUDA = -4         /* a kernel launch failed */
+};
+
+typedef enum { ZECO_F32 = 0, ZECO_BF16 = 1 } zeco_dtype;
+
+/* Kernel path.  AUTO picks the tcgen05 tensor-core kernels for bf16 shapes they
+ * support and the fp32 SIMT kernels otherwise; SIMT and TC force one path
+ * (TC on an unsupported shape returns ZECO_ERR_UNSUPPORTED). */
+typedef enum { ZECO_PATH_AUTO = 0, ZECO_PATH_SIMT = 1, ZECO_PATH_TC = 2 } zeco_path;
+
+typedef struct zeco_shape {
+    int64_t B, H, T; /* batch, heads, tokens per sequence */
+    int64_t dk, dv;  /* key/query width and value width (state is dk x dv) */
+    int32_t P;       /* segments per sequence (ZeCO's devices; here all on one GPU) */
+    int32_t K;       /* d_k blocks of the segment scan */
+    int32_t C;       /* chunk length inside a segment */
+    int32_t dtype;   /* zeco_dtype of q, k, v, log_alpha, o and all their gradients */
+    int32_t path;    /* zeco_path */
+    int32_t reserved;
+} zeco_shape;
+
+/*
+ * Bytes of the `saved` buffer written by zeco_gla_fwd and read by
+ * zeco_gla_bwd: the incoming global state of every segment, S_in [B,H,P+1,dk,dv]
+ * fp32 (S_in[0] = S0, S_in[P] = S_final), then the segment decays
+ * gamma [B,H,P,dk] fp32.  Returns 0 for an invalid shape.
+ */
+size_t zeco_gla_saved_bytes(const zeco_shape *shape);
+
+/*
+ * Bytes of scratch memory the forward (bwd = 0) or backward (bwd = 1) needs.
+ * The backward holds the adjoint of every segment's incoming state
+ * [B,H,P+1,dk,dv] fp32 and one carry row per segment [B,H,P,dk] fp32.
+ * Returns 0 when no scratch is needed or the shape is invalid.
+ */
+size_t zeco_gla_workspace_bytes(const zeco_shape *shape, int bwd);
+
+/*
+ * Forward: writes o, S_final (skipped when NULL) and `saved`.
+ *   S0 == NULL means a zero initial state.
+ *   saved: zeco_gla_saved_bytes(shape) bytes, kept unchanged until the matching
+ *          zeco_gla_bwd has run.
+ *   workspace / ws_bytes: at least zeco_gla_workspace_bytes(shape, 0) bytes
+ *          (may be NULL when that is 0).
+ */
+int zeco_gla_fwd(const zeco_shape *shape, const void *q, const void *k, const void *v,
+                 const void *log_alpha, const float *S0, void *o, float *S_final, void *saved,
+                 void *workspace, size_t ws_bytes, zeco_stream_t stream);
+
+/*
+ * Backward of the loss L(o, S_final) given d_o = dL/do and dS_final = dL/dS_final
+ * (NULL: zero).  Writes every element of dq, dk, dv, dlog_alpha and, when not
+ * NULL, dS0 = dL/dS0.  q, k, v, log_alpha must be the forward's inputs and
+ * `saved` the buffer that forward wrote (the global state held since the
+ * forward: Pith review of ZeCO, assumptions: Appendix A.4).  workspace needs
+ * zeco_gla_workspace_bytes(shape, 1) bytes and is overwritten.
+ */
+int zeco_gla_bwd(const zeco_shape *shape, const void *q, const void *k, const void *v,
+                 const void *log_alpha, const void *saved, const void *d_o,
+                 const float *dS_final, void *dq, void *dk, void *dv, void *dlog_alpha,
+                 float *dS0, void *workspace, size_t ws_bytes, zeco_stream_t stream);
+
+/* Static message for an error code (never NULL). */
+const char *zeco_strerror(int code);
+
+/*
+ * Optional per-kernel timing (measurement aid; not part of the method).
+ * After zeco_set_profile_events(events, n) with n > 0, every zeco_gla_fwd /
+ * zeco_gla_bwd call made on this host thread records events[0] on its stream
+ * before its first kernel and events[i] right after its i-th kernel, until n
+ * events are used; n = 0 (or events = NULL) switches it off.  `events` are
+ * cudaEvent_t handles created (and later destroyed) by the caller.  The calls
+ * return ZECO_OK.  zeco_profile_event_count() gives the number of events
+ * recorded so far and zeco_profile_kernel_name(i) the kernel that ended at
+ * event i (NULL when i is out of range).
+ */
+int zeco_set_profile_events(void *const *events, int n);
+int zeco_profile_event_count(void);
+const char *zeco_profile_kernel_name(int i);
+
+/* The path zeco_gla_fwd / zeco_gla_bwd would run for this shape
+ * (ZECO_PATH_SIMT or ZECO_PATH_TC), or a negative ZECO_ERR_* code. */
+int zeco_gla_resolve_path(const zeco_shape *shape);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ZECO_GLA_H */

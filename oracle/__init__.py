@@ -159,3 +159,27 @@ def boundary_states(q, k, v, log_alpha, S0, P, nthreads=None):
                        nthreads=nthreads)
         out[:, :, p + 1] = S
     return out
+
+
+def boundary_states_cols(q, k, v, log_alpha, S0, P, cols, nthreads=None):
+    """Columns ``cols`` of the segment-entry states S_in[p], p = 0..P (fp64).
+
+    Every column of the state evolves on its own (the decay scales rows), so the
+    selected columns can be carried from prefix to prefix without the others.
+    Returns [B,H,P+1,dk,ncols].
+    """
+    q, k, v, g, S0 = _f64(q), _f64(k), _f64(v), _f64(log_alpha), _f64(S0)
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    cols = _idx(cols)
+    L = T // P
+    S = np.zeros((B, H, dk, dv)) if S0 is None else S0.copy()
+    out = np.zeros((B, H, P + 1, dk, len(cols)))
+    out[:, :, 0] = S[..., cols]
+    for p in range(P):
+        sl = slice(p * L, (p + 1) * L)
+        _, sf = gla_fwd(q[:, :, sl], k[:, :, sl], v[:, :, sl], g[:, :, sl], S, cols=cols,
+                        nthreads=nthreads)
+        S[..., cols] = sf
+        out[:, :, p + 1] = sf
+    return out

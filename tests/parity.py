@@ -1,0 +1,74 @@
+"""Helpers for the GPU parity tests: run the library, run the oracle, compare."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+
+TOL_F32 = 1e-4  # max relative error (normwise infinity) for fp32 I/O
+TOL_BF16 = 2e-2  # relative L2 error for bf16 I/O with fp32 accumulation
+
+
+def max_rel(x, r) -> float:
+    """max|x - r| / max|r| over the tensor (normwise infinity relative error)."""
+    x = np.asarray(x, dtype=np.float64)
+    r = np.asarray(r, dtype=np.float64)
+    den = np.abs(r).max() if r.size else 0.0
+    return float(np.abs(x - r).max() / den) if den > 0 else float(np.abs(x - r).max())
+
+
+def rel_l2(x, r) -> float:
+    x = np.asarray(x, dtype=np.float64)
+    r = np.asarray(r, dtype=np.float64)
+    den = np.linalg.norm(r)
+    return float(np.linalg.norm(x - r) / den) if den > 0 else float(np.linalg.norm(x - r))
+
+
+def err(x, r, dtype) -> float:
+    return max_rel(x, r) if dtype == "f32" else rel_l2(x, r)
+
+
+def tol(dtype) -> float:
+    return TOL_F32 if dtype == "f32" else TOL_BF16
+
+
+def to_np(t):
+    return t.detach().float().cpu().numpy()
+
+
+def run_gpu(z, x, P, K, C, path="auto", bwd=True, dev="cuda"):
+    """Forward (+ backward) through the C ABI on device tensors."""
+    g = {n: (t.to(dev) if t is not None else None) for n, t in x.items()}
+    o, sf, saved = z.zeco_gla_fwd(g["q"], g["k"], g["v"], g["log_alpha"], g["S0"], P=P, K=K,
+                                  C=C, path=path)
+    out = dict(o=o, S_final=sf, saved=saved)
+    if bwd:
+        out.update(z.zeco_gla_bwd(g["q"], g["k"], g["v"], g["log_alpha"], saved, g["do"],
+                                  g["dS_final"], P=P, K=K, C=C, path=path))
+    torch.cuda.synchronize()
+    return out
+
+
+def saved_states(saved, B, H, P, dk, dv):
+    n = B * H * (P + 1) * dk * dv
+    return saved.view(torch.float32)[:n].view(B, H, P + 1, dk, dv)
+
+
+def compare_full(z, x, P, K, C, dtype, path="auto", bwd=True, check_states=True):
+    """Full-tensor parity of every output against the oracle; returns the errors."""
+    res = run_gpu(z, x, P, K, C, path=path, bwd=bwd)
+    B, H, T, dk = x["q"].shape
+    dv = x["v"].shape[-1]
+    ro, rsf = oracle.gla_fwd(x["q"], x["k"], x["v"], x["log_alpha"], x["S0"])
+    errs = {"o": err(to_np(res["o"]), ro, dtype), "S_final": err(to_np(res["S_final"]), rsf, dtype)}
+    if check_states:
+        bs = oracle.boundary_states(x["q"], x["k"], x["v"], x["log_alpha"], x["S0"], P)
+        got = to_np(saved_states(res["saved"], B, H, P, dk, dv))
+        errs["S_in"] = err(got, bs, dtype)
+    if bwd:
+        rg = oracle.gla_bwd(x["q"], x["k"], x["v"], x["log_alpha"], x["S0"], x["do"],
+                            x["dS_final"])
+        for n in ("dq", "dk", "dv", "dlog_alpha", "dS0"):
+            errs[n] = err(to_np(res[n]), rg[n], dtype)
+    return errs

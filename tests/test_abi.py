@@ -1,0 +1,98 @@
+"""The C-ABI library: builds, loads, exports what the header declares, and
+rejects bad arguments on the host (no GPU work is launched here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from chunked_state_scan_gb300 import build
+    build.build()
+    import chunked_state_scan_gb300 as z
+    return z.load_library()
+
+
+def _declared_functions():
+    names = []
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"\b(zeco_\w+)\s*\(", src)
+    return sorted(set(names))
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = _declared_functions()
+    assert "zeco_gla_fwd" in names and "zeco_gla_bwd" in names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def _shape(**kw):
+    import chunked_state_scan_gb300 as z
+    a = dict(B=1, H=4, T=1 << 20, dk=256, dv=512, P=64, K=8, C=64, dtype="bf16")
+    a.update(kw)
+    return z.make_shape(**a)
+
+
+def test_sizes_follow_the_layout(lib):
+    import chunked_state_scan_gb300 as z
+    s = _shape()
+    state = 4 * 65 * 256 * 512 * 4
+    gam = 4 * 64 * 256 * 4
+    assert z.saved_bytes(s) == state + gam
+    assert z.workspace_bytes(s, True) == state + gam
+    assert z.workspace_bytes(s, False) == 0
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(T=1000), -1),            # T not divisible by P
+    (dict(P=3), -1),
+    (dict(K=3), -1),               # dk % K != 0
+    (dict(C=48), -1),              # L % C != 0
+    (dict(C=8, T=8 * 64), -2),     # C outside {16,32,64,128}
+    (dict(dk=272), -2),
+    (dict(dv=48), -2),
+    (dict(dv=1024), -2),
+    (dict(B=0), -1),
+    (dict(dtype=7), -1),
+])
+def test_invalid_shapes_are_rejected(lib, kw, code):
+    s = _shape(**kw)
+    if kw.get("dtype") == 7:
+        s.dtype = 7
+    assert lib.zeco_gla_saved_bytes(ctypes.byref(s)) == 0
+    assert lib.zeco_gla_resolve_path(ctypes.byref(s)) == code
+    rc = lib.zeco_gla_fwd(ctypes.byref(s), *([ctypes.c_void_p(256)] * 4), None,
+                          ctypes.c_void_p(256), None, ctypes.c_void_p(256), None, 0, None)
+    assert rc == code
+
+
+def test_null_and_misaligned_pointers_are_rejected(lib):
+    s = _shape(T=4096, P=4)
+    ok = ctypes.c_void_p(4096)
+    bad = ctypes.c_void_p(4100)
+    args = [ok] * 4
+    assert lib.zeco_gla_fwd(ctypes.byref(s), *args, None, None, None, ok, None, 0, None) == -1
+    assert lib.zeco_gla_fwd(ctypes.byref(s), bad, ok, ok, ok, None, ok, None, ok, None, 0,
+                            None) == -1
+    # workspace too small for the backward
+    rc = lib.zeco_gla_bwd(ctypes.byref(s), ok, ok, ok, ok, ok, ok, None, ok, ok, ok, ok, None,
+                          ok, 16, None)
+    assert rc == -3
+    assert lib.zeco_strerror(-3) == b"workspace too small"
+    assert lib.zeco_strerror(12345) == b"unknown error code"
+
+
+def test_path_resolution(lib):
+    import chunked_state_scan_gb300 as z
+    assert z.resolve_path(_shape(dtype="f32", dk=64, dv=64, T=1024, P=4, K=2)) == "simt"
+    # fp32 at full width does not fit the SIMT kernels' shared memory with C=128
+    with pytest.raises(z.ZecoError):
+        z.resolve_path(_shape(dtype="f32", C=128, path="simt"))

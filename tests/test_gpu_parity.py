@@ -1,0 +1,129 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle.
+
+fp32 I/O: max relative error (normwise infinity) <= 1e-4 per output tensor.
+bf16 I/O: relative L2 error <= 2e-2 per output tensor.
+Inputs come from the seeded generators in workloads.py; the oracle sees the
+same (rounded) values widened to fp64.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def z():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from chunked_state_scan_gb300 import build
+    build.build()
+    import chunked_state_scan_gb300 as pkg
+    pkg.load_library()
+    return pkg
+
+
+def _assert(errs, dtype, what=""):
+    t = parity.tol(dtype)
+    bad = {k: v for k, v in errs.items() if not v <= t}
+    assert not bad, f"{what} errors above {t}: {bad} (all: {errs})"
+
+
+# ------------------------------------------------------------- tiny fp32
+
+
+def test_tiny_f32_workload_full(z):
+    """B1 H2 T1024 P4 C64 K2 d=64, fp32: every output, every state, fwd and bwd."""
+    w = workloads.TINY_F32
+    x = workloads.make_inputs(w)
+    errs = parity.compare_full(z, x, w.P, w.K, w.C, "f32")
+    _assert(errs, "f32", w.name)
+
+
+@pytest.mark.parametrize("P,K,C", [(1, 1, 64), (2, 4, 32), (8, 2, 16), (32, 8, 16),
+                                   (4, 32, 128), (16, 1, 32)])
+def test_f32_invariance_to_P_K_C(z, P, K, C):
+    """Every (P, K, C) grouping gives the recurrence's result (incl. P = T/C)."""
+    x = workloads.make_custom(2, 1, 512, 32, 64, dtype="f32", seed=P * 100 + K * 10 + C,
+                              s0_scale=0.5)
+    errs = parity.compare_full(z, x, P, K, C, "f32")
+    _assert(errs, "f32", f"P={P} K={K} C={C}")
+
+
+@pytest.mark.parametrize("case", ["no_decay", "slow_decay", "fast_decay", "single_chunk",
+                                  "ragged_tiles", "min_width", "no_init_no_dsf"])
+def test_f32_edge_cases(z, case):
+    kw = dict(B=1, H=2, T=256, dk=64, dv=64, dtype="f32", seed=7, s0_scale=0.3)
+    P, K, C = 4, 2, 32
+    if case == "no_decay":
+        kw["g_zero"] = True
+    elif case == "slow_decay":
+        kw["x_mean"] = 8.0
+    elif case == "fast_decay":
+        kw["x_mean"] = -6.0
+        kw["x_scale"] = 2.0
+    elif case == "single_chunk":
+        kw.update(T=64)
+        P, K, C = 1, 1, 64
+    elif case == "ragged_tiles":
+        kw.update(dk=48, dv=96, T=384)  # d_k tile of 64 and d_v slab of 64 both ragged
+        P, K, C = 3, 3, 32
+    elif case == "min_width":
+        kw.update(dk=16, dv=32, T=128, B=3, H=1)
+        P, K, C = 2, 1, 16
+    x = workloads.make_custom(**kw)
+    if case == "no_init_no_dsf":
+        x["S0"] = None
+        x["dS_final"] = None
+    errs = parity.compare_full(z, x, P, K, C, "f32")
+    _assert(errs, "f32", case)
+
+
+def test_f32_full_width_and_long_segments(z):
+    """d_k = 256, d_v = 512 (the GLA-1B head shape) in fp32, several 256-token segments."""
+    x = workloads.make_custom(1, 1, 1024, 256, 512, dtype="f32", seed=21, qk_scale=1 / 16,
+                              s0_scale=0.1)
+    errs = parity.compare_full(z, x, 4, 8, 64, "f32", check_states=True)
+    _assert(errs, "f32", "full width")
+
+
+def test_repeated_calls_are_deterministic(z):
+    w = workloads.TINY_F32
+    x = workloads.make_inputs(w)
+    a = parity.run_gpu(z, x, w.P, w.K, w.C)
+    b = parity.run_gpu(z, x, w.P, w.K, w.C)
+    for n in ("o", "S_final", "dq", "dk", "dv", "dlog_alpha", "dS0"):
+        assert torch.equal(a[n], b[n]), n
+
+
+# ------------------------------------------------------------------ bf16
+
+
+@pytest.mark.parametrize("path", ["simt", "auto"])
+def test_bf16_moderate_full(z, path):
+    """bf16, GLA-1B head widths, several segments and chunks: every output."""
+    x = workloads.make_custom(1, 2, 2048, 256, 512, dtype="bf16", seed=5, qk_scale=1 / 16,
+                              s0_scale=0.1)
+    errs = parity.compare_full(z, x, 4, 4, 64, "bf16", path=path)
+    _assert(errs, "bf16", path)
+
+
+@pytest.mark.parametrize("path", ["simt", "auto"])
+def test_bf16_slow_decay_carry_dominated(z, path):
+    """Slow decay: the state carried across segments dominates the outputs, so an
+    error in the segment scan cannot hide under the intra-chunk terms."""
+    x = workloads.make_custom(1, 2, 2048, 128, 256, dtype="bf16", seed=6, qk_scale=1 / 12,
+                              x_mean=8.0, s0_scale=0.5)
+    errs = parity.compare_full(z, x, 8, 2, 64, "bf16", path=path)
+    _assert(errs, "bf16", path)
+    # outputs of the first chunk of every segment only (the carry's share is largest there)
+    res = parity.run_gpu(z, x, 8, 2, 64, path=path, bwd=False)
+    ro, _ = oracle.gla_fwd(x["q"], x["k"], x["v"], x["log_alpha"], x["S0"])
+    L = 2048 // 8
+    idx = np.concatenate([np.arange(p * L, p * L + 64) for p in range(8)])
+    e = parity.rel_l2(parity.to_np(res["o"])[:, :, idx], ro[:, :, idx])
+    assert e <= parity.TOL_BF16, e

@@ -280,3 +280,12 @@ def test_empty_sequence():
     assert o.shape == (1, 1, 0, 2) and np.array_equal(sf, S0)
     gr = oracle.gla_bwd(q, q, v, q, S0, v, dSf)
     assert np.array_equal(gr["dS0"], dSf)
+
+
+def test_boundary_state_columns_match_full_states():
+    B, H, T, dk, dv, P = 1, 2, 240, 4, 6, 5
+    q, k, v, g, S0, _, _ = _rand_inputs(8, B, H, T, dk, dv)
+    full = oracle.boundary_states(q, k, v, g, S0, P)
+    cols = [5, 2]
+    part = oracle.boundary_states_cols(q, k, v, g, S0, P, cols)
+    np.testing.assert_allclose(part, full[..., cols], rtol=1e-13, atol=1e-13)
