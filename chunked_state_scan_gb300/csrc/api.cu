@@ -159,14 +159,15 @@ int zeco_gla_bwd(const zeco_shape* shape, const void* q, const void* k, const vo
   const float* gamma = (const float*)((const char*)saved + sl.gamma_off);
   float* D = (float*)((char*)workspace + wl.D_off);
   float* carry = (float*)((char*)workspace + wl.carry_off);
+  float* qdq = (float*)((char*)workspace + wl.qdq_off);
   cudaStream_t st = (cudaStream_t)stream;
   zeco::prof_begin(st);
   cudaError_t e =
       path == ZECO_PATH_TC
           ? zeco::tc_backward(d, q, k, v, log_alpha, S_in, gamma, d_o, dS_final, dq, dk, dv,
-                              dlog_alpha, dS0, D, carry, st)
+                              dlog_alpha, dS0, D, carry, qdq, st)
           : zeco::simt_backward(d, q, k, v, log_alpha, S_in, gamma, d_o, dS_final, dq, dk, dv,
-                                dlog_alpha, dS0, D, carry, st);
+                                dlog_alpha, dS0, D, carry, qdq, st);
   return e == cudaSuccess ? ZECO_OK : ZECO_ERR_CUDA;
 }
 

@@ -22,7 +22,7 @@ struct SavedLayout {
   size_t S_in_off, gamma_off, total;
 };
 struct BwdWsLayout {
-  size_t D_off, carry_off, total;
+  size_t D_off, carry_off, qdq_off, total;
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -41,7 +41,8 @@ inline BwdWsLayout bwd_ws_layout(const Dims& d) {
   const size_t bh = (size_t)d.B * d.H;
   w.D_off = 0;
   w.carry_off = align_up(bh * (d.P + 1) * d.dk * d.dv * sizeof(float), 256);
-  w.total = align_up(w.carry_off + bh * d.P * d.dk * sizeof(float), 256);
+  w.qdq_off = align_up(w.carry_off + bh * d.P * d.dk * sizeof(float), 256);
+  w.total = align_up(w.qdq_off + bh * d.T * d.dk * sizeof(float), 256);
   return w;
 }
 

@@ -23,7 +23,7 @@ cudaError_t simt_forward(const Dims& d, const void* q, const void* k, const void
 cudaError_t simt_backward(const Dims& d, const void* q, const void* k, const void* v,
                           const void* g, const float* S_in, const float* gamma, const void* d_o,
                           const float* dS_final, void* dq, void* dk, void* dv, void* dg,
-                          float* dS0, float* D, float* carry, cudaStream_t st);
+                          float* dS0, float* D, float* carry, float* qdq, cudaStream_t st);
 
 // ---- tcgen05 tensor-core path (tc_*.cu) --------------------------------
 bool tc_supported(const Dims& d);
@@ -33,6 +33,6 @@ cudaError_t tc_forward(const Dims& d, const void* q, const void* k, const void* 
 cudaError_t tc_backward(const Dims& d, const void* q, const void* k, const void* v,
                         const void* g, const float* S_in, const float* gamma, const void* d_o,
                         const float* dS_final, void* dq, void* dk, void* dv, void* dg,
-                        float* dS0, float* D, float* carry, cudaStream_t st);
+                        float* dS0, float* D, float* carry, float* qdq, cudaStream_t st);
 
 }  // namespace zeco

@@ -354,8 +354,9 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads)
 bwd_dqk_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
                const T* __restrict__ g, const T* __restrict__ dO, const float* __restrict__ S_in,
-               const float* __restrict__ D, const float* __restrict__ carry, T* dq,
-               T* __restrict__ dk_out, T* __restrict__ dg_out, Dims d) {
+               const float* __restrict__ D, const float* __restrict__ carry,
+               T* __restrict__ dq, T* __restrict__ dk_out, T* __restrict__ dg_out,
+               float* __restrict__ qdq, Dims d) {
   extern __shared__ float sm[];
   const int C = d.C, dk = (int)d.dk, dv = (int)d.dv, ldA = C + 1;
   float* Ss = sm;                  // state rows [kKB][dv]
@@ -378,6 +379,7 @@ bwd_dqk_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __rest
   T* dqb = dq + (size_t)bh * d.T * dk;
   T* dkb = dk_out + (size_t)bh * d.T * dk;
   T* dgb = dg_out + (size_t)bh * d.T * dk;
+  float* qdqb = qdq + (size_t)bh * d.T * dk;
   const int nc = (int)(d.L / C);
   const int nslab = dv / kSlab + (dv % kSlab ? 1 : 0);
 
@@ -460,7 +462,10 @@ bwd_dqk_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __rest
       const int t = e / kKB, ii = e % kKB;
       float s = acc[e];
       for (int u = 0; u <= t; ++u) s = fmaf(As[t * ldA + u], Kf[u * kKB + ii], s);
-      st(dqb + (size_t)(t0 + t) * dk + i0 + ii, Ef[e] * s);
+      const size_t off = (size_t)(t0 + t) * dk + i0 + ii;
+      const float dqv = Ef[e] * s;
+      st(dqb + off, dqv);
+      qdqb[off] = ld(qb + off) * dqv;  // fp32, for the dlog_alpha suffix sum
     }
   }
 
@@ -557,7 +562,7 @@ bwd_dqk_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __rest
       float r = run[ii];
       for (int t = C - 1; t >= 0; --t) {
         const size_t off = (size_t)(t0 + t) * dk + i;
-        r += ld(qb + off) * ld(dqb + off) - ld(kb + off) * acc[t * kKB + ii];
+        r += qdqb[off] - ld(kb + off) * acc[t * kKB + ii];
         st(dgb + off, r);
       }
       run[ii] = r;
@@ -599,7 +604,7 @@ template <typename T>
 cudaError_t backward_t(const Dims& d, const T* q, const T* k, const T* v, const T* g,
                        const float* S_in, const float* gamma, const T* dO,
                        const float* dS_final, T* dq, T* dk, T* dv, T* dg, float* dS0, float* D,
-                       float* carry, cudaStream_t st) {
+                       float* carry, float* qdq, cudaStream_t st) {
   const unsigned bhp = (unsigned)(d.B * d.H * d.P);
   dim3 g1((unsigned)((d.dv + 63) / 64), (unsigned)((d.dk + 63) / 64), bhp);
   seg_state_kernel<T, false><<<g1, kThreads, 0, st>>>(q, dO, g, D, nullptr, d, 0);
@@ -620,7 +625,8 @@ cudaError_t backward_t(const Dims& d, const T* q, const T* k, const T* v, const 
   e = allow_smem(bwd_dqk_kernel<T>, sm2);
   if (e != cudaSuccess) return e;
   dim3 g3((unsigned)(d.dk / kKB), bhp);
-  bwd_dqk_kernel<T><<<g3, kThreads, sm2, st>>>(q, k, v, g, dO, S_in, D, carry, dq, dk, dg, d);
+  bwd_dqk_kernel<T><<<g3, kThreads, sm2, st>>>(q, k, v, g, dO, S_in, D, carry, dq, dk, dg, qdq,
+                                               d);
   prof_mark("simt_bwd_dqk", st);
   return cudaGetLastError();
 }
@@ -647,17 +653,17 @@ cudaError_t simt_forward(const Dims& d, const void* q, const void* k, const void
 cudaError_t simt_backward(const Dims& d, const void* q, const void* k, const void* v,
                           const void* g, const float* S_in, const float* gamma, const void* d_o,
                           const float* dS_final, void* dq, void* dk, void* dv, void* dg,
-                          float* dS0, float* D, float* carry, cudaStream_t st) {
+                          float* dS0, float* D, float* carry, float* qdq, cudaStream_t st) {
   if (d.bf16) {
     using T = __nv_bfloat16;
     return backward_t<T>(d, (const T*)q, (const T*)k, (const T*)v, (const T*)g, S_in, gamma,
                          (const T*)d_o, dS_final, (T*)dq, (T*)dk, (T*)dv, (T*)dg, dS0, D, carry,
-                         st);
+                         qdq, st);
   }
   using T = float;
   return backward_t<T>(d, (const T*)q, (const T*)k, (const T*)v, (const T*)g, S_in, gamma,
                        (const T*)d_o, dS_final, (T*)dq, (T*)dk, (T*)dv, (T*)dg, dS0, D, carry,
-                       st);
+                       qdq, st);
 }
 
 }  // namespace zeco

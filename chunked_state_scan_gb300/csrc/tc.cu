@@ -16,7 +16,7 @@ cudaError_t tc_forward(const Dims&, const void*, const void*, const void*, const
 
 cudaError_t tc_backward(const Dims&, const void*, const void*, const void*, const void*,
                         const float*, const float*, const void*, const float*, void*, void*,
-                        void*, void*, float*, float*, float*, cudaStream_t) {
+                        void*, void*, float*, float*, float*, float*, cudaStream_t) {
   return cudaErrorNotSupported;
 }
 

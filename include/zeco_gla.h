@@ -103,7 +103,9 @@ size_t zeco_gla_saved_bytes(const zeco_shape *shape);
 /*
  * Bytes of scratch memory the forward (bwd = 0) or backward (bwd = 1) needs.
  * The backward holds the adjoint of every segment's incoming state
- * [B,H,P+1,dk,dv] fp32 and one carry row per segment [B,H,P,dk] fp32.
+ * [B,H,P+1,dk,dv] fp32, one dlog_alpha carry row per segment [B,H,P,dk] fp32,
+ * and q .* dq in fp32 [B,H,T,dk] (dlog_alpha is a long suffix sum of
+ * q .* dq - k .* dk that cancels heavily, so its terms are kept in fp32).
  * Returns 0 when no scratch is needed or the shape is invalid.
  */
 size_t zeco_gla_workspace_bytes(const zeco_shape *shape, int bwd);
