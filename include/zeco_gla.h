@@ -135,6 +135,30 @@ int zeco_gla_bwd(const zeco_shape *shape, const void *q, const void *k, const vo
                  const float *dS_final, void *dq, void *dk, void *dv, void *dlog_alpha,
                  float *dS0, void *workspace, size_t ws_bytes, zeco_stream_t stream);
 
+/*
+ * Backward without a caller-provided workspace (the ZeCO pages have no
+ * counterpart: this exists for callers that cannot allocate device memory --
+ * code that runs where cudaMalloc is unavailable or forbidden, or inside a
+ * host framework that owns all device memory and passes in only the tensors).
+ * Same arguments, results and errors as zeco_gla_bwd, minus workspace and
+ * ws_bytes: the scratch is a fixed array of ZECO_NOALLOC_MAX_WS_BYTES in the
+ * library's own device memory, which every GPU that loads the library holds
+ * until the process exits.  Nothing is allocated or freed by the call.
+ *   - Shapes needing more scratch than that (zeco_gla_workspace_bytes(shape, 1)
+ *     > ZECO_NOALLOC_MAX_WS_BYTES) return ZECO_ERR_WORKSPACE.
+ *   - All calls on one GPU share the array: calls whose GPU work could overlap
+ *     (other streams, other host threads) race on it and must be ordered by
+ *     the caller.  The array keeps the last call's contents; the backward
+ *     writes every scratch byte before reading it.
+ *   - The first call on each device looks up the array's device address with
+ *     that device current; make the first call before any stream capture.
+ */
+#define ZECO_NOALLOC_MAX_WS_BYTES (32u << 20)
+int zeco_gla_bwd_noalloc(const zeco_shape *shape, const void *q, const void *k, const void *v,
+                         const void *log_alpha, const void *saved, const void *d_o,
+                         const float *dS_final, void *dq, void *dk, void *dv,
+                         void *dlog_alpha, float *dS0, zeco_stream_t stream);
+
 /* Static message for an error code (never NULL). */
 const char *zeco_strerror(int code);
 
