@@ -25,7 +25,22 @@ cudaError_t simt_backward(const Dims& d, const void* q, const void* k, const voi
                           const float* dS_final, void* dq, void* dk, void* dv, void* dg,
                           float* dS0, float* D, float* carry, float* qdq, cudaStream_t st);
 
+cudaError_t simt_fwd_out_bf16(const Dims& d, const void* q, const void* k, const void* v,
+                              const void* g, const float* S_in, void* o, cudaStream_t st);
+cudaError_t simt_bwd_main_bf16(const Dims& d, const void* q, const void* k, const void* v,
+                               const void* g, const float* S_in, const void* d_o, void* dq,
+                               void* dk, void* dv, void* dg, float* D, float* carry, float* qdq,
+                               cudaStream_t st);
+
 // ---- tcgen05 tensor-core path (tc_*.cu) --------------------------------
+bool tc_state_supported(const Dims& d);
+cudaError_t tc_chunk_state(const Dims& d, const void* k, const void* v, const void* g,
+                           float* S_in, float* gamma, cudaStream_t st);
+cudaError_t tc_dstate_local(const Dims& d, const void* q, const void* d_o, const void* g,
+                            float* D, cudaStream_t st);
+bool tc_fwd_supported(const Dims& d);
+cudaError_t tc_fwd_out(const Dims& d, const void* q, const void* k, const void* v, const void* g,
+                       const float* S_in, void* o, cudaStream_t st);
 bool tc_supported(const Dims& d);
 cudaError_t tc_forward(const Dims& d, const void* q, const void* k, const void* v,
                        const void* g, const float* S0, void* o, float* S_final, float* S_in,

@@ -580,6 +580,19 @@ size_t dqk_smem(const Dims& d) {
 }
 
 template <typename T>
+cudaError_t fwd_out_t(const Dims& d, const T* q, const T* k, const T* v, const T* g,
+                      const float* S_in, T* o, cudaStream_t st) {
+  const unsigned bhp = (unsigned)(d.B * d.H * d.P);
+  const int sm = (int)fwd_smem(d);
+  cudaError_t e = allow_smem(fwd_out_kernel<T>, sm);
+  if (e != cudaSuccess) return e;
+  dim3 g2((unsigned)(d.dv / kNV), bhp);
+  fwd_out_kernel<T><<<g2, kThreads, sm, st>>>(q, k, v, g, S_in, o, d);
+  prof_mark("simt_fwd_out", st);
+  return cudaGetLastError();
+}
+
+template <typename T>
 cudaError_t forward_t(const Dims& d, const T* q, const T* k, const T* v, const T* g,
                       const float* S0, T* o, float* S_final, float* S_in, float* gamma,
                       cudaStream_t st) {
@@ -591,12 +604,29 @@ cudaError_t forward_t(const Dims& d, const T* q, const T* k, const T* v, const T
   if (e != cudaSuccess) return e;
   e = launch_seg_scan_fwd(d, S_in, gamma, S0, S_final, st);
   if (e != cudaSuccess) return e;
-  const int sm = (int)fwd_smem(d);
-  e = allow_smem(fwd_out_kernel<T>, sm);
+  return fwd_out_t<T>(d, q, k, v, g, S_in, o, st);
+}
+
+template <typename T>
+cudaError_t bwd_main_t(const Dims& d, const T* q, const T* k, const T* v, const T* g,
+                       const float* S_in, const T* dO, T* dq, T* dk, T* dv, T* dg, float* D,
+                       float* carry, float* qdq, cudaStream_t st) {
+  const unsigned bhp = (unsigned)(d.B * d.H * d.P);
+  const int sm1 = (int)fwd_smem(d);
+  cudaError_t e = allow_smem(bwd_dv_kernel<T>, sm1);
   if (e != cudaSuccess) return e;
   dim3 g2((unsigned)(d.dv / kNV), bhp);
-  fwd_out_kernel<T><<<g2, kThreads, sm, st>>>(q, k, v, g, S_in, o, d);
-  prof_mark("simt_fwd_out", st);
+  bwd_dv_kernel<T><<<g2, kThreads, sm1, st>>>(q, k, g, dO, D, dv, d);
+  prof_mark("simt_bwd_dv", st);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int sm2 = (int)dqk_smem(d);
+  e = allow_smem(bwd_dqk_kernel<T>, sm2);
+  if (e != cudaSuccess) return e;
+  dim3 g3((unsigned)(d.dk / kKB), bhp);
+  bwd_dqk_kernel<T><<<g3, kThreads, sm2, st>>>(q, k, v, g, dO, S_in, D, carry, dq, dk, dg, qdq,
+                                               d);
+  prof_mark("simt_bwd_dqk", st);
   return cudaGetLastError();
 }
 
@@ -613,22 +643,7 @@ cudaError_t backward_t(const Dims& d, const T* q, const T* k, const T* v, const 
   if (e != cudaSuccess) return e;
   e = launch_seg_scan_rev(d, D, S_in, gamma, dS_final, dS0, carry, st);
   if (e != cudaSuccess) return e;
-  const int sm1 = (int)fwd_smem(d);
-  e = allow_smem(bwd_dv_kernel<T>, sm1);
-  if (e != cudaSuccess) return e;
-  dim3 g2((unsigned)(d.dv / kNV), bhp);
-  bwd_dv_kernel<T><<<g2, kThreads, sm1, st>>>(q, k, g, dO, D, dv, d);
-  prof_mark("simt_bwd_dv", st);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  const int sm2 = (int)dqk_smem(d);
-  e = allow_smem(bwd_dqk_kernel<T>, sm2);
-  if (e != cudaSuccess) return e;
-  dim3 g3((unsigned)(d.dk / kKB), bhp);
-  bwd_dqk_kernel<T><<<g3, kThreads, sm2, st>>>(q, k, v, g, dO, S_in, D, carry, dq, dk, dg, qdq,
-                                               d);
-  prof_mark("simt_bwd_dqk", st);
-  return cudaGetLastError();
+  return bwd_main_t<T>(d, q, k, v, g, S_in, dO, dq, dk, dv, dg, D, carry, qdq, st);
 }
 
 }  // namespace
@@ -664,6 +679,23 @@ cudaError_t simt_backward(const Dims& d, const void* q, const void* k, const voi
   return backward_t<T>(d, (const T*)q, (const T*)k, (const T*)v, (const T*)g, S_in, gamma,
                        (const T*)d_o, dS_final, (T*)dq, (T*)dk, (T*)dv, (T*)dg, dS0, D, carry,
                        qdq, st);
+}
+
+// Single steps of the SIMT path (bf16 I/O), used by the tensor-core path for
+// the steps it does not replace.
+cudaError_t simt_fwd_out_bf16(const Dims& d, const void* q, const void* k, const void* v,
+                              const void* g, const float* S_in, void* o, cudaStream_t st) {
+  using T = __nv_bfloat16;
+  return fwd_out_t<T>(d, (const T*)q, (const T*)k, (const T*)v, (const T*)g, S_in, (T*)o, st);
+}
+
+cudaError_t simt_bwd_main_bf16(const Dims& d, const void* q, const void* k, const void* v,
+                               const void* g, const float* S_in, const void* d_o, void* dq,
+                               void* dk, void* dv, void* dg, float* D, float* carry, float* qdq,
+                               cudaStream_t st) {
+  using T = __nv_bfloat16;
+  return bwd_main_t<T>(d, (const T*)q, (const T*)k, (const T*)v, (const T*)g, S_in,
+                       (const T*)d_o, (T*)dq, (T*)dk, (T*)dv, (T*)dg, D, carry, qdq, st);
 }
 
 }  // namespace zeco

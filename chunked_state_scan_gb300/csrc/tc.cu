@@ -1,23 +1,33 @@
-// tc.cu -- tcgen05 tensor-core path (bf16 I/O, fp32 accumulation in TMEM).
+// tc.cu -- the tcgen05 tensor-core path (bf16 I/O, fp32 accumulation):
+// launch sequence of the forward and backward.  Steps without a tensor-core
+// kernel yet run their CUDA-core (SIMT) kernel.
 #include "common.cuh"
 #include "launch.h"
 
 namespace zeco {
 
-bool tc_supported(const Dims& d) {
-  (void)d;
-  return false;
+bool tc_supported(const Dims& d) { return tc_state_supported(d); }
+
+cudaError_t tc_forward(const Dims& d, const void* q, const void* k, const void* v,
+                       const void* g, const float* S0, void* o, float* S_final, float* S_in,
+                       float* gamma, cudaStream_t st) {
+  cudaError_t e = tc_chunk_state(d, k, v, g, S_in, gamma, st);
+  if (e != cudaSuccess) return e;
+  e = launch_seg_scan_fwd(d, S_in, gamma, S0, S_final, st);
+  if (e != cudaSuccess) return e;
+  return tc_fwd_supported(d) ? tc_fwd_out(d, q, k, v, g, S_in, o, st)
+                             : simt_fwd_out_bf16(d, q, k, v, g, S_in, o, st);
 }
 
-cudaError_t tc_forward(const Dims&, const void*, const void*, const void*, const void*,
-                       const float*, void*, float*, float*, float*, cudaStream_t) {
-  return cudaErrorNotSupported;
-}
-
-cudaError_t tc_backward(const Dims&, const void*, const void*, const void*, const void*,
-                        const float*, const float*, const void*, const float*, void*, void*,
-                        void*, void*, float*, float*, float*, float*, cudaStream_t) {
-  return cudaErrorNotSupported;
+cudaError_t tc_backward(const Dims& d, const void* q, const void* k, const void* v,
+                        const void* g, const float* S_in, const float* gamma, const void* d_o,
+                        const float* dS_final, void* dq, void* dk, void* dv, void* dg,
+                        float* dS0, float* D, float* carry, float* qdq, cudaStream_t st) {
+  cudaError_t e = tc_dstate_local(d, q, d_o, g, D, st);
+  if (e != cudaSuccess) return e;
+  e = launch_seg_scan_rev(d, D, S_in, gamma, dS_final, dS0, carry, st);
+  if (e != cudaSuccess) return e;
+  return simt_bwd_main_bf16(d, q, k, v, g, S_in, d_o, dq, dk, dv, dg, D, carry, qdq, st);
 }
 
 }  // namespace zeco

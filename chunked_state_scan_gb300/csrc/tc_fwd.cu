@@ -1,0 +1,316 @@
+// tc_fwd.cu -- pass 2 of the forward on tcgen05 tensor cores.
+//
+// Every segment re-runs its chunks from its incoming global state S_in[p] and
+// writes its outputs: intra-chunk decay-masked attention ("diagonal
+// attention") plus the inter-chunk state term, with the chunk state carried
+// on chip (ZeCO two-pass operator, second pass over Q, K, V: Pith review of
+// ZeCO, referee major comment 3 on Algorithm 1; the chunk loop is sequential,
+// minor comment 5 on Algorithm 3).  Per chunk of C = 64 tokens, with b the
+// inclusive cumulative log-decay from the chunk start (per d_k row):
+//
+//   Q~ = q .* e^{b},   K~ = k .* e^{-b}                   (Pith review, minor comment 4:
+//                                                          the K/Lambda, K.Gamma pair)
+//   A  = Q~ K~^T,  masked to s <= t                        (intra-chunk scores)
+//   o  = Q~ S + A V                                        (S = state before the chunk)
+//   S <- e^{b_last} .* (S + K~^T V)                        (state after the chunk)
+//
+// One CTA owns (b, h, segment, 128 d_v columns) and keeps S^T (lanes = d_v
+// column j, TMEM columns = d_k row i) in fp32 in tensor memory, plus a bf16
+// copy of S^T that is the A operand (read from TMEM) of o^T = S^T Q~^T.
+// e^{b_t} and e^{-b_t} come from one exponential per element: prefix products
+// of alpha give e^{b_t}, suffix products give e^{b_last - b_t}, and one
+// reciprocal per row gives e^{-b_last}.
+//
+// TMEM columns: [0, DK) S^T fp32 | [256, 256 + DK/2) S^T bf16 | [384, 448) A
+// (M = 64 layout) | [448, 512) o^T.
+#include <cuda.h>
+
+#include "common.cuh"
+#include "launch.h"
+#include "tc_common.cuh"
+
+namespace zeco {
+bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                    uint32_t box_rows);
+
+namespace {
+
+using namespace tc;
+
+constexpr int kC = 64;        // chunk length
+constexpr int kNV = 128;      // d_v columns per CTA
+constexpr int kThreads = 256;
+constexpr uint32_t kColS16 = 256, kColA = 384, kColO = 448;
+
+__device__ int g_fwd_status = 0;
+
+template <int DK>
+struct FwdSmem {
+  static constexpr int kTile = DK * kC * 2;  // q / k / g tile bytes
+  static constexpr int kQ = 0, kK = kTile, kG = 2 * kTile, kV = 3 * kTile;
+  static constexpr int kP = kV + kNV * kC * 2;
+  static constexpr int kE = kP + kC * kC * 2;
+  static constexpr int kBytes = kE + DK * 4;
+};
+
+template <int DK>
+__global__ void __launch_bounds__(kThreads, 1)
+tc_fwd_out_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmV,
+                  const float* __restrict__ S_in, __nv_bfloat16* __restrict__ o, int64_t T, int dv,
+                  int P, int64_t L) {
+  using SM = FwdSmem<DK>;
+  extern __shared__ __align__(1024) unsigned char smraw[];
+  unsigned char* sm = (unsigned char*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
+  unsigned char* sQ = sm + SM::kQ;
+  unsigned char* sK = sm + SM::kK;
+  unsigned char* sG = sm + SM::kG;
+  unsigned char* sV = sm + SM::kV;
+  unsigned char* sP = sm + SM::kP;
+  float* sE = reinterpret_cast<float*>(sm + SM::kE);
+  __shared__ uint64_t bar_qkg, bar_v, bar_g1, bar_g2;
+  __shared__ uint32_t tmem_base;
+  __shared__ int abort_flag;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int lg = warp & 3;       // TMEM lane group of this warp
+  const int half = warp >> 2;    // which half of the columns this warp handles
+  const int64_t bh = blockIdx.y / P;
+  const int p = blockIdx.y % P;
+  const int j0 = blockIdx.x * kNV;
+  const int64_t row0 = bh * T + (int64_t)p * L;
+  const int nc = (int)(L / kC);
+
+  if (tid == 0) {
+    mbar_init(&bar_qkg, 1);
+    mbar_init(&bar_v, 1);
+    mbar_init(&bar_g1, 1);
+    mbar_init(&bar_g2, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmQ);
+    prefetch_tmap(&tmK);
+    prefetch_tmap(&tmG);
+    prefetch_tmap(&tmV);
+  }
+  if (warp == 0) tmem_alloc(&tmem_base, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base;
+  const uint32_t lane_off = (uint32_t)(lg * 32) << 16;
+
+  auto issue_qkg = [&](int n) {
+    const int32_t r = (int32_t)(row0 + (int64_t)n * kC);
+    mbar_expect_tx(&bar_qkg, 3 * SM::kTile);
+    for (int b = 0; b < DK / 64; ++b) {
+      tma_load_2d(sQ + b * 8192, &tmQ, b * 64, r, &bar_qkg);
+      tma_load_2d(sK + b * 8192, &tmK, b * 64, r, &bar_qkg);
+      tma_load_2d(sG + b * 8192, &tmG, b * 64, r, &bar_qkg);
+    }
+  };
+  auto issue_v = [&](int n) {
+    const int32_t r = (int32_t)(row0 + (int64_t)n * kC);
+    mbar_expect_tx(&bar_v, kNV * kC * 2);
+    for (int b = 0; b < kNV / 64; ++b) tma_load_2d(sV + b * 8192, &tmV, j0 + b * 64, r, &bar_v);
+  };
+  if (tid == 0) {
+    issue_qkg(0);
+    issue_v(0);
+  }
+
+  // ---- initial state: S^T fp32 and its bf16 copy from S_in[p]
+  {
+    const float* Sp = S_in + ((size_t)bh * (P + 1) + p) * DK * dv + j0 + lg * 32 + lane;
+    for (int c = half * (DK / 2); c < (half + 1) * (DK / 2); c += 32) {
+      float r[32];
+#pragma unroll
+      for (int u = 0; u < 32; ++u) r[u] = Sp[(size_t)(c + u) * dv];
+      tmem_st32(tmem + lane_off + c, r);
+      uint32_t h[16];
+#pragma unroll
+      for (int u = 0; u < 16; ++u) h[u] = pack_bf16(r[2 * u], r[2 * u + 1]);
+      tmem_st16(tmem + lane_off + kColS16 + c / 2, h);
+    }
+    tmem_st_wait();
+  }
+
+  // prologue geometry: thread tid < DK owns d_k column i = tid
+  const uint32_t pe_off = (uint32_t)(tid >> 6) * 8192u;
+  const uint32_t pe_chunk = (uint32_t)((tid & 63) >> 3);
+  const uint32_t pe_sub = (uint32_t)(tid & 7) * 2u;
+
+  for (int n = 0; n < nc; ++n) {
+    const uint32_t par = (uint32_t)(n & 1);
+    // ------------------------------------------------ prologue: Q~, K~, e^{b_last}
+    if (!mbar_wait(&bar_qkg, par)) {
+      atomicExch(&g_fwd_status, 1);
+      abort_flag = 1;
+    }
+    if (tid < DK) {
+      float alpha[kC];
+      float pre = 1.f;
+#pragma unroll
+      for (int t = 0; t < kC; ++t) {
+        const uint32_t off = pe_off + sw128((uint32_t)t, pe_chunk) + pe_sub;
+        const float gv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(sG + off));
+        alpha[t] = __expf(gv);
+        pre *= alpha[t];
+        __nv_bfloat16* qe = reinterpret_cast<__nv_bfloat16*>(sQ + off);
+        *qe = __float2bfloat16_rn(__bfloat162float(*qe) * pre);
+      }
+      sE[tid] = pre;  // e^{b_last}
+      const float rinv = 1.0f / pre;
+      float suf = 1.f;
+#pragma unroll
+      for (int t = kC - 1; t >= 0; --t) {
+        const uint32_t off = pe_off + sw128((uint32_t)t, pe_chunk) + pe_sub;
+        __nv_bfloat16* ke = reinterpret_cast<__nv_bfloat16*>(sK + off);
+        *ke = __float2bfloat16_rn(__bfloat162float(*ke) * (suf * rinv));
+        suf *= alpha[t];
+      }
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (abort_flag) break;
+    // ------------------------------------------------ MMA group 1
+    if (tid == 0) {
+      tc_fence_after();
+      const uint32_t q0 = smem_u32(sQ), k0 = smem_u32(sK), v0 = smem_u32(sV);
+      // A = Q~ K~^T   (M = 64 tokens t, N = 64 tokens s, K = DK)
+      constexpr uint32_t idA = idesc_bf16(64, 64, false, false);
+      // o^T = S^T Q~^T   (M = 128 columns j, N = 64 tokens t, K = DK; A from TMEM)
+      constexpr uint32_t idO = idesc_bf16(128, 64, false, false);
+#pragma unroll
+      for (int kb = 0; kb < DK / 64; ++kb)
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t qd = sdesc_sw128(q0 + kb * 8192 + kk * 32, 16, 1024);
+          const uint64_t kd = sdesc_sw128(k0 + kb * 8192 + kk * 32, 16, 1024);
+          umma_bf16(tmem + kColA, qd, kd, idA, (kb | kk) ? 1u : 0u);
+          umma_bf16_ta(tmem + kColO, tmem + kColS16 + kb * 32 + kk * 8, qd, idO,
+                       (kb | kk) ? 1u : 0u);
+        }
+      // S^T += V^T K~   (M = 128 columns j, N = DK rows i, K = 64 tokens s)
+      if (!mbar_wait(&bar_v, par)) {
+        atomicExch(&g_fwd_status, 1);
+      }
+      tc_fence_after();
+      constexpr uint32_t idS = idesc_bf16(128, DK, true, true);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const uint64_t vd = sdesc_sw128(v0 + kk * 2048, 8192, 1024);
+        const uint64_t kd = sdesc_sw128(k0 + kk * 2048, 8192, 1024);
+        umma_bf16(tmem, vd, kd, idS, 1u);
+      }
+      umma_commit(&bar_g1);
+    }
+    if (!mbar_wait(&bar_g1, par)) atomicExch(&g_fwd_status, 1);
+    tc_fence_after();
+    // ------------------------------------------------ mask A -> P (bf16, K-major [t][s])
+    if (warp < 4) {
+      float a[64];
+      tmem_ld32(tmem + lane_off + kColA, a);
+      tmem_ld32(tmem + lane_off + kColA + 32, a + 32);
+      tmem_ld_wait();
+      if (lane < 16) {
+        const int t = warp * 16 + lane;  // M = 64 layout: row 16w + l sits in lane 32w + l
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          uint32_t w4[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int s0 = c * 8 + 2 * u;
+            w4[u] = pack_bf16(s0 <= t ? a[s0] : 0.f, s0 + 1 <= t ? a[s0 + 1] : 0.f);
+          }
+          *reinterpret_cast<uint4*>(sP + sw128((uint32_t)t, (uint32_t)c)) =
+              make_uint4(w4[0], w4[1], w4[2], w4[3]);
+        }
+      }
+    }
+    // ------------------------------------------------ S <- e^{b_last} .* S, refresh bf16 copy
+    for (int c = half * (DK / 2); c < (half + 1) * (DK / 2); c += 32) {
+      float r[32];
+      tmem_ld32(tmem + lane_off + c, r);
+      tmem_ld_wait();
+#pragma unroll
+      for (int u = 0; u < 32; ++u) r[u] *= sE[c + u];
+      tmem_st32(tmem + lane_off + c, r);
+      uint32_t h[16];
+#pragma unroll
+      for (int u = 0; u < 16; ++u) h[u] = pack_bf16(r[2 * u], r[2 * u + 1]);
+      tmem_st16(tmem + lane_off + kColS16 + c / 2, h);
+    }
+    tmem_st_wait();
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    // ------------------------------------------------ MMA group 2: o^T += V^T P^T
+    if (tid == 0) {
+      if (n + 1 < nc) issue_qkg(n + 1);  // q, k, g buffers are free now
+      tc_fence_after();
+      const uint32_t v0 = smem_u32(sV), p0 = smem_u32(sP);
+      constexpr uint32_t idO2 = idesc_bf16(128, 64, true, false);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const uint64_t vd = sdesc_sw128(v0 + kk * 2048, 8192, 1024);
+        const uint64_t pd = sdesc_sw128(p0 + kk * 32, 16, 1024);
+        umma_bf16(tmem + kColO, vd, pd, idO2, 1u);
+      }
+      umma_commit(&bar_g2);
+    }
+    if (!mbar_wait(&bar_g2, par)) atomicExch(&g_fwd_status, 1);
+    tc_fence_after();
+    if (tid == 0 && n + 1 < nc) issue_v(n + 1);  // V buffer is free now
+    // ------------------------------------------------ epilogue: o^T -> o
+    {
+      float r[32];
+      tmem_ld32(tmem + lane_off + kColO + half * 32, r);
+      tmem_ld_wait();
+      __nv_bfloat16* op = o + (size_t)(row0 + (int64_t)n * kC + half * 32) * dv + j0 + lg * 32 + lane;
+#pragma unroll
+      for (int u = 0; u < 32; ++u) op[(size_t)u * dv] = __float2bfloat16_rn(r[u]);
+    }
+    tc_fence_before();
+    __syncthreads();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+template <int DK>
+cudaError_t launch_fwd_out(const Dims& d, const void* q, const void* k, const void* v,
+                           const void* g, const float* S_in, void* o, cudaStream_t st) {
+  CUtensorMap tq, tk, tg, tv;
+  const uint64_t rows = (uint64_t)(d.B * d.H * d.T);
+  if (!make_tmap_bf16(&tq, q, rows, DK, kC) || !make_tmap_bf16(&tk, k, rows, DK, kC) ||
+      !make_tmap_bf16(&tg, g, rows, DK, kC) || !make_tmap_bf16(&tv, v, rows, d.dv, kC))
+    return cudaErrorInvalidValue;
+  const int smem = FwdSmem<DK>::kBytes + 1024;
+  auto kern = tc_fwd_out_kernel<DK>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((unsigned)(d.dv / kNV), (unsigned)(d.B * d.H * d.P));
+  kern<<<grid, kThreads, smem, st>>>(tq, tk, tg, tv, S_in, (__nv_bfloat16*)o, d.T, (int)d.dv,
+                                     d.P, d.L);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool tc_fwd_supported(const Dims& d) {
+  return d.bf16 && (d.dk == 128 || d.dk == 256) && d.dv % kNV == 0 && d.C == kC &&
+         d.L % kC == 0;
+}
+
+cudaError_t tc_fwd_out(const Dims& d, const void* q, const void* k, const void* v, const void* g,
+                       const float* S_in, void* o, cudaStream_t st) {
+  cudaError_t e = d.dk == 256 ? launch_fwd_out<256>(d, q, k, v, g, S_in, o, st)
+                              : launch_fwd_out<128>(d, q, k, v, g, S_in, o, st);
+  prof_mark("tc_fwd_out", st);
+  return e;
+}
+
+}  // namespace zeco

@@ -1,0 +1,240 @@
+// tc_state.cu -- segment-state contraction on tcgen05 tensor cores.
+//
+// Pass 1 of the forward (local state of every segment from a zero state;
+// ZeCO two-pass operator, Pith review of ZeCO, referee major comment 3 on
+// Algorithm 1, and the Appendix A.1 decomposition) and the backward's
+// pre-pass (the adjoint state each segment sends backward, the dKV pass of
+// Linear Attention Sequence Parallelism) are the same weighted contraction
+// over the L tokens of a segment:
+//
+//   out[i, j] = sum_{t in segment} w_t[i] * x_t[i] * y_t[j]
+//
+//   forward  (REV): x = k, y = v,  w_t = exp(sum_{r > t} g_r)   (decay t -> segment end)
+//   backward (FWD): x = q, y = do, w_t = exp(sum_{r <= t} g_r)  (decay segment start -> t)
+//
+// Both weights are <= 1, so no chunk-level rescaling of the accumulator is
+// needed: the running log-decay is carried by the thread that owns row i,
+// walking the segment backwards (REV) or forwards (FWD).  The forward also
+// writes gamma_p[i] = exp(sum_{t in segment} g_t[i]).
+//
+// Tiling: one CTA = 128 d_k rows (M) x NT d_v columns (N, 256 or 128) of one
+// (b, h, segment); K = 64 tokens per stage, 3 stages.  A = (w .* x)^T is
+// written by the threads straight into the 128B-swizzled MN-major operand
+// layout (row i contiguous over tokens' rows); B = y arrives by TMA in the
+// same layout.  The accumulator lives in TMEM (NT fp32 columns); one thread
+// issues the MMAs.
+#include <cuda.h>
+
+#include "common.cuh"
+#include "launch.h"
+#include "tc_common.cuh"
+
+namespace zeco {
+namespace {
+
+using namespace tc;
+
+constexpr int kStages = 3;
+constexpr int kTok = 64;                // tokens per stage (MMA K)
+constexpr int kM = 128;                 // d_k rows per CTA
+constexpr int kXBytes = kTok * kM * 2;  // 16 KB: x tile, overwritten in place by A = (w .* x)
+constexpr int kGBytes = kTok * kM * 2;  // 16 KB: log_alpha tile
+
+__device__ int g_tc_status = 0;  // set when a bounded wait gives up
+
+template <int NT, bool REV>
+__global__ void __launch_bounds__(128, 1)
+tc_seg_state_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmG,
+                    const __grid_constant__ CUtensorMap tmY, float* __restrict__ out,
+                    float* __restrict__ gamma, int64_t T, int dk, int dv, int P, int64_t L,
+                    int slot_off) {
+  constexpr int kBBytes = kTok * NT * 2;
+  constexpr int kStageBytes = kXBytes + kGBytes + kBBytes;
+  extern __shared__ __align__(1024) unsigned char smraw[];
+  unsigned char* sm = (unsigned char*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
+  __shared__ uint64_t tma_bar[kStages], mma_bar[kStages];
+  __shared__ uint32_t tmem_base;
+  __shared__ int abort_flag;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t bh = blockIdx.z / P;
+  const int p = blockIdx.z % P;
+  const int i0 = blockIdx.y * kM, j0 = blockIdx.x * NT;
+  const int i = i0 + tid;
+  const int64_t row0 = bh * T + (int64_t)p * L;  // first token row of the segment
+  const int nblk = (int)(L / kTok);
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&tma_bar[s], 1);
+      mbar_init(&mma_bar[s], 1);
+    }
+    abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmX);
+    prefetch_tmap(&tmG);
+    prefetch_tmap(&tmY);
+  }
+  if (warp == 0) tmem_alloc(&tmem_base, NT);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base;
+
+  auto blk_row = [&](int it) -> int32_t {  // first token row of the it-th stage
+    const int b = REV ? (nblk - 1 - it) : it;
+    return (int32_t)(row0 + (int64_t)b * kTok);
+  };
+  auto issue_tma = [&](int it) {
+    const int s = it % kStages;
+    unsigned char* base = sm + s * kStageBytes;
+    const int32_t r = blk_row(it);
+    mbar_expect_tx(&tma_bar[s], kStageBytes);
+    for (int mb = 0; mb < kM / 64; ++mb) {
+      tma_load_2d(base + mb * 8192, &tmX, i0 + mb * 64, r, &tma_bar[s]);
+      tma_load_2d(base + kXBytes + mb * 8192, &tmG, i0 + mb * 64, r, &tma_bar[s]);
+    }
+    for (int nb = 0; nb < NT / 64; ++nb)
+      tma_load_2d(base + kXBytes + kGBytes + nb * 8192, &tmY, j0 + nb * 64, r, &tma_bar[s]);
+  };
+
+  if (tid == 0) issue_tma(0);
+  float run = 0.f;  // running log-decay of row i
+  // row i of the tiles lives in MN block tid/64, 16-byte chunk (tid%64)/8, element tid%8
+  const uint32_t a_blk = (uint32_t)(tid >> 6) * 8192u;
+  const uint32_t a_chunk = (uint32_t)((tid & 63) >> 3);
+  const uint32_t a_sub = (uint32_t)(tid & 7) * 2u;
+
+  for (int it = 0; it < nblk; ++it) {
+    const int s = it % kStages;
+    unsigned char* xbuf = sm + s * kStageBytes;
+    // prefetch the next stage (its buffers were last read by MMA it+1-kStages)
+    if (tid == 0 && it + 1 < nblk) {
+      const int jn = it + 1 - kStages;
+      if (jn >= 0 && !mbar_wait(&mma_bar[(it + 1) % kStages], (jn / kStages) & 1)) {
+        atomicExch(&g_tc_status, 1);
+        abort_flag = 1;
+      }
+      issue_tma(it + 1);
+    }
+    if (!mbar_wait(&tma_bar[s], (it / kStages) & 1)) {
+      atomicExch(&g_tc_status, 1);
+      abort_flag = 1;
+    }
+    // A = (w .* x) written over x, row i = this thread
+#pragma unroll 8
+    for (int u = 0; u < kTok; ++u) {
+      const int tt = REV ? (kTok - 1 - u) : u;
+      const uint32_t off = a_blk + sw128((uint32_t)tt, a_chunk) + a_sub;
+      const float gv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(xbuf + kXBytes + off));
+      __nv_bfloat16* xe = reinterpret_cast<__nv_bfloat16*>(xbuf + off);
+      const float xv = __bfloat162float(*xe);
+      float w;
+      if (REV) {
+        w = __expf(run);
+        run += gv;
+      } else {
+        run += gv;
+        w = __expf(run);
+      }
+      *xe = __float2bfloat16_rn(xv * w);
+    }
+    fence_async_smem();
+    __syncthreads();
+    if (abort_flag) break;
+    if (tid == 0) {
+      tc_fence_after();
+      const uint32_t a0 = smem_u32(xbuf), b0 = a0 + kXBytes + kGBytes;
+      constexpr uint32_t id = idesc_bf16(kM, NT, true, true);
+#pragma unroll
+      for (int kk = 0; kk < kTok / 16; ++kk) {
+        const uint64_t ad = sdesc_sw128(a0 + kk * 2048, 8192, 1024);
+        const uint64_t bd = sdesc_sw128(b0 + kk * 2048, 8192, 1024);
+        umma_bf16(tmem, ad, bd, id, (it > 0 || kk > 0) ? 1u : 0u);
+      }
+      umma_commit(&mma_bar[s]);
+    }
+  }
+  __syncthreads();
+  const bool ok = !abort_flag;
+  if (ok) {
+    const int last = nblk - 1;
+    if (!mbar_wait(&mma_bar[last % kStages], (last / kStages) & 1)) atomicExch(&g_tc_status, 1);
+    tc_fence_after();
+    float* orow = out + (((size_t)bh * (P + 1) + p + slot_off) * dk + i) * dv + j0;
+#pragma unroll 1
+    for (int c = 0; c < NT; c += 32) {
+      float r[32];
+      tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + c, r);
+      tmem_ld_wait();
+      float4* dst = reinterpret_cast<float4*>(orow + c);
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        dst[u] = make_float4(r[4 * u], r[4 * u + 1], r[4 * u + 2], r[4 * u + 3]);
+    }
+    if (REV && gamma && blockIdx.x == 0) gamma[((size_t)bh * P + p) * dk + i] = __expf(run);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, NT);
+  (void)lane;
+}
+
+}  // namespace
+
+// 2D bf16 tensor map over a [rows, cols] row-major matrix with a box of
+// 64 columns x box_rows rows and 128-byte swizzle.
+bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                    uint32_t box_rows) {
+  cuuint64_t gdim[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t gstr[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return cuTensorMapEncodeTiled(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
+                                gdim, gstr, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int NT, bool REV>
+static cudaError_t launch_state(const Dims& d, const void* x, const void* y, const void* g,
+                                float* out, float* gamma, int slot_off, cudaStream_t st) {
+  CUtensorMap tx, tg, ty;
+  const uint64_t rows = (uint64_t)(d.B * d.H * d.T);
+  if (!make_tmap_bf16(&tx, x, rows, (uint64_t)d.dk, kTok) ||
+      !make_tmap_bf16(&tg, g, rows, (uint64_t)d.dk, kTok) ||
+      !make_tmap_bf16(&ty, y, rows, (uint64_t)d.dv, kTok))
+    return cudaErrorInvalidValue;
+  const int smem = kStages * (kXBytes + kGBytes + kTok * NT * 2) + 1024;
+  auto kern = tc_seg_state_kernel<NT, REV>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((unsigned)(d.dv / NT), (unsigned)(d.dk / kM), (unsigned)(d.B * d.H * d.P));
+  kern<<<grid, 128, smem, st>>>(tx, tg, ty, out, gamma, d.T, (int)d.dk, (int)d.dv, d.P, d.L,
+                                slot_off);
+  return cudaGetLastError();
+}
+
+bool tc_state_supported(const Dims& d) {
+  return d.bf16 && d.dk % kM == 0 && d.dv % 128 == 0 && d.L % kTok == 0;
+}
+
+cudaError_t tc_chunk_state(const Dims& d, const void* k, const void* v, const void* g,
+                           float* S_in, float* gamma, cudaStream_t st) {
+  cudaError_t e = (d.dv % 256 == 0)
+                      ? launch_state<256, true>(d, k, v, g, S_in, gamma, 1, st)
+                      : launch_state<128, true>(d, k, v, g, S_in, gamma, 1, st);
+  prof_mark("tc_chunk_state", st);
+  return e;
+}
+
+cudaError_t tc_dstate_local(const Dims& d, const void* q, const void* d_o, const void* g,
+                            float* D, cudaStream_t st) {
+  cudaError_t e = (d.dv % 256 == 0)
+                      ? launch_state<256, false>(d, q, d_o, g, D, nullptr, 0, st)
+                      : launch_state<128, false>(d, q, d_o, g, D, nullptr, 0, st);
+  prof_mark("tc_dstate_local", st);
+  return e;
+}
+
+}  // namespace zeco
