@@ -32,6 +32,11 @@ cudaError_t simt_bwd_main_bf16(const Dims& d, const void* q, const void* k, cons
                                void* dk, void* dv, void* dg, float* D, float* carry, float* qdq,
                                cudaStream_t st);
 
+cudaError_t simt_bwd_dqk_bf16(const Dims& d, const void* q, const void* k, const void* v,
+                              const void* g, const float* S_in, const void* d_o, void* dq,
+                              void* dk, void* dg, float* D, float* carry, float* qdq,
+                              cudaStream_t st);
+
 // ---- tcgen05 tensor-core path (tc_*.cu) --------------------------------
 bool tc_state_supported(const Dims& d);
 cudaError_t tc_chunk_state(const Dims& d, const void* k, const void* v, const void* g,
@@ -41,6 +46,8 @@ cudaError_t tc_dstate_local(const Dims& d, const void* q, const void* d_o, const
 bool tc_fwd_supported(const Dims& d);
 cudaError_t tc_fwd_out(const Dims& d, const void* q, const void* k, const void* v, const void* g,
                        const float* S_in, void* o, cudaStream_t st);
+cudaError_t tc_bwd_dv(const Dims& d, const void* q, const void* k, const void* d_o,
+                      const void* g, const float* D, void* dv, cudaStream_t st);
 bool tc_supported(const Dims& d);
 cudaError_t tc_forward(const Dims& d, const void* q, const void* k, const void* v,
                        const void* g, const float* S0, void* o, float* S_final, float* S_in,

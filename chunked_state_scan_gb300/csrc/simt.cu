@@ -698,4 +698,21 @@ cudaError_t simt_bwd_main_bf16(const Dims& d, const void* q, const void* k, cons
                        (const T*)d_o, (T*)dq, (T*)dk, (T*)dv, (T*)dg, D, carry, qdq, st);
 }
 
+cudaError_t simt_bwd_dqk_bf16(const Dims& d, const void* q, const void* k, const void* v,
+                              const void* g, const float* S_in, const void* d_o, void* dq,
+                              void* dk, void* dg, float* D, float* carry, float* qdq,
+                              cudaStream_t st) {
+  using T = __nv_bfloat16;
+  const unsigned bhp = (unsigned)(d.B * d.H * d.P);
+  const int sm2 = (int)dqk_smem(d);
+  cudaError_t e = allow_smem(bwd_dqk_kernel<T>, sm2);
+  if (e != cudaSuccess) return e;
+  dim3 g3((unsigned)(d.dk / kKB), bhp);
+  bwd_dqk_kernel<T><<<g3, kThreads, sm2, st>>>((const T*)q, (const T*)k, (const T*)v,
+                                               (const T*)g, (const T*)d_o, S_in, D, carry,
+                                               (T*)dq, (T*)dk, (T*)dg, qdq, d);
+  prof_mark("simt_bwd_dqk", st);
+  return cudaGetLastError();
+}
+
 }  // namespace zeco

@@ -27,7 +27,11 @@ cudaError_t tc_backward(const Dims& d, const void* q, const void* k, const void*
   if (e != cudaSuccess) return e;
   e = launch_seg_scan_rev(d, D, S_in, gamma, dS_final, dS0, carry, st);
   if (e != cudaSuccess) return e;
-  return simt_bwd_main_bf16(d, q, k, v, g, S_in, d_o, dq, dk, dv, dg, D, carry, qdq, st);
+  if (!tc_fwd_supported(d))
+    return simt_bwd_main_bf16(d, q, k, v, g, S_in, d_o, dq, dk, dv, dg, D, carry, qdq, st);
+  e = tc_bwd_dv(d, q, k, d_o, g, D, dv, st);
+  if (e != cudaSuccess) return e;
+  return simt_bwd_dqk_bf16(d, q, k, v, g, S_in, d_o, dq, dk, dg, D, carry, qdq, st);
 }
 
 }  // namespace zeco

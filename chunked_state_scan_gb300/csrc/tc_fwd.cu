@@ -21,8 +21,19 @@
 // of alpha give e^{b_t}, suffix products give e^{b_last - b_t}, and one
 // reciprocal per row gives e^{-b_last}.
 //
+// The same kernel, run backwards over the chunks (BWD = true), computes dv
+// from the adjoint state dS of the segment end (D[p+1], from the reverse
+// segment scan): per chunk, in reverse,
+//
+//   dS <- e^{b_last} .* dS                     (adjoint of the state after the chunk,
+//                                               carried to the chunk's tokens)
+//   dv = K~ dS + (A masked)^T do               (K~ (e^{b_last} dS) = K^ dS of the pages)
+//   dS <- dS + Q~^T do                         (adjoint of the state before the chunk)
+//
+// with q/k roles swapped on the output side and do in place of v.
+//
 // TMEM columns: [0, DK) S^T fp32 | [256, 256 + DK/2) S^T bf16 | [384, 448) A
-// (M = 64 layout) | [448, 512) o^T.
+// (M = 64 layout) | [448, 512) o^T (dv^T when BWD).
 #include <cuda.h>
 
 #include "common.cuh"
@@ -53,12 +64,12 @@ struct FwdSmem {
   static constexpr int kBytes = kE + DK * 4;
 };
 
-template <int DK>
+template <int DK, bool BWD>
 __global__ void __launch_bounds__(kThreads, 1)
-tc_fwd_out_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                  const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmV,
-                  const float* __restrict__ S_in, __nv_bfloat16* __restrict__ o, int64_t T, int dv,
-                  int P, int64_t L) {
+tc_sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmV,
+                const float* __restrict__ S_src, __nv_bfloat16* __restrict__ o, int64_t T, int dv,
+                int P, int64_t L) {
   using SM = FwdSmem<DK>;
   extern __shared__ __align__(1024) unsigned char smraw[];
   unsigned char* sm = (unsigned char*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
@@ -115,17 +126,39 @@ tc_fwd_out_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
     for (int b = 0; b < kNV / 64; ++b) tma_load_2d(sV + b * 8192, &tmV, j0 + b * 64, r, &bar_v);
   };
   if (tid == 0) {
-    issue_qkg(0);
-    issue_v(0);
+    issue_qkg(BWD ? nc - 1 : 0);
+    issue_v(BWD ? nc - 1 : 0);
   }
 
-  // ---- initial state: S^T fp32 and its bf16 copy from S_in[p]
+  // ---- initial state: S^T fp32 (and, forward, its bf16 copy) from the state
+  //      entering the segment (forward: S_in[p]) or the adjoint at its end
+  //      (backward: D[p+1]).
   {
-    const float* Sp = S_in + ((size_t)bh * (P + 1) + p) * DK * dv + j0 + lg * 32 + lane;
+    const float* Sp =
+        S_src + ((size_t)bh * (P + 1) + p + (BWD ? 1 : 0)) * DK * dv + j0 + lg * 32 + lane;
     for (int c = half * (DK / 2); c < (half + 1) * (DK / 2); c += 32) {
       float r[32];
 #pragma unroll
       for (int u = 0; u < 32; ++u) r[u] = Sp[(size_t)(c + u) * dv];
+      tmem_st32(tmem + lane_off + c, r);
+      if (!BWD) {
+        uint32_t h[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) h[u] = pack_bf16(r[2 * u], r[2 * u + 1]);
+        tmem_st16(tmem + lane_off + kColS16 + c / 2, h);
+      }
+    }
+    tmem_st_wait();
+  }
+
+  // S^T (fp32) <- e^{b_last} .* S^T (column i scaled by sE[i]) and its bf16 copy
+  auto state_pass = [&]() {
+    for (int c = half * (DK / 2); c < (half + 1) * (DK / 2); c += 32) {
+      float r[32];
+      tmem_ld32(tmem + lane_off + c, r);
+      tmem_ld_wait();
+#pragma unroll
+      for (int u = 0; u < 32; ++u) r[u] *= sE[c + u];
       tmem_st32(tmem + lane_off + c, r);
       uint32_t h[16];
 #pragma unroll
@@ -133,15 +166,16 @@ tc_fwd_out_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
       tmem_st16(tmem + lane_off + kColS16 + c / 2, h);
     }
     tmem_st_wait();
-  }
+  };
 
   // prologue geometry: thread tid < DK owns d_k column i = tid
   const uint32_t pe_off = (uint32_t)(tid >> 6) * 8192u;
   const uint32_t pe_chunk = (uint32_t)((tid & 63) >> 3);
   const uint32_t pe_sub = (uint32_t)(tid & 7) * 2u;
 
-  for (int n = 0; n < nc; ++n) {
-    const uint32_t par = (uint32_t)(n & 1);
+  for (int it = 0; it < nc; ++it) {
+    const int n = BWD ? (nc - 1 - it) : it;  // chunk index in the segment
+    const uint32_t par = (uint32_t)(it & 1);
     // ------------------------------------------------ prologue: Q~, K~, e^{b_last}
     if (!mbar_wait(&bar_qkg, par)) {
       atomicExch(&g_fwd_status, 1);
@@ -170,6 +204,10 @@ tc_fwd_out_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         suf *= alpha[t];
       }
     }
+    if (BWD) {
+      __syncthreads();  // sE complete
+      state_pass();
+    }
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -180,29 +218,34 @@ tc_fwd_out_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
       const uint32_t q0 = smem_u32(sQ), k0 = smem_u32(sK), v0 = smem_u32(sV);
       // A = Q~ K~^T   (M = 64 tokens t, N = 64 tokens s, K = DK)
       constexpr uint32_t idA = idesc_bf16(64, 64, false, false);
-      // o^T = S^T Q~^T   (M = 128 columns j, N = 64 tokens t, K = DK; A from TMEM)
+      // forward:  o^T  = S^T  Q~^T   (M = 128 columns j, N = 64 tokens t, K = DK; A from TMEM)
+      // backward: dv^T = dS^T K~^T   (M = 128 columns j, N = 64 tokens s, K = DK; A from TMEM)
       constexpr uint32_t idO = idesc_bf16(128, 64, false, false);
+      const uint32_t x0 = BWD ? k0 : q0;
 #pragma unroll
       for (int kb = 0; kb < DK / 64; ++kb)
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
           const uint64_t qd = sdesc_sw128(q0 + kb * 8192 + kk * 32, 16, 1024);
           const uint64_t kd = sdesc_sw128(k0 + kb * 8192 + kk * 32, 16, 1024);
+          const uint64_t xd = sdesc_sw128(x0 + kb * 8192 + kk * 32, 16, 1024);
           umma_bf16(tmem + kColA, qd, kd, idA, (kb | kk) ? 1u : 0u);
-          umma_bf16_ta(tmem + kColO, tmem + kColS16 + kb * 32 + kk * 8, qd, idO,
+          umma_bf16_ta(tmem + kColO, tmem + kColS16 + kb * 32 + kk * 8, xd, idO,
                        (kb | kk) ? 1u : 0u);
         }
-      // S^T += V^T K~   (M = 128 columns j, N = DK rows i, K = 64 tokens s)
+      // forward:  S^T  += V^T  K~   (M = 128 columns j, N = DK rows i, K = 64 tokens s)
+      // backward: dS^T += do^T Q~   (M = 128 columns j, N = DK rows i, K = 64 tokens t)
       if (!mbar_wait(&bar_v, par)) {
         atomicExch(&g_fwd_status, 1);
       }
       tc_fence_after();
+      const uint32_t u0 = BWD ? q0 : k0;
       constexpr uint32_t idS = idesc_bf16(128, DK, true, true);
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
         const uint64_t vd = sdesc_sw128(v0 + kk * 2048, 8192, 1024);
-        const uint64_t kd = sdesc_sw128(k0 + kk * 2048, 8192, 1024);
-        umma_bf16(tmem, vd, kd, idS, 1u);
+        const uint64_t ud = sdesc_sw128(u0 + kk * 2048, 8192, 1024);
+        umma_bf16(tmem, vd, ud, idS, 1u);
       }
       umma_commit(&bar_g1);
     }
@@ -229,40 +272,32 @@ tc_fwd_out_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         }
       }
     }
-    // ------------------------------------------------ S <- e^{b_last} .* S, refresh bf16 copy
-    for (int c = half * (DK / 2); c < (half + 1) * (DK / 2); c += 32) {
-      float r[32];
-      tmem_ld32(tmem + lane_off + c, r);
-      tmem_ld_wait();
-#pragma unroll
-      for (int u = 0; u < 32; ++u) r[u] *= sE[c + u];
-      tmem_st32(tmem + lane_off + c, r);
-      uint32_t h[16];
-#pragma unroll
-      for (int u = 0; u < 16; ++u) h[u] = pack_bf16(r[2 * u], r[2 * u + 1]);
-      tmem_st16(tmem + lane_off + kColS16 + c / 2, h);
-    }
+    // forward: S <- e^{b_last} .* S, refresh the bf16 copy for the next chunk
+    if (!BWD) state_pass();
     tmem_st_wait();
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
     // ------------------------------------------------ MMA group 2: o^T += V^T P^T
     if (tid == 0) {
-      if (n + 1 < nc) issue_qkg(n + 1);  // q, k, g buffers are free now
+      if (it + 1 < nc) issue_qkg(BWD ? n - 1 : n + 1);  // q, k, g buffers are free now
       tc_fence_after();
       const uint32_t v0 = smem_u32(sV), p0 = smem_u32(sP);
-      constexpr uint32_t idO2 = idesc_bf16(128, 64, true, false);
+      // forward:  o^T  += V^T  P^T  (B = P, K = s contiguous: K-major)
+      // backward: dv^T += do^T P    (B = P, K = t rows, N = s contiguous: MN-major)
+      constexpr uint32_t idO2 = idesc_bf16(128, 64, true, BWD);
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
         const uint64_t vd = sdesc_sw128(v0 + kk * 2048, 8192, 1024);
-        const uint64_t pd = sdesc_sw128(p0 + kk * 32, 16, 1024);
+        const uint64_t pd = BWD ? sdesc_sw128(p0 + kk * 2048, 8192, 1024)
+                                : sdesc_sw128(p0 + kk * 32, 16, 1024);
         umma_bf16(tmem + kColO, vd, pd, idO2, 1u);
       }
       umma_commit(&bar_g2);
     }
     if (!mbar_wait(&bar_g2, par)) atomicExch(&g_fwd_status, 1);
     tc_fence_after();
-    if (tid == 0 && n + 1 < nc) issue_v(n + 1);  // V buffer is free now
+    if (tid == 0 && it + 1 < nc) issue_v(BWD ? n - 1 : n + 1);  // V buffer is free now
     // ------------------------------------------------ epilogue: o^T -> o
     {
       float r[32];
@@ -280,20 +315,20 @@ tc_fwd_out_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
   if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
-template <int DK>
-cudaError_t launch_fwd_out(const Dims& d, const void* q, const void* k, const void* v,
-                           const void* g, const float* S_in, void* o, cudaStream_t st) {
+template <int DK, bool BWD>
+cudaError_t launch_sweep(const Dims& d, const void* q, const void* k, const void* v,
+                         const void* g, const float* S_src, void* o, cudaStream_t st) {
   CUtensorMap tq, tk, tg, tv;
   const uint64_t rows = (uint64_t)(d.B * d.H * d.T);
   if (!make_tmap_bf16(&tq, q, rows, DK, kC) || !make_tmap_bf16(&tk, k, rows, DK, kC) ||
       !make_tmap_bf16(&tg, g, rows, DK, kC) || !make_tmap_bf16(&tv, v, rows, d.dv, kC))
     return cudaErrorInvalidValue;
   const int smem = FwdSmem<DK>::kBytes + 1024;
-  auto kern = tc_fwd_out_kernel<DK>;
+  auto kern = tc_sweep_kernel<DK, BWD>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)(d.dv / kNV), (unsigned)(d.B * d.H * d.P));
-  kern<<<grid, kThreads, smem, st>>>(tq, tk, tg, tv, S_in, (__nv_bfloat16*)o, d.T, (int)d.dv,
+  kern<<<grid, kThreads, smem, st>>>(tq, tk, tg, tv, S_src, (__nv_bfloat16*)o, d.T, (int)d.dv,
                                      d.P, d.L);
   return cudaGetLastError();
 }
@@ -307,9 +342,17 @@ bool tc_fwd_supported(const Dims& d) {
 
 cudaError_t tc_fwd_out(const Dims& d, const void* q, const void* k, const void* v, const void* g,
                        const float* S_in, void* o, cudaStream_t st) {
-  cudaError_t e = d.dk == 256 ? launch_fwd_out<256>(d, q, k, v, g, S_in, o, st)
-                              : launch_fwd_out<128>(d, q, k, v, g, S_in, o, st);
+  cudaError_t e = d.dk == 256 ? launch_sweep<256, false>(d, q, k, v, g, S_in, o, st)
+                              : launch_sweep<128, false>(d, q, k, v, g, S_in, o, st);
   prof_mark("tc_fwd_out", st);
+  return e;
+}
+
+cudaError_t tc_bwd_dv(const Dims& d, const void* q, const void* k, const void* d_o,
+                      const void* g, const float* D, void* dv, cudaStream_t st) {
+  cudaError_t e = d.dk == 256 ? launch_sweep<256, true>(d, q, k, d_o, g, D, dv, st)
+                              : launch_sweep<128, true>(d, q, k, d_o, g, D, dv, st);
+  prof_mark("tc_bwd_dv", st);
   return e;
 }
 
