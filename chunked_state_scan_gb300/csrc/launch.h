@@ -48,6 +48,10 @@ cudaError_t tc_fwd_out(const Dims& d, const void* q, const void* k, const void* 
                        const float* S_in, void* o, cudaStream_t st);
 cudaError_t tc_bwd_dv(const Dims& d, const void* q, const void* k, const void* d_o,
                       const void* g, const float* D, void* dv, cudaStream_t st);
+bool tc_bwd_qk_supported(const Dims& d);
+cudaError_t tc_bwd_qk(const Dims& d, const void* q, const void* k, const void* v, const void* g,
+                      const float* S_in, const void* d_o, void* dq, void* dk, void* dg, float* D,
+                      float* carry, float* qdq, cudaStream_t st);
 bool tc_supported(const Dims& d);
 cudaError_t tc_forward(const Dims& d, const void* q, const void* k, const void* v,
                        const void* g, const float* S0, void* o, float* S_final, float* S_in,

@@ -31,6 +31,8 @@ cudaError_t tc_backward(const Dims& d, const void* q, const void* k, const void*
     return simt_bwd_main_bf16(d, q, k, v, g, S_in, d_o, dq, dk, dv, dg, D, carry, qdq, st);
   e = tc_bwd_dv(d, q, k, d_o, g, D, dv, st);
   if (e != cudaSuccess) return e;
+  if (tc_bwd_qk_supported(d))
+    return tc_bwd_qk(d, q, k, v, g, S_in, d_o, dq, dk, dg, D, carry, qdq, st);
   return simt_bwd_dqk_bf16(d, q, k, v, g, S_in, d_o, dq, dk, dg, D, carry, qdq, st);
 }
 

@@ -1,0 +1,444 @@
+// tc_bwd_qk.cu -- dq, dk and dlog_alpha of the backward on tcgen05 tensor cores.
+//
+// dq and dk contract over all d_v columns of the state, so the work is split
+// by d_k rows: a pair of CTAs (a thread-block cluster of 2) owns a block of 64
+// d_k rows i of one (b, h, segment); CTA r of the pair holds d_v columns
+// [256 r, 256 r + 256).  Two launches sweep the segment's chunks:
+//
+//   forward sweep, state S (from S_in[p], the global state held since the
+//   forward pass: Pith review of ZeCO, assumptions: Appendix A.4):
+//     dA = do v^T (masked s <= t)
+//     dq = e^{b} .* ( do S^T + dA K~ )          K~ = k .* e^{-b}
+//     S <- e^{b_last} .* (S + K~^T v)
+//   reverse sweep, adjoint dS (from D[p+1], the reverse segment scan):
+//     dS <- e^{b_last} .* dS
+//     dk = e^{-b} .* ( v dS^T + dA^T Q~ )       Q~ = q .* e^{b}
+//     dS <- dS + Q~^T do
+//     dlog_alpha_t = c_p + sum_{u >= t in segment} (q_u dq_u - k_u dk_u)
+//
+// (b: inclusive cumulative log-decay from the chunk start; c_p comes from the
+// reverse segment scan.)  Each CTA forms partial dq^T / dk^T over its half of
+// d_v (both products are linear in the d_v contraction, dA included); the pair
+// adds the two halves through distributed shared memory and each CTA finishes
+// 32 of the 64 rows.
+//
+// Precision of dlog_alpha.  Its suffix sum runs over the whole segment, so
+// errors in the terms add up like a random walk.  Two measures keep them
+// small: (1) the state copy used by the tensor cores is split into two bf16
+// parts (hi + lo), so the state products are accurate to ~2^-17; (2) the terms
+// use the rounded operands that the state itself was built from
+// (bf16(Q~) and bf16(K~) times the raw accumulators), so that the identity's
+// telescoping holds for the rounded model instead of breaking on the rounding.
+//
+// TMEM columns: [0, 128) state (d_v group g of this CTA at 64 g) | [128, 192)
+// dA (M = 64 layout) | [192, 256) dq^T or dk^T (M = 64 layout, lane = d_k row).
+#include <cuda.h>
+
+#include "common.cuh"
+#include "launch.h"
+#include "tc_common.cuh"
+
+namespace zeco {
+bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                    uint32_t box_rows);
+
+namespace {
+
+using namespace tc;
+
+constexpr int kC = 64;
+constexpr int kKB = 64;    // d_k rows per CTA pair
+constexpr int kDV = 512;   // d_v
+constexpr int kDVH = 256;  // d_v columns per CTA
+constexpr int kThreads = 256;
+constexpr uint32_t kColDA = 128, kColAcc = 192;
+
+// shared memory (bytes, 1024-aligned regions)
+constexpr int kOffDO = 0;                        // do tile [64 t][256 j] (4 blocks of 64 j)
+constexpr int kOffV = kOffDO + kC * kDVH * 2;    // v tile
+constexpr int kOffHi = kOffV + kC * kDVH * 2;    // state copy, high part [256 j][64 i]
+constexpr int kOffLo = kOffHi + kDVH * kKB * 2;  // state copy, low part
+constexpr int kOffQ = kOffLo + kDVH * kKB * 2;   // q tile [64 t][64 i]
+constexpr int kOffK = kOffQ + kC * kKB * 2;
+constexpr int kOffG = kOffK + kC * kKB * 2;
+constexpr int kOffP = kOffG + kC * kKB * 2;      // masked dA partial [64 t][64 s] bf16
+constexpr int kOffR = kOffP + kC * kC * 2;       // 2 x [32 rows][64] fp32 from the peer
+constexpr int kOffE = kOffR + 2 * 32 * kC * 4;   // e^{b_last} [64] fp32
+constexpr int kSmem = kOffE + 1024;
+
+__device__ int g_qk_status = 0;
+
+// The decay factors of one d_k column over a chunk, evaluated identically in
+// every place that needs them (so that the rounded operands can be rebuilt
+// bit for bit): alpha_t = exp(g_t), pre_t = prod_{r<=t} alpha_r.
+__device__ __forceinline__ float alpha_of(const __nv_bfloat16* ge) {
+  return __expf(__bfloat162float(*ge));
+}
+
+template <bool REV>
+__global__ void __launch_bounds__(kThreads, 1)
+tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                 const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmV,
+                 const __grid_constant__ CUtensorMap tmDO, const float* __restrict__ S_src,
+                 const float* __restrict__ carry, __nv_bfloat16* __restrict__ out,
+                 __nv_bfloat16* __restrict__ dg, float* __restrict__ qdq, int64_t T, int dk,
+                 int P, int64_t L) {
+  extern __shared__ __align__(1024) unsigned char smraw[];
+  unsigned char* sm = (unsigned char*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
+  unsigned char* sDO = sm + kOffDO;
+  unsigned char* sV = sm + kOffV;
+  unsigned char* sHi = sm + kOffHi;
+  unsigned char* sLo = sm + kOffLo;
+  unsigned char* sQ = sm + kOffQ;
+  unsigned char* sK = sm + kOffK;
+  unsigned char* sG = sm + kOffG;
+  unsigned char* sP = sm + kOffP;
+  float* sR = reinterpret_cast<float*>(sm + kOffR);
+  float* sE = reinterpret_cast<float*>(sm + kOffE);
+  __shared__ uint64_t bar_x, bar_dv, bar_g1, bar_g2;
+  __shared__ uint32_t tmem_base;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int lg = warp & 3, grp = warp >> 2;  // TMEM lane group; this warp's d_v group
+  const uint32_t rank = cluster_ctarank();   // which half of d_v
+  const int64_t bh = blockIdx.y / P;
+  const int p = blockIdx.y % P;
+  const int i0 = (blockIdx.x >> 1) * kKB;
+  const int jb = (int)rank * kDVH;
+  const int64_t row0 = bh * T + (int64_t)p * L;
+  const int nc = (int)(L / kC);
+  // the M = 64 TMEM layout: warp w < 4, lane l < 16 holds row 16 w + l
+  const bool rowt = warp < 4 && lane < 16;
+  const int ii = warp * 16 + lane;                      // d_k row within the block
+  const bool owned = rowt && (uint32_t)(ii >> 5) == rank;  // finished by this CTA
+
+  if (tid == 0) {
+    mbar_init(&bar_x, 1);
+    mbar_init(&bar_dv, 1);
+    mbar_init(&bar_g1, 1);
+    mbar_init(&bar_g2, 1);
+    fence_mbar_init();
+    prefetch_tmap(&tmQ);
+    prefetch_tmap(&tmK);
+    prefetch_tmap(&tmG);
+    prefetch_tmap(&tmV);
+    prefetch_tmap(&tmDO);
+  }
+  if (warp == 0) tmem_alloc(&tmem_base, 256);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base;
+  const uint32_t lane_off = (uint32_t)(lg * 32) << 16;
+
+  auto chunk_row = [&](int n) { return (int32_t)(row0 + (int64_t)n * kC); };
+  auto issue_x = [&](int n) {
+    const int32_t r = chunk_row(n);
+    mbar_expect_tx(&bar_x, 3 * kC * kKB * 2);
+    tma_load_2d(sQ, &tmQ, i0, r, &bar_x);
+    tma_load_2d(sK, &tmK, i0, r, &bar_x);
+    tma_load_2d(sG, &tmG, i0, r, &bar_x);
+  };
+  auto issue_dv = [&](int n) {
+    const int32_t r = chunk_row(n);
+    mbar_expect_tx(&bar_dv, 2 * kC * kDVH * 2);
+    for (int b = 0; b < kDVH / 64; ++b) {
+      tma_load_2d(sDO + b * 8192, &tmDO, jb + b * 64, r, &bar_dv);
+      tma_load_2d(sV + b * 8192, &tmV, jb + b * 64, r, &bar_dv);
+    }
+  };
+  if (tid == 0) {
+    issue_x(REV ? nc - 1 : 0);
+    issue_dv(REV ? nc - 1 : 0);
+  }
+
+  // bf16 hi/lo copy of this warp's state group (lanes = local d_v column j)
+  auto write_copy = [&](const float* r) {
+    const uint32_t j = (uint32_t)(grp * 128 + lg * 32 + lane);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      uint32_t hw[4], lw[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float a = r[8 * c + 2 * u], b = r[8 * c + 2 * u + 1];
+        const __nv_bfloat16 ha = __float2bfloat16_rn(a), hb = __float2bfloat16_rn(b);
+        __nv_bfloat162 h2, l2;
+        h2.x = ha;
+        h2.y = hb;
+        l2 = __floats2bfloat162_rn(a - __bfloat162float(ha), b - __bfloat162float(hb));
+        hw[u] = *reinterpret_cast<uint32_t*>(&h2);
+        lw[u] = *reinterpret_cast<uint32_t*>(&l2);
+      }
+      const uint32_t off = sw128(j, (uint32_t)c);
+      *reinterpret_cast<uint4*>(sHi + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+      *reinterpret_cast<uint4*>(sLo + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+    }
+  };
+
+  // ---- initial state: rows i0..i0+63, this CTA's columns
+  {
+    const float* Sp = S_src + (((size_t)bh * (P + 1) + p + (REV ? 1 : 0)) * dk + i0) * kDV + jb +
+                      grp * 128 + lg * 32 + lane;
+    float r[64];
+#pragma unroll
+    for (int u = 0; u < 64; ++u) r[u] = Sp[(size_t)u * kDV];
+    tmem_st32(tmem + lane_off + grp * 64, r);
+    tmem_st32(tmem + lane_off + grp * 64 + 32, r + 32);
+    if (!REV) write_copy(r);
+    tmem_st_wait();
+  }
+
+  // state <- e^{b_last} .* state (column i scaled by sE[i]) and its hi/lo copy
+  auto state_pass = [&]() {
+    float r[64];
+    tmem_ld32(tmem + lane_off + grp * 64, r);
+    tmem_ld32(tmem + lane_off + grp * 64 + 32, r + 32);
+    tmem_ld_wait();
+#pragma unroll
+    for (int u = 0; u < 64; ++u) r[u] *= sE[u];
+    tmem_st32(tmem + lane_off + grp * 64, r);
+    tmem_st32(tmem + lane_off + grp * 64 + 32, r + 32);
+    write_copy(r);
+    tmem_st_wait();
+  };
+
+  // element (t, ii) of a [64 t][64 i] tile
+  const uint32_t ce = (uint32_t)((ii & 63) >> 3), cs = (uint32_t)(ii & 7) * 2u;
+  auto tile_at = [&](unsigned char* base, int t) -> __nv_bfloat16* {
+    return reinterpret_cast<__nv_bfloat16*>(base + sw128((uint32_t)t, ce) + cs);
+  };
+
+  float run_dg = 0.f;  // dlog_alpha suffix of an owned row (reverse sweep)
+  if (REV && owned) run_dg = carry[((size_t)bh * P + p) * dk + i0 + ii];
+  // peer's partials for my rows land in sR[buf][ii - 32 rank][64]
+  const uint32_t peer = rank ^ 1u;
+
+  for (int it = 0; it < nc; ++it) {
+    const int n = REV ? (nc - 1 - it) : it;
+    const uint32_t par = (uint32_t)(it & 1);
+    if (!mbar_wait(&bar_x, par)) atomicExch(&g_qk_status, 1);
+    // ---- prologue (row-owner threads): forward K~ = bf16(k e^{-b}); reverse Q~ = bf16(q e^{b})
+    if (rowt) {
+      float alpha[kC];
+      float pre = 1.f;
+#pragma unroll
+      for (int t = 0; t < kC; ++t) {
+        alpha[t] = alpha_of(tile_at(sG, t));
+        pre *= alpha[t];
+        if (REV) {
+          __nv_bfloat16* qe = tile_at(sQ, t);
+          *qe = __float2bfloat16_rn(__bfloat162float(*qe) * pre);
+        }
+      }
+      sE[ii] = pre;
+      if (!REV) {
+        const float rinv = 1.0f / pre;
+        float suf = 1.f;
+#pragma unroll
+        for (int t = kC - 1; t >= 0; --t) {
+          __nv_bfloat16* ke = tile_at(sK, t);
+          *ke = __float2bfloat16_rn(__bfloat162float(*ke) * (suf * rinv));
+          suf *= alpha[t];
+        }
+      }
+    }
+    if (REV) {
+      __syncthreads();  // sE complete
+      state_pass();
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    // ---- MMA group 1
+    if (tid == 0) {
+      if (!mbar_wait(&bar_dv, par)) atomicExch(&g_qk_status, 1);
+      tc_fence_after();
+      const uint32_t o0 = smem_u32(sDO), v0 = smem_u32(sV), h0 = smem_u32(sHi),
+                     l0 = smem_u32(sLo);
+      const uint32_t x0 = smem_u32(REV ? sQ : sK);
+      constexpr uint32_t id64 = idesc_bf16(64, 64, false, false);  // dA
+      constexpr uint32_t idT = idesc_bf16(64, 64, true, false);    // copy (x) do or v
+#pragma unroll 4
+      for (int m = 0; m < kDVH / 16; ++m) {  // K = this CTA's d_v half, 16 per step
+        const uint32_t koff = (uint32_t)((m >> 2) * 8192 + (m & 3) * 32);
+        const uint64_t od = sdesc_sw128(o0 + koff, 16, 1024);
+        const uint64_t vd = sdesc_sw128(v0 + koff, 16, 1024);
+        const uint64_t hd = sdesc_sw128(h0 + m * 2048, 8192, 1024);
+        const uint64_t ld = sdesc_sw128(l0 + m * 2048, 8192, 1024);
+        const uint64_t yd = REV ? vd : od;
+        // dA (partial over this half) = do v^T      (M = 64 t, N = 64 s)
+        umma_bf16(tmem + kColDA, od, vd, id64, m ? 1u : 0u);
+        // forward: dq^T = S do^T     reverse: dk^T = (e^{b_last} dS) v^T   (M = 64 i, N = 64)
+        umma_bf16(tmem + kColAcc, hd, yd, idT, m ? 1u : 0u);
+        umma_bf16(tmem + kColAcc, ld, yd, idT, 1u);
+      }
+      // forward: S^T_g += v_g^T K~    reverse: dS^T_g += do_g^T Q~   (M = 128 j, N = 64 i, K = 64)
+      constexpr uint32_t idS = idesc_bf16(128, 64, true, true);
+      const uint32_t y0 = REV ? o0 : v0;
+#pragma unroll
+      for (int g = 0; g < 2; ++g)
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t yd = sdesc_sw128(y0 + g * 16384 + kk * 2048, 8192, 1024);
+          const uint64_t xd = sdesc_sw128(x0 + kk * 2048, 8192, 1024);
+          umma_bf16(tmem + g * 64, yd, xd, idS, 1u);
+        }
+      umma_commit(&bar_g1);
+    }
+    if (!mbar_wait(&bar_g1, par)) atomicExch(&g_qk_status, 1);
+    tc_fence_after();
+    if (tid == 0 && it + 1 < nc) issue_dv(REV ? n - 1 : n + 1);  // do, v buffers are free
+    // ---- mask the dA partial -> P [t][s]
+    if (warp < 4) {
+      float a[64];
+      tmem_ld32(tmem + lane_off + kColDA, a);
+      tmem_ld32(tmem + lane_off + kColDA + 32, a + 32);
+      tmem_ld_wait();
+      if (lane < 16) {
+        const int t = warp * 16 + lane;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          uint32_t w4[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int s0 = c * 8 + 2 * u;
+            w4[u] = pack_bf16(s0 <= t ? a[s0] : 0.f, s0 + 1 <= t ? a[s0 + 1] : 0.f);
+          }
+          *reinterpret_cast<uint4*>(sP + sw128((uint32_t)t, (uint32_t)c)) =
+              make_uint4(w4[0], w4[1], w4[2], w4[3]);
+        }
+      }
+    }
+    if (!REV) state_pass();  // forward: post-scale and copy for the next chunk
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    // ---- MMA group 2: forward dq^T += K~^T P^T ; reverse dk^T += Q~^T P
+    if (tid == 0) {
+      tc_fence_after();
+      const uint32_t x0 = smem_u32(REV ? sQ : sK), p0 = smem_u32(sP);
+      constexpr uint32_t id2 = idesc_bf16(64, 64, true, REV);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const uint64_t xd = sdesc_sw128(x0 + kk * 2048, 8192, 1024);
+        const uint64_t pd = REV ? sdesc_sw128(p0 + kk * 2048, 8192, 1024)
+                                : sdesc_sw128(p0 + kk * 32, 16, 1024);
+        umma_bf16(tmem + kColAcc, xd, pd, id2, 1u);
+      }
+      umma_commit(&bar_g2);
+    }
+    if (!mbar_wait(&bar_g2, par)) atomicExch(&g_qk_status, 1);
+    tc_fence_after();
+    // ---- add the two d_v halves: rows of the peer go to the peer's buffer
+    float a[64];
+    if (warp < 4) {
+      tmem_ld32(tmem + lane_off + kColAcc, a);
+      tmem_ld32(tmem + lane_off + kColAcc + 32, a + 32);
+      tmem_ld_wait();
+      if (rowt && !owned) {
+        const uint32_t dst = map_to_rank(
+            smem_u32(sR + ((it & 1) * 32 + (ii & 31)) * kC), peer);
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+          st_cluster_v4(dst + c * 16, a[4 * c], a[4 * c + 1], a[4 * c + 2], a[4 * c + 3]);
+      }
+    }
+    cluster_sync();
+    // ---- epilogue of the owned rows (one d_k row per thread, 64 tokens)
+    if (owned) {
+      const float* rv = sR + ((it & 1) * 32 + (ii & 31)) * kC;
+#pragma unroll
+      for (int t = 0; t < kC; ++t) a[t] += rv[t];
+      const size_t base = (size_t)chunk_row(n) * dk + i0 + ii;
+      if (!REV) {
+        float pre = 1.f;
+#pragma unroll
+        for (int t = 0; t < kC; ++t) {
+          pre *= alpha_of(tile_at(sG, t));
+          out[base + (size_t)t * dk] = __float2bfloat16_rn(a[t] * pre);
+          // the reverse sweep's rounded Q~ times the raw accumulator (= q_eff dq)
+          const float qr = __bfloat162float(
+              __float2bfloat16_rn(__bfloat162float(*tile_at(sQ, t)) * pre));
+          qdq[base + (size_t)t * dk] = qr * a[t];
+        }
+      } else {
+        float alpha[kC];
+        float pre = 1.f;
+#pragma unroll
+        for (int t = 0; t < kC; ++t) {
+          alpha[t] = alpha_of(tile_at(sG, t));
+          pre *= alpha[t];
+        }
+        const float rinv = 1.0f / pre;
+        float suf = 1.f;
+#pragma unroll
+        for (int t = kC - 1; t >= 0; --t) {
+          const float e = suf * rinv;
+          suf *= alpha[t];
+          out[base + (size_t)t * dk] = __float2bfloat16_rn(a[t] * e);
+          // the forward sweep's rounded K~ times the raw accumulator (= k_eff dk)
+          const float kr =
+              __bfloat162float(__float2bfloat16_rn(__bfloat162float(*tile_at(sK, t)) * e));
+          run_dg += qdq[base + (size_t)t * dk] - kr * a[t];
+          dg[base + (size_t)t * dk] = __float2bfloat16_rn(run_dg);
+        }
+      }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0 && it + 1 < nc) issue_x(REV ? n - 1 : n + 1);  // q, k, g tiles are free
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, 256);
+}
+
+template <bool REV>
+cudaError_t launch_qk(const Dims& d, const CUtensorMap& tq, const CUtensorMap& tk,
+                      const CUtensorMap& tg, const CUtensorMap& tv, const CUtensorMap& tdo,
+                      const float* S_src, const float* carry, void* out, void* dg, float* qdq,
+                      cudaStream_t st) {
+  auto kern = tc_bwd_qk_kernel<REV>;
+  const int smem = kSmem + 1024;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(2 * d.dk / kKB), (unsigned)(d.B * d.H * d.P), 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, tq, tk, tg, tv, tdo, S_src, carry, (__nv_bfloat16*)out,
+                            (__nv_bfloat16*)dg, qdq, d.T, (int)d.dk, d.P, d.L);
+}
+
+}  // namespace
+
+bool tc_bwd_qk_supported(const Dims& d) {
+  return d.bf16 && d.dk % kKB == 0 && d.dv == kDV && d.C == kC && d.L % kC == 0;
+}
+
+cudaError_t tc_bwd_qk(const Dims& d, const void* q, const void* k, const void* v, const void* g,
+                      const float* S_in, const void* d_o, void* dq, void* dk, void* dg, float* D,
+                      float* carry, float* qdq, cudaStream_t st) {
+  CUtensorMap tq, tk, tg, tv, tdo;
+  const uint64_t rows = (uint64_t)(d.B * d.H * d.T);
+  if (!make_tmap_bf16(&tq, q, rows, d.dk, kC) || !make_tmap_bf16(&tk, k, rows, d.dk, kC) ||
+      !make_tmap_bf16(&tg, g, rows, d.dk, kC) || !make_tmap_bf16(&tv, v, rows, d.dv, kC) ||
+      !make_tmap_bf16(&tdo, d_o, rows, d.dv, kC))
+    return cudaErrorInvalidValue;
+  cudaError_t e = launch_qk<false>(d, tq, tk, tg, tv, tdo, S_in, carry, dq, dg, qdq, st);
+  prof_mark("tc_bwd_dq", st);
+  if (e != cudaSuccess) return e;
+  e = launch_qk<true>(d, tq, tk, tg, tv, tdo, D, carry, dk, dg, qdq, st);
+  prof_mark("tc_bwd_dk", st);
+  return e;
+}
+
+}  // namespace zeco
