@@ -41,6 +41,8 @@
 namespace zeco {
 bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
                     uint32_t box_rows);
+bool make_tmap_f32_plain(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                         uint32_t box_cols, uint32_t box_rows);
 
 namespace {
 
@@ -58,10 +60,10 @@ constexpr int kOffDO = 0;                        // do tile [64 t][256 j] (4 blo
 constexpr int kOffV = kOffDO + kC * kDVH * 2;    // v tile
 constexpr int kOffHi = kOffV + kC * kDVH * 2;    // state copy, high part [256 j][64 i]
 constexpr int kOffLo = kOffHi + kDVH * kKB * 2;  // state copy, low part
-constexpr int kOffQ = kOffLo + kDVH * kKB * 2;   // q tile [64 t][64 i]
-constexpr int kOffK = kOffQ + kC * kKB * 2;
-constexpr int kOffG = kOffK + kC * kKB * 2;
-constexpr int kOffP = kOffG + kC * kKB * 2;      // masked dA partial [64 t][64 s] bf16
+constexpr int kXTile = kC * kKB * 2;             // one [64 t][64 i] bf16 tile
+constexpr int kXBuf = 3 * kXTile + 32 * kC * 4;  // q, k, g tiles + q.dq rows [64 t][32 i] fp32
+constexpr int kOffX = kOffLo + kDVH * kKB * 2;   // 2 buffers of kXBuf (chunk parity)
+constexpr int kOffP = kOffX + 2 * kXBuf;         // masked dA partial [64 t][64 s] bf16
 constexpr int kOffR = kOffP + kC * kC * 2;       // 2 x [32 rows][64] fp32 from the peer
 constexpr int kOffE = kOffR + 2 * 32 * kC * 4;   // e^{b_last} [64] fp32
 constexpr int kSmem = kOffE + 1024;
@@ -79,7 +81,8 @@ template <bool REV>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                  const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmV,
-                 const __grid_constant__ CUtensorMap tmDO, const float* __restrict__ S_src,
+                 const __grid_constant__ CUtensorMap tmDO, const __grid_constant__ CUtensorMap tmQD,
+                 const float* __restrict__ S_src,
                  const float* __restrict__ carry, __nv_bfloat16* __restrict__ out,
                  __nv_bfloat16* __restrict__ dg, float* __restrict__ qdq, int64_t T, int dk,
                  int P, int64_t L) {
@@ -89,13 +92,10 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   unsigned char* sV = sm + kOffV;
   unsigned char* sHi = sm + kOffHi;
   unsigned char* sLo = sm + kOffLo;
-  unsigned char* sQ = sm + kOffQ;
-  unsigned char* sK = sm + kOffK;
-  unsigned char* sG = sm + kOffG;
   unsigned char* sP = sm + kOffP;
   float* sR = reinterpret_cast<float*>(sm + kOffR);
   float* sE = reinterpret_cast<float*>(sm + kOffE);
-  __shared__ uint64_t bar_x, bar_dv, bar_g1, bar_g2;
+  __shared__ uint64_t bar_x[2], bar_dv, bar_g1, bar_g2;
   __shared__ uint32_t tmem_base;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -113,7 +113,8 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   const bool owned = rowt && (uint32_t)(ii >> 5) == rank;  // finished by this CTA
 
   if (tid == 0) {
-    mbar_init(&bar_x, 1);
+    mbar_init(&bar_x[0], 1);
+    mbar_init(&bar_x[1], 1);
     mbar_init(&bar_dv, 1);
     mbar_init(&bar_g1, 1);
     mbar_init(&bar_g2, 1);
@@ -123,6 +124,7 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     prefetch_tmap(&tmG);
     prefetch_tmap(&tmV);
     prefetch_tmap(&tmDO);
+    if (REV) prefetch_tmap(&tmQD);
   }
   if (warp == 0) tmem_alloc(&tmem_base, 256);
   tc_fence_before();
@@ -132,12 +134,15 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   const uint32_t lane_off = (uint32_t)(lg * 32) << 16;
 
   auto chunk_row = [&](int n) { return (int32_t)(row0 + (int64_t)n * kC); };
-  auto issue_x = [&](int n) {
+  // q, k, g tiles of chunk n (and, reverse, this CTA's q.dq rows) into buffer `buf`
+  auto issue_x = [&](int n, int buf) {
     const int32_t r = chunk_row(n);
-    mbar_expect_tx(&bar_x, 3 * kC * kKB * 2);
-    tma_load_2d(sQ, &tmQ, i0, r, &bar_x);
-    tma_load_2d(sK, &tmK, i0, r, &bar_x);
-    tma_load_2d(sG, &tmG, i0, r, &bar_x);
+    unsigned char* xb = sm + kOffX + buf * kXBuf;
+    mbar_expect_tx(&bar_x[buf], 3 * kXTile + (REV ? 32 * kC * 4 : 0));
+    tma_load_2d(xb, &tmQ, i0, r, &bar_x[buf]);
+    tma_load_2d(xb + kXTile, &tmK, i0, r, &bar_x[buf]);
+    tma_load_2d(xb + 2 * kXTile, &tmG, i0, r, &bar_x[buf]);
+    if (REV) tma_load_2d(xb + 3 * kXTile, &tmQD, i0 + 32 * (int)rank, r, &bar_x[buf]);
   };
   auto issue_dv = [&](int n) {
     const int32_t r = chunk_row(n);
@@ -148,7 +153,7 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     }
   };
   if (tid == 0) {
-    issue_x(REV ? nc - 1 : 0);
+    issue_x(REV ? nc - 1 : 0, 0);
     issue_dv(REV ? nc - 1 : 0);
   }
 
@@ -216,7 +221,14 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   for (int it = 0; it < nc; ++it) {
     const int n = REV ? (nc - 1 - it) : it;
     const uint32_t par = (uint32_t)(it & 1);
-    if (!mbar_wait(&bar_x, par)) atomicExch(&g_qk_status, 1);
+    const int xbuf = it & 1;
+    unsigned char* sQ = sm + kOffX + xbuf * kXBuf;
+    unsigned char* sK = sQ + kXTile;
+    unsigned char* sG = sQ + 2 * kXTile;
+    const float* sQD = reinterpret_cast<const float*>(sQ + 3 * kXTile);
+    // the next chunk's tiles go to the other buffer (freed at the end of the last iteration)
+    if (tid == 0 && it + 1 < nc) issue_x(REV ? n - 1 : n + 1, xbuf ^ 1);
+    if (!mbar_wait(&bar_x[xbuf], (uint32_t)((it >> 1) & 1))) atomicExch(&g_qk_status, 1);
     // ---- prologue (row-owner threads): forward K~ = bf16(k e^{-b}); reverse Q~ = bf16(q e^{b})
     if (rowt) {
       float alpha[kC];
@@ -379,14 +391,13 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
           // the forward sweep's rounded K~ times the raw accumulator (= k_eff dk)
           const float kr =
               __bfloat162float(__float2bfloat16_rn(__bfloat162float(*tile_at(sK, t)) * e));
-          run_dg += qdq[base + (size_t)t * dk] - kr * a[t];
+          run_dg += sQD[t * 32 + (ii & 31)] - kr * a[t];
           dg[base + (size_t)t * dk] = __float2bfloat16_rn(run_dg);
         }
       }
     }
     tc_fence_before();
     __syncthreads();
-    if (tid == 0 && it + 1 < nc) issue_x(REV ? n - 1 : n + 1);  // q, k, g tiles are free
   }
   tc_fence_before();
   __syncthreads();
@@ -396,7 +407,7 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
 template <bool REV>
 cudaError_t launch_qk(const Dims& d, const CUtensorMap& tq, const CUtensorMap& tk,
                       const CUtensorMap& tg, const CUtensorMap& tv, const CUtensorMap& tdo,
-                      const float* S_src, const float* carry, void* out, void* dg, float* qdq,
+                      const CUtensorMap& tqd, const float* S_src, const float* carry, void* out, void* dg, float* qdq,
                       cudaStream_t st) {
   auto kern = tc_bwd_qk_kernel<REV>;
   const int smem = kSmem + 1024;
@@ -414,7 +425,7 @@ cudaError_t launch_qk(const Dims& d, const CUtensorMap& tq, const CUtensorMap& t
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, tq, tk, tg, tv, tdo, S_src, carry, (__nv_bfloat16*)out,
+  return cudaLaunchKernelEx(&cfg, kern, tq, tk, tg, tv, tdo, tqd, S_src, carry, (__nv_bfloat16*)out,
                             (__nv_bfloat16*)dg, qdq, d.T, (int)d.dk, d.P, d.L);
 }
 
@@ -427,16 +438,17 @@ bool tc_bwd_qk_supported(const Dims& d) {
 cudaError_t tc_bwd_qk(const Dims& d, const void* q, const void* k, const void* v, const void* g,
                       const float* S_in, const void* d_o, void* dq, void* dk, void* dg, float* D,
                       float* carry, float* qdq, cudaStream_t st) {
-  CUtensorMap tq, tk, tg, tv, tdo;
+  CUtensorMap tq, tk, tg, tv, tdo, tqd;
   const uint64_t rows = (uint64_t)(d.B * d.H * d.T);
   if (!make_tmap_bf16(&tq, q, rows, d.dk, kC) || !make_tmap_bf16(&tk, k, rows, d.dk, kC) ||
       !make_tmap_bf16(&tg, g, rows, d.dk, kC) || !make_tmap_bf16(&tv, v, rows, d.dv, kC) ||
-      !make_tmap_bf16(&tdo, d_o, rows, d.dv, kC))
+      !make_tmap_bf16(&tdo, d_o, rows, d.dv, kC) ||
+      !make_tmap_f32_plain(&tqd, qdq, rows, d.dk, 32, kC))
     return cudaErrorInvalidValue;
-  cudaError_t e = launch_qk<false>(d, tq, tk, tg, tv, tdo, S_in, carry, dq, dg, qdq, st);
+  cudaError_t e = launch_qk<false>(d, tq, tk, tg, tv, tdo, tqd, S_in, carry, dq, dg, qdq, st);
   prof_mark("tc_bwd_dq", st);
   if (e != cudaSuccess) return e;
-  e = launch_qk<true>(d, tq, tk, tg, tv, tdo, D, carry, dk, dg, qdq, st);
+  e = launch_qk<true>(d, tq, tk, tg, tv, tdo, tqd, D, carry, dk, dg, qdq, st);
   prof_mark("tc_bwd_dk", st);
   return e;
 }

@@ -58,7 +58,9 @@ __device__ int g_fwd_status = 0;
 template <int DK>
 struct FwdSmem {
   static constexpr int kTile = DK * kC * 2;  // q / k / g tile bytes
-  static constexpr int kQ = 0, kK = kTile, kG = 2 * kTile, kV = 3 * kTile;
+  static constexpr int kXBuf = 3 * kTile;    // q, k, g tiles of one chunk
+  static constexpr int kX = 0;               // 2 buffers (chunk parity)
+  static constexpr int kV = 2 * kXBuf;
   static constexpr int kP = kV + kNV * kC * 2;
   static constexpr int kE = kP + kC * kC * 2;
   static constexpr int kBytes = kE + DK * 4;
@@ -73,13 +75,10 @@ tc_sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   using SM = FwdSmem<DK>;
   extern __shared__ __align__(1024) unsigned char smraw[];
   unsigned char* sm = (unsigned char*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
-  unsigned char* sQ = sm + SM::kQ;
-  unsigned char* sK = sm + SM::kK;
-  unsigned char* sG = sm + SM::kG;
   unsigned char* sV = sm + SM::kV;
   unsigned char* sP = sm + SM::kP;
   float* sE = reinterpret_cast<float*>(sm + SM::kE);
-  __shared__ uint64_t bar_qkg, bar_v, bar_g1, bar_g2;
+  __shared__ uint64_t bar_qkg[2], bar_v, bar_g1, bar_g2;
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
 
@@ -93,7 +92,8 @@ tc_sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   const int nc = (int)(L / kC);
 
   if (tid == 0) {
-    mbar_init(&bar_qkg, 1);
+    mbar_init(&bar_qkg[0], 1);
+    mbar_init(&bar_qkg[1], 1);
     mbar_init(&bar_v, 1);
     mbar_init(&bar_g1, 1);
     mbar_init(&bar_g2, 1);
@@ -111,13 +111,14 @@ tc_sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   const uint32_t tmem = tmem_base;
   const uint32_t lane_off = (uint32_t)(lg * 32) << 16;
 
-  auto issue_qkg = [&](int n) {
+  auto issue_qkg = [&](int n, int buf) {
     const int32_t r = (int32_t)(row0 + (int64_t)n * kC);
-    mbar_expect_tx(&bar_qkg, 3 * SM::kTile);
+    unsigned char* xb = sm + SM::kX + buf * SM::kXBuf;
+    mbar_expect_tx(&bar_qkg[buf], 3 * SM::kTile);
     for (int b = 0; b < DK / 64; ++b) {
-      tma_load_2d(sQ + b * 8192, &tmQ, b * 64, r, &bar_qkg);
-      tma_load_2d(sK + b * 8192, &tmK, b * 64, r, &bar_qkg);
-      tma_load_2d(sG + b * 8192, &tmG, b * 64, r, &bar_qkg);
+      tma_load_2d(xb + b * 8192, &tmQ, b * 64, r, &bar_qkg[buf]);
+      tma_load_2d(xb + SM::kTile + b * 8192, &tmK, b * 64, r, &bar_qkg[buf]);
+      tma_load_2d(xb + 2 * SM::kTile + b * 8192, &tmG, b * 64, r, &bar_qkg[buf]);
     }
   };
   auto issue_v = [&](int n) {
@@ -126,7 +127,7 @@ tc_sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     for (int b = 0; b < kNV / 64; ++b) tma_load_2d(sV + b * 8192, &tmV, j0 + b * 64, r, &bar_v);
   };
   if (tid == 0) {
-    issue_qkg(BWD ? nc - 1 : 0);
+    issue_qkg(BWD ? nc - 1 : 0, 0);
     issue_v(BWD ? nc - 1 : 0);
   }
 
@@ -176,8 +177,15 @@ tc_sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   for (int it = 0; it < nc; ++it) {
     const int n = BWD ? (nc - 1 - it) : it;  // chunk index in the segment
     const uint32_t par = (uint32_t)(it & 1);
+    const int xbuf = it & 1;
+    unsigned char* sQ = sm + SM::kX + xbuf * SM::kXBuf;
+    unsigned char* sK = sQ + SM::kTile;
+    unsigned char* sG = sQ + 2 * SM::kTile;
+    // the next chunk's q, k, g go to the other buffer (its last reader, MMA group 1
+    // of the previous chunk, has completed)
+    if (tid == 0 && it + 1 < nc) issue_qkg(BWD ? n - 1 : n + 1, xbuf ^ 1);
     // ------------------------------------------------ prologue: Q~, K~, e^{b_last}
-    if (!mbar_wait(&bar_qkg, par)) {
+    if (!mbar_wait(&bar_qkg[xbuf], (uint32_t)((it >> 1) & 1))) {
       atomicExch(&g_fwd_status, 1);
       abort_flag = 1;
     }
@@ -280,7 +288,6 @@ tc_sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     __syncthreads();
     // ------------------------------------------------ MMA group 2: o^T += V^T P^T
     if (tid == 0) {
-      if (it + 1 < nc) issue_qkg(BWD ? n - 1 : n + 1);  // q, k, g buffers are free now
       tc_fence_after();
       const uint32_t v0 = smem_u32(sV), p0 = smem_u32(sP);
       // forward:  o^T  += V^T  P^T  (B = P, K = s contiguous: K-major)

@@ -196,6 +196,19 @@ bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t co
                                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2D fp32 tensor map, box_cols x box_rows, no swizzle (rows of box_cols * 4 bytes).
+bool make_tmap_f32_plain(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                         uint32_t box_cols, uint32_t box_rows) {
+  cuuint64_t gdim[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t gstr[1] = {(cuuint64_t)cols * 4};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return cuTensorMapEncodeTiled(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base),
+                                gdim, gstr, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int NT, bool REV>
 static cudaError_t launch_state(const Dims& d, const void* x, const void* y, const void* g,
                                 float* out, float* gamma, int slot_off, cudaStream_t st) {
