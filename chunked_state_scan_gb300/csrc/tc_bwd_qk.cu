@@ -66,7 +66,10 @@ constexpr int kOffX = kOffLo + kDVH * kKB * 2;   // 2 buffers of kXBuf (chunk pa
 constexpr int kOffP = kOffX + 2 * kXBuf;         // masked dA partial [64 t][64 s] bf16
 constexpr int kOffR = kOffP + kC * kC * 2;       // 2 x [32 rows][64] fp32 from the peer
 constexpr int kOffE = kOffR + 2 * 32 * kC * 4;   // e^{b_last} [64] fp32
-constexpr int kSmem = kOffE + 1024;
+constexpr int kOffPq = kOffE + 256;              // quarter products of alpha [4][64] fp32
+constexpr int kOffQS = kOffPq + 1024;            // reverse: quarter sums of dg terms [4][32]
+constexpr int kOffRun = kOffQS + 512;            // reverse: dg suffix carried per row [32]
+constexpr int kSmem = kOffE + 2048;
 
 __device__ int g_qk_status = 0;
 
@@ -75,6 +78,21 @@ __device__ int g_qk_status = 0;
 // bit for bit): alpha_t = exp(g_t), pre_t = prod_{r<=t} alpha_r.
 __device__ __forceinline__ float alpha_of(const __nv_bfloat16* ge) {
   return __expf(__bfloat162float(*ge));
+}
+
+// Decay factors of column c over a chunk are built from four quarters of 16
+// tokens.  Pq[qd][c] = alpha over quarter qd (left to right); the prefix offset
+// of quarter qd, the suffix offset (product of the later quarters) and the
+// total are combined in one fixed order here, so every caller gets the same
+// bits.
+__device__ __forceinline__ void quarter_offsets(const float* Pq, int c, int qd, float& off,
+                                                float& sufq, float& total) {
+  const float P0 = Pq[c], P1 = Pq[64 + c], P2 = Pq[128 + c], P3 = Pq[192 + c];
+  const float o1 = P0, o2 = o1 * P1, o3 = o2 * P2;
+  off = qd == 0 ? 1.f : (qd == 1 ? o1 : (qd == 2 ? o2 : o3));
+  total = o3 * P3;
+  const float s2 = P3, s1 = s2 * P2, s0 = s1 * P1;
+  sufq = qd == 3 ? 1.f : (qd == 2 ? s2 : (qd == 1 ? s1 : s0));
 }
 
 template <bool REV>
@@ -95,6 +113,9 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   unsigned char* sP = sm + kOffP;
   float* sR = reinterpret_cast<float*>(sm + kOffR);
   float* sE = reinterpret_cast<float*>(sm + kOffE);
+  float* sPq = reinterpret_cast<float*>(sm + kOffPq);
+  float* sQS = reinterpret_cast<float*>(sm + kOffQS);
+  float* sRun = reinterpret_cast<float*>(sm + kOffRun);
   __shared__ uint64_t bar_x[2], bar_dv, bar_g1, bar_g2;
   __shared__ uint32_t tmem_base;
 
@@ -207,15 +228,19 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     tmem_st_wait();
   };
 
-  // element (t, ii) of a [64 t][64 i] tile
-  const uint32_t ce = (uint32_t)((ii & 63) >> 3), cs = (uint32_t)(ii & 7) * 2u;
-  auto tile_at = [&](unsigned char* base, int t) -> __nv_bfloat16* {
-    return reinterpret_cast<__nv_bfloat16*>(base + sw128((uint32_t)t, ce) + cs);
+  // element (t, column c) of a [64 t][64 i] tile
+  auto tile_at = [&](unsigned char* base, int t, int c) -> __nv_bfloat16* {
+    return reinterpret_cast<__nv_bfloat16*>(base + sw128((uint32_t)t, (uint32_t)((c & 63) >> 3)) +
+                                            (uint32_t)(c & 7) * 2u);
   };
+  // worker geometry of the prologue (64 columns x 4 quarters) and of the
+  // epilogue (32 owned rows x 4 quarters, threads 0..127)
+  const int pc = tid & 63, pq = tid >> 6;
+  const int er = tid & 31, eq = (tid >> 5) & 3;
+  const int ec = 32 * (int)rank + er;  // column (d_k row) of the epilogue worker
 
-  float run_dg = 0.f;  // dlog_alpha suffix of an owned row (reverse sweep)
-  if (REV && owned) run_dg = carry[((size_t)bh * P + p) * dk + i0 + ii];
-  // peer's partials for my rows land in sR[buf][ii - 32 rank][64]
+  if (REV && tid < 32) sRun[tid] = carry[((size_t)bh * P + p) * dk + i0 + 32 * (int)rank + tid];
+  // peer's partials for my rows land in sR[buf][row - 32 rank][64]
   const uint32_t peer = rank ^ 1u;
 
   for (int it = 0; it < nc; ++it) {
@@ -229,28 +254,36 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     // the next chunk's tiles go to the other buffer (freed at the end of the last iteration)
     if (tid == 0 && it + 1 < nc) issue_x(REV ? n - 1 : n + 1, xbuf ^ 1);
     if (!mbar_wait(&bar_x[xbuf], (uint32_t)((it >> 1) & 1))) atomicExch(&g_qk_status, 1);
-    // ---- prologue (row-owner threads): forward K~ = bf16(k e^{-b}); reverse Q~ = bf16(q e^{b})
-    if (rowt) {
-      float alpha[kC];
-      float pre = 1.f;
+    // ---- prologue (64 columns x 4 quarters): forward K~ = bf16(k e^{-b}); reverse Q~ = bf16(q e^{b})
+    {
+      float al[16];
+      float prod = 1.f;
 #pragma unroll
-      for (int t = 0; t < kC; ++t) {
-        alpha[t] = alpha_of(tile_at(sG, t));
-        pre *= alpha[t];
-        if (REV) {
-          __nv_bfloat16* qe = tile_at(sQ, t);
-          *qe = __float2bfloat16_rn(__bfloat162float(*qe) * pre);
-        }
+      for (int u = 0; u < 16; ++u) {
+        al[u] = alpha_of(tile_at(sG, 16 * pq + u, pc));
+        prod *= al[u];
       }
-      sE[ii] = pre;
-      if (!REV) {
-        const float rinv = 1.0f / pre;
-        float suf = 1.f;
+      sPq[pq * 64 + pc] = prod;
+      __syncthreads();
+      float off, sufq, total;
+      quarter_offsets(sPq, pc, pq, off, sufq, total);
+      if (pq == 3) sE[pc] = total;
+      if (REV) {
+        float run = off;
 #pragma unroll
-        for (int t = kC - 1; t >= 0; --t) {
-          __nv_bfloat16* ke = tile_at(sK, t);
-          *ke = __float2bfloat16_rn(__bfloat162float(*ke) * (suf * rinv));
-          suf *= alpha[t];
+        for (int u = 0; u < 16; ++u) {
+          run *= al[u];
+          __nv_bfloat16* qe = tile_at(sQ, 16 * pq + u, pc);
+          *qe = __float2bfloat16_rn(__bfloat162float(*qe) * run);
+        }
+      } else {
+        const float rinv = 1.0f / total;
+        float run = sufq;
+#pragma unroll
+        for (int u = 15; u >= 0; --u) {
+          __nv_bfloat16* ke = tile_at(sK, 16 * pq + u, pc);
+          *ke = __float2bfloat16_rn(__bfloat162float(*ke) * (run * rinv));
+          run *= al[u];
         }
       }
     }
@@ -356,44 +389,65 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       }
     }
     cluster_sync();
-    // ---- epilogue of the owned rows (one d_k row per thread, 64 tokens)
+    // ---- sum of the two halves for the owned rows, in place in the receive buffer
+    float* sAcc = sR + (it & 1) * 32 * kC;
     if (owned) {
-      const float* rv = sR + ((it & 1) * 32 + (ii & 31)) * kC;
+      float* rv = sAcc + (ii & 31) * kC;
 #pragma unroll
-      for (int t = 0; t < kC; ++t) a[t] += rv[t];
-      const size_t base = (size_t)chunk_row(n) * dk + i0 + ii;
+      for (int t = 0; t < kC; ++t) rv[t] += a[t];
+    }
+    __syncthreads();
+    // ---- epilogue: 32 owned rows x 4 quarters of 16 tokens
+    if (tid < 128) {
+      float al[16];
+#pragma unroll
+      for (int u = 0; u < 16; ++u) al[u] = alpha_of(tile_at(sG, 16 * eq + u, ec));
+      float off, sufq, total;
+      quarter_offsets(sPq, ec, eq, off, sufq, total);
+      const float* acc = sAcc + er * kC + 16 * eq;
+      const size_t base = (size_t)(chunk_row(n) + 16 * eq) * dk + i0 + ec;
       if (!REV) {
-        float pre = 1.f;
+        float run = off;
 #pragma unroll
-        for (int t = 0; t < kC; ++t) {
-          pre *= alpha_of(tile_at(sG, t));
-          out[base + (size_t)t * dk] = __float2bfloat16_rn(a[t] * pre);
+        for (int u = 0; u < 16; ++u) {
+          run *= al[u];
+          const float av = acc[u];
+          out[base + (size_t)u * dk] = __float2bfloat16_rn(av * run);
           // the reverse sweep's rounded Q~ times the raw accumulator (= q_eff dq)
           const float qr = __bfloat162float(
-              __float2bfloat16_rn(__bfloat162float(*tile_at(sQ, t)) * pre));
-          qdq[base + (size_t)t * dk] = qr * a[t];
+              __float2bfloat16_rn(__bfloat162float(*tile_at(sQ, 16 * eq + u, ec)) * run));
+          qdq[base + (size_t)u * dk] = qr * av;
         }
       } else {
-        float alpha[kC];
-        float pre = 1.f;
+        const float rinv = 1.0f / total;
+        float run = sufq;
+        float term[16];
 #pragma unroll
-        for (int t = 0; t < kC; ++t) {
-          alpha[t] = alpha_of(tile_at(sG, t));
-          pre *= alpha[t];
-        }
-        const float rinv = 1.0f / pre;
-        float suf = 1.f;
-#pragma unroll
-        for (int t = kC - 1; t >= 0; --t) {
-          const float e = suf * rinv;
-          suf *= alpha[t];
-          out[base + (size_t)t * dk] = __float2bfloat16_rn(a[t] * e);
+        for (int u = 15; u >= 0; --u) {
+          const float e = run * rinv;
+          run *= al[u];
+          const float av = acc[u];
+          out[base + (size_t)u * dk] = __float2bfloat16_rn(av * e);
           // the forward sweep's rounded K~ times the raw accumulator (= k_eff dk)
-          const float kr =
-              __bfloat162float(__float2bfloat16_rn(__bfloat162float(*tile_at(sK, t)) * e));
-          run_dg += sQD[t * 32 + (ii & 31)] - kr * a[t];
-          dg[base + (size_t)t * dk] = __float2bfloat16_rn(run_dg);
+          const float kr = __bfloat162float(
+              __float2bfloat16_rn(__bfloat162float(*tile_at(sK, 16 * eq + u, ec)) * e));
+          term[u] = sQD[(16 * eq + u) * 32 + er] - kr * av;
         }
+        float qsum = 0.f;
+#pragma unroll
+        for (int u = 0; u < 16; ++u) qsum += term[u];
+        sQS[eq * 32 + er] = qsum;
+        asm volatile("bar.sync 1, 128;" ::: "memory");  // the 128 epilogue threads
+        float carry_in = sRun[er];
+        for (int q2 = 3; q2 > eq; --q2) carry_in += sQS[q2 * 32 + er];
+        float runq = carry_in;
+#pragma unroll
+        for (int u = 15; u >= 0; --u) {
+          runq += term[u];
+          dg[base + (size_t)u * dk] = __float2bfloat16_rn(runq);
+        }
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        if (eq == 0) sRun[er] = runq;  // suffix through the whole chunk
       }
     }
     tc_fence_before();
