@@ -42,8 +42,10 @@ constexpr int kGBytes = kTok * kM * 2;  // 16 KB: log_alpha tile
 
 __device__ int g_tc_status = 0;  // set when a bounded wait gives up
 
+constexpr int kStateThreads = 512;  // 128 rows x 4 token quarters
+
 template <int NT, bool REV>
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(kStateThreads, 1)
 tc_seg_state_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmG,
                     const __grid_constant__ CUtensorMap tmY, float* __restrict__ out,
                     float* __restrict__ gamma, int64_t T, int dk, int dv, int P, int64_t L,
@@ -55,12 +57,14 @@ tc_seg_state_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
   __shared__ uint64_t tma_bar[kStages], mma_bar[kStages];
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
+  __shared__ float Gq[4][kM];  // per-quarter sums of log_alpha of the current stage
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int row = tid & (kM - 1), qd = tid >> 7;  // row within the tile, token quarter
   const int64_t bh = blockIdx.z / P;
   const int p = blockIdx.z % P;
   const int i0 = blockIdx.y * kM, j0 = blockIdx.x * NT;
-  const int i = i0 + tid;
+  const int i = i0 + row;
   const int64_t row0 = bh * T + (int64_t)p * L;  // first token row of the segment
   const int nblk = (int)(L / kTok);
 
@@ -99,11 +103,11 @@ tc_seg_state_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
   };
 
   if (tid == 0) issue_tma(0);
-  float run = 0.f;  // running log-decay of row i
-  // row i of the tiles lives in MN block tid/64, 16-byte chunk (tid%64)/8, element tid%8
-  const uint32_t a_blk = (uint32_t)(tid >> 6) * 8192u;
-  const uint32_t a_chunk = (uint32_t)((tid & 63) >> 3);
-  const uint32_t a_sub = (uint32_t)(tid & 7) * 2u;
+  float run = 0.f;  // log-decay of row i summed over the stages already done
+  // row i of the tiles lives in MN block row/64, 16-byte chunk (row%64)/8, element row%8
+  const uint32_t a_blk = (uint32_t)(row >> 6) * 8192u;
+  const uint32_t a_chunk = (uint32_t)((row & 63) >> 3);
+  const uint32_t a_sub = (uint32_t)(row & 7) * 2u;
 
   for (int it = 0; it < nblk; ++it) {
     const int s = it % kStages;
@@ -121,23 +125,48 @@ tc_seg_state_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
       atomicExch(&g_tc_status, 1);
       abort_flag = 1;
     }
-    // A = (w .* x) written over x, row i = this thread
-#pragma unroll 8
-    for (int u = 0; u < kTok; ++u) {
-      const int tt = REV ? (kTok - 1 - u) : u;
-      const uint32_t off = a_blk + sw128((uint32_t)tt, a_chunk) + a_sub;
-      const float gv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(xbuf + kXBytes + off));
-      __nv_bfloat16* xe = reinterpret_cast<__nv_bfloat16*>(xbuf + off);
-      const float xv = __bfloat162float(*xe);
-      float w;
-      if (REV) {
-        w = __expf(run);
-        run += gv;
-      } else {
-        run += gv;
-        w = __expf(run);
+    // A = (w .* x) written over x; this thread: row i, tokens 16 qd .. 16 qd + 15
+    {
+      float gl[16];
+      float gsum = 0.f;
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        const uint32_t off = a_blk + sw128((uint32_t)(16 * qd + u), a_chunk) + a_sub;
+        gl[u] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(xbuf + kXBytes + off));
+        gsum += gl[u];
       }
-      *xe = __float2bfloat16_rn(xv * w);
+      Gq[qd][row] = gsum;
+      __syncthreads();
+      float off_q = run;  // log-decay from the processed stages plus the other quarters
+      float stage = 0.f;
+#pragma unroll
+      for (int q2 = 0; q2 < 4; ++q2) {
+        const float gq = Gq[q2][row];
+        stage += gq;
+        if (REV ? (q2 > qd) : (q2 < qd)) off_q += gq;
+      }
+      if (REV) {
+        // w_t = exp(sum of g over the later tokens of the segment)
+        float loc = off_q;
+#pragma unroll
+        for (int u = 15; u >= 0; --u) {
+          const uint32_t off = a_blk + sw128((uint32_t)(16 * qd + u), a_chunk) + a_sub;
+          __nv_bfloat16* xe = reinterpret_cast<__nv_bfloat16*>(xbuf + off);
+          *xe = __float2bfloat16_rn(__bfloat162float(*xe) * __expf(loc));
+          loc += gl[u];
+        }
+      } else {
+        // w_t = exp(sum of g from the segment start through t)
+        float loc = off_q;
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+          loc += gl[u];
+          const uint32_t off = a_blk + sw128((uint32_t)(16 * qd + u), a_chunk) + a_sub;
+          __nv_bfloat16* xe = reinterpret_cast<__nv_bfloat16*>(xbuf + off);
+          *xe = __float2bfloat16_rn(__bfloat162float(*xe) * __expf(loc));
+        }
+      }
+      run += stage;
     }
     fence_async_smem();
     __syncthreads();
@@ -157,7 +186,7 @@ tc_seg_state_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
   }
   __syncthreads();
   const bool ok = !abort_flag;
-  if (ok) {
+  if (ok && warp < 4) {
     const int last = nblk - 1;
     if (!mbar_wait(&mma_bar[last % kStages], (last / kStages) & 1)) atomicExch(&g_tc_status, 1);
     tc_fence_after();
@@ -173,6 +202,7 @@ tc_seg_state_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
         dst[u] = make_float4(r[4 * u], r[4 * u + 1], r[4 * u + 2], r[4 * u + 3]);
     }
     if (REV && gamma && blockIdx.x == 0) gamma[((size_t)bh * P + p) * dk + i] = __expf(run);
+    (void)lane;
   }
   tc_fence_before();
   __syncthreads();
@@ -223,8 +253,8 @@ static cudaError_t launch_state(const Dims& d, const void* x, const void* y, con
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)(d.dv / NT), (unsigned)(d.dk / kM), (unsigned)(d.B * d.H * d.P));
-  kern<<<grid, 128, smem, st>>>(tx, tg, ty, out, gamma, d.T, (int)d.dk, (int)d.dv, d.P, d.L,
-                                slot_off);
+  kern<<<grid, kStateThreads, smem, st>>>(tx, tg, ty, out, gamma, d.T, (int)d.dk, (int)d.dv, d.P,
+                                          d.L, slot_off);
   return cudaGetLastError();
 }
 
