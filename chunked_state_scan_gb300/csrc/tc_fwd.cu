@@ -50,7 +50,7 @@ using namespace tc;
 
 constexpr int kC = 64;        // chunk length
 constexpr int kNV = 128;      // d_v columns per CTA
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;  // 16 warps
 constexpr uint32_t kColS16 = 256, kColA = 384, kColO = 448;
 
 __device__ int g_fwd_status = 0;
@@ -63,7 +63,8 @@ struct FwdSmem {
   static constexpr int kV = 2 * kXBuf;
   static constexpr int kP = kV + kNV * kC * 2;
   static constexpr int kE = kP + kC * kC * 2;
-  static constexpr int kBytes = kE + DK * 4;
+  static constexpr int kPq = kE + DK * 4;  // per-quarter alpha products [4][DK]
+  static constexpr int kBytes = kPq + 4 * DK * 4;
 };
 
 template <int DK, bool BWD>
@@ -78,13 +79,15 @@ tc_sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   unsigned char* sV = sm + SM::kV;
   unsigned char* sP = sm + SM::kP;
   float* sE = reinterpret_cast<float*>(sm + SM::kE);
+  float* sPq = reinterpret_cast<float*>(sm + SM::kPq);
   __shared__ uint64_t bar_qkg[2], bar_v, bar_g1, bar_g2;
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int lg = warp & 3;       // TMEM lane group of this warp
-  const int half = warp >> 2;    // which half of the columns this warp handles
+  const int cq = warp >> 2;      // which quarter of the d_k columns this warp's state pass handles
+  const int half = (warp >> 2) & 1;  // epilogue: which half of the 64 tokens (warps 0..7)
   const int64_t bh = blockIdx.y / P;
   const int p = blockIdx.y % P;
   const int j0 = blockIdx.x * kNV;
@@ -137,7 +140,7 @@ tc_sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   {
     const float* Sp =
         S_src + ((size_t)bh * (P + 1) + p + (BWD ? 1 : 0)) * DK * dv + j0 + lg * 32 + lane;
-    for (int c = half * (DK / 2); c < (half + 1) * (DK / 2); c += 32) {
+    for (int c = cq * (DK / 4); c < (cq + 1) * (DK / 4); c += 32) {
       float r[32];
 #pragma unroll
       for (int u = 0; u < 32; ++u) r[u] = Sp[(size_t)(c + u) * dv];
@@ -154,7 +157,7 @@ tc_sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 
   // S^T (fp32) <- e^{b_last} .* S^T (column i scaled by sE[i]) and its bf16 copy
   auto state_pass = [&]() {
-    for (int c = half * (DK / 2); c < (half + 1) * (DK / 2); c += 32) {
+    for (int c = cq * (DK / 4); c < (cq + 1) * (DK / 4); c += 32) {
       float r[32];
       tmem_ld32(tmem + lane_off + c, r);
       tmem_ld_wait();
@@ -169,10 +172,12 @@ tc_sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     tmem_st_wait();
   };
 
-  // prologue geometry: thread tid < DK owns d_k column i = tid
-  const uint32_t pe_off = (uint32_t)(tid >> 6) * 8192u;
-  const uint32_t pe_chunk = (uint32_t)((tid & 63) >> 3);
-  const uint32_t pe_sub = (uint32_t)(tid & 7) * 2u;
+  // element (t, column c) of a [64 t][DK] tile stored as DK/64 blocks of 64 columns
+  auto tile_off = [](int t, int c) -> uint32_t {
+    return (uint32_t)(c >> 6) * 8192u + sw128((uint32_t)t, (uint32_t)((c & 63) >> 3)) +
+           (uint32_t)(c & 7) * 2u;
+  };
+  constexpr int kTasks = DK * 4 / kThreads;  // (column, token quarter) tasks per thread
 
   for (int it = 0; it < nc; ++it) {
     const int n = BWD ? (nc - 1 - it) : it;  // chunk index in the segment
@@ -189,27 +194,46 @@ tc_sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       atomicExch(&g_fwd_status, 1);
       abort_flag = 1;
     }
-    if (tid < DK) {
-      float alpha[kC];
-      float pre = 1.f;
+    {
+      // decay factors per (column c, quarter q of 16 tokens): alpha products of the
+      // quarters first, then prefix products for Q~ and suffix products for K~
+      float al[kTasks][16];
 #pragma unroll
-      for (int t = 0; t < kC; ++t) {
-        const uint32_t off = pe_off + sw128((uint32_t)t, pe_chunk) + pe_sub;
-        const float gv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(sG + off));
-        alpha[t] = __expf(gv);
-        pre *= alpha[t];
-        __nv_bfloat16* qe = reinterpret_cast<__nv_bfloat16*>(sQ + off);
-        *qe = __float2bfloat16_rn(__bfloat162float(*qe) * pre);
+      for (int k2 = 0; k2 < kTasks; ++k2) {
+        const int task = tid + k2 * kThreads, c = task % DK, q = task / DK;
+        float prod = 1.f;
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+          al[k2][u] = __expf(__bfloat162float(
+              *reinterpret_cast<const __nv_bfloat16*>(sG + tile_off(16 * q + u, c))));
+          prod *= al[k2][u];
+        }
+        sPq[q * DK + c] = prod;
       }
-      sE[tid] = pre;  // e^{b_last}
-      const float rinv = 1.0f / pre;
-      float suf = 1.f;
+      __syncthreads();
 #pragma unroll
-      for (int t = kC - 1; t >= 0; --t) {
-        const uint32_t off = pe_off + sw128((uint32_t)t, pe_chunk) + pe_sub;
-        __nv_bfloat16* ke = reinterpret_cast<__nv_bfloat16*>(sK + off);
-        *ke = __float2bfloat16_rn(__bfloat162float(*ke) * (suf * rinv));
-        suf *= alpha[t];
+      for (int k2 = 0; k2 < kTasks; ++k2) {
+        const int task = tid + k2 * kThreads, c = task % DK, q = task / DK;
+        const float P0 = sPq[c], P1 = sPq[DK + c], P2 = sPq[2 * DK + c], P3 = sPq[3 * DK + c];
+        const float off = q == 0 ? 1.f : (q == 1 ? P0 : (q == 2 ? P0 * P1 : (P0 * P1) * P2));
+        const float sufq = q == 3 ? 1.f : (q == 2 ? P3 : (q == 1 ? P3 * P2 : (P3 * P2) * P1));
+        const float total = ((P0 * P1) * P2) * P3;
+        if (q == 3) sE[c] = total;  // e^{b_last}
+        float run = off;
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+          run *= al[k2][u];
+          __nv_bfloat16* qe = reinterpret_cast<__nv_bfloat16*>(sQ + tile_off(16 * q + u, c));
+          *qe = __float2bfloat16_rn(__bfloat162float(*qe) * run);
+        }
+        const float rinv = 1.0f / total;
+        float suf = sufq;
+#pragma unroll
+        for (int u = 15; u >= 0; --u) {
+          __nv_bfloat16* ke = reinterpret_cast<__nv_bfloat16*>(sK + tile_off(16 * q + u, c));
+          *ke = __float2bfloat16_rn(__bfloat162float(*ke) * (suf * rinv));
+          suf *= al[k2][u];
+        }
       }
     }
     if (BWD) {
@@ -306,7 +330,7 @@ tc_sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     tc_fence_after();
     if (tid == 0 && it + 1 < nc) issue_v(BWD ? n - 1 : n + 1);  // V buffer is free now
     // ------------------------------------------------ epilogue: o^T -> o
-    {
+    if (warp < 8) {
       float r[32];
       tmem_ld32(tmem + lane_off + kColO + half * 32, r);
       tmem_ld_wait();
