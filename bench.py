@@ -57,8 +57,12 @@ def kernel_bytes_per_token(dk, dv, L, e=E):
         "seg_scan_rev": 3 * st,
         # dv: read q, k, g, do and D[p+1]; write dv
         "bwd_dv": e * (3 * dk + 2 * dv) + st,
-        # dq, dk, dg: read q, k, v, g, do, S_in[p], D[p+1]; write dq, dk, dg
+        # dq, dk, dg (one launch): read q, k, v, g, do, S_in[p], D[p+1]; write dq, dk, dg
         "bwd_dqk": e * (3 * dk + 2 * dv) + e * 3 * dk + 2 * st,
+        # dq sweep: read q, k, v, g, do and S_in[p]; write dq
+        "bwd_dq": e * (3 * dk + 2 * dv) + e * dk + st,
+        # dk sweep: read q, k, v, g, do and D[p+1]; write dk, dlog_alpha
+        "bwd_dk": e * (3 * dk + 2 * dv) + 2 * e * dk + st,
     }
 
 
@@ -78,7 +82,7 @@ def zeco_operator_flops_per_token(dk, dv, C):
 
 def canonical_kernel(name):
     for key in ("chunk_state", "seg_scan_fwd", "fwd_out", "dstate_local", "seg_scan_rev",
-                "bwd_dv", "bwd_dqk"):
+                "bwd_dv", "bwd_dqk", "bwd_dq", "bwd_dk"):
         if key in name:
             return key
     return name
