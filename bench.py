@@ -44,25 +44,29 @@ METRIC = "GLA fwd+bwd tokens/sec on 1 GB300 and % of roofline (1M tok, P=64)"
 E = 2  # bytes per bf16 element
 
 
-def kernel_bytes_per_token(dk, dv, L, e=E):
+def kernel_bytes_per_token(dk, dv, L, e=E, C=64):
     st = dk * dv * 4 / L  # one fp32 state per segment, per token
+    eb = dk * 4 / C       # e^{b_last}: one fp32 row per chunk, per token
     return {
         # pass 1: read k, v, g; write one local state per segment
         "chunk_state": e * (2 * dk + dv) + st,
         "seg_scan_fwd": 2 * st,
-        # pass 2: read q, k, v, g and S_in[p]; write o
-        "fwd_out": e * (3 * dk + 2 * dv) + st,
+        # decay pass: read q, k, g; write Q~, K~ and e^{b_last}
+        "decay": e * 5 * dk + eb,
+        # pass 2: read Q~, K~, v, e^{b_last} and S_in[p]; write o
+        "fwd_out": e * (2 * dk + 2 * dv) + eb + st,
         # bwd pre-pass: read q, do, g; write one adjoint state per segment
         "dstate_local": e * (2 * dk + dv) + st,
         "seg_scan_rev": 3 * st,
-        # dv: read q, k, g, do and D[p+1]; write dv
-        "bwd_dv": e * (3 * dk + 2 * dv) + st,
-        # dq, dk, dg (one launch): read q, k, v, g, do, S_in[p], D[p+1]; write dq, dk, dg
+        # dv: read Q~, K~, do, e^{b_last} and D[p+1]; write dv
+        "bwd_dv": e * (2 * dk + 2 * dv) + eb + st,
+        # dq, dk, dg (one launch, CUDA-core path): read q, k, v, g, do, S_in[p], D[p+1];
+        # write dq, dk, dg
         "bwd_dqk": e * (3 * dk + 2 * dv) + e * 3 * dk + 2 * st,
-        # dq sweep: read q, k, v, g, do and S_in[p]; write dq
-        "bwd_dq": e * (3 * dk + 2 * dv) + e * dk + st,
-        # dk sweep: read q, k, v, g, do and D[p+1]; write dk, dlog_alpha
-        "bwd_dk": e * (3 * dk + 2 * dv) + 2 * e * dk + st,
+        # dq sweep: read Q~, K~, g, v, do, e^{b_last} and S_in[p]; write dq and q.dq (fp32)
+        "bwd_dq": e * (3 * dk + 2 * dv) + eb + e * dk + 4 * dk + st,
+        # dk sweep: read Q~, K~, g, v, do, e^{b_last}, q.dq and D[p+1]; write dk, dlog_alpha
+        "bwd_dk": e * (3 * dk + 2 * dv) + eb + 4 * dk + 2 * e * dk + st,
     }
 
 
@@ -81,8 +85,8 @@ def zeco_operator_flops_per_token(dk, dv, C):
 
 
 def canonical_kernel(name):
-    for key in ("chunk_state", "seg_scan_fwd", "fwd_out", "dstate_local", "seg_scan_rev",
-                "bwd_dv", "bwd_dqk", "bwd_dq", "bwd_dk"):
+    for key in ("chunk_state", "seg_scan_fwd", "decay", "fwd_out", "dstate_local",
+                "seg_scan_rev", "bwd_dv", "bwd_dqk", "bwd_dq", "bwd_dk"):
         if key in name:
             return key
     return name
@@ -288,13 +292,15 @@ def main(argv=None):
     S_final = torch.empty_like(x["S0"])
     saved = torch.empty(z.saved_bytes(shape), dtype=torch.uint8, device=dev)
     ws = torch.empty(max(z.workspace_bytes(shape, True), 16), dtype=torch.uint8, device=dev)
+    ws_f = torch.empty(max(z.workspace_bytes(shape, False), 16), dtype=torch.uint8, device=dev)
     grads = dict(dq=torch.empty_like(x["q"]), dk=torch.empty_like(x["k"]),
                  dv=torch.empty_like(x["v"]), dlog_alpha=torch.empty_like(x["log_alpha"]),
                  dS0=torch.empty_like(x["S0"]))
 
     def step(xx):
         z.zeco_gla_fwd(xx["q"], xx["k"], xx["v"], xx["log_alpha"], xx["S0"], P=w.P, K=w.K,
-                       C=w.C, path=args.path, o=o, S_final=S_final, saved=saved, stream=stream)
+                       C=w.C, path=args.path, o=o, S_final=S_final, saved=saved,
+                       workspace=ws_f, stream=stream)
         if w.bwd:
             z.zeco_gla_bwd(xx["q"], xx["k"], xx["v"], xx["log_alpha"], saved, xx["do"],
                            xx["dS_final"], P=w.P, K=w.K, C=w.C, path=args.path, grads=grads,

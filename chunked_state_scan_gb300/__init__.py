@@ -8,6 +8,7 @@ library is not built, or no GPU is present, the calls raise.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import threading
@@ -107,32 +108,45 @@ def resolve_path(shape: ZecoShape) -> str:
     return {PATH_SIMT: "simt", PATH_TC: "tc"}[rc]
 
 
+def _on(stream):
+    """Allocate on the stream the kernels run on, so the caching allocator
+    orders reuse of these blocks after the launches that use them."""
+    if isinstance(stream, torch.cuda.Stream):
+        return torch.cuda.stream(stream)
+    return contextlib.nullcontext()
+
+
 def _shape_of(q, v, P, K, C, path):
     B, H, T, dk = q.shape
     return make_shape(B, H, T, dk, v.shape[-1], P, K, C, q.dtype, path)
 
 
 def zeco_gla_fwd(q, k, v, log_alpha, S0=None, *, P, K, C, path="auto", o=None, S_final=None,
-                 saved=None, stream=None, want_S_final=True):
+                 saved=None, workspace=None, stream=None, want_S_final=True):
     """Forward through the C ABI.  Returns (o, S_final or None, saved).
 
     q, k, log_alpha: [B,H,T,dk]; v: [B,H,T,dv] (fp32 or bf16, CUDA, contiguous);
     S0: [B,H,dk,dv] fp32 or None (zeros).  ``saved`` must be passed to the backward.
+    ``workspace``: a uint8 buffer of at least workspace_bytes(shape, False) bytes,
+    allocated here when None.
     """
     shape = _shape_of(q, v, P, K, C, path)
     dev = q.device
-    if o is None:
-        o = torch.empty(v.shape, dtype=v.dtype, device=dev)
-    if want_S_final and S_final is None:
-        S_final = torch.empty(q.shape[0], q.shape[1], q.shape[-1], v.shape[-1],
-                              dtype=torch.float32, device=dev)
-    if saved is None:
-        saved = torch.empty(max(saved_bytes(shape), 16), dtype=torch.uint8, device=dev)
     nws = workspace_bytes(shape, False)
-    ws = torch.empty(nws, dtype=torch.uint8, device=dev) if nws else None
+    with _on(stream):
+        if o is None:
+            o = torch.empty(v.shape, dtype=v.dtype, device=dev)
+        if want_S_final and S_final is None:
+            S_final = torch.empty(q.shape[0], q.shape[1], q.shape[-1], v.shape[-1],
+                                  dtype=torch.float32, device=dev)
+        if saved is None:
+            saved = torch.empty(max(saved_bytes(shape), 16), dtype=torch.uint8, device=dev)
+        if workspace is None and nws:
+            workspace = torch.empty(nws, dtype=torch.uint8, device=dev)
+    ws_len = workspace.numel() if workspace is not None else 0
     rc = load_library().zeco_gla_fwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v),
                                      _ptr(log_alpha), _ptr(S0), _ptr(o), _ptr(S_final),
-                                     _ptr(saved), _ptr(ws), nws, _stream_ptr(stream))
+                                     _ptr(saved), _ptr(workspace), ws_len, _stream_ptr(stream))
     _check(rc)
     return o, S_final, saved
 
@@ -142,15 +156,16 @@ def zeco_gla_bwd(q, k, v, log_alpha, saved, do, dS_final=None, *, P, K, C, path=
     """Backward through the C ABI.  Returns dict(dq, dk, dv, dlog_alpha, dS0)."""
     shape = _shape_of(q, v, P, K, C, path)
     dev = q.device
-    if grads is None:
-        grads = dict(dq=torch.empty_like(q), dk=torch.empty_like(k), dv=torch.empty_like(v),
-                     dlog_alpha=torch.empty_like(log_alpha))
-        if want_dS0:
-            grads["dS0"] = torch.empty(q.shape[0], q.shape[1], q.shape[-1], v.shape[-1],
-                                       dtype=torch.float32, device=dev)
     nws = workspace_bytes(shape, True)
-    if workspace is None:
-        workspace = torch.empty(max(nws, 16), dtype=torch.uint8, device=dev)
+    with _on(stream):
+        if grads is None:
+            grads = dict(dq=torch.empty_like(q), dk=torch.empty_like(k),
+                         dv=torch.empty_like(v), dlog_alpha=torch.empty_like(log_alpha))
+            if want_dS0:
+                grads["dS0"] = torch.empty(q.shape[0], q.shape[1], q.shape[-1], v.shape[-1],
+                                           dtype=torch.float32, device=dev)
+        if workspace is None:
+            workspace = torch.empty(max(nws, 16), dtype=torch.uint8, device=dev)
     rc = load_library().zeco_gla_bwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v),
                                      _ptr(log_alpha), _ptr(saved), _ptr(do), _ptr(dS_final),
                                      _ptr(grads["dq"]), _ptr(grads["dk"]), _ptr(grads["dv"]),

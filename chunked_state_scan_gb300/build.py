@@ -64,7 +64,7 @@ def build(force: bool = False, verbose: bool = False, extra=None) -> str:
     with cf.ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 1)) as ex:
         objs = list(ex.map(compile_one, sources()))
     tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [cc, *ARCH, "-shared", "-o", tmp, *objs, "-lcudart", "-lcuda"]
+    cmd = [cc, *ARCH, "-shared", "-o", tmp, *objs, "-lcudart"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

@@ -57,6 +57,25 @@ int resolve(const zeco_shape* s, const Dims& d) {
   return ZECO_PATH_SIMT;
 }
 
+// Scratch layout of one call: the backward's own buffers (bwd only) followed,
+// on the tensor-core path, by the decay pass's Q~, K~ and e^{b_last}.
+struct WsPlan {
+  zeco::BwdWsLayout bwd;
+  zeco::DecayLayout decay;
+  bool uses_decay;
+  size_t total;
+};
+
+WsPlan plan_ws(const Dims& d, int path, bool bwd) {
+  WsPlan w;
+  w.bwd = zeco::bwd_ws_layout(d);
+  const size_t base = bwd ? w.bwd.total : 0;
+  w.uses_decay = path == ZECO_PATH_TC && zeco::tc_uses_decay(d);
+  w.decay = zeco::decay_layout(d, base);
+  w.total = w.uses_decay ? w.decay.total : base;
+  return w;
+}
+
 }  // namespace
 
 namespace zeco {
@@ -103,7 +122,9 @@ size_t zeco_gla_saved_bytes(const zeco_shape* shape) {
 size_t zeco_gla_workspace_bytes(const zeco_shape* shape, int bwd) {
   Dims d;
   if (check_shape(shape, &d) != ZECO_OK) return 0;
-  return bwd ? zeco::bwd_ws_layout(d).total : 0;
+  const int path = resolve(shape, d);
+  if (path < 0) return 0;
+  return plan_ws(d, path, bwd != 0).total;
 }
 
 int zeco_gla_resolve_path(const zeco_shape* shape) {
@@ -116,8 +137,6 @@ int zeco_gla_resolve_path(const zeco_shape* shape) {
 int zeco_gla_fwd(const zeco_shape* shape, const void* q, const void* k, const void* v,
                  const void* log_alpha, const float* S0, void* o, float* S_final, void* saved,
                  void* workspace, size_t ws_bytes, zeco_stream_t stream) {
-  (void)workspace;
-  (void)ws_bytes;
   Dims d;
   int rc = check_shape(shape, &d);
   if (rc != ZECO_OK) return rc;
@@ -127,13 +146,17 @@ int zeco_gla_fwd(const zeco_shape* shape, const void* q, const void* k, const vo
   if ((S0 && !aligned16(S0)) || (S_final && !aligned16(S_final))) return ZECO_ERR_ARG;
   const int path = resolve(shape, d);
   if (path < 0) return path;
+  const WsPlan wp = plan_ws(d, path, false);
+  if (wp.total > 0 && (!workspace || !aligned16(workspace))) return ZECO_ERR_ARG;
+  if (ws_bytes < wp.total) return ZECO_ERR_WORKSPACE;
   const zeco::SavedLayout sl = zeco::saved_layout(d);
   float* S_in = (float*)((char*)saved + sl.S_in_off);
   float* gamma = (float*)((char*)saved + sl.gamma_off);
   cudaStream_t st = (cudaStream_t)stream;
   zeco::prof_begin(st);
   cudaError_t e = path == ZECO_PATH_TC
-                      ? zeco::tc_forward(d, q, k, v, log_alpha, S0, o, S_final, S_in, gamma, st)
+                      ? zeco::tc_forward(d, q, k, v, log_alpha, S0, o, S_final, S_in, gamma,
+                                         wp.decay, workspace, st)
                       : zeco::simt_forward(d, q, k, v, log_alpha, S0, o, S_final, S_in, gamma,
                                            st);
   return e == cudaSuccess ? ZECO_OK : ZECO_ERR_CUDA;
@@ -152,8 +175,9 @@ int zeco_gla_bwd(const zeco_shape* shape, const void* q, const void* k, const vo
   if ((dS_final && !aligned16(dS_final)) || (dS0 && !aligned16(dS0))) return ZECO_ERR_ARG;
   const int path = resolve(shape, d);
   if (path < 0) return path;
-  const zeco::BwdWsLayout wl = zeco::bwd_ws_layout(d);
-  if (ws_bytes < wl.total) return ZECO_ERR_WORKSPACE;
+  const WsPlan wp = plan_ws(d, path, true);
+  const zeco::BwdWsLayout& wl = wp.bwd;
+  if (ws_bytes < wp.total) return ZECO_ERR_WORKSPACE;
   const zeco::SavedLayout sl = zeco::saved_layout(d);
   const float* S_in = (const float*)((const char*)saved + sl.S_in_off);
   const float* gamma = (const float*)((const char*)saved + sl.gamma_off);
@@ -165,7 +189,7 @@ int zeco_gla_bwd(const zeco_shape* shape, const void* q, const void* k, const vo
   cudaError_t e =
       path == ZECO_PATH_TC
           ? zeco::tc_backward(d, q, k, v, log_alpha, S_in, gamma, d_o, dS_final, dq, dk, dv,
-                              dlog_alpha, dS0, D, carry, qdq, st)
+                              dlog_alpha, dS0, D, carry, qdq, wp.decay, workspace, st)
           : zeco::simt_backward(d, q, k, v, log_alpha, S_in, gamma, d_o, dS_final, dq, dk, dv,
                                 dlog_alpha, dS0, D, carry, qdq, st);
   return e == cudaSuccess ? ZECO_OK : ZECO_ERR_CUDA;

@@ -44,21 +44,29 @@ cudaError_t tc_chunk_state(const Dims& d, const void* k, const void* v, const vo
 cudaError_t tc_dstate_local(const Dims& d, const void* q, const void* d_o, const void* g,
                             float* D, cudaStream_t st);
 bool tc_fwd_supported(const Dims& d);
-cudaError_t tc_fwd_out(const Dims& d, const void* q, const void* k, const void* v, const void* g,
-                       const float* S_in, void* o, cudaStream_t st);
-cudaError_t tc_bwd_dv(const Dims& d, const void* q, const void* k, const void* d_o,
-                      const void* g, const float* D, void* dv, cudaStream_t st);
+// Q~ = bf16(q e^{b}), K~ = bf16(k e^{-b}) and e^{b_last} per chunk (tc_decay.cu)
+cudaError_t tc_decay(const Dims& d, const void* q, const void* k, const void* g, void* Qt,
+                     void* Kt, float* Eb, cudaStream_t st);
+cudaError_t tc_fwd_out(const Dims& d, const void* Qt, const void* Kt, const void* v,
+                       const float* Eb, const float* S_in, void* o, cudaStream_t st);
+cudaError_t tc_bwd_dv(const Dims& d, const void* Qt, const void* Kt, const void* d_o,
+                      const float* Eb, const float* D, void* dv, cudaStream_t st);
 bool tc_bwd_qk_supported(const Dims& d);
-cudaError_t tc_bwd_qk(const Dims& d, const void* q, const void* k, const void* v, const void* g,
-                      const float* S_in, const void* d_o, void* dq, void* dk, void* dg, float* D,
-                      float* carry, float* qdq, cudaStream_t st);
+cudaError_t tc_bwd_qk(const Dims& d, const void* Qt, const void* Kt, const void* v,
+                      const void* g, const float* Eb, const float* S_in, const void* d_o,
+                      void* dq, void* dk, void* dg, float* D, float* carry, float* qdq,
+                      cudaStream_t st);
 bool tc_supported(const Dims& d);
+// Whether the tensor-core path of this shape runs the decay pass (and so needs
+// decay_layout's buffers in its workspace).
+bool tc_uses_decay(const Dims& d);
 cudaError_t tc_forward(const Dims& d, const void* q, const void* k, const void* v,
                        const void* g, const float* S0, void* o, float* S_final, float* S_in,
-                       float* gamma, cudaStream_t st);
+                       float* gamma, const DecayLayout& dl, void* ws, cudaStream_t st);
 cudaError_t tc_backward(const Dims& d, const void* q, const void* k, const void* v,
                         const void* g, const float* S_in, const float* gamma, const void* d_o,
                         const float* dS_final, void* dq, void* dk, void* dv, void* dg,
-                        float* dS0, float* D, float* carry, float* qdq, cudaStream_t st);
+                        float* dS0, float* D, float* carry, float* qdq, const DecayLayout& dl,
+                        void* ws, cudaStream_t st);
 
 }  // namespace zeco

@@ -1,6 +1,6 @@
 // tc.cu -- the tcgen05 tensor-core path (bf16 I/O, fp32 accumulation):
 // launch sequence of the forward and backward.  Steps without a tensor-core
-// kernel yet run their CUDA-core (SIMT) kernel.
+// kernel for the shape run their CUDA-core (SIMT) kernel.
 #include "common.cuh"
 #include "launch.h"
 
@@ -8,31 +8,46 @@ namespace zeco {
 
 bool tc_supported(const Dims& d) { return tc_state_supported(d); }
 
+bool tc_uses_decay(const Dims& d) { return tc_supported(d) && tc_fwd_supported(d); }
+
 cudaError_t tc_forward(const Dims& d, const void* q, const void* k, const void* v,
                        const void* g, const float* S0, void* o, float* S_final, float* S_in,
-                       float* gamma, cudaStream_t st) {
+                       float* gamma, const DecayLayout& dl, void* ws, cudaStream_t st) {
   cudaError_t e = tc_chunk_state(d, k, v, g, S_in, gamma, st);
   if (e != cudaSuccess) return e;
   e = launch_seg_scan_fwd(d, S_in, gamma, S0, S_final, st);
   if (e != cudaSuccess) return e;
-  return tc_fwd_supported(d) ? tc_fwd_out(d, q, k, v, g, S_in, o, st)
-                             : simt_fwd_out_bf16(d, q, k, v, g, S_in, o, st);
+  if (!tc_fwd_supported(d)) return simt_fwd_out_bf16(d, q, k, v, g, S_in, o, st);
+  char* w = (char*)ws;
+  void* Qt = w + dl.Qt_off;
+  void* Kt = w + dl.Kt_off;
+  float* Eb = (float*)(w + dl.Eb_off);
+  e = tc_decay(d, q, k, g, Qt, Kt, Eb, st);
+  if (e != cudaSuccess) return e;
+  return tc_fwd_out(d, Qt, Kt, v, Eb, S_in, o, st);
 }
 
 cudaError_t tc_backward(const Dims& d, const void* q, const void* k, const void* v,
                         const void* g, const float* S_in, const float* gamma, const void* d_o,
                         const float* dS_final, void* dq, void* dk, void* dv, void* dg,
-                        float* dS0, float* D, float* carry, float* qdq, cudaStream_t st) {
+                        float* dS0, float* D, float* carry, float* qdq, const DecayLayout& dl,
+                        void* ws, cudaStream_t st) {
   cudaError_t e = tc_dstate_local(d, q, d_o, g, D, st);
   if (e != cudaSuccess) return e;
   e = launch_seg_scan_rev(d, D, S_in, gamma, dS_final, dS0, carry, st);
   if (e != cudaSuccess) return e;
   if (!tc_fwd_supported(d))
     return simt_bwd_main_bf16(d, q, k, v, g, S_in, d_o, dq, dk, dv, dg, D, carry, qdq, st);
-  e = tc_bwd_dv(d, q, k, d_o, g, D, dv, st);
+  char* w = (char*)ws;
+  void* Qt = w + dl.Qt_off;
+  void* Kt = w + dl.Kt_off;
+  float* Eb = (float*)(w + dl.Eb_off);
+  e = tc_decay(d, q, k, g, Qt, Kt, Eb, st);
+  if (e != cudaSuccess) return e;
+  e = tc_bwd_dv(d, Qt, Kt, d_o, Eb, D, dv, st);
   if (e != cudaSuccess) return e;
   if (tc_bwd_qk_supported(d))
-    return tc_bwd_qk(d, q, k, v, g, S_in, d_o, dq, dk, dg, D, carry, qdq, st);
+    return tc_bwd_qk(d, Qt, Kt, v, g, Eb, S_in, d_o, dq, dk, dg, D, carry, qdq, st);
   return simt_bwd_dqk_bf16(d, q, k, v, g, S_in, d_o, dq, dk, dg, D, carry, qdq, st);
 }
 

@@ -22,13 +22,17 @@
 // adds the two halves through distributed shared memory and each CTA finishes
 // 32 of the 64 rows.
 //
+// Q~, K~ (bf16) and e^{b_last} come from the decay pass (tc_decay.cu); the
+// epilogue rebuilds e^{+-b_t} of its own elements from log_alpha.
+//
 // Precision of dlog_alpha.  Its suffix sum runs over the whole segment, so
 // errors in the terms add up like a random walk.  Two measures keep them
 // small: (1) the state copy used by the tensor cores is split into two bf16
 // parts (hi + lo), so the state products are accurate to ~2^-17; (2) the terms
 // use the rounded operands that the state itself was built from
-// (bf16(Q~) and bf16(K~) times the raw accumulators), so that the identity's
-// telescoping holds for the rounded model instead of breaking on the rounding.
+// (the stored bf16 Q~ and K~ times the raw accumulators), so that the
+// identity's telescoping holds for the rounded model instead of breaking on
+// the rounding.
 //
 // TMEM columns: [0, 128) state (d_v group g of this CTA at 64 g) | [128, 192)
 // dA (M = 64 layout) | [192, 256) dq^T or dk^T (M = 64 layout, lane = d_k row).
@@ -61,46 +65,24 @@ constexpr int kOffV = kOffDO + kC * kDVH * 2;    // v tile
 constexpr int kOffHi = kOffV + kC * kDVH * 2;    // state copy, high part [256 j][64 i]
 constexpr int kOffLo = kOffHi + kDVH * kKB * 2;  // state copy, low part
 constexpr int kXTile = kC * kKB * 2;             // one [64 t][64 i] bf16 tile
-constexpr int kXBuf = 3 * kXTile + 32 * kC * 4;  // q, k, g tiles + q.dq rows [64 t][32 i] fp32
+// Q~, K~, log_alpha tiles + q.dq rows [64 t][32 i] fp32 + e^{b_last} [64] fp32
+constexpr int kXBuf = 3 * kXTile + 32 * kC * 4 + 1024;
 constexpr int kOffX = kOffLo + kDVH * kKB * 2;   // 2 buffers of kXBuf (chunk parity)
 constexpr int kOffP = kOffX + 2 * kXBuf;         // masked dA partial [64 t][64 s] bf16
 constexpr int kOffR = kOffP + kC * kC * 2;       // 2 x [32 rows][64] fp32 from the peer
-constexpr int kOffE = kOffR + 2 * 32 * kC * 4;   // e^{b_last} [64] fp32
-constexpr int kOffPq = kOffE + 256;              // quarter products of alpha [4][64] fp32
-constexpr int kOffQS = kOffPq + 1024;            // reverse: quarter sums of dg terms [4][32]
+constexpr int kOffGq = kOffR + 2 * 32 * kC * 4;  // quarter sums of log_alpha [4][32] fp32
+constexpr int kOffQS = kOffGq + 512;             // reverse: quarter sums of dg terms [4][32]
 constexpr int kOffRun = kOffQS + 512;            // reverse: dg suffix carried per row [32]
-constexpr int kSmem = kOffE + 2048;
+constexpr int kSmem = kOffRun + 128;
 
 __device__ int g_qk_status = 0;
-
-// The decay factors of one d_k column over a chunk, evaluated identically in
-// every place that needs them (so that the rounded operands can be rebuilt
-// bit for bit): alpha_t = exp(g_t), pre_t = prod_{r<=t} alpha_r.
-__device__ __forceinline__ float alpha_of(const __nv_bfloat16* ge) {
-  return __expf(__bfloat162float(*ge));
-}
-
-// Decay factors of column c over a chunk are built from four quarters of 16
-// tokens.  Pq[qd][c] = alpha over quarter qd (left to right); the prefix offset
-// of quarter qd, the suffix offset (product of the later quarters) and the
-// total are combined in one fixed order here, so every caller gets the same
-// bits.
-__device__ __forceinline__ void quarter_offsets(const float* Pq, int c, int qd, float& off,
-                                                float& sufq, float& total) {
-  const float P0 = Pq[c], P1 = Pq[64 + c], P2 = Pq[128 + c], P3 = Pq[192 + c];
-  const float o1 = P0, o2 = o1 * P1, o3 = o2 * P2;
-  off = qd == 0 ? 1.f : (qd == 1 ? o1 : (qd == 2 ? o2 : o3));
-  total = o3 * P3;
-  const float s2 = P3, s1 = s2 * P2, s0 = s1 * P1;
-  sufq = qd == 3 ? 1.f : (qd == 2 ? s2 : (qd == 1 ? s1 : s0));
-}
 
 template <bool REV>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                  const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmV,
                  const __grid_constant__ CUtensorMap tmDO, const __grid_constant__ CUtensorMap tmQD,
-                 const float* __restrict__ S_src,
+                 const float* __restrict__ Eb, const float* __restrict__ S_src,
                  const float* __restrict__ carry, __nv_bfloat16* __restrict__ out,
                  __nv_bfloat16* __restrict__ dg, float* __restrict__ qdq, int64_t T, int dk,
                  int P, int64_t L) {
@@ -112,8 +94,7 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   unsigned char* sLo = sm + kOffLo;
   unsigned char* sP = sm + kOffP;
   float* sR = reinterpret_cast<float*>(sm + kOffR);
-  float* sE = reinterpret_cast<float*>(sm + kOffE);
-  float* sPq = reinterpret_cast<float*>(sm + kOffPq);
+  float* sGq = reinterpret_cast<float*>(sm + kOffGq);
   float* sQS = reinterpret_cast<float*>(sm + kOffQS);
   float* sRun = reinterpret_cast<float*>(sm + kOffRun);
   __shared__ uint64_t bar_x[2], bar_dv, bar_g1, bar_g2;
@@ -155,14 +136,17 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   const uint32_t lane_off = (uint32_t)(lg * 32) << 16;
 
   auto chunk_row = [&](int n) { return (int32_t)(row0 + (int64_t)n * kC); };
-  // q, k, g tiles of chunk n (and, reverse, this CTA's q.dq rows) into buffer `buf`
+  // Q~, K~, log_alpha tiles of chunk n, its e^{b_last} for rows i0.. and, reverse,
+  // this CTA's q.dq rows, into buffer `buf`
   auto issue_x = [&](int n, int buf) {
     const int32_t r = chunk_row(n);
     unsigned char* xb = sm + kOffX + buf * kXBuf;
-    mbar_expect_tx(&bar_x[buf], 3 * kXTile + (REV ? 32 * kC * 4 : 0));
+    mbar_expect_tx(&bar_x[buf], 3 * kXTile + kKB * 4 + (REV ? 32 * kC * 4 : 0));
     tma_load_2d(xb, &tmQ, i0, r, &bar_x[buf]);
     tma_load_2d(xb + kXTile, &tmK, i0, r, &bar_x[buf]);
     tma_load_2d(xb + 2 * kXTile, &tmG, i0, r, &bar_x[buf]);
+    bulk_load(xb + 3 * kXTile + 32 * kC * 4, Eb + (size_t)(r / kC) * dk + i0, kKB * 4,
+              &bar_x[buf]);
     if (REV) tma_load_2d(xb + 3 * kXTile, &tmQD, i0 + 32 * (int)rank, r, &bar_x[buf]);
   };
   auto issue_dv = [&](int n) {
@@ -215,7 +199,7 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   }
 
   // state <- e^{b_last} .* state (column i scaled by sE[i]) and its hi/lo copy
-  auto state_pass = [&]() {
+  auto state_pass = [&](const float* sE) {
     float r[64];
     tmem_ld32(tmem + lane_off + grp * 64, r);
     tmem_ld32(tmem + lane_off + grp * 64 + 32, r + 32);
@@ -233,9 +217,7 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     return reinterpret_cast<__nv_bfloat16*>(base + sw128((uint32_t)t, (uint32_t)((c & 63) >> 3)) +
                                             (uint32_t)(c & 7) * 2u);
   };
-  // worker geometry of the prologue (64 columns x 4 quarters) and of the
-  // epilogue (32 owned rows x 4 quarters, threads 0..127)
-  const int pc = tid & 63, pq = tid >> 6;
+  // worker geometry of the epilogue (32 owned rows x 4 quarters, threads 0..127)
   const int er = tid & 31, eq = (tid >> 5) & 3;
   const int ec = 32 * (int)rank + er;  // column (d_k row) of the epilogue worker
 
@@ -251,46 +233,11 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     unsigned char* sK = sQ + kXTile;
     unsigned char* sG = sQ + 2 * kXTile;
     const float* sQD = reinterpret_cast<const float*>(sQ + 3 * kXTile);
+    const float* sE = sQD + 32 * kC;  // e^{b_last} of rows i0..i0+63
     // the next chunk's tiles go to the other buffer (freed at the end of the last iteration)
     if (tid == 0 && it + 1 < nc) issue_x(REV ? n - 1 : n + 1, xbuf ^ 1);
     if (!mbar_wait(&bar_x[xbuf], (uint32_t)((it >> 1) & 1))) atomicExch(&g_qk_status, 1);
-    // ---- prologue (64 columns x 4 quarters): forward K~ = bf16(k e^{-b}); reverse Q~ = bf16(q e^{b})
-    {
-      float al[16];
-      float prod = 1.f;
-#pragma unroll
-      for (int u = 0; u < 16; ++u) {
-        al[u] = alpha_of(tile_at(sG, 16 * pq + u, pc));
-        prod *= al[u];
-      }
-      sPq[pq * 64 + pc] = prod;
-      __syncthreads();
-      float off, sufq, total;
-      quarter_offsets(sPq, pc, pq, off, sufq, total);
-      if (pq == 3) sE[pc] = total;
-      if (REV) {
-        float run = off;
-#pragma unroll
-        for (int u = 0; u < 16; ++u) {
-          run *= al[u];
-          __nv_bfloat16* qe = tile_at(sQ, 16 * pq + u, pc);
-          *qe = __float2bfloat16_rn(__bfloat162float(*qe) * run);
-        }
-      } else {
-        const float rinv = 1.0f / total;
-        float run = sufq;
-#pragma unroll
-        for (int u = 15; u >= 0; --u) {
-          __nv_bfloat16* ke = tile_at(sK, 16 * pq + u, pc);
-          *ke = __float2bfloat16_rn(__bfloat162float(*ke) * (run * rinv));
-          run *= al[u];
-        }
-      }
-    }
-    if (REV) {
-      __syncthreads();  // sE complete
-      state_pass();
-    }
+    if (REV) state_pass(sE);
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -354,7 +301,7 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         }
       }
     }
-    if (!REV) state_pass();  // forward: post-scale and copy for the next chunk
+    if (!REV) state_pass(sE);  // forward: post-scale and copy for the next chunk
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -397,47 +344,49 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       for (int t = 0; t < kC; ++t) rv[t] += a[t];
     }
     __syncthreads();
-    // ---- epilogue: 32 owned rows x 4 quarters of 16 tokens
+    // ---- epilogue: 32 owned rows x 4 quarters of 16 tokens.  b_t of row ec is the
+    //      sum of log_alpha over the earlier quarters plus the running sum in this one.
     if (tid < 128) {
-      float al[16];
+      float gl[16];
+      float gq = 0.f;
 #pragma unroll
-      for (int u = 0; u < 16; ++u) al[u] = alpha_of(tile_at(sG, 16 * eq + u, ec));
-      float off, sufq, total;
-      quarter_offsets(sPq, ec, eq, off, sufq, total);
+      for (int u = 0; u < 16; ++u) {
+        gl[u] = __bfloat162float(*tile_at(sG, 16 * eq + u, ec));
+        gq += gl[u];
+      }
+      sGq[eq * 32 + er] = gq;
+      asm volatile("bar.sync 1, 128;" ::: "memory");  // the 128 epilogue threads
+      float boff = 0.f;
+      for (int q2 = 0; q2 < eq; ++q2) boff += sGq[q2 * 32 + er];
       const float* acc = sAcc + er * kC + 16 * eq;
       const size_t base = (size_t)(chunk_row(n) + 16 * eq) * dk + i0 + ec;
       if (!REV) {
-        float run = off;
+        float b = boff;
 #pragma unroll
         for (int u = 0; u < 16; ++u) {
-          run *= al[u];
+          b += gl[u];
           const float av = acc[u];
-          out[base + (size_t)u * dk] = __float2bfloat16_rn(av * run);
-          // the reverse sweep's rounded Q~ times the raw accumulator (= q_eff dq)
-          const float qr = __bfloat162float(
-              __float2bfloat16_rn(__bfloat162float(*tile_at(sQ, 16 * eq + u, ec)) * run));
-          qdq[base + (size_t)u * dk] = qr * av;
+          out[base + (size_t)u * dk] = __float2bfloat16_rn(av * __expf(b));
+          // the stored rounded Q~ times the raw accumulator (= q_eff dq)
+          qdq[base + (size_t)u * dk] = __bfloat162float(*tile_at(sQ, 16 * eq + u, ec)) * av;
         }
       } else {
-        const float rinv = 1.0f / total;
-        float run = sufq;
+        float b = boff;
         float term[16];
 #pragma unroll
-        for (int u = 15; u >= 0; --u) {
-          const float e = run * rinv;
-          run *= al[u];
+        for (int u = 0; u < 16; ++u) {
+          b += gl[u];
           const float av = acc[u];
-          out[base + (size_t)u * dk] = __float2bfloat16_rn(av * e);
-          // the forward sweep's rounded K~ times the raw accumulator (= k_eff dk)
-          const float kr = __bfloat162float(
-              __float2bfloat16_rn(__bfloat162float(*tile_at(sK, 16 * eq + u, ec)) * e));
-          term[u] = sQD[(16 * eq + u) * 32 + er] - kr * av;
+          out[base + (size_t)u * dk] = __float2bfloat16_rn(av * __expf(-b));
+          // the stored rounded K~ times the raw accumulator (= k_eff dk)
+          term[u] = sQD[(16 * eq + u) * 32 + er] -
+                    __bfloat162float(*tile_at(sK, 16 * eq + u, ec)) * av;
         }
         float qsum = 0.f;
 #pragma unroll
         for (int u = 0; u < 16; ++u) qsum += term[u];
         sQS[eq * 32 + er] = qsum;
-        asm volatile("bar.sync 1, 128;" ::: "memory");  // the 128 epilogue threads
+        asm volatile("bar.sync 1, 128;" ::: "memory");
         float carry_in = sRun[er];
         for (int q2 = 3; q2 > eq; --q2) carry_in += sQS[q2 * 32 + er];
         float runq = carry_in;
@@ -461,8 +410,8 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
 template <bool REV>
 cudaError_t launch_qk(const Dims& d, const CUtensorMap& tq, const CUtensorMap& tk,
                       const CUtensorMap& tg, const CUtensorMap& tv, const CUtensorMap& tdo,
-                      const CUtensorMap& tqd, const float* S_src, const float* carry, void* out, void* dg, float* qdq,
-                      cudaStream_t st) {
+                      const CUtensorMap& tqd, const float* Eb, const float* S_src,
+                      const float* carry, void* out, void* dg, float* qdq, cudaStream_t st) {
   auto kern = tc_bwd_qk_kernel<REV>;
   const int smem = kSmem + 1024;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -479,7 +428,7 @@ cudaError_t launch_qk(const Dims& d, const CUtensorMap& tq, const CUtensorMap& t
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, tq, tk, tg, tv, tdo, tqd, S_src, carry, (__nv_bfloat16*)out,
+  return cudaLaunchKernelEx(&cfg, kern, tq, tk, tg, tv, tdo, tqd, Eb, S_src, carry, (__nv_bfloat16*)out,
                             (__nv_bfloat16*)dg, qdq, d.T, (int)d.dk, d.P, d.L);
 }
 
@@ -489,20 +438,21 @@ bool tc_bwd_qk_supported(const Dims& d) {
   return d.bf16 && d.dk % kKB == 0 && d.dv == kDV && d.C == kC && d.L % kC == 0;
 }
 
-cudaError_t tc_bwd_qk(const Dims& d, const void* q, const void* k, const void* v, const void* g,
-                      const float* S_in, const void* d_o, void* dq, void* dk, void* dg, float* D,
-                      float* carry, float* qdq, cudaStream_t st) {
+cudaError_t tc_bwd_qk(const Dims& d, const void* Qt, const void* Kt, const void* v,
+                      const void* g, const float* Eb, const float* S_in, const void* d_o,
+                      void* dq, void* dk, void* dg, float* D, float* carry, float* qdq,
+                      cudaStream_t st) {
   CUtensorMap tq, tk, tg, tv, tdo, tqd;
   const uint64_t rows = (uint64_t)(d.B * d.H * d.T);
-  if (!make_tmap_bf16(&tq, q, rows, d.dk, kC) || !make_tmap_bf16(&tk, k, rows, d.dk, kC) ||
+  if (!make_tmap_bf16(&tq, Qt, rows, d.dk, kC) || !make_tmap_bf16(&tk, Kt, rows, d.dk, kC) ||
       !make_tmap_bf16(&tg, g, rows, d.dk, kC) || !make_tmap_bf16(&tv, v, rows, d.dv, kC) ||
       !make_tmap_bf16(&tdo, d_o, rows, d.dv, kC) ||
       !make_tmap_f32_plain(&tqd, qdq, rows, d.dk, 32, kC))
     return cudaErrorInvalidValue;
-  cudaError_t e = launch_qk<false>(d, tq, tk, tg, tv, tdo, tqd, S_in, carry, dq, dg, qdq, st);
+  cudaError_t e = launch_qk<false>(d, tq, tk, tg, tv, tdo, tqd, Eb, S_in, carry, dq, dg, qdq, st);
   prof_mark("tc_bwd_dq", st);
   if (e != cudaSuccess) return e;
-  e = launch_qk<true>(d, tq, tk, tg, tv, tdo, tqd, D, carry, dk, dg, qdq, st);
+  e = launch_qk<true>(d, tq, tk, tg, tv, tdo, tqd, Eb, D, carry, dk, dg, qdq, st);
   prof_mark("tc_bwd_dk", st);
   return e;
 }

@@ -239,3 +239,18 @@ __device__ __forceinline__ void cluster_sync() {
 }
 }  // namespace tc
 }  // namespace zeco
+
+namespace zeco {
+namespace tc {
+// Bulk copy of `bytes` contiguous bytes global -> shared (both addresses
+// 16-byte aligned, bytes a multiple of 16), completing on `bar`.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+}  // namespace tc
+}  // namespace zeco

@@ -17,9 +17,8 @@
 // One CTA owns (b, h, segment, 128 d_v columns) and keeps S^T (lanes = d_v
 // column j, TMEM columns = d_k row i) in fp32 in tensor memory, plus a bf16
 // copy of S^T that is the A operand (read from TMEM) of o^T = S^T Q~^T.
-// e^{b_t} and e^{-b_t} come from one exponential per element: prefix products
-// of alpha give e^{b_t}, suffix products give e^{b_last - b_t}, and one
-// reciprocal per row gives e^{-b_last}.
+// Q~, K~ and e^{b_last} come from the decay pass (tc_decay.cu) and arrive by
+// TMA, one chunk ahead, with no per-element work in the kernel.
 //
 // The same kernel, run backwards over the chunks (BWD = true), computes dv
 // from the adjoint state dS of the segment end (D[p+1], from the reverse
@@ -57,20 +56,18 @@ __device__ int g_fwd_status = 0;
 
 template <int DK>
 struct FwdSmem {
-  static constexpr int kTile = DK * kC * 2;  // q / k / g tile bytes
-  static constexpr int kXBuf = 3 * kTile;    // q, k, g tiles of one chunk
-  static constexpr int kX = 0;               // 2 buffers (chunk parity)
+  static constexpr int kTile = DK * kC * 2;                   // Q~ / K~ tile bytes
+  static constexpr int kXBuf = (2 * kTile + DK * 4 + 1023) / 1024 * 1024;  // Q~, K~, e^{b_last}
+  static constexpr int kX = 0;                                // 2 buffers (chunk parity)
   static constexpr int kV = 2 * kXBuf;
   static constexpr int kP = kV + kNV * kC * 2;
-  static constexpr int kE = kP + kC * kC * 2;
-  static constexpr int kPq = kE + DK * 4;  // per-quarter alpha products [4][DK]
-  static constexpr int kBytes = kPq + 4 * DK * 4;
+  static constexpr int kBytes = kP + kC * kC * 2;
 };
 
 template <int DK, bool BWD>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmV,
+                const __grid_constant__ CUtensorMap tmV, const float* __restrict__ Eb,
                 const float* __restrict__ S_src, __nv_bfloat16* __restrict__ o, int64_t T, int dv,
                 int P, int64_t L) {
   using SM = FwdSmem<DK>;
@@ -78,8 +75,6 @@ tc_sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   unsigned char* sm = (unsigned char*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
   unsigned char* sV = sm + SM::kV;
   unsigned char* sP = sm + SM::kP;
-  float* sE = reinterpret_cast<float*>(sm + SM::kE);
-  float* sPq = reinterpret_cast<float*>(sm + SM::kPq);
   __shared__ uint64_t bar_qkg[2], bar_v, bar_g1, bar_g2;
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
@@ -104,7 +99,6 @@ tc_sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     fence_mbar_init();
     prefetch_tmap(&tmQ);
     prefetch_tmap(&tmK);
-    prefetch_tmap(&tmG);
     prefetch_tmap(&tmV);
   }
   if (warp == 0) tmem_alloc(&tmem_base, 512);
@@ -114,15 +108,16 @@ tc_sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   const uint32_t tmem = tmem_base;
   const uint32_t lane_off = (uint32_t)(lg * 32) << 16;
 
+  // Q~, K~ tiles and the e^{b_last} row of chunk n into buffer `buf`
   auto issue_qkg = [&](int n, int buf) {
     const int32_t r = (int32_t)(row0 + (int64_t)n * kC);
     unsigned char* xb = sm + SM::kX + buf * SM::kXBuf;
-    mbar_expect_tx(&bar_qkg[buf], 3 * SM::kTile);
+    mbar_expect_tx(&bar_qkg[buf], 2 * SM::kTile + DK * 4);
     for (int b = 0; b < DK / 64; ++b) {
       tma_load_2d(xb + b * 8192, &tmQ, b * 64, r, &bar_qkg[buf]);
       tma_load_2d(xb + SM::kTile + b * 8192, &tmK, b * 64, r, &bar_qkg[buf]);
-      tma_load_2d(xb + 2 * SM::kTile + b * 8192, &tmG, b * 64, r, &bar_qkg[buf]);
     }
+    bulk_load(xb + 2 * SM::kTile, Eb + (size_t)(r / kC) * DK, DK * 4, &bar_qkg[buf]);
   };
   auto issue_v = [&](int n) {
     const int32_t r = (int32_t)(row0 + (int64_t)n * kC);
@@ -156,7 +151,7 @@ tc_sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   }
 
   // S^T (fp32) <- e^{b_last} .* S^T (column i scaled by sE[i]) and its bf16 copy
-  auto state_pass = [&]() {
+  auto state_pass = [&](const float* sE) {
     for (int c = cq * (DK / 4); c < (cq + 1) * (DK / 4); c += 32) {
       float r[32];
       tmem_ld32(tmem + lane_off + c, r);
@@ -172,75 +167,21 @@ tc_sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     tmem_st_wait();
   };
 
-  // element (t, column c) of a [64 t][DK] tile stored as DK/64 blocks of 64 columns
-  auto tile_off = [](int t, int c) -> uint32_t {
-    return (uint32_t)(c >> 6) * 8192u + sw128((uint32_t)t, (uint32_t)((c & 63) >> 3)) +
-           (uint32_t)(c & 7) * 2u;
-  };
-  constexpr int kTasks = DK * 4 / kThreads;  // (column, token quarter) tasks per thread
-
   for (int it = 0; it < nc; ++it) {
     const int n = BWD ? (nc - 1 - it) : it;  // chunk index in the segment
     const uint32_t par = (uint32_t)(it & 1);
     const int xbuf = it & 1;
     unsigned char* sQ = sm + SM::kX + xbuf * SM::kXBuf;
     unsigned char* sK = sQ + SM::kTile;
-    unsigned char* sG = sQ + 2 * SM::kTile;
-    // the next chunk's q, k, g go to the other buffer (its last reader, MMA group 1
-    // of the previous chunk, has completed)
+    const float* sE = reinterpret_cast<const float*>(sQ + 2 * SM::kTile);  // e^{b_last}
+    // the next chunk's tiles go to the other buffer (its last readers, MMA group 1
+    // and the state pass of the previous chunk, have completed)
     if (tid == 0 && it + 1 < nc) issue_qkg(BWD ? n - 1 : n + 1, xbuf ^ 1);
-    // ------------------------------------------------ prologue: Q~, K~, e^{b_last}
     if (!mbar_wait(&bar_qkg[xbuf], (uint32_t)((it >> 1) & 1))) {
       atomicExch(&g_fwd_status, 1);
       abort_flag = 1;
     }
-    {
-      // decay factors per (column c, quarter q of 16 tokens): alpha products of the
-      // quarters first, then prefix products for Q~ and suffix products for K~
-      float al[kTasks][16];
-#pragma unroll
-      for (int k2 = 0; k2 < kTasks; ++k2) {
-        const int task = tid + k2 * kThreads, c = task % DK, q = task / DK;
-        float prod = 1.f;
-#pragma unroll
-        for (int u = 0; u < 16; ++u) {
-          al[k2][u] = __expf(__bfloat162float(
-              *reinterpret_cast<const __nv_bfloat16*>(sG + tile_off(16 * q + u, c))));
-          prod *= al[k2][u];
-        }
-        sPq[q * DK + c] = prod;
-      }
-      __syncthreads();
-#pragma unroll
-      for (int k2 = 0; k2 < kTasks; ++k2) {
-        const int task = tid + k2 * kThreads, c = task % DK, q = task / DK;
-        const float P0 = sPq[c], P1 = sPq[DK + c], P2 = sPq[2 * DK + c], P3 = sPq[3 * DK + c];
-        const float off = q == 0 ? 1.f : (q == 1 ? P0 : (q == 2 ? P0 * P1 : (P0 * P1) * P2));
-        const float sufq = q == 3 ? 1.f : (q == 2 ? P3 : (q == 1 ? P3 * P2 : (P3 * P2) * P1));
-        const float total = ((P0 * P1) * P2) * P3;
-        if (q == 3) sE[c] = total;  // e^{b_last}
-        float run = off;
-#pragma unroll
-        for (int u = 0; u < 16; ++u) {
-          run *= al[k2][u];
-          __nv_bfloat16* qe = reinterpret_cast<__nv_bfloat16*>(sQ + tile_off(16 * q + u, c));
-          *qe = __float2bfloat16_rn(__bfloat162float(*qe) * run);
-        }
-        const float rinv = 1.0f / total;
-        float suf = sufq;
-#pragma unroll
-        for (int u = 15; u >= 0; --u) {
-          __nv_bfloat16* ke = reinterpret_cast<__nv_bfloat16*>(sK + tile_off(16 * q + u, c));
-          *ke = __float2bfloat16_rn(__bfloat162float(*ke) * (suf * rinv));
-          suf *= al[k2][u];
-        }
-      }
-    }
-    if (BWD) {
-      __syncthreads();  // sE complete
-      state_pass();
-    }
-    fence_async_smem();
+    if (BWD) state_pass(sE);
     tc_fence_before();
     __syncthreads();
     if (abort_flag) break;
@@ -305,7 +246,7 @@ tc_sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       }
     }
     // forward: S <- e^{b_last} .* S, refresh the bf16 copy for the next chunk
-    if (!BWD) state_pass();
+    if (!BWD) state_pass(sE);
     tmem_st_wait();
     fence_async_smem();
     tc_fence_before();
@@ -347,19 +288,19 @@ tc_sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 }
 
 template <int DK, bool BWD>
-cudaError_t launch_sweep(const Dims& d, const void* q, const void* k, const void* v,
-                         const void* g, const float* S_src, void* o, cudaStream_t st) {
-  CUtensorMap tq, tk, tg, tv;
+cudaError_t launch_sweep(const Dims& d, const void* Qt, const void* Kt, const void* v,
+                         const float* Eb, const float* S_src, void* o, cudaStream_t st) {
+  CUtensorMap tq, tk, tv;
   const uint64_t rows = (uint64_t)(d.B * d.H * d.T);
-  if (!make_tmap_bf16(&tq, q, rows, DK, kC) || !make_tmap_bf16(&tk, k, rows, DK, kC) ||
-      !make_tmap_bf16(&tg, g, rows, DK, kC) || !make_tmap_bf16(&tv, v, rows, d.dv, kC))
+  if (!make_tmap_bf16(&tq, Qt, rows, DK, kC) || !make_tmap_bf16(&tk, Kt, rows, DK, kC) ||
+      !make_tmap_bf16(&tv, v, rows, d.dv, kC))
     return cudaErrorInvalidValue;
   const int smem = FwdSmem<DK>::kBytes + 1024;
   auto kern = tc_sweep_kernel<DK, BWD>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)(d.dv / kNV), (unsigned)(d.B * d.H * d.P));
-  kern<<<grid, kThreads, smem, st>>>(tq, tk, tg, tv, S_src, (__nv_bfloat16*)o, d.T, (int)d.dv,
+  kern<<<grid, kThreads, smem, st>>>(tq, tk, tv, Eb, S_src, (__nv_bfloat16*)o, d.T, (int)d.dv,
                                      d.P, d.L);
   return cudaGetLastError();
 }
@@ -371,18 +312,18 @@ bool tc_fwd_supported(const Dims& d) {
          d.L % kC == 0;
 }
 
-cudaError_t tc_fwd_out(const Dims& d, const void* q, const void* k, const void* v, const void* g,
-                       const float* S_in, void* o, cudaStream_t st) {
-  cudaError_t e = d.dk == 256 ? launch_sweep<256, false>(d, q, k, v, g, S_in, o, st)
-                              : launch_sweep<128, false>(d, q, k, v, g, S_in, o, st);
+cudaError_t tc_fwd_out(const Dims& d, const void* Qt, const void* Kt, const void* v,
+                       const float* Eb, const float* S_in, void* o, cudaStream_t st) {
+  cudaError_t e = d.dk == 256 ? launch_sweep<256, false>(d, Qt, Kt, v, Eb, S_in, o, st)
+                              : launch_sweep<128, false>(d, Qt, Kt, v, Eb, S_in, o, st);
   prof_mark("tc_fwd_out", st);
   return e;
 }
 
-cudaError_t tc_bwd_dv(const Dims& d, const void* q, const void* k, const void* d_o,
-                      const void* g, const float* D, void* dv, cudaStream_t st) {
-  cudaError_t e = d.dk == 256 ? launch_sweep<256, true>(d, q, k, d_o, g, D, dv, st)
-                              : launch_sweep<128, true>(d, q, k, d_o, g, D, dv, st);
+cudaError_t tc_bwd_dv(const Dims& d, const void* Qt, const void* Kt, const void* d_o,
+                      const float* Eb, const float* D, void* dv, cudaStream_t st) {
+  cudaError_t e = d.dk == 256 ? launch_sweep<256, true>(d, Qt, Kt, d_o, Eb, D, dv, st)
+                              : launch_sweep<128, true>(d, Qt, Kt, d_o, Eb, D, dv, st);
   prof_mark("tc_bwd_dv", st);
   return e;
 }

@@ -101,12 +101,18 @@ typedef struct zeco_shape {
 size_t zeco_gla_saved_bytes(const zeco_shape *shape);
 
 /*
- * Bytes of scratch memory the forward (bwd = 0) or backward (bwd = 1) needs.
+ * Bytes of scratch memory the forward (bwd = 0) or backward (bwd = 1) needs,
+ * for the path the shape resolves to (shape->path, see zeco_gla_resolve_path).
  * The backward holds the adjoint of every segment's incoming state
  * [B,H,P+1,dk,dv] fp32, one dlog_alpha carry row per segment [B,H,P,dk] fp32,
  * and q .* dq in fp32 [B,H,T,dk] (dlog_alpha is a long suffix sum of
  * q .* dq - k .* dk that cancels heavily, so its terms are kept in fp32).
- * Returns 0 when no scratch is needed or the shape is invalid.
+ * On the tensor-core path both directions also hold the decay-weighted
+ * operands of the chunked form (Pith review of ZeCO, minor comment 4):
+ * Q~ = q .* e^{b} and K~ = k .* e^{-b} [B,H,T,dk] bf16 and e^{b_last} of every
+ * chunk [B,H,T/64,dk] fp32, b being the cumulative log-decay from the chunk
+ * start.  Returns 0 when no scratch is needed or the shape is invalid or
+ * unsupported.
  */
 size_t zeco_gla_workspace_bytes(const zeco_shape *shape, int bwd);
 
@@ -115,8 +121,10 @@ size_t zeco_gla_workspace_bytes(const zeco_shape *shape, int bwd);
  *   S0 == NULL means a zero initial state.
  *   saved: zeco_gla_saved_bytes(shape) bytes, kept unchanged until the matching
  *          zeco_gla_bwd has run.
- *   workspace / ws_bytes: at least zeco_gla_workspace_bytes(shape, 0) bytes
- *          (may be NULL when that is 0).
+ *   workspace / ws_bytes: at least zeco_gla_workspace_bytes(shape, 0) bytes,
+ *          16-byte aligned and overwritten (may be NULL when that is 0);
+ *          ZECO_ERR_WORKSPACE when ws_bytes is smaller, ZECO_ERR_ARG when a
+ *          needed workspace is NULL or misaligned.
  */
 int zeco_gla_fwd(const zeco_shape *shape, const void *q, const void *k, const void *v,
                  const void *log_alpha, const float *S0, void *o, float *S_final, void *saved,

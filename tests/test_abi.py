@@ -47,8 +47,16 @@ def test_sizes_follow_the_layout(lib):
     state = 4 * 65 * 256 * 512 * 4
     gam = 4 * 64 * 256 * 4
     assert z.saved_bytes(s) == state + gam
-    assert z.workspace_bytes(s, True) == state + gam + 4 * (1 << 20) * 256 * 4
-    assert z.workspace_bytes(s, False) == 0
+    qdq = 4 * (1 << 20) * 256 * 4
+    # tensor-core path: Q~ and K~ (bf16) and e^{b_last} per 64-token chunk (fp32)
+    decay = 2 * 4 * (1 << 20) * 256 * 2 + 4 * (1 << 20) // 64 * 256 * 4
+    assert z.workspace_bytes(s, True) == state + gam + qdq + decay
+    assert z.workspace_bytes(s, False) == decay
+    # the SIMT path keeps no decay-weighted operands
+    simt = _shape(path="simt", dtype="f32", dk=64, dv=64)
+    st64 = 4 * 65 * 64 * 64 * 4
+    assert z.workspace_bytes(simt, False) == 0
+    assert z.workspace_bytes(simt, True) == st64 + 4 * 64 * 64 * 4 + 4 * (1 << 20) * 64 * 4
 
 
 @pytest.mark.parametrize("kw,code", [
@@ -82,6 +90,9 @@ def test_null_and_misaligned_pointers_are_rejected(lib):
     assert lib.zeco_gla_fwd(ctypes.byref(s), *args, None, None, None, ok, None, 0, None) == -1
     assert lib.zeco_gla_fwd(ctypes.byref(s), bad, ok, ok, ok, None, ok, None, ok, None, 0,
                             None) == -1
+    # forward on the tensor-core path: workspace missing, then too small
+    assert lib.zeco_gla_fwd(ctypes.byref(s), *args, None, ok, None, ok, None, 0, None) == -1
+    assert lib.zeco_gla_fwd(ctypes.byref(s), *args, None, ok, None, ok, ok, 16, None) == -3
     # workspace too small for the backward
     rc = lib.zeco_gla_bwd(ctypes.byref(s), ok, ok, ok, ok, ok, ok, None, ok, ok, ok, ok, None,
                           ok, 16, None)
