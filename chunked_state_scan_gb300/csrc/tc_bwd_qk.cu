@@ -69,10 +69,12 @@ constexpr int kXTile = kC * kKB * 2;             // one [64 t][64 i] bf16 tile
 constexpr int kXBuf = 3 * kXTile + 32 * kC * 4 + 1024;
 constexpr int kOffX = kOffLo + kDVH * kKB * 2;   // 2 buffers of kXBuf (chunk parity)
 constexpr int kOffP = kOffX + 2 * kXBuf;         // masked dA partial [64 t][64 s] bf16
-constexpr int kOffR = kOffP + kC * kC * 2;       // 2 x [32 rows][64] fp32 from the peer
-constexpr int kOffGq = kOffR + 2 * 32 * kC * 4;  // quarter sums of log_alpha [4][32] fp32
-constexpr int kOffQS = kOffGq + 512;             // reverse: quarter sums of dg terms [4][32]
-constexpr int kOffRun = kOffQS + 512;            // reverse: dg suffix carried per row [32]
+constexpr int kRS = kC + 4;                      // row stride of the partial sums (floats)
+constexpr int kOffR = kOffP + kC * kC * 2;       // peer's partial for my rows [32][kRS] fp32
+constexpr int kOffOwn = kOffR + 32 * kRS * 4;    // my own partial for my rows [32][kRS] fp32
+constexpr int kOffGq = kOffOwn + 32 * kRS * 4;   // sums of log_alpha per 8 tokens [8][32]
+constexpr int kOffQS = kOffGq + 1024;            // reverse: sums of dg terms per 8 tokens [8][32]
+constexpr int kOffRun = kOffQS + 1024;           // reverse: dg suffix carried per row [32]
 constexpr int kSmem = kOffRun + 128;
 
 __device__ int g_qk_status = 0;
@@ -94,6 +96,7 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   unsigned char* sLo = sm + kOffLo;
   unsigned char* sP = sm + kOffP;
   float* sR = reinterpret_cast<float*>(sm + kOffR);
+  float* sOwn = reinterpret_cast<float*>(sm + kOffOwn);
   float* sGq = reinterpret_cast<float*>(sm + kOffGq);
   float* sQS = reinterpret_cast<float*>(sm + kOffQS);
   float* sRun = reinterpret_cast<float*>(sm + kOffRun);
@@ -217,14 +220,84 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     return reinterpret_cast<__nv_bfloat16*>(base + sw128((uint32_t)t, (uint32_t)((c & 63) >> 3)) +
                                             (uint32_t)(c & 7) * 2u);
   };
-  // worker geometry of the epilogue (32 owned rows x 4 quarters, threads 0..127)
-  const int er = tid & 31, eq = (tid >> 5) & 3;
-  const int ec = 32 * (int)rank + er;  // column (d_k row) of the epilogue worker
+  // epilogue workers: owned row er (d_k row ec of the block) x 8 tokens 8 eg..8 eg+7
+  const int er = tid & 31, eg = tid >> 5;
+  const int ec = 32 * (int)rank + er;
 
   if (REV && tid < 32) sRun[tid] = carry[((size_t)bh * P + p) * dk + i0 + 32 * (int)rank + tid];
-  // peer's partials for my rows land in sR[buf][row - 32 rank][64]
   const uint32_t peer = rank ^ 1u;
 
+  // Per-element factors of a chunk's epilogue, read from the chunk's tiles in its
+  // own iteration and kept in registers until the epilogue runs in the next one
+  // (so the tile buffers are free for the next prefetch): ef = e^{b_t} (forward)
+  // or e^{-b_t} (reverse), xr = the stored rounded Q~ (forward) or K~ (reverse),
+  // qd = q.dq (reverse).  b_t sums log_alpha over the earlier 8-token groups of
+  // the chunk plus the running sum within this one.
+  float ef[8], xr[8], qd[8];
+  auto prefetch = [&](const unsigned char* sQ, const unsigned char* sK,
+                      const unsigned char* sG, const float* sQD) {
+    float gl[8];
+    float gs = 0.f;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      gl[u] = __bfloat162float(*tile_at(const_cast<unsigned char*>(sG), 8 * eg + u, ec));
+      gs += gl[u];
+    }
+    sGq[eg * 32 + er] = gs;
+    __syncthreads();
+    float b = 0.f;
+    for (int g2 = 0; g2 < eg; ++g2) b += sGq[g2 * 32 + er];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      b += gl[u];
+      ef[u] = __expf(REV ? -b : b);
+      xr[u] = __bfloat162float(*tile_at(const_cast<unsigned char*>(REV ? sK : sQ), 8 * eg + u, ec));
+      if (REV) qd[u] = sQD[(8 * eg + u) * 32 + er];
+    }
+  };
+  // outputs of chunk n from the two partial sums (peer's + own)
+  auto epilogue = [&](int n) {
+    const float4* rp = reinterpret_cast<const float4*>(sR + er * kRS + 8 * eg);
+    const float4* op = reinterpret_cast<const float4*>(sOwn + er * kRS + 8 * eg);
+    const float4 r0 = rp[0], r1 = rp[1], o0 = op[0], o1 = op[1];
+    const float acc[8] = {r0.x + o0.x, r0.y + o0.y, r0.z + o0.z, r0.w + o0.w,
+                          r1.x + o1.x, r1.y + o1.y, r1.z + o1.z, r1.w + o1.w};
+    const size_t base = (size_t)(chunk_row(n) + 8 * eg) * dk + i0 + ec;
+    if (!REV) {
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        out[base + (size_t)u * dk] = __float2bfloat16_rn(acc[u] * ef[u]);
+        // the stored rounded Q~ times the raw accumulator (= q_eff dq)
+        qdq[base + (size_t)u * dk] = xr[u] * acc[u];
+      }
+    } else {
+      float term[8];
+      float s = 0.f;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        out[base + (size_t)u * dk] = __float2bfloat16_rn(acc[u] * ef[u]);
+        // the stored rounded K~ times the raw accumulator (= k_eff dk)
+        term[u] = qd[u] - xr[u] * acc[u];
+        s += term[u];
+      }
+      sQS[eg * 32 + er] = s;
+      __syncthreads();
+      float runq = sRun[er];
+      for (int g2 = 7; g2 > eg; --g2) runq += sQS[g2 * 32 + er];
+#pragma unroll
+      for (int u = 7; u >= 0; --u) {
+        runq += term[u];
+        dg[base + (size_t)u * dk] = __float2bfloat16_rn(runq);
+      }
+      __syncthreads();
+      if (eg == 0) sRun[er] = runq;  // suffix through the whole chunk
+    }
+  };
+
+  // Exchange of the partial sums with the peer CTA: two alternating phases of
+  // the cluster barrier per chunk -- "sR free" (arrived after the epilogue has
+  // read it, waited on before writing into the peer's sR) and "partial sent"
+  // (arrived after the writes, waited on before the epilogue).
   for (int it = 0; it < nc; ++it) {
     const int n = REV ? (nc - 1 - it) : it;
     const uint32_t par = (uint32_t)(it & 1);
@@ -277,6 +350,14 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         }
       umma_commit(&bar_g1);
     }
+    // ---- while the tensor cores run group 1: the previous chunk's epilogue,
+    //      then this chunk's epilogue factors
+    if (it > 0) {
+      cluster_wait();  // "partial sent" of the previous chunk
+      epilogue(REV ? n + 1 : n - 1);
+    }
+    cluster_arrive();  // "sR free"
+    prefetch(sQ, sK, sG, sQD);
     if (!mbar_wait(&bar_g1, par)) atomicExch(&g_qk_status, 1);
     tc_fence_after();
     if (tid == 0 && it + 1 < nc) issue_dv(REV ? n - 1 : n + 1);  // do, v buffers are free
@@ -321,87 +402,33 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     }
     if (!mbar_wait(&bar_g2, par)) atomicExch(&g_qk_status, 1);
     tc_fence_after();
-    // ---- add the two d_v halves: rows of the peer go to the peer's buffer
+    // ---- partial sums of this chunk: the peer's rows into the peer's sR, mine into sOwn
     float a[64];
     if (warp < 4) {
       tmem_ld32(tmem + lane_off + kColAcc, a);
       tmem_ld32(tmem + lane_off + kColAcc + 32, a + 32);
       tmem_ld_wait();
-      if (rowt && !owned) {
-        const uint32_t dst = map_to_rank(
-            smem_u32(sR + ((it & 1) * 32 + (ii & 31)) * kC), peer);
+    }
+    cluster_wait();  // "sR free": the peer's epilogue has read its sR
+    if (rowt) {
+      if (owned) {
+        float4* dst = reinterpret_cast<float4*>(sOwn + (ii & 31) * kRS);
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+          dst[c] = make_float4(a[4 * c], a[4 * c + 1], a[4 * c + 2], a[4 * c + 3]);
+      } else {
+        const uint32_t dst = map_to_rank(smem_u32(sR + (ii & 31) * kRS), peer);
 #pragma unroll
         for (int c = 0; c < 16; ++c)
           st_cluster_v4(dst + c * 16, a[4 * c], a[4 * c + 1], a[4 * c + 2], a[4 * c + 3]);
       }
     }
-    cluster_sync();
-    // ---- sum of the two halves for the owned rows, in place in the receive buffer
-    float* sAcc = sR + (it & 1) * 32 * kC;
-    if (owned) {
-      float* rv = sAcc + (ii & 31) * kC;
-#pragma unroll
-      for (int t = 0; t < kC; ++t) rv[t] += a[t];
-    }
-    __syncthreads();
-    // ---- epilogue: 32 owned rows x 4 quarters of 16 tokens.  b_t of row ec is the
-    //      sum of log_alpha over the earlier quarters plus the running sum in this one.
-    if (tid < 128) {
-      float gl[16];
-      float gq = 0.f;
-#pragma unroll
-      for (int u = 0; u < 16; ++u) {
-        gl[u] = __bfloat162float(*tile_at(sG, 16 * eq + u, ec));
-        gq += gl[u];
-      }
-      sGq[eq * 32 + er] = gq;
-      asm volatile("bar.sync 1, 128;" ::: "memory");  // the 128 epilogue threads
-      float boff = 0.f;
-      for (int q2 = 0; q2 < eq; ++q2) boff += sGq[q2 * 32 + er];
-      const float* acc = sAcc + er * kC + 16 * eq;
-      const size_t base = (size_t)(chunk_row(n) + 16 * eq) * dk + i0 + ec;
-      if (!REV) {
-        float b = boff;
-#pragma unroll
-        for (int u = 0; u < 16; ++u) {
-          b += gl[u];
-          const float av = acc[u];
-          out[base + (size_t)u * dk] = __float2bfloat16_rn(av * __expf(b));
-          // the stored rounded Q~ times the raw accumulator (= q_eff dq)
-          qdq[base + (size_t)u * dk] = __bfloat162float(*tile_at(sQ, 16 * eq + u, ec)) * av;
-        }
-      } else {
-        float b = boff;
-        float term[16];
-#pragma unroll
-        for (int u = 0; u < 16; ++u) {
-          b += gl[u];
-          const float av = acc[u];
-          out[base + (size_t)u * dk] = __float2bfloat16_rn(av * __expf(-b));
-          // the stored rounded K~ times the raw accumulator (= k_eff dk)
-          term[u] = sQD[(16 * eq + u) * 32 + er] -
-                    __bfloat162float(*tile_at(sK, 16 * eq + u, ec)) * av;
-        }
-        float qsum = 0.f;
-#pragma unroll
-        for (int u = 0; u < 16; ++u) qsum += term[u];
-        sQS[eq * 32 + er] = qsum;
-        asm volatile("bar.sync 1, 128;" ::: "memory");
-        float carry_in = sRun[er];
-        for (int q2 = 3; q2 > eq; --q2) carry_in += sQS[q2 * 32 + er];
-        float runq = carry_in;
-#pragma unroll
-        for (int u = 15; u >= 0; --u) {
-          runq += term[u];
-          dg[base + (size_t)u * dk] = __float2bfloat16_rn(runq);
-        }
-        asm volatile("bar.sync 1, 128;" ::: "memory");
-        if (eq == 0) sRun[er] = runq;  // suffix through the whole chunk
-      }
-    }
+    cluster_arrive();  // "partial sent"
     tc_fence_before();
     __syncthreads();
   }
+  cluster_wait();  // "partial sent" of the last chunk
+  epilogue(REV ? 0 : nc - 1);
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, 256);
