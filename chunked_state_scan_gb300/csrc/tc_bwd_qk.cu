@@ -100,7 +100,9 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   float* sGq = reinterpret_cast<float*>(sm + kOffGq);
   float* sQS = reinterpret_cast<float*>(sm + kOffQS);
   float* sRun = reinterpret_cast<float*>(sm + kOffRun);
-  __shared__ uint64_t bar_x[2], bar_dv, bar_g1, bar_g2;
+  // bar_full: the peer's partial for my rows has landed in sR (complete_tx from
+  // the peer's st.async); bar_empty: the peer has read the partial I sent it.
+  __shared__ uint64_t bar_x[2], bar_dv, bar_g1, bar_g2, bar_full, bar_empty;
   __shared__ uint32_t tmem_base;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -123,6 +125,8 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     mbar_init(&bar_dv, 1);
     mbar_init(&bar_g1, 1);
     mbar_init(&bar_g2, 1);
+    mbar_init(&bar_full, 1);
+    mbar_init(&bar_empty, 1);
     fence_mbar_init();
     prefetch_tmap(&tmQ);
     prefetch_tmap(&tmK);
@@ -135,6 +139,7 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  cluster_sync();  // both CTAs' barriers exist before any remote arrive or st.async
   const uint32_t tmem = tmem_base;
   const uint32_t lane_off = (uint32_t)(lg * 32) << 16;
 
@@ -220,84 +225,108 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     return reinterpret_cast<__nv_bfloat16*>(base + sw128((uint32_t)t, (uint32_t)((c & 63) >> 3)) +
                                             (uint32_t)(c & 7) * 2u);
   };
-  // epilogue workers: owned row er (d_k row ec of the block) x 8 tokens 8 eg..8 eg+7
-  const int er = tid & 31, eg = tid >> 5;
+  // Warp roles within a chunk: thread 0 issues the TMA copies and the MMAs;
+  // warps 0-3 read the dA and partial-sum accumulators (the M = 64 layout puts
+  // rows in their lanes) and mask dA; all 8 warps run the state pass; warps 4-7
+  // run the previous chunk's epilogue and this chunk's epilogue prefetch while
+  // the tensor cores execute MMA group 1.
+  // Epilogue workers (warps 4-7): owned row er (d_k row ec of the block) x the
+  // 16 tokens 16 eq .. 16 eq + 15.
+  const int er = tid & 31, eq = (warp - 4) & 3;
   const int ec = 32 * (int)rank + er;
+  const bool epi = warp >= 4;
 
   if (REV && tid < 32) sRun[tid] = carry[((size_t)bh * P + p) * dk + i0 + 32 * (int)rank + tid];
   const uint32_t peer = rank ^ 1u;
+  const uint32_t peer_full = map_to_rank(smem_u32(&bar_full), peer);
+  const uint32_t peer_empty = map_to_rank(smem_u32(&bar_empty), peer);
+  if (tid == 128) mbar_expect_tx(&bar_full, 32 * kC * 4);  // phase 0: the first partial
 
   // Per-element factors of a chunk's epilogue, read from the chunk's tiles in its
   // own iteration and kept in registers until the epilogue runs in the next one
   // (so the tile buffers are free for the next prefetch): ef = e^{b_t} (forward)
   // or e^{-b_t} (reverse), xr = the stored rounded Q~ (forward) or K~ (reverse),
-  // qd = q.dq (reverse).  b_t sums log_alpha over the earlier 8-token groups of
-  // the chunk plus the running sum within this one.
-  float ef[8], xr[8], qd[8];
+  // qd = q.dq (reverse).  b_t sums log_alpha over the earlier 16-token quarters
+  // of the chunk plus the running sum within this one.
+  float ef[16], xr[16], qd[16];
+  auto epi_sync = []() { asm volatile("bar.sync 1, 128;" ::: "memory"); };
   auto prefetch = [&](const unsigned char* sQ, const unsigned char* sK,
                       const unsigned char* sG, const float* sQD) {
-    float gl[8];
+    float gl[16];
     float gs = 0.f;
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      gl[u] = __bfloat162float(*tile_at(const_cast<unsigned char*>(sG), 8 * eg + u, ec));
+    for (int u = 0; u < 16; ++u) {
+      gl[u] = __bfloat162float(*tile_at(const_cast<unsigned char*>(sG), 16 * eq + u, ec));
       gs += gl[u];
     }
-    sGq[eg * 32 + er] = gs;
-    __syncthreads();
+    sGq[eq * 32 + er] = gs;
+    epi_sync();
     float b = 0.f;
-    for (int g2 = 0; g2 < eg; ++g2) b += sGq[g2 * 32 + er];
+    for (int q2 = 0; q2 < eq; ++q2) b += sGq[q2 * 32 + er];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
+    for (int u = 0; u < 16; ++u) {
       b += gl[u];
       ef[u] = __expf(REV ? -b : b);
-      xr[u] = __bfloat162float(*tile_at(const_cast<unsigned char*>(REV ? sK : sQ), 8 * eg + u, ec));
-      if (REV) qd[u] = sQD[(8 * eg + u) * 32 + er];
+      xr[u] = __bfloat162float(*tile_at(const_cast<unsigned char*>(REV ? sK : sQ), 16 * eq + u, ec));
+      if (REV) qd[u] = sQD[(16 * eq + u) * 32 + er];
     }
   };
   // outputs of chunk n from the two partial sums (peer's + own)
   auto epilogue = [&](int n) {
-    const float4* rp = reinterpret_cast<const float4*>(sR + er * kRS + 8 * eg);
-    const float4* op = reinterpret_cast<const float4*>(sOwn + er * kRS + 8 * eg);
-    const float4 r0 = rp[0], r1 = rp[1], o0 = op[0], o1 = op[1];
-    const float acc[8] = {r0.x + o0.x, r0.y + o0.y, r0.z + o0.z, r0.w + o0.w,
-                          r1.x + o1.x, r1.y + o1.y, r1.z + o1.z, r1.w + o1.w};
-    const size_t base = (size_t)(chunk_row(n) + 8 * eg) * dk + i0 + ec;
+    const float4* rp = reinterpret_cast<const float4*>(sR + er * kRS + 16 * eq);
+    const float4* op = reinterpret_cast<const float4*>(sOwn + er * kRS + 16 * eq);
+    float acc[16];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const float4 r4 = rp[c], o4 = op[c];
+      acc[4 * c] = r4.x + o4.x;
+      acc[4 * c + 1] = r4.y + o4.y;
+      acc[4 * c + 2] = r4.z + o4.z;
+      acc[4 * c + 3] = r4.w + o4.w;
+    }
+    const size_t base = (size_t)(chunk_row(n) + 16 * eq) * dk + i0 + ec;
     if (!REV) {
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
+      for (int u = 0; u < 16; ++u) {
         out[base + (size_t)u * dk] = __float2bfloat16_rn(acc[u] * ef[u]);
         // the stored rounded Q~ times the raw accumulator (= q_eff dq)
         qdq[base + (size_t)u * dk] = xr[u] * acc[u];
       }
     } else {
-      float term[8];
+      float term[16];
       float s = 0.f;
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
+      for (int u = 0; u < 16; ++u) {
         out[base + (size_t)u * dk] = __float2bfloat16_rn(acc[u] * ef[u]);
         // the stored rounded K~ times the raw accumulator (= k_eff dk)
         term[u] = qd[u] - xr[u] * acc[u];
         s += term[u];
       }
-      sQS[eg * 32 + er] = s;
-      __syncthreads();
+      sQS[eq * 32 + er] = s;
+      epi_sync();
       float runq = sRun[er];
-      for (int g2 = 7; g2 > eg; --g2) runq += sQS[g2 * 32 + er];
+      for (int q2 = 3; q2 > eq; --q2) runq += sQS[q2 * 32 + er];
 #pragma unroll
-      for (int u = 7; u >= 0; --u) {
+      for (int u = 15; u >= 0; --u) {
         runq += term[u];
         dg[base + (size_t)u * dk] = __float2bfloat16_rn(runq);
       }
-      __syncthreads();
-      if (eg == 0) sRun[er] = runq;  // suffix through the whole chunk
+      epi_sync();
+      if (eq == 0) sRun[er] = runq;  // suffix through the whole chunk
+    }
+  };
+  // epilogue of chunk n = the it-th processed (warps 4-7): wait for the peer's
+  // partial, then release sR back to the peer and arm bar_full for the next one
+  auto finish = [&](int n, int it) {
+    if (!mbar_wait(&bar_full, (uint32_t)(it & 1))) atomicExch(&g_qk_status, 1);
+    epilogue(n);
+    epi_sync();  // every epilogue thread has read sR
+    if (tid == 128 && it + 1 < nc) {
+      mbar_arrive_remote(peer_empty);
+      mbar_expect_tx(&bar_full, 32 * kC * 4);
     }
   };
 
-  // Exchange of the partial sums with the peer CTA: two alternating phases of
-  // the cluster barrier per chunk -- "sR free" (arrived after the epilogue has
-  // read it, waited on before writing into the peer's sR) and "partial sent"
-  // (arrived after the writes, waited on before the epilogue).
   for (int it = 0; it < nc; ++it) {
     const int n = REV ? (nc - 1 - it) : it;
     const uint32_t par = (uint32_t)(it & 1);
@@ -350,14 +379,12 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         }
       umma_commit(&bar_g1);
     }
-    // ---- while the tensor cores run group 1: the previous chunk's epilogue,
-    //      then this chunk's epilogue factors
-    if (it > 0) {
-      cluster_wait();  // "partial sent" of the previous chunk
-      epilogue(REV ? n + 1 : n - 1);
+    // ---- warps 4-7, while the tensor cores run group 1: the previous chunk's
+    //      epilogue, then this chunk's epilogue factors
+    if (epi) {
+      if (it > 0) finish(REV ? n + 1 : n - 1, it - 1);
+      prefetch(sQ, sK, sG, sQD);
     }
-    cluster_arrive();  // "sR free"
-    prefetch(sQ, sK, sG, sQD);
     if (!mbar_wait(&bar_g1, par)) atomicExch(&g_qk_status, 1);
     tc_fence_after();
     if (tid == 0 && it + 1 < nc) issue_dv(REV ? n - 1 : n + 1);  // do, v buffers are free
@@ -382,7 +409,6 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         }
       }
     }
-    if (!REV) state_pass(sE);  // forward: post-scale and copy for the next chunk
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -400,37 +426,43 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       }
       umma_commit(&bar_g2);
     }
+    // forward: post-scale the state and copy it for the next chunk while group 2 runs
+    // (group 2 reads neither the state nor its copy)
+    if (!REV) state_pass(sE);
     if (!mbar_wait(&bar_g2, par)) atomicExch(&g_qk_status, 1);
     tc_fence_after();
-    // ---- partial sums of this chunk: the peer's rows into the peer's sR, mine into sOwn
-    float a[64];
+    // ---- partial sums of this chunk: the peer's rows into the peer's sR
+    //      (st.async, completing on the peer's bar_full), mine into sOwn
     if (warp < 4) {
+      float a[64];
       tmem_ld32(tmem + lane_off + kColAcc, a);
       tmem_ld32(tmem + lane_off + kColAcc + 32, a + 32);
       tmem_ld_wait();
-    }
-    cluster_wait();  // "sR free": the peer's epilogue has read its sR
-    if (rowt) {
-      if (owned) {
-        float4* dst = reinterpret_cast<float4*>(sOwn + (ii & 31) * kRS);
+      if (rowt) {
+        if (owned) {
+          float4* dst = reinterpret_cast<float4*>(sOwn + (ii & 31) * kRS);
 #pragma unroll
-        for (int c = 0; c < 16; ++c)
-          dst[c] = make_float4(a[4 * c], a[4 * c + 1], a[4 * c + 2], a[4 * c + 3]);
-      } else {
-        const uint32_t dst = map_to_rank(smem_u32(sR + (ii & 31) * kRS), peer);
+          for (int c = 0; c < 16; ++c)
+            dst[c] = make_float4(a[4 * c], a[4 * c + 1], a[4 * c + 2], a[4 * c + 3]);
+        } else {
+          // the peer has read the partial of the previous chunk
+          if (!mbar_wait(&bar_empty, par ^ 1u)) atomicExch(&g_qk_status, 1);
+          const uint32_t dst = map_to_rank(smem_u32(sR + (ii & 31) * kRS), peer);
 #pragma unroll
-        for (int c = 0; c < 16; ++c)
-          st_cluster_v4(dst + c * 16, a[4 * c], a[4 * c + 1], a[4 * c + 2], a[4 * c + 3]);
+          for (int c = 0; c < 16; ++c)
+            st_async_v4(dst + c * 16, a[4 * c], a[4 * c + 1], a[4 * c + 2], a[4 * c + 3],
+                        peer_full);
+        }
       }
     }
-    cluster_arrive();  // "partial sent"
+    fence_async_smem();  // forward: the state copy, read by the next group 1
     tc_fence_before();
     __syncthreads();
   }
-  cluster_wait();  // "partial sent" of the last chunk
-  epilogue(REV ? 0 : nc - 1);
+  if (epi) finish(REV ? 0 : nc - 1, nc - 1);
   tc_fence_before();
   __syncthreads();
+  cluster_sync();  // no st.async or remote arrive is still in flight to either CTA
   if (warp == 0) tmem_dealloc(tmem, 256);
 }
 

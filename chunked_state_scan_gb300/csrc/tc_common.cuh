@@ -262,3 +262,24 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
 }
 }  // namespace tc
 }  // namespace zeco
+
+namespace zeco {
+namespace tc {
+// 16-byte store into the shared memory of another CTA of the cluster (`addr`
+// from map_to_rank) that signals `remote_bar` (an mbarrier of that CTA, also
+// mapped) with complete_tx of 16 bytes; the issuing thread does not wait.
+__device__ __forceinline__ void st_async_v4(uint32_t addr, float a, float b, float c, float d,
+                                            uint32_t remote_bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+          addr),
+      "f"(a), "f"(b), "f"(c), "f"(d), "r"(remote_bar)
+      : "memory");
+}
+// Arrive (release, cluster scope) on an mbarrier of another CTA of the cluster.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t remote_bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar)
+               : "memory");
+}
+}  // namespace tc
+}  // namespace zeco
