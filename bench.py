@@ -63,10 +63,12 @@ def kernel_bytes_per_token(dk, dv, L, e=E, C=64):
         # dq, dk, dg (one launch, CUDA-core path): read q, k, v, g, do, S_in[p], D[p+1];
         # write dq, dk, dg
         "bwd_dqk": e * (3 * dk + 2 * dv) + e * 3 * dk + 2 * st,
-        # dq sweep: read Q~, K~, g, v, do, e^{b_last} and S_in[p]; write dq and q.dq (fp32)
-        "bwd_dq": e * (3 * dk + 2 * dv) + eb + e * dk + 4 * dk + st,
-        # dk sweep: read Q~, K~, g, v, do, e^{b_last}, q.dq and D[p+1]; write dk, dlog_alpha
-        "bwd_dk": e * (3 * dk + 2 * dv) + eb + 4 * dk + 2 * e * dk + st,
+        # intra-chunk score gradients: read do, v; write the masked dA (64 per token)
+        "dA": e * (2 * dv + C),
+        # dq sweep: read Q~, K~, g, v, do, dA, e^{b_last} and S_in[p]; write dq, q.dq (fp32)
+        "bwd_dq": e * (3 * dk + 2 * dv + C) + eb + e * dk + 4 * dk + st,
+        # dk sweep: read Q~, K~, g, v, do, dA, e^{b_last}, q.dq, D[p+1]; write dk, dlog_alpha
+        "bwd_dk": e * (3 * dk + 2 * dv + C) + eb + 4 * dk + 2 * e * dk + st,
     }
 
 
@@ -86,7 +88,7 @@ def zeco_operator_flops_per_token(dk, dv, C):
 
 def canonical_kernel(name):
     for key in ("chunk_state", "seg_scan_fwd", "decay", "fwd_out", "dstate_local",
-                "seg_scan_rev", "bwd_dv", "bwd_dqk", "bwd_dq", "bwd_dk"):
+                "seg_scan_rev", "bwd_dv", "dA", "bwd_dqk", "bwd_dq", "bwd_dk"):
         if key in name:
             return key
     return name

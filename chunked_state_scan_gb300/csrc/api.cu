@@ -71,7 +71,7 @@ WsPlan plan_ws(const Dims& d, int path, bool bwd) {
   w.bwd = zeco::bwd_ws_layout(d);
   const size_t base = bwd ? w.bwd.total : 0;
   w.uses_decay = path == ZECO_PATH_TC && zeco::tc_uses_decay(d);
-  w.decay = zeco::decay_layout(d, base);
+  w.decay = zeco::decay_layout(d, base, bwd && zeco::tc_uses_dA(d));
   w.total = w.uses_decay ? w.decay.total : base;
   return w;
 }

@@ -51,15 +51,20 @@ cudaError_t tc_fwd_out(const Dims& d, const void* Qt, const void* Kt, const void
                        const float* Eb, const float* S_in, void* o, cudaStream_t st);
 cudaError_t tc_bwd_dv(const Dims& d, const void* Qt, const void* Kt, const void* d_o,
                       const float* Eb, const float* D, void* dv, cudaStream_t st);
+// masked bf16 dA = do v^T of every chunk (tc_dA.cu)
+bool tc_dA_supported(const Dims& d);
+cudaError_t tc_dA(const Dims& d, const void* d_o, const void* v, void* P, cudaStream_t st);
 bool tc_bwd_qk_supported(const Dims& d);
 cudaError_t tc_bwd_qk(const Dims& d, const void* Qt, const void* Kt, const void* v,
-                      const void* g, const float* Eb, const float* S_in, const void* d_o,
-                      void* dq, void* dk, void* dg, float* D, float* carry, float* qdq,
-                      cudaStream_t st);
+                      const void* g, const float* Eb, const void* dA, const float* S_in,
+                      const void* d_o, void* dq, void* dk, void* dg, float* D, float* carry,
+                      float* qdq, cudaStream_t st);
 bool tc_supported(const Dims& d);
 // Whether the tensor-core path of this shape runs the decay pass (and so needs
 // decay_layout's buffers in its workspace).
 bool tc_uses_decay(const Dims& d);
+// Whether its backward also runs tc_dA (and so needs decay_layout's dA buffer).
+bool tc_uses_dA(const Dims& d);
 cudaError_t tc_forward(const Dims& d, const void* q, const void* k, const void* v,
                        const void* g, const float* S0, void* o, float* S_final, float* S_in,
                        float* gamma, const DecayLayout& dl, void* ws, cudaStream_t st);

@@ -10,6 +10,10 @@ bool tc_supported(const Dims& d) { return tc_state_supported(d); }
 
 bool tc_uses_decay(const Dims& d) { return tc_supported(d) && tc_fwd_supported(d); }
 
+bool tc_uses_dA(const Dims& d) {
+  return tc_uses_decay(d) && tc_bwd_qk_supported(d) && tc_dA_supported(d);
+}
+
 cudaError_t tc_forward(const Dims& d, const void* q, const void* k, const void* v,
                        const void* g, const float* S0, void* o, float* S_final, float* S_in,
                        float* gamma, const DecayLayout& dl, void* ws, cudaStream_t st) {
@@ -46,8 +50,12 @@ cudaError_t tc_backward(const Dims& d, const void* q, const void* k, const void*
   if (e != cudaSuccess) return e;
   e = tc_bwd_dv(d, Qt, Kt, d_o, Eb, D, dv, st);
   if (e != cudaSuccess) return e;
-  if (tc_bwd_qk_supported(d))
-    return tc_bwd_qk(d, Qt, Kt, v, g, Eb, S_in, d_o, dq, dk, dg, D, carry, qdq, st);
+  if (tc_uses_dA(d)) {
+    void* dA = w + dl.dA_off;
+    e = tc_dA(d, d_o, v, dA, st);
+    if (e != cudaSuccess) return e;
+    return tc_bwd_qk(d, Qt, Kt, v, g, Eb, dA, S_in, d_o, dq, dk, dg, D, carry, qdq, st);
+  }
   return simt_bwd_dqk_bf16(d, q, k, v, g, S_in, d_o, dq, dk, dg, D, carry, qdq, st);
 }
 

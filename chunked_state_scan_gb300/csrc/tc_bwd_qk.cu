@@ -34,8 +34,11 @@
 // identity's telescoping holds for the rounded model instead of breaking on
 // the rounding.
 //
-// TMEM columns: [0, 128) state (d_v group g of this CTA at 64 g) | [128, 192)
-// dA (M = 64 layout) | [192, 256) dq^T or dk^T (M = 64 layout, lane = d_k row).
+// The masked intra-chunk score gradient dA = do v^T comes precomputed in bf16
+// (tc_dA.cu); CTA rank 0 of the pair adds its term.
+//
+// TMEM columns: [0, 128) state (d_v group g of this CTA at 64 g) | [192, 256)
+// dq^T or dk^T (M = 64 layout, lane = d_k row).
 #include <cuda.h>
 
 #include "common.cuh"
@@ -57,7 +60,7 @@ constexpr int kKB = 64;    // d_k rows per CTA pair
 constexpr int kDV = 512;   // d_v
 constexpr int kDVH = 256;  // d_v columns per CTA
 constexpr int kThreads = 256;
-constexpr uint32_t kColDA = 128, kColAcc = 192;
+constexpr uint32_t kColAcc = 192;
 
 // shared memory (bytes, 1024-aligned regions)
 constexpr int kOffDO = 0;                        // do tile [64 t][256 j] (4 blocks of 64 j)
@@ -68,7 +71,7 @@ constexpr int kXTile = kC * kKB * 2;             // one [64 t][64 i] bf16 tile
 // Q~, K~, log_alpha tiles + q.dq rows [64 t][32 i] fp32 + e^{b_last} [64] fp32
 constexpr int kXBuf = 3 * kXTile + 32 * kC * 4 + 1024;
 constexpr int kOffX = kOffLo + kDVH * kKB * 2;   // 2 buffers of kXBuf (chunk parity)
-constexpr int kOffP = kOffX + 2 * kXBuf;         // masked dA partial [64 t][64 s] bf16
+constexpr int kOffP = kOffX + 2 * kXBuf;         // masked dA [64 t][64 s] bf16 (with do, v)
 constexpr int kRS = kC + 4;                      // row stride of the partial sums (floats)
 constexpr int kOffR = kOffP + kC * kC * 2;       // peer's partial for my rows [32][kRS] fp32
 constexpr int kOffOwn = kOffR + 32 * kRS * 4;    // my own partial for my rows [32][kRS] fp32
@@ -84,7 +87,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                  const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmV,
                  const __grid_constant__ CUtensorMap tmDO, const __grid_constant__ CUtensorMap tmQD,
-                 const float* __restrict__ Eb, const float* __restrict__ S_src,
+                 const __grid_constant__ CUtensorMap tmP, const float* __restrict__ Eb,
+                 const float* __restrict__ S_src,
                  const float* __restrict__ carry, __nv_bfloat16* __restrict__ out,
                  __nv_bfloat16* __restrict__ dg, float* __restrict__ qdq, int64_t T, int dk,
                  int P, int64_t L) {
@@ -102,7 +106,7 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   float* sRun = reinterpret_cast<float*>(sm + kOffRun);
   // bar_full: the peer's partial for my rows has landed in sR (complete_tx from
   // the peer's st.async); bar_empty: the peer has read the partial I sent it.
-  __shared__ uint64_t bar_x[2], bar_dv, bar_g1, bar_g2, bar_full, bar_empty;
+  __shared__ uint64_t bar_x[2], bar_dv, bar_g1, bar_full, bar_empty;
   __shared__ uint32_t tmem_base;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -124,7 +128,6 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     mbar_init(&bar_x[1], 1);
     mbar_init(&bar_dv, 1);
     mbar_init(&bar_g1, 1);
-    mbar_init(&bar_g2, 1);
     mbar_init(&bar_full, 1);
     mbar_init(&bar_empty, 1);
     fence_mbar_init();
@@ -133,6 +136,7 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     prefetch_tmap(&tmG);
     prefetch_tmap(&tmV);
     prefetch_tmap(&tmDO);
+    prefetch_tmap(&tmP);
     if (REV) prefetch_tmap(&tmQD);
   }
   if (warp == 0) tmem_alloc(&tmem_base, 256);
@@ -157,13 +161,15 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
               &bar_x[buf]);
     if (REV) tma_load_2d(xb + 3 * kXTile, &tmQD, i0 + 32 * (int)rank, r, &bar_x[buf]);
   };
+  // do, v halves and the masked dA of chunk n
   auto issue_dv = [&](int n) {
     const int32_t r = chunk_row(n);
-    mbar_expect_tx(&bar_dv, 2 * kC * kDVH * 2);
+    mbar_expect_tx(&bar_dv, 2 * kC * kDVH * 2 + kC * kC * 2);
     for (int b = 0; b < kDVH / 64; ++b) {
       tma_load_2d(sDO + b * 8192, &tmDO, jb + b * 64, r, &bar_dv);
       tma_load_2d(sV + b * 8192, &tmV, jb + b * 64, r, &bar_dv);
     }
+    tma_load_2d(sP, &tmP, 0, r, &bar_dv);
   };
   if (tid == 0) {
     issue_x(REV ? nc - 1 : 0, 0);
@@ -350,21 +356,28 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       const uint32_t o0 = smem_u32(sDO), v0 = smem_u32(sV), h0 = smem_u32(sHi),
                      l0 = smem_u32(sLo);
       const uint32_t x0 = smem_u32(REV ? sQ : sK);
-      constexpr uint32_t id64 = idesc_bf16(64, 64, false, false);  // dA
       constexpr uint32_t idT = idesc_bf16(64, 64, true, false);    // copy (x) do or v
 #pragma unroll 4
       for (int m = 0; m < kDVH / 16; ++m) {  // K = this CTA's d_v half, 16 per step
         const uint32_t koff = (uint32_t)((m >> 2) * 8192 + (m & 3) * 32);
-        const uint64_t od = sdesc_sw128(o0 + koff, 16, 1024);
-        const uint64_t vd = sdesc_sw128(v0 + koff, 16, 1024);
+        const uint64_t yd = sdesc_sw128((REV ? v0 : o0) + koff, 16, 1024);
         const uint64_t hd = sdesc_sw128(h0 + m * 2048, 8192, 1024);
         const uint64_t ld = sdesc_sw128(l0 + m * 2048, 8192, 1024);
-        const uint64_t yd = REV ? vd : od;
-        // dA (partial over this half) = do v^T      (M = 64 t, N = 64 s)
-        umma_bf16(tmem + kColDA, od, vd, id64, m ? 1u : 0u);
         // forward: dq^T = S do^T     reverse: dk^T = (e^{b_last} dS) v^T   (M = 64 i, N = 64)
         umma_bf16(tmem + kColAcc, hd, yd, idT, m ? 1u : 0u);
         umma_bf16(tmem + kColAcc, ld, yd, idT, 1u);
+      }
+      // rank 0: forward dq^T += K~^T dA^T ; reverse dk^T += Q~^T dA   (M = 64 i, N = 64, K = 64)
+      if (rank == 0) {
+        const uint32_t p0 = smem_u32(sP);
+        constexpr uint32_t id2 = idesc_bf16(64, 64, true, REV);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t xd = sdesc_sw128(x0 + kk * 2048, 8192, 1024);
+          const uint64_t pd = REV ? sdesc_sw128(p0 + kk * 2048, 8192, 1024)
+                                  : sdesc_sw128(p0 + kk * 32, 16, 1024);
+          umma_bf16(tmem + kColAcc, xd, pd, id2, 1u);
+        }
       }
       // forward: S^T_g += v_g^T K~    reverse: dS^T_g += do_g^T Q~   (M = 128 j, N = 64 i, K = 64)
       constexpr uint32_t idS = idesc_bf16(128, 64, true, true);
@@ -387,50 +400,8 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     }
     if (!mbar_wait(&bar_g1, par)) atomicExch(&g_qk_status, 1);
     tc_fence_after();
-    if (tid == 0 && it + 1 < nc) issue_dv(REV ? n - 1 : n + 1);  // do, v buffers are free
-    // ---- mask the dA partial -> P [t][s]
-    if (warp < 4) {
-      float a[64];
-      tmem_ld32(tmem + lane_off + kColDA, a);
-      tmem_ld32(tmem + lane_off + kColDA + 32, a + 32);
-      tmem_ld_wait();
-      if (lane < 16) {
-        const int t = warp * 16 + lane;
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          uint32_t w4[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int s0 = c * 8 + 2 * u;
-            w4[u] = pack_bf16(s0 <= t ? a[s0] : 0.f, s0 + 1 <= t ? a[s0 + 1] : 0.f);
-          }
-          *reinterpret_cast<uint4*>(sP + sw128((uint32_t)t, (uint32_t)c)) =
-              make_uint4(w4[0], w4[1], w4[2], w4[3]);
-        }
-      }
-    }
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    // ---- MMA group 2: forward dq^T += K~^T P^T ; reverse dk^T += Q~^T P
-    if (tid == 0) {
-      tc_fence_after();
-      const uint32_t x0 = smem_u32(REV ? sQ : sK), p0 = smem_u32(sP);
-      constexpr uint32_t id2 = idesc_bf16(64, 64, true, REV);
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        const uint64_t xd = sdesc_sw128(x0 + kk * 2048, 8192, 1024);
-        const uint64_t pd = REV ? sdesc_sw128(p0 + kk * 2048, 8192, 1024)
-                                : sdesc_sw128(p0 + kk * 32, 16, 1024);
-        umma_bf16(tmem + kColAcc, xd, pd, id2, 1u);
-      }
-      umma_commit(&bar_g2);
-    }
-    // forward: post-scale the state and copy it for the next chunk while group 2 runs
-    // (group 2 reads neither the state nor its copy)
-    if (!REV) state_pass(sE);
-    if (!mbar_wait(&bar_g2, par)) atomicExch(&g_qk_status, 1);
-    tc_fence_after();
+    if (tid == 0 && it + 1 < nc) issue_dv(REV ? n - 1 : n + 1);  // do, v, dA buffers are free
+    if (!REV) state_pass(sE);  // forward: post-scale and copy for the next chunk
     // ---- partial sums of this chunk: the peer's rows into the peer's sR
     //      (st.async, completing on the peer's bar_full), mine into sOwn
     if (warp < 4) {
@@ -469,8 +440,9 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
 template <bool REV>
 cudaError_t launch_qk(const Dims& d, const CUtensorMap& tq, const CUtensorMap& tk,
                       const CUtensorMap& tg, const CUtensorMap& tv, const CUtensorMap& tdo,
-                      const CUtensorMap& tqd, const float* Eb, const float* S_src,
-                      const float* carry, void* out, void* dg, float* qdq, cudaStream_t st) {
+                      const CUtensorMap& tqd, const CUtensorMap& tp, const float* Eb,
+                      const float* S_src, const float* carry, void* out, void* dg, float* qdq,
+                      cudaStream_t st) {
   auto kern = tc_bwd_qk_kernel<REV>;
   const int smem = kSmem + 1024;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -487,7 +459,8 @@ cudaError_t launch_qk(const Dims& d, const CUtensorMap& tq, const CUtensorMap& t
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, tq, tk, tg, tv, tdo, tqd, Eb, S_src, carry, (__nv_bfloat16*)out,
+  return cudaLaunchKernelEx(&cfg, kern, tq, tk, tg, tv, tdo, tqd, tp, Eb, S_src, carry,
+                            (__nv_bfloat16*)out,
                             (__nv_bfloat16*)dg, qdq, d.T, (int)d.dk, d.P, d.L);
 }
 
@@ -498,20 +471,21 @@ bool tc_bwd_qk_supported(const Dims& d) {
 }
 
 cudaError_t tc_bwd_qk(const Dims& d, const void* Qt, const void* Kt, const void* v,
-                      const void* g, const float* Eb, const float* S_in, const void* d_o,
-                      void* dq, void* dk, void* dg, float* D, float* carry, float* qdq,
-                      cudaStream_t st) {
-  CUtensorMap tq, tk, tg, tv, tdo, tqd;
+                      const void* g, const float* Eb, const void* dA, const float* S_in,
+                      const void* d_o, void* dq, void* dk, void* dg, float* D, float* carry,
+                      float* qdq, cudaStream_t st) {
+  CUtensorMap tq, tk, tg, tv, tdo, tqd, tp;
   const uint64_t rows = (uint64_t)(d.B * d.H * d.T);
   if (!make_tmap_bf16(&tq, Qt, rows, d.dk, kC) || !make_tmap_bf16(&tk, Kt, rows, d.dk, kC) ||
       !make_tmap_bf16(&tg, g, rows, d.dk, kC) || !make_tmap_bf16(&tv, v, rows, d.dv, kC) ||
-      !make_tmap_bf16(&tdo, d_o, rows, d.dv, kC) ||
+      !make_tmap_bf16(&tdo, d_o, rows, d.dv, kC) || !make_tmap_bf16(&tp, dA, rows, kC, kC) ||
       !make_tmap_f32_plain(&tqd, qdq, rows, d.dk, 32, kC))
     return cudaErrorInvalidValue;
-  cudaError_t e = launch_qk<false>(d, tq, tk, tg, tv, tdo, tqd, Eb, S_in, carry, dq, dg, qdq, st);
+  cudaError_t e =
+      launch_qk<false>(d, tq, tk, tg, tv, tdo, tqd, tp, Eb, S_in, carry, dq, dg, qdq, st);
   prof_mark("tc_bwd_dq", st);
   if (e != cudaSuccess) return e;
-  e = launch_qk<true>(d, tq, tk, tg, tv, tdo, tqd, Eb, D, carry, dk, dg, qdq, st);
+  e = launch_qk<true>(d, tq, tk, tg, tv, tdo, tqd, tp, Eb, D, carry, dk, dg, qdq, st);
   prof_mark("tc_bwd_dk", st);
   return e;
 }

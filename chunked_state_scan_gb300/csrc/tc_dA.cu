@@ -1,0 +1,172 @@
+// tc_dA.cu -- gradient of the intra-chunk scores, dA = do v^T masked to s <= t,
+// for every chunk of C = 64 tokens, in bf16 ([B,H,T,64]: row t of a chunk holds
+// its 64 scores over s).  It does not depend on the state, so it is computed
+// once per chunk here and read by both dq/dk sweeps (tc_bwd_qk.cu), which use
+// dq~ += dA K~ and dk~ += dA^T Q~ (chunkwise backward of the diagonal
+// attention: Pith review of ZeCO, referee major comment 3 on Algorithm 1).
+//
+// A persistent kernel, one CTA per SM, bound by reading do and v once from HBM.
+// Warp 4 streams do/v tiles of 64 tokens x 128 d_v columns through a 4-stage
+// ring (TMA, 128B swizzle); warp 5 issues the tcgen05 MMAs (M = 64 t, N = 64 s,
+// K = d_v) into one of two TMEM accumulators; warps 0-3 read a finished
+// accumulator (the M = 64 layout puts row t in lane 32 (t / 16) + t % 16),
+// mask, round and store it while the next chunk accumulates.
+#include <cuda.h>
+
+#include "common.cuh"
+#include "launch.h"
+#include "tc_common.cuh"
+
+namespace zeco {
+bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                    uint32_t box_rows);
+
+namespace {
+
+using namespace tc;
+
+constexpr int kC = 64;
+constexpr int kQ = 128;                     // d_v columns per stage
+constexpr int kStages = 4;
+constexpr int kHalf = kC * kQ * 2;          // do or v part of a stage (16 KB)
+constexpr int kStageBytes = 2 * kHalf;
+constexpr int kThreads = 192;
+
+__device__ int g_dA_status = 0;
+
+__global__ void __launch_bounds__(kThreads, 1)
+tc_dA_kernel(const __grid_constant__ CUtensorMap tmDO, const __grid_constant__ CUtensorMap tmV,
+             __nv_bfloat16* __restrict__ P, int64_t nchunks, int dv) {
+  extern __shared__ __align__(1024) unsigned char smraw[];
+  unsigned char* sm = (unsigned char*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
+  __shared__ uint64_t full[kStages], empty[kStages], accfull[2], accempty[2];
+  __shared__ uint32_t tmem_base;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nq = dv / kQ;
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&accfull[b], 1);
+      mbar_init(&accempty[b], 128);
+    }
+    fence_mbar_init();
+    prefetch_tmap(&tmDO);
+    prefetch_tmap(&tmV);
+  }
+  if (warp == 0) tmem_alloc(&tmem_base, 128);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base;
+
+  if (warp == 4) {
+    // ---- producer: do and v tiles of every (chunk, d_v quarter) this CTA owns
+    if (lane == 0) {
+      int64_t gi = 0;
+      for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x) {
+        const int32_t r = (int32_t)(c * kC);
+        for (int q = 0; q < nq; ++q, ++gi) {
+          const int s = (int)(gi % kStages);
+          const uint32_t ph = (uint32_t)((gi / kStages) & 1);
+          if (!mbar_wait(&empty[s], ph ^ 1u)) atomicExch(&g_dA_status, 1);
+          unsigned char* st = sm + s * kStageBytes;
+          mbar_expect_tx(&full[s], kStageBytes);
+          for (int b = 0; b < kQ / 64; ++b) {
+            tma_load_2d(st + b * 8192, &tmDO, q * kQ + b * 64, r, &full[s]);
+            tma_load_2d(st + kHalf + b * 8192, &tmV, q * kQ + b * 64, r, &full[s]);
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 5) {
+    // ---- MMA issuer: dA = do v^T, accumulated over the d_v quarters
+    if (lane == 0) {
+      constexpr uint32_t id = idesc_bf16(64, 64, false, false);
+      int64_t gi = 0;
+      int k = 0;
+      for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x, ++k) {
+        const int b = k & 1;
+        if (!mbar_wait(&accempty[b], (uint32_t)(((k >> 1) & 1) ^ 1))) atomicExch(&g_dA_status, 1);
+        tc_fence_after();
+        for (int q = 0; q < nq; ++q, ++gi) {
+          const int s = (int)(gi % kStages);
+          if (!mbar_wait(&full[s], (uint32_t)((gi / kStages) & 1))) atomicExch(&g_dA_status, 1);
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(sm + s * kStageBytes), b0 = a0 + kHalf;
+#pragma unroll
+          for (int m = 0; m < kQ / 16; ++m) {
+            const uint32_t koff = (uint32_t)((m >> 2) * 8192 + (m & 3) * 32);
+            umma_bf16(tmem + b * 64, sdesc_sw128(a0 + koff, 16, 1024),
+                      sdesc_sw128(b0 + koff, 16, 1024), id, (q | m) ? 1u : 0u);
+          }
+          umma_commit(&empty[s]);
+        }
+        umma_commit(&accfull[b]);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ---- epilogue (warps 0-3): mask s <= t, round, store row t
+    int k = 0;
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x, ++k) {
+      const int b = k & 1;
+      if (!mbar_wait(&accfull[b], (uint32_t)((k >> 1) & 1))) atomicExch(&g_dA_status, 1);
+      tc_fence_after();
+      float a[64];
+      tmem_ld32(tmem + lane_off + b * 64, a);
+      tmem_ld32(tmem + lane_off + b * 64 + 32, a + 32);
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(&accempty[b]);
+      if (lane < 16) {
+        const int t = warp * 16 + lane;
+        uint4* dst = reinterpret_cast<uint4*>(P + (size_t)(c * kC + t) * kC);
+#pragma unroll
+        for (int c8 = 0; c8 < 8; ++c8) {
+          uint32_t w4[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int s0 = c8 * 8 + 2 * u;
+            w4[u] = pack_bf16(s0 <= t ? a[s0] : 0.f, s0 + 1 <= t ? a[s0 + 1] : 0.f);
+          }
+          dst[c8] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, 128);
+}
+
+}  // namespace
+
+bool tc_dA_supported(const Dims& d) { return d.bf16 && d.C == kC && d.dv % kQ == 0; }
+
+cudaError_t tc_dA(const Dims& d, const void* d_o, const void* v, void* P, cudaStream_t st) {
+  CUtensorMap tdo, tv;
+  const uint64_t rows = (uint64_t)(d.B * d.H * d.T);
+  if (!make_tmap_bf16(&tdo, d_o, rows, d.dv, kC) || !make_tmap_bf16(&tv, v, rows, d.dv, kC))
+    return cudaErrorInvalidValue;
+  const int smem = kStages * kStageBytes + 1024;
+  cudaError_t e = cudaFuncSetAttribute(tc_dA_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       smem);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return e;
+  const int64_t nchunks = (int64_t)rows / kC;
+  const unsigned grid = (unsigned)(nchunks < sms ? nchunks : sms);
+  tc_dA_kernel<<<grid, kThreads, smem, st>>>(tdo, tv, (__nv_bfloat16*)P, nchunks, (int)d.dv);
+  prof_mark("tc_dA", st);
+  return cudaGetLastError();
+}
+
+}  // namespace zeco

@@ -50,7 +50,9 @@ def test_sizes_follow_the_layout(lib):
     qdq = 4 * (1 << 20) * 256 * 4
     # tensor-core path: Q~ and K~ (bf16) and e^{b_last} per 64-token chunk (fp32)
     decay = 2 * 4 * (1 << 20) * 256 * 2 + 4 * (1 << 20) // 64 * 256 * 4
-    assert z.workspace_bytes(s, True) == state + gam + qdq + decay
+    # backward only: the masked intra-chunk score gradients [B,H,T,64] bf16
+    dA = 4 * (1 << 20) * 64 * 2
+    assert z.workspace_bytes(s, True) == state + gam + qdq + decay + dA
     assert z.workspace_bytes(s, False) == decay
     # the SIMT path keeps no decay-weighted operands
     simt = _shape(path="simt", dtype="f32", dk=64, dv=64)
