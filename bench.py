@@ -53,13 +53,15 @@ def kernel_bytes_per_token(dk, dv, L, e=E, C=64):
         "seg_scan_fwd": 2 * st,
         # decay pass: read q, k, g; write Q~, K~ and e^{b_last}
         "decay": e * 5 * dk + eb,
-        # pass 2: read Q~, K~, v, e^{b_last} and S_in[p]; write o
-        "fwd_out": e * (2 * dk + 2 * dv) + eb + st,
+        # intra-chunk scores: read Q~, K~; write the masked A (64 per token)
+        "A": e * (2 * dk + C),
+        # pass 2: read Q~, K~, A, v, e^{b_last} and S_in[p]; write o
+        "fwd_out": e * (2 * dk + 2 * dv + C) + eb + st,
         # bwd pre-pass: read q, do, g; write one adjoint state per segment
         "dstate_local": e * (2 * dk + dv) + st,
         "seg_scan_rev": 3 * st,
-        # dv: read Q~, K~, do, e^{b_last} and D[p+1]; write dv
-        "bwd_dv": e * (2 * dk + 2 * dv) + eb + st,
+        # dv: read Q~, K~, A, do, e^{b_last} and D[p+1]; write dv
+        "bwd_dv": e * (2 * dk + 2 * dv + C) + eb + st,
         # dq, dk, dg (one launch, CUDA-core path): read q, k, v, g, do, S_in[p], D[p+1];
         # write dq, dk, dg
         "bwd_dqk": e * (3 * dk + 2 * dv) + e * 3 * dk + 2 * st,
@@ -87,6 +89,8 @@ def zeco_operator_flops_per_token(dk, dv, C):
 
 
 def canonical_kernel(name):
+    if name == "tc_A":
+        return "A"
     for key in ("chunk_state", "seg_scan_fwd", "decay", "fwd_out", "dstate_local",
                 "seg_scan_rev", "bwd_dv", "dA", "bwd_dqk", "bwd_dq", "bwd_dk"):
         if key in name:

@@ -27,21 +27,23 @@ struct BwdWsLayout {
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Decay-weighted operands of the tensor-core sweeps (tc_decay.cu): Q~, K~
-// [B,H,T,dk] bf16 and e^{b_last} of every chunk [B,H,T/64,dk] fp32; with
-// `with_dA` (backward) also the masked intra-chunk score gradients
-// [B,H,T,64] bf16 (tc_dA.cu).
+// Operands of the tensor-core sweeps computed once per call: Q~, K~
+// [B,H,T,dk] bf16 and e^{b_last} of every chunk [B,H,T/64,dk] fp32
+// (tc_decay.cu), the masked intra-chunk scores A [B,H,T,64] bf16 and, with
+// `with_dA` (backward), their gradient dA [B,H,T,64] bf16 (tc_scores.cu).
 struct DecayLayout {
-  size_t Qt_off, Kt_off, Eb_off, dA_off, total;
+  size_t Qt_off, Kt_off, Eb_off, A_off, dA_off, total;
 };
 inline DecayLayout decay_layout(const Dims& d, size_t base, bool with_dA) {
   DecayLayout l;
   const size_t n = (size_t)d.B * d.H * d.T * d.dk;
+  const size_t np = (size_t)d.B * d.H * d.T * 64 * 2;
   l.Qt_off = align_up(base, 256);
   l.Kt_off = align_up(l.Qt_off + n * 2, 256);
   l.Eb_off = align_up(l.Kt_off + n * 2, 256);
-  l.dA_off = align_up(l.Eb_off + n / 64 * sizeof(float), 256);
-  l.total = with_dA ? align_up(l.dA_off + (size_t)d.B * d.H * d.T * 64 * 2, 256) : l.dA_off;
+  l.A_off = align_up(l.Eb_off + n / 64 * sizeof(float), 256);
+  l.dA_off = align_up(l.A_off + np, 256);
+  l.total = with_dA ? align_up(l.dA_off + np, 256) : l.dA_off;
   return l;
 }
 

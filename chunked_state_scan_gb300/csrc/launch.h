@@ -48,10 +48,14 @@ bool tc_fwd_supported(const Dims& d);
 cudaError_t tc_decay(const Dims& d, const void* q, const void* k, const void* g, void* Qt,
                      void* Kt, float* Eb, cudaStream_t st);
 cudaError_t tc_fwd_out(const Dims& d, const void* Qt, const void* Kt, const void* v,
-                       const float* Eb, const float* S_in, void* o, cudaStream_t st);
+                       const void* A, const float* Eb, const float* S_in, void* o,
+                       cudaStream_t st);
 cudaError_t tc_bwd_dv(const Dims& d, const void* Qt, const void* Kt, const void* d_o,
-                      const float* Eb, const float* D, void* dv, cudaStream_t st);
-// masked bf16 dA = do v^T of every chunk (tc_dA.cu)
+                      const void* A, const float* Eb, const float* D, void* dv,
+                      cudaStream_t st);
+// masked bf16 A = Q~ K~^T and dA = do v^T of every chunk (tc_scores.cu)
+bool tc_A_supported(const Dims& d);
+cudaError_t tc_A(const Dims& d, const void* Qt, const void* Kt, void* P, cudaStream_t st);
 bool tc_dA_supported(const Dims& d);
 cudaError_t tc_dA(const Dims& d, const void* d_o, const void* v, void* P, cudaStream_t st);
 bool tc_bwd_qk_supported(const Dims& d);

@@ -26,9 +26,12 @@ cudaError_t tc_forward(const Dims& d, const void* q, const void* k, const void* 
   void* Qt = w + dl.Qt_off;
   void* Kt = w + dl.Kt_off;
   float* Eb = (float*)(w + dl.Eb_off);
+  void* A = w + dl.A_off;
   e = tc_decay(d, q, k, g, Qt, Kt, Eb, st);
   if (e != cudaSuccess) return e;
-  return tc_fwd_out(d, Qt, Kt, v, Eb, S_in, o, st);
+  e = tc_A(d, Qt, Kt, A, st);
+  if (e != cudaSuccess) return e;
+  return tc_fwd_out(d, Qt, Kt, v, A, Eb, S_in, o, st);
 }
 
 cudaError_t tc_backward(const Dims& d, const void* q, const void* k, const void* v,
@@ -46,9 +49,12 @@ cudaError_t tc_backward(const Dims& d, const void* q, const void* k, const void*
   void* Qt = w + dl.Qt_off;
   void* Kt = w + dl.Kt_off;
   float* Eb = (float*)(w + dl.Eb_off);
+  void* A = w + dl.A_off;
   e = tc_decay(d, q, k, g, Qt, Kt, Eb, st);
   if (e != cudaSuccess) return e;
-  e = tc_bwd_dv(d, Qt, Kt, d_o, Eb, D, dv, st);
+  e = tc_A(d, Qt, Kt, A, st);
+  if (e != cudaSuccess) return e;
+  e = tc_bwd_dv(d, Qt, Kt, d_o, A, Eb, D, dv, st);
   if (e != cudaSuccess) return e;
   if (tc_uses_dA(d)) {
     void* dA = w + dl.dA_off;

@@ -35,7 +35,7 @@
 // the rounding.
 //
 // The masked intra-chunk score gradient dA = do v^T comes precomputed in bf16
-// (tc_dA.cu); CTA rank 0 of the pair adds its term.
+// (tc_scores.cu); CTA rank 0 of the pair adds its term.
 //
 // TMEM columns: [0, 128) state (d_v group g of this CTA at 64 g) | [192, 256)
 // dq^T or dk^T (M = 64 layout, lane = d_k row).

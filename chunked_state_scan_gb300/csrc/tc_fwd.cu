@@ -17,8 +17,11 @@
 // One CTA owns (b, h, segment, 128 d_v columns) and keeps S^T (lanes = d_v
 // column j, TMEM columns = d_k row i) in fp32 in tensor memory, plus a bf16
 // copy of S^T that is the A operand (read from TMEM) of o^T = S^T Q~^T.
-// Q~, K~ and e^{b_last} come from the decay pass (tc_decay.cu) and arrive by
-// TMA, one chunk ahead, with no per-element work in the kernel.
+// Q~, K~, e^{b_last} (tc_decay.cu) and the masked scores A (tc_scores.cu)
+// arrive by TMA one chunk ahead, so a chunk is one group of MMAs plus the
+// state pass; the output accumulator is double-buffered so that warps 0-7
+// write chunk n-1 while the tensor cores run chunk n.  Thread 256 issues the
+// MMAs and thread 288 the copies, away from the epilogue warps.
 //
 // The same kernel, run backwards over the chunks (BWD = true), computes dv
 // from the adjoint state dS of the segment end (D[p+1], from the reverse
@@ -31,8 +34,8 @@
 //
 // with q/k roles swapped on the output side and do in place of v.
 //
-// TMEM columns: [0, DK) S^T fp32 | [256, 256 + DK/2) S^T bf16 | [384, 448) A
-// (M = 64 layout) | [448, 512) o^T (dv^T when BWD).
+// TMEM columns: [0, DK) S^T fp32 | [256, 256 + DK/2) S^T bf16 | [384, 448) and
+// [448, 512) o^T (dv^T when BWD), chunk parity.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -50,34 +53,34 @@ using namespace tc;
 constexpr int kC = 64;        // chunk length
 constexpr int kNV = 128;      // d_v columns per CTA
 constexpr int kThreads = 512;  // 16 warps
-constexpr uint32_t kColS16 = 256, kColA = 384, kColO = 448;
+constexpr uint32_t kColS16 = 256, kColO = 384;
+constexpr int kMmaTid = 256, kTmaTid = 288;
 
 __device__ int g_fwd_status = 0;
 
 template <int DK>
 struct FwdSmem {
-  static constexpr int kTile = DK * kC * 2;                   // Q~ / K~ tile bytes
-  static constexpr int kXBuf = (2 * kTile + DK * 4 + 1023) / 1024 * 1024;  // Q~, K~, e^{b_last}
-  static constexpr int kX = 0;                                // 2 buffers (chunk parity)
+  static constexpr int kTile = DK * kC * 2;  // Q~ / K~ tile bytes
+  static constexpr int kP = 2 * kTile;       // masked scores [64 t][64 s] bf16
+  static constexpr int kE = kP + kC * kC * 2;  // e^{b_last} [DK] fp32
+  static constexpr int kXBuf = (kE + DK * 4 + 1023) / 1024 * 1024;
+  static constexpr int kX = 0;               // 2 buffers (chunk parity)
   static constexpr int kV = 2 * kXBuf;
-  static constexpr int kP = kV + kNV * kC * 2;
-  static constexpr int kBytes = kP + kC * kC * 2;
+  static constexpr int kBytes = kV + kNV * kC * 2;
 };
 
 template <int DK, bool BWD>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                const __grid_constant__ CUtensorMap tmV, const float* __restrict__ Eb,
-                const float* __restrict__ S_src, __nv_bfloat16* __restrict__ o, int64_t T, int dv,
-                int P, int64_t L) {
+                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmP,
+                const float* __restrict__ Eb, const float* __restrict__ S_src,
+                __nv_bfloat16* __restrict__ o, int64_t T, int dv, int P, int64_t L) {
   using SM = FwdSmem<DK>;
   extern __shared__ __align__(1024) unsigned char smraw[];
   unsigned char* sm = (unsigned char*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
   unsigned char* sV = sm + SM::kV;
-  unsigned char* sP = sm + SM::kP;
-  __shared__ uint64_t bar_qkg[2], bar_v, bar_g1, bar_g2;
+  __shared__ uint64_t bar_x[2], bar_v, bar_g;
   __shared__ uint32_t tmem_base;
-  __shared__ int abort_flag;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int lg = warp & 3;       // TMEM lane group of this warp
@@ -90,16 +93,17 @@ tc_sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   const int nc = (int)(L / kC);
 
   if (tid == 0) {
-    mbar_init(&bar_qkg[0], 1);
-    mbar_init(&bar_qkg[1], 1);
+    mbar_init(&bar_x[0], 1);
+    mbar_init(&bar_x[1], 1);
     mbar_init(&bar_v, 1);
-    mbar_init(&bar_g1, 1);
-    mbar_init(&bar_g2, 1);
-    abort_flag = 0;
+    mbar_init(&bar_g, 1);
     fence_mbar_init();
+  }
+  if (tid == kTmaTid) {
     prefetch_tmap(&tmQ);
     prefetch_tmap(&tmK);
     prefetch_tmap(&tmV);
+    prefetch_tmap(&tmP);
   }
   if (warp == 0) tmem_alloc(&tmem_base, 512);
   tc_fence_before();
@@ -108,24 +112,25 @@ tc_sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   const uint32_t tmem = tmem_base;
   const uint32_t lane_off = (uint32_t)(lg * 32) << 16;
 
-  // Q~, K~ tiles and the e^{b_last} row of chunk n into buffer `buf`
-  auto issue_qkg = [&](int n, int buf) {
+  // Q~, K~ and masked-score tiles and the e^{b_last} row of chunk n into buffer `buf`
+  auto issue_x = [&](int n, int buf) {
     const int32_t r = (int32_t)(row0 + (int64_t)n * kC);
     unsigned char* xb = sm + SM::kX + buf * SM::kXBuf;
-    mbar_expect_tx(&bar_qkg[buf], 2 * SM::kTile + DK * 4);
+    mbar_expect_tx(&bar_x[buf], 2 * SM::kTile + kC * kC * 2 + DK * 4);
     for (int b = 0; b < DK / 64; ++b) {
-      tma_load_2d(xb + b * 8192, &tmQ, b * 64, r, &bar_qkg[buf]);
-      tma_load_2d(xb + SM::kTile + b * 8192, &tmK, b * 64, r, &bar_qkg[buf]);
+      tma_load_2d(xb + b * 8192, &tmQ, b * 64, r, &bar_x[buf]);
+      tma_load_2d(xb + SM::kTile + b * 8192, &tmK, b * 64, r, &bar_x[buf]);
     }
-    bulk_load(xb + 2 * SM::kTile, Eb + (size_t)(r / kC) * DK, DK * 4, &bar_qkg[buf]);
+    tma_load_2d(xb + SM::kP, &tmP, 0, r, &bar_x[buf]);
+    bulk_load(xb + SM::kE, Eb + (size_t)(r / kC) * DK, DK * 4, &bar_x[buf]);
   };
   auto issue_v = [&](int n) {
     const int32_t r = (int32_t)(row0 + (int64_t)n * kC);
     mbar_expect_tx(&bar_v, kNV * kC * 2);
     for (int b = 0; b < kNV / 64; ++b) tma_load_2d(sV + b * 8192, &tmV, j0 + b * 64, r, &bar_v);
   };
-  if (tid == 0) {
-    issue_qkg(BWD ? nc - 1 : 0, 0);
+  if (tid == kTmaTid) {
+    issue_x(BWD ? nc - 1 : 0, 0);
     issue_v(BWD ? nc - 1 : 0);
   }
 
@@ -156,8 +161,15 @@ tc_sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       float r[32];
       tmem_ld32(tmem + lane_off + c, r);
       tmem_ld_wait();
+      const float4* e4 = reinterpret_cast<const float4*>(sE + c);
 #pragma unroll
-      for (int u = 0; u < 32; ++u) r[u] *= sE[c + u];
+      for (int u = 0; u < 8; ++u) {
+        const float4 e = e4[u];
+        r[4 * u] *= e.x;
+        r[4 * u + 1] *= e.y;
+        r[4 * u + 2] *= e.z;
+        r[4 * u + 3] *= e.w;
+      }
       tmem_st32(tmem + lane_off + c, r);
       uint32_t h[16];
 #pragma unroll
@@ -167,30 +179,36 @@ tc_sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     tmem_st_wait();
   };
 
+  // o^T of chunk n (TMEM buffer ob) -> o  (warps 0-7: lane group lg, token half)
+  auto epilogue = [&](int n, int ob) {
+    float r[32];
+    tmem_ld32(tmem + lane_off + kColO + ob * 64 + half * 32, r);
+    tmem_ld_wait();
+    __nv_bfloat16* op = o + (size_t)(row0 + (int64_t)n * kC + half * 32) * dv + j0 + lg * 32 + lane;
+#pragma unroll
+    for (int u = 0; u < 32; ++u) op[(size_t)u * dv] = __float2bfloat16_rn(r[u]);
+  };
+
   for (int it = 0; it < nc; ++it) {
     const int n = BWD ? (nc - 1 - it) : it;  // chunk index in the segment
     const uint32_t par = (uint32_t)(it & 1);
     const int xbuf = it & 1;
     unsigned char* sQ = sm + SM::kX + xbuf * SM::kXBuf;
     unsigned char* sK = sQ + SM::kTile;
-    const float* sE = reinterpret_cast<const float*>(sQ + 2 * SM::kTile);  // e^{b_last}
-    // the next chunk's tiles go to the other buffer (its last readers, MMA group 1
-    // and the state pass of the previous chunk, have completed)
-    if (tid == 0 && it + 1 < nc) issue_qkg(BWD ? n - 1 : n + 1, xbuf ^ 1);
-    if (!mbar_wait(&bar_qkg[xbuf], (uint32_t)((it >> 1) & 1))) {
-      atomicExch(&g_fwd_status, 1);
-      abort_flag = 1;
-    }
+    unsigned char* sP = sQ + SM::kP;
+    const float* sE = reinterpret_cast<const float*>(sQ + SM::kE);  // e^{b_last}
+    if (!mbar_wait(&bar_x[xbuf], (uint32_t)((it >> 1) & 1))) atomicExch(&g_fwd_status, 1);
     if (BWD) state_pass(sE);
     tc_fence_before();
     __syncthreads();
-    if (abort_flag) break;
-    // ------------------------------------------------ MMA group 1
-    if (tid == 0) {
+    // the next chunk's tiles go to the other buffer (its last readers, the MMAs
+    // and the state pass of the previous chunk, have completed)
+    if (tid == kTmaTid && it + 1 < nc) issue_x(BWD ? n - 1 : n + 1, xbuf ^ 1);
+    // ------------------------------------------------ the chunk's MMAs
+    if (tid == kMmaTid) {
       tc_fence_after();
-      const uint32_t q0 = smem_u32(sQ), k0 = smem_u32(sK), v0 = smem_u32(sV);
-      // A = Q~ K~^T   (M = 64 tokens t, N = 64 tokens s, K = DK)
-      constexpr uint32_t idA = idesc_bf16(64, 64, false, false);
+      const uint32_t q0 = smem_u32(sQ), k0 = smem_u32(sK), v0 = smem_u32(sV), p0 = smem_u32(sP);
+      const uint32_t oc = tmem + kColO + (uint32_t)xbuf * 64;
       // forward:  o^T  = S^T  Q~^T   (M = 128 columns j, N = 64 tokens t, K = DK; A from TMEM)
       // backward: dv^T = dS^T K~^T   (M = 128 columns j, N = 64 tokens s, K = DK; A from TMEM)
       constexpr uint32_t idO = idesc_bf16(128, 64, false, false);
@@ -199,19 +217,23 @@ tc_sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       for (int kb = 0; kb < DK / 64; ++kb)
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t qd = sdesc_sw128(q0 + kb * 8192 + kk * 32, 16, 1024);
-          const uint64_t kd = sdesc_sw128(k0 + kb * 8192 + kk * 32, 16, 1024);
           const uint64_t xd = sdesc_sw128(x0 + kb * 8192 + kk * 32, 16, 1024);
-          umma_bf16(tmem + kColA, qd, kd, idA, (kb | kk) ? 1u : 0u);
-          umma_bf16_ta(tmem + kColO, tmem + kColS16 + kb * 32 + kk * 8, xd, idO,
-                       (kb | kk) ? 1u : 0u);
+          umma_bf16_ta(oc, tmem + kColS16 + kb * 32 + kk * 8, xd, idO, (kb | kk) ? 1u : 0u);
         }
+      if (!mbar_wait(&bar_v, par)) atomicExch(&g_fwd_status, 1);
+      tc_fence_after();
+      // forward:  o^T  += V^T  A^T  (B = A, K = s contiguous: K-major)
+      // backward: dv^T += do^T A    (B = A, K = t rows, N = s contiguous: MN-major)
+      constexpr uint32_t idO2 = idesc_bf16(128, 64, true, BWD);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const uint64_t vd = sdesc_sw128(v0 + kk * 2048, 8192, 1024);
+        const uint64_t pd = BWD ? sdesc_sw128(p0 + kk * 2048, 8192, 1024)
+                                : sdesc_sw128(p0 + kk * 32, 16, 1024);
+        umma_bf16(oc, vd, pd, idO2, 1u);
+      }
       // forward:  S^T  += V^T  K~   (M = 128 columns j, N = DK rows i, K = 64 tokens s)
       // backward: dS^T += do^T Q~   (M = 128 columns j, N = DK rows i, K = 64 tokens t)
-      if (!mbar_wait(&bar_v, par)) {
-        atomicExch(&g_fwd_status, 1);
-      }
-      tc_fence_after();
       const uint32_t u0 = BWD ? q0 : k0;
       constexpr uint32_t idS = idesc_bf16(128, DK, true, true);
 #pragma unroll
@@ -220,68 +242,19 @@ tc_sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         const uint64_t ud = sdesc_sw128(u0 + kk * 2048, 8192, 1024);
         umma_bf16(tmem, vd, ud, idS, 1u);
       }
-      umma_commit(&bar_g1);
+      umma_commit(&bar_g);
     }
-    if (!mbar_wait(&bar_g1, par)) atomicExch(&g_fwd_status, 1);
+    // ------------------------------------------------ the previous chunk's output
+    if (warp < 8 && it > 0) epilogue(BWD ? n + 1 : n - 1, xbuf ^ 1);
+    if (!mbar_wait(&bar_g, par)) atomicExch(&g_fwd_status, 1);
     tc_fence_after();
-    // ------------------------------------------------ mask A -> P (bf16, K-major [t][s])
-    if (warp < 4) {
-      float a[64];
-      tmem_ld32(tmem + lane_off + kColA, a);
-      tmem_ld32(tmem + lane_off + kColA + 32, a + 32);
-      tmem_ld_wait();
-      if (lane < 16) {
-        const int t = warp * 16 + lane;  // M = 64 layout: row 16w + l sits in lane 32w + l
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          uint32_t w4[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int s0 = c * 8 + 2 * u;
-            w4[u] = pack_bf16(s0 <= t ? a[s0] : 0.f, s0 + 1 <= t ? a[s0 + 1] : 0.f);
-          }
-          *reinterpret_cast<uint4*>(sP + sw128((uint32_t)t, (uint32_t)c)) =
-              make_uint4(w4[0], w4[1], w4[2], w4[3]);
-        }
-      }
-    }
+    if (tid == kTmaTid && it + 1 < nc) issue_v(BWD ? n - 1 : n + 1);  // V buffer is free now
     // forward: S <- e^{b_last} .* S, refresh the bf16 copy for the next chunk
     if (!BWD) state_pass(sE);
-    tmem_st_wait();
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    // ------------------------------------------------ MMA group 2: o^T += V^T P^T
-    if (tid == 0) {
-      tc_fence_after();
-      const uint32_t v0 = smem_u32(sV), p0 = smem_u32(sP);
-      // forward:  o^T  += V^T  P^T  (B = P, K = s contiguous: K-major)
-      // backward: dv^T += do^T P    (B = P, K = t rows, N = s contiguous: MN-major)
-      constexpr uint32_t idO2 = idesc_bf16(128, 64, true, BWD);
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        const uint64_t vd = sdesc_sw128(v0 + kk * 2048, 8192, 1024);
-        const uint64_t pd = BWD ? sdesc_sw128(p0 + kk * 2048, 8192, 1024)
-                                : sdesc_sw128(p0 + kk * 32, 16, 1024);
-        umma_bf16(tmem + kColO, vd, pd, idO2, 1u);
-      }
-      umma_commit(&bar_g2);
-    }
-    if (!mbar_wait(&bar_g2, par)) atomicExch(&g_fwd_status, 1);
-    tc_fence_after();
-    if (tid == 0 && it + 1 < nc) issue_v(BWD ? n - 1 : n + 1);  // V buffer is free now
-    // ------------------------------------------------ epilogue: o^T -> o
-    if (warp < 8) {
-      float r[32];
-      tmem_ld32(tmem + lane_off + kColO + half * 32, r);
-      tmem_ld_wait();
-      __nv_bfloat16* op = o + (size_t)(row0 + (int64_t)n * kC + half * 32) * dv + j0 + lg * 32 + lane;
-#pragma unroll
-      for (int u = 0; u < 32; ++u) op[(size_t)u * dv] = __float2bfloat16_rn(r[u]);
-    }
     tc_fence_before();
     __syncthreads();
   }
+  if (warp < 8) epilogue(BWD ? 0 : nc - 1, (nc - 1) & 1);
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, 512);
@@ -289,19 +262,20 @@ tc_sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 
 template <int DK, bool BWD>
 cudaError_t launch_sweep(const Dims& d, const void* Qt, const void* Kt, const void* v,
-                         const float* Eb, const float* S_src, void* o, cudaStream_t st) {
-  CUtensorMap tq, tk, tv;
+                         const void* A, const float* Eb, const float* S_src, void* o,
+                         cudaStream_t st) {
+  CUtensorMap tq, tk, tv, tp;
   const uint64_t rows = (uint64_t)(d.B * d.H * d.T);
   if (!make_tmap_bf16(&tq, Qt, rows, DK, kC) || !make_tmap_bf16(&tk, Kt, rows, DK, kC) ||
-      !make_tmap_bf16(&tv, v, rows, d.dv, kC))
+      !make_tmap_bf16(&tv, v, rows, d.dv, kC) || !make_tmap_bf16(&tp, A, rows, kC, kC))
     return cudaErrorInvalidValue;
   const int smem = FwdSmem<DK>::kBytes + 1024;
   auto kern = tc_sweep_kernel<DK, BWD>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)(d.dv / kNV), (unsigned)(d.B * d.H * d.P));
-  kern<<<grid, kThreads, smem, st>>>(tq, tk, tv, Eb, S_src, (__nv_bfloat16*)o, d.T, (int)d.dv,
-                                     d.P, d.L);
+  kern<<<grid, kThreads, smem, st>>>(tq, tk, tv, tp, Eb, S_src, (__nv_bfloat16*)o, d.T,
+                                     (int)d.dv, d.P, d.L);
   return cudaGetLastError();
 }
 
@@ -313,17 +287,19 @@ bool tc_fwd_supported(const Dims& d) {
 }
 
 cudaError_t tc_fwd_out(const Dims& d, const void* Qt, const void* Kt, const void* v,
-                       const float* Eb, const float* S_in, void* o, cudaStream_t st) {
-  cudaError_t e = d.dk == 256 ? launch_sweep<256, false>(d, Qt, Kt, v, Eb, S_in, o, st)
-                              : launch_sweep<128, false>(d, Qt, Kt, v, Eb, S_in, o, st);
+                       const void* A, const float* Eb, const float* S_in, void* o,
+                       cudaStream_t st) {
+  cudaError_t e = d.dk == 256 ? launch_sweep<256, false>(d, Qt, Kt, v, A, Eb, S_in, o, st)
+                              : launch_sweep<128, false>(d, Qt, Kt, v, A, Eb, S_in, o, st);
   prof_mark("tc_fwd_out", st);
   return e;
 }
 
 cudaError_t tc_bwd_dv(const Dims& d, const void* Qt, const void* Kt, const void* d_o,
-                      const float* Eb, const float* D, void* dv, cudaStream_t st) {
-  cudaError_t e = d.dk == 256 ? launch_sweep<256, true>(d, Qt, Kt, d_o, Eb, D, dv, st)
-                              : launch_sweep<128, true>(d, Qt, Kt, d_o, Eb, D, dv, st);
+                      const void* A, const float* Eb, const float* D, void* dv,
+                      cudaStream_t st) {
+  cudaError_t e = d.dk == 256 ? launch_sweep<256, true>(d, Qt, Kt, d_o, A, Eb, D, dv, st)
+                              : launch_sweep<128, true>(d, Qt, Kt, d_o, A, Eb, D, dv, st);
   prof_mark("tc_bwd_dv", st);
   return e;
 }

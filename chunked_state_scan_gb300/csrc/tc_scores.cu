@@ -1,16 +1,20 @@
-// tc_dA.cu -- gradient of the intra-chunk scores, dA = do v^T masked to s <= t,
-// for every chunk of C = 64 tokens, in bf16 ([B,H,T,64]: row t of a chunk holds
-// its 64 scores over s).  It does not depend on the state, so it is computed
-// once per chunk here and read by both dq/dk sweeps (tc_bwd_qk.cu), which use
-// dq~ += dA K~ and dk~ += dA^T Q~ (chunkwise backward of the diagonal
-// attention: Pith review of ZeCO, referee major comment 3 on Algorithm 1).
+// tc_scores.cu -- masked intra-chunk products P = X Y^T (s <= t) for every chunk
+// of C = 64 tokens, in bf16 ([B,H,T,64]: row t of a chunk holds its 64 values
+// over s).  Neither depends on the state, so each is computed once per chunk
+// here and read by the sweeps (chunkwise form of the diagonal attention: Pith
+// review of ZeCO, referee major comment 3 on Algorithm 1):
 //
-// A persistent kernel, one CTA per SM, bound by reading do and v once from HBM.
-// Warp 4 streams do/v tiles of 64 tokens x 128 d_v columns through a 4-stage
-// ring (TMA, 128B swizzle); warp 5 issues the tcgen05 MMAs (M = 64 t, N = 64 s,
-// K = d_v) into one of two TMEM accumulators; warps 0-3 read a finished
-// accumulator (the M = 64 layout puts row t in lane 32 (t / 16) + t % 16),
-// mask, round and store it while the next chunk accumulates.
+//   A  = Q~ K~^T   (X = Q~, Y = K~, K = d_k): the intra-chunk scores, read by
+//                  the forward sweep (o += A v) and the dv sweep (dv += A^T do);
+//   dA = do v^T    (X = do, Y = v,  K = d_v): their gradient, read by the dq/dk
+//                  sweeps (dq~ += dA K~, dk~ += dA^T Q~).
+//
+// A persistent kernel, one CTA per SM, bound by reading X and Y once from HBM.
+// Warp 4 streams X/Y tiles of 64 tokens x 128 columns through a 4-stage ring
+// (TMA, 128B swizzle); warp 5 issues the tcgen05 MMAs (M = 64 t, N = 64 s,
+// K) into one of two TMEM accumulators; warps 0-3 read a finished accumulator
+// (the M = 64 layout puts row t in lane 32 (t / 16) + t % 16), mask, round and
+// store it while the next chunk accumulates.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -26,23 +30,23 @@ namespace {
 using namespace tc;
 
 constexpr int kC = 64;
-constexpr int kQ = 128;                     // d_v columns per stage
+constexpr int kQ = 128;                     // columns of K per stage
 constexpr int kStages = 4;
-constexpr int kHalf = kC * kQ * 2;          // do or v part of a stage (16 KB)
+constexpr int kHalf = kC * kQ * 2;          // X or Y part of a stage (16 KB)
 constexpr int kStageBytes = 2 * kHalf;
 constexpr int kThreads = 192;
 
-__device__ int g_dA_status = 0;
+__device__ int g_scores_status = 0;
 
 __global__ void __launch_bounds__(kThreads, 1)
-tc_dA_kernel(const __grid_constant__ CUtensorMap tmDO, const __grid_constant__ CUtensorMap tmV,
-             __nv_bfloat16* __restrict__ P, int64_t nchunks, int dv) {
+tc_masked_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmY,
+                 __nv_bfloat16* __restrict__ P, int64_t nchunks, int K) {
   extern __shared__ __align__(1024) unsigned char smraw[];
   unsigned char* sm = (unsigned char*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
   __shared__ uint64_t full[kStages], empty[kStages], accfull[2], accempty[2];
   __shared__ uint32_t tmem_base;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int nq = dv / kQ;
+  const int nq = K / kQ;
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -54,8 +58,8 @@ tc_dA_kernel(const __grid_constant__ CUtensorMap tmDO, const __grid_constant__ C
       mbar_init(&accempty[b], 128);
     }
     fence_mbar_init();
-    prefetch_tmap(&tmDO);
-    prefetch_tmap(&tmV);
+    prefetch_tmap(&tmX);
+    prefetch_tmap(&tmY);
   }
   if (warp == 0) tmem_alloc(&tmem_base, 128);
   tc_fence_before();
@@ -64,7 +68,7 @@ tc_dA_kernel(const __grid_constant__ CUtensorMap tmDO, const __grid_constant__ C
   const uint32_t tmem = tmem_base;
 
   if (warp == 4) {
-    // ---- producer: do and v tiles of every (chunk, d_v quarter) this CTA owns
+    // ---- producer: X and Y tiles of every (chunk, K slice) this CTA owns
     if (lane == 0) {
       int64_t gi = 0;
       for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x) {
@@ -72,30 +76,30 @@ tc_dA_kernel(const __grid_constant__ CUtensorMap tmDO, const __grid_constant__ C
         for (int q = 0; q < nq; ++q, ++gi) {
           const int s = (int)(gi % kStages);
           const uint32_t ph = (uint32_t)((gi / kStages) & 1);
-          if (!mbar_wait(&empty[s], ph ^ 1u)) atomicExch(&g_dA_status, 1);
+          if (!mbar_wait(&empty[s], ph ^ 1u)) atomicExch(&g_scores_status, 1);
           unsigned char* st = sm + s * kStageBytes;
           mbar_expect_tx(&full[s], kStageBytes);
           for (int b = 0; b < kQ / 64; ++b) {
-            tma_load_2d(st + b * 8192, &tmDO, q * kQ + b * 64, r, &full[s]);
-            tma_load_2d(st + kHalf + b * 8192, &tmV, q * kQ + b * 64, r, &full[s]);
+            tma_load_2d(st + b * 8192, &tmX, q * kQ + b * 64, r, &full[s]);
+            tma_load_2d(st + kHalf + b * 8192, &tmY, q * kQ + b * 64, r, &full[s]);
           }
         }
       }
     }
     __syncwarp();
   } else if (warp == 5) {
-    // ---- MMA issuer: dA = do v^T, accumulated over the d_v quarters
+    // ---- MMA issuer: X Y^T, accumulated over the K slices
     if (lane == 0) {
       constexpr uint32_t id = idesc_bf16(64, 64, false, false);
       int64_t gi = 0;
       int k = 0;
       for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x, ++k) {
         const int b = k & 1;
-        if (!mbar_wait(&accempty[b], (uint32_t)(((k >> 1) & 1) ^ 1))) atomicExch(&g_dA_status, 1);
+        if (!mbar_wait(&accempty[b], (uint32_t)(((k >> 1) & 1) ^ 1))) atomicExch(&g_scores_status, 1);
         tc_fence_after();
         for (int q = 0; q < nq; ++q, ++gi) {
           const int s = (int)(gi % kStages);
-          if (!mbar_wait(&full[s], (uint32_t)((gi / kStages) & 1))) atomicExch(&g_dA_status, 1);
+          if (!mbar_wait(&full[s], (uint32_t)((gi / kStages) & 1))) atomicExch(&g_scores_status, 1);
           tc_fence_after();
           const uint32_t a0 = smem_u32(sm + s * kStageBytes), b0 = a0 + kHalf;
 #pragma unroll
@@ -116,7 +120,7 @@ tc_dA_kernel(const __grid_constant__ CUtensorMap tmDO, const __grid_constant__ C
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
     for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x, ++k) {
       const int b = k & 1;
-      if (!mbar_wait(&accfull[b], (uint32_t)((k >> 1) & 1))) atomicExch(&g_dA_status, 1);
+      if (!mbar_wait(&accfull[b], (uint32_t)((k >> 1) & 1))) atomicExch(&g_scores_status, 1);
       tc_fence_after();
       float a[64];
       tmem_ld32(tmem + lane_off + b * 64, a);
@@ -148,15 +152,18 @@ tc_dA_kernel(const __grid_constant__ CUtensorMap tmDO, const __grid_constant__ C
 }  // namespace
 
 bool tc_dA_supported(const Dims& d) { return d.bf16 && d.C == kC && d.dv % kQ == 0; }
+bool tc_A_supported(const Dims& d) { return d.bf16 && d.C == kC && d.dk % kQ == 0; }
 
-cudaError_t tc_dA(const Dims& d, const void* d_o, const void* v, void* P, cudaStream_t st) {
-  CUtensorMap tdo, tv;
+namespace {
+cudaError_t launch_masked(const Dims& d, const void* X, const void* Y, int K, void* P,
+                          cudaStream_t st) {
+  CUtensorMap tx, ty;
   const uint64_t rows = (uint64_t)(d.B * d.H * d.T);
-  if (!make_tmap_bf16(&tdo, d_o, rows, d.dv, kC) || !make_tmap_bf16(&tv, v, rows, d.dv, kC))
+  if (!make_tmap_bf16(&tx, X, rows, K, kC) || !make_tmap_bf16(&ty, Y, rows, K, kC))
     return cudaErrorInvalidValue;
   const int smem = kStages * kStageBytes + 1024;
-  cudaError_t e = cudaFuncSetAttribute(tc_dA_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       smem);
+  cudaError_t e = cudaFuncSetAttribute(tc_masked_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
@@ -164,9 +171,21 @@ cudaError_t tc_dA(const Dims& d, const void* d_o, const void* v, void* P, cudaSt
     return e;
   const int64_t nchunks = (int64_t)rows / kC;
   const unsigned grid = (unsigned)(nchunks < sms ? nchunks : sms);
-  tc_dA_kernel<<<grid, kThreads, smem, st>>>(tdo, tv, (__nv_bfloat16*)P, nchunks, (int)d.dv);
-  prof_mark("tc_dA", st);
+  tc_masked_kernel<<<grid, kThreads, smem, st>>>(tx, ty, (__nv_bfloat16*)P, nchunks, K);
   return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t tc_dA(const Dims& d, const void* d_o, const void* v, void* P, cudaStream_t st) {
+  cudaError_t e = launch_masked(d, d_o, v, (int)d.dv, P, st);
+  prof_mark("tc_dA", st);
+  return e;
+}
+
+cudaError_t tc_A(const Dims& d, const void* Qt, const void* Kt, void* P, cudaStream_t st) {
+  cudaError_t e = launch_masked(d, Qt, Kt, (int)d.dk, P, st);
+  prof_mark("tc_A", st);
+  return e;
 }
 
 }  // namespace zeco

@@ -48,8 +48,10 @@ def test_sizes_follow_the_layout(lib):
     gam = 4 * 64 * 256 * 4
     assert z.saved_bytes(s) == state + gam
     qdq = 4 * (1 << 20) * 256 * 4
-    # tensor-core path: Q~ and K~ (bf16) and e^{b_last} per 64-token chunk (fp32)
-    decay = 2 * 4 * (1 << 20) * 256 * 2 + 4 * (1 << 20) // 64 * 256 * 4
+    # tensor-core path: Q~ and K~ (bf16), e^{b_last} per 64-token chunk (fp32) and
+    # the masked intra-chunk scores [B,H,T,64] (bf16)
+    decay = (2 * 4 * (1 << 20) * 256 * 2 + 4 * (1 << 20) // 64 * 256 * 4
+             + 4 * (1 << 20) * 64 * 2)
     # backward only: the masked intra-chunk score gradients [B,H,T,64] bf16
     dA = 4 * (1 << 20) * 64 * 2
     assert z.workspace_bytes(s, True) == state + gam + qdq + decay + dA
