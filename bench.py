@@ -98,6 +98,28 @@ def canonical_kernel(name):
     return name
 
 
+def measured_traffic(path, kernel, token_heads):
+    """DRAM bytes of one launch of `kernel` from the committed ncu capture
+    (profiles/traffic.json, per token-head, scaled to this launch), or None when
+    there is no capture or the kernel's sources changed since it was taken."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            ent = json.load(f).get(f"{path}:{kernel}")
+    except (OSError, ValueError):
+        return None
+    if not ent:
+        return None
+    for rel, digest in ent.get("sources", {}).items():
+        try:
+            with open(os.path.join(ROOT, rel), "rb") as f:
+                if hashlib.sha256(f.read()).hexdigest() != digest:
+                    return None
+        except OSError:
+            return None
+    return ent["bytes_per_token_head"] * token_heads
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -378,17 +400,7 @@ def main(argv=None):
     op_flops = zeco_operator_flops_per_token(w.dk, w.dv, w.C) * w.T * bh
     t_roof = max(op_bytes / (hbm_peak * 1e9), op_flops / (float(peaks["bf16_tflops"]) * 1e12))
     step_s = ms_step * 1e-3
-    traffic = None
-    tr_path = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(tr_path):
-        try:
-            with open(tr_path) as f:
-                tr = json.load(f)
-            ent = tr.get(f"{path}:{dom}")
-            if ent:
-                traffic = ent
-        except (OSError, ValueError):
-            traffic = None
+    traffic = measured_traffic(path, dom, w.T * bh)
     scan_ms = sum(v for k, v in kern_ms.items() if "seg_scan" in k)
 
     line = {
@@ -402,6 +414,7 @@ def main(argv=None):
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": dom_gbs, "peak": hbm_peak,
                      "unit": "GB/s", "frac": dom_gbs / hbm_peak, "traffic": traffic,
+                     "traffic_unit": "DRAM bytes per launch (ncu capture, scaled by tokens)",
                      "peak_source": f"{peak_kind} hbm_gbs",
                      "algorithmic_bytes_per_launch": dom_bytes},
         "operator_roofline": {"bytes": op_bytes, "flops": op_flops, "t_roof_ms": t_roof * 1e3,

@@ -37,8 +37,25 @@
 // The masked intra-chunk score gradient dA = do v^T comes precomputed in bf16
 // (tc_scores.cu); CTA rank 0 of the pair adds its term.
 //
-// TMEM columns: [0, 128) state (d_v group g of this CTA at 64 g) | [192, 256)
-// dq^T or dk^T (M = 64 layout, lane = d_k row).
+// Tensor-memory layout.  A CTA keeps its 64 x 256 block of the state (or the
+// adjoint) S[i, j] in fp32 twice, in lanes i and 64 + i (columns j): the
+// update S += K~^T v is one M = 128, N = 256 MMA per 16 tokens whose A operand
+// reads the [t][i] tile twice (both 64-row blocks at the same address).  Lanes
+// 0-63 turn their copy into the bf16 high part of S and lanes 64-127 into the
+// low part, which together are the A operand (rows = lanes, K = j in bf16
+// pairs) of dq^T = S do^T: one M = 128 MMA per 16 columns j gives the high-part
+// product in rows 0-63 and the low-part product in rows 64-127 of the
+// accumulator.  The dA term joins rows 0-63 (its A operand's second block is a
+// zero tile).  The two parts of each row go to separate partial-sum buffers
+// that the epilogue adds.
+//
+// Warp roles (384 threads): thread 0 issues the copies and the MMAs; warps 0-7
+// (warps w and w + 4 share lane quarter w % 4, each half of the columns) rescale
+// the state, rebuild its hi/lo copy and send the partial sums; warps 8-11 run
+// the epilogue of the previous chunk and read this chunk's epilogue factors.
+//
+// TMEM columns: [0, 256) state fp32 (two copies) | [256, 384) hi/lo copy |
+// [384, 448) dq^T or dk^T (rows 0-63 hi part + dA term, 64-127 lo part).
 #include <cuda.h>
 
 #include "common.cuh"
@@ -59,24 +76,25 @@ constexpr int kC = 64;
 constexpr int kKB = 64;    // d_k rows per CTA pair
 constexpr int kDV = 512;   // d_v
 constexpr int kDVH = 256;  // d_v columns per CTA
-constexpr int kThreads = 256;
-constexpr uint32_t kColAcc = 192;
+constexpr int kThreads = 384;
+constexpr uint32_t kColS = 0, kColHL = 256, kColAcc = 384;
 
 // shared memory (bytes, 1024-aligned regions)
 constexpr int kOffDO = 0;                        // do tile [64 t][256 j] (4 blocks of 64 j)
 constexpr int kOffV = kOffDO + kC * kDVH * 2;    // v tile
-constexpr int kOffHi = kOffV + kC * kDVH * 2;    // state copy, high part [256 j][64 i]
-constexpr int kOffLo = kOffHi + kDVH * kKB * 2;  // state copy, low part
 constexpr int kXTile = kC * kKB * 2;             // one [64 t][64 i] bf16 tile
 // Q~, K~, log_alpha tiles + q.dq rows [64 t][32 i] fp32 + e^{b_last} [64] fp32
 constexpr int kXBuf = 3 * kXTile + 32 * kC * 4 + 1024;
-constexpr int kOffX = kOffLo + kDVH * kKB * 2;   // 2 buffers of kXBuf (chunk parity)
+constexpr int kOffX = kOffV + kC * kDVH * 2;     // 2 buffers of kXBuf (chunk parity)
 constexpr int kOffP = kOffX + 2 * kXBuf;         // masked dA [64 t][64 s] bf16 (with do, v)
 constexpr int kRS = kC + 4;                      // row stride of the partial sums (floats)
-constexpr int kOffR = kOffP + kC * kC * 2;       // peer's partial for my rows [32][kRS] fp32
-constexpr int kOffOwn = kOffR + 32 * kRS * 4;    // my own partial for my rows [32][kRS] fp32
-constexpr int kOffGq = kOffOwn + 32 * kRS * 4;   // sums of log_alpha per 8 tokens [8][32]
-constexpr int kOffQS = kOffGq + 1024;            // reverse: sums of dg terms per 8 tokens [8][32]
+constexpr int kPart = 32 * kRS * 4;              // one [32 rows][kRS] fp32 partial-sum buffer
+// partial sums for my 32 rows: the peer's high and low parts, then my own
+constexpr int kOffR = kOffP + kC * kC * 2;       // peer: hi at +0, lo at +kPart
+constexpr int kOffOwn = kOffR + 2 * kPart;       // own:  hi at +0, lo at +kPart
+constexpr int kOffZero = kOffOwn + 2 * kPart;    // zero tile [64][64] bf16 (dA term's A rows 64-127)
+constexpr int kOffGq = kOffZero + kC * kC * 2;   // sums of log_alpha per 16 tokens [4][32]
+constexpr int kOffQS = kOffGq + 1024;            // reverse: sums of dg terms per 16 tokens [4][32]
 constexpr int kOffRun = kOffQS + 1024;           // reverse: dg suffix carried per row [32]
 constexpr int kSmem = kOffRun + 128;
 
@@ -96,8 +114,6 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   unsigned char* sm = (unsigned char*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
   unsigned char* sDO = sm + kOffDO;
   unsigned char* sV = sm + kOffV;
-  unsigned char* sHi = sm + kOffHi;
-  unsigned char* sLo = sm + kOffLo;
   unsigned char* sP = sm + kOffP;
   float* sR = reinterpret_cast<float*>(sm + kOffR);
   float* sOwn = reinterpret_cast<float*>(sm + kOffOwn);
@@ -106,11 +122,13 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   float* sRun = reinterpret_cast<float*>(sm + kOffRun);
   // bar_full: the peer's partial for my rows has landed in sR (complete_tx from
   // the peer's st.async); bar_empty: the peer has read the partial I sent it.
-  __shared__ uint64_t bar_x[2], bar_dv, bar_g1, bar_full, bar_empty;
+  // bar_a: the state update of the chunk is done, so the state may be rescaled
+  // while the dq^T / dk^T MMAs run.
+  __shared__ uint64_t bar_x[2], bar_dv, bar_a, bar_g1, bar_full, bar_empty;
   __shared__ uint32_t tmem_base;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int lg = warp & 3, grp = warp >> 2;  // TMEM lane group; this warp's d_v group
+  const int lg = warp & 3;                   // TMEM lane quarter of this warp
   const uint32_t rank = cluster_ctarank();   // which half of d_v
   const int64_t bh = blockIdx.y / P;
   const int p = blockIdx.y % P;
@@ -118,15 +136,20 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   const int jb = (int)rank * kDVH;
   const int64_t row0 = bh * T + (int64_t)p * L;
   const int nc = (int)(L / kC);
-  // the M = 64 TMEM layout: warp w < 4, lane l < 16 holds row 16 w + l
-  const bool rowt = warp < 4 && lane < 16;
-  const int ii = warp * 16 + lane;                      // d_k row within the block
-  const bool owned = rowt && (uint32_t)(ii >> 5) == rank;  // finished by this CTA
+  // state warps 0-7: lane `lane` of quarter lg is TMEM row r = 32 lg + lane, the
+  // high part (r < 64) or low part (r >= 64) of d_k row ii = r % 64 of the block;
+  // warp w handles columns [128 ch, 128 ch + 128) of the state with ch = w / 4
+  const int r_tm = 32 * lg + lane;
+  const int ii = r_tm & 63;                              // d_k row within the block
+  const int part = r_tm >> 6;                            // 0: high part, 1: low part
+  const int ch = (warp >> 2) & 1;
+  const bool owned = (uint32_t)(ii >> 5) == rank;       // finished by this CTA
 
   if (tid == 0) {
     mbar_init(&bar_x[0], 1);
     mbar_init(&bar_x[1], 1);
     mbar_init(&bar_dv, 1);
+    mbar_init(&bar_a, 1);
     mbar_init(&bar_g1, 1);
     mbar_init(&bar_full, 1);
     mbar_init(&bar_empty, 1);
@@ -139,7 +162,10 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     prefetch_tmap(&tmP);
     if (REV) prefetch_tmap(&tmQD);
   }
-  if (warp == 0) tmem_alloc(&tmem_base, 256);
+  if (warp == 0) tmem_alloc(&tmem_base, 512);
+  for (int u = tid; u < kC * kC * 2 / 16; u += kThreads)
+    reinterpret_cast<uint4*>(sm + kOffZero)[u] = make_uint4(0u, 0u, 0u, 0u);
+  fence_async_smem();  // the zero tile is read by the tensor cores
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -176,77 +202,91 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     issue_dv(REV ? nc - 1 : 0);
   }
 
-  // bf16 hi/lo copy of this warp's state group (lanes = local d_v column j)
-  auto write_copy = [&](const float* r) {
-    const uint32_t j = (uint32_t)(grp * 128 + lg * 32 + lane);
+  // ---- state helpers (warps 0-7): this thread's TMEM row r_tm, the columns
+  //      [128 ch, 128 ch + 128) of the state
+  const uint32_t srow = tmem + lane_off + kColS + 128 * (uint32_t)ch;
+  // S <- e^{b_last} .* S (row ii scaled by sE[ii]); 64 columns per load batch
+  auto scale_state = [&](const float* sE) {
+    const float e = sE[ii];
+#pragma unroll 1
+    for (int h = 0; h < 2; ++h) {
+      float r[64];
+      tmem_ld32(srow + 64 * h, r);
+      tmem_ld32(srow + 64 * h + 32, r + 32);
+      tmem_ld_wait();
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      uint32_t hw[4], lw[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const float a = r[8 * c + 2 * u], b = r[8 * c + 2 * u + 1];
-        const __nv_bfloat16 ha = __float2bfloat16_rn(a), hb = __float2bfloat16_rn(b);
-        __nv_bfloat162 h2, l2;
-        h2.x = ha;
-        h2.y = hb;
-        l2 = __floats2bfloat162_rn(a - __bfloat162float(ha), b - __bfloat162float(hb));
-        hw[u] = *reinterpret_cast<uint32_t*>(&h2);
-        lw[u] = *reinterpret_cast<uint32_t*>(&l2);
-      }
-      const uint32_t off = sw128(j, (uint32_t)c);
-      *reinterpret_cast<uint4*>(sHi + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-      *reinterpret_cast<uint4*>(sLo + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+      for (int u = 0; u < 64; ++u) r[u] *= e;
+      tmem_st32(srow + 64 * h, r);
+      tmem_st32(srow + 64 * h + 32, r + 32);
     }
+    tmem_st_wait();
+  };
+  // this thread's part (high: bf16(S); low: bf16(S - high)) of the bf16 copy
+  auto make_copy = [&]() {
+    const uint32_t crow = tmem + lane_off + kColHL + 64 * (uint32_t)ch;
+#pragma unroll 1
+    for (int h = 0; h < 2; ++h) {
+      float r[64];
+      tmem_ld32(srow + 64 * h, r);
+      tmem_ld32(srow + 64 * h + 32, r + 32);
+      tmem_ld_wait();
+      uint32_t w32[32];
+#pragma unroll
+      for (int u = 0; u < 32; ++u) {
+        const __nv_bfloat162 h2 = __floats2bfloat162_rn(r[2 * u], r[2 * u + 1]);
+        const float2 hf = __bfloat1622float2(h2);
+        const __nv_bfloat162 l2 = __floats2bfloat162_rn(r[2 * u] - hf.x, r[2 * u + 1] - hf.y);
+        w32[u] = part ? *reinterpret_cast<const uint32_t*>(&l2)
+                      : *reinterpret_cast<const uint32_t*>(&h2);
+      }
+      tmem_st16(crow + 32 * h, w32);
+      tmem_st16(crow + 32 * h + 16, w32 + 16);
+    }
+    tmem_st_wait();
   };
 
-  // ---- initial state: rows i0..i0+63, this CTA's columns
-  {
-    const float* Sp = S_src + (((size_t)bh * (P + 1) + p + (REV ? 1 : 0)) * dk + i0) * kDV + jb +
-                      grp * 128 + lg * 32 + lane;
-    float r[64];
+  // ---- initial state: rows i0..i0+63, this CTA's columns (both copies)
+  if (warp < 8) {
+    const float* Sp = S_src + (((size_t)bh * (P + 1) + p + (REV ? 1 : 0)) * dk + i0 + ii) * kDV +
+                      jb + 128 * ch;
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+      float r[32];
 #pragma unroll
-    for (int u = 0; u < 64; ++u) r[u] = Sp[(size_t)u * kDV];
-    tmem_st32(tmem + lane_off + grp * 64, r);
-    tmem_st32(tmem + lane_off + grp * 64 + 32, r + 32);
-    if (!REV) write_copy(r);
+      for (int u = 0; u < 8; ++u) {
+        const float4 x = reinterpret_cast<const float4*>(Sp + 32 * c)[u];
+        r[4 * u] = x.x;
+        r[4 * u + 1] = x.y;
+        r[4 * u + 2] = x.z;
+        r[4 * u + 3] = x.w;
+      }
+      tmem_st32(srow + 32 * c, r);
+    }
     tmem_st_wait();
+    if (REV) {
+      // the first chunk's adjoint is scaled by its e^{b_last} before its MMAs
+      if (!mbar_wait(&bar_x[0], 0u)) atomicExch(&g_qk_status, 1);
+      scale_state(reinterpret_cast<const float*>(sm + kOffX + 3 * kXTile + 32 * kC * 4));
+    }
+    make_copy();
   }
-
-  // state <- e^{b_last} .* state (column i scaled by sE[i]) and its hi/lo copy
-  auto state_pass = [&](const float* sE) {
-    float r[64];
-    tmem_ld32(tmem + lane_off + grp * 64, r);
-    tmem_ld32(tmem + lane_off + grp * 64 + 32, r + 32);
-    tmem_ld_wait();
-#pragma unroll
-    for (int u = 0; u < 64; ++u) r[u] *= sE[u];
-    tmem_st32(tmem + lane_off + grp * 64, r);
-    tmem_st32(tmem + lane_off + grp * 64 + 32, r + 32);
-    write_copy(r);
-    tmem_st_wait();
-  };
 
   // element (t, column c) of a [64 t][64 i] tile
   auto tile_at = [&](unsigned char* base, int t, int c) -> __nv_bfloat16* {
     return reinterpret_cast<__nv_bfloat16*>(base + sw128((uint32_t)t, (uint32_t)((c & 63) >> 3)) +
                                             (uint32_t)(c & 7) * 2u);
   };
-  // Warp roles within a chunk: thread 0 issues the TMA copies and the MMAs;
-  // warps 0-3 read the dA and partial-sum accumulators (the M = 64 layout puts
-  // rows in their lanes) and mask dA; all 8 warps run the state pass; warps 4-7
-  // run the previous chunk's epilogue and this chunk's epilogue prefetch while
-  // the tensor cores execute MMA group 1.
-  // Epilogue workers (warps 4-7): owned row er (d_k row ec of the block) x the
+  // Epilogue workers (warps 8-11): owned row er (d_k row ec of the block) x the
   // 16 tokens 16 eq .. 16 eq + 15.
-  const int er = tid & 31, eq = (warp - 4) & 3;
+  const int er = tid & 31, eq = (warp - 8) & 3;
   const int ec = 32 * (int)rank + er;
-  const bool epi = warp >= 4;
+  const bool epi = warp >= 8;
 
   if (REV && tid < 32) sRun[tid] = carry[((size_t)bh * P + p) * dk + i0 + 32 * (int)rank + tid];
   const uint32_t peer = rank ^ 1u;
   const uint32_t peer_full = map_to_rank(smem_u32(&bar_full), peer);
   const uint32_t peer_empty = map_to_rank(smem_u32(&bar_empty), peer);
-  if (tid == 128) mbar_expect_tx(&bar_full, 32 * kC * 4);  // phase 0: the first partial
+  if (tid == 256) mbar_expect_tx(&bar_full, 2 * 32 * kC * 4);  // phase 0: the first partial
 
   // Per-element factors of a chunk's epilogue, read from the chunk's tiles in its
   // own iteration and kept in registers until the epilogue runs in the next one
@@ -277,18 +317,21 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       if (REV) qd[u] = sQD[(16 * eq + u) * 32 + er];
     }
   };
-  // outputs of chunk n from the two partial sums (peer's + own)
+  // outputs of chunk n from the four partial sums (peer's and own, high and low
+  // parts)
   auto epilogue = [&](int n) {
-    const float4* rp = reinterpret_cast<const float4*>(sR + er * kRS + 16 * eq);
-    const float4* op = reinterpret_cast<const float4*>(sOwn + er * kRS + 16 * eq);
+    const float4* rh = reinterpret_cast<const float4*>(sR + er * kRS + 16 * eq);
+    const float4* rl = reinterpret_cast<const float4*>(sR + kPart / 4 + er * kRS + 16 * eq);
+    const float4* oh = reinterpret_cast<const float4*>(sOwn + er * kRS + 16 * eq);
+    const float4* ol = reinterpret_cast<const float4*>(sOwn + kPart / 4 + er * kRS + 16 * eq);
     float acc[16];
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-      const float4 r4 = rp[c], o4 = op[c];
-      acc[4 * c] = r4.x + o4.x;
-      acc[4 * c + 1] = r4.y + o4.y;
-      acc[4 * c + 2] = r4.z + o4.z;
-      acc[4 * c + 3] = r4.w + o4.w;
+      const float4 a4 = rh[c], b4 = rl[c], c4 = oh[c], d4 = ol[c];
+      acc[4 * c] = (a4.x + c4.x) + (b4.x + d4.x);
+      acc[4 * c + 1] = (a4.y + c4.y) + (b4.y + d4.y);
+      acc[4 * c + 2] = (a4.z + c4.z) + (b4.z + d4.z);
+      acc[4 * c + 3] = (a4.w + c4.w) + (b4.w + d4.w);
     }
     const size_t base = (size_t)(chunk_row(n) + 16 * eq) * dk + i0 + ec;
     if (!REV) {
@@ -321,20 +364,29 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       if (eq == 0) sRun[er] = runq;  // suffix through the whole chunk
     }
   };
-  // epilogue of chunk n = the it-th processed (warps 4-7): wait for the peer's
+  // epilogue of chunk n = the it-th processed (warps 8-11): wait for the peer's
   // partial, then release sR back to the peer and arm bar_full for the next one
   auto finish = [&](int n, int it) {
     if (!mbar_wait(&bar_full, (uint32_t)(it & 1))) atomicExch(&g_qk_status, 1);
     epilogue(n);
     epi_sync();  // every epilogue thread has read sR
-    if (tid == 128 && it + 1 < nc) {
+    if (tid == 256 && it + 1 < nc) {
       mbar_arrive_remote(peer_empty);
-      mbar_expect_tx(&bar_full, 32 * kC * 4);
+      mbar_expect_tx(&bar_full, 2 * 32 * kC * 4);
     }
   };
 
+  // Per chunk: thread 0 issues the state update (one M = 128, N = 256 MMA per 16
+  // tokens, both copies) and commits bar_a, then dq^T / dk^T from the hi/lo copy
+  // (16 M = 128 MMAs, A in tensor memory) and, rank 0, the dA term, and commits
+  // bar_g1.  Warps 0-7 rescale the state once bar_a completes (forward: by this
+  // chunk's e^{b_last}; reverse: by the next chunk's), send this chunk's partial
+  // sums after bar_g1 and rebuild the hi/lo copy; warps 8-11 run the previous
+  // chunk's epilogue and read this chunk's epilogue factors meanwhile.
   for (int it = 0; it < nc; ++it) {
     const int n = REV ? (nc - 1 - it) : it;
+    const int nn = REV ? n - 1 : n + 1;  // the next chunk processed
+    const bool more = it + 1 < nc;
     const uint32_t par = (uint32_t)(it & 1);
     const int xbuf = it & 1;
     unsigned char* sQ = sm + kOffX + xbuf * kXBuf;
@@ -342,91 +394,102 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     unsigned char* sG = sQ + 2 * kXTile;
     const float* sQD = reinterpret_cast<const float*>(sQ + 3 * kXTile);
     const float* sE = sQD + 32 * kC;  // e^{b_last} of rows i0..i0+63
+    const float* sEn =                // the next chunk's, in the other buffer
+        reinterpret_cast<const float*>(sm + kOffX + (xbuf ^ 1) * kXBuf + 3 * kXTile + 32 * kC * 4);
     // the next chunk's tiles go to the other buffer (freed at the end of the last iteration)
-    if (tid == 0 && it + 1 < nc) issue_x(REV ? n - 1 : n + 1, xbuf ^ 1);
+    if (tid == 0 && more) issue_x(nn, xbuf ^ 1);
     if (!mbar_wait(&bar_x[xbuf], (uint32_t)((it >> 1) & 1))) atomicExch(&g_qk_status, 1);
-    if (REV) state_pass(sE);
-    fence_async_smem();
     tc_fence_before();
     __syncthreads();
-    // ---- MMA group 1
+    // ---- the chunk's MMAs
     if (tid == 0) {
       if (!mbar_wait(&bar_dv, par)) atomicExch(&g_qk_status, 1);
       tc_fence_after();
-      const uint32_t o0 = smem_u32(sDO), v0 = smem_u32(sV), h0 = smem_u32(sHi),
-                     l0 = smem_u32(sLo);
+      const uint32_t o0 = smem_u32(sDO), v0 = smem_u32(sV);
       const uint32_t x0 = smem_u32(REV ? sQ : sK);
-      constexpr uint32_t idT = idesc_bf16(64, 64, true, false);    // copy (x) do or v
+      // forward: S += K~^T v    reverse: dS += Q~^T do   (M = 128: rows 0-63 and 64-127
+      // both read the [t][i] tile (block stride 0), N = 256 j, K = 64 t; B = the
+      // [t][j] tile read MN-major)
+      constexpr uint32_t idU = idesc_bf16(128, 256, true, true);
+      const uint32_t u0 = REV ? o0 : v0;
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        umma_bf16(tmem + kColS, sdesc_sw128(x0 + kk * 2048, 0, 1024),
+                  sdesc_sw128(u0 + kk * 2048, 8192, 1024), idU, 1u);
+      umma_commit(&bar_a);
+      // forward: dq^T = S do^T    reverse: dk^T = (e^{b_last} dS) v^T, hi and lo parts
+      // (M = 128 hi/lo rows, A = the copy in tensor memory; N = 64, K = 256 j)
+      constexpr uint32_t idT = idesc_bf16(128, 64, false, false);
+      const uint32_t z0 = REV ? v0 : o0;
 #pragma unroll 4
-      for (int m = 0; m < kDVH / 16; ++m) {  // K = this CTA's d_v half, 16 per step
+      for (int m = 0; m < kDVH / 16; ++m) {
         const uint32_t koff = (uint32_t)((m >> 2) * 8192 + (m & 3) * 32);
-        const uint64_t yd = sdesc_sw128((REV ? v0 : o0) + koff, 16, 1024);
-        const uint64_t hd = sdesc_sw128(h0 + m * 2048, 8192, 1024);
-        const uint64_t ld = sdesc_sw128(l0 + m * 2048, 8192, 1024);
-        // forward: dq^T = S do^T     reverse: dk^T = (e^{b_last} dS) v^T   (M = 64 i, N = 64)
-        umma_bf16(tmem + kColAcc, hd, yd, idT, m ? 1u : 0u);
-        umma_bf16(tmem + kColAcc, ld, yd, idT, 1u);
+        umma_bf16_ta(tmem + kColAcc, tmem + kColHL + m * 8, sdesc_sw128(z0 + koff, 16, 1024),
+                     idT, m ? 1u : 0u);
       }
-      // rank 0: forward dq^T += K~^T dA^T ; reverse dk^T += Q~^T dA   (M = 64 i, N = 64, K = 64)
+      // rank 0: forward K~^T dA^T ; reverse Q~^T dA into rows 0-63 (M = 128: the A
+      // operand's second 64-row block is the zero tile; N = 64, K = 64)
       if (rank == 0) {
         const uint32_t p0 = smem_u32(sP);
-        constexpr uint32_t id2 = idesc_bf16(64, 64, true, REV);
+        const uint32_t zoff = smem_u32(sm + kOffZero) - x0;  // block stride to the zero tile
+        constexpr uint32_t id2 = idesc_bf16(128, 64, true, REV);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t xd = sdesc_sw128(x0 + kk * 2048, 8192, 1024);
+          const uint64_t xd = sdesc_sw128(x0 + kk * 2048, zoff, 1024);
           const uint64_t pd = REV ? sdesc_sw128(p0 + kk * 2048, 8192, 1024)
                                   : sdesc_sw128(p0 + kk * 32, 16, 1024);
           umma_bf16(tmem + kColAcc, xd, pd, id2, 1u);
         }
       }
-      // forward: S^T_g += v_g^T K~    reverse: dS^T_g += do_g^T Q~   (M = 128 j, N = 64 i, K = 64)
-      constexpr uint32_t idS = idesc_bf16(128, 64, true, true);
-      const uint32_t y0 = REV ? o0 : v0;
-#pragma unroll
-      for (int g = 0; g < 2; ++g)
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t yd = sdesc_sw128(y0 + g * 16384 + kk * 2048, 8192, 1024);
-          const uint64_t xd = sdesc_sw128(x0 + kk * 2048, 8192, 1024);
-          umma_bf16(tmem + g * 64, yd, xd, idS, 1u);
-        }
       umma_commit(&bar_g1);
     }
-    // ---- warps 4-7, while the tensor cores run group 1: the previous chunk's
-    //      epilogue, then this chunk's epilogue factors
-    if (epi) {
-      if (it > 0) finish(REV ? n + 1 : n - 1, it - 1);
-      prefetch(sQ, sK, sG, sQD);
-    }
-    if (!mbar_wait(&bar_g1, par)) atomicExch(&g_qk_status, 1);
-    tc_fence_after();
-    if (tid == 0 && it + 1 < nc) issue_dv(REV ? n - 1 : n + 1);  // do, v, dA buffers are free
-    if (!REV) state_pass(sE);  // forward: post-scale and copy for the next chunk
-    // ---- partial sums of this chunk: the peer's rows into the peer's sR
-    //      (st.async, completing on the peer's bar_full), mine into sOwn
-    if (warp < 4) {
-      float a[64];
-      tmem_ld32(tmem + lane_off + kColAcc, a);
-      tmem_ld32(tmem + lane_off + kColAcc + 32, a + 32);
-      tmem_ld_wait();
-      if (rowt) {
+    if (!epi) {
+      // ---- warps 0-7: rescale the state while dq^T / dk^T run
+      if (!mbar_wait(&bar_a, par)) atomicExch(&g_qk_status, 1);
+      tc_fence_after();
+      if (more) {
+        if (!REV) {
+          scale_state(sE);
+        } else {
+          if (!mbar_wait(&bar_x[xbuf ^ 1], (uint32_t)(((it + 1) >> 1) & 1)))
+            atomicExch(&g_qk_status, 1);
+          scale_state(sEn);
+        }
+      }
+      if (!mbar_wait(&bar_g1, par)) atomicExch(&g_qk_status, 1);
+      tc_fence_after();
+      if (tid == 0 && more) issue_dv(nn);  // do, v, dA buffers are free
+      // ---- partial sums of this chunk, this thread's part of row ii, tokens
+      //      [32 ch, 32 ch + 32): the peer's rows into the peer's buffers
+      //      (st.async, completing on the peer's bar_full), mine into sOwn
+      {
+        float a[32];
+        tmem_ld32(tmem + lane_off + kColAcc + 32 * ch, a);
+        tmem_ld_wait();
+        const int off = part * (kPart / 4) + (ii & 31) * kRS + 32 * ch;
         if (owned) {
-          float4* dst = reinterpret_cast<float4*>(sOwn + (ii & 31) * kRS);
+          float4* dst = reinterpret_cast<float4*>(sOwn + off);
 #pragma unroll
-          for (int c = 0; c < 16; ++c)
+          for (int c = 0; c < 8; ++c)
             dst[c] = make_float4(a[4 * c], a[4 * c + 1], a[4 * c + 2], a[4 * c + 3]);
         } else {
           // the peer has read the partial of the previous chunk
           if (!mbar_wait(&bar_empty, par ^ 1u)) atomicExch(&g_qk_status, 1);
-          const uint32_t dst = map_to_rank(smem_u32(sR + (ii & 31) * kRS), peer);
+          const uint32_t dst = map_to_rank(smem_u32(sR + off), peer);
 #pragma unroll
-          for (int c = 0; c < 16; ++c)
+          for (int c = 0; c < 8; ++c)
             st_async_v4(dst + c * 16, a[4 * c], a[4 * c + 1], a[4 * c + 2], a[4 * c + 3],
                         peer_full);
         }
       }
+      // ---- the next chunk's hi/lo copy
+      if (more) make_copy();
+    } else {
+      // ---- warps 8-11: the previous chunk's epilogue, then this chunk's factors
+      if (it > 0) finish(REV ? n + 1 : n - 1, it - 1);
+      prefetch(sQ, sK, sG, sQD);
+      if (!mbar_wait(&bar_g1, par)) atomicExch(&g_qk_status, 1);
     }
-    fence_async_smem();  // forward: the state copy, read by the next group 1
     tc_fence_before();
     __syncthreads();
   }
@@ -434,7 +497,7 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   tc_fence_before();
   __syncthreads();
   cluster_sync();  // no st.async or remote arrive is still in flight to either CTA
-  if (warp == 0) tmem_dealloc(tmem, 256);
+  if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
 template <bool REV>

@@ -82,7 +82,12 @@ BATCHED_FWDBWD = Workload("batched_fwdbwd_B8_T32768_P2", B=8, H=4, T=32768, dk=2
                           x_mean=2.0, s0_scale=0.1, bwd=True)
 
 WORKLOADS = [TINY_F32, GLA1B_FWD, SEG_FWD, LONG_FWDBWD, BATCHED_FWDBWD]
-BY_NAME = {w.name: w for w in WORKLOADS}
+
+# Small case of the throughput workload for ncu captures: the same kernels and
+# shapes per token, 1/32 of the tokens (one wave of CTAs, inputs 470 MB > L2).
+PROFILE_FWDBWD = LONG_FWDBWD.replace(name="profile_fwdbwd_T32768_P8", T=32768, P=8)
+
+BY_NAME = {w.name: w for w in WORKLOADS + [PROFILE_FWDBWD]}
 
 
 def make_inputs(w: Workload, device="cpu", seed: int | None = None):
