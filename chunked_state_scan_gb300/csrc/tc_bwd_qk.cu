@@ -91,8 +91,10 @@ constexpr int kRS = kC + 4;                      // row stride of the partial su
 constexpr int kPart = 32 * kRS * 4;              // one [32 rows][kRS] fp32 partial-sum buffer
 // partial sums for my 32 rows: the peer's high and low parts, then my own
 constexpr int kOffR = kOffP + kC * kC * 2;       // peer: hi at +0, lo at +kPart
-constexpr int kOffOwn = kOffR + 2 * kPart;       // own:  hi at +0, lo at +kPart
-constexpr int kOffZero = kOffOwn + 2 * kPart;    // zero tile [64][64] bf16 (dA term's A rows 64-127)
+// own partials, double-buffered by chunk parity (written in a chunk's iteration,
+// read by its epilogue in the next one): [parity][hi, lo]
+constexpr int kOffOwn = kOffR + 2 * kPart;
+constexpr int kOffZero = kOffOwn + 4 * kPart;    // zero tile [64][64] bf16 (dA term's A rows 64-127)
 constexpr int kOffGq = kOffZero + kC * kC * 2;   // sums of log_alpha per 16 tokens [4][32]
 constexpr int kOffQS = kOffGq + 1024;            // reverse: sums of dg terms per 16 tokens [4][32]
 constexpr int kOffRun = kOffQS + 1024;           // reverse: dg suffix carried per row [32]
@@ -319,11 +321,12 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   };
   // outputs of chunk n from the four partial sums (peer's and own, high and low
   // parts)
-  auto epilogue = [&](int n) {
+  auto epilogue = [&](int n, int it) {
+    const float* own = sOwn + (it & 1) * (2 * kPart / 4);
     const float4* rh = reinterpret_cast<const float4*>(sR + er * kRS + 16 * eq);
     const float4* rl = reinterpret_cast<const float4*>(sR + kPart / 4 + er * kRS + 16 * eq);
-    const float4* oh = reinterpret_cast<const float4*>(sOwn + er * kRS + 16 * eq);
-    const float4* ol = reinterpret_cast<const float4*>(sOwn + kPart / 4 + er * kRS + 16 * eq);
+    const float4* oh = reinterpret_cast<const float4*>(own + er * kRS + 16 * eq);
+    const float4* ol = reinterpret_cast<const float4*>(own + kPart / 4 + er * kRS + 16 * eq);
     float acc[16];
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
@@ -368,7 +371,7 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   // partial, then release sR back to the peer and arm bar_full for the next one
   auto finish = [&](int n, int it) {
     if (!mbar_wait(&bar_full, (uint32_t)(it & 1))) atomicExch(&g_qk_status, 1);
-    epilogue(n);
+    epilogue(n, it);
     epi_sync();  // every epilogue thread has read sR
     if (tid == 256 && it + 1 < nc) {
       mbar_arrive_remote(peer_empty);
@@ -468,7 +471,7 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         tmem_ld_wait();
         const int off = part * (kPart / 4) + (ii & 31) * kRS + 32 * ch;
         if (owned) {
-          float4* dst = reinterpret_cast<float4*>(sOwn + off);
+          float4* dst = reinterpret_cast<float4*>(sOwn + (it & 1) * (2 * kPart / 4) + off);
 #pragma unroll
           for (int c = 0; c < 8; ++c)
             dst[c] = make_float4(a[4 * c], a[4 * c + 1], a[4 * c + 2], a[4 * c + 3]);
