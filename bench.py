@@ -387,6 +387,31 @@ def main(argv=None):
     elapsed_max = max_over_ranks(elapsed, world)
     value, ms_step = aggregate(elapsed_max, w.tokens, args.steps, world)
 
+    # ---- the overlap instrument: the same steps with every kernel on one stream.
+    # The passes that do not depend on the segment scan (decay, scores, score
+    # gradient) run on a second stream by default; hidden = the share of their
+    # time that the overlap removed from the step.
+    overlap = None
+    if path == "tc":
+        lib.zeco_set_overlap.argtypes = [ctypes.c_int]
+        lib.zeco_set_overlap(0)
+        step(x)
+        torch.cuda.synchronize(dev)
+        s0 = torch.cuda.Event(enable_timing=True)
+        s1 = torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for _ in range(args.steps):
+            step(x)
+        s1.record(stream)
+        torch.cuda.synchronize(dev)
+        lib.zeco_set_overlap(1)
+        serial_ms = s0.elapsed_time(s1) / args.steps
+        aux_ms = sum(v for k, v in kern_ms.items() if canonical_kernel(k) in ("decay", "A", "dA"))
+        overlap = {"serial_ms": serial_ms, "overlapped_ms": ms_step, "aux_stream_ms": aux_ms,
+                   "hidden_frac": (serial_ms - ms_step) / aux_ms if aux_ms > 0 else None,
+                   "note": "decay pass, masked scores and score gradient on a second stream, "
+                           "concurrent with the segment-state pass and the scan"}
+
     # ---- roofline of the dominant kernel and of the whole step
     peaks, peak_kind = load_peaks()
     hbm_peak = float(peaks["hbm_gbs"])
@@ -421,7 +446,7 @@ def main(argv=None):
                               "frac": t_roof / step_s,
                               "note": "ZeCO two-pass algorithmic bytes/flops per step vs "
                                       f"{peak_kind} peaks"},
-        "kernels_ms": kern_ms, "scan_share": scan_ms / sum(kern_ms.values()),
+        "kernels_ms": kern_ms, "overlap": overlap, "scan_share": scan_ms / sum(kern_ms.values()),
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
     }

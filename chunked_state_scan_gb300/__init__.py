@@ -57,6 +57,8 @@ def load_library(path: str = LIB_PATH):
             vp, sz, sp = ctypes.c_void_p, ctypes.c_size_t, ctypes.POINTER(ZecoShape)
             lib.zeco_gla_saved_bytes.argtypes = [sp]
             lib.zeco_gla_saved_bytes.restype = sz
+            lib.zeco_set_overlap.argtypes = [ctypes.c_int]
+            lib.zeco_set_overlap.restype = ctypes.c_int
             lib.zeco_gla_workspace_bytes.argtypes = [sp, ctypes.c_int]
             lib.zeco_gla_workspace_bytes.restype = sz
             lib.zeco_gla_fwd.argtypes = [sp] + [vp] * 8 + [vp, sz, vp]
@@ -99,6 +101,11 @@ def saved_bytes(shape: ZecoShape) -> int:
 
 def workspace_bytes(shape: ZecoShape, bwd: bool) -> int:
     return load_library().zeco_gla_workspace_bytes(ctypes.byref(shape), int(bwd))
+
+
+def set_overlap(on: bool) -> None:
+    """Run the scan-independent passes on a second stream (default) or not."""
+    load_library().zeco_set_overlap(int(bool(on)))
 
 
 def resolve_path(shape: ZecoShape) -> str:

@@ -80,6 +80,8 @@ WsPlan plan_ws(const Dims& d, int path, bool bwd) {
 
 namespace zeco {
 
+bool prof_active() { return g_prof.events != nullptr; }
+
 void prof_begin(cudaStream_t st) {
   if (!g_prof.events || g_prof.count >= g_prof.cap) return;
   if (g_prof.count == 0) {

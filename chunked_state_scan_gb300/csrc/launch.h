@@ -7,6 +7,19 @@
 
 namespace zeco {
 
+// ---- auxiliary stream for the scan-independent passes (overlap.cu) -----
+struct Fork {
+  cudaStream_t aux;   // where the forked kernels go (the caller's stream when off)
+  cudaEvent_t ev[2];  // recorded on aux by fork_mark, waited on by fork_join
+  bool on;
+};
+// Forks from st (aux waits for st's work so far); off when overlap is disabled.
+Fork fork_begin(cudaStream_t st);
+cudaError_t fork_mark(const Fork& f, int i);
+cudaError_t fork_join(const Fork& f, cudaStream_t st, int i);
+// Whether per-kernel profiling marks are being recorded (api.cu).
+bool prof_active();
+
 // ---- segment scans (scan.cu) ------------------------------------------
 cudaError_t launch_seg_scan_fwd(const Dims& d, float* S_in, const float* gamma, const float* S0,
                                 float* S_final, cudaStream_t st);

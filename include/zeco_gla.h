@@ -185,6 +185,23 @@ int zeco_set_profile_events(void *const *events, int n);
 int zeco_profile_event_count(void);
 const char *zeco_profile_kernel_name(int i);
 
+/*
+ * Overlap of the scan-independent passes (on by default).  The pages' central
+ * claim is that the exchange of segment states (the All-Scan) hides behind
+ * work that does not need it (ZeCO, Pith review, "What carries the argument").
+ * On the tensor-core path the passes that build the decay-weighted operands
+ * and the intra-chunk scores (and, backward, their gradient) do not depend on
+ * the segment scan; with overlap on they run on an auxiliary stream
+ * concurrently with the segment-state pass and the scan (and, backward, the dv
+ * sweep).  The call forks from and joins back into its `stream` with events, so
+ * all its work stays ordered on `stream` and it can be captured into a CUDA
+ * graph.  The auxiliary stream and three events are created on the first such
+ * call of each host thread on each device and destroyed when the thread exits.
+ * on = 0 runs everything on `stream`; active profiling events (above) do too.
+ * Process-wide; returns ZECO_OK.
+ */
+int zeco_set_overlap(int on);
+
 /* The path zeco_gla_fwd / zeco_gla_bwd would run for this shape
  * (ZECO_PATH_SIMT or ZECO_PATH_TC), or a negative ZECO_ERR_* code. */
 int zeco_gla_resolve_path(const zeco_shape *shape);

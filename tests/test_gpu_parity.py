@@ -142,3 +142,19 @@ def test_bf16_tensor_core_path_shapes(z, B, H, T, dk, dv, P, K):
                               qk_scale=1 / 16, s0_scale=0.2)
     errs = parity.compare_full(z, x, P, K, 64, "bf16", path="tc")
     _assert(errs, "bf16", f"tc B{B} H{H} T{T} dk{dk} dv{dv} P{P}")
+
+
+def test_overlap_stream_gives_identical_results(z):
+    # the scan-independent passes on a second stream (default) or all on one
+    # stream: same kernels, same inputs, so bit-identical outputs
+    w = workloads.LONG_FWDBWD.replace(T=16384, P=4)
+    x = workloads.make_inputs(w)
+    lib = z.load_library()
+    a = parity.run_gpu(z, x, w.P, w.K, w.C)
+    lib.zeco_set_overlap(0)
+    try:
+        b = parity.run_gpu(z, x, w.P, w.K, w.C)
+    finally:
+        lib.zeco_set_overlap(1)
+    for n in ("o", "S_final", "dq", "dk", "dv", "dlog_alpha", "dS0"):
+        assert torch.equal(a[n], b[n]), n
