@@ -183,3 +183,44 @@ def boundary_states_cols(q, k, v, log_alpha, S0, P, cols, nthreads=None):
         S[..., cols] = sf
         out[:, :, p + 1] = sf
     return out
+
+
+# ---- other decay forms.  The ZeCO pages leave linear attention with other
+# decays to future work (ZeCO: Limitations); the LASP page's linear attention
+# has none.  A per-token scalar decay multiplies every d_k row of the state by
+# the same alpha_t (RetNet / Lightning-style); "none" is alpha = 1.  Both are the
+# diagonal recurrence with log_alpha[t, i] = g_t (resp. 0), and the gradient
+# with respect to a scalar g_t is the sum over i of the diagonal one (chain
+# rule through the broadcast).  Pinned by a closed form (constant scalar
+# decay = causal attention weighted by e^{c (t - s)}), by the alpha = 1 causal
+# form and by central finite differences with respect to the scalar g.
+
+DECAY_DIAG, DECAY_SCALAR, DECAY_NONE = 0, 1, 2
+
+
+def expand_log_alpha(log_alpha, decay, shape):
+    """The [B,H,T,dk] log-decay of a decay form (log_alpha [B,H,T] when scalar,
+    ignored when none)."""
+    if decay == DECAY_DIAG:
+        return _f64(log_alpha)
+    B, H, T, dk = shape
+    if decay == DECAY_SCALAR:
+        return np.ascontiguousarray(np.broadcast_to(_f64(log_alpha)[..., None], (B, H, T, dk)))
+    return np.zeros((B, H, T, dk))
+
+
+def gla_fwd_decay(q, k, v, log_alpha, S0, decay, cols=None, nthreads=None):
+    """Forward of a decay form: (o, S_final)."""
+    return gla_fwd(q, k, v, expand_log_alpha(log_alpha, decay, q.shape), S0, cols, nthreads)
+
+
+def gla_bwd_decay(q, k, v, log_alpha, S0, do, dS_final, decay, nthreads=None):
+    """Backward of a decay form: dlog_alpha is [B,H,T] for a scalar decay and
+    None without decay."""
+    r = gla_bwd(q, k, v, expand_log_alpha(log_alpha, decay, q.shape), S0, do, dS_final,
+                nthreads=nthreads)
+    if decay == DECAY_SCALAR:
+        r["dlog_alpha"] = r["dlog_alpha"].sum(axis=-1)
+    elif decay == DECAY_NONE:
+        r["dlog_alpha"] = None
+    return r

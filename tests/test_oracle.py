@@ -289,3 +289,65 @@ def test_boundary_state_columns_match_full_states():
     cols = [5, 2]
     part = oracle.boundary_states_cols(q, k, v, g, S0, P, cols)
     np.testing.assert_allclose(part, full[..., cols], rtol=1e-13, atol=1e-13)
+
+
+# ------------------------------------------------------------ other decay forms
+
+
+def test_constant_scalar_decay_is_exponentially_weighted_causal_attention():
+    # alpha_t = e^c for every token and every d_k row: S_t = sum_{s<=t} e^{c (t-s)} k_s^T v_s
+    # (+ e^{c (t+1)} S0), so o = ((Q K^T) .* D) V + (e^{c (t+1)} q_t) S0 with
+    # D[t, s] = e^{c (t - s)} for s <= t and 0 above the diagonal.
+    B, H, T, dk, dv = 1, 2, 40, 5, 3
+    q, k, v, _, S0, _, _ = _rand_inputs(11, B, H, T, dk, dv)
+    c = -0.07
+    g = np.full((B, H, T), c)
+    o, sf = oracle.gla_fwd_decay(q, k, v, g, S0, oracle.DECAY_SCALAR)
+    t = np.arange(T)
+    D = np.where(t[:, None] >= t[None, :], np.exp(c * (t[:, None] - t[None, :])), 0.0)
+    for b in range(B):
+        for h in range(H):
+            ref = ((q[b, h] @ k[b, h].T) * D) @ v[b, h]
+            ref += (np.exp(c * (t + 1))[:, None] * q[b, h]) @ S0[b, h]
+            assert np.abs(o[b, h] - ref).max() <= 1e-12 * max(1.0, np.abs(ref).max())
+            sref = (np.exp(c * (T - 1 - t))[:, None] * k[b, h]).T @ v[b, h] + np.exp(c * T) * S0[b, h]
+            assert np.abs(sf[b, h] - sref).max() <= 1e-12 * max(1.0, np.abs(sref).max())
+
+
+def test_no_decay_is_causal_linear_attention():
+    B, H, T, dk, dv = 1, 1, 30, 4, 6
+    q, k, v, _, S0, _, _ = _rand_inputs(12, B, H, T, dk, dv)
+    o, sf = oracle.gla_fwd_decay(q, k, v, None, S0, oracle.DECAY_NONE)
+    M = np.tril(np.ones((T, T)))
+    ref = ((q[0, 0] @ k[0, 0].T) * M) @ v[0, 0] + q[0, 0] @ S0[0, 0]
+    assert np.abs(o[0, 0] - ref).max() <= 1e-12 * np.abs(ref).max()
+    assert np.abs(sf[0, 0] - (k[0, 0].T @ v[0, 0] + S0[0, 0])).max() <= 1e-12 * 10
+
+
+def test_scalar_decay_gradient_matches_central_differences():
+    B, H, T, dk, dv = 1, 2, 10, 3, 4
+    q, k, v, _, S0, do, dSf = _rand_inputs(13, B, H, T, dk, dv)
+    g = -np.abs(_rng(14).standard_normal((B, H, T))) * 0.3
+    gr = oracle.gla_bwd_decay(q, k, v, g, S0, do, dSf, oracle.DECAY_SCALAR)
+    assert gr["dlog_alpha"].shape == (B, H, T)
+
+    def loss(gs):
+        o, sf = oracle.gla_fwd_decay(q, k, v, gs, S0, oracle.DECAY_SCALAR, nthreads=1)
+        return float(np.sum(o * do) + np.sum(sf * dSf))
+
+    h = 1e-6
+    fd = np.zeros_like(g)
+    for idx in np.ndindex(*g.shape):
+        old = g[idx]
+        g[idx] = old + h
+        lp = loss(g)
+        g[idx] = old - h
+        lm = loss(g)
+        g[idx] = old
+        fd[idx] = (lp - lm) / (2 * h)
+    scale = max(1.0, np.abs(gr["dlog_alpha"]).max())
+    assert np.abs(fd - gr["dlog_alpha"]).max() <= 1e-7 * scale
+    # the other gradients are those of the broadcast diagonal decay
+    full = oracle.gla_bwd(q, k, v, np.repeat(g[..., None], dk, axis=-1), S0, do, dSf)
+    for n in ("dq", "dk", "dv", "dS0"):
+        assert np.array_equal(gr[n], full[n]), n
