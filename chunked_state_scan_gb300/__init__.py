@@ -31,7 +31,7 @@ class ZecoShape(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int64), ("H", ctypes.c_int64), ("T", ctypes.c_int64),
                 ("dk", ctypes.c_int64), ("dv", ctypes.c_int64), ("P", ctypes.c_int32),
                 ("K", ctypes.c_int32), ("C", ctypes.c_int32), ("dtype", ctypes.c_int32),
-                ("path", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("path", ctypes.c_int32), ("decay", ctypes.c_int32)]
 
 
 class ZecoError(RuntimeError):
@@ -73,12 +73,18 @@ def load_library(path: str = LIB_PATH):
     return _lib
 
 
-def make_shape(B, H, T, dk, dv, P, K, C, dtype, path="auto") -> ZecoShape:
+# decay forms: per d_k row (gated linear attention), one per token, none
+DECAY_DIAG, DECAY_SCALAR, DECAY_NONE = 0, 1, 2
+_DECAYS = {"diag": DECAY_DIAG, "scalar": DECAY_SCALAR, "none": DECAY_NONE}
+
+
+def make_shape(B, H, T, dk, dv, P, K, C, dtype, path="auto", decay="diag") -> ZecoShape:
     if isinstance(dtype, torch.dtype):
         dt = ZECO_BF16 if dtype == torch.bfloat16 else ZECO_F32
     else:
         dt = ZECO_BF16 if dtype in ("bf16", ZECO_BF16) else ZECO_F32
-    return ZecoShape(B, H, T, dk, dv, P, K, C, dt, _PATHS.get(path, path), 0)
+    return ZecoShape(B, H, T, dk, dv, P, K, C, dt, _PATHS.get(path, path),
+                     _DECAYS.get(decay, decay))
 
 
 def _check(rc):
@@ -123,21 +129,22 @@ def _on(stream):
     return contextlib.nullcontext()
 
 
-def _shape_of(q, v, P, K, C, path):
+def _shape_of(q, v, P, K, C, path, decay="diag"):
     B, H, T, dk = q.shape
-    return make_shape(B, H, T, dk, v.shape[-1], P, K, C, q.dtype, path)
+    return make_shape(B, H, T, dk, v.shape[-1], P, K, C, q.dtype, path, decay)
 
 
 def zeco_gla_fwd(q, k, v, log_alpha, S0=None, *, P, K, C, path="auto", o=None, S_final=None,
-                 saved=None, workspace=None, stream=None, want_S_final=True):
+                 saved=None, workspace=None, stream=None, want_S_final=True, decay="diag"):
     """Forward through the C ABI.  Returns (o, S_final or None, saved).
 
-    q, k, log_alpha: [B,H,T,dk]; v: [B,H,T,dv] (fp32 or bf16, CUDA, contiguous);
+    q, k: [B,H,T,dk]; v: [B,H,T,dv] (fp32 or bf16, CUDA, contiguous); log_alpha:
+    [B,H,T,dk] (decay "diag"), [B,H,T] ("scalar") or None ("none").
     S0: [B,H,dk,dv] fp32 or None (zeros).  ``saved`` must be passed to the backward.
     ``workspace``: a uint8 buffer of at least workspace_bytes(shape, False) bytes,
     allocated here when None.
     """
-    shape = _shape_of(q, v, P, K, C, path)
+    shape = _shape_of(q, v, P, K, C, path, decay)
     dev = q.device
     nws = workspace_bytes(shape, False)
     with _on(stream):
@@ -159,15 +166,17 @@ def zeco_gla_fwd(q, k, v, log_alpha, S0=None, *, P, K, C, path="auto", o=None, S
 
 
 def zeco_gla_bwd(q, k, v, log_alpha, saved, do, dS_final=None, *, P, K, C, path="auto",
-                 grads=None, workspace=None, stream=None, want_dS0=True):
-    """Backward through the C ABI.  Returns dict(dq, dk, dv, dlog_alpha, dS0)."""
-    shape = _shape_of(q, v, P, K, C, path)
+                 grads=None, workspace=None, stream=None, want_dS0=True, decay="diag"):
+    """Backward through the C ABI.  Returns dict(dq, dk, dv, dlog_alpha, dS0);
+    dlog_alpha has log_alpha's shape and is None without decay."""
+    shape = _shape_of(q, v, P, K, C, path, decay)
     dev = q.device
     nws = workspace_bytes(shape, True)
     with _on(stream):
         if grads is None:
             grads = dict(dq=torch.empty_like(q), dk=torch.empty_like(k),
-                         dv=torch.empty_like(v), dlog_alpha=torch.empty_like(log_alpha))
+                         dv=torch.empty_like(v),
+                         dlog_alpha=None if log_alpha is None else torch.empty_like(log_alpha))
             if want_dS0:
                 grads["dS0"] = torch.empty(q.shape[0], q.shape[1], q.shape[-1], v.shape[-1],
                                            dtype=torch.float32, device=dev)

@@ -28,6 +28,7 @@ int check_shape(const zeco_shape* s, Dims* d) {
     return ZECO_ERR_ARG;
   if (s->dtype != ZECO_F32 && s->dtype != ZECO_BF16) return ZECO_ERR_ARG;
   if (s->path < ZECO_PATH_AUTO || s->path > ZECO_PATH_TC) return ZECO_ERR_ARG;
+  if (s->decay < ZECO_DECAY_DIAG || s->decay > ZECO_DECAY_NONE) return ZECO_ERR_ARG;
   if (s->T % s->P != 0 || s->dk % s->K != 0) return ZECO_ERR_ARG;
   const int64_t L = s->T / s->P;
   if (L % s->C != 0) return ZECO_ERR_ARG;
@@ -45,6 +46,7 @@ int check_shape(const zeco_shape* s, Dims* d) {
   d->C = s->C;
   d->L = L;
   d->bf16 = s->dtype == ZECO_BF16;
+  d->decay = s->decay;
   return ZECO_OK;
 }
 
@@ -57,11 +59,14 @@ int resolve(const zeco_shape* s, const Dims& d) {
   return ZECO_PATH_SIMT;
 }
 
-// Scratch layout of one call: the backward's own buffers (bwd only) followed,
-// on the tensor-core path, by the decay pass's Q~, K~ and e^{b_last}.
+// Scratch layout of one call: the backward's own buffers (bwd only), then, on
+// the tensor-core path, the operands computed once per call (decay_layout),
+// then, for the SCALAR / NONE decay forms, the broadcast log-decay and its
+// per-row gradient (forms_layout).
 struct WsPlan {
   zeco::BwdWsLayout bwd;
   zeco::DecayLayout decay;
+  zeco::FormsLayout forms;
   bool uses_decay;
   size_t total;
 };
@@ -72,7 +77,8 @@ WsPlan plan_ws(const Dims& d, int path, bool bwd) {
   const size_t base = bwd ? w.bwd.total : 0;
   w.uses_decay = path == ZECO_PATH_TC && zeco::tc_uses_decay(d);
   w.decay = zeco::decay_layout(d, base, bwd && zeco::tc_uses_dA(d));
-  w.total = w.uses_decay ? w.decay.total : base;
+  w.forms = zeco::forms_layout(d, w.uses_decay ? w.decay.total : base, bwd);
+  w.total = w.forms.total;
   return w;
 }
 
@@ -142,10 +148,11 @@ int zeco_gla_fwd(const zeco_shape* shape, const void* q, const void* k, const vo
   Dims d;
   int rc = check_shape(shape, &d);
   if (rc != ZECO_OK) return rc;
-  const void* req[] = {q, k, v, log_alpha, o, saved};
+  const void* req[] = {q, k, v, o, saved};
   for (const void* p : req)
     if (!p || !aligned16(p)) return ZECO_ERR_ARG;
   if ((S0 && !aligned16(S0)) || (S_final && !aligned16(S_final))) return ZECO_ERR_ARG;
+  if (d.decay != ZECO_DECAY_NONE && (!log_alpha || !aligned16(log_alpha))) return ZECO_ERR_ARG;
   const int path = resolve(shape, d);
   if (path < 0) return path;
   const WsPlan wp = plan_ws(d, path, false);
@@ -156,11 +163,17 @@ int zeco_gla_fwd(const zeco_shape* shape, const void* q, const void* k, const vo
   float* gamma = (float*)((char*)saved + sl.gamma_off);
   cudaStream_t st = (cudaStream_t)stream;
   zeco::prof_begin(st);
-  cudaError_t e = path == ZECO_PATH_TC
-                      ? zeco::tc_forward(d, q, k, v, log_alpha, S0, o, S_final, S_in, gamma,
-                                         wp.decay, workspace, st)
-                      : zeco::simt_forward(d, q, k, v, log_alpha, S0, o, S_final, S_in, gamma,
-                                           st);
+  cudaError_t e = cudaSuccess;
+  const void* g = log_alpha;
+  if (d.decay != ZECO_DECAY_DIAG) {
+    g = (char*)workspace + wp.forms.gx_off;
+    e = zeco::launch_expand_log_alpha(d, log_alpha, (void*)g, st);
+  }
+  if (e == cudaSuccess)
+    e = path == ZECO_PATH_TC
+            ? zeco::tc_forward(d, q, k, v, g, S0, o, S_final, S_in, gamma, wp.decay, workspace,
+                               st)
+            : zeco::simt_forward(d, q, k, v, g, S0, o, S_final, S_in, gamma, st);
   return e == cudaSuccess ? ZECO_OK : ZECO_ERR_CUDA;
 }
 
@@ -171,9 +184,12 @@ int zeco_gla_bwd(const zeco_shape* shape, const void* q, const void* k, const vo
   Dims d;
   int rc = check_shape(shape, &d);
   if (rc != ZECO_OK) return rc;
-  const void* req[] = {q, k, v, log_alpha, saved, d_o, dq, dk, dv, dlog_alpha, workspace};
+  const void* req[] = {q, k, v, saved, d_o, dq, dk, dv, workspace};
   for (const void* p : req)
     if (!p || !aligned16(p)) return ZECO_ERR_ARG;
+  if (d.decay != ZECO_DECAY_NONE && (!log_alpha || !aligned16(log_alpha) || !dlog_alpha ||
+                                     !aligned16(dlog_alpha)))
+    return ZECO_ERR_ARG;
   if ((dS_final && !aligned16(dS_final)) || (dS0 && !aligned16(dS0))) return ZECO_ERR_ARG;
   const int path = resolve(shape, d);
   if (path < 0) return path;
@@ -188,12 +204,22 @@ int zeco_gla_bwd(const zeco_shape* shape, const void* q, const void* k, const vo
   float* qdq = (float*)((char*)workspace + wl.qdq_off);
   cudaStream_t st = (cudaStream_t)stream;
   zeco::prof_begin(st);
-  cudaError_t e =
-      path == ZECO_PATH_TC
-          ? zeco::tc_backward(d, q, k, v, log_alpha, S_in, gamma, d_o, dS_final, dq, dk, dv,
-                              dlog_alpha, dS0, D, carry, qdq, wp.decay, workspace, st)
-          : zeco::simt_backward(d, q, k, v, log_alpha, S_in, gamma, d_o, dS_final, dq, dk, dv,
-                                dlog_alpha, dS0, D, carry, qdq, st);
+  cudaError_t e = cudaSuccess;
+  const void* g = log_alpha;
+  void* dg = dlog_alpha;
+  if (d.decay != ZECO_DECAY_DIAG) {
+    g = (char*)workspace + wp.forms.gx_off;
+    dg = (char*)workspace + wp.forms.dgx_off;
+    e = zeco::launch_expand_log_alpha(d, log_alpha, (void*)g, st);
+  }
+  if (e == cudaSuccess)
+    e = path == ZECO_PATH_TC
+            ? zeco::tc_backward(d, q, k, v, g, S_in, gamma, d_o, dS_final, dq, dk, dv, dg, dS0, D,
+                                carry, qdq, wp.decay, workspace, st)
+            : zeco::simt_backward(d, q, k, v, g, S_in, gamma, d_o, dS_final, dq, dk, dv, dg,
+                                  dS0, D, carry, qdq, st);
+  if (e == cudaSuccess && d.decay == ZECO_DECAY_SCALAR)
+    e = zeco::launch_reduce_dlog_alpha(d, dg, dlog_alpha, st);
   return e == cudaSuccess ? ZECO_OK : ZECO_ERR_CUDA;
 }
 

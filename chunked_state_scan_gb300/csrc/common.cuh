@@ -15,6 +15,7 @@ struct Dims {
   int P, K, C;
   int64_t L;  // tokens per segment
   bool bf16;
+  int decay;  // zeco_decay
 };
 
 // Byte layout of the `saved` buffer and the backward workspace.
@@ -64,6 +65,20 @@ inline BwdWsLayout bwd_ws_layout(const Dims& d) {
   w.qdq_off = align_up(w.carry_off + bh * d.P * d.dk * sizeof(float), 256);
   w.total = align_up(w.qdq_off + bh * d.T * d.dk * sizeof(float), 256);
   return w;
+}
+
+// SCALAR / NONE decay forms (decay_forms.cu): the log-decay broadcast to
+// [B,H,T,dk] and, backward, the per-row gradient [B,H,T,dk] (I/O dtype).
+struct FormsLayout {
+  size_t gx_off, dgx_off, total;
+};
+inline FormsLayout forms_layout(const Dims& d, size_t base, bool bwd) {
+  FormsLayout l;
+  const size_t n = (size_t)d.B * d.H * d.T * d.dk * (d.bf16 ? 2 : 4);
+  l.gx_off = align_up(base, 256);
+  l.dgx_off = align_up(l.gx_off + n, 256);
+  l.total = d.decay == ZECO_DECAY_DIAG ? base : (bwd ? align_up(l.dgx_off + n, 256) : l.dgx_off);
+  return l;
 }
 
 // ------------------------------------------------------------ element I/O

@@ -20,6 +20,12 @@ cudaError_t fork_join(const Fork& f, cudaStream_t st, int i);
 // Whether per-kernel profiling marks are being recorded (api.cu).
 bool prof_active();
 
+// ---- decay forms (decay_forms.cu) --------------------------------------
+// gx[b,h,t,i] = g[b,h,t] (SCALAR) or 0 (NONE)
+cudaError_t launch_expand_log_alpha(const Dims& d, const void* g, void* gx, cudaStream_t st);
+// dg[b,h,t] = sum_i dgx[b,h,t,i] (SCALAR)
+cudaError_t launch_reduce_dlog_alpha(const Dims& d, const void* dgx, void* dg, cudaStream_t st);
+
 // ---- segment scans (scan.cu) ------------------------------------------
 cudaError_t launch_seg_scan_fwd(const Dims& d, float* S_in, const float* gamma, const float* S0,
                                 float* S_final, cudaStream_t st);

@@ -81,6 +81,20 @@ typedef enum { ZECO_F32 = 0, ZECO_BF16 = 1 } zeco_dtype;
  * (TC on an unsupported shape returns ZECO_ERR_UNSUPPORTED). */
 typedef enum { ZECO_PATH_AUTO = 0, ZECO_PATH_SIMT = 1, ZECO_PATH_TC = 2 } zeco_path;
 
+/* Form of the decay (the ZeCO pages study the diagonal, per-d_k-row decay of
+ * gated linear attention and leave other linear-attention forms to future
+ * work: ZeCO, Limitations; the LASP page's linear attention has none).
+ *   DIAG:   log_alpha [B,H,T,dk]; dlog_alpha [B,H,T,dk].
+ *   SCALAR: one log-decay per token for all d_k rows (RetNet / Lightning
+ *           style); log_alpha [B,H,T], dlog_alpha [B,H,T] (the sum over d_k
+ *           of the per-row gradient).
+ *   NONE:   alpha = 1 (plain causal linear attention); log_alpha and
+ *           dlog_alpha are not used and may be NULL.
+ * SCALAR and NONE run the same kernels as DIAG on a log-decay broadcast to
+ * [B,H,T,dk] in the workspace (and, backward, a [B,H,T,dk] gradient that
+ * SCALAR reduces over d_k). */
+typedef enum { ZECO_DECAY_DIAG = 0, ZECO_DECAY_SCALAR = 1, ZECO_DECAY_NONE = 2 } zeco_decay;
+
 typedef struct zeco_shape {
     int64_t B, H, T; /* batch, heads, tokens per sequence */
     int64_t dk, dv;  /* key/query width and value width (state is dk x dv) */
@@ -89,7 +103,7 @@ typedef struct zeco_shape {
     int32_t C;       /* chunk length inside a segment */
     int32_t dtype;   /* zeco_dtype of q, k, v, log_alpha, o and all their gradients */
     int32_t path;    /* zeco_path */
-    int32_t reserved;
+    int32_t decay;   /* zeco_decay (0 = DIAG, the default of a zeroed struct) */
 } zeco_shape;
 
 /*

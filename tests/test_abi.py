@@ -111,3 +111,24 @@ def test_path_resolution(lib):
     # fp32 at full width does not fit the SIMT kernels' shared memory with C=128
     with pytest.raises(z.ZecoError):
         z.resolve_path(_shape(dtype="f32", C=128, path="simt"))
+
+
+def test_decay_forms_workspace_and_arguments(lib):
+    import chunked_state_scan_gb300 as z
+    diag = _shape(T=4096, P=4)
+    for name in ("scalar", "none"):
+        s = _shape(T=4096, P=4, decay=name)
+        extra = 4 * 4096 * 256 * 2  # broadcast log-decay [B,H,T,dk] bf16
+        assert z.workspace_bytes(s, False) == z.workspace_bytes(diag, False) + extra
+        assert z.workspace_bytes(s, True) == z.workspace_bytes(diag, True) + 2 * extra
+    ok = ctypes.c_void_p(4096)
+    # without decay log_alpha may be NULL (the call then fails only on the tiny
+    # workspace); with decay it may not
+    none = _shape(T=4096, P=4, decay="none")
+    assert lib.zeco_gla_fwd(ctypes.byref(none), ok, ok, ok, None, None, ok, None, ok, ok, 16,
+                            None) == -3
+    assert lib.zeco_gla_fwd(ctypes.byref(diag), ok, ok, ok, None, None, ok, None, ok, ok, 16,
+                            None) == -1
+    bad = _shape(T=4096, P=4)
+    bad.decay = 3
+    assert lib.zeco_gla_resolve_path(ctypes.byref(bad)) == -1

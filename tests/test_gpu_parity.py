@@ -158,3 +158,49 @@ def test_overlap_stream_gives_identical_results(z):
         lib.zeco_set_overlap(1)
     for n in ("o", "S_final", "dq", "dk", "dv", "dlog_alpha", "dS0"):
         assert torch.equal(a[n], b[n]), n
+
+
+# ------------------------------------------------------------ decay forms
+
+
+def _decay_case(z, decay, dtype, B, H, T, dk, dv, P, K, path):
+    x = workloads.make_custom(B, H, T, dk, dv, dtype=dtype, seed=T + dk + 7 * decay,
+                              qk_scale=1 / 16 if dtype == "bf16" else None, s0_scale=0.2)
+    name = {oracle.DECAY_SCALAR: "scalar", oracle.DECAY_NONE: "none"}[decay]
+    g = x["log_alpha"][..., 0].contiguous() if decay == oracle.DECAY_SCALAR else None
+    dev = {n: (t.cuda() if t is not None else None) for n, t in x.items()}
+    gd = g.cuda() if g is not None else None
+    o, sf, saved = z.zeco_gla_fwd(dev["q"], dev["k"], dev["v"], gd, dev["S0"], P=P, K=K, C=64,
+                                  path=path, decay=name)
+    gr = z.zeco_gla_bwd(dev["q"], dev["k"], dev["v"], gd, saved, dev["do"], dev["dS_final"],
+                        P=P, K=K, C=64, path=path, decay=name)
+    torch.cuda.synchronize()
+    np_in = {n: (parity.to_np(t) if t is not None else None) for n, t in x.items()}
+    gn = parity.to_np(g) if g is not None else None
+    ro, rsf = oracle.gla_fwd_decay(np_in["q"], np_in["k"], np_in["v"], gn, np_in["S0"], decay)
+    rg = oracle.gla_bwd_decay(np_in["q"], np_in["k"], np_in["v"], gn, np_in["S0"], np_in["do"],
+                              np_in["dS_final"], decay)
+    errs = {"o": parity.err(parity.to_np(o), ro, dtype),
+            "S_final": parity.err(parity.to_np(sf), rsf, dtype)}
+    for n in ("dq", "dk", "dv", "dS0"):
+        errs[n] = parity.err(parity.to_np(gr[n]), rg[n], dtype)
+    if decay == oracle.DECAY_SCALAR:
+        assert gr["dlog_alpha"].shape == (B, H, T)
+        errs["dlog_alpha"] = parity.err(parity.to_np(gr["dlog_alpha"]), rg["dlog_alpha"], dtype)
+    else:
+        assert gr["dlog_alpha"] is None
+    return errs
+
+
+@pytest.mark.parametrize("decay", [1, 2])
+def test_f32_decay_forms(z, decay):
+    errs = _decay_case(z, decay, "f32", 1, 2, 1024, 64, 64, 4, 2, "auto")
+    _assert(errs, "f32", f"f32 decay form {decay}")
+
+
+@pytest.mark.parametrize("decay", [1, 2])
+def test_bf16_decay_forms_on_tensor_cores(z, decay):
+    shape = z.make_shape(1, 2, 2048, 128, 512, 2, 4, 64, "bf16", "tc", decay)
+    assert z.resolve_path(shape) == "tc"
+    errs = _decay_case(z, decay, "bf16", 1, 2, 2048, 128, 512, 2, 4, "tc")
+    _assert(errs, "bf16", f"bf16 tc decay form {decay}")
