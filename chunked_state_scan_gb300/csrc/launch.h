@@ -58,10 +58,13 @@ cudaError_t simt_bwd_dqk_bf16(const Dims& d, const void* q, const void* k, const
 
 // ---- tcgen05 tensor-core path (tc_*.cu) --------------------------------
 bool tc_state_supported(const Dims& d);
+// Segment states; with Eb != NULL the operand is the decay pass's K~ (resp. Q~)
+// and the per-chunk e^{b_last} replaces log_alpha (tc_state.cu, PRE).
 cudaError_t tc_chunk_state(const Dims& d, const void* k, const void* v, const void* g,
-                           float* S_in, float* gamma, cudaStream_t st);
+                           const void* Kt, const float* Eb, float* S_in, float* gamma,
+                           cudaStream_t st);
 cudaError_t tc_dstate_local(const Dims& d, const void* q, const void* d_o, const void* g,
-                            float* D, cudaStream_t st);
+                            const void* Qt, const float* Eb, float* D, cudaStream_t st);
 bool tc_fwd_supported(const Dims& d);
 // Q~ = bf16(q e^{b}), K~ = bf16(k e^{-b}) and e^{b_last} per chunk (tc_decay.cu)
 cudaError_t tc_decay(const Dims& d, const void* q, const void* k, const void* g, void* Qt,

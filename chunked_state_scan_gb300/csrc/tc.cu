@@ -14,14 +14,14 @@ bool tc_uses_dA(const Dims& d) {
   return tc_uses_decay(d) && tc_bwd_qk_supported(d) && tc_dA_supported(d);
 }
 
-// Forward: pass 1 and the scan on the caller's stream; the decay pass and the
-// scores on the auxiliary stream meanwhile (they do not depend on the scan);
-// pass 2 joins both.
+// Forward: the decay pass, then pass 1 (on its K~ and e^{b_last}) and the scan on
+// the caller's stream while the scores run on the auxiliary stream (they do not
+// depend on the scan); pass 2 joins both.
 cudaError_t tc_forward(const Dims& d, const void* q, const void* k, const void* v,
                        const void* g, const float* S0, void* o, float* S_final, float* S_in,
                        float* gamma, const DecayLayout& dl, void* ws, cudaStream_t st) {
   if (!tc_fwd_supported(d)) {
-    cudaError_t e = tc_chunk_state(d, k, v, g, S_in, gamma, st);
+    cudaError_t e = tc_chunk_state(d, k, v, g, nullptr, nullptr, S_in, gamma, st);
     if (e != cudaSuccess) return e;
     e = launch_seg_scan_fwd(d, S_in, gamma, S0, S_final, st);
     if (e != cudaSuccess) return e;
@@ -32,27 +32,29 @@ cudaError_t tc_forward(const Dims& d, const void* q, const void* k, const void* 
   void* Kt = w + dl.Kt_off;
   float* Eb = (float*)(w + dl.Eb_off);
   void* A = w + dl.A_off;
+  cudaError_t e = tc_decay(d, q, k, g, Qt, Kt, Eb, st);
+  if (e != cudaSuccess) return e;
   const Fork f = fork_begin(st);
-  cudaError_t e = tc_decay(d, q, k, g, Qt, Kt, Eb, f.aux);
-  if (e == cudaSuccess) e = tc_A(d, Qt, Kt, A, f.aux);
+  e = tc_A(d, Qt, Kt, A, f.aux);
   if (e == cudaSuccess) e = fork_mark(f, 0);
   if (e != cudaSuccess) return e;
-  e = tc_chunk_state(d, k, v, g, S_in, gamma, st);
+  e = tc_chunk_state(d, k, v, g, Kt, Eb, S_in, gamma, st);
   if (e == cudaSuccess) e = launch_seg_scan_fwd(d, S_in, gamma, S0, S_final, st);
   if (e == cudaSuccess) e = fork_join(f, st, 0);
   if (e != cudaSuccess) return e;
   return tc_fwd_out(d, Qt, Kt, v, A, Eb, S_in, o, st);
 }
 
-// Backward: the pre-pass, the reverse scan and the dv sweep on the caller's
-// stream; the decay pass, the scores and their gradient on the auxiliary stream.
+// Backward: the decay pass, then the pre-pass (on its Q~ and e^{b_last}), the
+// reverse scan and the dv sweep on the caller's stream while the scores and
+// their gradient run on the auxiliary stream.
 cudaError_t tc_backward(const Dims& d, const void* q, const void* k, const void* v,
                         const void* g, const float* S_in, const float* gamma, const void* d_o,
                         const float* dS_final, void* dq, void* dk, void* dv, void* dg,
                         float* dS0, float* D, float* carry, float* qdq, const DecayLayout& dl,
                         void* ws, cudaStream_t st) {
   if (!tc_fwd_supported(d)) {
-    cudaError_t e = tc_dstate_local(d, q, d_o, g, D, st);
+    cudaError_t e = tc_dstate_local(d, q, d_o, g, nullptr, nullptr, D, st);
     if (e != cudaSuccess) return e;
     e = launch_seg_scan_rev(d, D, S_in, gamma, dS_final, dS0, carry, st);
     if (e != cudaSuccess) return e;
@@ -65,14 +67,15 @@ cudaError_t tc_backward(const Dims& d, const void* q, const void* k, const void*
   void* A = w + dl.A_off;
   const bool qk_tc = tc_uses_dA(d);
   void* dA = w + dl.dA_off;
+  cudaError_t e = tc_decay(d, q, k, g, Qt, Kt, Eb, st);
+  if (e != cudaSuccess) return e;
   const Fork f = fork_begin(st);
-  cudaError_t e = tc_decay(d, q, k, g, Qt, Kt, Eb, f.aux);
-  if (e == cudaSuccess) e = tc_A(d, Qt, Kt, A, f.aux);
+  e = tc_A(d, Qt, Kt, A, f.aux);
   if (e == cudaSuccess) e = fork_mark(f, 0);
   if (e == cudaSuccess && qk_tc) e = tc_dA(d, d_o, v, dA, f.aux);
   if (e == cudaSuccess) e = fork_mark(f, 1);
   if (e != cudaSuccess) return e;
-  e = tc_dstate_local(d, q, d_o, g, D, st);
+  e = tc_dstate_local(d, q, d_o, g, Qt, Eb, D, st);
   if (e == cudaSuccess) e = launch_seg_scan_rev(d, D, S_in, gamma, dS_final, dS0, carry, st);
   if (e == cudaSuccess) e = fork_join(f, st, 0);
   if (e == cudaSuccess) e = tc_bwd_dv(d, Qt, Kt, d_o, A, Eb, D, dv, st);

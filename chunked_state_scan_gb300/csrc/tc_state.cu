@@ -44,12 +44,19 @@ __device__ int g_tc_status = 0;  // set when a bounded wait gives up
 
 constexpr int kStateThreads = 512;  // 128 rows x 4 token quarters
 
-template <int NT, bool REV>
+// PRE: x is the decay pass's K~ = k e^{-b} (REV) or Q~ = q e^{b} (forward), and
+// the weight of a token of chunk n factors into one value per row and chunk:
+//   REV:  e^{G_end - G_t} = e^{-b_t} * prod_{m >= n} e^{b_last,m}
+//   fwd:  e^{G_t}         = e^{b_t}  * prod_{m <  n} e^{b_last,m}
+// (G: cumulative log-decay from the segment start, b: from the chunk start), so a
+// stage loads the chunk's e^{b_last} row instead of the log_alpha tile and scales
+// the tile by a running product, with no exponential per element.
+template <int NT, bool REV, bool PRE>
 __global__ void __launch_bounds__(kStateThreads, 1)
 tc_seg_state_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmG,
-                    const __grid_constant__ CUtensorMap tmY, float* __restrict__ out,
-                    float* __restrict__ gamma, int64_t T, int dk, int dv, int P, int64_t L,
-                    int slot_off) {
+                    const __grid_constant__ CUtensorMap tmY, const float* __restrict__ Eb,
+                    float* __restrict__ out, float* __restrict__ gamma, int64_t T, int dk, int dv,
+                    int P, int64_t L, int slot_off) {
   constexpr int kBBytes = kTok * NT * 2;
   constexpr int kStageBytes = kXBytes + kGBytes + kBBytes;
   extern __shared__ __align__(1024) unsigned char smraw[];
@@ -58,6 +65,7 @@ tc_seg_state_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
   __shared__ float Gq[4][kM];  // per-quarter sums of log_alpha of the current stage
+  __shared__ float sF[kM];     // PRE: this stage's factor of each row
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int row = tid & (kM - 1), qd = tid >> 7;  // row within the tile, token quarter
@@ -76,7 +84,7 @@ tc_seg_state_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
     abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tmX);
-    prefetch_tmap(&tmG);
+    if (!PRE) prefetch_tmap(&tmG);
     prefetch_tmap(&tmY);
   }
   if (warp == 0) tmem_alloc(&tmem_base, NT);
@@ -93,17 +101,19 @@ tc_seg_state_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
     const int s = it % kStages;
     unsigned char* base = sm + s * kStageBytes;
     const int32_t r = blk_row(it);
-    mbar_expect_tx(&tma_bar[s], kStageBytes);
+    mbar_expect_tx(&tma_bar[s], PRE ? kXBytes + kM * 4 + kBBytes : kStageBytes);
     for (int mb = 0; mb < kM / 64; ++mb) {
       tma_load_2d(base + mb * 8192, &tmX, i0 + mb * 64, r, &tma_bar[s]);
-      tma_load_2d(base + kXBytes + mb * 8192, &tmG, i0 + mb * 64, r, &tma_bar[s]);
+      if (!PRE) tma_load_2d(base + kXBytes + mb * 8192, &tmG, i0 + mb * 64, r, &tma_bar[s]);
     }
+    if (PRE) bulk_load(base + kXBytes, Eb + (size_t)(r / kTok) * dk + i0, kM * 4, &tma_bar[s]);
     for (int nb = 0; nb < NT / 64; ++nb)
       tma_load_2d(base + kXBytes + kGBytes + nb * 8192, &tmY, j0 + nb * 64, r, &tma_bar[s]);
   };
 
   if (tid == 0) issue_tma(0);
   float run = 0.f;  // log-decay of row i summed over the stages already done
+  float run_f = 1.f;  // PRE: product of e^{b_last} over the chunks already done
   // row i of the tiles lives in MN block row/64, 16-byte chunk (row%64)/8, element row%8
   const uint32_t a_blk = (uint32_t)(row >> 6) * 8192u;
   const uint32_t a_chunk = (uint32_t)((row & 63) >> 3);
@@ -125,6 +135,32 @@ tc_seg_state_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
       atomicExch(&g_tc_status, 1);
       abort_flag = 1;
     }
+    if (PRE) {
+      // this stage's factor of row `row`, then every 16-byte group of 8 rows of the
+      // tile scaled in place (2 per thread)
+      if (tid < kM) {
+        const float e = reinterpret_cast<const float*>(xbuf + kXBytes)[tid];
+        if (REV) run_f *= e;
+        sF[tid] = run_f;
+        if (!REV) run_f *= e;
+      }
+      __syncthreads();
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int c = tid + h * kStateThreads;  // 64 tokens x 2 row blocks x 8 groups
+        const int t = c >> 4, mb = (c >> 3) & 1, c8 = c & 7;
+        uint4* ptr = reinterpret_cast<uint4*>(xbuf + mb * 8192 + sw128((uint32_t)t, (uint32_t)c8));
+        uint4 wv = *ptr;
+        __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(&wv);
+        const float* f = sF + 64 * mb + 8 * c8;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float2 x2 = __bfloat1622float2(h2[u]);
+          h2[u] = __floats2bfloat162_rn(x2.x * f[2 * u], x2.y * f[2 * u + 1]);
+        }
+        *ptr = wv;
+      }
+    } else
     // A = (w .* x) written over x; this thread: row i, tokens 16 qd .. 16 qd + 15
     {
       float gl[16];
@@ -201,7 +237,8 @@ tc_seg_state_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
       for (int u = 0; u < 8; ++u)
         dst[u] = make_float4(r[4 * u], r[4 * u + 1], r[4 * u + 2], r[4 * u + 3]);
     }
-    if (REV && gamma && blockIdx.x == 0) gamma[((size_t)bh * P + p) * dk + i] = __expf(run);
+    if (REV && gamma && blockIdx.x == 0)
+      gamma[((size_t)bh * P + p) * dk + i] = PRE ? run_f : __expf(run);
     (void)lane;
   }
   tc_fence_before();
@@ -262,23 +299,35 @@ bool make_tmap_f32_plain(CUtensorMap* m, const void* base, uint64_t rows, uint64
                                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int NT, bool REV>
+template <int NT, bool REV, bool PRE>
 static cudaError_t launch_state(const Dims& d, const void* x, const void* y, const void* g,
-                                float* out, float* gamma, int slot_off, cudaStream_t st) {
+                                const float* Eb, float* out, float* gamma, int slot_off,
+                                cudaStream_t st) {
   CUtensorMap tx, tg, ty;
   const uint64_t rows = (uint64_t)(d.B * d.H * d.T);
   if (!make_tmap_bf16(&tx, x, rows, (uint64_t)d.dk, kTok) ||
-      !make_tmap_bf16(&tg, g, rows, (uint64_t)d.dk, kTok) ||
+      !make_tmap_bf16(&tg, PRE ? x : g, rows, (uint64_t)d.dk, kTok) ||
       !make_tmap_bf16(&ty, y, rows, (uint64_t)d.dv, kTok))
     return cudaErrorInvalidValue;
   const int smem = kStages * (kXBytes + kGBytes + kTok * NT * 2) + 1024;
-  auto kern = tc_seg_state_kernel<NT, REV>;
+  auto kern = tc_seg_state_kernel<NT, REV, PRE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)(d.dv / NT), (unsigned)(d.dk / kM), (unsigned)(d.B * d.H * d.P));
-  kern<<<grid, kStateThreads, smem, st>>>(tx, tg, ty, out, gamma, d.T, (int)d.dk, (int)d.dv, d.P,
-                                          d.L, slot_off);
+  kern<<<grid, kStateThreads, smem, st>>>(tx, tg, ty, Eb, out, gamma, d.T, (int)d.dk,
+                                          (int)d.dv, d.P, d.L, slot_off);
   return cudaGetLastError();
+}
+
+template <bool REV>
+static cudaError_t launch_state_any(const Dims& d, const void* x, const void* y, const void* g,
+                                    const float* Eb, float* out, float* gamma, int slot_off,
+                                    cudaStream_t st) {
+  if (Eb)
+    return d.dv % 256 == 0 ? launch_state<256, REV, true>(d, x, y, g, Eb, out, gamma, slot_off, st)
+                           : launch_state<128, REV, true>(d, x, y, g, Eb, out, gamma, slot_off, st);
+  return d.dv % 256 == 0 ? launch_state<256, REV, false>(d, x, y, g, Eb, out, gamma, slot_off, st)
+                         : launch_state<128, REV, false>(d, x, y, g, Eb, out, gamma, slot_off, st);
 }
 
 bool tc_state_supported(const Dims& d) {
@@ -286,19 +335,18 @@ bool tc_state_supported(const Dims& d) {
 }
 
 cudaError_t tc_chunk_state(const Dims& d, const void* k, const void* v, const void* g,
-                           float* S_in, float* gamma, cudaStream_t st) {
-  cudaError_t e = (d.dv % 256 == 0)
-                      ? launch_state<256, true>(d, k, v, g, S_in, gamma, 1, st)
-                      : launch_state<128, true>(d, k, v, g, S_in, gamma, 1, st);
+                           const void* Kt, const float* Eb, float* S_in, float* gamma,
+                           cudaStream_t st) {
+  cudaError_t e = Eb ? launch_state_any<true>(d, Kt, v, g, Eb, S_in, gamma, 1, st)
+                     : launch_state_any<true>(d, k, v, g, nullptr, S_in, gamma, 1, st);
   prof_mark("tc_chunk_state", st);
   return e;
 }
 
 cudaError_t tc_dstate_local(const Dims& d, const void* q, const void* d_o, const void* g,
-                            float* D, cudaStream_t st) {
-  cudaError_t e = (d.dv % 256 == 0)
-                      ? launch_state<256, false>(d, q, d_o, g, D, nullptr, 0, st)
-                      : launch_state<128, false>(d, q, d_o, g, D, nullptr, 0, st);
+                            const void* Qt, const float* Eb, float* D, cudaStream_t st) {
+  cudaError_t e = Eb ? launch_state_any<false>(d, Qt, d_o, g, Eb, D, nullptr, 0, st)
+                     : launch_state_any<false>(d, q, d_o, g, nullptr, D, nullptr, 0, st);
   prof_mark("tc_dstate_local", st);
   return e;
 }
