@@ -57,6 +57,8 @@ def load_library(path: str = LIB_PATH):
             vp, sz, sp = ctypes.c_void_p, ctypes.c_size_t, ctypes.POINTER(ZecoShape)
             lib.zeco_gla_saved_bytes.argtypes = [sp]
             lib.zeco_gla_saved_bytes.restype = sz
+            lib.zeco_gla_segments.argtypes = [sp]
+            lib.zeco_gla_segments.restype = ctypes.c_int64
             lib.zeco_set_overlap.argtypes = [ctypes.c_int]
             lib.zeco_set_overlap.restype = ctypes.c_int
             lib.zeco_gla_workspace_bytes.argtypes = [sp, ctypes.c_int]
@@ -107,6 +109,15 @@ def saved_bytes(shape: ZecoShape) -> int:
 
 def workspace_bytes(shape: ZecoShape, bwd: bool) -> int:
     return load_library().zeco_gla_workspace_bytes(ctypes.byref(shape), int(bwd))
+
+
+def segments(shape: ZecoShape) -> int:
+    """Segments the library evaluates for this shape (P, or P split further when
+    B*H*P is too small to fill the GPU); the `saved` layout follows it."""
+    n = load_library().zeco_gla_segments(ctypes.byref(shape))
+    if n < 0:
+        _check(int(n))
+    return int(n)
 
 
 def set_overlap(on: bool) -> None:

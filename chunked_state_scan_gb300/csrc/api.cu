@@ -47,6 +47,20 @@ int check_shape(const zeco_shape* s, Dims* d) {
   d->L = L;
   d->bf16 = s->dtype == ZECO_BF16;
   d->decay = s->decay;
+  // Segments on one GPU.  The P segments of the method exchange their states
+  // through the segment scan; the decomposition is exact for any split, so when
+  // B*H*P is too small to give the chunk sweeps a wave of CTAs (one per 128 d_v
+  // columns of a segment; 152 SMs), each segment is split further into 2^m equal
+  // sub-segments of at least 4 chunks (at most 64 per segment).  Everything
+  // below, the `saved` layout included, uses the effective count.
+  constexpr int64_t kWave = 152;
+  const int64_t tiles = (s->dv + 127) / 128;
+  int64_t m = 1;
+  while (s->B * s->H * s->P * m * tiles < kWave && m < 64 && s->T % (s->P * m * 2 * s->C) == 0 &&
+         s->T / (s->P * m * 2) >= 4 * (int64_t)s->C && s->B * s->H * s->P * m * 2 <= 65535)
+    m *= 2;
+  d->P = (int)(s->P * m);
+  d->L = s->T / d->P;
   return ZECO_OK;
 }
 
@@ -133,6 +147,12 @@ size_t zeco_gla_workspace_bytes(const zeco_shape* shape, int bwd) {
   const int path = resolve(shape, d);
   if (path < 0) return 0;
   return plan_ws(d, path, bwd != 0).total;
+}
+
+int64_t zeco_gla_segments(const zeco_shape* shape) {
+  Dims d;
+  const int rc = check_shape(shape, &d);
+  return rc != ZECO_OK ? rc : d.P;
 }
 
 int zeco_gla_resolve_path(const zeco_shape* shape) {

@@ -20,8 +20,10 @@
 // Layout: one warp owns one d_k row of one (b,h); lane l holds the float4
 // columns l, l+32, ... of that row, so every access is a coalesced 512-byte
 // warp transaction and the row sums of the carry are warp-shuffle reductions.
-// The p loop is sequential; the loads of step p+1 do not depend on step p, so
-// they are issued ahead (unrolled) and only the FMA chain is serial.
+// The p loop is sequential, but the loads of a step do not depend on the steps
+// before it: they are issued kBatch steps at a time and only the FMA chain is
+// serial, so the scan streams at memory bandwidth even for very many segments
+// (a tree scan would move at least as many bytes).
 #include "common.cuh"
 #include "launch.h"
 
@@ -30,6 +32,7 @@ namespace {
 
 constexpr int kWarps = 8;
 constexpr int kMaxU = 4;  // dv <= 512: at most 4 float4 per lane
+constexpr int kBatch = 4;  // segment steps whose loads are issued together
 
 __device__ __forceinline__ float4 fma4(float a, float4 x, float4 y) {
   return make_float4(fmaf(a, x.x, y.x), fmaf(a, x.y, y.y), fmaf(a, x.z, y.z), fmaf(a, x.w, y.w));
@@ -53,21 +56,40 @@ seg_scan_fwd_kernel(float* __restrict__ S_in, const float* __restrict__ gamma,
 #pragma unroll
   for (int u = 0; u < kMaxU; ++u) {
     const int j4 = lane + 32 * u;
+    s[u] = make_float4(0.f, 0.f, 0.f, 0.f);
     if (j4 < nv4) {
       s[u] = S0 ? reinterpret_cast<const float4*>(S0 + ((size_t)bh * dk + i) * dv)[j4]
                 : make_float4(0.f, 0.f, 0.f, 0.f);
       base[j4] = s[u];
     }
   }
-  for (int p = 0; p < P; ++p) {
-    const float gm = gam[(size_t)p * dk];
-    float4* dst = base + (size_t)(p + 1) * (slot >> 2);
+  for (int p0 = 0; p0 < P; p0 += kBatch) {
+    // the loads of kBatch steps go out together; only the FMA chain is serial
+    float4 x[kBatch][kMaxU];
+    float gm[kBatch];
 #pragma unroll
-    for (int u = 0; u < kMaxU; ++u) {
-      const int j4 = lane + 32 * u;
-      if (j4 < nv4) {
-        s[u] = fma4(gm, s[u], dst[j4]);  // gamma_p * S_in[p] + S_loc[p]
-        dst[j4] = s[u];
+    for (int b = 0; b < kBatch; ++b) {
+      const int p = p0 + b;
+      gm[b] = p < P ? gam[(size_t)p * dk] : 0.f;
+#pragma unroll
+      for (int u = 0; u < kMaxU; ++u) {
+        const int j4 = lane + 32 * u;
+        x[b][u] = (p < P && j4 < nv4) ? base[(size_t)(p + 1) * (slot >> 2) + j4]
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const int p = p0 + b;
+      if (p >= P) break;
+      float4* dst = base + (size_t)(p + 1) * (slot >> 2);
+#pragma unroll
+      for (int u = 0; u < kMaxU; ++u) {
+        const int j4 = lane + 32 * u;
+        if (j4 < nv4) {
+          s[u] = fma4(gm[b], s[u], x[b][u]);  // gamma_p * S_in[p] + S_loc[p]
+          dst[j4] = s[u];
+        }
       }
     }
   }
@@ -102,34 +124,50 @@ seg_scan_rev_kernel(float* __restrict__ D, const float* __restrict__ S_in,
 #pragma unroll
   for (int u = 0; u < kMaxU; ++u) {
     const int j4 = lane + 32 * u;
+    s[u] = make_float4(0.f, 0.f, 0.f, 0.f);  // columns past dv stay 0 (they enter the carry)
     if (j4 < nv4) {
       s[u] = dS_final ? reinterpret_cast<const float4*>(dS_final + ((size_t)bh * dk + i) * dv)[j4]
                       : make_float4(0.f, 0.f, 0.f, 0.f);
       Db[(size_t)P * slot4 + j4] = s[u];
     }
   }
-  for (int p = P - 1; p >= 0; --p) {
-    // carry c_p = rowsum(D[p+1] .* S_in[p+1])
-    float part = 0.f;
+  for (int p0 = P - 1; p0 >= 0; p0 -= kBatch) {
+    // the loads of kBatch steps (S_in[p+1], dS_loc[p], gamma_p) go out together
+    float4 y[kBatch][kMaxU], x[kBatch][kMaxU];
+    float gm[kBatch];
 #pragma unroll
-    for (int u = 0; u < kMaxU; ++u) {
-      const int j4 = lane + 32 * u;
-      if (j4 < nv4) {
-        const float4 y = Sb[(size_t)(p + 1) * slot4 + j4];
-        part = fmaf(s[u].x, y.x, fmaf(s[u].y, y.y, fmaf(s[u].z, y.z, fmaf(s[u].w, y.w, part))));
+    for (int b = 0; b < kBatch; ++b) {
+      const int p = p0 - b;
+      gm[b] = p >= 0 ? gam[(size_t)p * dk] : 0.f;
+#pragma unroll
+      for (int u = 0; u < kMaxU; ++u) {
+        const int j4 = lane + 32 * u;
+        const bool ok = p >= 0 && j4 < nv4;
+        y[b][u] = ok ? Sb[(size_t)(p + 1) * slot4 + j4] : make_float4(0.f, 0.f, 0.f, 0.f);
+        x[b][u] = ok ? Db[(size_t)p * slot4 + j4] : make_float4(0.f, 0.f, 0.f, 0.f);
       }
     }
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
-    if (lane == 0) carry[((size_t)bh * P + p) * dk + i] = part;
-    const float gm = gam[(size_t)p * dk];
+    for (int b = 0; b < kBatch; ++b) {
+      const int p = p0 - b;
+      if (p < 0) break;
+      // carry c_p = rowsum(D[p+1] .* S_in[p+1])
+      float part = 0.f;
 #pragma unroll
-    for (int u = 0; u < kMaxU; ++u) {
-      const int j4 = lane + 32 * u;
-      if (j4 < nv4) {
-        float4* dst = Db + (size_t)p * slot4 + j4;
-        s[u] = fma4(gm, s[u], *dst);  // dS_loc[p] + gamma_p * D[p+1]
-        *dst = s[u];
+      for (int u = 0; u < kMaxU; ++u) {
+        const float4 yy = y[b][u];
+        part = fmaf(s[u].x, yy.x, fmaf(s[u].y, yy.y, fmaf(s[u].z, yy.z, fmaf(s[u].w, yy.w, part))));
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
+      if (lane == 0) carry[((size_t)bh * P + p) * dk + i] = part;
+#pragma unroll
+      for (int u = 0; u < kMaxU; ++u) {
+        const int j4 = lane + 32 * u;
+        if (j4 < nv4) {
+          s[u] = fma4(gm[b], s[u], x[b][u]);  // dS_loc[p] + gamma_p * D[p+1]
+          Db[(size_t)p * slot4 + j4] = s[u];
+        }
       }
     }
   }

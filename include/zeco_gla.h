@@ -107,10 +107,22 @@ typedef struct zeco_shape {
 } zeco_shape;
 
 /*
+ * Number of segments the library evaluates on one GPU for this shape (or a
+ * negative ZECO_ERR_* code).  The segmented decomposition is exact for any
+ * split of the sequence (ZeCO two-pass operator: the local states plus the
+ * segment scan reproduce the recurrence), so when B*H*P gives the chunk sweeps
+ * fewer CTAs than one wave of the GPU (152), each of the P segments is split
+ * further into 2^m equal sub-segments of at least 4 chunks (m <= 6): config-2
+ * shapes with P = 1 run as 16 segments.  Results differ only by rounding.
+ * Below, "P_eff" is this number.
+ */
+int64_t zeco_gla_segments(const zeco_shape *shape);
+
+/*
  * Bytes of the `saved` buffer written by zeco_gla_fwd and read by
- * zeco_gla_bwd: the incoming global state of every segment, S_in [B,H,P+1,dk,dv]
- * fp32 (S_in[0] = S0, S_in[P] = S_final), then the segment decays
- * gamma [B,H,P,dk] fp32.  Returns 0 for an invalid shape.
+ * zeco_gla_bwd: the incoming global state of every segment, S_in
+ * [B,H,P_eff+1,dk,dv] fp32 (S_in[0] = S0, S_in[P_eff] = S_final), then the
+ * segment decays gamma [B,H,P_eff,dk] fp32.  Returns 0 for an invalid shape.
  */
 size_t zeco_gla_saved_bytes(const zeco_shape *shape);
 
@@ -118,7 +130,7 @@ size_t zeco_gla_saved_bytes(const zeco_shape *shape);
  * Bytes of scratch memory the forward (bwd = 0) or backward (bwd = 1) needs,
  * for the path the shape resolves to (shape->path, see zeco_gla_resolve_path).
  * The backward holds the adjoint of every segment's incoming state
- * [B,H,P+1,dk,dv] fp32, one dlog_alpha carry row per segment [B,H,P,dk] fp32,
+ * [B,H,P_eff+1,dk,dv] fp32, one dlog_alpha carry row per segment [B,H,P_eff,dk] fp32,
  * and q .* dq in fp32 [B,H,T,dk] (dlog_alpha is a long suffix sum of
  * q .* dq - k .* dk that cancels heavily, so its terms are kept in fp32).
  * On the tensor-core path both directions also hold the decay-weighted

@@ -63,8 +63,11 @@ def compare_full(z, x, P, K, C, dtype, path="auto", bwd=True, check_states=True)
     ro, rsf = oracle.gla_fwd(x["q"], x["k"], x["v"], x["log_alpha"], x["S0"])
     errs = {"o": err(to_np(res["o"]), ro, dtype), "S_final": err(to_np(res["S_final"]), rsf, dtype)}
     if check_states:
-        bs = oracle.boundary_states(x["q"], x["k"], x["v"], x["log_alpha"], x["S0"], P)
-        got = to_np(saved_states(res["saved"], B, H, P, dk, dv))
+        # the library may split the P segments further (zeco_gla_segments)
+        pe = z.segments(z.make_shape(B, H, T, dk, dv, P, K, C, dtype, path))
+        assert pe % P == 0
+        bs = oracle.boundary_states(x["q"], x["k"], x["v"], x["log_alpha"], x["S0"], pe)
+        got = to_np(saved_states(res["saved"], B, H, pe, dk, dv))
         errs["S_in"] = err(got, bs, dtype)
     if bwd:
         rg = oracle.gla_bwd(x["q"], x["k"], x["v"], x["log_alpha"], x["S0"], x["do"],

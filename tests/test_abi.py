@@ -132,3 +132,18 @@ def test_decay_forms_workspace_and_arguments(lib):
     bad = _shape(T=4096, P=4)
     bad.decay = 3
     assert lib.zeco_gla_resolve_path(ctypes.byref(bad)) == -1
+
+
+def test_segment_count_fills_the_gpu(lib):
+    import chunked_state_scan_gb300 as z
+    # the 1M-token workload already gives 1024 CTAs: no split
+    assert z.segments(_shape()) == 64
+    # GLA-1B layer shape with one segment: 16 sub-segments of 1024 tokens
+    assert z.segments(_shape(T=16384, P=1, K=1)) == 16
+    # 8-segment forward at 131K tokens: split in two
+    assert z.segments(_shape(T=131072, P=8, K=4)) == 16
+    # the saved buffer follows the effective count
+    s = _shape(T=16384, P=1, K=1)
+    assert z.saved_bytes(s) == 4 * 17 * 256 * 512 * 4 + 4 * 16 * 256 * 4
+    # too short to split (fewer than 4 chunks per sub-segment)
+    assert z.segments(_shape(T=512, P=2, K=8)) == 2

@@ -204,3 +204,32 @@ def test_bf16_decay_forms_on_tensor_cores(z, decay):
     assert z.resolve_path(shape) == "tc"
     errs = _decay_case(z, decay, "bf16", 1, 2, 2048, 128, 512, 2, 4, "tc")
     _assert(errs, "bf16", f"bf16 tc decay form {decay}")
+
+
+# ------------------------------------------------------------ segment counts
+
+
+@pytest.mark.parametrize("dtype,dv,path", [("bf16", 512, "tc"), ("f32", 64, "simt")])
+def test_one_chunk_per_segment(z, dtype, dv, path):
+    # P = T / C: every segment is one chunk, the scans carry 128 steps
+    B, H, T, dk = 1, 1, 8192, 128 if dtype == "bf16" else 64
+    P, K = T // 64, 4
+    x = workloads.make_custom(B, H, T, dk, dv, dtype=dtype, seed=5,
+                              qk_scale=1 / 16 if dtype == "bf16" else None, s0_scale=0.2)
+    shape = z.make_shape(B, H, T, dk, dv, P, K, 64, dtype, path)
+    assert z.segments(shape) == P
+    errs = parity.compare_full(z, x, P, K, 64, dtype, path=path)
+    _assert(errs, dtype, f"P = T/C ({path})")
+
+
+def test_low_parallelism_shape_is_split_and_unchanged(z):
+    # one segment of 16K tokens, 2 heads: 2 x 4 d_v tiles per segment, so the
+    # library evaluates 32 sub-segments of 512 tokens (256 CTAs); the outputs
+    # match the oracle as for any split
+    B, H, T, dk, dv = 1, 2, 16384, 128, 512
+    shape = z.make_shape(B, H, T, dk, dv, 1, 1, 64, "bf16", "auto")
+    assert z.segments(shape) == 32
+    x = workloads.make_custom(B, H, T, dk, dv, dtype="bf16", seed=6, qk_scale=1 / 16,
+                              s0_scale=0.2)
+    errs = parity.compare_full(z, x, 1, 1, 64, "bf16")
+    _assert(errs, "bf16", "P = 1 split")

@@ -41,7 +41,8 @@ def _sample_check(z, w, heads, with_bwd):
         grads = z.zeco_gla_bwd(x["q"], x["k"], x["v"], x["log_alpha"], saved, x["do"],
                                x["dS_final"], P=w.P, K=w.K, C=w.C)
     torch.cuda.synchronize()
-    states = parity.saved_states(saved, w.B, w.H, w.P, w.dk, w.dv)
+    pe = z.segments(z.make_shape(w.B, w.H, w.T, w.dk, w.dv, w.P, w.K, w.C, w.dtype))
+    states = parity.saved_states(saved, w.B, w.H, pe, w.dk, w.dv)
     errs = {}
     for b, h in heads:
         sl = lambda t: t[b:b + 1, h:h + 1].cpu()  # noqa: E731
@@ -51,7 +52,7 @@ def _sample_check(z, w, heads, with_bwd):
         errs[f"o[{b},{h}]"] = parity.rel_l2(parity.to_np(o[b, h][:, COLS]), ro[0, 0])
         errs[f"S_final[{b},{h}]"] = parity.rel_l2(parity.to_np(sf[b, h][:, COLS]), rsf[0, 0])
         bs = oracle.boundary_states_cols(xs["q"], xs["k"], xs["v"], xs["log_alpha"], xs["S0"],
-                                         w.P, COLS)
+                                         pe, COLS)
         errs[f"S_in[{b},{h}]"] = parity.rel_l2(parity.to_np(states[b, h][..., COLS]), bs[0, 0])
         if with_bwd:
             rg = oracle.gla_bwd(xs["q"], xs["k"], xs["v"], xs["log_alpha"], xs["S0"], xs["do"],
