@@ -383,6 +383,7 @@ def main(argv=None):
     torch.cuda.synchronize(dev)
     barrier(world)
     clk = clocks.stop()
+    dev_status = lib.zeco_check_device_status()  # 0: no bounded device wait gave up
     elapsed = e0.elapsed_time(e1) / 1e3
     elapsed_max = max_over_ranks(elapsed, world)
     value, ms_step = aggregate(elapsed_max, w.tokens, args.steps, world)
@@ -446,6 +447,7 @@ def main(argv=None):
                               "frac": t_roof / step_s,
                               "note": "ZeCO two-pass algorithmic bytes/flops per step vs "
                                       f"{peak_kind} peaks"},
+        "device_status": "ok" if dev_status == 0 else f"error {dev_status}",
         "kernels_ms": kern_ms, "overlap": overlap, "scan_share": scan_ms / sum(kern_ms.values()),
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,

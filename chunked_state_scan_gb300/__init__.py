@@ -120,6 +120,12 @@ def segments(shape: ZecoShape) -> int:
     return int(n)
 
 
+def check_device_status() -> None:
+    """Raise ZecoError if a bounded device wait gave up since the last check
+    (synchronise the streams of the calls to cover first)."""
+    _check(load_library().zeco_check_device_status())
+
+
 def set_overlap(on: bool) -> None:
     """Run the scan-independent passes on a second stream (default) or not."""
     load_library().zeco_set_overlap(int(bool(on)))

@@ -243,6 +243,17 @@ int zeco_gla_bwd(const zeco_shape* shape, const void* q, const void* k, const vo
   return e == cudaSuccess ? ZECO_OK : ZECO_ERR_CUDA;
 }
 
+int zeco_check_device_status(void) {
+  const int v[] = {zeco::tc_state_take_status(), zeco::tc_fwd_take_status(),
+                   zeco::tc_scores_take_status(), zeco::tc_bwd_qk_take_status()};
+  int rc = ZECO_OK;
+  for (int x : v) {
+    if (x < 0) return ZECO_ERR_CUDA;
+    if (x > 0) rc = ZECO_ERR_TIMEOUT;
+  }
+  return rc;
+}
+
 const char* zeco_strerror(int code) {
   switch (code) {
     case ZECO_OK:
@@ -255,6 +266,8 @@ const char* zeco_strerror(int code) {
       return "workspace too small";
     case ZECO_ERR_CUDA:
       return "CUDA kernel launch failed";
+    case ZECO_ERR_TIMEOUT:
+      return "a bounded device wait gave up (results of that call are not valid)";
     default:
       return "unknown error code";
   }

@@ -20,6 +20,13 @@ cudaError_t fork_join(const Fork& f, cudaStream_t st, int i);
 // Whether per-kernel profiling marks are being recorded (api.cu).
 bool prof_active();
 
+// ---- bounded-wait flags of the tensor-core kernels: read and clear; -1 when
+//      the flag cannot be read
+int tc_bwd_qk_take_status();
+int tc_fwd_take_status();
+int tc_scores_take_status();
+int tc_state_take_status();
+
 // ---- decay forms (decay_forms.cu) --------------------------------------
 // gx[b,h,t,i] = g[b,h,t] (SCALAR) or 0 (NONE)
 cudaError_t launch_expand_log_alpha(const Dims& d, const void* g, void* gx, cudaStream_t st);

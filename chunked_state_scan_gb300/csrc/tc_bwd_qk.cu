@@ -556,4 +556,15 @@ cudaError_t tc_bwd_qk(const Dims& d, const void* Qt, const void* Kt, const void*
   return e;
 }
 
+// Reads and clears this file's bounded-wait flag (nonzero: a wait gave up).
+int tc_bwd_qk_take_status() {
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_qk_status, sizeof(v)) != cudaSuccess) return -1;
+  if (v != 0) {
+    const int zero = 0;
+    cudaMemcpyToSymbol(g_qk_status, &zero, sizeof(zero));
+  }
+  return v;
+}
+
 }  // namespace zeco

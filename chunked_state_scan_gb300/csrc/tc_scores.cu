@@ -188,4 +188,15 @@ cudaError_t tc_A(const Dims& d, const void* Qt, const void* Kt, void* P, cudaStr
   return e;
 }
 
+// Reads and clears this file's bounded-wait flag (nonzero: a wait gave up).
+int tc_scores_take_status() {
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_scores_status, sizeof(v)) != cudaSuccess) return -1;
+  if (v != 0) {
+    const int zero = 0;
+    cudaMemcpyToSymbol(g_scores_status, &zero, sizeof(zero));
+  }
+  return v;
+}
+
 }  // namespace zeco

@@ -351,4 +351,15 @@ cudaError_t tc_dstate_local(const Dims& d, const void* q, const void* d_o, const
   return e;
 }
 
+// Reads and clears this file's bounded-wait flag (nonzero: a wait gave up).
+int tc_state_take_status() {
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_tc_status, sizeof(v)) != cudaSuccess) return -1;
+  if (v != 0) {
+    const int zero = 0;
+    cudaMemcpyToSymbol(g_tc_status, &zero, sizeof(zero));
+  }
+  return v;
+}
+
 }  // namespace zeco

@@ -71,7 +71,8 @@ enum {
     ZECO_ERR_ARG = -1,         /* null / misaligned pointer or invalid shape value */
     ZECO_ERR_UNSUPPORTED = -2, /* valid shape outside the supported set above */
     ZECO_ERR_WORKSPACE = -3,   /* ws_bytes smaller than zeco_gla_workspace_bytes() */
-    ZECO_ERR_CUDA = -4         /* a kernel launch failed */
+    ZECO_ERR_CUDA = -4,        /* a kernel launch failed */
+    ZECO_ERR_TIMEOUT = -5      /* a bounded device wait gave up (zeco_check_device_status) */
 };
 
 typedef enum { ZECO_F32 = 0, ZECO_BF16 = 1 } zeco_dtype;
@@ -192,6 +193,18 @@ int zeco_gla_bwd_noalloc(const zeco_shape *shape, const void *q, const void *k, 
                          const void *log_alpha, const void *saved, const void *d_o,
                          const float *dS_final, void *dq, void *dk, void *dv,
                          void *dlog_alpha, float *dS0, zeco_stream_t stream);
+
+/*
+ * Every wait of the tensor-core kernels on an mbarrier (a copy or an MMA group
+ * to complete, a peer CTA's partial sums) gives up after a bounded number of
+ * polls instead of hanging the GPU; the kernel then records it in a device
+ * flag and continues, so that call's outputs are not valid.  This reads and
+ * clears the flags of the current device: ZECO_OK when no wait gave up since
+ * the last check, ZECO_ERR_TIMEOUT when one did, ZECO_ERR_CUDA when the flags
+ * cannot be read.  It copies from device memory: call it after the streams of
+ * the calls it should cover have been synchronised.
+ */
+int zeco_check_device_status(void);
 
 /* Static message for an error code (never NULL). */
 const char *zeco_strerror(int code);

@@ -47,6 +47,7 @@ def run_gpu(z, x, P, K, C, path="auto", bwd=True, dev="cuda"):
         out.update(z.zeco_gla_bwd(g["q"], g["k"], g["v"], g["log_alpha"], saved, g["do"],
                                   g["dS_final"], P=P, K=K, C=C, path=path))
     torch.cuda.synchronize()
+    z.check_device_status()  # no bounded device wait gave up
     return out
 
 
