@@ -48,8 +48,8 @@ def kernel_bytes_per_token(dk, dv, L, e=E, C=64):
     st = dk * dv * 4 / L  # one fp32 state per segment, per token
     eb = dk * 4 / C       # e^{b_last}: one fp32 row per chunk, per token
     return {
-        # pass 1: read k, v, g; write one local state per segment
-        "chunk_state": e * (2 * dk + dv) + st,
+        # pass 1: read K~, v, e^{b_last}; write one local state per segment
+        "chunk_state": e * (dk + dv) + eb + st,
         "seg_scan_fwd": 2 * st,
         # decay pass: read q, k, g; write Q~, K~ and e^{b_last}
         "decay": e * 5 * dk + eb,
@@ -57,8 +57,8 @@ def kernel_bytes_per_token(dk, dv, L, e=E, C=64):
         "A": e * (2 * dk + C),
         # pass 2: read Q~, K~, A, v, e^{b_last} and S_in[p]; write o
         "fwd_out": e * (2 * dk + 2 * dv + C) + eb + st,
-        # bwd pre-pass: read q, do, g; write one adjoint state per segment
-        "dstate_local": e * (2 * dk + dv) + st,
+        # bwd pre-pass: read Q~, do, e^{b_last}; write one adjoint state per segment
+        "dstate_local": e * (dk + dv) + eb + st,
         "seg_scan_rev": 3 * st,
         # dv: read Q~, K~, A, do, e^{b_last} and D[p+1]; write dv
         "bwd_dv": e * (2 * dk + 2 * dv + C) + eb + st,
@@ -427,6 +427,9 @@ def main(argv=None):
     t_roof = max(op_bytes / (hbm_peak * 1e9), op_flops / (float(peaks["bf16_tflops"]) * 1e12))
     step_s = ms_step * 1e-3
     traffic = measured_traffic(path, dom, w.T * bh)
+    # every kernel's algorithmic bytes over its event-timed duration (GB/s)
+    kern_gbs = {k: kb[canonical_kernel(k)] * w.T * bh / (ms * 1e-3) / 1e9
+                for k, ms in kern_ms.items() if canonical_kernel(k) in kb and ms > 0}
     scan_ms = sum(v for k, v in kern_ms.items() if "seg_scan" in k)
 
     line = {
@@ -448,7 +451,7 @@ def main(argv=None):
                               "note": "ZeCO two-pass algorithmic bytes/flops per step vs "
                                       f"{peak_kind} peaks"},
         "device_status": "ok" if dev_status == 0 else f"error {dev_status}",
-        "kernels_ms": kern_ms, "overlap": overlap, "scan_share": scan_ms / sum(kern_ms.values()),
+        "kernels_ms": kern_ms, "kernels_gbs": kern_gbs, "overlap": overlap, "scan_share": scan_ms / sum(kern_ms.values()),
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
     }
