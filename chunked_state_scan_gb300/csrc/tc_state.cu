@@ -52,13 +52,17 @@ constexpr int kStateThreads = 512;  // 128 rows x 4 token quarters
 // stage loads the chunk's e^{b_last} row instead of the log_alpha tile and scales
 // the tile by a running product, with no exponential per element.
 template <int NT, bool REV, bool PRE>
-__global__ void __launch_bounds__(kStateThreads, 1)
+__global__ void __launch_bounds__(kStateThreads, PRE ? 2 : 1)
 tc_seg_state_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmG,
                     const __grid_constant__ CUtensorMap tmY, const float* __restrict__ Eb,
                     float* __restrict__ out, float* __restrict__ gamma, int64_t T, int dk, int dv,
                     int P, int64_t L, int slot_off) {
   constexpr int kBBytes = kTok * NT * 2;
-  constexpr int kStageBytes = kXBytes + kGBytes + kBBytes;
+  // PRE: the log_alpha slot holds only the e^{b_last} row; two stages of ~49 KB
+  // let two CTAs share an SM (one's barriers overlap the other's MMAs)
+  constexpr int SG = PRE ? 2 : kStages;
+  constexpr int GB = PRE ? 1024 : kGBytes;
+  constexpr int kStageBytes = kXBytes + GB + kBBytes;
   extern __shared__ __align__(1024) unsigned char smraw[];
   unsigned char* sm = (unsigned char*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
   __shared__ uint64_t tma_bar[kStages], mma_bar[kStages];
@@ -77,7 +81,7 @@ tc_seg_state_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
   const int nblk = (int)(L / kTok);
 
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < SG; ++s) {
       mbar_init(&tma_bar[s], 1);
       mbar_init(&mma_bar[s], 1);
     }
@@ -98,7 +102,7 @@ tc_seg_state_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
     return (int32_t)(row0 + (int64_t)b * kTok);
   };
   auto issue_tma = [&](int it) {
-    const int s = it % kStages;
+    const int s = it % SG;
     unsigned char* base = sm + s * kStageBytes;
     const int32_t r = blk_row(it);
     mbar_expect_tx(&tma_bar[s], PRE ? kXBytes + kM * 4 + kBBytes : kStageBytes);
@@ -108,7 +112,7 @@ tc_seg_state_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
     }
     if (PRE) bulk_load(base + kXBytes, Eb + (size_t)(r / kTok) * dk + i0, kM * 4, &tma_bar[s]);
     for (int nb = 0; nb < NT / 64; ++nb)
-      tma_load_2d(base + kXBytes + kGBytes + nb * 8192, &tmY, j0 + nb * 64, r, &tma_bar[s]);
+      tma_load_2d(base + kXBytes + GB + nb * 8192, &tmY, j0 + nb * 64, r, &tma_bar[s]);
   };
 
   if (tid == 0) issue_tma(0);
@@ -120,18 +124,18 @@ tc_seg_state_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
   const uint32_t a_sub = (uint32_t)(row & 7) * 2u;
 
   for (int it = 0; it < nblk; ++it) {
-    const int s = it % kStages;
+    const int s = it % SG;
     unsigned char* xbuf = sm + s * kStageBytes;
-    // prefetch the next stage (its buffers were last read by MMA it+1-kStages)
+    // prefetch the next stage (its buffers were last read by MMA it+1-SG)
     if (tid == 0 && it + 1 < nblk) {
-      const int jn = it + 1 - kStages;
-      if (jn >= 0 && !mbar_wait(&mma_bar[(it + 1) % kStages], (jn / kStages) & 1)) {
+      const int jn = it + 1 - SG;
+      if (jn >= 0 && !mbar_wait(&mma_bar[(it + 1) % SG], (jn / SG) & 1)) {
         atomicExch(&g_tc_status, 1);
         abort_flag = 1;
       }
       issue_tma(it + 1);
     }
-    if (!mbar_wait(&tma_bar[s], (it / kStages) & 1)) {
+    if (!mbar_wait(&tma_bar[s], (it / SG) & 1)) {
       atomicExch(&g_tc_status, 1);
       abort_flag = 1;
     }
@@ -209,7 +213,7 @@ tc_seg_state_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
     if (abort_flag) break;
     if (tid == 0) {
       tc_fence_after();
-      const uint32_t a0 = smem_u32(xbuf), b0 = a0 + kXBytes + kGBytes;
+      const uint32_t a0 = smem_u32(xbuf), b0 = a0 + kXBytes + GB;
       constexpr uint32_t id = idesc_bf16(kM, NT, true, true);
 #pragma unroll
       for (int kk = 0; kk < kTok / 16; ++kk) {
@@ -224,7 +228,7 @@ tc_seg_state_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
   const bool ok = !abort_flag;
   if (ok && warp < 4) {
     const int last = nblk - 1;
-    if (!mbar_wait(&mma_bar[last % kStages], (last / kStages) & 1)) atomicExch(&g_tc_status, 1);
+    if (!mbar_wait(&mma_bar[last % SG], (last / SG) & 1)) atomicExch(&g_tc_status, 1);
     tc_fence_after();
     float* orow = out + (((size_t)bh * (P + 1) + p + slot_off) * dk + i) * dv + j0;
 #pragma unroll 1
@@ -309,7 +313,7 @@ static cudaError_t launch_state(const Dims& d, const void* x, const void* y, con
       !make_tmap_bf16(&tg, PRE ? x : g, rows, (uint64_t)d.dk, kTok) ||
       !make_tmap_bf16(&ty, y, rows, (uint64_t)d.dv, kTok))
     return cudaErrorInvalidValue;
-  const int smem = kStages * (kXBytes + kGBytes + kTok * NT * 2) + 1024;
+  const int smem = (PRE ? 2 : kStages) * (kXBytes + (PRE ? 1024 : kGBytes) + kTok * NT * 2) + 1024;
   auto kern = tc_seg_state_kernel<NT, REV, PRE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
