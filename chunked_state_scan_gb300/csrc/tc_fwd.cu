@@ -77,7 +77,7 @@ tc_sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 __nv_bfloat16* __restrict__ o, int64_t T, int dv, int P, int64_t L) {
   using SM = FwdSmem<DK>;
   extern __shared__ __align__(1024) unsigned char smraw[];
-  unsigned char* sm = (unsigned char*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
+  unsigned char* sm = align1024(smraw);
   unsigned char* sV = sm + SM::kV;
   __shared__ uint64_t bar_x[2], bar_v, bar_g;
   __shared__ uint32_t tmem_base;

@@ -42,7 +42,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 tc_masked_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmY,
                  __nv_bfloat16* __restrict__ P, int64_t nchunks, int K) {
   extern __shared__ __align__(1024) unsigned char smraw[];
-  unsigned char* sm = (unsigned char*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
+  unsigned char* sm = align1024(smraw);
   __shared__ uint64_t full[kStages], empty[kStages], accfull[2], accempty[2];
   __shared__ uint32_t tmem_base;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;

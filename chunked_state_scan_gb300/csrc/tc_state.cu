@@ -64,7 +64,7 @@ tc_seg_state_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
   constexpr int GB = PRE ? 1024 : kGBytes;
   constexpr int kStageBytes = kXBytes + GB + kBBytes;
   extern __shared__ __align__(1024) unsigned char smraw[];
-  unsigned char* sm = (unsigned char*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
+  unsigned char* sm = align1024(smraw);
   __shared__ uint64_t tma_bar[kStages], mma_bar[kStages];
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
@@ -298,6 +298,20 @@ bool make_tmap_f32_plain(CUtensorMap* m, const void* base, uint64_t rows, uint64
   cuuint32_t es[2] = {1, 1};
   EncodeTiledFn enc = encode_tiled();
   return enc && enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base),
+                                gdim, gstr, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 2D bf16 tensor map, box_cols x box_rows, no swizzle (rows of box_cols * 2 bytes).
+bool make_tmap_bf16_plain(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                          uint32_t box_cols, uint32_t box_rows) {
+  cuuint64_t gdim[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t gstr[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  EncodeTiledFn enc = encode_tiled();
+  return enc && enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
                                 gdim, gstr, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                                 CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
