@@ -73,27 +73,45 @@ int resolve(const zeco_shape* s, const Dims& d) {
   return ZECO_PATH_SIMT;
 }
 
-// Scratch layout of one call: the backward's own buffers (bwd only), then, on
-// the tensor-core path, the operands computed once per call (decay_layout),
-// then, for the SCALAR / NONE decay forms, the broadcast log-decay and its
-// per-row gradient (forms_layout).
+// Scratch layout of one call: the backward's own buffers (bwd only), then, for
+// the backward on the tensor-core path, the score gradient dA, then, for the
+// SCALAR / NONE decay forms, the broadcast log-decay and its per-row gradient
+// (forms_layout).  The operands the forward computes once (decay_layout) live
+// in `saved`, not here.
 struct WsPlan {
   zeco::BwdWsLayout bwd;
-  zeco::DecayLayout decay;
+  size_t dA_off;  // backward on the tensor-core path: the score gradient dA
   zeco::FormsLayout forms;
-  bool uses_decay;
   size_t total;
 };
 
 WsPlan plan_ws(const Dims& d, int path, bool bwd) {
   WsPlan w;
   w.bwd = zeco::bwd_ws_layout(d);
-  const size_t base = bwd ? w.bwd.total : 0;
-  w.uses_decay = path == ZECO_PATH_TC && zeco::tc_uses_decay(d);
-  w.decay = zeco::decay_layout(d, base, bwd && zeco::tc_uses_dA(d));
-  w.forms = zeco::forms_layout(d, w.uses_decay ? w.decay.total : base, bwd);
+  size_t base = bwd ? w.bwd.total : 0;
+  w.dA_off = zeco::align_up(base, 256);
+  if (bwd && path == ZECO_PATH_TC && zeco::tc_uses_dA(d))
+    base = zeco::align_up(w.dA_off + zeco::scores_bytes(d), 256);
+  w.forms = zeco::forms_layout(d, base, bwd);
   w.total = w.forms.total;
   return w;
+}
+
+// Whether the forward keeps the tensor-core operands (Q~, K~, e^{b_last}, A) in
+// `saved` for the backward.
+bool keeps_ops(const Dims& d, int path) {
+  return path == ZECO_PATH_TC && zeco::tc_uses_decay(d);
+}
+
+zeco::TcOps tc_ops(const zeco::SavedLayout& sl, const void* saved, void* ws, size_t dA_off) {
+  char* b = (char*)saved;
+  zeco::TcOps o;
+  o.Qt = b + sl.ops.Qt_off;
+  o.Kt = b + sl.ops.Kt_off;
+  o.Eb = (float*)(b + sl.ops.Eb_off);
+  o.A = b + sl.ops.A_off;
+  o.dA = ws ? (char*)ws + dA_off : nullptr;
+  return o;
 }
 
 }  // namespace
@@ -138,7 +156,9 @@ const char* zeco_profile_kernel_name(int i) {
 size_t zeco_gla_saved_bytes(const zeco_shape* shape) {
   Dims d;
   if (check_shape(shape, &d) != ZECO_OK) return 0;
-  return zeco::saved_layout(d).total;
+  const int path = resolve(shape, d);
+  if (path < 0) return 0;
+  return zeco::saved_layout(d, keeps_ops(d, path)).total;
 }
 
 size_t zeco_gla_workspace_bytes(const zeco_shape* shape, int bwd) {
@@ -178,7 +198,7 @@ int zeco_gla_fwd(const zeco_shape* shape, const void* q, const void* k, const vo
   const WsPlan wp = plan_ws(d, path, false);
   if (wp.total > 0 && (!workspace || !aligned16(workspace))) return ZECO_ERR_ARG;
   if (ws_bytes < wp.total) return ZECO_ERR_WORKSPACE;
-  const zeco::SavedLayout sl = zeco::saved_layout(d);
+  const zeco::SavedLayout sl = zeco::saved_layout(d, keeps_ops(d, path));
   float* S_in = (float*)((char*)saved + sl.S_in_off);
   float* gamma = (float*)((char*)saved + sl.gamma_off);
   cudaStream_t st = (cudaStream_t)stream;
@@ -191,8 +211,8 @@ int zeco_gla_fwd(const zeco_shape* shape, const void* q, const void* k, const vo
   }
   if (e == cudaSuccess)
     e = path == ZECO_PATH_TC
-            ? zeco::tc_forward(d, q, k, v, g, S0, o, S_final, S_in, gamma, wp.decay, workspace,
-                               st)
+            ? zeco::tc_forward(d, q, k, v, g, S0, o, S_final, S_in, gamma,
+                               tc_ops(sl, saved, nullptr, 0), st)
             : zeco::simt_forward(d, q, k, v, g, S0, o, S_final, S_in, gamma, st);
   return e == cudaSuccess ? ZECO_OK : ZECO_ERR_CUDA;
 }
@@ -216,7 +236,7 @@ int zeco_gla_bwd(const zeco_shape* shape, const void* q, const void* k, const vo
   const WsPlan wp = plan_ws(d, path, true);
   const zeco::BwdWsLayout& wl = wp.bwd;
   if (ws_bytes < wp.total) return ZECO_ERR_WORKSPACE;
-  const zeco::SavedLayout sl = zeco::saved_layout(d);
+  const zeco::SavedLayout sl = zeco::saved_layout(d, keeps_ops(d, path));
   const float* S_in = (const float*)((const char*)saved + sl.S_in_off);
   const float* gamma = (const float*)((const char*)saved + sl.gamma_off);
   float* D = (float*)((char*)workspace + wl.D_off);
@@ -235,7 +255,7 @@ int zeco_gla_bwd(const zeco_shape* shape, const void* q, const void* k, const vo
   if (e == cudaSuccess)
     e = path == ZECO_PATH_TC
             ? zeco::tc_backward(d, q, k, v, g, S_in, gamma, d_o, dS_final, dq, dk, dv, dg, dS0, D,
-                                carry, qdq, wp.decay, workspace, st)
+                                carry, qdq, tc_ops(sl, saved, workspace, wp.dA_off), st)
             : zeco::simt_backward(d, q, k, v, g, S_in, gamma, d_o, dS_final, dq, dk, dv, dg,
                                   dS0, D, carry, qdq, st);
   if (e == cudaSuccess && d.decay == ZECO_DECAY_SCALAR)

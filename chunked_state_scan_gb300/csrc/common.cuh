@@ -18,42 +18,47 @@ struct Dims {
   int decay;  // zeco_decay
 };
 
-// Byte layout of the `saved` buffer and the backward workspace.
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Operands of the tensor-core sweeps computed once by the forward and kept in
+// `saved` for the backward: Q~, K~ [B,H,T,dk] bf16, e^{b_last} of every chunk
+// [B,H,T/64,dk] fp32 (tc_decay.cu) and the masked intra-chunk scores A
+// [B,H,T,64] bf16 (tc_scores.cu).
+struct DecayLayout {
+  size_t Qt_off, Kt_off, Eb_off, A_off, total;
+};
+// One [B,H,T,64] bf16 score array (A, or the backward's dA).
+inline size_t scores_bytes(const Dims& d) { return (size_t)d.B * d.H * d.T * 64 * 2; }
+inline DecayLayout decay_layout(const Dims& d, size_t base) {
+  DecayLayout l;
+  const size_t n = (size_t)d.B * d.H * d.T * d.dk;
+  l.Qt_off = align_up(base, 256);
+  l.Kt_off = align_up(l.Qt_off + n * 2, 256);
+  l.Eb_off = align_up(l.Kt_off + n * 2, 256);
+  l.A_off = align_up(l.Eb_off + n / 64 * sizeof(float), 256);
+  l.total = align_up(l.A_off + scores_bytes(d), 256);
+  return l;
+}
+
+// Byte layout of the `saved` buffer (with `ops`: followed by the operands
+// above) and of the backward workspace.
 struct SavedLayout {
-  size_t S_in_off, gamma_off, total;
+  size_t S_in_off, gamma_off;
+  DecayLayout ops;
+  size_t total;
 };
 struct BwdWsLayout {
   size_t D_off, carry_off, qdq_off, total;
 };
 
-inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
-
-// Operands of the tensor-core sweeps computed once per call: Q~, K~
-// [B,H,T,dk] bf16 and e^{b_last} of every chunk [B,H,T/64,dk] fp32
-// (tc_decay.cu), the masked intra-chunk scores A [B,H,T,64] bf16 and, with
-// `with_dA` (backward), their gradient dA [B,H,T,64] bf16 (tc_scores.cu).
-struct DecayLayout {
-  size_t Qt_off, Kt_off, Eb_off, A_off, dA_off, total;
-};
-inline DecayLayout decay_layout(const Dims& d, size_t base, bool with_dA) {
-  DecayLayout l;
-  const size_t n = (size_t)d.B * d.H * d.T * d.dk;
-  const size_t np = (size_t)d.B * d.H * d.T * 64 * 2;
-  l.Qt_off = align_up(base, 256);
-  l.Kt_off = align_up(l.Qt_off + n * 2, 256);
-  l.Eb_off = align_up(l.Kt_off + n * 2, 256);
-  l.A_off = align_up(l.Eb_off + n / 64 * sizeof(float), 256);
-  l.dA_off = align_up(l.A_off + np, 256);
-  l.total = with_dA ? align_up(l.dA_off + np, 256) : l.dA_off;
-  return l;
-}
-
-inline SavedLayout saved_layout(const Dims& d) {
+inline SavedLayout saved_layout(const Dims& d, bool ops) {
   SavedLayout s;
   const size_t bh = (size_t)d.B * d.H;
   s.S_in_off = 0;
   s.gamma_off = align_up(bh * (d.P + 1) * d.dk * d.dv * sizeof(float), 256);
-  s.total = align_up(s.gamma_off + bh * d.P * d.dk * sizeof(float), 256);
+  const size_t end = align_up(s.gamma_off + bh * d.P * d.dk * sizeof(float), 256);
+  s.ops = decay_layout(d, end);
+  s.total = ops ? s.ops.total : end;
   return s;
 }
 

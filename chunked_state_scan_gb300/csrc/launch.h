@@ -93,18 +93,27 @@ cudaError_t tc_bwd_qk(const Dims& d, const void* Qt, const void* Kt, const void*
                       const void* d_o, void* dq, void* dk, void* dg, float* D, float* carry,
                       float* qdq, cudaStream_t st);
 bool tc_supported(const Dims& d);
-// Whether the tensor-core path of this shape runs the decay pass (and so needs
-// decay_layout's buffers in its workspace).
+// Whether the tensor-core path of this shape runs the decay pass (its forward
+// then keeps decay_layout's operands in `saved` for the backward).
 bool tc_uses_decay(const Dims& d);
-// Whether its backward also runs tc_dA (and so needs decay_layout's dA buffer).
+// Whether its backward also runs tc_dA (and so needs a dA buffer in its workspace).
 bool tc_uses_dA(const Dims& d);
+// Device buffers of the operands computed once per forward (decay_layout) and
+// of the backward's score gradient dA [B,H,T,64] bf16.
+struct TcOps {
+  void* Qt;
+  void* Kt;
+  float* Eb;
+  void* A;
+  void* dA;
+};
 cudaError_t tc_forward(const Dims& d, const void* q, const void* k, const void* v,
                        const void* g, const float* S0, void* o, float* S_final, float* S_in,
-                       float* gamma, const DecayLayout& dl, void* ws, cudaStream_t st);
+                       float* gamma, const TcOps& ops, cudaStream_t st);
 cudaError_t tc_backward(const Dims& d, const void* q, const void* k, const void* v,
                         const void* g, const float* S_in, const float* gamma, const void* d_o,
                         const float* dS_final, void* dq, void* dk, void* dv, void* dg,
-                        float* dS0, float* D, float* carry, float* qdq, const DecayLayout& dl,
-                        void* ws, cudaStream_t st);
+                        float* dS0, float* D, float* carry, float* qdq, const TcOps& ops,
+                        cudaStream_t st);
 
 }  // namespace zeco

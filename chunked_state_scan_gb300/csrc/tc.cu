@@ -19,7 +19,7 @@ bool tc_uses_dA(const Dims& d) {
 // depend on the scan); pass 2 joins both.
 cudaError_t tc_forward(const Dims& d, const void* q, const void* k, const void* v,
                        const void* g, const float* S0, void* o, float* S_final, float* S_in,
-                       float* gamma, const DecayLayout& dl, void* ws, cudaStream_t st) {
+                       float* gamma, const TcOps& ops, cudaStream_t st) {
   if (!tc_fwd_supported(d)) {
     cudaError_t e = tc_chunk_state(d, k, v, g, nullptr, nullptr, S_in, gamma, st);
     if (e != cudaSuccess) return e;
@@ -27,11 +27,10 @@ cudaError_t tc_forward(const Dims& d, const void* q, const void* k, const void* 
     if (e != cudaSuccess) return e;
     return simt_fwd_out_bf16(d, q, k, v, g, S_in, o, st);
   }
-  char* w = (char*)ws;
-  void* Qt = w + dl.Qt_off;
-  void* Kt = w + dl.Kt_off;
-  float* Eb = (float*)(w + dl.Eb_off);
-  void* A = w + dl.A_off;
+  void* Qt = ops.Qt;
+  void* Kt = ops.Kt;
+  float* Eb = ops.Eb;
+  void* A = ops.A;
   cudaError_t e = tc_decay(d, q, k, g, Qt, Kt, Eb, st);
   if (e != cudaSuccess) return e;
   const Fork f = fork_begin(st);
@@ -45,14 +44,14 @@ cudaError_t tc_forward(const Dims& d, const void* q, const void* k, const void* 
   return tc_fwd_out(d, Qt, Kt, v, A, Eb, S_in, o, st);
 }
 
-// Backward: the decay pass, then the pre-pass (on its Q~ and e^{b_last}), the
-// reverse scan and the dv sweep on the caller's stream while the scores and
-// their gradient run on the auxiliary stream.
+// Backward: Q~, K~, e^{b_last} and the masked scores A are the forward's (kept in
+// `saved`); the pre-pass, the reverse scan and the dv sweep run on the caller's
+// stream while the score gradient dA runs on the auxiliary stream.
 cudaError_t tc_backward(const Dims& d, const void* q, const void* k, const void* v,
                         const void* g, const float* S_in, const float* gamma, const void* d_o,
                         const float* dS_final, void* dq, void* dk, void* dv, void* dg,
-                        float* dS0, float* D, float* carry, float* qdq, const DecayLayout& dl,
-                        void* ws, cudaStream_t st) {
+                        float* dS0, float* D, float* carry, float* qdq, const TcOps& ops,
+                        cudaStream_t st) {
   if (!tc_fwd_supported(d)) {
     cudaError_t e = tc_dstate_local(d, q, d_o, g, nullptr, nullptr, D, st);
     if (e != cudaSuccess) return e;
@@ -60,26 +59,20 @@ cudaError_t tc_backward(const Dims& d, const void* q, const void* k, const void*
     if (e != cudaSuccess) return e;
     return simt_bwd_main_bf16(d, q, k, v, g, S_in, d_o, dq, dk, dv, dg, D, carry, qdq, st);
   }
-  char* w = (char*)ws;
-  void* Qt = w + dl.Qt_off;
-  void* Kt = w + dl.Kt_off;
-  float* Eb = (float*)(w + dl.Eb_off);
-  void* A = w + dl.A_off;
+  const void* Qt = ops.Qt;
+  const void* Kt = ops.Kt;
+  const float* Eb = ops.Eb;
+  const void* A = ops.A;
   const bool qk_tc = tc_uses_dA(d);
-  void* dA = w + dl.dA_off;
-  cudaError_t e = tc_decay(d, q, k, g, Qt, Kt, Eb, st);
-  if (e != cudaSuccess) return e;
+  void* dA = ops.dA;
   const Fork f = fork_begin(st);
-  e = tc_A(d, Qt, Kt, A, f.aux);
+  cudaError_t e = qk_tc ? tc_dA(d, d_o, v, dA, f.aux) : cudaSuccess;
   if (e == cudaSuccess) e = fork_mark(f, 0);
-  if (e == cudaSuccess && qk_tc) e = tc_dA(d, d_o, v, dA, f.aux);
-  if (e == cudaSuccess) e = fork_mark(f, 1);
   if (e != cudaSuccess) return e;
   e = tc_dstate_local(d, q, d_o, g, Qt, Eb, D, st);
   if (e == cudaSuccess) e = launch_seg_scan_rev(d, D, S_in, gamma, dS_final, dS0, carry, st);
-  if (e == cudaSuccess) e = fork_join(f, st, 0);
   if (e == cudaSuccess) e = tc_bwd_dv(d, Qt, Kt, d_o, A, Eb, D, dv, st);
-  if (e == cudaSuccess) e = fork_join(f, st, 1);
+  if (e == cudaSuccess) e = fork_join(f, st, 0);
   if (e != cudaSuccess) return e;
   if (qk_tc) return tc_bwd_qk(d, Qt, Kt, v, g, Eb, dA, S_in, d_o, dq, dk, dg, D, carry, qdq, st);
   return simt_bwd_dqk_bf16(d, q, k, v, g, S_in, d_o, dq, dk, dg, D, carry, qdq, st);

@@ -56,8 +56,11 @@
 // the MMAs; warp 18 joins the epilogue's barrier after it has read a receive
 // buffer and hands the buffer back (locally and to the other three CTAs): the
 // epilogue threads have output stores in flight, and a release issued by them
-// waits behind those; warp 18 has none.  The epilogue's first thread copies
-// the epilogue factors two chunks ahead.  The partials are received
+// waits behind those; warp 18 has none (and its arrives are relaxed: the reads
+// they release were performed before the barrier).  The epilogue's first
+// thread copies the epilogue factors two chunks ahead and stores each chunk's
+// outputs (dq or dk, and q.dq or dlog_alpha) by TMA from a staging tile that
+// the epilogue threads fill.  The partials are received
 // double-buffered, so that the four CTAs of a cluster need not move in
 // lockstep.
 #include <cuda.h>
@@ -97,21 +100,30 @@ constexpr int kMsX = 0, kMsU = 2 * kTile, kMsZ = 4 * kTile, kMsP = 6 * kTile, kM
 constexpr int kMsStage = 7 * kTile + 1024;
 constexpr int kMsStages = 2;
 // epilogue stage (this CTA's 32 rows, no swizzle): Y = Q~ (fwd) / K~ (rev) and
-// G = log_alpha [64 t][32 i] bf16; QD = q.dq [64 t][32 i] fp32 (rev)
+// G = log_alpha [64 t][32 i] bf16; QD = q.dq [64 t][32 i] fp32 (rev only)
 constexpr int kEpY = 0, kEpG = kC * kOwn * 2, kEpQD = 2 * kC * kOwn * 2;
-constexpr int kEpStage = kEpQD + kC * kOwn * 4;
 constexpr int kEpStages = 2;
 constexpr int kRS = kC + 4;                    // row stride of a received partial (floats)
 constexpr int kSlot = kOwn * kRS;              // one sender's [32 rows][kRS] fp32 (floats)
-constexpr int kOffMs = 0;
-constexpr int kOffEp = kOffMs + kMsStages * kMsStage;
-constexpr int kOffRcv = kOffEp + kEpStages * kEpStage;  // [2 buffers][4 slots by sender rank]
-constexpr int kOffGq = kOffRcv + 2 * kRanks * kSlot * 4; // sums of log_alpha per 16 tokens [4][32]
-constexpr int kOffQS = kOffGq + 4 * kOwn * 4;           // reverse: dg-term sums per 16 tokens
-constexpr int kOffRun = kOffQS + 4 * kOwn * 4;          // reverse: dg suffix carried per row
-constexpr int kSmem = kOffRun + kOwn * 4;
-static_assert(kMsStage % 1024 == 0 && kEpStage % 1024 == 0, "stage alignment");
-static_assert(kSmem + 1024 <= 227 * 1024, "shared memory");
+template <bool REV>
+struct QkSmem {
+  static constexpr int kEpStage = REV ? kEpQD + kC * kOwn * 4 : kEpQD;
+  static constexpr int kOffMs = 0;
+  static constexpr int kOffEp = kOffMs + kMsStages * kMsStage;
+  static constexpr int kOffRcv = kOffEp + kEpStages * kEpStage;  // [2 buffers][4 slots by sender]
+  // output staging of the TMA stores, [64 t][32 i] each: dq / dk (bf16), then
+  // q.dq (fwd, fp32) or dlog_alpha (rev, bf16)
+  static constexpr int kOffStg = kOffRcv + 2 * kRanks * kSlot * 4;
+  static constexpr int kStgAux = kC * kOwn * 2;
+  static constexpr int kStgBytes = kStgAux + kC * kOwn * (REV ? 2 : 4);
+  static constexpr int kOffGq = kOffStg + kStgBytes;   // sums of log_alpha per 16 tokens [4][32]
+  static constexpr int kOffQS = kOffGq + 4 * kOwn * 4;  // reverse: dg-term sums per 16 tokens
+  static constexpr int kOffRun = kOffQS + 4 * kOwn * 4; // reverse: dg suffix carried per row
+  static constexpr int kSmem = kOffRun + kOwn * 4;
+  static_assert(kMsStage % 1024 == 0 && kEpStage % 1024 == 0 && kOffStg % 1024 == 0,
+                "stage alignment");
+  static_assert(kSmem + 1024 <= 227 * 1024, "shared memory");
+};
 
 __device__ int g_qk_status = 0;
 
@@ -120,12 +132,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmU,
                  const __grid_constant__ CUtensorMap tmZ, const __grid_constant__ CUtensorMap tmP,
                  const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmG,
-                 const __grid_constant__ CUtensorMap tmQD, const float* __restrict__ Eb,
-                 const float* __restrict__ S_src, const float* __restrict__ carry,
-                 __nv_bfloat16* __restrict__ out, __nv_bfloat16* __restrict__ dg,
-                 float* __restrict__ qdq, int64_t T, int dk, int P, int64_t L) {
+                 const __grid_constant__ CUtensorMap tmQD, const __grid_constant__ CUtensorMap tmOut,
+                 const __grid_constant__ CUtensorMap tmAux, const float* __restrict__ Eb,
+                 const float* __restrict__ S_src, const float* __restrict__ carry, int64_t T,
+                 int dk, int P, int64_t L) {
+  using SM = QkSmem<REV>;
+  constexpr int kOffMs = SM::kOffMs, kOffEp = SM::kOffEp, kOffRcv = SM::kOffRcv;
+  constexpr int kOffGq = SM::kOffGq, kOffQS = SM::kOffQS, kOffRun = SM::kOffRun;
+  constexpr int kEpStage = SM::kEpStage;
   extern __shared__ __align__(1024) unsigned char smraw[];
   unsigned char* sm = align1024(smraw);
+  __nv_bfloat16* stgO = reinterpret_cast<__nv_bfloat16*>(sm + SM::kOffStg);  // dq / dk
+  unsigned char* stgA = sm + SM::kOffStg + SM::kStgAux;                      // q.dq / dlog_alpha
   float* sRcv = reinterpret_cast<float*>(sm + kOffRcv);
   float* sGq = reinterpret_cast<float*>(sm + kOffGq);
   float* sQS = reinterpret_cast<float*>(sm + kOffQS);
@@ -269,11 +287,14 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
 #pragma unroll 1
     for (int it = 0; it < nc; ++it) {
       asm volatile("bar.sync 2, 160;" ::: "memory");
+      // relaxed: the epilogue's reads of the buffer were performed before the
+      // barrier, and a release arrive would wait for the epilogue's output
+      // stores in flight (thousands of cycles per chunk)
       if (lane == 0 && it + 2 < nc && ok) {
-        mbar_arrive(&consumed[it & 1]);
+        mbar_arrive_relaxed(&consumed[it & 1]);
         const uint32_t mine = mine0 + 8u * (uint32_t)(it & 1);
         for (uint32_t q = 0; q < (uint32_t)kRanks; ++q)
-          if (q != rank) mbar_arrive_remote(map_to_rank(mine, q));
+          if (q != rank) mbar_arrive_remote_relaxed(map_to_rank(mine, q));
       }
       __syncwarp();
     }
@@ -447,6 +468,9 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
           acc[4 * c + 3] += v4.w;
         }
       }
+      // the previous chunk's output stores have read the staging tile, which is
+      // rewritten after the barrier
+      if (leader) bulk_wait_read_all();
       // every epilogue thread has read buffer rb: warp 18 hands it back
       __syncwarp();
       asm volatile("bar.sync 2, 160;" ::: "memory");
@@ -454,7 +478,7 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
       //      K~ (rev), q.dq (rev)
       wait(&ep_full[s], (uint32_t)((it / kEpStages) & 1));
       const unsigned char* ep = sm + kOffEp + s * kEpStage;
-      const size_t base = (size_t)(chunk_row(n) + 16 * eq) * dk + i0 + ec;
+      const int sb = 16 * eq * kOwn + er;  // staging element of (token 16 eq, row er)
       float gl[16], xa[16], term[16];
 #pragma unroll
       for (int u = 0; u < 16; ++u) {
@@ -471,7 +495,7 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
       for (int u = 0; u < 16; ++u) {
         gs += gl[u];
         if (!REV)
-          qdq[base + (size_t)u * dk] = xa[u];
+          reinterpret_cast<float*>(stgA)[sb + u * kOwn] = xa[u];
         else
           ssum += term[u];
       }
@@ -489,20 +513,30 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
 #pragma unroll
       for (int u = 0; u < 16; ++u) {
         bsum += gl[u];
-        out[base + (size_t)u * dk] = __float2bfloat16_rn(acc[u] * __expf(REV ? -bsum : bsum));
+        stgO[sb + u * kOwn] = __float2bfloat16_rn(acc[u] * __expf(REV ? -bsum : bsum));
       }
+      float runq = 0.f;
       if (REV) {
-        float runq = sRun[er];
+        runq = sRun[er];
         for (int q2 = 3; q2 > eq; --q2) runq += sQS[q2 * 32 + er];
 #pragma unroll
         for (int u = 15; u >= 0; --u) {
           runq += term[u];
-          dg[base + (size_t)u * dk] = __float2bfloat16_rn(runq);
+          reinterpret_cast<__nv_bfloat16*>(stgA)[sb + u * kOwn] = __float2bfloat16_rn(runq);
         }
-        epi_sync();
-        if (eq == 0) sRun[er] = runq;  // suffix through the whole chunk
+      }
+      // the chunk's outputs leave by TMA from the staging tile
+      fence_async_smem();
+      epi_sync();
+      if (REV && eq == 0) sRun[er] = runq;  // suffix through the whole chunk
+      if (leader) {
+        const int32_t r = chunk_row(n), x = i0 + kOwn * (int)rank;
+        tma_store_2d(&tmOut, stgO, x, r);
+        tma_store_2d(&tmAux, stgA, x, r);
+        bulk_commit();
       }
     }
+    if (leader) bulk_wait_all();
     // the last factor copies have landed (normally seen already)
     if (leader)
       for (int it = issued > kEpStages ? issued - kEpStages : 0; it < issued; ++it)
@@ -521,11 +555,11 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
 template <bool REV>
 cudaError_t launch_qk(const Dims& d, const CUtensorMap& tx, const CUtensorMap& tu,
                       const CUtensorMap& tz, const CUtensorMap& tp, const CUtensorMap& ty,
-                      const CUtensorMap& tg, const CUtensorMap& tqd, const float* Eb,
-                      const float* S_src, const float* carry, void* out, void* dg, float* qdq,
-                      cudaStream_t st) {
+                      const CUtensorMap& tg, const CUtensorMap& tqd, const CUtensorMap& tout,
+                      const CUtensorMap& taux, const float* Eb, const float* S_src,
+                      const float* carry, cudaStream_t st) {
   auto kern = tc_bwd_qk_kernel<REV>;
-  const int smem = kSmem + 1024;
+  const int smem = QkSmem<REV>::kSmem + 1024;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -540,9 +574,8 @@ cudaError_t launch_qk(const Dims& d, const CUtensorMap& tx, const CUtensorMap& t
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, tx, tu, tz, tp, ty, tg, tqd, Eb, S_src, carry,
-                            (__nv_bfloat16*)out, (__nv_bfloat16*)dg, qdq, d.T, (int)d.dk, d.P,
-                            d.L);
+  return cudaLaunchKernelEx(&cfg, kern, tx, tu, tz, tp, ty, tg, tqd, tout, taux, Eb, S_src,
+                            carry, d.T, (int)d.dk, d.P, d.L);
 }
 
 }  // namespace
@@ -556,7 +589,7 @@ cudaError_t tc_bwd_qk(const Dims& d, const void* Qt, const void* Kt, const void*
                       const void* d_o, void* dq, void* dk, void* dg, float* D, float* carry,
                       float* qdq, cudaStream_t st) {
   // swizzled [64 t][64] tiles for the MMAs; plain [64 t][32 i] tiles for the epilogue
-  CUtensorMap tqs, tks, tv, tdo, tp, tqp, tkp, tgp, tqd;
+  CUtensorMap tqs, tks, tv, tdo, tp, tqp, tkp, tgp, tqd, tdq, tdk, tdg;
   const uint64_t rows = (uint64_t)(d.B * d.H * d.T);
   if (!make_tmap_bf16(&tqs, Qt, rows, d.dk, kC) || !make_tmap_bf16(&tks, Kt, rows, d.dk, kC) ||
       !make_tmap_bf16(&tv, v, rows, d.dv, kC) || !make_tmap_bf16(&tdo, d_o, rows, d.dv, kC) ||
@@ -564,13 +597,16 @@ cudaError_t tc_bwd_qk(const Dims& d, const void* Qt, const void* Kt, const void*
       !make_tmap_bf16_plain(&tqp, Qt, rows, d.dk, kOwn, kC) ||
       !make_tmap_bf16_plain(&tkp, Kt, rows, d.dk, kOwn, kC) ||
       !make_tmap_bf16_plain(&tgp, g, rows, d.dk, kOwn, kC) ||
-      !make_tmap_f32_plain(&tqd, qdq, rows, d.dk, kOwn, kC))
+      !make_tmap_f32_plain(&tqd, qdq, rows, d.dk, kOwn, kC) ||
+      !make_tmap_bf16_plain(&tdq, dq, rows, d.dk, kOwn, kC) ||
+      !make_tmap_bf16_plain(&tdk, dk, rows, d.dk, kOwn, kC) ||
+      !make_tmap_bf16_plain(&tdg, dg, rows, d.dk, kOwn, kC))
     return cudaErrorInvalidValue;
   cudaError_t e =
-      launch_qk<false>(d, tks, tv, tdo, tp, tqp, tgp, tqd, Eb, S_in, carry, dq, dg, qdq, st);
+      launch_qk<false>(d, tks, tv, tdo, tp, tqp, tgp, tqd, tdq, tqd, Eb, S_in, carry, st);
   prof_mark("tc_bwd_dq", st);
   if (e != cudaSuccess) return e;
-  e = launch_qk<true>(d, tqs, tdo, tv, tp, tkp, tgp, tqd, Eb, D, carry, dk, dg, qdq, st);
+  e = launch_qk<true>(d, tqs, tdo, tv, tp, tkp, tgp, tqd, tdk, tdg, Eb, D, carry, st);
   prof_mark("tc_bwd_dk", st);
   return e;
 }

@@ -305,3 +305,67 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* u) {
 }
 }  // namespace tc
 }  // namespace zeco
+
+namespace zeco {
+namespace tc {
+// L2 prefetch of the tile at (x, y) of a tensor map (no shared memory, no
+// completion): brings later chunks' operands from HBM into L2 ahead of the
+// copies that the pipeline stages can hold.
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+// L2 prefetch of `bytes` contiguous bytes (16-byte aligned, a multiple of 16).
+__device__ __forceinline__ void bulk_prefetch(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
+                   reinterpret_cast<uint64_t>(src)),
+               "r"(bytes)
+               : "memory");
+}
+}  // namespace tc
+}  // namespace zeco
+
+namespace zeco {
+namespace tc {
+// Relaxed arrives (no release fence): for handing back a buffer whose reads
+// were all performed before a barrier the arriving thread has passed.  A
+// release arrive would first wait for every memory operation in flight,
+// including unrelated global stores, to complete.
+__device__ __forceinline__ void mbar_arrive_relaxed(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.relaxed.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t remote_bar) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar)
+               : "memory");
+}
+}  // namespace tc
+}  // namespace zeco
+
+namespace zeco {
+namespace tc {
+// TMA tile store shared -> global at (x, y) of a tensor map, in this thread's
+// current bulk-async group.  The shared source must have been written before a
+// fence_async_smem() by the writing threads.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int32_t x,
+                                             int32_t y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_u32(src)), "r"(x), "r"(y)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// This thread's committed bulk stores have finished reading their shared source.
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// This thread's committed bulk stores have completed.
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+}  // namespace tc
+}  // namespace zeco

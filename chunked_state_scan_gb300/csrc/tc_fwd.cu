@@ -17,8 +17,9 @@
 // One CTA owns (b, h, segment, 128 d_v columns) and keeps S^T (lanes = d_v
 // column j, TMEM columns = d_k row i) in fp32 in tensor memory, plus a bf16
 // copy of S^T that is the A operand (read from TMEM) of o^T = S^T Q~^T.
-// Q~, K~, e^{b_last} (tc_decay.cu) and the masked scores A (tc_scores.cu)
-// arrive by TMA one chunk ahead, so a chunk is one group of MMAs plus the
+// Q~, K~, e^{b_last} (tc_decay.cu), the masked scores A (tc_scores.cu) and
+// the V tile arrive by TMA one chunk ahead (two buffers each; later chunks are
+// prefetched into L2), so a chunk is one group of MMAs plus the
 // state pass; the output accumulator is double-buffered so that warps 0-7
 // write chunk n-1 while the tensor cores run chunk n.  Thread 256 issues the
 // MMAs and thread 288 the copies, away from the epilogue warps.
@@ -55,6 +56,12 @@ constexpr int kNV = 128;      // d_v columns per CTA
 constexpr int kThreads = 512;  // 16 warps
 constexpr uint32_t kColS16 = 256, kColO = 384;
 constexpr int kMmaTid = 256, kTmaTid = 288;
+#ifndef ZECO_PF_SWEEP
+#define ZECO_PF_SWEEP 2
+#endif
+// chunks ahead whose operands are prefetched into L2 (the shared memory holds
+// the current and the next chunk); <= 1: none
+constexpr int kPf = ZECO_PF_SWEEP;
 
 __device__ int g_fwd_status = 0;
 
@@ -65,8 +72,9 @@ struct FwdSmem {
   static constexpr int kE = kP + kC * kC * 2;  // e^{b_last} [DK] fp32
   static constexpr int kXBuf = (kE + DK * 4 + 1023) / 1024 * 1024;
   static constexpr int kX = 0;               // 2 buffers (chunk parity)
-  static constexpr int kV = 2 * kXBuf;
-  static constexpr int kBytes = kV + kNV * kC * 2;
+  static constexpr int kV = 2 * kXBuf;       // V / do tiles, 2 buffers (chunk parity)
+  static constexpr int kVBuf = kNV * kC * 2;
+  static constexpr int kBytes = kV + 2 * kVBuf;
 };
 
 template <int DK, bool BWD>
@@ -79,7 +87,7 @@ tc_sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   extern __shared__ __align__(1024) unsigned char smraw[];
   unsigned char* sm = align1024(smraw);
   unsigned char* sV = sm + SM::kV;
-  __shared__ uint64_t bar_x[2], bar_v, bar_g;
+  __shared__ uint64_t bar_x[2], bar_v[2], bar_g;
   __shared__ uint32_t tmem_base;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -95,7 +103,8 @@ tc_sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   if (tid == 0) {
     mbar_init(&bar_x[0], 1);
     mbar_init(&bar_x[1], 1);
-    mbar_init(&bar_v, 1);
+    mbar_init(&bar_v[0], 1);
+    mbar_init(&bar_v[1], 1);
     mbar_init(&bar_g, 1);
     fence_mbar_init();
   }
@@ -124,14 +133,31 @@ tc_sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     tma_load_2d(xb + SM::kP, &tmP, 0, r, &bar_x[buf]);
     bulk_load(xb + SM::kE, Eb + (size_t)(r / kC) * DK, DK * 4, &bar_x[buf]);
   };
-  auto issue_v = [&](int n) {
+  auto issue_v = [&](int n, int buf) {
     const int32_t r = (int32_t)(row0 + (int64_t)n * kC);
-    mbar_expect_tx(&bar_v, kNV * kC * 2);
-    for (int b = 0; b < kNV / 64; ++b) tma_load_2d(sV + b * 8192, &tmV, j0 + b * 64, r, &bar_v);
+    unsigned char* vb = sV + buf * SM::kVBuf;
+    mbar_expect_tx(&bar_v[buf], kNV * kC * 2);
+    for (int b = 0; b < kNV / 64; ++b)
+      tma_load_2d(vb + b * 8192, &tmV, j0 + b * 64, r, &bar_v[buf]);
+  };
+  // L2 prefetch of chunk n's operands (the tiles shared by the d_v tiles of a
+  // segment, by the first of them only)
+  auto prefetch = [&](int n) {
+    const int32_t r = (int32_t)(row0 + (int64_t)n * kC);
+    if (blockIdx.x == 0) {
+      for (int b = 0; b < DK / 64; ++b) {
+        tma_prefetch_2d(&tmQ, b * 64, r);
+        tma_prefetch_2d(&tmK, b * 64, r);
+      }
+      tma_prefetch_2d(&tmP, 0, r);
+      bulk_prefetch(Eb + (size_t)(r / kC) * DK, DK * 4);
+    }
+    for (int b = 0; b < kNV / 64; ++b) tma_prefetch_2d(&tmV, j0 + b * 64, r);
   };
   if (tid == kTmaTid) {
     issue_x(BWD ? nc - 1 : 0, 0);
-    issue_v(BWD ? nc - 1 : 0);
+    issue_v(BWD ? nc - 1 : 0, 0);
+    for (int it = 1; it < kPf && it < nc; ++it) prefetch(BWD ? nc - 1 - it : it);
   }
 
   // ---- initial state: S^T fp32 (and, forward, its bf16 copy) from the state
@@ -203,11 +229,16 @@ tc_sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     __syncthreads();
     // the next chunk's tiles go to the other buffer (its last readers, the MMAs
     // and the state pass of the previous chunk, have completed)
-    if (tid == kTmaTid && it + 1 < nc) issue_x(BWD ? n - 1 : n + 1, xbuf ^ 1);
+    if (tid == kTmaTid && it + 1 < nc) {
+      issue_x(BWD ? n - 1 : n + 1, xbuf ^ 1);
+      issue_v(BWD ? n - 1 : n + 1, xbuf ^ 1);
+      if (kPf > 1 && it + kPf < nc) prefetch(BWD ? n - kPf : n + kPf);
+    }
     // ------------------------------------------------ the chunk's MMAs
     if (tid == kMmaTid) {
       tc_fence_after();
-      const uint32_t q0 = smem_u32(sQ), k0 = smem_u32(sK), v0 = smem_u32(sV), p0 = smem_u32(sP);
+      const uint32_t q0 = smem_u32(sQ), k0 = smem_u32(sK), p0 = smem_u32(sP);
+      const uint32_t v0 = smem_u32(sV + xbuf * SM::kVBuf);
       const uint32_t oc = tmem + kColO + (uint32_t)xbuf * 64;
       // forward:  o^T  = S^T  Q~^T   (M = 128 columns j, N = 64 tokens t, K = DK; A from TMEM)
       // backward: dv^T = dS^T K~^T   (M = 128 columns j, N = 64 tokens s, K = DK; A from TMEM)
@@ -220,7 +251,7 @@ tc_sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           const uint64_t xd = sdesc_sw128(x0 + kb * 8192 + kk * 32, 16, 1024);
           umma_bf16_ta(oc, tmem + kColS16 + kb * 32 + kk * 8, xd, idO, (kb | kk) ? 1u : 0u);
         }
-      if (!mbar_wait(&bar_v, par)) atomicExch(&g_fwd_status, 1);
+      if (!mbar_wait(&bar_v[xbuf], (uint32_t)((it >> 1) & 1))) atomicExch(&g_fwd_status, 1);
       tc_fence_after();
       // forward:  o^T  += V^T  A^T  (B = A, K = s contiguous: K-major)
       // backward: dv^T += do^T A    (B = A, K = t rows, N = s contiguous: MN-major)
@@ -248,7 +279,6 @@ tc_sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     if (warp < 8 && it > 0) epilogue(BWD ? n + 1 : n - 1, xbuf ^ 1);
     if (!mbar_wait(&bar_g, par)) atomicExch(&g_fwd_status, 1);
     tc_fence_after();
-    if (tid == kTmaTid && it + 1 < nc) issue_v(BWD ? n - 1 : n + 1);  // V buffer is free now
     // forward: S <- e^{b_last} .* S, refresh the bf16 copy for the next chunk
     if (!BWD) state_pass(sE);
     tc_fence_before();

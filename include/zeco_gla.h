@@ -123,7 +123,17 @@ int64_t zeco_gla_segments(const zeco_shape *shape);
  * Bytes of the `saved` buffer written by zeco_gla_fwd and read by
  * zeco_gla_bwd: the incoming global state of every segment, S_in
  * [B,H,P_eff+1,dk,dv] fp32 (S_in[0] = S0, S_in[P_eff] = S_final), then the
- * segment decays gamma [B,H,P_eff,dk] fp32.  Returns 0 for an invalid shape.
+ * segment decays gamma [B,H,P_eff,dk] fp32.  When the shape resolves to the
+ * tensor-core path with its decay pass (d_k in {128, 256}, d_v a multiple of
+ * 128, C = 64), `saved` also keeps the operands the forward computes once
+ * and the backward reads again instead of recomputing them: the
+ * decay-weighted Q~ = q .* e^{b} and K~ = k .* e^{-b} [B,H,T,dk] bf16 (Pith
+ * review of ZeCO, minor comment 4; b the cumulative log-decay from the chunk
+ * start), e^{b_last} of every 64-token chunk [B,H,T/64,dk] fp32 and the masked
+ * intra-chunk scores A = Q~ K~^T [B,H,T,64] bf16 (row t holds its chunk's 64
+ * scores).  The size depends on the resolved path, so the forward and the
+ * backward must be given the same shape, path included.  Returns 0 for an
+ * invalid or unsupported shape.
  */
 size_t zeco_gla_saved_bytes(const zeco_shape *shape);
 
@@ -134,12 +144,11 @@ size_t zeco_gla_saved_bytes(const zeco_shape *shape);
  * [B,H,P_eff+1,dk,dv] fp32, one dlog_alpha carry row per segment [B,H,P_eff,dk] fp32,
  * and q .* dq in fp32 [B,H,T,dk] (dlog_alpha is a long suffix sum of
  * q .* dq - k .* dk that cancels heavily, so its terms are kept in fp32).
- * On the tensor-core path both directions also hold the decay-weighted
- * operands of the chunked form (Pith review of ZeCO, minor comment 4):
- * Q~ = q .* e^{b} and K~ = k .* e^{-b} [B,H,T,dk] bf16 and e^{b_last} of every
- * chunk [B,H,T/64,dk] fp32, b being the cumulative log-decay from the chunk
- * start.  Returns 0 when no scratch is needed or the shape is invalid or
- * unsupported.
+ * On the tensor-core path the backward also holds the masked gradient of the
+ * intra-chunk scores dA = do v^T [B,H,T,64] bf16.  The SCALAR and NONE decay
+ * forms add the log-decay broadcast to [B,H,T,dk] (both directions) and its
+ * per-row gradient (backward).  Returns 0 when no scratch is needed or the
+ * shape is invalid or unsupported.
  */
 size_t zeco_gla_workspace_bytes(const zeco_shape *shape, int bwd);
 

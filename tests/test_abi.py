@@ -46,16 +46,17 @@ def test_sizes_follow_the_layout(lib):
     s = _shape()
     state = 4 * 65 * 256 * 512 * 4
     gam = 4 * 64 * 256 * 4
-    assert z.saved_bytes(s) == state + gam
-    qdq = 4 * (1 << 20) * 256 * 4
-    # tensor-core path: Q~ and K~ (bf16), e^{b_last} per 64-token chunk (fp32) and
-    # the masked intra-chunk scores [B,H,T,64] (bf16)
+    # tensor-core path: the forward keeps Q~ and K~ (bf16), e^{b_last} per 64-token
+    # chunk (fp32) and the masked intra-chunk scores [B,H,T,64] (bf16) in `saved`
     decay = (2 * 4 * (1 << 20) * 256 * 2 + 4 * (1 << 20) // 64 * 256 * 4
              + 4 * (1 << 20) * 64 * 2)
+    assert z.saved_bytes(s) == state + gam + decay
+    assert z.saved_bytes(_shape(path="simt")) == state + gam
+    qdq = 4 * (1 << 20) * 256 * 4
     # backward only: the masked intra-chunk score gradients [B,H,T,64] bf16
     dA = 4 * (1 << 20) * 64 * 2
-    assert z.workspace_bytes(s, True) == state + gam + qdq + decay + dA
-    assert z.workspace_bytes(s, False) == decay
+    assert z.workspace_bytes(s, True) == state + gam + qdq + dA
+    assert z.workspace_bytes(s, False) == 0
     # the SIMT path keeps no decay-weighted operands
     simt = _shape(path="simt", dtype="f32", dk=64, dv=64)
     st64 = 4 * 65 * 64 * 64 * 4
@@ -94,9 +95,11 @@ def test_null_and_misaligned_pointers_are_rejected(lib):
     assert lib.zeco_gla_fwd(ctypes.byref(s), *args, None, None, None, ok, None, 0, None) == -1
     assert lib.zeco_gla_fwd(ctypes.byref(s), bad, ok, ok, ok, None, ok, None, ok, None, 0,
                             None) == -1
-    # forward on the tensor-core path: workspace missing, then too small
-    assert lib.zeco_gla_fwd(ctypes.byref(s), *args, None, ok, None, ok, None, 0, None) == -1
-    assert lib.zeco_gla_fwd(ctypes.byref(s), *args, None, ok, None, ok, ok, 16, None) == -3
+    # forward with the scalar decay form (it needs scratch for the broadcast
+    # log-decay): workspace missing, then too small
+    sc = _shape(T=4096, P=4, decay="scalar")
+    assert lib.zeco_gla_fwd(ctypes.byref(sc), *args, None, ok, None, ok, None, 0, None) == -1
+    assert lib.zeco_gla_fwd(ctypes.byref(sc), *args, None, ok, None, ok, ok, 16, None) == -3
     # workspace too small for the backward
     rc = lib.zeco_gla_bwd(ctypes.byref(s), ok, ok, ok, ok, ok, ok, None, ok, ok, ok, ok, None,
                           ok, 16, None)
@@ -143,7 +146,7 @@ def test_segment_count_fills_the_gpu(lib):
     # 8-segment forward at 131K tokens: split in two
     assert z.segments(_shape(T=131072, P=8, K=4)) == 16
     # the saved buffer follows the effective count
-    s = _shape(T=16384, P=1, K=1)
+    s = _shape(T=16384, P=1, K=1, path="simt")
     assert z.saved_bytes(s) == 4 * 17 * 256 * 512 * 4 + 4 * 16 * 256 * 4
     # too short to split (fewer than 4 chunks per sub-segment)
     assert z.segments(_shape(T=512, P=2, K=8)) == 2
