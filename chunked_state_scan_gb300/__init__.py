@@ -71,6 +71,8 @@ def load_library(path: str = LIB_PATH):
             lib.zeco_strerror.restype = ctypes.c_char_p
             lib.zeco_gla_resolve_path.argtypes = [sp]
             lib.zeco_gla_resolve_path.restype = ctypes.c_int
+            lib.zeco_selftest_bounded_wait.argtypes = [vp]
+            lib.zeco_selftest_bounded_wait.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -124,6 +126,14 @@ def check_device_status() -> None:
     """Raise ZecoError if a bounded device wait gave up since the last check
     (synchronise the streams of the calls to cover first)."""
     _check(load_library().zeco_check_device_status())
+
+
+def selftest_bounded_wait(stream=None) -> None:
+    """Launch the library's diagnostic kernel whose single wait can never
+    complete (it gives up after 2 s and records ZECO_ERR_TIMEOUT for
+    check_device_status)."""
+    st = stream if stream is not None else torch.cuda.current_stream()
+    _check(load_library().zeco_selftest_bounded_wait(ctypes.c_void_p(st.cuda_stream)))
 
 
 def set_overlap(on: bool) -> None:

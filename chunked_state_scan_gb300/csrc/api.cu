@@ -265,7 +265,8 @@ int zeco_gla_bwd(const zeco_shape* shape, const void* q, const void* k, const vo
 
 int zeco_check_device_status(void) {
   const int v[] = {zeco::tc_state_take_status(), zeco::tc_fwd_take_status(),
-                   zeco::tc_scores_take_status(), zeco::tc_bwd_qk_take_status()};
+                   zeco::tc_scores_take_status(), zeco::tc_bwd_qk_take_status(),
+                   zeco::selftest_take_status()};
   int rc = ZECO_OK;
   for (int x : v) {
     if (x < 0) return ZECO_ERR_CUDA;

@@ -26,6 +26,7 @@ int tc_bwd_qk_take_status();
 int tc_fwd_take_status();
 int tc_scores_take_status();
 int tc_state_take_status();
+int selftest_take_status();
 
 // ---- decay forms (decay_forms.cu) --------------------------------------
 // gx[b,h,t,i] = g[b,h,t] (SCALAR) or 0 (NONE)

@@ -49,20 +49,23 @@
 // parity; copies run two chunks ahead; the exchange and epilogue of a chunk
 // overlap the next chunks.
 //
-// Warp roles (608 threads): warps 0-7 state (warps w and w + 4 share TMEM lane
+// Warp roles (704 threads): warps 0-7 state (warps w and w + 4 share TMEM lane
 // quarter w % 4, each half of the columns); warps 8-11 exchange (lane quarter
-// w - 8 of the accumulator goes to CTA w - 8); warps 12-15 epilogue (16 tokens
-// each of this CTA's 32 rows); warp 16 copies the MMA operands; warp 17 issues
-// the MMAs; warp 18 joins the epilogue's barrier after it has read a receive
-// buffer and hands the buffer back (locally and to the other three CTAs): the
-// epilogue threads have output stores in flight, and a release issued by them
-// waits behind those; warp 18 has none (and its arrives are relaxed: the reads
-// they release were performed before the barrier).  The epilogue's first
-// thread copies the epilogue factors two chunks ahead and stores each chunk's
-// outputs (dq or dk, and q.dq or dlog_alpha) by TMA from a staging tile that
-// the epilogue threads fill.  The partials are received
-// double-buffered, so that the four CTAs of a cluster need not move in
-// lockstep.
+// w - 8 of the accumulator goes to CTA w - 8); warps 12-19 epilogue in two
+// groups of four that take alternate chunks (receive buffer, factor stage and
+// named barriers by chunk parity), each warp 16 tokens of this CTA's 32 rows,
+// so that one chunk's epilogue may take up to two chunk periods; warp 20
+// copies the MMA operands; warp 21 issues the MMAs.  A group's first thread
+// copies the group's epilogue factors two chunks ahead, hands each receive
+// buffer back once the group has read it (locally and to the other three
+// CTAs; relaxed arrives, as the reads they release were performed before the
+// group's barrier, while a release arrive would wait for memory operations in
+// flight), and stores the chunk's outputs (dq or dk, and q.dq or dlog_alpha)
+// by TMA from the factor stage, where the group's threads write each output
+// over the factor they read at the same position.  The reverse sweep's
+// dlog_alpha suffix passes from group to group through shared memory and an
+// mbarrier.  The partials are received double-buffered, so that the four CTAs
+// of a cluster need not move in lockstep.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -87,8 +90,8 @@ constexpr int kDV = 512;     // d_v
 constexpr int kNB = 128;     // d_v columns per CTA
 constexpr int kRanks = 4;    // CTAs per cluster
 constexpr int kOwn = 32;     // rows finished per CTA
-constexpr int kThreads = 608;
-constexpr int kWarpEx = 8, kWarpEpi = 12, kWarpLoad = 16, kWarpMma = 17, kWarpRel = 18;
+constexpr int kThreads = 704;
+constexpr int kWarpEx = 8, kWarpEpi = 12, kWarpLoad = 20, kWarpMma = 21;
 constexpr uint32_t kColS = 0, kColHL = 128, kColAcc = 384;
 
 // shared memory (bytes; tiles 1024-aligned)
@@ -99,31 +102,25 @@ constexpr int kTile = kC * 64 * 2;            // one [64 t][64] bf16 tile, 128-b
 constexpr int kMsX = 0, kMsU = 2 * kTile, kMsZ = 4 * kTile, kMsP = 6 * kTile, kMsE = 7 * kTile;
 constexpr int kMsStage = 7 * kTile + 1024;
 constexpr int kMsStages = 2;
-// epilogue stage (this CTA's 32 rows, no swizzle): Y = Q~ (fwd) / K~ (rev) and
-// G = log_alpha [64 t][32 i] bf16; QD = q.dq [64 t][32 i] fp32 (rev only)
+// epilogue stage (this CTA's 32 rows, no swizzle), one per epilogue group:
+// Y = Q~ (fwd) / K~ (rev) and G = log_alpha [64 t][32 i] bf16, QD = q.dq
+// [64 t][32 i] fp32 (loaded by the reverse sweep).  The outputs are staged in
+// place for their TMA stores: dq / dk over Y, q.dq (fwd) over QD, dlog_alpha
+// (rev) over G -- each thread overwrites only the elements it has read.
 constexpr int kEpY = 0, kEpG = kC * kOwn * 2, kEpQD = 2 * kC * kOwn * 2;
+constexpr int kEpStage = kEpQD + kC * kOwn * 4;
 constexpr int kEpStages = 2;
 constexpr int kRS = kC + 4;                    // row stride of a received partial (floats)
 constexpr int kSlot = kOwn * kRS;              // one sender's [32 rows][kRS] fp32 (floats)
-template <bool REV>
-struct QkSmem {
-  static constexpr int kEpStage = REV ? kEpQD + kC * kOwn * 4 : kEpQD;
-  static constexpr int kOffMs = 0;
-  static constexpr int kOffEp = kOffMs + kMsStages * kMsStage;
-  static constexpr int kOffRcv = kOffEp + kEpStages * kEpStage;  // [2 buffers][4 slots by sender]
-  // output staging of the TMA stores, [64 t][32 i] each: dq / dk (bf16), then
-  // q.dq (fwd, fp32) or dlog_alpha (rev, bf16)
-  static constexpr int kOffStg = kOffRcv + 2 * kRanks * kSlot * 4;
-  static constexpr int kStgAux = kC * kOwn * 2;
-  static constexpr int kStgBytes = kStgAux + kC * kOwn * (REV ? 2 : 4);
-  static constexpr int kOffGq = kOffStg + kStgBytes;   // sums of log_alpha per 16 tokens [4][32]
-  static constexpr int kOffQS = kOffGq + 4 * kOwn * 4;  // reverse: dg-term sums per 16 tokens
-  static constexpr int kOffRun = kOffQS + 4 * kOwn * 4; // reverse: dg suffix carried per row
-  static constexpr int kSmem = kOffRun + kOwn * 4;
-  static_assert(kMsStage % 1024 == 0 && kEpStage % 1024 == 0 && kOffStg % 1024 == 0,
-                "stage alignment");
-  static_assert(kSmem + 1024 <= 227 * 1024, "shared memory");
-};
+constexpr int kOffMs = 0;
+constexpr int kOffEp = kOffMs + kMsStages * kMsStage;
+constexpr int kOffRcv = kOffEp + kEpStages * kEpStage;   // [2 buffers][4 slots by sender]
+constexpr int kOffGq = kOffRcv + 2 * kRanks * kSlot * 4;  // per group: log_alpha sums [4][32]
+constexpr int kOffQS = kOffGq + 2 * 4 * kOwn * 4;        // per group: dg-term sums [4][32]
+constexpr int kOffRun = kOffQS + 2 * 4 * kOwn * 4;       // reverse: dg suffix carried per row
+constexpr int kSmem = kOffRun + kOwn * 4;
+static_assert(kMsStage % 1024 == 0 && kEpStage % 1024 == 0, "stage alignment");
+static_assert(kSmem + 1024 <= 227 * 1024, "shared memory");
 
 __device__ int g_qk_status = 0;
 
@@ -136,14 +133,8 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
                  const __grid_constant__ CUtensorMap tmAux, const float* __restrict__ Eb,
                  const float* __restrict__ S_src, const float* __restrict__ carry, int64_t T,
                  int dk, int P, int64_t L) {
-  using SM = QkSmem<REV>;
-  constexpr int kOffMs = SM::kOffMs, kOffEp = SM::kOffEp, kOffRcv = SM::kOffRcv;
-  constexpr int kOffGq = SM::kOffGq, kOffQS = SM::kOffQS, kOffRun = SM::kOffRun;
-  constexpr int kEpStage = SM::kEpStage;
   extern __shared__ __align__(1024) unsigned char smraw[];
   unsigned char* sm = align1024(smraw);
-  __nv_bfloat16* stgO = reinterpret_cast<__nv_bfloat16*>(sm + SM::kOffStg);  // dq / dk
-  unsigned char* stgA = sm + SM::kOffStg + SM::kStgAux;                      // q.dq / dlog_alpha
   float* sRcv = reinterpret_cast<float*>(sm + kOffRcv);
   float* sGq = reinterpret_cast<float*>(sm + kOffGq);
   float* sQS = reinterpret_cast<float*>(sm + kOffQS);
@@ -155,9 +146,12 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
   // partials of a chunk for this CTA's rows are in receive buffer rb;
   // consumed[rb]: this CTA's epilogue has read its receive buffer rb;
   // empty_from[q][rb]: CTA q has read its receive buffer rb (so this CTA's slot
-  // there may be rewritten); fin: every MMA of this CTA has completed.
+  // there may be rewritten); carry_full[g]: (reverse) the other epilogue group
+  // has left the dlog_alpha suffix of its chunk in sRun for group g; fin: every
+  // MMA of this CTA has completed.
   __shared__ uint64_t ms_full[kMsStages], ms_empty[kMsStages], ep_full[kEpStages], u_done,
-      s_ready, q_done[2], acc_free[2], rcv_full[2], consumed[2], empty_from[kRanks][2], fin;
+      s_ready, q_done[2], acc_free[2], rcv_full[2], consumed[2], empty_from[kRanks][2],
+      carry_full[2], fin;
   __shared__ uint32_t tmem_base;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -192,6 +186,7 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
       mbar_init(&rcv_full[rb], 32);  // the own-quarter warp's lanes (+ the peers' bytes)
       mbar_init(&consumed[rb], 1);
       for (int q = 0; q < kRanks; ++q) mbar_init(&empty_from[q][rb], 1);
+      mbar_init(&carry_full[rb], 32);  // the first warp of the other group
     }
     mbar_init(&fin, 1);
     fence_mbar_init();
@@ -278,25 +273,6 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
       }
       umma_commit(&fin);
       if (!mbar_wait(&fin, 0u)) atomicExch(&g_qk_status, 1);
-    }
-  } else if (warp == kWarpRel) {
-    // ---- after the epilogue has read chunk it out of receive buffer it % 2
-    //      (barrier 2, with the epilogue warps): hand the buffer back to this
-    //      CTA's own-quarter sender and to the three other CTAs
-    const uint32_t mine0 = smem_u32(&empty_from[rank][0]);
-#pragma unroll 1
-    for (int it = 0; it < nc; ++it) {
-      asm volatile("bar.sync 2, 160;" ::: "memory");
-      // relaxed: the epilogue's reads of the buffer were performed before the
-      // barrier, and a release arrive would wait for the epilogue's output
-      // stores in flight (thousands of cycles per chunk)
-      if (lane == 0 && it + 2 < nc && ok) {
-        mbar_arrive_relaxed(&consumed[it & 1]);
-        const uint32_t mine = mine0 + 8u * (uint32_t)(it & 1);
-        for (uint32_t q = 0; q < (uint32_t)kRanks; ++q)
-          if (q != rank) mbar_arrive_remote_relaxed(map_to_rank(mine, q));
-      }
-      __syncwarp();
     }
   } else if (warp < 8) {
     // ---- state warps: TMEM lane quarter lg (rows 32 lg ..), columns [64 h, 64 h + 64)
@@ -423,42 +399,56 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
       }
     }
   } else if (warp < kWarpLoad) {
-    // ---- epilogue: this CTA's 32 rows x tokens [16 eq, 16 eq + 16)
-    const int eq = warp - kWarpEpi, er = lane;
+    // ---- epilogue, two groups of four warps: group g takes the chunks of parity
+    //      g (receive buffer g, factor stage g), so that each group has two chunk
+    //      periods per chunk; warp eq of a group takes this CTA's 32 rows x tokens
+    //      [16 eq, 16 eq + 16)
+    const int g = (warp - kWarpEpi) >> 2, eq = (warp - kWarpEpi) & 3, er = lane;
     const int ec = kOwn * (int)rank + er;  // d_k row within the block finished here
-    const bool leader = tid == kWarpEpi * 32;
-    auto epi_sync = []() { asm volatile("bar.sync 1, 128;" ::: "memory"); };
-    // the epilogue factors of chunk `it` into stage it % 2 (issued by the leader)
+    const bool leader = eq == 0 && lane == 0;
+    const uint32_t bar_read = 1 + 2 * g, bar_sync = 2 + 2 * g;
+    auto grp_bar = [](uint32_t id) { asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory"); };
+    float* gq = sGq + g * 4 * kOwn;
+    float* qs = sQS + g * 4 * kOwn;
+    unsigned char* ep = sm + kOffEp + g * kEpStage;
+    __nv_bfloat16* epY = reinterpret_cast<__nv_bfloat16*>(ep + kEpY);
+    __nv_bfloat16* epG = reinterpret_cast<__nv_bfloat16*>(ep + kEpG);
+    float* epQD = reinterpret_cast<float*>(ep + kEpQD);
+    // the epilogue factors of chunk `it` into this group's stage (leader)
     auto issue_ep = [&](int it) {
-      const int s = it % kEpStages;
-      unsigned char* stg = sm + kOffEp + s * kEpStage;
       const int32_t r = chunk_row(chunk_of(it));
       const int x = i0 + kOwn * (int)rank;
-      mbar_expect_tx(&ep_full[s], 2 * kC * kOwn * 2 + (REV ? kC * kOwn * 4 : 0));
-      tma_load_2d(stg + kEpY, &tmY, x, r, &ep_full[s]);
-      tma_load_2d(stg + kEpG, &tmG, x, r, &ep_full[s]);
-      if (REV) tma_load_2d(stg + kEpQD, &tmQD, x, r, &ep_full[s]);
+      mbar_expect_tx(&ep_full[g], 2 * kC * kOwn * 2 + (REV ? kC * kOwn * 4 : 0));
+      tma_load_2d(ep + kEpY, &tmY, x, r, &ep_full[g]);
+      tma_load_2d(ep + kEpG, &tmG, x, r, &ep_full[g]);
+      if (REV) tma_load_2d(ep + kEpQD, &tmQD, x, r, &ep_full[g]);
     };
-    int issued = 0;  // chunks whose factors have been requested (leader)
+    int last = -1;  // leader: the last chunk whose factors were requested
     if (leader) {
       prefetch_tmap(&tmY);
       prefetch_tmap(&tmG);
       if (REV) prefetch_tmap(&tmQD);
-      for (; issued < nc && issued < kEpStages; ++issued) issue_ep(issued);
+      prefetch_tmap(&tmOut);
+      prefetch_tmap(&tmAux);
+      if (g < nc) {
+        issue_ep(g);
+        last = g;
+      }
     }
-    if (REV && eq == 0) sRun[er] = carry[((size_t)bh * P + p) * dk + i0 + ec];
+    if (REV && g == 0 && eq == 0) sRun[er] = carry[((size_t)bh * P + p) * dk + i0 + ec];
 #pragma unroll 1
-    for (int it = 0; it < nc; ++it) {
-      const int rb = it & 1, n = chunk_of(it), s = it % kEpStages;
+    for (int it = g; it < nc; it += 2) {
+      const int n = chunk_of(it);
+      const uint32_t ph = (uint32_t)((it >> 1) & 1);
       // ---- the four partials of my rows, summed in rank order
-      wait(&rcv_full[rb], (uint32_t)((it >> 1) & 1));
+      wait(&rcv_full[g], ph);
       float acc[16];
 #pragma unroll
       for (int u = 0; u < 16; ++u) acc[u] = 0.f;
 #pragma unroll
       for (int q = 0; q < kRanks; ++q) {
         const float4* src =
-            reinterpret_cast<const float4*>(sRcv + (rb * kRanks + q) * kSlot + er * kRS + 16 * eq);
+            reinterpret_cast<const float4*>(sRcv + (g * kRanks + q) * kSlot + er * kRS + 16 * eq);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           const float4 v4 = src[c];
@@ -468,80 +458,86 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
           acc[4 * c + 3] += v4.w;
         }
       }
-      // the previous chunk's output stores have read the staging tile, which is
-      // rewritten after the barrier
-      if (leader) bulk_wait_read_all();
-      // every epilogue thread has read buffer rb: warp 18 hands it back
-      __syncwarp();
-      asm volatile("bar.sync 2, 160;" ::: "memory");
+      // every thread of the group has read receive buffer g: hand it back to this
+      // CTA's own-quarter sender and to the three other CTAs.  Relaxed arrives:
+      // the reads were performed before the barrier, and a release arrive would
+      // wait for memory operations in flight (thousands of cycles per chunk).
+      grp_bar(bar_read);
+      if (leader && it + 2 < nc && ok) {
+        mbar_arrive_relaxed(&consumed[g]);
+        const uint32_t mine = smem_u32(&empty_from[rank][g]);
+        for (uint32_t q = 0; q < (uint32_t)kRanks; ++q)
+          if (q != rank) mbar_arrive_remote_relaxed(map_to_rank(mine, q));
+      }
       // ---- factors: e^{+-b_t} from log_alpha, the stored rounded Q~ (fwd) or
       //      K~ (rev), q.dq (rev)
-      wait(&ep_full[s], (uint32_t)((it / kEpStages) & 1));
-      const unsigned char* ep = sm + kOffEp + s * kEpStage;
-      const int sb = 16 * eq * kOwn + er;  // staging element of (token 16 eq, row er)
+      wait(&ep_full[g], ph);
+      const int sb = 16 * eq * kOwn + er;  // stage element of (token 16 eq, row er)
       float gl[16], xa[16], term[16];
 #pragma unroll
       for (int u = 0; u < 16; ++u) {
-        const int t = 16 * eq + u;
-        gl[u] = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(ep + kEpG)[t * kOwn + er]);
+        gl[u] = __bfloat162float(epG[sb + u * kOwn]);
         // the stored rounded Q~ (fwd) / K~ (rev) times the raw accumulator
         // (= q_eff dq / k_eff dk)
-        xa[u] = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(ep + kEpY)[t * kOwn + er]) *
-                acc[u];
-        if (REV) term[u] = reinterpret_cast<const float*>(ep + kEpQD)[t * kOwn + er] - xa[u];
+        xa[u] = __bfloat162float(epY[sb + u * kOwn]) * acc[u];
+        if (REV) term[u] = epQD[sb + u * kOwn] - xa[u];
       }
       float gs = 0.f, ssum = 0.f;
 #pragma unroll
       for (int u = 0; u < 16; ++u) {
         gs += gl[u];
         if (!REV)
-          reinterpret_cast<float*>(stgA)[sb + u * kOwn] = xa[u];
+          epQD[sb + u * kOwn] = xa[u];  // q.dq, staged for its store
         else
           ssum += term[u];
       }
-      sGq[eq * 32 + er] = gs;
-      if (REV) sQS[eq * 32 + er] = ssum;
-      // every factor read has been used in a value stored above, so stage s may be
-      // refilled with chunk it + 2
-      epi_sync();
-      if (leader && it + kEpStages < nc && ok) {
-        issue_ep(it + kEpStages);
-        issued = it + kEpStages + 1;
-      }
+      gq[eq * 32 + er] = gs;
+      if (REV) qs[eq * 32 + er] = ssum;
+      grp_bar(bar_sync);
       float bsum = 0.f;  // log-decay of the earlier 16-token quarters of the chunk
-      for (int q2 = 0; q2 < eq; ++q2) bsum += sGq[q2 * 32 + er];
+      for (int q2 = 0; q2 < eq; ++q2) bsum += gq[q2 * 32 + er];
 #pragma unroll
       for (int u = 0; u < 16; ++u) {
         bsum += gl[u];
-        stgO[sb + u * kOwn] = __float2bfloat16_rn(acc[u] * __expf(REV ? -bsum : bsum));
+        epY[sb + u * kOwn] = __float2bfloat16_rn(acc[u] * __expf(REV ? -bsum : bsum));
       }
       float runq = 0.f;
       if (REV) {
+        // the suffix of the chunks after this one, left by the other group
+        if (it > 0) wait(&carry_full[g], (uint32_t)(((it - 1) >> 1) & 1));
         runq = sRun[er];
-        for (int q2 = 3; q2 > eq; --q2) runq += sQS[q2 * 32 + er];
+        for (int q2 = 3; q2 > eq; --q2) runq += qs[q2 * 32 + er];
 #pragma unroll
         for (int u = 15; u >= 0; --u) {
           runq += term[u];
-          reinterpret_cast<__nv_bfloat16*>(stgA)[sb + u * kOwn] = __float2bfloat16_rn(runq);
+          epG[sb + u * kOwn] = __float2bfloat16_rn(runq);
         }
       }
-      // the chunk's outputs leave by TMA from the staging tile
+      // the chunk's outputs leave by TMA from the stage
       fence_async_smem();
-      epi_sync();
-      if (REV && eq == 0) sRun[er] = runq;  // suffix through the whole chunk
+      grp_bar(bar_sync);
+      if (REV && eq == 0) {
+        sRun[er] = runq;  // suffix through the whole chunk, for the other group
+        if (it + 1 < nc) mbar_arrive(&carry_full[g ^ 1]);
+      }
       if (leader) {
         const int32_t r = chunk_row(n), x = i0 + kOwn * (int)rank;
-        tma_store_2d(&tmOut, stgO, x, r);
-        tma_store_2d(&tmAux, stgA, x, r);
+        tma_store_2d(&tmOut, ep + kEpY, x, r);
+        tma_store_2d(&tmAux, ep + (REV ? kEpG : kEpQD), x, r);
         bulk_commit();
+        if (it + 2 < nc && ok) {
+          bulk_wait_read_all();  // the stores have read the stage: refill it
+          issue_ep(it + 2);
+          last = it + 2;
+        }
       }
     }
-    if (leader) bulk_wait_all();
-    // the last factor copies have landed (normally seen already)
-    if (leader)
-      for (int it = issued > kEpStages ? issued - kEpStages : 0; it < issued; ++it)
-        if (!mbar_wait(&ep_full[it % kEpStages], (uint32_t)((it / kEpStages) & 1)))
-          atomicExch(&g_qk_status, 1);
+    if (leader) {
+      bulk_wait_all();
+      // the last factor copy has landed (normally seen already)
+      if (last >= 0 && !mbar_wait(&ep_full[g], (uint32_t)((last >> 1) & 1)))
+        atomicExch(&g_qk_status, 1);
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -559,7 +555,7 @@ cudaError_t launch_qk(const Dims& d, const CUtensorMap& tx, const CUtensorMap& t
                       const CUtensorMap& taux, const float* Eb, const float* S_src,
                       const float* carry, cudaStream_t st) {
   auto kern = tc_bwd_qk_kernel<REV>;
-  const int smem = QkSmem<REV>::kSmem + 1024;
+  const int smem = kSmem + 1024;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};

@@ -10,10 +10,17 @@
 namespace zeco {
 namespace tc {
 
-// Poll limit of every mbarrier wait (each poll is a try_wait that itself
-// suspends for a while), so a wait that can never succeed ends the kernel with
-// an error status instead of hanging the GPU.
-constexpr uint32_t kWaitLimit = 1u << 26;
+// Time limit of every mbarrier wait: a wait that has not completed after this
+// many nanoseconds of %globaltimer gives up, so a wait that can never succeed
+// ends the kernel with an error status within seconds instead of hanging the
+// GPU.  (Legitimate waits here last microseconds.)
+constexpr uint64_t kWaitNs = 2000000000ull;
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -43,11 +50,12 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
-// Returns true when the phase with parity `parity` has completed; false after
-// kWaitLimit polls.
+// Returns true when the phase with parity `parity` has completed; false once
+// kWaitNs have passed without it (the clock is read only after polls fail).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   const uint32_t a = smem_u32(bar);
-  for (uint32_t it = 0; it < kWaitLimit; ++it) {
+  uint64_t t0 = 0;
+  for (uint32_t it = 0;; ++it) {
     uint32_t done;
     asm volatile(
         "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
@@ -56,8 +64,12 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
         : "r"(a), "r"(parity)
         : "memory");
     if (done) return true;
+    if ((it & 63u) == 63u) {
+      const uint64_t now = global_ns();
+      if (t0 == 0) t0 = now;
+      else if (now - t0 > kWaitNs) return false;
+    }
   }
-  return false;
 }
 
 // ------------------------------------------------------------------ TMA

@@ -205,8 +205,8 @@ int zeco_gla_bwd_noalloc(const zeco_shape *shape, const void *q, const void *k, 
 
 /*
  * Every wait of the tensor-core kernels on an mbarrier (a copy or an MMA group
- * to complete, a peer CTA's partial sums) gives up after a bounded number of
- * polls instead of hanging the GPU; the kernel then records it in a device
+ * to complete, a peer CTA's partial sums) gives up after 2 seconds (device
+ * %globaltimer) instead of hanging the GPU; the kernel then records it in a device
  * flag and continues, so that call's outputs are not valid.  This reads and
  * clears the flags of the current device: ZECO_OK when no wait gave up since
  * the last check, ZECO_ERR_TIMEOUT when one did, ZECO_ERR_CUDA when the flags
@@ -214,6 +214,16 @@ int zeco_gla_bwd_noalloc(const zeco_shape *shape, const void *q, const void *k, 
  * the calls it should cover have been synchronised.
  */
 int zeco_check_device_status(void);
+
+/*
+ * Diagnostic of the bounded waits above (the ZeCO pages have no counterpart):
+ * launches on `stream` one single-thread kernel whose mbarrier wait can never
+ * complete.  The wait gives up after its time limit (2 s), the kernel records
+ * it and returns; the next zeco_check_device_status() then reports
+ * ZECO_ERR_TIMEOUT and the CUDA context stays usable.  Returns ZECO_ERR_CUDA
+ * if the launch fails.
+ */
+int zeco_selftest_bounded_wait(zeco_stream_t stream);
 
 /* Static message for an error code (never NULL). */
 const char *zeco_strerror(int code);
