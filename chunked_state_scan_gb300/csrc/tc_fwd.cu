@@ -56,6 +56,9 @@ constexpr int kNV = 128;      // d_v columns per CTA
 constexpr int kThreads = 512;  // 16 warps
 constexpr uint32_t kColS16 = 256, kColO = 384;
 constexpr int kMmaTid = 256, kTmaTid = 288;
+// backward: the state pass after chunk n scales by the next chunk's e^{b_last},
+// so those rows come through a ring loaded two chunks ahead
+constexpr int kESlots = 3;
 #ifndef ZECO_PF_SWEEP
 #define ZECO_PF_SWEEP 2
 #endif
@@ -69,12 +72,13 @@ template <int DK>
 struct FwdSmem {
   static constexpr int kTile = DK * kC * 2;  // Q~ / K~ tile bytes
   static constexpr int kP = 2 * kTile;       // masked scores [64 t][64 s] bf16
-  static constexpr int kE = kP + kC * kC * 2;  // e^{b_last} [DK] fp32
-  static constexpr int kXBuf = (kE + DK * 4 + 1023) / 1024 * 1024;
+  static constexpr int kEx = kP + kC * kC * 2;  // forward: the chunk's e^{b_last} [DK] fp32
+  static constexpr int kXBuf = (kEx + DK * 4 + 1023) / 1024 * 1024;
   static constexpr int kX = 0;               // 2 buffers (chunk parity)
   static constexpr int kV = 2 * kXBuf;       // V / do tiles, 2 buffers (chunk parity)
   static constexpr int kVBuf = kNV * kC * 2;
-  static constexpr int kBytes = kV + 2 * kVBuf;
+  static constexpr int kE = kV + 2 * kVBuf;  // backward: e^{b_last} [DK] fp32, a ring of kESlots
+  static constexpr int kBytes = kE + kESlots * DK * 4;
 };
 
 template <int DK, bool BWD>
@@ -87,7 +91,7 @@ tc_sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   extern __shared__ __align__(1024) unsigned char smraw[];
   unsigned char* sm = align1024(smraw);
   unsigned char* sV = sm + SM::kV;
-  __shared__ uint64_t bar_x[2], bar_v[2], bar_g;
+  __shared__ uint64_t bar_x[2], bar_v[2], bar_e[kESlots], bar_u, bar_g;
   __shared__ uint32_t tmem_base;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -105,6 +109,8 @@ tc_sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     mbar_init(&bar_x[1], 1);
     mbar_init(&bar_v[0], 1);
     mbar_init(&bar_v[1], 1);
+    for (int k = 0; k < kESlots; ++k) mbar_init(&bar_e[k], 1);
+    mbar_init(&bar_u, 1);
     mbar_init(&bar_g, 1);
     fence_mbar_init();
   }
@@ -121,17 +127,31 @@ tc_sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   const uint32_t tmem = tmem_base;
   const uint32_t lane_off = (uint32_t)(lg * 32) << 16;
 
-  // Q~, K~ and masked-score tiles and the e^{b_last} row of chunk n into buffer `buf`
+  // Q~, K~ and masked-score tiles (forward: and the e^{b_last} row) of chunk n
+  // into buffer `buf`
   auto issue_x = [&](int n, int buf) {
     const int32_t r = (int32_t)(row0 + (int64_t)n * kC);
     unsigned char* xb = sm + SM::kX + buf * SM::kXBuf;
-    mbar_expect_tx(&bar_x[buf], 2 * SM::kTile + kC * kC * 2 + DK * 4);
+    mbar_expect_tx(&bar_x[buf], 2 * SM::kTile + kC * kC * 2 + (BWD ? 0 : DK * 4));
     for (int b = 0; b < DK / 64; ++b) {
       tma_load_2d(xb + b * 8192, &tmQ, b * 64, r, &bar_x[buf]);
       tma_load_2d(xb + SM::kTile + b * 8192, &tmK, b * 64, r, &bar_x[buf]);
     }
     tma_load_2d(xb + SM::kP, &tmP, 0, r, &bar_x[buf]);
-    bulk_load(xb + SM::kE, Eb + (size_t)(r / kC) * DK, DK * 4, &bar_x[buf]);
+    if (!BWD) bulk_load(xb + SM::kEx, Eb + (size_t)(r / kC) * DK, DK * 4, &bar_x[buf]);
+  };
+  // e^{b_last} of the chunk processed at iteration `it` into ring slot it % kESlots
+  auto issue_e = [&](int it) {
+    const int n = BWD ? nc - 1 - it : it;
+    const int k = it % kESlots;
+    const int32_t r = (int32_t)(row0 + (int64_t)n * kC);
+    mbar_expect_tx(&bar_e[k], DK * 4);
+    bulk_load(sm + SM::kE + k * DK * 4, Eb + (size_t)(r / kC) * DK, DK * 4, &bar_e[k]);
+  };
+  auto e_slot = [&](int it) -> const float* {  // waits for, and returns, iteration it's row
+    const int k = it % kESlots;
+    if (!mbar_wait(&bar_e[k], (uint32_t)((it / kESlots) & 1))) atomicExch(&g_fwd_status, 1);
+    return reinterpret_cast<const float*>(sm + SM::kE + k * DK * 4);
   };
   auto issue_v = [&](int n, int buf) {
     const int32_t r = (int32_t)(row0 + (int64_t)n * kC);
@@ -157,6 +177,8 @@ tc_sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   if (tid == kTmaTid) {
     issue_x(BWD ? nc - 1 : 0, 0);
     issue_v(BWD ? nc - 1 : 0, 0);
+    if (BWD)
+      for (int it = 0; it < kESlots - 1 && it < nc; ++it) issue_e(it);
     for (int it = 1; it < kPf && it < nc; ++it) prefetch(BWD ? nc - 1 - it : it);
   }
 
@@ -181,26 +203,37 @@ tc_sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     tmem_st_wait();
   }
 
-  // S^T (fp32) <- e^{b_last} .* S^T (column i scaled by sE[i]) and its bf16 copy
-  auto state_pass = [&](const float* sE) {
-    for (int c = cq * (DK / 4); c < (cq + 1) * (DK / 4); c += 32) {
-      float r[32];
-      tmem_ld32(tmem + lane_off + c, r);
-      tmem_ld_wait();
-      const float4* e4 = reinterpret_cast<const float4*>(sE + c);
+  // The state pass in two parts.  Part 1: S^T (fp32) <- e^{b_last} .* S^T (column
+  // i scaled by sE[i]), the scaled values kept in r; it needs only the chunk's
+  // state update.  Part 2: the bf16 copy of the scaled state (the A operand of
+  // the next chunk's output MMAs); it waits until this chunk's output MMAs have
+  // read the old copy.
+  constexpr int kQ = DK / 4;  // TMEM columns of one warp's quarter
+  auto scale_part = [&](const float* sE, float* r) {
+    const int c0 = cq * kQ;
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const float4 e = e4[u];
-        r[4 * u] *= e.x;
-        r[4 * u + 1] *= e.y;
-        r[4 * u + 2] *= e.z;
-        r[4 * u + 3] *= e.w;
-      }
-      tmem_st32(tmem + lane_off + c, r);
+    for (int c = 0; c < kQ; c += 32) tmem_ld32(tmem + lane_off + c0 + c, r + c);
+    tmem_ld_wait();
+    const float4* e4 = reinterpret_cast<const float4*>(sE + c0);
+#pragma unroll
+    for (int u = 0; u < kQ / 4; ++u) {
+      const float4 e = e4[u];
+      r[4 * u] *= e.x;
+      r[4 * u + 1] *= e.y;
+      r[4 * u + 2] *= e.z;
+      r[4 * u + 3] *= e.w;
+    }
+#pragma unroll
+    for (int c = 0; c < kQ; c += 32) tmem_st32(tmem + lane_off + c0 + c, r + c);
+  };
+  auto copy_part = [&](const float* r) {
+    const int c0 = cq * kQ;
+#pragma unroll
+    for (int c = 0; c < kQ; c += 32) {
       uint32_t h[16];
 #pragma unroll
-      for (int u = 0; u < 16; ++u) h[u] = pack_bf16(r[2 * u], r[2 * u + 1]);
-      tmem_st16(tmem + lane_off + kColS16 + c / 2, h);
+      for (int u = 0; u < 16; ++u) h[u] = pack_bf16(r[c + 2 * u], r[c + 2 * u + 1]);
+      tmem_st16(tmem + lane_off + kColS16 + (c0 + c) / 2, h);
     }
     tmem_st_wait();
   };
@@ -215,6 +248,16 @@ tc_sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     for (int u = 0; u < 32; ++u) op[(size_t)u * dv] = __float2bfloat16_rn(r[u]);
   };
 
+  // backward: the adjoint entering the first chunk (the segment's last) is
+  // scaled by that chunk's e^{b_last} before the chunk's products
+  if (BWD) {
+    float r[kQ];
+    scale_part(e_slot(0), r);
+    copy_part(r);
+  }
+  tc_fence_before();
+  __syncthreads();
+
   for (int it = 0; it < nc; ++it) {
     const int n = BWD ? (nc - 1 - it) : it;  // chunk index in the segment
     const uint32_t par = (uint32_t)(it & 1);
@@ -222,16 +265,15 @@ tc_sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     unsigned char* sQ = sm + SM::kX + xbuf * SM::kXBuf;
     unsigned char* sK = sQ + SM::kTile;
     unsigned char* sP = sQ + SM::kP;
-    const float* sE = reinterpret_cast<const float*>(sQ + SM::kE);  // e^{b_last}
     if (!mbar_wait(&bar_x[xbuf], (uint32_t)((it >> 1) & 1))) atomicExch(&g_fwd_status, 1);
-    if (BWD) state_pass(sE);
-    tc_fence_before();
-    __syncthreads();
-    // the next chunk's tiles go to the other buffer (its last readers, the MMAs
-    // and the state pass of the previous chunk, have completed)
+    // the next chunk's tiles go to the other buffers (their last readers, the MMAs
+    // and the state pass of the previous chunk, completed before the block barrier
+    // that ended the previous iteration)
     if (tid == kTmaTid && it + 1 < nc) {
       issue_x(BWD ? n - 1 : n + 1, xbuf ^ 1);
       issue_v(BWD ? n - 1 : n + 1, xbuf ^ 1);
+      // (slot (it + 2) % 3 was last read by the state pass of iteration it - 1)
+      if (BWD && it + kESlots - 1 < nc) issue_e(it + kESlots - 1);
       if (kPf > 1 && it + kPf < nc) prefetch(BWD ? n - kPf : n + kPf);
     }
     // ------------------------------------------------ the chunk's MMAs
@@ -240,29 +282,9 @@ tc_sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       const uint32_t q0 = smem_u32(sQ), k0 = smem_u32(sK), p0 = smem_u32(sP);
       const uint32_t v0 = smem_u32(sV + xbuf * SM::kVBuf);
       const uint32_t oc = tmem + kColO + (uint32_t)xbuf * 64;
-      // forward:  o^T  = S^T  Q~^T   (M = 128 columns j, N = 64 tokens t, K = DK; A from TMEM)
-      // backward: dv^T = dS^T K~^T   (M = 128 columns j, N = 64 tokens s, K = DK; A from TMEM)
-      constexpr uint32_t idO = idesc_bf16(128, 64, false, false);
-      const uint32_t x0 = BWD ? k0 : q0;
-#pragma unroll
-      for (int kb = 0; kb < DK / 64; ++kb)
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t xd = sdesc_sw128(x0 + kb * 8192 + kk * 32, 16, 1024);
-          umma_bf16_ta(oc, tmem + kColS16 + kb * 32 + kk * 8, xd, idO, (kb | kk) ? 1u : 0u);
-        }
       if (!mbar_wait(&bar_v[xbuf], (uint32_t)((it >> 1) & 1))) atomicExch(&g_fwd_status, 1);
       tc_fence_after();
-      // forward:  o^T  += V^T  A^T  (B = A, K = s contiguous: K-major)
-      // backward: dv^T += do^T A    (B = A, K = t rows, N = s contiguous: MN-major)
-      constexpr uint32_t idO2 = idesc_bf16(128, 64, true, BWD);
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        const uint64_t vd = sdesc_sw128(v0 + kk * 2048, 8192, 1024);
-        const uint64_t pd = BWD ? sdesc_sw128(p0 + kk * 2048, 8192, 1024)
-                                : sdesc_sw128(p0 + kk * 32, 16, 1024);
-        umma_bf16(oc, vd, pd, idO2, 1u);
-      }
+      // the state update first: its completion releases part 1 of the state pass
       // forward:  S^T  += V^T  K~   (M = 128 columns j, N = DK rows i, K = 64 tokens s)
       // backward: dS^T += do^T Q~   (M = 128 columns j, N = DK rows i, K = 64 tokens t)
       const uint32_t u0 = BWD ? q0 : k0;
@@ -273,14 +295,47 @@ tc_sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         const uint64_t ud = sdesc_sw128(u0 + kk * 2048, 8192, 1024);
         umma_bf16(tmem, vd, ud, idS, 1u);
       }
+      umma_commit(&bar_u);
+      // forward:  o^T  = S^T  Q~^T   (M = 128 columns j, N = 64 tokens t, K = DK; A from TMEM)
+      // backward: dv^T = dS^T K~^T   (M = 128 columns j, N = 64 tokens s, K = DK; A from TMEM)
+      // (A = the bf16 copy of the state before this chunk's update)
+      constexpr uint32_t idO = idesc_bf16(128, 64, false, false);
+      const uint32_t x0 = BWD ? k0 : q0;
+#pragma unroll
+      for (int kb = 0; kb < DK / 64; ++kb)
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t xd = sdesc_sw128(x0 + kb * 8192 + kk * 32, 16, 1024);
+          umma_bf16_ta(oc, tmem + kColS16 + kb * 32 + kk * 8, xd, idO, (kb | kk) ? 1u : 0u);
+        }
+      // forward:  o^T  += V^T  A^T  (B = A, K = s contiguous: K-major)
+      // backward: dv^T += do^T A    (B = A, K = t rows, N = s contiguous: MN-major)
+      constexpr uint32_t idO2 = idesc_bf16(128, 64, true, BWD);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const uint64_t vd = sdesc_sw128(v0 + kk * 2048, 8192, 1024);
+        const uint64_t pd = BWD ? sdesc_sw128(p0 + kk * 2048, 8192, 1024)
+                                : sdesc_sw128(p0 + kk * 32, 16, 1024);
+        umma_bf16(oc, vd, pd, idO2, 1u);
+      }
       umma_commit(&bar_g);
     }
+    __syncwarp();
     // ------------------------------------------------ the previous chunk's output
     if (warp < 8 && it > 0) epilogue(BWD ? n + 1 : n - 1, xbuf ^ 1);
+    // ------------------------------------------------ the state pass for the next chunk
+    //   forward:  S  <- e^{b_last}(this chunk) .* S
+    //   backward: dS <- e^{b_last}(next chunk) .* dS  (the adjoint carried to its tokens)
+    const bool more = it + 1 < nc;
+    float r[kQ];
+    if (more) {
+      if (!mbar_wait(&bar_u, par)) atomicExch(&g_fwd_status, 1);
+      tc_fence_after();
+      scale_part(BWD ? e_slot(it + 1) : reinterpret_cast<const float*>(sQ + SM::kEx), r);
+    }
     if (!mbar_wait(&bar_g, par)) atomicExch(&g_fwd_status, 1);
     tc_fence_after();
-    // forward: S <- e^{b_last} .* S, refresh the bf16 copy for the next chunk
-    if (!BWD) state_pass(sE);
+    if (more) copy_part(r);
     tc_fence_before();
     __syncthreads();
   }
