@@ -241,8 +241,9 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
       constexpr uint32_t idT = idesc_bf16(kKB, kC, false, false);
       for (int it = 0; it < nc; ++it) {
         const int s = it % kMsStages, b = it & 1;
-        wait(&s_ready, (uint32_t)(it & 1));  // state rescaled, hi/lo copy b written
+        // the operands first (normally long landed), then the state warps' hand-off
         wait(&ms_full[s], (uint32_t)((it / kMsStages) & 1));
+        wait(&s_ready, (uint32_t)(it & 1));  // state rescaled, hi/lo copy b written
         if (!ok) break;
         tc_fence_after();
         const uint32_t stg = smem_u32(sm + kOffMs + s * kMsStage);
@@ -348,11 +349,12 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
     pass(REV ? e_of(0) : 1.f, REV, 0);
     ready();
     for (int it = 0; it + 1 < nc; ++it) {
+      // forward: S_{n+1} = e^{b_last,n} (S_n + K~^T v); reverse: the next chunk's
+      // factor (read before the update completes, off the serial chain)
+      const float e = e_of(REV ? it + 1 : it);
       wait(&u_done, (uint32_t)(it & 1));
       __syncwarp();
       tc_fence_after();
-      // forward: S_{n+1} = e^{b_last,n} (S_n + K~^T v); reverse: the next chunk's factor
-      const float e = e_of(REV ? it + 1 : it);
       pass(e, true, (it + 1) & 1);
       ready();
     }
