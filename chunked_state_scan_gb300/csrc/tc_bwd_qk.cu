@@ -110,8 +110,11 @@ constexpr int kMsStages = 2;
 constexpr int kEpY = 0, kEpG = kC * kOwn * 2, kEpQD = 2 * kC * kOwn * 2;
 constexpr int kEpStage = kEpQD + kC * kOwn * 4;
 constexpr int kEpStages = 2;
-constexpr int kRS = kC + 4;                    // row stride of a received partial (floats)
-constexpr int kSlot = kOwn * kRS;              // one sender's [32 rows][kRS] fp32 (floats)
+// one sender's partial for this CTA's 32 rows, token-quad major: element (row,
+// t) at ((t / 4) * 32 + row) * 4 + t % 4, so that a warp's 16-byte store of four
+// tokens of its 32 rows covers 512 contiguous bytes and the epilogue's 16-byte
+// reads are conflict-free
+constexpr int kSlot = kOwn * kC;  // floats
 constexpr int kOffMs = 0;
 constexpr int kOffEp = kOffMs + kMsStages * kMsStage;
 constexpr int kOffRcv = kOffEp + kEpStages * kEpStage;   // [2 buffers][4 slots by sender]
@@ -380,18 +383,19 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
       if (it >= 2)
         wait((uint32_t)eq == rank ? &consumed[b] : &empty_from[eq][b],
              (uint32_t)(((it >> 1) - 1) & 1));
-      float* row = sRcv + (b * kRanks + (int)rank) * kSlot + lane * kRS;
+      float* slot = sRcv + (b * kRanks + (int)rank) * kSlot;
       if ((uint32_t)eq == rank) {
-        float4* d4 = reinterpret_cast<float4*>(row);
+        float4* d4 = reinterpret_cast<float4*>(slot);
 #pragma unroll
         for (int c = 0; c < kC / 4; ++c)
-          d4[c] = make_float4(a[4 * c], a[4 * c + 1], a[4 * c + 2], a[4 * c + 3]);
+          d4[c * 32 + lane] = make_float4(a[4 * c], a[4 * c + 1], a[4 * c + 2], a[4 * c + 3]);
       } else if (ok) {
-        const uint32_t dst = map_to_rank(smem_u32(row), (uint32_t)eq);
+        const uint32_t dst = map_to_rank(smem_u32(slot), (uint32_t)eq) + 16u * (uint32_t)lane;
         const uint32_t full = map_to_rank(smem_u32(&rcv_full[b]), (uint32_t)eq);
 #pragma unroll
         for (int c = 0; c < kC / 4; ++c)
-          st_async_v4(dst + 16 * c, a[4 * c], a[4 * c + 1], a[4 * c + 2], a[4 * c + 3], full);
+          st_async_v4(dst + 512u * (uint32_t)c, a[4 * c], a[4 * c + 1], a[4 * c + 2],
+                      a[4 * c + 3], full);
       }
       if ((uint32_t)eq == rank) {
         if (lane == 0)
@@ -449,11 +453,10 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
       for (int u = 0; u < 16; ++u) acc[u] = 0.f;
 #pragma unroll
       for (int q = 0; q < kRanks; ++q) {
-        const float4* src =
-            reinterpret_cast<const float4*>(sRcv + (g * kRanks + q) * kSlot + er * kRS + 16 * eq);
+        const float4* src = reinterpret_cast<const float4*>(sRcv + (g * kRanks + q) * kSlot);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          const float4 v4 = src[c];
+          const float4 v4 = src[(4 * eq + c) * 32 + er];
           acc[4 * c] += v4.x;
           acc[4 * c + 1] += v4.y;
           acc[4 * c + 2] += v4.z;
