@@ -98,9 +98,10 @@ constexpr uint32_t kColS = 0, kColHL = 128, kColAcc = 384;
 constexpr int kTile = kC * 64 * 2;            // one [64 t][64] bf16 tile, 128-byte swizzle
 // MMA stage: X = K~ (fwd) / Q~ (rev) [64 t][128 i]; U = v / do [64 t][128 j] (B of
 // the state update); Z = do / v [64 t][128 j] (B of dq^T / dk^T); P = masked dA
-// [64][64]; E = e^{b_last} of the 128 rows
-constexpr int kMsX = 0, kMsU = 2 * kTile, kMsZ = 4 * kTile, kMsP = 6 * kTile, kMsE = 7 * kTile;
-constexpr int kMsStage = 7 * kTile + 1024;
+// [64][64].  (The state warps read e^{b_last} of their rows straight from global
+// memory a chunk ahead, so the state chain never waits on a stage.)
+constexpr int kMsX = 0, kMsU = 2 * kTile, kMsZ = 4 * kTile, kMsP = 6 * kTile;
+constexpr int kMsStage = 7 * kTile;
 constexpr int kMsStages = 2;
 // epilogue stage (this CTA's 32 rows, no swizzle), one per epilogue group:
 // Y = Q~ (fwd) / K~ (rev) and G = log_alpha [64 t][32 i] bf16, QD = q.dq
@@ -120,8 +121,8 @@ constexpr int kOffEp = kOffMs + kMsStages * kMsStage;
 constexpr int kOffRcv = kOffEp + kEpStages * kEpStage;   // [2 buffers][4 slots by sender]
 constexpr int kOffGq = kOffRcv + 2 * kRanks * kSlot * 4;  // per group: log_alpha sums [4][32]
 constexpr int kOffQS = kOffGq + 2 * 4 * kOwn * 4;        // per group: dg-term sums [4][32]
-constexpr int kOffRun = kOffQS + 2 * 4 * kOwn * 4;       // reverse: dg suffix carried per row
-constexpr int kSmem = kOffRun + kOwn * 4;
+constexpr int kOffRun = kOffQS + 2 * 4 * kOwn * 4;       // reverse: dg carry into a chunk [2][32]
+constexpr int kSmem = kOffRun + 2 * kOwn * 4;
 static_assert(kMsStage % 1024 == 0 && kEpStage % 1024 == 0, "stage alignment");
 static_assert(kSmem + 1024 <= 227 * 1024, "shared memory");
 
@@ -176,7 +177,7 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
   if (tid == 0) {
     for (int s = 0; s < kMsStages; ++s) {
       mbar_init(&ms_full[s], 1);
-      mbar_init(&ms_empty[s], 1 + 8);  // the MMA commit + one arrive per state warp
+      mbar_init(&ms_empty[s], 1);  // the MMA commit
     }
     for (int s = 0; s < kEpStages; ++s) mbar_init(&ep_full[s], 1);
     mbar_init(&u_done, 1);
@@ -217,14 +218,13 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
         if (!ok) break;
         unsigned char* stg = sm + kOffMs + s * kMsStage;
         const int32_t r = chunk_row(chunk_of(it));
-        mbar_expect_tx(&ms_full[s], 7 * kTile + kKB * 4);
+        mbar_expect_tx(&ms_full[s], 7 * kTile);
         for (int b = 0; b < 2; ++b) {
           tma_load_2d(stg + kMsX + b * kTile, &tmX, i0 + 64 * b, r, &ms_full[s]);
           tma_load_2d(stg + kMsU + b * kTile, &tmU, j0 + 64 * b, r, &ms_full[s]);
           tma_load_2d(stg + kMsZ + b * kTile, &tmZ, j0 + 64 * b, r, &ms_full[s]);
         }
         tma_load_2d(stg + kMsP, &tmP, 0, r, &ms_full[s]);
-        bulk_load(stg + kMsE, Eb + (size_t)(r / kC) * dk + i0, kKB * 4, &ms_full[s]);
         issued = it + 1;
       }
       // the last copy into each stage has landed (normally seen long ago)
@@ -335,13 +335,10 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
       }
       tmem_st_wait();
     };
-    auto e_of = [&](int ie) {  // e^{b_last} of row `row` for the chunk processed at ie
-      const int se = ie % kMsStages;
-      wait(&ms_full[se], (uint32_t)((ie / kMsStages) & 1));
-      const float e = reinterpret_cast<const float*>(sm + kOffMs + se * kMsStage + kMsE)[row];
-      __syncwarp();
-      if (lane == 0 && ie + kMsStages < nc) mbar_arrive(&ms_empty[se]);  // E read
-      return e;
+    // e^{b_last} of row `row` for the chunk processed at iteration ie (1 past the end)
+    auto e_of = [&](int ie) -> float {
+      if (ie >= nc) return 1.f;
+      return __ldg(Eb + (size_t)(chunk_row(chunk_of(ie)) / kC) * dk + i0 + row);
     };
     auto ready = [&]() {
       tc_fence_before();
@@ -351,15 +348,17 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
     // the first chunk's copy (reverse: of the adjoint rescaled by that chunk's e^{b_last})
     pass(REV ? e_of(0) : 1.f, REV, 0);
     ready();
+    // forward: S_{n+1} = e^{b_last,n} (S_n + K~^T v); reverse: the next chunk's
+    // factor.  Each is loaded one iteration before it is used.
+    float e = e_of(REV ? 1 : 0);
     for (int it = 0; it + 1 < nc; ++it) {
-      // forward: S_{n+1} = e^{b_last,n} (S_n + K~^T v); reverse: the next chunk's
-      // factor (read before the update completes, off the serial chain)
-      const float e = e_of(REV ? it + 1 : it);
+      const float e_next = e_of(REV ? it + 2 : it + 1);
       wait(&u_done, (uint32_t)(it & 1));
       __syncwarp();
       tc_fence_after();
       pass(e, true, (it + 1) & 1);
       ready();
+      e = e_next;
     }
   } else if (warp < kWarpEpi) {
     // ---- exchange: lane quarter eq of the accumulator (rows 32 eq ..) to CTA eq,
@@ -506,12 +505,26 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
         bsum += gl[u];
         epY[sb + u * kOwn] = __float2bfloat16_rn(acc[u] * __expf(REV ? -bsum : bsum));
       }
-      float runq = 0.f;
       if (REV) {
-        // the suffix of the chunks after this one, left by the other group
+        // this chunk's total, and the part of it after this warp's 16 tokens
+        float tot = 0.f, after = 0.f;
+#pragma unroll
+        for (int q2 = 0; q2 < 4; ++q2) {
+          const float v = qs[q2 * 32 + er];
+          tot += v;
+          if (q2 > eq) after += v;
+        }
+        // the suffix of the chunks after this one (left by the other group in slot
+        // g); once the whole group has read it, the carry into the next chunk goes
+        // on at once -- the serial chain between the groups is one add per chunk
         if (it > 0) wait(&carry_full[g], (uint32_t)(((it - 1) >> 1) & 1));
-        runq = sRun[er];
-        for (int q2 = 3; q2 > eq; --q2) runq += qs[q2 * 32 + er];
+        const float cin = sRun[g * kOwn + er];
+        grp_bar(bar_read);
+        if (eq == 0) {
+          sRun[(g ^ 1) * kOwn + er] = cin + tot;
+          if (it + 1 < nc) mbar_arrive(&carry_full[g ^ 1]);
+        }
+        float runq = cin + after;
 #pragma unroll
         for (int u = 15; u >= 0; --u) {
           runq += term[u];
@@ -521,10 +534,6 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
       // the chunk's outputs leave by TMA from the stage
       fence_async_smem();
       grp_bar(bar_sync);
-      if (REV && eq == 0) {
-        sRun[er] = runq;  // suffix through the whole chunk, for the other group
-        if (it + 1 < nc) mbar_arrive(&carry_full[g ^ 1]);
-      }
       if (leader) {
         const int32_t r = chunk_row(n), x = i0 + kOwn * (int)rank;
         tma_store_2d(&tmOut, ep + kEpY, x, r);
