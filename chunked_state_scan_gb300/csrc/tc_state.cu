@@ -42,7 +42,10 @@ constexpr int kGBytes = kTok * kM * 2;  // 16 KB: log_alpha tile
 
 __device__ int g_tc_status = 0;  // set when a bounded wait gives up
 
-constexpr int kStateThreads = 512;  // 128 rows x 4 token quarters
+constexpr int kStateThreads = 512;  // compute threads: 128 rows x 4 token quarters
+// plus one producer warp that issues the copies (waiting for a stage's previous
+// MMAs without holding up the compute threads)
+constexpr int kStateBlock = kStateThreads + 32;
 
 // PRE: x is the decay pass's K~ = k e^{-b} (REV) or Q~ = q e^{b} (forward), and
 // the weight of a token of chunk n factors into one value per row and chunk:
@@ -52,7 +55,7 @@ constexpr int kStateThreads = 512;  // 128 rows x 4 token quarters
 // stage loads the chunk's e^{b_last} row instead of the log_alpha tile and scales
 // the tile by a running product, with no exponential per element.
 template <int NT, bool REV, bool PRE>
-__global__ void __launch_bounds__(kStateThreads, PRE ? 2 : 1)
+__global__ void __launch_bounds__(kStateBlock, PRE ? 2 : 1)
 tc_seg_state_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmG,
                     const __grid_constant__ CUtensorMap tmY, const float* __restrict__ Eb,
                     float* __restrict__ out, float* __restrict__ gamma, int64_t T, int dk, int dv,
@@ -115,7 +118,24 @@ tc_seg_state_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
       tma_load_2d(base + kXBytes + GB + nb * 8192, &tmY, j0 + nb * 64, r, &tma_bar[s]);
   };
 
-  if (tid == 0) issue_tma(0);
+  // the compute threads' barrier (the producer warp does not take part)
+  auto cbar = []() { asm volatile("bar.sync 1, %0;" ::"n"(kStateThreads) : "memory"); };
+  if (warp == kStateThreads / 32) {
+    // ---- producer: stage it once the MMAs that last read its buffers are done
+    if (lane == 0) {
+      for (int it = 0; it < nblk; ++it) {
+        const int jn = it - SG;
+        if (jn >= 0 && !mbar_wait(&mma_bar[it % SG], (jn / SG) & 1)) {
+          atomicExch(&g_tc_status, 1);
+          break;
+        }
+        issue_tma(it);
+      }
+    }
+    tc_fence_before();
+    __syncthreads();
+    return;
+  }
   float run = 0.f;  // log-decay of row i summed over the stages already done
   float run_f = 1.f;  // PRE: product of e^{b_last} over the chunks already done
   // row i of the tiles lives in MN block row/64, 16-byte chunk (row%64)/8, element row%8
@@ -126,15 +146,6 @@ tc_seg_state_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
   for (int it = 0; it < nblk; ++it) {
     const int s = it % SG;
     unsigned char* xbuf = sm + s * kStageBytes;
-    // prefetch the next stage (its buffers were last read by MMA it+1-SG)
-    if (tid == 0 && it + 1 < nblk) {
-      const int jn = it + 1 - SG;
-      if (jn >= 0 && !mbar_wait(&mma_bar[(it + 1) % SG], (jn / SG) & 1)) {
-        atomicExch(&g_tc_status, 1);
-        abort_flag = 1;
-      }
-      issue_tma(it + 1);
-    }
     if (!mbar_wait(&tma_bar[s], (it / SG) & 1)) {
       atomicExch(&g_tc_status, 1);
       abort_flag = 1;
@@ -148,7 +159,7 @@ tc_seg_state_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
         sF[tid] = run_f;
         if (!REV) run_f *= e;
       }
-      __syncthreads();
+      cbar();
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int c = tid + h * kStateThreads;  // 64 tokens x 2 row blocks x 8 groups
@@ -176,7 +187,7 @@ tc_seg_state_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
         gsum += gl[u];
       }
       Gq[qd][row] = gsum;
-      __syncthreads();
+      cbar();
       float off_q = run;  // log-decay from the processed stages plus the other quarters
       float stage = 0.f;
 #pragma unroll
@@ -209,7 +220,7 @@ tc_seg_state_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
       run += stage;
     }
     fence_async_smem();
-    __syncthreads();
+    cbar();
     if (abort_flag) break;
     if (tid == 0) {
       tc_fence_after();
@@ -224,7 +235,7 @@ tc_seg_state_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
       umma_commit(&mma_bar[s]);
     }
   }
-  __syncthreads();
+  cbar();
   const bool ok = !abort_flag;
   if (ok && warp < 4) {
     const int last = nblk - 1;
@@ -248,7 +259,6 @@ tc_seg_state_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, NT);
-  (void)lane;
 }
 
 // cuTensorMapEncodeTiled, looked up once through the runtime's driver entry
@@ -332,7 +342,7 @@ static cudaError_t launch_state(const Dims& d, const void* x, const void* y, con
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)(d.dv / NT), (unsigned)(d.dk / kM), (unsigned)(d.B * d.H * d.P));
-  kern<<<grid, kStateThreads, smem, st>>>(tx, tg, ty, Eb, out, gamma, d.T, (int)d.dk,
+  kern<<<grid, kStateBlock, smem, st>>>(tx, tg, ty, Eb, out, gamma, d.T, (int)d.dk,
                                           (int)d.dv, d.P, d.L, slot_off);
   return cudaGetLastError();
 }
