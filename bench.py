@@ -407,11 +407,11 @@ def main(argv=None):
         torch.cuda.synchronize(dev)
         lib.zeco_set_overlap(1)
         serial_ms = s0.elapsed_time(s1) / args.steps
-        aux_ms = sum(v for k, v in kern_ms.items() if canonical_kernel(k) in ("decay", "A", "dA"))
+        aux_ms = sum(v for k, v in kern_ms.items() if canonical_kernel(k) in ("A", "dA"))
         overlap = {"serial_ms": serial_ms, "overlapped_ms": ms_step, "aux_stream_ms": aux_ms,
                    "hidden_frac": (serial_ms - ms_step) / aux_ms if aux_ms > 0 else None,
-                   "note": "decay pass, masked scores and score gradient on a second stream, "
-                           "concurrent with the segment-state pass and the scan"}
+                   "note": "masked scores (forward) and score gradient (backward) on a second "
+                           "stream, concurrent with the segment-state passes and the scans"}
 
     # ---- roofline of the dominant kernel and of the whole step
     peaks, peak_kind = load_peaks()
