@@ -144,6 +144,22 @@ def test_bf16_tensor_core_path_shapes(z, B, H, T, dk, dv, P, K):
     _assert(errs, "bf16", f"tc B{B} H{H} T{T} dk{dk} dv{dv} P{P}")
 
 
+@pytest.mark.parametrize("B,H,T,dk,P,K", [(1, 1, 384, 256, 2, 8),    # 3 chunks per segment
+                                         (1, 2, 640, 128, 2, 4),    # 5 chunks per segment
+                                         (2, 1, 896, 256, 2, 2)])   # 7 chunks per segment
+def test_bf16_odd_chunk_counts_in_the_dq_dk_sweeps(z, B, H, T, dk, P, K):
+    """The dq/dk sweeps give alternate chunks to two epilogue groups and pass the
+    dlog_alpha suffix between them: segments with an odd number of chunks leave
+    the first group with the last chunk."""
+    shape = z.make_shape(B, H, T, dk, 512, P, K, 64, "bf16", "tc")
+    assert z.resolve_path(shape) == "tc"
+    assert z.segments(shape) == P  # too short to be split further
+    x = workloads.make_custom(B, H, T, dk, 512, dtype="bf16", seed=T + dk, qk_scale=1 / 16,
+                              s0_scale=0.2)
+    errs = parity.compare_full(z, x, P, K, 64, "bf16", path="tc")
+    _assert(errs, "bf16", f"tc odd chunks B{B} H{H} T{T} dk{dk} P{P}")
+
+
 def test_overlap_stream_gives_identical_results(z):
     # the scan-independent passes on a second stream (default) or all on one
     # stream: same kernels, same inputs, so bit-identical outputs
