@@ -72,7 +72,6 @@ tc_seg_state_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
   __shared__ float Gq[4][kM];  // per-quarter sums of log_alpha of the current stage
-  __shared__ float sF[kM];     // PRE: this stage's factor of each row
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int row = tid & (kM - 1), qd = tid >> 7;  // row within the tile, token quarter
@@ -137,7 +136,12 @@ tc_seg_state_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
     return;
   }
   float run = 0.f;  // log-decay of row i summed over the stages already done
-  float run_f = 1.f;  // PRE: product of e^{b_last} over the chunks already done
+  // PRE: this thread's 8 rows (p_r8 ..) of the tile and the products of e^{b_last}
+  // over the chunks already done for each
+  const int p_r8 = 64 * ((tid >> 3) & 1) + 8 * (tid & 7);
+  float run8[8];
+#pragma unroll
+  for (int u = 0; u < 8; ++u) run8[u] = 1.f;
   // row i of the tiles lives in MN block row/64, 16-byte chunk (row%64)/8, element row%8
   const uint32_t a_blk = (uint32_t)(row >> 6) * 8192u;
   const uint32_t a_chunk = (uint32_t)((row & 63) >> 3);
@@ -151,15 +155,19 @@ tc_seg_state_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
       abort_flag = 1;
     }
     if (PRE) {
-      // this stage's factor of row `row`, then every 16-byte group of 8 rows of the
-      // tile scaled in place (2 per thread)
-      if (tid < kM) {
-        const float e = reinterpret_cast<const float*>(xbuf + kXBytes)[tid];
-        if (REV) run_f *= e;
-        sF[tid] = run_f;
-        if (!REV) run_f *= e;
+      // every 16-byte group of 8 rows of the tile scaled in place (2 per thread, the
+      // same 8 rows in every stage): this stage's factor of each of those rows from
+      // the running products this thread carries
+      const float4* e4 = reinterpret_cast<const float4*>(xbuf + kXBytes + 4 * p_r8);
+      const float4 ea = e4[0], eb = e4[1];
+      const float ev[8] = {ea.x, ea.y, ea.z, ea.w, eb.x, eb.y, eb.z, eb.w};
+      float f[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (REV) run8[u] *= ev[u];
+        f[u] = run8[u];
+        if (!REV) run8[u] *= ev[u];
       }
-      cbar();
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int c = tid + h * kStateThreads;  // 64 tokens x 2 row blocks x 8 groups
@@ -167,7 +175,6 @@ tc_seg_state_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
         uint4* ptr = reinterpret_cast<uint4*>(xbuf + mb * 8192 + sw128((uint32_t)t, (uint32_t)c8));
         uint4 wv = *ptr;
         __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(&wv);
-        const float* f = sF + 64 * mb + 8 * c8;
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const float2 x2 = __bfloat1622float2(h2[u]);
@@ -237,6 +244,10 @@ tc_seg_state_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
   }
   cbar();
   const bool ok = !abort_flag;
+  // PRE: gamma_p of every row is the product over all the segment's chunks
+  if (PRE && REV && ok && gamma && blockIdx.x == 0 && tid < 16)
+#pragma unroll
+    for (int u = 0; u < 8; ++u) gamma[((size_t)bh * P + p) * dk + i0 + p_r8 + u] = run8[u];
   if (ok && warp < 4) {
     const int last = nblk - 1;
     if (!mbar_wait(&mma_bar[last % SG], (last / SG) & 1)) atomicExch(&g_tc_status, 1);
@@ -252,8 +263,7 @@ tc_seg_state_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
       for (int u = 0; u < 8; ++u)
         dst[u] = make_float4(r[4 * u], r[4 * u + 1], r[4 * u + 2], r[4 * u + 3]);
     }
-    if (REV && gamma && blockIdx.x == 0)
-      gamma[((size_t)bh * P + p) * dk + i] = PRE ? run_f : __expf(run);
+    if (!PRE && REV && gamma && blockIdx.x == 0) gamma[((size_t)bh * P + p) * dk + i] = __expf(run);
     (void)lane;
   }
   tc_fence_before();
