@@ -59,12 +59,9 @@ constexpr int kMmaTid = 256, kTmaTid = 288;
 // backward: the state pass after chunk n scales by the next chunk's e^{b_last},
 // so those rows come through a ring loaded two chunks ahead
 constexpr int kESlots = 3;
-#ifndef ZECO_PF_SWEEP
-#define ZECO_PF_SWEEP 2
-#endif
 // chunks ahead whose operands are prefetched into L2 (the shared memory holds
-// the current and the next chunk); <= 1: none
-constexpr int kPf = ZECO_PF_SWEEP;
+// the current and the next chunk)
+constexpr int kPf = 2;
 
 __device__ int g_fwd_status = 0;
 
