@@ -460,7 +460,9 @@ def main(argv=None):
     # its inputs from pinned host memory and downloads all its outputs; the steps
     # are pipelined the way a caller would run them: uploads and downloads have
     # their own streams, inputs and outputs are double-buffered on the device, so
-    # step i+1's upload and step i-1's download overlap step i's kernels.
+    # step i+1's upload and step i-1's download overlap step i's kernels.  Each
+    # tensor's copy is cut into kCopyStreams contiguous pieces on as many streams
+    # per direction, so that several copy engines share the transfer.
     if not args.no_e2e and w.bwd:
         names_in = ["q", "k", "v", "log_alpha", "do", "dS_final", "S0"]
         host_in = {n: x[n].cpu().pin_memory() for n in names_in}
@@ -474,11 +476,18 @@ def main(argv=None):
         del x
         bi = sum(t.numel() * t.element_size() for t in host_in.values())
         bo = sum(t.numel() * t.element_size() for t in host_out.values())
-        s_up = torch.cuda.Stream(device=dev)
-        s_down = torch.cuda.Stream(device=dev)
-        ev_up = [torch.cuda.Event() for _ in range(2)]
+        kCopyStreams = 4
+        s_up = [torch.cuda.Stream(device=dev) for _ in range(kCopyStreams)]
+        s_down = [torch.cuda.Stream(device=dev) for _ in range(kCopyStreams)]
+        ev_up = [[torch.cuda.Event() for _ in range(kCopyStreams)] for _ in range(2)]
         ev_run = [torch.cuda.Event() for _ in range(2)]
-        ev_down = [torch.cuda.Event() for _ in range(2)]
+        ev_down = [[torch.cuda.Event() for _ in range(kCopyStreams)] for _ in range(2)]
+
+        def pieces(t):  # kCopyStreams contiguous views of a contiguous tensor
+            flat = t.view(-1)
+            n = flat.numel()
+            step = -(-n // kCopyStreams)
+            return [flat[c * step:min(n, (c + 1) * step)] for c in range(kCopyStreams)]
 
         def run_into(xx, od):
             z.zeco_gla_fwd(xx["q"], xx["k"], xx["v"], xx["log_alpha"], xx["S0"], P=w.P, K=w.K,
@@ -489,25 +498,35 @@ def main(argv=None):
                            grads={n: od[n] for n in ("dq", "dk", "dv", "dlog_alpha", "dS0")},
                            workspace=ws, stream=stream)
 
+        up_pieces = [{nm: (pieces(dev_in[b][nm]), pieces(host_in[nm])) for nm in names_in}
+                     for b in range(2)]
+        down_pieces = [{nm: (pieces(host_out[nm]), pieces(dev_out[b][nm])) for nm in out_names}
+                       for b in range(2)]
+
         def e2e_steps(n_steps):
             for i in range(n_steps):
                 b = i % 2
-                with torch.cuda.stream(s_up):
+                for c, su in enumerate(s_up):
+                    with torch.cuda.stream(su):
+                        if i >= 2:
+                            su.wait_event(ev_run[b])  # step i-2 is done with these inputs
+                        for nm in names_in:
+                            dst, src = up_pieces[b][nm]
+                            dst[c].copy_(src[c], non_blocking=True)
+                        ev_up[b][c].record(su)
+                for c in range(kCopyStreams):
+                    stream.wait_event(ev_up[b][c])
                     if i >= 2:
-                        s_up.wait_event(ev_run[b])  # step i-2 is done with these inputs
-                    for nm in names_in:
-                        dev_in[b][nm].copy_(host_in[nm], non_blocking=True)
-                    ev_up[b].record(s_up)
-                stream.wait_event(ev_up[b])
-                if i >= 2:
-                    stream.wait_event(ev_down[b])  # step i-2's outputs are downloaded
+                        stream.wait_event(ev_down[b][c])  # step i-2's outputs are downloaded
                 run_into(dev_in[b], dev_out[b])
                 ev_run[b].record(stream)
-                with torch.cuda.stream(s_down):
-                    s_down.wait_event(ev_run[b])
-                    for nm in out_names:
-                        host_out[nm].copy_(dev_out[b][nm], non_blocking=True)
-                    ev_down[b].record(s_down)
+                for c, sd in enumerate(s_down):
+                    with torch.cuda.stream(sd):
+                        sd.wait_event(ev_run[b])
+                        for nm in out_names:
+                            dst, src = down_pieces[b][nm]
+                            dst[c].copy_(src[c], non_blocking=True)
+                        ev_down[b][c].record(sd)
 
         e2e_steps(2)
         torch.cuda.synchronize(dev)
@@ -522,7 +541,8 @@ def main(argv=None):
         line["e2e"] = {"value": ev, "unit": "tokens/s", "h2d_bytes_per_step": bi,
                        "d2h_bytes_per_step": bo, "steps": args.e2e_steps,
                        "note": "uploads, kernels and downloads of consecutive steps pipelined "
-                               "on three streams; every step's copies inside the timed region"}
+                               "(each tensor's copy in 4 pieces on 4 streams per direction); "
+                               "every step's copies inside the timed region"}
 
     # ---- CPU baseline (rank 0 only, N = 1 only)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
