@@ -23,9 +23,13 @@
 // the four quarters meet in distributed shared memory, and CTA r finishes the 32
 // rows [32 r, 32 r + 32) of the block.
 //
-// Q~, K~ (bf16) and e^{b_last} come from the decay pass (tc_decay.cu); the
-// masked dA = do v^T from the score pass (tc_scores.cu); the epilogue rebuilds
-// e^{+-b_t} of its own elements from log_alpha.
+// Q~, K~ (bf16) and e^{b_last} come from the decay pass (tc_decay.cu; the
+// forward keeps them for the backward); the masked dA = do v^T from the score
+// pass (tc_scores.cu); the epilogue rebuilds e^{+-b_t} of its own elements from
+// log_alpha.  The state warps read their rows' e^{b_last} straight from global
+// memory a chunk ahead, so the serial state chain never waits on an operand
+// copy.  The partial sums travel in token-quad-major slots: each st.async of a
+// warp writes 512 contiguous bytes.
 //
 // Precision of dlog_alpha.  Its suffix sum runs over the whole segment, so
 // errors in the terms add up like a random walk.  Two measures keep them
