@@ -167,7 +167,10 @@ def zeco_gla_fwd(q, k, v, log_alpha, S0=None, *, P, K, C, path="auto", o=None, S
 
     q, k: [B,H,T,dk]; v: [B,H,T,dv] (fp32 or bf16, CUDA, contiguous); log_alpha:
     [B,H,T,dk] (decay "diag"), [B,H,T] ("scalar") or None ("none").
-    S0: [B,H,dk,dv] fp32 or None (zeros).  ``saved`` must be passed to the backward.
+    S0: [B,H,dk,dv] fp32 or None (zeros).  ``saved`` must be passed to the backward
+    with the same P, K, C, path and decay: its layout follows the resolved path (on the
+    tensor-core path it also keeps the forward's decay-weighted operands and masked
+    scores, which the backward reads instead of recomputing).
     ``workspace``: a uint8 buffer of at least workspace_bytes(shape, False) bytes,
     allocated here when None.
     """
