@@ -78,7 +78,7 @@ def test_noalloc_matches_workspace_backward_twice(z, dtype):
 
 
 def test_noalloc_refuses_shapes_beyond_its_scratch(z):
-    # the 1M-token workload needs ~4.4 GB of backward scratch, far above the array
+    # the 1M-token workload needs ~5 GB of backward scratch, far above the array
     w = workloads.LONG_FWDBWD
     shape = z.make_shape(w.B, w.H, w.T, w.dk, w.dv, w.P, w.K, w.C, w.dtype)
     assert z.workspace_bytes(shape, True) > 32 << 20
