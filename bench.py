@@ -5,15 +5,18 @@ B=1, H=4, T=1,048,576, P=64 (L=16,384), C=64, K=8, d_k=256, d_v=512, bf16 I/O,
 fp32 accumulation, synthetic inputs from workloads.py.  One step is one
 zeco_gla_fwd plus one zeco_gla_bwd over the whole batch (every kernel of the
 path).  Inputs (14 GiB) are far larger than the 126 MB L2, so no L2 flush is
-needed between steps.
+needed between steps (workloads whose inputs are under ~0.5 GB get an untimed
+L2 flush before every timed step).
 
 Timing: W untimed warm-up steps, then K timed steps bracketed by a barrier and
 torch.cuda.synchronize() on both sides, CUDA events on the library's stream,
 maximum over ranks.  N > 1 (torchrun) runs N independent replicas, one per GPU
 (weak scaling; the path has no cross-GPU exchange in this build).
 
-`--impl reference` times the fp64 CPU oracle instead, on a bounded sample of
-the same workload, on this host's cores.
+Other modes: `--secondary` prints one line per secondary workload (GLA-1B layer
+forward, 8-segment forward, batched forward+backward); `--scan-sweep` times the
+segment scans at many segments; `--impl reference` times the fp64 CPU oracle
+instead, on a bounded sample of the same workload, on this host's cores.
 """
 from __future__ import annotations
 
@@ -37,15 +40,26 @@ import workloads  # noqa: E402
 
 METRIC = "GLA fwd+bwd tokens/sec on 1 GB300 and % of roofline (1M tok, P=64)"
 
-# Algorithmic HBM bytes per token per head (bf16, d_k=256, d_v=512), per kernel.
-# Inputs read once and outputs written once; segment states counted per token
-# as state_bytes / L.  The ZeCO operator total (fwd 5632 + bwd 8192 B per
-# token-head, plus segment states) is the roofline denominator of the step.
+# HBM bytes per token per head (bf16, d_k=256, d_v=512), per kernel, in two
+# accountings.  Segment states are counted per token as state_bytes / L.
+#   method: the bytes of the method's own tensors that the step a kernel carries
+#     out must move -- its inputs (q, k, v, log_alpha, do, segment states) read
+#     once and its outputs (o, dq, dk, dv, dlog_alpha, segment states) written
+#     once; intermediates this implementation keeps (Q~, K~, e^{b_last}, A, dA,
+#     q.dq) count zero.  The roofline fraction of a kernel is taken on these.
+#   impl: what the kernel actually reads and writes, intermediates included.
+# The ZeCO operator total (fwd 5632 + bwd 8192 B per token-head, plus segment
+# states) is the roofline denominator of the whole step.
 E = 2  # bytes per bf16 element
 
 
+def _state(dk, dv, L):
+    return dk * dv * 4 / L  # one fp32 dk x dv state per segment, per token
+
+
 def kernel_bytes_per_token(dk, dv, L, e=E, C=64):
-    st = dk * dv * 4 / L  # one fp32 state per segment, per token
+    """Implementation bytes per token-head of every kernel (what it moves)."""
+    st = _state(dk, dv, L)
     eb = dk * 4 / C       # e^{b_last}: one fp32 row per chunk, per token
     return {
         # pass 1: read K~, v, e^{b_last}; write one local state per segment
@@ -74,18 +88,40 @@ def kernel_bytes_per_token(dk, dv, L, e=E, C=64):
     }
 
 
-def zeco_operator_bytes_per_token(dk, dv, L, e=E):
-    """ZeCO two-pass algorithmic bytes per token-head (fwd + bwd + segment states)."""
+def method_bytes_per_token(dk, dv, L, e=E):
+    """The method's bytes per token-head for the step each kernel carries out."""
+    st = _state(dk, dv, L)
+    return {
+        "chunk_state": e * (2 * dk + dv) + st,        # k, g, v -> S_loc
+        "seg_scan_fwd": 2 * st,                       # S_loc, S_in
+        "decay": e * 3 * dk,                          # q, k, g (outputs are intermediates)
+        "A": 0.0,                                     # intermediates only
+        "fwd_out": e * (3 * dk + 2 * dv) + st,        # q, k, g, v, S_in -> o
+        "dstate_local": e * (2 * dk + dv) + st,       # q, g, do -> dS_loc
+        "seg_scan_rev": 3 * st,
+        "bwd_dv": e * (3 * dk + 2 * dv) + st,         # q, k, g, do, D -> dv
+        "bwd_dqk": e * (3 * dk + 2 * dv) + e * 3 * dk + 2 * st,
+        "dA": e * 2 * dv,                             # v, do (output is an intermediate)
+        "bwd_dq": e * (3 * dk + 2 * dv) + e * dk + st,       # q, k, g, v, do, S_in -> dq
+        "bwd_dk": e * (3 * dk + 2 * dv) + 2 * e * dk + st,   # q, k, g, v, do, D -> dk, dg
+    }
+
+
+def zeco_operator_bytes_per_token(dk, dv, L, e=E, bwd=True):
+    """ZeCO two-pass algorithmic bytes per token-head (fwd [+ bwd] + segment states)."""
     fwd = e * (5 * dk + 3 * dv)
-    bwd = e * (8 * dk + 4 * dv)
+    if not bwd:
+        return fwd + 16 * dk * dv / L
+    bwd_b = e * (8 * dk + 4 * dv)
     states = (16 + 20) * dk * dv / L
-    return fwd + bwd + states
+    return fwd + bwd_b + states
 
 
-def zeco_operator_flops_per_token(dk, dv, C):
+def zeco_operator_flops_per_token(dk, dv, C, bwd=True):
     fwd = 2 * C * (dk + dv) + 6 * dk * dv
-    bwd = 2 * C * (3 * dk + 2 * dv) + 12 * dk * dv
-    return fwd + bwd
+    if not bwd:
+        return fwd
+    return fwd + 2 * C * (3 * dk + 2 * dv) + 12 * dk * dv
 
 
 def canonical_kernel(name):
@@ -236,45 +272,50 @@ def aggregate(elapsed_s_max: float, tokens_per_rank_step: int, steps: int, world
 
 
 def cpu_oracle_sample(w, sample_tokens, nthreads=None):
-    """Time the fp64 oracle (fwd + full bwd) on the first `sample_tokens` tokens of
-    every head of batch 0.  Returns tokens/s in the workload's unit and details."""
+    """Time the fp64 oracle (fwd, + full bwd when the workload has a backward) on
+    the first `sample_tokens` tokens of every head of batch 0.  Returns tokens/s in
+    the workload's unit and details."""
     import oracle
     x = workloads.make_inputs(w.replace(T=sample_tokens, P=1, B=1), device="cpu")
     nt = nthreads or oracle.default_threads()
     t0 = time.perf_counter()
     oracle.gla_fwd(x["q"], x["k"], x["v"], x["log_alpha"], x["S0"], nthreads=nt)
-    oracle.gla_bwd(x["q"], x["k"], x["v"], x["log_alpha"], x["S0"], x["do"], x["dS_final"],
-                   nthreads=nt)
+    if w.bwd:
+        oracle.gla_bwd(x["q"], x["k"], x["v"], x["log_alpha"], x["S0"], x["do"],
+                       x["dS_final"], nthreads=nt)
     dt = time.perf_counter() - t0
     # all H heads of the sample were processed: the sample covers sample_tokens tokens
     return sample_tokens / dt, dt, nt
 
 
-# ---------------------------------------------------------------- main
-
-
 def run_reference(args, world, rank):
+    """The reference arm: the fp64 CPU oracle as it stands, on this host's cores.
+    Each step is a bounded sample of the workload (the first ``--ref-sample-tokens``
+    tokens of batch 0, all heads, forward + backward), so ``value`` is the oracle's
+    rate on that sample and ``ms_per_step`` the measured time of one sample step."""
     if rank != 0:
         return 0
+    import oracle
     w = workloads.BY_NAME[args.workload]
     sample = args.ref_sample_tokens
-    vals = []
-    nt = None
-    for _ in range(args.warmup):
-        pass  # the oracle has no warm-up state worth timing
-    t_all = 0.0
+    for _ in range(args.warmup):  # loads the oracle library and warms its threads
+        xs = workloads.make_inputs(w.replace(T=64, P=1, B=1), device="cpu")
+        oracle.gla_fwd(xs["q"], xs["k"], xs["v"], xs["log_alpha"], xs["S0"])
+    vals, times, nt = [], [], None
     for _ in range(args.steps):
         v, dt, nt = cpu_oracle_sample(w, sample)
         vals.append(v)
-        t_all += dt
+        times.append(dt)
     value = sum(vals) / len(vals)
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": 1e3 * w.tokens / value, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "ms_per_step": 1e3 * sum(times) / len(times), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "dk": w.dk, "dv": w.dv,
-                   "P": w.P, "K": w.K, "C": w.C},
+                   "P": w.P, "K": w.K, "C": w.C, "step_tokens": sample,
+                   "step": f"a sample of the workload: batch 0, all {w.H} heads, the first "
+                           f"{sample} tokens (the rate is tokens/s on that sample)"},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": nt, "kind": "oracle",
                          "sample": f"batch 0, all {w.H} heads, first {sample} tokens, fp64 "
                                    f"recurrence fwd + brute-force adjoint bwd, per step"},
@@ -285,31 +326,89 @@ def run_reference(args, world, rank):
     return 0
 
 
-def main(argv=None):
-    ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
-    ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--workload", default=workloads.LONG_FWDBWD.name)
-    ap.add_argument("--path", default="auto", choices=["auto", "simt", "tc"])
-    ap.add_argument("--e2e-steps", type=int, default=6)
-    ap.add_argument("--cpu-sample-tokens", type=int, default=16384)
-    ap.add_argument("--ref-sample-tokens", type=int, default=4096)
-    ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-e2e", action="store_true")
-    args = ap.parse_args(argv)
-    if args.warmup < 3 and args.impl != "reference":
-        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+# ------------------------------------------------------------ GPU measurement
 
-    world, rank, local = dist_setup()
-    if args.impl == "reference":
-        rc = run_reference(args, world, rank)
-        return rc
 
+def profile_step(lib, step, dev, n_ev=64):
+    """One step with the library's per-kernel start/end events.  Returns a list
+    of (kernel, start_ms, end_ms) on one timeline (relative to the first start)."""
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
+    for e in evs:
+        e.record()  # materialise the handles
+    torch.cuda.synchronize(dev)
+    handles = (ctypes.c_void_p * n_ev)(*[e.cuda_event for e in evs])
+    lib.zeco_set_profile_events.argtypes = [ctypes.c_void_p, ctypes.c_int]
+    lib.zeco_profile_kernel_name.restype = ctypes.c_char_p
+    lib.zeco_set_profile_events(ctypes.cast(handles, ctypes.c_void_p), n_ev)
+    try:
+        step()
+        n = lib.zeco_profile_event_count() // 2
+        names = [lib.zeco_profile_kernel_name(i).decode() for i in range(n)]
+    finally:
+        lib.zeco_set_profile_events(None, 0)
+    torch.cuda.synchronize(dev)
+    base = evs[0]
+    return [(names[i], base.elapsed_time(evs[2 * i]), base.elapsed_time(evs[2 * i + 1]))
+            for i in range(n)]
+
+
+def scan_overlap(intervals):
+    """The pages' overlap instrument (Pith review, 'What would settle it'; Eq. 11):
+    the share of the segment scan's time during which no diagonal-attention kernel
+    (the intra-chunk scores A, forward; their gradient dA, backward) runs."""
+    def span(name):
+        return [(a, b) for n, a, b in intervals if canonical_kernel(n) == name]
+    out = {}
+    for direction, scan, diag in (("fwd", "seg_scan_fwd", "A"), ("bwd", "seg_scan_rev", "dA")):
+        sc, dg = span(scan), span(diag)
+        if not sc or not dg:
+            continue
+        s_len = sum(b - a for a, b in sc)
+        ov = sum(max(0.0, min(b, d1) - max(a, d0)) for a, b in sc for d0, d1 in dg)
+        out[direction] = {"scan_ms": s_len, "overlapped_ms": ov,
+                          "non_overlapped_frac": 1.0 - ov / s_len if s_len > 0 else None}
+    return out
+
+
+def copy_bound(dev, nbytes=1 << 31):
+    """Pinned host <-> device copy rates on this machine (GB/s): each direction alone
+    and both at once (best of 3), the bound of any step that moves its inputs in
+    and its outputs out."""
+    h_in = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    h_out = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    d_in = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    d_out = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    s_up, s_dn = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+
+    def timed(up, down):
+        best = None
+        for _ in range(3):
+            torch.cuda.synchronize(dev)
+            t0 = time.perf_counter()
+            if up:
+                with torch.cuda.stream(s_up):
+                    d_in.copy_(h_in, non_blocking=True)
+            if down:
+                with torch.cuda.stream(s_dn):
+                    h_out.copy_(d_out, non_blocking=True)
+            torch.cuda.synchronize(dev)
+            dt = time.perf_counter() - t0
+            best = dt if best is None else min(best, dt)
+        return nbytes / best / 1e9
+
+    res = {"h2d_gbs": timed(True, False), "d2h_gbs": timed(False, True)}
+    both = timed(True, True)  # each direction moved nbytes in that time
+    res["both_each_gbs"] = both
+    res["bytes"] = nbytes
+    del h_in, h_out, d_in, d_out
+    return res
+
+
+def measure(w, args, world, rank, local, want_e2e=True, want_cpu=True, quiet=False):
+    """Time ``args.steps`` steps of workload ``w`` (forward, plus the backward when the
+    workload has one) and return the JSON line as a dict."""
     import chunked_state_scan_gb300 as z
-    z.load_library()
-    w = workloads.BY_NAME[args.workload]
+    lib = z.load_library()
     dev = torch.device("cuda", local)
     stream = torch.cuda.Stream(device=dev)
     x = workloads.make_inputs(w, device=dev)
@@ -324,8 +423,13 @@ def main(argv=None):
     grads = dict(dq=torch.empty_like(x["q"]), dk=torch.empty_like(x["k"]),
                  dv=torch.empty_like(x["v"]), dlog_alpha=torch.empty_like(x["log_alpha"]),
                  dS0=torch.empty_like(x["S0"]))
+    in_bytes = sum(t.numel() * t.element_size() for t in x.values())
+    # inputs smaller than a few L2s (126 MB) could be served from L2 on the next
+    # step: then L2 is flushed (a 512 MB write, untimed) before every timed step
+    flush = in_bytes < 4 * 126e6
+    flush_buf = torch.empty(512 << 20, dtype=torch.uint8, device=dev) if flush else None
 
-    def step(xx):
+    def step(xx=x):
         z.zeco_gla_fwd(xx["q"], xx["k"], xx["v"], xx["log_alpha"], xx["S0"], P=w.P, K=w.K,
                        C=w.C, path=args.path, o=o, S_final=S_final, saved=saved,
                        workspace=ws_f, stream=stream)
@@ -334,39 +438,48 @@ def main(argv=None):
                            xx["dS_final"], P=w.P, K=w.K, C=w.C, path=args.path, grads=grads,
                            workspace=ws, stream=stream)
 
+    def timed_steps(n):
+        """Device time of n steps (ms), L2 flushed before each when the inputs are small."""
+        if not flush:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(n):
+                step()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            return e0.elapsed_time(e1)
+        total = 0.0
+        for _ in range(n):
+            with torch.cuda.stream(stream):
+                flush_buf.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            step()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            total += e0.elapsed_time(e1)
+        return total
+
     torch.cuda.synchronize(dev)
     for _ in range(args.warmup):
-        step(x)
+        step()
     torch.cuda.synchronize(dev)
 
-    # ---- per-kernel durations (library-recorded events on the same stream)
-    lib = z.load_library()
-    n_ev = 16
-    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
-    with torch.cuda.stream(stream):
-        for e in evs:
-            e.record(stream)  # materialise the handles
-    torch.cuda.synchronize(dev)
-    handles = (ctypes.c_void_p * n_ev)(*[e.cuda_event for e in evs])
+    # ---- per-kernel durations: start/end events of every kernel, with every
+    #      kernel on one stream (zeco_set_overlap(0)), so that no kernel's time is
+    #      stretched by another running beside it
+    lib.zeco_set_overlap.argtypes = [ctypes.c_int]
+    lib.zeco_set_overlap(0)
+    try:
+        prof = [profile_step(lib, step, dev) for _ in range(2)]
+    finally:
+        lib.zeco_set_overlap(1)
     per_kernel = {}
-    prof_steps = 2
-    for _ in range(prof_steps):
-        lib.zeco_set_profile_events.argtypes = [ctypes.c_void_p, ctypes.c_int]
-        lib.zeco_set_profile_events(ctypes.cast(handles, ctypes.c_void_p), n_ev)
-        step(x)
-        n = lib.zeco_profile_event_count()
-        names = []
-        lib.zeco_profile_kernel_name.restype = ctypes.c_char_p
-        for i in range(n):
-            names.append(lib.zeco_profile_kernel_name(i).decode())
-        lib.zeco_set_profile_events(None, 0)
-        torch.cuda.synchronize(dev)
-        for i in range(1, n):
-            per_kernel.setdefault(names[i], []).append(evs[i - 1].elapsed_time(evs[i]))
-    # event 0 is recorded before the forward's first kernel; the backward's first
-    # kernel is timed from the forward's last kernel (same stream, back to back)
+    for run in prof:
+        for n, a, b in run:
+            per_kernel.setdefault(n, []).append(b - a)
     kern_ms = {k: sum(v) / len(v) for k, v in per_kernel.items()}
-    launches_per_step = len(kern_ms)
+    launches_per_step = len(prof[0])
 
     # ---- timed region
     clocks = ClockSampler(torch.cuda.current_device() if world == 1 else local)
@@ -374,84 +487,95 @@ def main(argv=None):
     time.sleep(0.3)
     barrier(world)
     torch.cuda.synchronize(dev)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        step(x)
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
+    elapsed = timed_steps(args.steps) / 1e3
     barrier(world)
     clk = clocks.stop()
-    dev_status = lib.zeco_check_device_status()  # 0: no bounded device wait gave up
-    elapsed = e0.elapsed_time(e1) / 1e3
+    dev_status = lib.zeco_last_device_status(ctypes.c_void_p(stream.cuda_stream))
     elapsed_max = max_over_ranks(elapsed, world)
     value, ms_step = aggregate(elapsed_max, w.tokens, args.steps, world)
 
-    # ---- the overlap instrument: the same steps with every kernel on one stream.
-    # The passes that do not depend on the segment scan (decay, scores, score
-    # gradient) run on a second stream by default; hidden = the share of their
-    # time that the overlap removed from the step.
+    # ---- the other schedules of the work beside the scan (zeco_set_overlap):
+    #      0 = one stream, 2 = the scan on a second stream beside the diagonal
+    #      attention (the pages' schedule); the instrument for each
     overlap = None
     if path == "tc":
-        lib.zeco_set_overlap.argtypes = [ctypes.c_int]
-        lib.zeco_set_overlap(0)
-        step(x)
-        torch.cuda.synchronize(dev)
-        s0 = torch.cuda.Event(enable_timing=True)
-        s1 = torch.cuda.Event(enable_timing=True)
-        s0.record(stream)
-        for _ in range(args.steps):
-            step(x)
-        s1.record(stream)
-        torch.cuda.synchronize(dev)
-        lib.zeco_set_overlap(1)
-        serial_ms = s0.elapsed_time(s1) / args.steps
-        aux_ms = sum(v for k, v in kern_ms.items() if canonical_kernel(k) in ("A", "dA"))
-        overlap = {"serial_ms": serial_ms, "overlapped_ms": ms_step, "aux_stream_ms": aux_ms,
-                   "hidden_frac": (serial_ms - ms_step) / aux_ms if aux_ms > 0 else None,
-                   "note": "masked scores (forward) and score gradient (backward) on a second "
-                           "stream, concurrent with the segment-state passes and the scans"}
+        modes = {}
+        try:
+            for mode in (0, 2, 1):
+                lib.zeco_set_overlap(mode)
+                step()
+                torch.cuda.synchronize(dev)
+                modes[mode] = (timed_steps(args.steps) / args.steps, profile_step(lib, step, dev))
+        finally:
+            lib.zeco_set_overlap(1)
+        overlap = {
+            "step_ms": {"mode1_aux_scores": ms_step, "mode2_aux_scan": modes[2][0],
+                        "mode0_one_stream": modes[0][0]},
+            "scan_not_overlapped": {"mode1_aux_scores": scan_overlap(modes[1][1]),
+                                    "mode2_aux_scan": scan_overlap(modes[2][1])},
+            "note": "mode 1 (default): scores A / dA on a second stream beside pass 1, the "
+                    "scans (and the dv sweep); mode 2: the segment scans on a second stream "
+                    "beside the A / dA pass; non_overlapped_frac = share of the scan's "
+                    "kernel time with no A / dA kernel running (Eq. 11 instrument)"}
 
     # ---- roofline of the dominant kernel and of the whole step
     peaks, peak_kind = load_peaks()
     hbm_peak = float(peaks["hbm_gbs"])
     bh = w.B * w.H
     kb = kernel_bytes_per_token(w.dk, w.dv, w.L)
+    mb = method_bytes_per_token(w.dk, w.dv, w.L)
     dom = max(kern_ms, key=kern_ms.get)
     dom_key = canonical_kernel(dom)
-    dom_bytes = kb.get(dom_key, 0.0) * w.T * bh
+    dom_bytes = mb.get(dom_key, 0.0) * w.T * bh
+    dom_impl_bytes = kb.get(dom_key, 0.0) * w.T * bh
     dom_gbs = dom_bytes / (kern_ms[dom] * 1e-3) / 1e9
-    op_bytes = zeco_operator_bytes_per_token(w.dk, w.dv, w.L) * w.T * bh
-    op_flops = zeco_operator_flops_per_token(w.dk, w.dv, w.C) * w.T * bh
+    op_bytes = zeco_operator_bytes_per_token(w.dk, w.dv, w.L, bwd=w.bwd) * w.T * bh
+    op_flops = zeco_operator_flops_per_token(w.dk, w.dv, w.C, bwd=w.bwd) * w.T * bh
     t_roof = max(op_bytes / (hbm_peak * 1e9), op_flops / (float(peaks["bf16_tflops"]) * 1e12))
     step_s = ms_step * 1e-3
     traffic = measured_traffic(path, dom, w.T * bh)
-    # every kernel's algorithmic bytes over its event-timed duration (GB/s)
-    kern_gbs = {k: kb[canonical_kernel(k)] * w.T * bh / (ms * 1e-3) / 1e9
+    # every kernel's bytes over its event-timed duration (GB/s), both accountings
+    kern_gbs = {k: {"method": mb[canonical_kernel(k)] * w.T * bh / (ms * 1e-3) / 1e9,
+                    "impl": kb[canonical_kernel(k)] * w.T * bh / (ms * 1e-3) / 1e9}
                 for k, ms in kern_ms.items() if canonical_kernel(k) in kb and ms > 0}
+    impl_total = sum(kb[canonical_kernel(k)] for k in kern_ms if canonical_kernel(k) in kb)
+    method_total = zeco_operator_bytes_per_token(w.dk, w.dv, w.L, bwd=w.bwd)
     scan_ms = sum(v for k, v in kern_ms.items() if "seg_scan" in k)
 
     line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "metric": METRIC if w.name == workloads.LONG_FWDBWD.name else
+        f"GLA {'fwd+bwd' if w.bwd else 'fwd'} tokens/sec on 1 GB300 and % of roofline "
+        f"({w.name})",
+        "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
         "data": "synthetic (seeded; shapes and distributions of the GLA-1B layer workload)",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "dk": w.dk, "dv": w.dv,
-                   "P": w.P, "K": w.K, "C": w.C, "path": path,
-                   "l2": "no flush: inputs 14 GiB >> 126 MB L2",
+                   "P": w.P, "K": w.K, "C": w.C, "path": path, "step": "fwd+bwd" if w.bwd
+                   else "fwd", "segments_evaluated": z.segments(shape),
+                   "l2": ("flushed before every timed step (512 MB write, untimed): inputs "
+                          f"{in_bytes / 1e6:.0f} MB") if flush else
+                   f"no flush: inputs {in_bytes / 2**30:.1f} GiB >> 126 MB L2",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": dom_gbs, "peak": hbm_peak,
                      "unit": "GB/s", "frac": dom_gbs / hbm_peak, "traffic": traffic,
                      "traffic_unit": "DRAM bytes per launch (ncu capture, scaled by tokens)",
                      "peak_source": f"{peak_kind} hbm_gbs",
-                     "algorithmic_bytes_per_launch": dom_bytes},
+                     "algorithmic_bytes_per_launch": dom_bytes,
+                     "algorithmic_bytes": "the method's inputs and outputs of this step "
+                                          "(no intermediates)",
+                     "impl_bytes_per_launch": dom_impl_bytes,
+                     "impl_frac": dom_impl_bytes / (kern_ms[dom] * 1e-3) / 1e9 / hbm_peak},
         "operator_roofline": {"bytes": op_bytes, "flops": op_flops, "t_roof_ms": t_roof * 1e3,
                               "frac": t_roof / step_s,
+                              "impl_bytes_per_token_head": impl_total,
+                              "method_bytes_per_token_head": method_total,
+                              "impl_over_method": impl_total / method_total,
                               "note": "ZeCO two-pass algorithmic bytes/flops per step vs "
                                       f"{peak_kind} peaks"},
         "device_status": "ok" if dev_status == 0 else f"error {dev_status}",
-        "kernels_ms": kern_ms, "kernels_gbs": kern_gbs, "overlap": overlap, "scan_share": scan_ms / sum(kern_ms.values()),
+        "kernels_ms": kern_ms, "kernels_gbs": kern_gbs, "overlap": overlap,
+        "scan_share": scan_ms / sum(kern_ms.values()),
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
     }
@@ -463,7 +587,7 @@ def main(argv=None):
     # step i+1's upload and step i-1's download overlap step i's kernels.  Each
     # tensor's copy is cut into kCopyStreams contiguous pieces on as many streams
     # per direction, so that several copy engines share the transfer.
-    if not args.no_e2e and w.bwd:
+    if want_e2e and w.bwd:
         names_in = ["q", "k", "v", "log_alpha", "do", "dS_final", "S0"]
         host_in = {n: x[n].cpu().pin_memory() for n in names_in}
         out_names = ("o", "S_final", "dq", "dk", "dv", "dlog_alpha", "dS0")
@@ -486,8 +610,8 @@ def main(argv=None):
         def pieces(t):  # kCopyStreams contiguous views of a contiguous tensor
             flat = t.view(-1)
             n = flat.numel()
-            step = -(-n // kCopyStreams)
-            return [flat[c * step:min(n, (c + 1) * step)] for c in range(kCopyStreams)]
+            stp = -(-n // kCopyStreams)
+            return [flat[c * stp:min(n, (c + 1) * stp)] for c in range(kCopyStreams)]
 
         def run_into(xx, od):
             z.zeco_gla_fwd(xx["q"], xx["k"], xx["v"], xx["log_alpha"], xx["S0"], P=w.P, K=w.K,
@@ -538,21 +662,122 @@ def main(argv=None):
         barrier(world)
         el = max_over_ranks(t1 - t0, world)
         ev, _ = aggregate(el, w.tokens, args.e2e_steps, world)
+        # the copy bound: a step cannot beat moving its bytes at the box's pinned
+        # copy rates (both directions at once), nor its own device time
+        del dev_in, dev_out, out1, up_pieces, down_pieces
+        torch.cuda.empty_cache()
+        cb = copy_bound(dev)
+        t_copy = max(bi / (cb["both_each_gbs"] * 1e9), bo / (cb["both_each_gbs"] * 1e9))
+        bound = w.tokens * world / max(t_copy, step_s)
         line["e2e"] = {"value": ev, "unit": "tokens/s", "h2d_bytes_per_step": bi,
                        "d2h_bytes_per_step": bo, "steps": args.e2e_steps,
+                       "copy_bound": {**cb, "t_copy_ms": t_copy * 1e3, "bound_tokens_s": bound,
+                                      "frac": ev / bound},
                        "note": "uploads, kernels and downloads of consecutive steps pipelined "
                                "(each tensor's copy in 4 pieces on 4 streams per direction); "
-                               "every step's copies inside the timed region"}
+                               "every step's copies inside the timed region; copy_bound: plain "
+                               "pinned copies of 2 GiB on this box"}
 
     # ---- CPU baseline (rank 0 only, N = 1 only)
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, dt, nt = cpu_oracle_sample(w, args.cpu_sample_tokens)
+    if want_cpu and rank == 0 and world == 1:
+        sample = min(args.cpu_sample_tokens, w.T)
+        v, dt, nt = cpu_oracle_sample(w, sample)
         line["cpu_baseline"] = {
             "value": v, "unit": "tokens/s", "cores": nt, "kind": "oracle",
-            "sample": f"batch 0, all {w.H} heads, first {args.cpu_sample_tokens} tokens: fp64 "
-                      f"token recurrence fwd + brute-force adjoint bwd ({dt:.1f} s)"}
-    if rank == 0:
-        print(json.dumps(line), flush=True)
+            "sample": f"batch 0, all {w.H} heads, first {sample} tokens: fp64 "
+                      f"token recurrence fwd" + (" + brute-force adjoint bwd" if w.bwd else "")
+                      + f" ({dt:.1f} s)"}
+    return line
+
+
+def scan_sweep(args, local):
+    """The segment scans at many segments (``--scan-sweep``): the 1M-token workload's
+    inputs with P in {64, 1024, 4096, T/(2C)}; each scan's time and bytes/s."""
+    import chunked_state_scan_gb300 as z
+    lib = z.load_library()
+    dev = torch.device("cuda", local)
+    peaks, peak_kind = load_peaks()
+    base = workloads.LONG_FWDBWD
+    x = workloads.make_inputs(base, device=dev)
+    out = []
+    # (B*H*P is capped at 65535 by the grid; P = T/C = 16384 with 4 heads is one over)
+    for P in (64, 1024, 4096, base.T // (2 * base.C)):
+        w = base.replace(P=P, name=f"scan_sweep_P{P}")
+        stream = torch.cuda.Stream(device=dev)
+        shape = z.make_shape(w.B, w.H, w.T, w.dk, w.dv, w.P, w.K, w.C, w.dtype)
+        saved = torch.empty(z.saved_bytes(shape), dtype=torch.uint8, device=dev)
+        ws = torch.empty(z.workspace_bytes(shape, True), dtype=torch.uint8, device=dev)
+
+        def step():
+            _, _, _ = z.zeco_gla_fwd(x["q"], x["k"], x["v"], x["log_alpha"], x["S0"], P=P,
+                                     K=w.K, C=w.C, saved=saved, stream=stream)
+            z.zeco_gla_bwd(x["q"], x["k"], x["v"], x["log_alpha"], saved, x["do"],
+                           x["dS_final"], P=P, K=w.K, C=w.C, workspace=ws, stream=stream)
+
+        step()
+        torch.cuda.synchronize(dev)
+        runs = [profile_step(lib, step, dev) for _ in range(3)]
+        kb = kernel_bytes_per_token(w.dk, w.dv, w.L)
+        res = {"P": P, "L": w.L}
+        for name in ("seg_scan_fwd", "seg_scan_rev"):
+            ms = [b - a for r in runs for n, a, b in r if n == name]
+            t = sum(ms) / len(ms)
+            gbs = kb[name] * w.T * w.B * w.H / (t * 1e-3) / 1e9
+            res[name] = {"ms": t, "gbs": gbs, "frac_of_hbm": gbs / float(peaks["hbm_gbs"])}
+        out.append(res)
+        del saved, ws
+        torch.cuda.empty_cache()
+    return {"scan_sweep": out, "peak_source": f"{peak_kind} hbm_gbs",
+            "workload": base.name + " inputs, P varied"}
+
+
+# ---------------------------------------------------------------- main
+
+
+SECONDARY = [workloads.GLA1B_FWD.name, workloads.SEG_FWD.name, workloads.BATCHED_FWDBWD.name]
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default=workloads.LONG_FWDBWD.name)
+    ap.add_argument("--path", default="auto", choices=["auto", "simt", "tc"])
+    ap.add_argument("--e2e-steps", type=int, default=6)
+    ap.add_argument("--cpu-sample-tokens", type=int, default=16384)
+    ap.add_argument("--ref-sample-tokens", type=int, default=4096)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--secondary", action="store_true",
+                    help="one JSON line per secondary workload (GLA-1B layer fwd, "
+                         "8-segment fwd, batched fwd+bwd) instead of the headline")
+    ap.add_argument("--scan-sweep", action="store_true",
+                    help="time the segment scans at P in {64, 1024, 4096, T/(2C)}")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl != "reference":
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+
+    import chunked_state_scan_gb300 as z
+    z.load_library()
+    if args.scan_sweep:
+        res = scan_sweep(args, local)
+        if rank == 0:
+            print(json.dumps(res), flush=True)
+        return 0
+    names = SECONDARY if args.secondary else [args.workload]
+    for name in names:
+        w = workloads.BY_NAME[name]
+        line = measure(w, args, world, rank, local, want_e2e=not args.no_e2e and not args.secondary,
+                       want_cpu=not args.no_cpu_baseline)
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+        torch.cuda.empty_cache()
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()

@@ -19,12 +19,16 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libzeco_gla.so")
 
 ZECO_OK, ZECO_ERR_ARG, ZECO_ERR_UNSUPPORTED, ZECO_ERR_WORKSPACE, ZECO_ERR_CUDA = 0, -1, -2, -3, -4
+ZECO_ERR_TIMEOUT = -5
 ZECO_F32, ZECO_BF16 = 0, 1
 PATH_AUTO, PATH_SIMT, PATH_TC = 0, 1, 2
 _PATHS = {"auto": PATH_AUTO, "simt": PATH_SIMT, "tc": PATH_TC}
 
 EXPORTED = ["zeco_gla_saved_bytes", "zeco_gla_workspace_bytes", "zeco_gla_fwd", "zeco_gla_bwd",
-            "zeco_strerror", "zeco_gla_resolve_path"]
+            "zeco_strerror", "zeco_gla_resolve_path", "zeco_gla_segments",
+            "zeco_check_device_status", "zeco_last_device_status", "zeco_selftest_bounded_wait",
+            "zeco_set_profile_events", "zeco_profile_event_count", "zeco_profile_kernel_name",
+            "zeco_set_overlap", "zeco_gla_bwd_noalloc"]
 
 
 class ZecoShape(ctypes.Structure):
@@ -73,6 +77,12 @@ def load_library(path: str = LIB_PATH):
             lib.zeco_gla_resolve_path.restype = ctypes.c_int
             lib.zeco_selftest_bounded_wait.argtypes = [vp]
             lib.zeco_selftest_bounded_wait.restype = ctypes.c_int
+            lib.zeco_check_device_status.argtypes = []
+            lib.zeco_check_device_status.restype = ctypes.c_int
+            lib.zeco_last_device_status.argtypes = [vp]
+            lib.zeco_last_device_status.restype = ctypes.c_int
+            lib.zeco_gla_bwd_noalloc.argtypes = [sp] + [vp] * 13
+            lib.zeco_gla_bwd_noalloc.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -124,21 +134,31 @@ def segments(shape: ZecoShape) -> int:
 
 def check_device_status() -> None:
     """Raise ZecoError if a bounded device wait gave up since the last check
-    (synchronise the streams of the calls to cover first)."""
+    (synchronise the streams of the calls to cover first).  The flags are per
+    device: a give-up on any stream of the current device is reported."""
     _check(load_library().zeco_check_device_status())
 
 
+def last_device_status(stream=None) -> int:
+    """zeco_last_device_status: synchronise ``stream`` (default: the current
+    stream), then read and clear the device's bounded-wait flags.  Returns the
+    code (ZECO_OK or ZECO_ERR_TIMEOUT, ZECO_ERR_CUDA) without raising."""
+    return int(load_library().zeco_last_device_status(_stream_ptr(stream)))
+
+
 def selftest_bounded_wait(stream=None) -> None:
-    """Launch the library's diagnostic kernel whose single wait can never
-    complete (it gives up after 2 s and records ZECO_ERR_TIMEOUT for
-    check_device_status)."""
+    """Launch the library's diagnostic kernel, four warps whose waits can never
+    complete (the first gives up after 2 s, the others then at once; it records
+    ZECO_ERR_TIMEOUT for check_device_status)."""
     st = stream if stream is not None else torch.cuda.current_stream()
     _check(load_library().zeco_selftest_bounded_wait(ctypes.c_void_p(st.cuda_stream)))
 
 
-def set_overlap(on: bool) -> None:
-    """Run the scan-independent passes on a second stream (default) or not."""
-    load_library().zeco_set_overlap(int(bool(on)))
+def set_overlap(mode: int) -> None:
+    """Schedule of the work beside the segment scan: 1 (default) the
+    scan-independent score passes on a second stream, 2 the segment scan on a
+    second stream beside them (the pages' schedule), 0 everything on one stream."""
+    _check(load_library().zeco_set_overlap(int(mode)))
 
 
 def resolve_path(shape: ZecoShape) -> str:

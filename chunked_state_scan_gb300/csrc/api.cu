@@ -8,13 +8,15 @@ namespace {
 
 using zeco::Dims;
 
-// Per-thread profiling state (zeco_set_profile_events).
-constexpr int kMaxProf = 256;
+// Per-thread profiling state (zeco_set_profile_events): events[2i] and
+// events[2i + 1] bracket kernel i on its own stream.
+constexpr int kMaxProf = 256;  // events (two per kernel)
 struct ProfState {
   void* const* events = nullptr;
   int cap = 0;
-  int count = 0;
-  const char* names[kMaxProf] = {};
+  int count = 0;      // events recorded
+  bool open = false;  // a start event waits for its kernel's end event
+  const char* names[kMaxProf / 2] = {};
 };
 thread_local ProfState g_prof;
 
@@ -118,22 +120,19 @@ zeco::TcOps tc_ops(const zeco::SavedLayout& sl, const void* saved, void* ws, siz
 
 namespace zeco {
 
-bool prof_active() { return g_prof.events != nullptr; }
-
-void prof_begin(cudaStream_t st) {
-  if (!g_prof.events || g_prof.count >= g_prof.cap) return;
-  if (g_prof.count == 0) {
-    cudaEventRecord((cudaEvent_t)g_prof.events[0], st);
-    g_prof.names[0] = "begin";
-    g_prof.count = 1;
-  }
+void prof_start(cudaStream_t st) {
+  g_prof.open = false;
+  if (!g_prof.events || g_prof.count + 2 > g_prof.cap) return;
+  if (cudaEventRecord((cudaEvent_t)g_prof.events[g_prof.count], st) == cudaSuccess)
+    g_prof.open = true;
 }
 
 void prof_mark(const char* kernel, cudaStream_t st) {
-  if (!g_prof.events || g_prof.count >= g_prof.cap || g_prof.count >= kMaxProf) return;
-  cudaEventRecord((cudaEvent_t)g_prof.events[g_prof.count], st);
-  g_prof.names[g_prof.count] = kernel;
-  ++g_prof.count;
+  if (!g_prof.events || !g_prof.open) return;
+  g_prof.open = false;
+  if (cudaEventRecord((cudaEvent_t)g_prof.events[g_prof.count + 1], st) != cudaSuccess) return;
+  g_prof.names[g_prof.count / 2] = kernel;
+  g_prof.count += 2;
 }
 
 }  // namespace zeco
@@ -144,13 +143,14 @@ int zeco_set_profile_events(void* const* events, int n) {
   g_prof.events = (n > 0) ? events : nullptr;
   g_prof.cap = (n > 0 && events) ? (n < kMaxProf ? n : kMaxProf) : 0;
   g_prof.count = 0;
+  g_prof.open = false;
   return ZECO_OK;
 }
 
 int zeco_profile_event_count(void) { return g_prof.count; }
 
 const char* zeco_profile_kernel_name(int i) {
-  return (i >= 0 && i < g_prof.count) ? g_prof.names[i] : nullptr;
+  return (i >= 0 && i < g_prof.count / 2) ? g_prof.names[i] : nullptr;
 }
 
 size_t zeco_gla_saved_bytes(const zeco_shape* shape) {
@@ -202,7 +202,6 @@ int zeco_gla_fwd(const zeco_shape* shape, const void* q, const void* k, const vo
   float* S_in = (float*)((char*)saved + sl.S_in_off);
   float* gamma = (float*)((char*)saved + sl.gamma_off);
   cudaStream_t st = (cudaStream_t)stream;
-  zeco::prof_begin(st);
   cudaError_t e = cudaSuccess;
   const void* g = log_alpha;
   if (d.decay != ZECO_DECAY_DIAG) {
@@ -243,7 +242,6 @@ int zeco_gla_bwd(const zeco_shape* shape, const void* q, const void* k, const vo
   float* carry = (float*)((char*)workspace + wl.carry_off);
   float* qdq = (float*)((char*)workspace + wl.qdq_off);
   cudaStream_t st = (cudaStream_t)stream;
-  zeco::prof_begin(st);
   cudaError_t e = cudaSuccess;
   const void* g = log_alpha;
   void* dg = dlog_alpha;
@@ -273,6 +271,11 @@ int zeco_check_device_status(void) {
     if (x > 0) rc = ZECO_ERR_TIMEOUT;
   }
   return rc;
+}
+
+int zeco_last_device_status(zeco_stream_t stream) {
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return ZECO_ERR_CUDA;
+  return zeco_check_device_status();
 }
 
 const char* zeco_strerror(int code) {

@@ -109,7 +109,9 @@ __device__ __forceinline__ void st<__nv_bfloat16>(__nv_bfloat16* p, float x) {
 // ------------------------------------------------------- launch bookkeeping
 
 // Per-kernel timing marks (see zeco_set_profile_events); no-ops when off.
-void prof_begin(cudaStream_t st);
+// prof_start right before a kernel's launch, prof_mark(name) right after it,
+// both on the stream the kernel is launched on.
+void prof_start(cudaStream_t st);
 void prof_mark(const char* kernel, cudaStream_t st);
 
 // Sets the dynamic shared-memory limit of a kernel once per process.

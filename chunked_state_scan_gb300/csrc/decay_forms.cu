@@ -48,6 +48,7 @@ cudaError_t launch_expand_log_alpha(const Dims& d, const void* g, void* gx, cuda
   const int64_t n4 = rows * d.dk / 4;
   const unsigned blocks = (unsigned)((n4 + 255) / 256 < 65535 * 16 ? (n4 + 255) / 256 : 65535 * 16);
   const bool scalar = d.decay == ZECO_DECAY_SCALAR;
+  prof_start(st);
   if (d.bf16)
     expand_kernel<<<blocks, 256, 0, st>>>((const __nv_bfloat16*)g, (__nv_bfloat16*)gx, rows,
                                           (int)d.dk, scalar);
@@ -60,6 +61,7 @@ cudaError_t launch_expand_log_alpha(const Dims& d, const void* g, void* gx, cuda
 cudaError_t launch_reduce_dlog_alpha(const Dims& d, const void* dgx, void* dg, cudaStream_t st) {
   const int64_t rows = d.B * d.H * d.T;
   const unsigned blocks = (unsigned)((rows * 32 + 255) / 256);
+  prof_start(st);
   if (d.bf16)
     reduce_kernel<<<blocks, 256, 0, st>>>((const __nv_bfloat16*)dgx, (__nv_bfloat16*)dg, rows,
                                           (int)d.dk);

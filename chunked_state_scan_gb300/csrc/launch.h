@@ -15,10 +15,11 @@ struct Fork {
 };
 // Forks from st (aux waits for st's work so far); off when overlap is disabled.
 Fork fork_begin(cudaStream_t st);
+// The schedule chosen with zeco_set_overlap: 0 one stream, 1 the scan-independent
+// passes on the auxiliary stream, 2 the segment scan on the auxiliary stream.
+int overlap_mode();
 cudaError_t fork_mark(const Fork& f, int i);
 cudaError_t fork_join(const Fork& f, cudaStream_t st, int i);
-// Whether per-kernel profiling marks are being recorded (api.cu).
-bool prof_active();
 
 // ---- bounded-wait flags of the tensor-core kernels: read and clear; -1 when
 //      the flag cannot be read

@@ -18,8 +18,12 @@
 //   - all calls on one GPU share the array, so calls whose GPU work overlaps
 //     (different streams, or threads without ordering) race on it; callers
 //     must order them;
-//   - the first call on each device looks up the array's device address; make
-//     that first call before starting any stream capture on that device.
+//   - the first call on each device looks up the array's device address, with
+//     that device current, and caches it for the life of the process; make that
+//     first call before any stream capture on that device.  A cudaDeviceReset
+//     frees the array with the rest of the device's memory and leaves the cached
+//     address stale, so a process must not call this entry point on a device
+//     after resetting it.
 #include <mutex>
 
 #include "common.cuh"
@@ -35,7 +39,8 @@ constexpr int kMaxDevices = 128;
 std::mutex g_mu;
 void* g_ws_ptr[kMaxDevices] = {};
 
-// Device address of the array on the current device (looked up once per device).
+// Device address of the array on the current device (looked up by the first
+// call on each device, with that device current).
 int noalloc_workspace(void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ZECO_ERR_CUDA;
@@ -56,14 +61,16 @@ extern "C" int zeco_gla_bwd_noalloc(const zeco_shape* shape, const void* q, cons
                                     const void* d_o, const float* dS_final, void* dq, void* dk,
                                     void* dv, void* dlog_alpha, float* dS0,
                                     zeco_stream_t stream) {
-  const size_t need = zeco_gla_workspace_bytes(shape, 1);
-  if (need == 0) return ZECO_ERR_ARG;  // invalid shape (the backward always needs scratch)
-  if (need > (size_t)ZECO_NOALLOC_MAX_WS_BYTES) return ZECO_ERR_WORKSPACE;
+  // invalid or unsupported shapes: the same code as zeco_gla_bwd, before any CUDA call
+  const int path = zeco_gla_resolve_path(shape);
+  if (path < 0) return path;
   void* ws = nullptr;
   const int rc = noalloc_workspace(&ws);
   if (rc != ZECO_OK) return rc;
-  // Every byte of the workspace that the backward reads it has written earlier in
-  // the same call, so the previous call's leftovers need no clearing.
+  // zeco_gla_bwd checks the pointers and then the scratch size against the
+  // array's: oversized shapes get ZECO_ERR_WORKSPACE from it.  Every byte of the
+  // workspace that the backward reads it has written earlier in the same call,
+  // so the previous call's leftovers need no clearing.
   return zeco_gla_bwd(shape, q, k, v, log_alpha, saved, d_o, dS_final, dq, dk, dv, dlog_alpha,
                       dS0, ws, (size_t)ZECO_NOALLOC_MAX_WS_BYTES, stream);
 }

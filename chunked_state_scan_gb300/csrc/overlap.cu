@@ -1,22 +1,25 @@
-// overlap.cu -- a second stream for the steps that do not depend on the
-// segment scan.
+// overlap.cu -- a second stream for work that runs beside the segment scan.
 //
 // The pages' central claim is that the state exchange between segments (the
-// All-Scan) hides behind work that does not need it (ZeCO: Pith review,
-// "What carries the argument"; the diagonal attention overlaps the All-Scan).
-// On one GPU the scan itself is short, but the passes that build the
-// scan-independent operands -- the decay-weighted Q~, K~ (tc_decay.cu), the
-// intra-chunk scores A and their gradient dA (tc_scores.cu) -- run on an
-// auxiliary stream concurrently with pass 1 and the scan (forward) or with the
-// backward pre-pass, the reverse scan and the dv sweep (backward).  The caller's
-// stream forks to the auxiliary stream with an event and joins it with another
-// before the first kernel that reads those operands, so the call stays ordered
-// on the caller's stream (and capturable into a CUDA graph).
+// All-Scan) hides behind work that does not need it (ZeCO: Pith review, "What
+// carries the argument"; Algorithm 1 runs the All-Scan and the intra-chunk
+// diagonal attention on two streams, Eq. 11).  Two schedules use an auxiliary
+// stream:
+//   1 (default): the passes that do not depend on the scan -- the intra-chunk
+//     scores A (forward) and their gradient dA (backward) -- go to the
+//     auxiliary stream as soon as their inputs exist, concurrently with pass 1
+//     and the scan (forward) or with the backward pre-pass, the reverse scan
+//     and the dv sweep;
+//   2 (the pages' schedule): the segment scan itself goes to the auxiliary
+//     stream, concurrently with the diagonal-attention pass (A, or dA) on the
+//     caller's stream.
+// The caller's stream forks to the auxiliary stream with an event and joins it
+// with another before the first kernel that needs the forked work, so the call
+// stays ordered on the caller's stream (and capturable into a CUDA graph).
 //
 // The auxiliary stream and its events are created on first use, once per host
 // thread and device, and live until the thread exits.  zeco_set_overlap(0)
-// turns the fork off (everything on the caller's stream); so does an active
-// zeco_set_profile_events, whose per-kernel marks assume one stream.
+// turns the fork off (everything on the caller's stream).
 #include <atomic>
 
 #include "common.cuh"
@@ -65,11 +68,13 @@ AuxState* aux_for_current_device() {
 
 }  // namespace
 
+int overlap_mode() { return g_overlap.load(std::memory_order_relaxed); }
+
 Fork fork_begin(cudaStream_t st) {
   Fork f;
   f.aux = st;
   f.on = false;
-  if (!g_overlap.load(std::memory_order_relaxed) || prof_active()) return f;
+  if (!g_overlap.load(std::memory_order_relaxed)) return f;
   AuxState* a = aux_for_current_device();
   if (!a) return f;
   if (cudaEventRecord(a->ev[0], st) != cudaSuccess) return f;
@@ -91,7 +96,8 @@ cudaError_t fork_join(const Fork& f, cudaStream_t st, int i) {
 
 }  // namespace zeco
 
-extern "C" int zeco_set_overlap(int on) {
-  zeco::g_overlap.store(on ? 1 : 0, std::memory_order_relaxed);
+extern "C" int zeco_set_overlap(int mode) {
+  if (mode < 0 || mode > 2) return ZECO_ERR_ARG;
+  zeco::g_overlap.store(mode, std::memory_order_relaxed);
   return ZECO_OK;
 }

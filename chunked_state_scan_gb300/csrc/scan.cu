@@ -187,6 +187,7 @@ cudaError_t launch_seg_scan_fwd(const Dims& d, float* S_in, const float* gamma, 
                                 float* S_final, cudaStream_t st) {
   const int rows = (int)(d.dk / d.K);
   dim3 grid((rows + kWarps - 1) / kWarps, d.K, (unsigned)(d.B * d.H));
+  prof_start(st);
   seg_scan_fwd_kernel<<<grid, kWarps * 32, 0, st>>>(S_in, gamma, S0, S_final, d.P, (int)d.dk,
                                                     (int)d.dv, rows);
   prof_mark("seg_scan_fwd", st);
@@ -198,6 +199,7 @@ cudaError_t launch_seg_scan_rev(const Dims& d, float* D, const float* S_in, cons
                                 cudaStream_t st) {
   const int rows = (int)(d.dk / d.K);
   dim3 grid((rows + kWarps - 1) / kWarps, d.K, (unsigned)(d.B * d.H));
+  prof_start(st);
   seg_scan_rev_kernel<<<grid, kWarps * 32, 0, st>>>(D, S_in, gamma, dS_final, dS0, carry, d.P,
                                                     (int)d.dk, (int)d.dv, rows);
   prof_mark("seg_scan_rev", st);

@@ -587,6 +587,7 @@ cudaError_t fwd_out_t(const Dims& d, const T* q, const T* k, const T* v, const T
   cudaError_t e = allow_smem(fwd_out_kernel<T>, sm);
   if (e != cudaSuccess) return e;
   dim3 g2((unsigned)(d.dv / kNV), bhp);
+  prof_start(st);
   fwd_out_kernel<T><<<g2, kThreads, sm, st>>>(q, k, v, g, S_in, o, d);
   prof_mark("simt_fwd_out", st);
   return cudaGetLastError();
@@ -598,6 +599,7 @@ cudaError_t forward_t(const Dims& d, const T* q, const T* k, const T* v, const T
                       cudaStream_t st) {
   const unsigned bhp = (unsigned)(d.B * d.H * d.P);
   dim3 g1((unsigned)((d.dv + 63) / 64), (unsigned)((d.dk + 63) / 64), bhp);
+  prof_start(st);
   seg_state_kernel<T, true><<<g1, kThreads, 0, st>>>(k, v, g, S_in, gamma, d, 1);
   prof_mark("simt_chunk_state", st);
   cudaError_t e = cudaGetLastError();
@@ -616,6 +618,7 @@ cudaError_t bwd_main_t(const Dims& d, const T* q, const T* k, const T* v, const 
   cudaError_t e = allow_smem(bwd_dv_kernel<T>, sm1);
   if (e != cudaSuccess) return e;
   dim3 g2((unsigned)(d.dv / kNV), bhp);
+  prof_start(st);
   bwd_dv_kernel<T><<<g2, kThreads, sm1, st>>>(q, k, g, dO, D, dv, d);
   prof_mark("simt_bwd_dv", st);
   e = cudaGetLastError();
@@ -624,6 +627,7 @@ cudaError_t bwd_main_t(const Dims& d, const T* q, const T* k, const T* v, const 
   e = allow_smem(bwd_dqk_kernel<T>, sm2);
   if (e != cudaSuccess) return e;
   dim3 g3((unsigned)(d.dk / kKB), bhp);
+  prof_start(st);
   bwd_dqk_kernel<T><<<g3, kThreads, sm2, st>>>(q, k, v, g, dO, S_in, D, carry, dq, dk, dg, qdq,
                                                d);
   prof_mark("simt_bwd_dqk", st);
@@ -637,6 +641,7 @@ cudaError_t backward_t(const Dims& d, const T* q, const T* k, const T* v, const 
                        float* carry, float* qdq, cudaStream_t st) {
   const unsigned bhp = (unsigned)(d.B * d.H * d.P);
   dim3 g1((unsigned)((d.dv + 63) / 64), (unsigned)((d.dk + 63) / 64), bhp);
+  prof_start(st);
   seg_state_kernel<T, false><<<g1, kThreads, 0, st>>>(q, dO, g, D, nullptr, d, 0);
   prof_mark("simt_dstate_local", st);
   cudaError_t e = cudaGetLastError();
@@ -708,6 +713,7 @@ cudaError_t simt_bwd_dqk_bf16(const Dims& d, const void* q, const void* k, const
   cudaError_t e = allow_smem(bwd_dqk_kernel<T>, sm2);
   if (e != cudaSuccess) return e;
   dim3 g3((unsigned)(d.dk / kKB), bhp);
+  prof_start(st);
   bwd_dqk_kernel<T><<<g3, kThreads, sm2, st>>>((const T*)q, (const T*)k, (const T*)v,
                                                (const T*)g, (const T*)d_o, S_in, D, carry,
                                                (T*)dq, (T*)dk, (T*)dg, qdq, d);

@@ -16,7 +16,8 @@ bool tc_uses_dA(const Dims& d) {
 
 // Forward: the decay pass, then pass 1 (on its K~ and e^{b_last}) and the scan on
 // the caller's stream while the scores run on the auxiliary stream (they do not
-// depend on the scan); pass 2 joins both.
+// depend on the scan); pass 2 joins both.  In overlap mode 2 the scan runs on the
+// auxiliary stream instead, beside the scores (the pages' schedule).
 cudaError_t tc_forward(const Dims& d, const void* q, const void* k, const void* v,
                        const void* g, const float* S0, void* o, float* S_final, float* S_in,
                        float* gamma, const TcOps& ops, cudaStream_t st) {
@@ -33,6 +34,18 @@ cudaError_t tc_forward(const Dims& d, const void* q, const void* k, const void* 
   void* A = ops.A;
   cudaError_t e = tc_decay(d, q, k, g, Qt, Kt, Eb, st);
   if (e != cudaSuccess) return e;
+  if (overlap_mode() == 2) {
+    // the pages' schedule: the scan on the second stream beside the scores
+    e = tc_chunk_state(d, k, v, g, Kt, Eb, S_in, gamma, st);
+    if (e != cudaSuccess) return e;
+    const Fork f = fork_begin(st);
+    e = launch_seg_scan_fwd(d, S_in, gamma, S0, S_final, f.aux);
+    if (e == cudaSuccess) e = fork_mark(f, 0);
+    if (e == cudaSuccess) e = tc_A(d, Qt, Kt, A, st);
+    if (e == cudaSuccess) e = fork_join(f, st, 0);
+    if (e != cudaSuccess) return e;
+    return tc_fwd_out(d, Qt, Kt, v, A, Eb, S_in, o, st);
+  }
   const Fork f = fork_begin(st);
   e = tc_A(d, Qt, Kt, A, f.aux);
   if (e == cudaSuccess) e = fork_mark(f, 0);
@@ -46,7 +59,8 @@ cudaError_t tc_forward(const Dims& d, const void* q, const void* k, const void* 
 
 // Backward: Q~, K~, e^{b_last} and the masked scores A are the forward's (kept in
 // `saved`); the pre-pass, the reverse scan and the dv sweep run on the caller's
-// stream while the score gradient dA runs on the auxiliary stream.
+// stream while the score gradient dA runs on the auxiliary stream (overlap mode 2:
+// the reverse scan on the auxiliary stream beside dA).
 cudaError_t tc_backward(const Dims& d, const void* q, const void* k, const void* v,
                         const void* g, const float* S_in, const float* gamma, const void* d_o,
                         const float* dS_final, void* dq, void* dk, void* dv, void* dg,
@@ -65,14 +79,27 @@ cudaError_t tc_backward(const Dims& d, const void* q, const void* k, const void*
   const void* A = ops.A;
   const bool qk_tc = tc_uses_dA(d);
   void* dA = ops.dA;
-  const Fork f = fork_begin(st);
-  cudaError_t e = qk_tc ? tc_dA(d, d_o, v, dA, f.aux) : cudaSuccess;
-  if (e == cudaSuccess) e = fork_mark(f, 0);
-  if (e != cudaSuccess) return e;
-  e = tc_dstate_local(d, q, d_o, g, Qt, Eb, D, st);
-  if (e == cudaSuccess) e = launch_seg_scan_rev(d, D, S_in, gamma, dS_final, dS0, carry, st);
-  if (e == cudaSuccess) e = tc_bwd_dv(d, Qt, Kt, d_o, A, Eb, D, dv, st);
-  if (e == cudaSuccess) e = fork_join(f, st, 0);
+  cudaError_t e = cudaSuccess;
+  if (overlap_mode() == 2) {
+    // the pages' schedule: the reverse scan on the second stream beside dA
+    e = tc_dstate_local(d, q, d_o, g, Qt, Eb, D, st);
+    if (e != cudaSuccess) return e;
+    const Fork f = fork_begin(st);
+    e = launch_seg_scan_rev(d, D, S_in, gamma, dS_final, dS0, carry, f.aux);
+    if (e == cudaSuccess) e = fork_mark(f, 0);
+    if (e == cudaSuccess && qk_tc) e = tc_dA(d, d_o, v, dA, st);
+    if (e == cudaSuccess) e = fork_join(f, st, 0);
+    if (e == cudaSuccess) e = tc_bwd_dv(d, Qt, Kt, d_o, A, Eb, D, dv, st);
+  } else {
+    const Fork f = fork_begin(st);
+    e = qk_tc ? tc_dA(d, d_o, v, dA, f.aux) : cudaSuccess;
+    if (e == cudaSuccess) e = fork_mark(f, 0);
+    if (e != cudaSuccess) return e;
+    e = tc_dstate_local(d, q, d_o, g, Qt, Eb, D, st);
+    if (e == cudaSuccess) e = launch_seg_scan_rev(d, D, S_in, gamma, dS_final, dS0, carry, st);
+    if (e == cudaSuccess) e = tc_bwd_dv(d, Qt, Kt, d_o, A, Eb, D, dv, st);
+    if (e == cudaSuccess) e = fork_join(f, st, 0);
+  }
   if (e != cudaSuccess) return e;
   if (qk_tc) return tc_bwd_qk(d, Qt, Kt, v, g, Eb, dA, S_in, d_o, dq, dk, dg, D, carry, qdq, st);
   return simt_bwd_dqk_bf16(d, q, k, v, g, S_in, d_o, dq, dk, dg, D, carry, qdq, st);

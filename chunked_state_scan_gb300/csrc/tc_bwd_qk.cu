@@ -588,6 +588,7 @@ cudaError_t launch_qk(const Dims& d, const CUtensorMap& tx, const CUtensorMap& t
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  prof_start(st);
   return cudaLaunchKernelEx(&cfg, kern, tx, tu, tz, tp, ty, tg, tqd, tout, taux, Eb, S_src,
                             carry, d.T, (int)d.dk, d.P, d.L);
 }

@@ -72,6 +72,71 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
+// The CTA's abort word: a 32-bit word in shared memory that a thread reads and
+// sets through its 32-bit shared address with volatile shared accesses.
+__device__ __forceinline__ bool abort_is_set(uint32_t saddr) {
+  uint32_t v;
+  asm volatile("ld.volatile.shared.u32 %0, [%1];" : "=r"(v) : "r"(saddr));
+  return v != 0;
+}
+__device__ __forceinline__ void abort_raise(uint32_t saddr) {
+  asm volatile("st.volatile.shared.u32 [%0], %1;" ::"r"(saddr), "r"(1u) : "memory");
+}
+
+// The same wait for kernels whose threads share an abort word: it also gives up
+// once the word is set, and sets it itself when its own time limit runs out.  So
+// once one wait of a CTA has given up, every other wait of the CTA gives up after
+// at most 64 more polls instead of its own time limit: a wait that cannot
+// complete costs the CTA about one time limit, not one per wait.  The word is
+// read only where the clock is (every 64 failed polls), so a wait costs what
+// mbar_wait costs.
+__device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parity,
+                                                   uint32_t abort_saddr) {
+  const uint32_t a = smem_u32(bar);
+  uint64_t t0 = 0;
+  for (uint32_t it = 0;; ++it) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(a), "r"(parity)
+        : "memory");
+    if (done) return true;
+    if ((it & 63u) == 63u) {
+      if (abort_is_set(abort_saddr)) return false;
+      const uint64_t now = global_ns();
+      if (t0 == 0) t0 = now;
+      else if (now - t0 > kWaitNs) {
+        abort_raise(abort_saddr);
+        return false;
+      }
+    }
+  }
+}
+
+// A CTA's view of its bounded waits: the shared address of its abort word and
+// the file's global status flag (set, for the host to read, whenever a wait
+// gives up).
+struct Waits {
+  uint32_t abort;
+  int* status;
+  __device__ __forceinline__ bool operator()(uint64_t* bar, uint32_t parity) const {
+    if (mbar_wait_or_abort(bar, parity, abort)) return true;
+    atomicExch(status, 1);
+    return false;
+  }
+  __device__ __forceinline__ bool aborted() const { return abort_is_set(abort); }
+};
+
+// After an abort: wait (again bounded, ignoring the abort word) for the last
+// phase that this thread's copies were to complete on `bar` (`issued` phases in
+// all), so that no copy is still writing into the CTA's shared memory when it
+// exits.  Phases complete in order, so the last one covers the earlier ones.
+__device__ __forceinline__ void drain_phase(uint64_t* bar, uint32_t issued) {
+  if (issued > 0) (void)mbar_wait(bar, (issued - 1u) & 1u);
+}
+
 // ------------------------------------------------------------------ TMA
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int32_t x,
                                             int32_t y, uint64_t* bar) {

@@ -85,6 +85,7 @@ cudaError_t tc_decay(const Dims& d, const void* q, const void* k, const void* g,
   auto qb = (const __nv_bfloat16*)q;
   auto kb = (const __nv_bfloat16*)k;
   auto gb = (const __nv_bfloat16*)g;
+  prof_start(st);
   if (d.dk == 256)
     decay_kernel<256><<<blocks, 256, 0, st>>>(qb, kb, gb, (__nv_bfloat16*)Qt,
                                               (__nv_bfloat16*)Kt, Eb, nchunks);

@@ -88,8 +88,15 @@ tc_sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   extern __shared__ __align__(1024) unsigned char smraw[];
   unsigned char* sm = align1024(smraw);
   unsigned char* sV = sm + SM::kV;
-  __shared__ uint64_t bar_x[2], bar_v[2], bar_e[kESlots], bar_u, bar_g;
+  __shared__ uint64_t bar_x[2], bar_v[2], bar_e[kESlots], bar_u, bar_g, bar_fin;
   __shared__ uint32_t tmem_base;
+  __shared__ int abort_word;  // set when a bounded wait of this CTA gives up
+  // After a wait of this CTA has given up, the abort word makes every later wait
+  // of the CTA give up within 64 polls and the copy thread issues no further
+  // copies: the chunk loop runs to its end without waiting, and the CTA drains
+  // what it has in flight before exit.
+  const Waits wait{smem_u32(&abort_word), &g_fwd_status};
+  auto wt = [&](uint64_t* bar, uint32_t parity) { (void)wait(bar, parity); };
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int lg = warp & 3;       // TMEM lane group of this warp
@@ -109,6 +116,8 @@ tc_sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     for (int k = 0; k < kESlots; ++k) mbar_init(&bar_e[k], 1);
     mbar_init(&bar_u, 1);
     mbar_init(&bar_g, 1);
+    mbar_init(&bar_fin, 1);
+    abort_word = 0;
     fence_mbar_init();
   }
   if (tid == kTmaTid) {
@@ -124,9 +133,15 @@ tc_sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   const uint32_t tmem = tmem_base;
   const uint32_t lane_off = (uint32_t)(lg * 32) << 16;
 
+  // chunks whose tiles (x and v) and e^{b_last} rows the copy thread has
+  // requested: chunk c of the sweep goes to buffer c % 2 and ring slot c % kESlots,
+  // so these totals give the phases issued on every copy barrier (after an abort
+  // the copies still in flight are waited for before the CTA exits)
+  uint32_t n_xv = 0, n_e = 0;
   // Q~, K~ and masked-score tiles (forward: and the e^{b_last} row) of chunk n
   // into buffer `buf`
   auto issue_x = [&](int n, int buf) {
+    ++n_xv;
     const int32_t r = (int32_t)(row0 + (int64_t)n * kC);
     unsigned char* xb = sm + SM::kX + buf * SM::kXBuf;
     mbar_expect_tx(&bar_x[buf], 2 * SM::kTile + kC * kC * 2 + (BWD ? 0 : DK * 4));
@@ -142,12 +157,13 @@ tc_sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const int n = BWD ? nc - 1 - it : it;
     const int k = it % kESlots;
     const int32_t r = (int32_t)(row0 + (int64_t)n * kC);
+    ++n_e;
     mbar_expect_tx(&bar_e[k], DK * 4);
     bulk_load(sm + SM::kE + k * DK * 4, Eb + (size_t)(r / kC) * DK, DK * 4, &bar_e[k]);
   };
   auto e_slot = [&](int it) -> const float* {  // waits for, and returns, iteration it's row
     const int k = it % kESlots;
-    if (!mbar_wait(&bar_e[k], (uint32_t)((it / kESlots) & 1))) atomicExch(&g_fwd_status, 1);
+    wt(&bar_e[k], (uint32_t)((it / kESlots) & 1));
     return reinterpret_cast<const float*>(sm + SM::kE + k * DK * 4);
   };
   auto issue_v = [&](int n, int buf) {
@@ -262,11 +278,11 @@ tc_sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     unsigned char* sQ = sm + SM::kX + xbuf * SM::kXBuf;
     unsigned char* sK = sQ + SM::kTile;
     unsigned char* sP = sQ + SM::kP;
-    if (!mbar_wait(&bar_x[xbuf], (uint32_t)((it >> 1) & 1))) atomicExch(&g_fwd_status, 1);
+    wt(&bar_x[xbuf], (uint32_t)((it >> 1) & 1));
     // the next chunk's tiles go to the other buffers (their last readers, the MMAs
     // and the state pass of the previous chunk, completed before the block barrier
-    // that ended the previous iteration)
-    if (tid == kTmaTid && it + 1 < nc) {
+    // that ended the previous iteration); none once a wait has given up
+    if (tid == kTmaTid && it + 1 < nc && !wait.aborted()) {
       issue_x(BWD ? n - 1 : n + 1, xbuf ^ 1);
       issue_v(BWD ? n - 1 : n + 1, xbuf ^ 1);
       // (slot (it + 2) % 3 was last read by the state pass of iteration it - 1)
@@ -279,7 +295,7 @@ tc_sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       const uint32_t q0 = smem_u32(sQ), k0 = smem_u32(sK), p0 = smem_u32(sP);
       const uint32_t v0 = smem_u32(sV + xbuf * SM::kVBuf);
       const uint32_t oc = tmem + kColO + (uint32_t)xbuf * 64;
-      if (!mbar_wait(&bar_v[xbuf], (uint32_t)((it >> 1) & 1))) atomicExch(&g_fwd_status, 1);
+      wt(&bar_v[xbuf], (uint32_t)((it >> 1) & 1));
       tc_fence_after();
       // the state update first: its completion releases part 1 of the state pass
       // forward:  S^T  += V^T  K~   (M = 128 columns j, N = DK rows i, K = 64 tokens s)
@@ -326,17 +342,35 @@ tc_sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const bool more = it + 1 < nc;
     float r[kQ];
     if (more) {
-      if (!mbar_wait(&bar_u, par)) atomicExch(&g_fwd_status, 1);
+      wt(&bar_u, par);
       tc_fence_after();
       scale_part(BWD ? e_slot(it + 1) : reinterpret_cast<const float*>(sQ + SM::kEx), r);
     }
-    if (!mbar_wait(&bar_g, par)) atomicExch(&g_fwd_status, 1);
+    wt(&bar_g, par);
     tc_fence_after();
     if (more) copy_part(r);
     tc_fence_before();
     __syncthreads();
   }
-  if (warp < 8) epilogue(BWD ? 0 : nc - 1, (nc - 1) & 1);
+  if (!wait.aborted()) {
+    if (warp < 8) epilogue(BWD ? 0 : nc - 1, (nc - 1) & 1);
+  } else {
+    // a wait gave up: no MMA may still write tensor memory and no copy may still
+    // write shared memory when the CTA exits (both waits bounded again)
+    if (tid == kMmaTid) {
+      umma_commit(&bar_fin);
+      (void)mbar_wait(&bar_fin, 0u);
+    }
+    if (tid == kTmaTid) {
+      for (uint32_t b = 0; b < 2; ++b) {
+        const uint32_t ph = n_xv > b ? (n_xv - b + 1) / 2 : 0;
+        drain_phase(&bar_x[b], ph);
+        drain_phase(&bar_v[b], ph);
+      }
+      for (uint32_t k = 0; k < (uint32_t)kESlots; ++k)
+        drain_phase(&bar_e[k], n_e > k ? (n_e - k + kESlots - 1) / kESlots : 0);
+    }
+  }
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, 512);
@@ -356,6 +390,7 @@ cudaError_t launch_sweep(const Dims& d, const void* Qt, const void* Kt, const vo
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)(d.dv / kNV), (unsigned)(d.B * d.H * d.P));
+  prof_start(st);
   kern<<<grid, kThreads, smem, st>>>(tq, tk, tv, tp, Eb, S_src, (__nv_bfloat16*)o, d.T,
                                      (int)d.dv, d.P, d.L);
   return cudaGetLastError();

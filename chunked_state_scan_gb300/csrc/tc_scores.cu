@@ -43,10 +43,13 @@ tc_masked_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
                  __nv_bfloat16* __restrict__ P, int64_t nchunks, int K) {
   extern __shared__ __align__(1024) unsigned char smraw[];
   unsigned char* sm = align1024(smraw);
-  __shared__ uint64_t full[kStages], empty[kStages], accfull[2], accempty[2];
+  __shared__ uint64_t full[kStages], empty[kStages], accfull[2], accempty[2], fin;
   __shared__ uint32_t tmem_base;
+  __shared__ int abort_word;  // set when a bounded wait of this CTA gives up
+  const Waits wait{smem_u32(&abort_word), &g_scores_status};
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nq = K / kQ;
+  int64_t gi = 0;  // producer: (chunk, K slice) stages issued
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -57,6 +60,8 @@ tc_masked_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
       mbar_init(&accfull[b], 1);
       mbar_init(&accempty[b], 128);
     }
+    mbar_init(&fin, 1);
+    abort_word = 0;
     fence_mbar_init();
     prefetch_tmap(&tmX);
     prefetch_tmap(&tmY);
@@ -70,13 +75,16 @@ tc_masked_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
   if (warp == 4) {
     // ---- producer: X and Y tiles of every (chunk, K slice) this CTA owns
     if (lane == 0) {
-      int64_t gi = 0;
-      for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x) {
+      bool go = true;
+      for (int64_t c = blockIdx.x; go && c < nchunks; c += gridDim.x) {
         const int32_t r = (int32_t)(c * kC);
         for (int q = 0; q < nq; ++q, ++gi) {
           const int s = (int)(gi % kStages);
           const uint32_t ph = (uint32_t)((gi / kStages) & 1);
-          if (!mbar_wait(&empty[s], ph ^ 1u)) atomicExch(&g_scores_status, 1);
+          if (!wait(&empty[s], ph ^ 1u)) {
+            go = false;  // no further copies
+            break;
+          }
           unsigned char* st = sm + s * kStageBytes;
           mbar_expect_tx(&full[s], kStageBytes);
           for (int b = 0; b < kQ / 64; ++b) {
@@ -93,13 +101,13 @@ tc_masked_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
       constexpr uint32_t id = idesc_bf16(64, 64, false, false);
       int64_t gi = 0;
       int k = 0;
-      for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x, ++k) {
+      for (int64_t c = blockIdx.x; c < nchunks && !wait.aborted(); c += gridDim.x, ++k) {
         const int b = k & 1;
-        if (!mbar_wait(&accempty[b], (uint32_t)(((k >> 1) & 1) ^ 1))) atomicExch(&g_scores_status, 1);
+        if (!wait(&accempty[b], (uint32_t)(((k >> 1) & 1) ^ 1))) break;
         tc_fence_after();
         for (int q = 0; q < nq; ++q, ++gi) {
           const int s = (int)(gi % kStages);
-          if (!mbar_wait(&full[s], (uint32_t)((gi / kStages) & 1))) atomicExch(&g_scores_status, 1);
+          if (!wait(&full[s], (uint32_t)((gi / kStages) & 1))) break;
           tc_fence_after();
           const uint32_t a0 = smem_u32(sm + s * kStageBytes), b0 = a0 + kHalf;
 #pragma unroll
@@ -112,6 +120,11 @@ tc_masked_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
         }
         umma_commit(&accfull[b]);
       }
+      if (wait.aborted()) {
+        // no MMA may still write tensor memory when it is freed
+        umma_commit(&fin);
+        (void)mbar_wait(&fin, 0u);
+      }
     }
     __syncwarp();
   } else {
@@ -120,7 +133,7 @@ tc_masked_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
     for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x, ++k) {
       const int b = k & 1;
-      if (!mbar_wait(&accfull[b], (uint32_t)((k >> 1) & 1))) atomicExch(&g_scores_status, 1);
+      if (!wait(&accfull[b], (uint32_t)((k >> 1) & 1))) break;
       tc_fence_after();
       float a[64];
       tmem_ld32(tmem + lane_off + b * 64, a);
@@ -147,6 +160,14 @@ tc_masked_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, 128);
+  // after the CTA's last barrier every thread has finished: if any wait gave up,
+  // copies still in flight land before the CTA exits (stage s has been issued
+  // ceil((gi - s) / kStages) times; bounded waits)
+  if (warp == 4 && lane == 0 && wait.aborted())
+    for (int s = 0; s < kStages; ++s) {
+      const int64_t n = gi > s ? (gi - s + kStages - 1) / kStages : 0;
+      drain_phase(&full[s], (uint32_t)n);
+    }
 }
 
 }  // namespace
@@ -171,6 +192,7 @@ cudaError_t launch_masked(const Dims& d, const void* X, const void* Y, int K, vo
     return e;
   const int64_t nchunks = (int64_t)rows / kC;
   const unsigned grid = (unsigned)(nchunks < sms ? nchunks : sms);
+  prof_start(st);
   tc_masked_kernel<<<grid, kThreads, smem, st>>>(tx, ty, (__nv_bfloat16*)P, nchunks, K);
   return cudaGetLastError();
 }

@@ -68,9 +68,15 @@ tc_seg_state_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
   constexpr int kStageBytes = kXBytes + GB + kBBytes;
   extern __shared__ __align__(1024) unsigned char smraw[];
   unsigned char* sm = align1024(smraw);
-  __shared__ uint64_t tma_bar[kStages], mma_bar[kStages];
+  __shared__ uint64_t tma_bar[kStages], mma_bar[kStages], fin_bar;
   __shared__ uint32_t tmem_base;
-  __shared__ int abort_flag;
+  __shared__ int abort_flag;  // set when a bounded wait of this CTA gives up
+  // After a wait of this CTA has given up, the abort word makes every later wait
+  // of the CTA give up within 64 polls and the producer issues no further copies:
+  // the stage loop runs to its end without waiting and the CTA drains what it has
+  // in flight before exit.
+  const Waits wait{smem_u32(&abort_flag), &g_tc_status};
+  auto wt = [&](uint64_t* bar, uint32_t parity) { return wait(bar, parity); };
   __shared__ float Gq[4][kM];  // per-quarter sums of log_alpha of the current stage
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -87,6 +93,7 @@ tc_seg_state_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
       mbar_init(&tma_bar[s], 1);
       mbar_init(&mma_bar[s], 1);
     }
+    mbar_init(&fin_bar, 1);
     abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tmX);
@@ -121,18 +128,23 @@ tc_seg_state_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
   auto cbar = []() { asm volatile("bar.sync 1, %0;" ::"n"(kStateThreads) : "memory"); };
   if (warp == kStateThreads / 32) {
     // ---- producer: stage it once the MMAs that last read its buffers are done
+    int issued = 0;
     if (lane == 0) {
       for (int it = 0; it < nblk; ++it) {
         const int jn = it - SG;
-        if (jn >= 0 && !mbar_wait(&mma_bar[it % SG], (jn / SG) & 1)) {
-          atomicExch(&g_tc_status, 1);
-          break;
-        }
+        if (jn >= 0 && !wt(&mma_bar[it % SG], (jn / SG) & 1)) break;
+        if (wait.aborted()) break;  // another thread's wait gave up: no further copies
         issue_tma(it);
+        issued = it + 1;
       }
     }
     tc_fence_before();
     __syncthreads();
+    // after the CTA's last barrier every thread has finished: if any wait gave
+    // up, copies still in flight land before the CTA exits (bounded waits)
+    if (lane == 0 && wait.aborted())
+      for (int s = 0; s < SG; ++s)
+        drain_phase(&tma_bar[s], (uint32_t)(issued > s ? (issued - s + SG - 1) / SG : 0));
     return;
   }
   float run = 0.f;  // log-decay of row i summed over the stages already done
@@ -150,10 +162,7 @@ tc_seg_state_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
   for (int it = 0; it < nblk; ++it) {
     const int s = it % SG;
     unsigned char* xbuf = sm + s * kStageBytes;
-    if (!mbar_wait(&tma_bar[s], (it / SG) & 1)) {
-      atomicExch(&g_tc_status, 1);
-      abort_flag = 1;
-    }
+    wt(&tma_bar[s], (it / SG) & 1);
     if (PRE) {
       // every 16-byte group of 8 rows of the tile scaled in place (2 per thread, the
       // same 8 rows in every stage): this stage's factor of each of those rows from
@@ -228,7 +237,6 @@ tc_seg_state_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
     }
     fence_async_smem();
     cbar();
-    if (abort_flag) break;
     if (tid == 0) {
       tc_fence_after();
       const uint32_t a0 = smem_u32(xbuf), b0 = a0 + kXBytes + GB;
@@ -243,14 +251,14 @@ tc_seg_state_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
     }
   }
   cbar();
-  const bool ok = !abort_flag;
+  const bool ok = !wait.aborted();
   // PRE: gamma_p of every row is the product over all the segment's chunks
   if (PRE && REV && ok && gamma && blockIdx.x == 0 && tid < 16)
 #pragma unroll
     for (int u = 0; u < 8; ++u) gamma[((size_t)bh * P + p) * dk + i0 + p_r8 + u] = run8[u];
   if (ok && warp < 4) {
     const int last = nblk - 1;
-    if (!mbar_wait(&mma_bar[last % SG], (last / SG) & 1)) atomicExch(&g_tc_status, 1);
+    wt(&mma_bar[last % SG], (last / SG) & 1);
     tc_fence_after();
     float* orow = out + (((size_t)bh * (P + 1) + p + slot_off) * dk + i) * dv + j0;
 #pragma unroll 1
@@ -265,6 +273,12 @@ tc_seg_state_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
     }
     if (!PRE && REV && gamma && blockIdx.x == 0) gamma[((size_t)bh * P + p) * dk + i] = __expf(run);
     (void)lane;
+  }
+  if (tid == 0 && wait.aborted()) {
+    // a wait gave up: no MMA may still write tensor memory when it is freed
+    // (bounded wait)
+    umma_commit(&fin_bar);
+    (void)mbar_wait(&fin_bar, 0u);
   }
   tc_fence_before();
   __syncthreads();
@@ -352,6 +366,7 @@ static cudaError_t launch_state(const Dims& d, const void* x, const void* y, con
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)(d.dv / NT), (unsigned)(d.dk / kM), (unsigned)(d.B * d.H * d.P));
+  prof_start(st);
   kern<<<grid, kStateBlock, smem, st>>>(tx, tg, ty, Eb, out, gamma, d.T, (int)d.dk,
                                           (int)d.dv, d.P, d.L, slot_off);
   return cudaGetLastError();

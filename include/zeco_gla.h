@@ -40,7 +40,7 @@
  *     bf16 tensor-core products accumulate in fp32).
  *   - Every pointer is DEVICE memory owned by the caller and must be 16-byte
  *     aligned.  The library never allocates, never frees, never synchronises
- *     and never prints.  Work is enqueued on `stream` (NULL: the legacy default
+ *     (except zeco_last_device_status, whose job it is) and never prints.  Work is enqueued on `stream` (NULL: the legacy default
  *     stream) and is asynchronous; outputs are valid once the stream reaches
  *     that point.  Calls that share `saved` or `workspace` must be ordered.
  *   - Return value: ZECO_OK (0) or a negative ZECO_ERR_* code; nothing is
@@ -184,18 +184,23 @@ int zeco_gla_bwd(const zeco_shape *shape, const void *q, const void *k, const vo
  * counterpart: this exists for callers that cannot allocate device memory --
  * code that runs where cudaMalloc is unavailable or forbidden, or inside a
  * host framework that owns all device memory and passes in only the tensors).
- * Same arguments, results and errors as zeco_gla_bwd, minus workspace and
- * ws_bytes: the scratch is a fixed array of ZECO_NOALLOC_MAX_WS_BYTES in the
- * library's own device memory, which every GPU that loads the library holds
- * until the process exits.  Nothing is allocated or freed by the call.
+ * Same arguments, results and return codes as zeco_gla_bwd, minus workspace
+ * and ws_bytes: the scratch is a fixed array of ZECO_NOALLOC_MAX_WS_BYTES in
+ * the library's own device memory, which every GPU that loads the library
+ * holds until the process exits.  Nothing is allocated or freed by the call.
  *   - Shapes needing more scratch than that (zeco_gla_workspace_bytes(shape, 1)
- *     > ZECO_NOALLOC_MAX_WS_BYTES) return ZECO_ERR_WORKSPACE.
+ *     > ZECO_NOALLOC_MAX_WS_BYTES) return ZECO_ERR_WORKSPACE, after the same
+ *     shape and pointer checks as zeco_gla_bwd.
  *   - All calls on one GPU share the array: calls whose GPU work could overlap
  *     (other streams, other host threads) race on it and must be ordered by
  *     the caller.  The array keeps the last call's contents; the backward
  *     writes every scratch byte before reading it.
  *   - The first call on each device looks up the array's device address with
- *     that device current; make the first call before any stream capture.
+ *     that device current and caches it for the life of the process: make that
+ *     first call before any stream capture on the device.  A cudaDeviceReset
+ *     frees the array with the rest of the device's memory and leaves the
+ *     cached address stale: do not call this entry point on a device after
+ *     resetting it in the same process.
  */
 #define ZECO_NOALLOC_MAX_WS_BYTES (32u << 20)
 int zeco_gla_bwd_noalloc(const zeco_shape *shape, const void *q, const void *k, const void *v,
@@ -206,22 +211,43 @@ int zeco_gla_bwd_noalloc(const zeco_shape *shape, const void *q, const void *k, 
 /*
  * Every wait of the tensor-core kernels on an mbarrier (a copy or an MMA group
  * to complete, a peer CTA's partial sums) gives up after 2 seconds (device
- * %globaltimer) instead of hanging the GPU; the kernel then records it in a device
- * flag and continues, so that call's outputs are not valid.  This reads and
- * clears the flags of the current device: ZECO_OK when no wait gave up since
- * the last check, ZECO_ERR_TIMEOUT when one did, ZECO_ERR_CUDA when the flags
- * cannot be read.  It copies from device memory: call it after the streams of
- * the calls it should cover have been synchronised.
+ * %globaltimer) instead of hanging the GPU.  The first wait of a CTA that gives
+ * up sets a device flag and an abort word of that CTA: every other wait of the
+ * CTA then returns at once, it issues no further copies, MMAs, remote stores
+ * or remote arrives, waits (bounded again) for the copies and MMAs it has in
+ * flight, frees its tensor memory and exits.  A wait that can never complete
+ * therefore costs each CTA that meets it about one time limit.  The outputs of
+ * that call are not valid.
+ *
+ * zeco_check_device_status reads and clears the flags of the current device:
+ * ZECO_OK when no wait gave up since the last check, ZECO_ERR_TIMEOUT when one
+ * did, ZECO_ERR_CUDA when the flags cannot be read.  The flags are per device,
+ * not per stream or per call: a check reports (and clears) a give-up of any
+ * call on any stream of this device since the previous check, so two host
+ * threads that check the same device at once can clear each other's reports.
+ * It copies from device memory and synchronises nothing itself: call it after
+ * the streams of the calls it should cover have been synchronised.
  */
 int zeco_check_device_status(void);
 
 /*
+ * Checked mode: synchronises `stream` (so every call enqueued on it so far has
+ * finished), then reads and clears the bounded-wait flags of the current device
+ * as zeco_check_device_status does (same codes; ZECO_ERR_CUDA also when the
+ * synchronisation fails).  The only entry point that synchronises.  The flags
+ * are per device, so a give-up in a call on another stream of the device that
+ * finished before the read is reported too.
+ */
+int zeco_last_device_status(zeco_stream_t stream);
+
+/*
  * Diagnostic of the bounded waits above (the ZeCO pages have no counterpart):
- * launches on `stream` one single-thread kernel whose mbarrier wait can never
- * complete.  The wait gives up after its time limit (2 s), the kernel records
- * it and returns; the next zeco_check_device_status() then reports
- * ZECO_ERR_TIMEOUT and the CUDA context stays usable.  Returns ZECO_ERR_CUDA
- * if the launch fails.
+ * launches on `stream` one CTA of four warps whose threads each wait 64 times
+ * on mbarriers that can never complete.  The first wait gives up after its
+ * time limit (2 s), the CTA's other waits then return at once, the kernel
+ * records the timeout and returns: it ends after about one time limit, the
+ * next zeco_check_device_status() reports ZECO_ERR_TIMEOUT and the CUDA
+ * context stays usable.  Returns ZECO_ERR_CUDA if the launch fails.
  */
 int zeco_selftest_bounded_wait(zeco_stream_t stream);
 
@@ -231,34 +257,44 @@ const char *zeco_strerror(int code);
 /*
  * Optional per-kernel timing (measurement aid; not part of the method).
  * After zeco_set_profile_events(events, n) with n > 0, every zeco_gla_fwd /
- * zeco_gla_bwd call made on this host thread records events[0] on its stream
- * before its first kernel and events[i] right after its i-th kernel, until n
- * events are used; n = 0 (or events = NULL) switches it off.  `events` are
+ * zeco_gla_bwd call made on this host thread records, for its i-th kernel
+ * counted from the set call, events[2i] right before the launch and
+ * events[2i + 1] right after it, both on the stream the kernel runs on (the
+ * caller's, or the auxiliary stream of zeco_set_overlap), until the n events
+ * are used; n = 0 (or events = NULL) switches it off.  So the elapsed time from
+ * events[2i] to events[2i + 1] is kernel i's duration, and intervals of kernels
+ * on the two streams can be compared on one timeline.  `events` are
  * cudaEvent_t handles created (and later destroyed) by the caller.  The calls
  * return ZECO_OK.  zeco_profile_event_count() gives the number of events
- * recorded so far and zeco_profile_kernel_name(i) the kernel that ended at
- * event i (NULL when i is out of range).
+ * recorded so far (two per kernel) and zeco_profile_kernel_name(i) the name of
+ * kernel i (NULL when i is out of range).
  */
 int zeco_set_profile_events(void *const *events, int n);
 int zeco_profile_event_count(void);
 const char *zeco_profile_kernel_name(int i);
 
 /*
- * Overlap of the scan-independent passes (on by default).  The pages' central
- * claim is that the exchange of segment states (the All-Scan) hides behind
- * work that does not need it (ZeCO, Pith review, "What carries the argument").
- * On the tensor-core path the passes that build the decay-weighted operands
- * and the intra-chunk scores (and, backward, their gradient) do not depend on
- * the segment scan; with overlap on they run on an auxiliary stream
- * concurrently with the segment-state pass and the scan (and, backward, the dv
- * sweep).  The call forks from and joins back into its `stream` with events, so
- * all its work stays ordered on `stream` and it can be captured into a CUDA
- * graph.  The auxiliary stream and three events are created on the first such
- * call of each host thread on each device and destroyed when the thread exits.
- * on = 0 runs everything on `stream`; active profiling events (above) do too.
- * Process-wide; returns ZECO_OK.
+ * Schedule of the work beside the segment scan.  The pages' central claim is
+ * that the exchange of segment states (the All-Scan) hides behind work that
+ * does not need it (ZeCO, Pith review, "What carries the argument"; Algorithm 1
+ * runs the All-Scan and the intra-chunk diagonal attention on two streams,
+ * Eq. 11).  On the tensor-core path the passes that build the intra-chunk
+ * scores A (forward) and their gradient dA (backward) do not depend on the
+ * segment scan.
+ *   mode 1 (default): A and dA run on an auxiliary stream as soon as their
+ *     inputs exist, concurrently with the segment-state pass and the scan (and,
+ *     backward, the dv sweep);
+ *   mode 2 (the pages' schedule): the segment scan (forward and reverse) runs
+ *     on the auxiliary stream, concurrently with the A (dA) pass on `stream`;
+ *   mode 0: everything on `stream`.
+ * The call forks from and joins back into its `stream` with events, so all its
+ * work stays ordered on `stream` and it can be captured into a CUDA graph.
+ * Results are identical in every mode.  The auxiliary stream and three events
+ * are created on the first such call of each host thread on each device and
+ * destroyed when the thread exits.  Process-wide; returns ZECO_OK, or
+ * ZECO_ERR_ARG for a mode outside 0..2.
  */
-int zeco_set_overlap(int on);
+int zeco_set_overlap(int mode);
 
 /* The path zeco_gla_fwd / zeco_gla_bwd would run for this shape
  * (ZECO_PATH_SIMT or ZECO_PATH_TC), or a negative ZECO_ERR_* code. */

@@ -1,6 +1,8 @@
 """Helpers for the GPU parity tests: run the library, run the oracle, compare."""
 from __future__ import annotations
 
+import ctypes
+
 import numpy as np
 import torch
 
@@ -76,3 +78,38 @@ def compare_full(z, x, P, K, C, dtype, path="auto", bwd=True, check_states=True)
         for n in ("dq", "dk", "dv", "dlog_alpha", "dS0"):
             errs[n] = err(to_np(res[n]), rg[n], dtype)
     return errs
+
+
+def kernel_names(z, run):
+    """Run ``run()`` with the library's per-kernel profiling marks on and return
+    (names of the kernels it launched, in launch order; run's result)."""
+    lib = z.load_library()
+    n = 64
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    for e in evs:
+        e.record()  # materialise the handles
+    torch.cuda.synchronize()
+    handles = (ctypes.c_void_p * n)(*[e.cuda_event for e in evs])
+    lib.zeco_set_profile_events.argtypes = [ctypes.c_void_p, ctypes.c_int]
+    lib.zeco_profile_kernel_name.restype = ctypes.c_char_p
+    lib.zeco_set_profile_events(ctypes.cast(handles, ctypes.c_void_p), n)
+    try:
+        out = run()
+        cnt = lib.zeco_profile_event_count()
+        names = [lib.zeco_profile_kernel_name(i).decode() for i in range(cnt // 2)]
+    finally:
+        lib.zeco_set_profile_events(None, 0)
+    torch.cuda.synchronize()
+    return names, out
+
+
+def chunk_rows(T, segments, C=64, first=2, last=2):
+    """Token indices of the first ``first`` and last ``last`` chunks of every one
+    of ``segments`` equal segments (where the carried states weigh most)."""
+    L = T // segments
+    idx = []
+    for p in range(segments):
+        a = p * L
+        idx.extend(range(a, a + first * C))
+        idx.extend(range(a + L - last * C, a + L))
+    return np.unique(np.asarray(idx))

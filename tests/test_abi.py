@@ -150,3 +150,16 @@ def test_segment_count_fills_the_gpu(lib):
     assert z.saved_bytes(s) == 4 * 17 * 256 * 512 * 4 + 4 * 16 * 256 * 4
     # too short to split (fewer than 4 chunks per sub-segment)
     assert z.segments(_shape(T=512, P=2, K=8)) == 2
+
+
+def test_noalloc_shape_errors_match_the_workspace_backward(lib):
+    # invalid and unsupported shapes return zeco_gla_bwd's codes before any CUDA call
+    import chunked_state_scan_gb300 as z
+    cases = [z.make_shape(1, 1, 100, 64, 64, 3, 1, 64, "f32"),      # T % P != 0
+             z.make_shape(1, 1, 1024, 64, 64, 4, 1, 256, "f32"),    # C outside the set
+             z.make_shape(1, 1, 1024, 64, 1024, 4, 1, 64, "f32"),   # d_v too wide
+             z.make_shape(0, 1, 1024, 64, 64, 4, 1, 64, "f32")]     # B = 0
+    for shape in cases:
+        rc_na = lib.zeco_gla_bwd_noalloc(ctypes.byref(shape), *([None] * 13))
+        rc_ws = lib.zeco_gla_bwd(ctypes.byref(shape), *([None] * 12), None, 0, None)
+        assert rc_na == rc_ws < 0, (rc_na, rc_ws)

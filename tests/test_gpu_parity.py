@@ -160,14 +160,16 @@ def test_bf16_odd_chunk_counts_in_the_dq_dk_sweeps(z, B, H, T, dk, P, K):
     _assert(errs, "bf16", f"tc odd chunks B{B} H{H} T{T} dk{dk} P{P}")
 
 
-def test_overlap_stream_gives_identical_results(z):
-    # the scan-independent passes on a second stream (default) or all on one
-    # stream: same kernels, same inputs, so bit-identical outputs
+@pytest.mark.parametrize("mode", [0, 2])
+def test_overlap_schedules_give_identical_results(z, mode):
+    # the scan-independent passes on a second stream (mode 1, the default), the
+    # scan on a second stream (mode 2) or all on one stream (mode 0): the same
+    # kernels on the same inputs, so bit-identical outputs
     w = workloads.LONG_FWDBWD.replace(T=16384, P=4)
     x = workloads.make_inputs(w)
     lib = z.load_library()
     a = parity.run_gpu(z, x, w.P, w.K, w.C)
-    lib.zeco_set_overlap(0)
+    assert lib.zeco_set_overlap(mode) == z.ZECO_OK
     try:
         b = parity.run_gpu(z, x, w.P, w.K, w.C)
     finally:
@@ -249,3 +251,77 @@ def test_low_parallelism_shape_is_split_and_unchanged(z):
                               s0_scale=0.2)
     errs = parity.compare_full(z, x, 1, 1, 64, "bf16")
     _assert(errs, "bf16", "P = 1 split")
+
+
+# ------------------------------------- edge cases on the tensor-core dq/dk kernel
+
+
+def _tc_edge_inputs(case, device="cpu"):
+    kw = dict(B=1, H=2, T=2048, dk=128, dv=512, dtype="bf16", seed=31, qk_scale=1 / 12,
+              s0_scale=0.3, device=device)
+    if case == "slow_decay":
+        kw.update(x_mean=8.0, s0_scale=0.5)   # log_alpha ~ -2e-5: the carry dominates
+    elif case == "fast_decay":
+        kw.update(x_mean=-18.0)               # log_alpha ~ -1.1: chunk sums near -72
+    elif case == "no_decay":
+        kw.update(g_zero=True)                # log_alpha = 0 exactly
+    return workloads.make_custom(**kw)
+
+
+@pytest.mark.parametrize("case", ["slow_decay", "fast_decay", "no_decay"])
+def test_bf16_tc_dq_dk_kernel_edge_cases(z, case):
+    """The decay regimes the method has, on the tensor-core dq/dk/dlog_alpha
+    kernel (d_v = 512): the carry-dominated slow decay, a fast decay whose chunk
+    log-decay sums reach about -72 (the chunk factorisation's range ends at -80),
+    and exactly no decay.  Besides every full tensor, the first and last two
+    chunks of every segment are checked on their own: there the states carried
+    across segments (forward) and back (adjoint) weigh most."""
+    B, H, T, dk, dv, P, K = 1, 2, 2048, 128, 512, 8, 2
+    shape = z.make_shape(B, H, T, dk, dv, P, K, 64, "bf16", "tc")
+    assert z.resolve_path(shape) == "tc"
+    x = _tc_edge_inputs(case)
+    csum = x["log_alpha"].float().view(B, H, T // 64, 64, dk).sum(3)
+    if case == "fast_decay":
+        assert -80.0 < float(csum.min()) and float(csum.max()) < -60.0
+    names, res = parity.kernel_names(z, lambda: parity.run_gpu(z, x, P, K, 64, path="tc"))
+    assert "tc_bwd_dq" in names and "tc_bwd_dk" in names, names
+    ro, rsf = oracle.gla_fwd(x["q"], x["k"], x["v"], x["log_alpha"], x["S0"])
+    rg = oracle.gla_bwd(x["q"], x["k"], x["v"], x["log_alpha"], x["S0"], x["do"],
+                        x["dS_final"])
+    errs = {"o": parity.rel_l2(parity.to_np(res["o"]), ro),
+            "S_final": parity.rel_l2(parity.to_np(res["S_final"]), rsf)}
+    for n in ("dq", "dk", "dv", "dlog_alpha", "dS0"):
+        errs[n] = parity.rel_l2(parity.to_np(res[n]), rg[n])
+    idx = parity.chunk_rows(T, z.segments(shape))
+    for n, r in (("o", ro), ("dq", rg["dq"]), ("dk", rg["dk"]), ("dv", rg["dv"]),
+                 ("dlog_alpha", rg["dlog_alpha"])):
+        errs[n + "[segment ends]"] = parity.rel_l2(parity.to_np(res[n])[:, :, idx],
+                                                   r[:, :, idx])
+    _assert(errs, "bf16", f"tc {case}")
+
+
+@pytest.mark.parametrize("x_mean", [0.0, 8.0])
+def test_bf16_tc_whole_16k_token_segments(z, x_mean):
+    """Segments of L = 16,384 tokens on the tensor-core path, as in the 1M-token
+    workload (38 sequences of one segment each fill one wave, so the library
+    does not split them): the dlog_alpha suffix sums run over all 16K tokens of a
+    segment.  The first and last sequences are checked in full."""
+    B, H, T, dk, dv = 38, 1, 16384, 128, 512
+    shape = z.make_shape(B, H, T, dk, dv, 1, 1, 64, "bf16", "tc")
+    assert z.resolve_path(shape) == "tc"
+    assert z.segments(shape) == 1
+    x = workloads.make_custom(B, H, T, dk, dv, dtype="bf16", seed=16, qk_scale=1 / 16,
+                              x_mean=x_mean, s0_scale=0.3, device="cuda")
+    names, res = parity.kernel_names(z, lambda: parity.run_gpu(z, x, 1, 1, 64, path="tc"))
+    assert "tc_bwd_dq" in names and "tc_bwd_dk" in names, names
+    errs = {}
+    for b in (0, B - 1):
+        xs = {n: t[b:b + 1].cpu() for n, t in x.items()}
+        ro, rsf = oracle.gla_fwd(xs["q"], xs["k"], xs["v"], xs["log_alpha"], xs["S0"])
+        rg = oracle.gla_bwd(xs["q"], xs["k"], xs["v"], xs["log_alpha"], xs["S0"], xs["do"],
+                            xs["dS_final"])
+        errs[f"o[{b}]"] = parity.rel_l2(parity.to_np(res["o"][b:b + 1]), ro)
+        errs[f"S_final[{b}]"] = parity.rel_l2(parity.to_np(res["S_final"][b:b + 1]), rsf)
+        for n in ("dq", "dk", "dv", "dlog_alpha", "dS0"):
+            errs[f"{n}[{b}]"] = parity.rel_l2(parity.to_np(res[n][b:b + 1]), rg[n])
+    _assert(errs, "bf16", f"L=16384 x_mean={x_mean}")
