@@ -716,7 +716,12 @@ def scan_sweep(args, local):
 
         step()
         torch.cuda.synchronize(dev)
-        runs = [profile_step(lib, step, dev) for _ in range(3)]
+        lib.zeco_set_overlap.argtypes = [ctypes.c_int]
+        lib.zeco_set_overlap(0)  # every kernel alone: the scans' own times
+        try:
+            runs = [profile_step(lib, step, dev) for _ in range(3)]
+        finally:
+            lib.zeco_set_overlap(1)
         kb = kernel_bytes_per_token(w.dk, w.dv, w.L)
         res = {"P": P, "L": w.L}
         for name in ("seg_scan_fwd", "seg_scan_rev"):
