@@ -2,8 +2,11 @@
 //
 // dq and dk contract over all d_v columns of the state.  A cluster of four CTAs
 // owns a block of 128 d_k rows i of one (b, h, segment); CTA r of the cluster
-// holds the d_v columns [128 r, 128 r + 128).  Two launches sweep the segment's
-// chunks:
+// holds the d_v columns [128 r, 128 r + 128).  For d_v < 512 (a multiple of 128)
+// the CTAs whose columns lie beyond d_v hold a zero state and receive zero v / do
+// tiles (the copies of boxes past the end of a tensor read zeros), so their
+// partial sums are zero and the results are those of the d_v columns that exist.
+// Two launches sweep the segment's chunks:
 //
 //   forward sweep, state S (from S_in[p], the global state held since the
 //   forward pass: Pith review of ZeCO, assumptions: Appendix A.4):
@@ -90,7 +93,7 @@ using namespace tc;
 
 constexpr int kC = 64;       // tokens per chunk
 constexpr int kKB = 128;     // d_k rows per cluster
-constexpr int kDV = 512;     // d_v
+constexpr int kDVMax = 512;  // d_v covered by the four CTAs of a cluster
 constexpr int kNB = 128;     // d_v columns per CTA
 constexpr int kRanks = 4;    // CTAs per cluster
 constexpr int kOwn = 32;     // rows finished per CTA
@@ -140,7 +143,7 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
                  const __grid_constant__ CUtensorMap tmQD, const __grid_constant__ CUtensorMap tmOut,
                  const __grid_constant__ CUtensorMap tmAux, const float* __restrict__ Eb,
                  const float* __restrict__ S_src, const float* __restrict__ carry, int64_t T,
-                 int dk, int P, int64_t L) {
+                 int dk, int dv, int P, int64_t L) {
   extern __shared__ __align__(1024) unsigned char smraw[];
   unsigned char* sm = align1024(smraw);
   float* sRcv = reinterpret_cast<float*>(sm + kOffRcv);
@@ -289,15 +292,18 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
     const uint32_t lane_off = (uint32_t)(lg * 32) << 16;
     const uint32_t sS = tmem + lane_off + kColS + 64 * h;
     {
+      // (a CTA past d_v starts from a zero state: d_v and j0 are multiples of 128)
+      const bool live = j0 < dv;
       const float* Sp = S_src +
-                        (((size_t)bh * (P + 1) + p + (REV ? 1 : 0)) * dk + i0 + row) * kDV + j0 +
-                        64 * h;
+                        (((size_t)bh * (P + 1) + p + (REV ? 1 : 0)) * dk + i0 + row) * dv +
+                        (live ? j0 + 64 * h : 0);
 #pragma unroll 1
       for (int c = 0; c < 2; ++c) {
         float r[32];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-          const float4 x4 = reinterpret_cast<const float4*>(Sp + 32 * c)[u];
+          const float4 x4 = live ? reinterpret_cast<const float4*>(Sp + 32 * c)[u]
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
           r[4 * u] = x4.x;
           r[4 * u + 1] = x4.y;
           r[4 * u + 2] = x4.z;
@@ -590,13 +596,14 @@ cudaError_t launch_qk(const Dims& d, const CUtensorMap& tx, const CUtensorMap& t
   cfg.numAttrs = 1;
   prof_start(st);
   return cudaLaunchKernelEx(&cfg, kern, tx, tu, tz, tp, ty, tg, tqd, tout, taux, Eb, S_src,
-                            carry, d.T, (int)d.dk, d.P, d.L);
+                            carry, d.T, (int)d.dk, (int)d.dv, d.P, d.L);
 }
 
 }  // namespace
 
 bool tc_bwd_qk_supported(const Dims& d) {
-  return d.bf16 && d.dk % kKB == 0 && d.dv == kDV && d.C == kC && d.L % kC == 0;
+  return d.bf16 && d.dk % kKB == 0 && d.dv % kNB == 0 && d.dv <= kDVMax && d.C == kC &&
+         d.L % kC == 0;
 }
 
 cudaError_t tc_bwd_qk(const Dims& d, const void* Qt, const void* Kt, const void* v,

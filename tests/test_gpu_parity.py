@@ -132,14 +132,20 @@ def test_bf16_slow_decay_carry_dominated(z, path):
 @pytest.mark.parametrize("B,H,T,dk,dv,P,K", [(2, 1, 1024, 128, 128, 16, 2),
                                              (1, 2, 512, 256, 256, 8, 4),
                                              (1, 1, 4096, 128, 384, 2, 1),
-                                             (1, 1, 256, 256, 512, 4, 8)])
+                                             (1, 1, 256, 256, 512, 4, 8),
+                                             (1, 2, 2048, 256, 128, 4, 2),
+                                             (1, 1, 2048, 256, 384, 2, 4)])
 def test_bf16_tensor_core_path_shapes(z, B, H, T, dk, dv, P, K):
     """The tcgen05 path on several tilings: one token block per segment (L = 64),
-    d_v tiles of 128 and 256, one and several d_k tiles, several batches."""
+    d_v tiles of 128 and 256, one and several d_k tiles, several batches.  Every
+    d_v (128, 256, 384, 512) runs dq, dk and dlog_alpha on the tensor-core kernel."""
     shape = z.make_shape(B, H, T, dk, dv, P, K, 64, "bf16", "tc")
     assert z.resolve_path(shape) == "tc"
     x = workloads.make_custom(B, H, T, dk, dv, dtype="bf16", seed=T + dk + dv,
                               qk_scale=1 / 16, s0_scale=0.2)
+    names, _ = parity.kernel_names(z, lambda: parity.run_gpu(z, x, P, K, 64, path="tc"))
+    assert "tc_bwd_dq" in names and "tc_bwd_dk" in names, names
+    assert not any(n.startswith("simt") for n in names), names
     errs = parity.compare_full(z, x, P, K, 64, "bf16", path="tc")
     _assert(errs, "bf16", f"tc B{B} H{H} T{T} dk{dk} dv{dv} P{P}")
 
