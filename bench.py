@@ -134,17 +134,18 @@ def canonical_kernel(name):
     return name
 
 
-def measured_traffic(path, kernel, token_heads):
+def measured_traffic(path, kernel, impl_bytes):
     """DRAM bytes of one launch of `kernel` from the committed ncu capture
-    (profiles/traffic.json, per token-head, scaled to this launch), or None when
-    there is no capture or the kernel's sources changed since it was taken."""
+    (profiles/traffic.json): the launch's implementation bytes `impl_bytes` times
+    the captured ratio of DRAM traffic to implementation bytes; None when there is
+    no capture or the kernel's sources changed since it was taken."""
     import hashlib
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             ent = json.load(f).get(f"{path}:{kernel}")
     except (OSError, ValueError):
         return None
-    if not ent:
+    if not ent or not ent.get("impl_bytes_per_token_head"):
         return None
     for rel, digest in ent.get("sources", {}).items():
         try:
@@ -153,7 +154,7 @@ def measured_traffic(path, kernel, token_heads):
                     return None
         except OSError:
             return None
-    return ent["bytes_per_token_head"] * token_heads
+    return impl_bytes * ent["bytes_per_token_head"] / ent["impl_bytes_per_token_head"]
 
 
 def load_peaks():
@@ -533,7 +534,7 @@ def measure(w, args, world, rank, local, want_e2e=True, want_cpu=True, quiet=Fal
     op_flops = zeco_operator_flops_per_token(w.dk, w.dv, w.C, bwd=w.bwd) * w.T * bh
     t_roof = max(op_bytes / (hbm_peak * 1e9), op_flops / (float(peaks["bf16_tflops"]) * 1e12))
     step_s = ms_step * 1e-3
-    traffic = measured_traffic(path, dom, w.T * bh)
+    traffic = measured_traffic(path, dom, dom_impl_bytes)
     # every kernel's bytes over its event-timed duration (GB/s), both accountings
     kern_gbs = {k: {"method": mb[canonical_kernel(k)] * w.T * bh / (ms * 1e-3) / 1e9,
                     "impl": kb[canonical_kernel(k)] * w.T * bh / (ms * 1e-3) / 1e9}
@@ -559,7 +560,9 @@ def measure(w, args, world, rank, local, want_e2e=True, want_cpu=True, quiet=Fal
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": dom_gbs, "peak": hbm_peak,
                      "unit": "GB/s", "frac": dom_gbs / hbm_peak, "traffic": traffic,
-                     "traffic_unit": "DRAM bytes per launch (ncu capture, scaled by tokens)",
+                     "traffic_unit": "DRAM bytes per launch (ncu capture of the small case: its "
+                                     "traffic / implementation-bytes ratio times this launch's "
+                                     "implementation bytes)",
                      "peak_source": f"{peak_kind} hbm_gbs",
                      "algorithmic_bytes_per_launch": dom_bytes,
                      "algorithmic_bytes": "the method's inputs and outputs of this step "
