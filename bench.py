@@ -502,7 +502,7 @@ def measure(w, args, world, rank, local, want_e2e=True, want_cpu=True, quiet=Fal
     if path == "tc":
         modes = {}
         try:
-            for mode in (0, 2, 1):
+            for mode in (0, 2, 3, 1):
                 lib.zeco_set_overlap(mode)
                 step()
                 torch.cuda.synchronize(dev)
@@ -511,13 +511,17 @@ def measure(w, args, world, rank, local, want_e2e=True, want_cpu=True, quiet=Fal
             lib.zeco_set_overlap(1)
         overlap = {
             "step_ms": {"mode1_aux_scores": ms_step, "mode2_aux_scan": modes[2][0],
+                        "mode3_pass2_per_segment_block": modes[3][0],
                         "mode0_one_stream": modes[0][0]},
             "scan_not_overlapped": {"mode1_aux_scores": scan_overlap(modes[1][1]),
-                                    "mode2_aux_scan": scan_overlap(modes[2][1])},
+                                    "mode2_aux_scan": scan_overlap(modes[2][1]),
+                                    "mode3_pass2_per_segment_block": scan_overlap(modes[3][1])},
             "note": "mode 1 (default): scores A / dA on a second stream beside pass 1, the "
                     "scans (and the dv sweep); mode 2: the segment scans on a second stream "
-                    "beside the A / dA pass; non_overlapped_frac = share of the scan's "
-                    "kernel time with no A / dA kernel running (Eq. 11 instrument)"}
+                    "beside the A / dA pass; mode 3: the forward scan in blocks of segments, "
+                    "pass 2 of each block on the second stream as soon as its block is "
+                    "scanned; non_overlapped_frac = share of the scan's kernel time with no "
+                    "A / dA kernel running (Eq. 11 instrument)"}
 
     # ---- roofline of the dominant kernel and of the whole step
     peaks, peak_kind = load_peaks()

@@ -11,15 +11,20 @@ namespace zeco {
 struct Fork {
   cudaStream_t aux;   // where the forked kernels go (the caller's stream when off)
   cudaEvent_t ev[2];  // recorded on aux by fork_mark, waited on by fork_join
+  cudaEvent_t* step;  // recorded on the caller's stream by fork_follow
   bool on;
 };
 // Forks from st (aux waits for st's work so far); off when overlap is disabled.
 Fork fork_begin(cudaStream_t st);
 // The schedule chosen with zeco_set_overlap: 0 one stream, 1 the scan-independent
-// passes on the auxiliary stream, 2 the segment scan on the auxiliary stream.
+// passes on the auxiliary stream, 2 the segment scan on the auxiliary stream, 3 pass 2
+// per block of segments as soon as the scan has reached it.
 int overlap_mode();
 cudaError_t fork_mark(const Fork& f, int i);
 cudaError_t fork_join(const Fork& f, cudaStream_t st, int i);
+// Makes the auxiliary stream wait for st's work so far (event i of kStepEvents).
+constexpr int kStepEvents = 8;
+cudaError_t fork_follow(const Fork& f, cudaStream_t st, int i);
 
 // ---- bounded-wait flags of the tensor-core kernels: read and clear; -1 when
 //      the flag cannot be read
@@ -36,8 +41,10 @@ cudaError_t launch_expand_log_alpha(const Dims& d, const void* g, void* gx, cuda
 cudaError_t launch_reduce_dlog_alpha(const Dims& d, const void* dgx, void* dg, cudaStream_t st);
 
 // ---- segment scans (scan.cu) ------------------------------------------
+// segments [p_begin, p_end) (p_end < 0: to the last); S_final when p_end is the last
 cudaError_t launch_seg_scan_fwd(const Dims& d, float* S_in, const float* gamma, const float* S0,
-                                float* S_final, cudaStream_t st);
+                                float* S_final, cudaStream_t st, int p_begin = 0,
+                                int p_end = -1);
 cudaError_t launch_seg_scan_rev(const Dims& d, float* D, const float* S_in, const float* gamma,
                                 const float* dS_final, float* dS0, float* carry,
                                 cudaStream_t st);
@@ -78,9 +85,10 @@ bool tc_fwd_supported(const Dims& d);
 // Q~ = bf16(q e^{b}), K~ = bf16(k e^{-b}) and e^{b_last} per chunk (tc_decay.cu)
 cudaError_t tc_decay(const Dims& d, const void* q, const void* k, const void* g, void* Qt,
                      void* Kt, float* Eb, cudaStream_t st);
+// segments [p_begin, p_begin + p_count) (p_count < 0: all)
 cudaError_t tc_fwd_out(const Dims& d, const void* Qt, const void* Kt, const void* v,
                        const void* A, const float* Eb, const float* S_in, void* o,
-                       cudaStream_t st);
+                       cudaStream_t st, int p_begin = 0, int p_count = -1);
 cudaError_t tc_bwd_dv(const Dims& d, const void* Qt, const void* Kt, const void* d_o,
                       const void* A, const float* Eb, const float* D, void* dv,
                       cudaStream_t st);

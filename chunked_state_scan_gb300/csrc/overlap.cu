@@ -12,7 +12,10 @@
 //     and the dv sweep;
 //   2 (the pages' schedule): the segment scan itself goes to the auxiliary
 //     stream, concurrently with the diagonal-attention pass (A, or dA) on the
-//     caller's stream.
+//     caller's stream;
+//   3 (forward): pass 2 of each block of segments starts as soon as the scan has
+//     produced that block's incoming states (the scan runs block by block on the
+//     caller's stream, pass 2 of each block on the auxiliary stream).
 // The caller's stream forks to the auxiliary stream with an event and joins it
 // with another before the first kernel that needs the forked work, so the call
 // stays ordered on the caller's stream (and capturable into a CUDA graph).
@@ -29,7 +32,7 @@ namespace zeco {
 namespace {
 
 constexpr int kMaxDevices = 128;
-constexpr int kEvents = 3;
+constexpr int kEvents = 3 + kStepEvents;
 
 struct AuxState {
   cudaStream_t stream = nullptr;
@@ -73,6 +76,7 @@ int overlap_mode() { return g_overlap.load(std::memory_order_relaxed); }
 Fork fork_begin(cudaStream_t st) {
   Fork f;
   f.aux = st;
+  f.step = nullptr;
   f.on = false;
   if (!g_overlap.load(std::memory_order_relaxed)) return f;
   AuxState* a = aux_for_current_device();
@@ -82,6 +86,7 @@ Fork fork_begin(cudaStream_t st) {
   f.aux = a->stream;
   f.ev[0] = a->ev[1];
   f.ev[1] = a->ev[2];
+  f.step = a->ev + 3;
   f.on = true;
   return f;
 }
@@ -94,10 +99,16 @@ cudaError_t fork_join(const Fork& f, cudaStream_t st, int i) {
   return f.on ? cudaStreamWaitEvent(st, f.ev[i], 0) : cudaSuccess;
 }
 
+cudaError_t fork_follow(const Fork& f, cudaStream_t st, int i) {
+  if (!f.on) return cudaSuccess;
+  cudaError_t e = cudaEventRecord(f.step[i], st);
+  return e == cudaSuccess ? cudaStreamWaitEvent(f.aux, f.step[i], 0) : e;
+}
+
 }  // namespace zeco
 
 extern "C" int zeco_set_overlap(int mode) {
-  if (mode < 0 || mode > 2) return ZECO_ERR_ARG;
+  if (mode < 0 || mode > 3) return ZECO_ERR_ARG;
   zeco::g_overlap.store(mode, std::memory_order_relaxed);
   return ZECO_OK;
 }

@@ -41,7 +41,7 @@ __device__ __forceinline__ float4 fma4(float a, float4 x, float4 y) {
 __global__ void __launch_bounds__(kWarps * 32)
 seg_scan_fwd_kernel(float* __restrict__ S_in, const float* __restrict__ gamma,
                     const float* __restrict__ S0, float* __restrict__ S_final, int P, int dk,
-                    int dv, int rows_per_kblock) {
+                    int dv, int rows_per_kblock, int p_begin, int p_end) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int local_row = blockIdx.x * kWarps + warp;
   if (local_row >= rows_per_kblock) return;
@@ -52,36 +52,42 @@ seg_scan_fwd_kernel(float* __restrict__ S_in, const float* __restrict__ gamma,
   float4* base = reinterpret_cast<float4*>(S_in + (size_t)bh * (P + 1) * slot + (size_t)i * dv);
   const float* gam = gamma + (size_t)bh * P * dk + i;
 
+  // segments [p_begin, p_end): the state entering p_begin is S0 (p_begin = 0) or the
+  // one an earlier launch left in slot p_begin
   float4 s[kMaxU];
 #pragma unroll
   for (int u = 0; u < kMaxU; ++u) {
     const int j4 = lane + 32 * u;
     s[u] = make_float4(0.f, 0.f, 0.f, 0.f);
     if (j4 < nv4) {
-      s[u] = S0 ? reinterpret_cast<const float4*>(S0 + ((size_t)bh * dk + i) * dv)[j4]
-                : make_float4(0.f, 0.f, 0.f, 0.f);
-      base[j4] = s[u];
+      if (p_begin == 0) {
+        s[u] = S0 ? reinterpret_cast<const float4*>(S0 + ((size_t)bh * dk + i) * dv)[j4]
+                  : make_float4(0.f, 0.f, 0.f, 0.f);
+        base[j4] = s[u];
+      } else {
+        s[u] = base[(size_t)p_begin * (slot >> 2) + j4];
+      }
     }
   }
-  for (int p0 = 0; p0 < P; p0 += kBatch) {
+  for (int p0 = p_begin; p0 < p_end; p0 += kBatch) {
     // the loads of kBatch steps go out together; only the FMA chain is serial
     float4 x[kBatch][kMaxU];
     float gm[kBatch];
 #pragma unroll
     for (int b = 0; b < kBatch; ++b) {
       const int p = p0 + b;
-      gm[b] = p < P ? gam[(size_t)p * dk] : 0.f;
+      gm[b] = p < p_end ? gam[(size_t)p * dk] : 0.f;
 #pragma unroll
       for (int u = 0; u < kMaxU; ++u) {
         const int j4 = lane + 32 * u;
-        x[b][u] = (p < P && j4 < nv4) ? base[(size_t)(p + 1) * (slot >> 2) + j4]
-                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+        x[b][u] = (p < p_end && j4 < nv4) ? base[(size_t)(p + 1) * (slot >> 2) + j4]
+                                          : make_float4(0.f, 0.f, 0.f, 0.f);
       }
     }
 #pragma unroll
     for (int b = 0; b < kBatch; ++b) {
       const int p = p0 + b;
-      if (p >= P) break;
+      if (p >= p_end) break;
       float4* dst = base + (size_t)(p + 1) * (slot >> 2);
 #pragma unroll
       for (int u = 0; u < kMaxU; ++u) {
@@ -93,7 +99,7 @@ seg_scan_fwd_kernel(float* __restrict__ S_in, const float* __restrict__ gamma,
       }
     }
   }
-  if (S_final) {
+  if (S_final && p_end == P) {
     float4* sf = reinterpret_cast<float4*>(S_final + ((size_t)bh * dk + i) * dv);
 #pragma unroll
     for (int u = 0; u < kMaxU; ++u) {
@@ -184,12 +190,13 @@ seg_scan_rev_kernel(float* __restrict__ D, const float* __restrict__ S_in,
 }  // namespace
 
 cudaError_t launch_seg_scan_fwd(const Dims& d, float* S_in, const float* gamma, const float* S0,
-                                float* S_final, cudaStream_t st) {
+                                float* S_final, cudaStream_t st, int p_begin, int p_end) {
   const int rows = (int)(d.dk / d.K);
+  if (p_end < 0) p_end = d.P;
   dim3 grid((rows + kWarps - 1) / kWarps, d.K, (unsigned)(d.B * d.H));
   prof_start(st);
   seg_scan_fwd_kernel<<<grid, kWarps * 32, 0, st>>>(S_in, gamma, S0, S_final, d.P, (int)d.dk,
-                                                    (int)d.dv, rows);
+                                                    (int)d.dv, rows, p_begin, p_end);
   prof_mark("seg_scan_fwd", st);
   return cudaGetLastError();
 }

@@ -34,6 +34,25 @@ cudaError_t tc_forward(const Dims& d, const void* q, const void* k, const void* 
   void* A = ops.A;
   cudaError_t e = tc_decay(d, q, k, g, Qt, Kt, Eb, st);
   if (e != cudaSuccess) return e;
+  if (overlap_mode() == 3) {
+    // pass 2 of a block of segments starts as soon as the scan has given that block
+    // its incoming states: the scan runs block by block on the caller's stream, and
+    // pass 2 of each block on the auxiliary stream after the scores and after the
+    // scan of its block
+    const Fork f = fork_begin(st);
+    e = tc_A(d, Qt, Kt, A, f.aux);
+    if (e == cudaSuccess) e = tc_chunk_state(d, k, v, g, Kt, Eb, S_in, gamma, st);
+    const int nb = d.P < kStepEvents ? d.P : kStepEvents;
+    for (int b = 0; e == cudaSuccess && b < nb; ++b) {
+      const int p0 = (int)((int64_t)d.P * b / nb), p1 = (int)((int64_t)d.P * (b + 1) / nb);
+      e = launch_seg_scan_fwd(d, S_in, gamma, S0, S_final, st, p0, p1);
+      if (e == cudaSuccess) e = fork_follow(f, st, b);
+      if (e == cudaSuccess) e = tc_fwd_out(d, Qt, Kt, v, A, Eb, S_in, o, f.aux, p0, p1 - p0);
+    }
+    if (e == cudaSuccess) e = fork_mark(f, 0);
+    if (e == cudaSuccess) e = fork_join(f, st, 0);
+    return e;
+  }
   if (overlap_mode() == 2) {
     // the pages' schedule: the scan on the second stream beside the scores
     e = tc_chunk_state(d, k, v, g, Kt, Eb, S_in, gamma, st);

@@ -83,7 +83,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 tc_sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmP,
                 const float* __restrict__ Eb, const float* __restrict__ S_src,
-                __nv_bfloat16* __restrict__ o, int64_t T, int dv, int P, int64_t L) {
+                __nv_bfloat16* __restrict__ o, int64_t T, int dv, int P, int64_t L,
+                int p_begin, int p_count) {
   using SM = FwdSmem<DK>;
   extern __shared__ __align__(1024) unsigned char smraw[];
   unsigned char* sm = align1024(smraw);
@@ -102,8 +103,9 @@ tc_sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   const int lg = warp & 3;       // TMEM lane group of this warp
   const int cq = warp >> 2;      // which quarter of the d_k columns this warp's state pass handles
   const int half = (warp >> 2) & 1;  // epilogue: which half of the 64 tokens (warps 0..7)
-  const int64_t bh = blockIdx.y / P;
-  const int p = blockIdx.y % P;
+  // segments [p_begin, p_begin + p_count) of every (b, h)
+  const int64_t bh = blockIdx.y / p_count;
+  const int p = p_begin + (int)(blockIdx.y % p_count);
   const int j0 = blockIdx.x * kNV;
   const int64_t row0 = bh * T + (int64_t)p * L;
   const int nc = (int)(L / kC);
@@ -379,7 +381,7 @@ tc_sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 template <int DK, bool BWD>
 cudaError_t launch_sweep(const Dims& d, const void* Qt, const void* Kt, const void* v,
                          const void* A, const float* Eb, const float* S_src, void* o,
-                         cudaStream_t st) {
+                         cudaStream_t st, int p_begin, int p_count) {
   CUtensorMap tq, tk, tv, tp;
   const uint64_t rows = (uint64_t)(d.B * d.H * d.T);
   if (!make_tmap_bf16(&tq, Qt, rows, DK, kC) || !make_tmap_bf16(&tk, Kt, rows, DK, kC) ||
@@ -389,10 +391,10 @@ cudaError_t launch_sweep(const Dims& d, const void* Qt, const void* Kt, const vo
   auto kern = tc_sweep_kernel<DK, BWD>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)(d.dv / kNV), (unsigned)(d.B * d.H * d.P));
+  dim3 grid((unsigned)(d.dv / kNV), (unsigned)(d.B * d.H * p_count));
   prof_start(st);
   kern<<<grid, kThreads, smem, st>>>(tq, tk, tv, tp, Eb, S_src, (__nv_bfloat16*)o, d.T,
-                                     (int)d.dv, d.P, d.L);
+                                     (int)d.dv, d.P, d.L, p_begin, p_count);
   return cudaGetLastError();
 }
 
@@ -405,9 +407,11 @@ bool tc_fwd_supported(const Dims& d) {
 
 cudaError_t tc_fwd_out(const Dims& d, const void* Qt, const void* Kt, const void* v,
                        const void* A, const float* Eb, const float* S_in, void* o,
-                       cudaStream_t st) {
-  cudaError_t e = d.dk == 256 ? launch_sweep<256, false>(d, Qt, Kt, v, A, Eb, S_in, o, st)
-                              : launch_sweep<128, false>(d, Qt, Kt, v, A, Eb, S_in, o, st);
+                       cudaStream_t st, int p_begin, int p_count) {
+  if (p_count < 0) p_count = d.P - p_begin;
+  cudaError_t e =
+      d.dk == 256 ? launch_sweep<256, false>(d, Qt, Kt, v, A, Eb, S_in, o, st, p_begin, p_count)
+                  : launch_sweep<128, false>(d, Qt, Kt, v, A, Eb, S_in, o, st, p_begin, p_count);
   prof_mark("tc_fwd_out", st);
   return e;
 }
@@ -415,8 +419,8 @@ cudaError_t tc_fwd_out(const Dims& d, const void* Qt, const void* Kt, const void
 cudaError_t tc_bwd_dv(const Dims& d, const void* Qt, const void* Kt, const void* d_o,
                       const void* A, const float* Eb, const float* D, void* dv,
                       cudaStream_t st) {
-  cudaError_t e = d.dk == 256 ? launch_sweep<256, true>(d, Qt, Kt, d_o, A, Eb, D, dv, st)
-                              : launch_sweep<128, true>(d, Qt, Kt, d_o, A, Eb, D, dv, st);
+  cudaError_t e = d.dk == 256 ? launch_sweep<256, true>(d, Qt, Kt, d_o, A, Eb, D, dv, st, 0, d.P)
+                              : launch_sweep<128, true>(d, Qt, Kt, d_o, A, Eb, D, dv, st, 0, d.P);
   prof_mark("tc_bwd_dv", st);
   return e;
 }

@@ -286,13 +286,17 @@ const char *zeco_profile_kernel_name(int i);
  *     backward, the dv sweep);
  *   mode 2 (the pages' schedule): the segment scan (forward and reverse) runs
  *     on the auxiliary stream, concurrently with the A (dA) pass on `stream`;
+ *   mode 3 (forward; the backward as mode 1): pass 2 of each of up to 8 blocks of
+ *     segments starts as soon as the scan has produced that block's incoming
+ *     states -- the scan runs block by block on `stream`, pass 2 of each block
+ *     on the auxiliary stream after the A pass and after its block's scan;
  *   mode 0: everything on `stream`.
  * The call forks from and joins back into its `stream` with events, so all its
  * work stays ordered on `stream` and it can be captured into a CUDA graph.
- * Results are identical in every mode.  The auxiliary stream and three events
+ * Results are identical in every mode.  The auxiliary stream and eleven events
  * are created on the first such call of each host thread on each device and
  * destroyed when the thread exits.  Process-wide; returns ZECO_OK, or
- * ZECO_ERR_ARG for a mode outside 0..2.
+ * ZECO_ERR_ARG for a mode outside 0..3.
  */
 int zeco_set_overlap(int mode);
 
