@@ -743,6 +743,69 @@ def scan_sweep(args, local):
             "workload": base.name + " inputs, P varied"}
 
 
+def decay_forms(args, local):
+    """The headline workload's fwd+bwd step in each decay form (``--forms``): per-token
+    scalar and no decay beside the diagonal form, each with its step time (L2 flushed
+    before every step when the inputs are small; here they are not) and the per-kernel
+    times with every kernel on one stream."""
+    import chunked_state_scan_gb300 as z
+    lib = z.load_library()
+    dev = torch.device("cuda", local)
+    w = workloads.LONG_FWDBWD
+    x = workloads.make_inputs(w, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    out = []
+    for form in ("diag", "scalar", "none"):
+        g = {"diag": x["log_alpha"], "scalar": x["log_alpha"][..., 0].contiguous(),
+             "none": None}[form]
+        shape = z.make_shape(w.B, w.H, w.T, w.dk, w.dv, w.P, w.K, w.C, w.dtype, "auto", form)
+        saved = torch.empty(z.saved_bytes(shape), dtype=torch.uint8, device=dev)
+        ws = torch.empty(max(z.workspace_bytes(shape, True), 16), dtype=torch.uint8,
+                         device=dev)
+        ws_f = torch.empty(max(z.workspace_bytes(shape, False), 16), dtype=torch.uint8,
+                           device=dev)
+        o = torch.empty_like(x["v"])
+        S_final = torch.empty_like(x["S0"])
+        grads = dict(dq=torch.empty_like(x["q"]), dk=torch.empty_like(x["k"]),
+                     dv=torch.empty_like(x["v"]),
+                     dlog_alpha=torch.empty_like(g) if g is not None else None,
+                     dS0=torch.empty_like(x["S0"]))
+
+        def step():
+            z.zeco_gla_fwd(x["q"], x["k"], x["v"], g, x["S0"], P=w.P, K=w.K, C=w.C, o=o,
+                           S_final=S_final, saved=saved, workspace=ws_f, stream=stream,
+                           decay=form)
+            z.zeco_gla_bwd(x["q"], x["k"], x["v"], g, saved, x["do"], x["dS_final"], P=w.P,
+                           K=w.K, C=w.C, grads=grads, workspace=ws, stream=stream, decay=form)
+
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = e0.elapsed_time(e1) / args.steps
+        lib.zeco_set_overlap.argtypes = [ctypes.c_int]
+        lib.zeco_set_overlap(0)
+        try:
+            runs = [profile_step(lib, step, dev) for _ in range(3)]
+        finally:
+            lib.zeco_set_overlap(1)
+        kms = {}
+        for r in runs:
+            for n, a, b in r:
+                kms[n] = kms.get(n, 0.0) + (b - a) / len(runs)
+        out.append({"decay": form, "ms_per_step": ms, "tokens_per_s": w.tokens / (ms * 1e-3),
+                    "workspace_bytes_bwd": z.workspace_bytes(shape, True),
+                    "kernels_ms": kms})
+        del saved, ws, ws_f, grads, o, S_final
+        torch.cuda.empty_cache()
+    return {"decay_forms": out, "workload": w.name, "steps": args.steps, "warmup": args.warmup}
+
+
 # ---------------------------------------------------------------- main
 
 
@@ -767,6 +830,8 @@ def main(argv=None):
                          "8-segment fwd, batched fwd+bwd) instead of the headline")
     ap.add_argument("--scan-sweep", action="store_true",
                     help="time the segment scans at P in {64, 1024, 4096, T/(2C)}")
+    ap.add_argument("--forms", action="store_true",
+                    help="time the headline step in the diagonal, scalar and no-decay forms")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl != "reference":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
@@ -777,8 +842,8 @@ def main(argv=None):
 
     import chunked_state_scan_gb300 as z
     z.load_library()
-    if args.scan_sweep:
-        res = scan_sweep(args, local)
+    if args.scan_sweep or args.forms:
+        res = scan_sweep(args, local) if args.scan_sweep else decay_forms(args, local)
         if rank == 0:
             print(json.dumps(res), flush=True)
         return 0

@@ -77,12 +77,14 @@ int resolve(const zeco_shape* s, const Dims& d) {
 
 // Scratch layout of one call: the backward's own buffers (bwd only), then, for
 // the backward on the tensor-core path, the score gradient dA, then, for the
-// SCALAR / NONE decay forms, the broadcast log-decay and its per-row gradient
-// (forms_layout).  The operands the forward computes once (decay_layout) live
-// in `saved`, not here.
+// SCALAR / NONE decay forms, the broadcast log-decay and its per-row gradient,
+// or, where the kernels read the form in its own layout, the SCALAR gradient's
+// partial sums (forms_layout).  The operands the forward computes once
+// (decay_layout) live in `saved`, not here.
 struct WsPlan {
   zeco::BwdWsLayout bwd;
   size_t dA_off;  // backward on the tensor-core path: the score gradient dA
+  bool native;    // the decay form is read in its own layout (tc_native_forms)
   zeco::FormsLayout forms;
   size_t total;
 };
@@ -94,7 +96,8 @@ WsPlan plan_ws(const Dims& d, int path, bool bwd) {
   w.dA_off = zeco::align_up(base, 256);
   if (bwd && path == ZECO_PATH_TC && zeco::tc_uses_dA(d))
     base = zeco::align_up(w.dA_off + zeco::scores_bytes(d), 256);
-  w.forms = zeco::forms_layout(d, base, bwd);
+  w.native = path == ZECO_PATH_TC && zeco::tc_native_forms(d, bwd);
+  w.forms = zeco::forms_layout(d, base, bwd, w.native);
   w.total = w.forms.total;
   return w;
 }
@@ -204,7 +207,7 @@ int zeco_gla_fwd(const zeco_shape* shape, const void* q, const void* k, const vo
   cudaStream_t st = (cudaStream_t)stream;
   cudaError_t e = cudaSuccess;
   const void* g = log_alpha;
-  if (d.decay != ZECO_DECAY_DIAG) {
+  if (d.decay != ZECO_DECAY_DIAG && !wp.native) {
     g = (char*)workspace + wp.forms.gx_off;
     e = zeco::launch_expand_log_alpha(d, log_alpha, (void*)g, st);
   }
@@ -245,9 +248,12 @@ int zeco_gla_bwd(const zeco_shape* shape, const void* q, const void* k, const vo
   cudaError_t e = cudaSuccess;
   const void* g = log_alpha;
   void* dg = dlog_alpha;
-  if (d.decay != ZECO_DECAY_DIAG) {
+  if (d.decay == ZECO_DECAY_SCALAR || (d.decay == ZECO_DECAY_NONE && !wp.native))
+    dg = (char*)workspace + wp.forms.dgx_off;  // NONE: a gradient nobody reads
+  else if (d.decay == ZECO_DECAY_NONE)
+    dg = nullptr;
+  if (d.decay != ZECO_DECAY_DIAG && !wp.native) {
     g = (char*)workspace + wp.forms.gx_off;
-    dg = (char*)workspace + wp.forms.dgx_off;
     e = zeco::launch_expand_log_alpha(d, log_alpha, (void*)g, st);
   }
   if (e == cudaSuccess)
@@ -257,7 +263,8 @@ int zeco_gla_bwd(const zeco_shape* shape, const void* q, const void* k, const vo
             : zeco::simt_backward(d, q, k, v, g, S_in, gamma, d_o, dS_final, dq, dk, dv, dg,
                                   dS0, D, carry, qdq, st);
   if (e == cudaSuccess && d.decay == ZECO_DECAY_SCALAR)
-    e = zeco::launch_reduce_dlog_alpha(d, dg, dlog_alpha, st);
+    e = wp.native ? zeco::launch_sum_dlog_alpha_parts(d, (const float*)dg, dlog_alpha, st)
+                  : zeco::launch_reduce_dlog_alpha(d, dg, dlog_alpha, st);
   return e == cudaSuccess ? ZECO_OK : ZECO_ERR_CUDA;
 }
 

@@ -77,10 +77,21 @@ inline BwdWsLayout bwd_ws_layout(const Dims& d) {
 struct FormsLayout {
   size_t gx_off, dgx_off, total;
 };
-inline FormsLayout forms_layout(const Dims& d, size_t base, bool bwd) {
+// native: the form is read in its own layout (tc_native_forms); then only the
+// SCALAR backward needs scratch, the fp32 partial sums [dk / 32][B,H,T] of its
+// gradient (at dgx_off).
+inline FormsLayout forms_layout(const Dims& d, size_t base, bool bwd, bool native) {
   FormsLayout l;
-  const size_t n = (size_t)d.B * d.H * d.T * d.dk * (d.bf16 ? 2 : 4);
+  const size_t rows = (size_t)d.B * d.H * d.T;
+  const size_t n = rows * d.dk * (d.bf16 ? 2 : 4);
   l.gx_off = align_up(base, 256);
+  if (native) {
+    l.dgx_off = l.gx_off;
+    l.total = (bwd && d.decay == ZECO_DECAY_SCALAR)
+                  ? align_up(l.dgx_off + rows * (size_t)(d.dk / 32) * 4, 256)
+                  : base;
+    return l;
+  }
   l.dgx_off = align_up(l.gx_off + n, 256);
   l.total = d.decay == ZECO_DECAY_DIAG ? base : (bwd ? align_up(l.dgx_off + n, 256) : l.dgx_off);
   return l;

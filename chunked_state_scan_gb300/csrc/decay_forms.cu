@@ -7,7 +7,10 @@
 // same log-decay in every d_k row, and no decay is log-decay 0, so both run the
 // diagonal kernels on a broadcast log-decay.  By the chain rule through the
 // broadcast, the gradient of a scalar log-decay is the sum over d_k of the
-// per-row gradient.
+// per-row gradient.  Where every kernel that reads the log-decay has the form
+// built in (the tensor-core path: the decay pass and the dq/dk sweeps), no
+// broadcast is made; the dq/dk reverse sweep leaves fp32 sums over blocks of 32
+// d_k rows, which the last kernel here adds up per token.
 #include "common.cuh"
 #include "launch.h"
 
@@ -41,7 +44,29 @@ __global__ void reduce_kernel(const T* __restrict__ dgx, T* __restrict__ dg, int
   if (lane == 0) st(dg + r, s);
 }
 
+// one thread per token: the sum of its nparts partials (partial c at c * rows)
+__global__ void sum_parts_kernel(const float* __restrict__ part, __nv_bfloat16* __restrict__ dg,
+                                 int64_t rows, int nparts) {
+  for (int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; r < rows;
+       r += (int64_t)gridDim.x * blockDim.x) {
+    float s = 0.f;
+    for (int c = 0; c < nparts; ++c) s += part[(size_t)c * rows + r];
+    dg[r] = __float2bfloat16_rn(s);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_sum_dlog_alpha_parts(const Dims& d, const float* part, void* dg,
+                                        cudaStream_t st) {
+  const int64_t rows = d.B * d.H * d.T;
+  const int64_t nb = (rows + 255) / 256;
+  const unsigned blocks = (unsigned)(nb < 65535 * 16 ? nb : 65535 * 16);
+  prof_start(st);
+  sum_parts_kernel<<<blocks, 256, 0, st>>>(part, (__nv_bfloat16*)dg, rows, (int)(d.dk / 32));
+  prof_mark("sum_dlog_alpha_parts", st);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_expand_log_alpha(const Dims& d, const void* g, void* gx, cudaStream_t st) {
   const int64_t rows = d.B * d.H * d.T;

@@ -39,6 +39,10 @@ int selftest_take_status();
 cudaError_t launch_expand_log_alpha(const Dims& d, const void* g, void* gx, cudaStream_t st);
 // dg[b,h,t] = sum_i dgx[b,h,t,i] (SCALAR)
 cudaError_t launch_reduce_dlog_alpha(const Dims& d, const void* dgx, void* dg, cudaStream_t st);
+// dg[b,h,t] = sum_c part[c][b,h,t], c < d_k / 32 (SCALAR on the tensor-core path:
+// part holds the dq/dk reverse sweep's fp32 sums over blocks of 32 rows)
+cudaError_t launch_sum_dlog_alpha_parts(const Dims& d, const float* part, void* dg,
+                                        cudaStream_t st);
 
 // ---- segment scans (scan.cu) ------------------------------------------
 // segments [p_begin, p_end) (p_end < 0: to the last); S_final when p_end is the last
@@ -82,7 +86,8 @@ cudaError_t tc_chunk_state(const Dims& d, const void* k, const void* v, const vo
 cudaError_t tc_dstate_local(const Dims& d, const void* q, const void* d_o, const void* g,
                             const void* Qt, const float* Eb, float* D, cudaStream_t st);
 bool tc_fwd_supported(const Dims& d);
-// Q~ = bf16(q e^{b}), K~ = bf16(k e^{-b}) and e^{b_last} per chunk (tc_decay.cu)
+// Q~ = bf16(q e^{b}), K~ = bf16(k e^{-b}) and e^{b_last} per chunk (tc_decay.cu);
+// g in the layout of d.decay: [B,H,T,dk] (DIAG), [B,H,T] (SCALAR), unread (NONE)
 cudaError_t tc_decay(const Dims& d, const void* q, const void* k, const void* g, void* Qt,
                      void* Kt, float* Eb, cudaStream_t st);
 // segments [p_begin, p_begin + p_count) (p_count < 0: all)
@@ -98,6 +103,8 @@ cudaError_t tc_A(const Dims& d, const void* Qt, const void* Kt, void* P, cudaStr
 bool tc_dA_supported(const Dims& d);
 cudaError_t tc_dA(const Dims& d, const void* d_o, const void* v, void* P, cudaStream_t st);
 bool tc_bwd_qk_supported(const Dims& d);
+// g and dg by d.decay: DIAG [B,H,T,dk] bf16 both; SCALAR g [B,H,T] bf16, dg the
+// fp32 partial sums [dk / 32][B,H,T]; NONE neither is used
 cudaError_t tc_bwd_qk(const Dims& d, const void* Qt, const void* Kt, const void* v,
                       const void* g, const float* Eb, const void* dA, const float* S_in,
                       const void* d_o, void* dq, void* dk, void* dg, float* D, float* carry,
@@ -108,6 +115,11 @@ bool tc_supported(const Dims& d);
 bool tc_uses_decay(const Dims& d);
 // Whether its backward also runs tc_dA (and so needs a dA buffer in its workspace).
 bool tc_uses_dA(const Dims& d);
+// Whether the tensor-core forward (bwd = false) or backward (bwd = true) of this
+// shape reads the SCALAR / NONE log-decay in its own layout ([B,H,T] or none)
+// rather than broadcast to [B,H,T,dk]: every kernel of that direction that reads
+// the log-decay is one with the form built in (tc_decay, tc_bwd_qk).
+bool tc_native_forms(const Dims& d, bool bwd);
 // Device buffers of the operands computed once per forward (decay_layout) and
 // of the backward's score gradient dA [B,H,T,64] bf16.
 struct TcOps {

@@ -14,6 +14,8 @@ bool tc_uses_dA(const Dims& d) {
   return tc_uses_decay(d) && tc_bwd_qk_supported(d) && tc_dA_supported(d);
 }
 
+bool tc_native_forms(const Dims& d, bool bwd) { return bwd ? tc_uses_dA(d) : tc_uses_decay(d); }
+
 // Forward: the decay pass, then pass 1 (on its K~ and e^{b_last}) and the scan on
 // the caller's stream while the scores run on the auxiliary stream (they do not
 // depend on the scan); pass 2 joins both.  In overlap mode 2 the scan runs on the

@@ -73,6 +73,14 @@
 // dlog_alpha suffix passes from group to group through shared memory and an
 // mbarrier.  The partials are received double-buffered, so that the four CTAs
 // of a cluster need not move in lockstep.
+//
+// Decay forms.  The scalar-decay form copies the chunk's 64 log-decays (one per
+// token) instead of a [64 t][32 i] tile, and its reverse sweep sums each
+// token's dlog_alpha over this CTA's 32 rows in the warp (a shuffle tree) and
+// stores the fp32 partial of the rows [32 c, 32 c + 32), c = i0 / 32 + rank,
+// at dlog_alpha_part[c][t]; a small kernel adds the d_k / 32 partials of a
+// token (decay_forms.cu).  The no-decay form (b = 0) copies no log-decay and
+// neither writes q.dq nor computes dlog_alpha.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -135,15 +143,21 @@ static_assert(kSmem + 1024 <= 227 * 1024, "shared memory");
 
 __device__ int g_qk_status = 0;
 
-template <bool REV>
+template <bool REV, int FORM>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmU,
                  const __grid_constant__ CUtensorMap tmZ, const __grid_constant__ CUtensorMap tmP,
                  const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmG,
                  const __grid_constant__ CUtensorMap tmQD, const __grid_constant__ CUtensorMap tmOut,
                  const __grid_constant__ CUtensorMap tmAux, const float* __restrict__ Eb,
-                 const float* __restrict__ S_src, const float* __restrict__ carry, int64_t T,
-                 int dk, int dv, int P, int64_t L) {
+                 const float* __restrict__ S_src, const float* __restrict__ carry,
+                 float* __restrict__ dg_part, int64_t T, int64_t nrows, int dk, int dv, int P,
+                 int64_t L) {
+  constexpr bool kDiag = FORM == ZECO_DECAY_DIAG, kScalar = FORM == ZECO_DECAY_SCALAR;
+  constexpr bool kDecay = FORM != ZECO_DECAY_NONE;
+  // the second output of the sweep, stored by TMA: q.dq (forward, both decaying
+  // forms), dlog_alpha (reverse, diagonal form)
+  constexpr bool kAux = REV ? kDiag : kDecay;
   extern __shared__ __align__(1024) unsigned char smraw[];
   unsigned char* sm = align1024(smraw);
   float* sRcv = reinterpret_cast<float*>(sm + kOffRcv);
@@ -433,24 +447,28 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
     auto issue_ep = [&](int it) {
       const int32_t r = chunk_row(chunk_of(it));
       const int x = i0 + kOwn * (int)rank;
-      mbar_expect_tx(&ep_full[g], 2 * kC * kOwn * 2 + (REV ? kC * kOwn * 4 : 0));
+      constexpr uint32_t kGBytes = kDiag ? kC * kOwn * 2 : kScalar ? kC * 2 : 0;
+      mbar_expect_tx(&ep_full[g], kC * kOwn * 2 + kGBytes + (REV && kDecay ? kC * kOwn * 4 : 0));
       tma_load_2d(ep + kEpY, &tmY, x, r, &ep_full[g]);
-      tma_load_2d(ep + kEpG, &tmG, x, r, &ep_full[g]);
-      if (REV) tma_load_2d(ep + kEpQD, &tmQD, x, r, &ep_full[g]);
+      // scalar form: the map views log_alpha as rows of one chunk's 64 tokens
+      if (kDiag) tma_load_2d(ep + kEpG, &tmG, x, r, &ep_full[g]);
+      if (kScalar) tma_load_2d(ep + kEpG, &tmG, 0, r / kC, &ep_full[g]);
+      if (REV && kDecay) tma_load_2d(ep + kEpQD, &tmQD, x, r, &ep_full[g]);
     };
     int last = -1;  // leader: the last chunk whose factors were requested
     if (leader) {
       prefetch_tmap(&tmY);
-      prefetch_tmap(&tmG);
-      if (REV) prefetch_tmap(&tmQD);
+      if (kDecay) prefetch_tmap(&tmG);
+      if (REV && kDecay) prefetch_tmap(&tmQD);
       prefetch_tmap(&tmOut);
-      prefetch_tmap(&tmAux);
+      if (kAux) prefetch_tmap(&tmAux);
       if (g < nc) {
         issue_ep(g);
         last = g;
       }
     }
-    if (REV && g == 0 && eq == 0) sRun[er] = carry[((size_t)bh * P + p) * dk + i0 + ec];
+    if (REV && kDecay && g == 0 && eq == 0)
+      sRun[er] = carry[((size_t)bh * P + p) * dk + i0 + ec];
 #pragma unroll 1
     for (int it = g; it < nc; it += 2) {
       const int n = chunk_of(it);
@@ -490,32 +508,35 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
       float gl[16], xa[16], term[16];
 #pragma unroll
       for (int u = 0; u < 16; ++u) {
-        gl[u] = __bfloat162float(epG[sb + u * kOwn]);
+        gl[u] = kDiag     ? __bfloat162float(epG[sb + u * kOwn])
+                : kScalar ? __bfloat162float(epG[16 * eq + u])
+                          : 0.f;
         // the stored rounded Q~ (fwd) / K~ (rev) times the raw accumulator
         // (= q_eff dq / k_eff dk)
         xa[u] = __bfloat162float(epY[sb + u * kOwn]) * acc[u];
-        if (REV) term[u] = epQD[sb + u * kOwn] - xa[u];
+        if (REV && kDecay) term[u] = epQD[sb + u * kOwn] - xa[u];
       }
       float gs = 0.f, ssum = 0.f;
 #pragma unroll
       for (int u = 0; u < 16; ++u) {
         gs += gl[u];
-        if (!REV)
+        if (!REV && kDecay)
           epQD[sb + u * kOwn] = xa[u];  // q.dq, staged for its store
-        else
+        else if (REV && kDecay)
           ssum += term[u];
       }
       gq[eq * 32 + er] = gs;
-      if (REV) qs[eq * 32 + er] = ssum;
+      if (REV && kDecay) qs[eq * 32 + er] = ssum;
       grp_bar(bar_sync);
       float bsum = 0.f;  // log-decay of the earlier 16-token quarters of the chunk
       for (int q2 = 0; q2 < eq; ++q2) bsum += gq[q2 * 32 + er];
 #pragma unroll
       for (int u = 0; u < 16; ++u) {
         bsum += gl[u];
-        epY[sb + u * kOwn] = __float2bfloat16_rn(acc[u] * __expf(REV ? -bsum : bsum));
+        const float x = kDecay ? acc[u] * __expf(REV ? -bsum : bsum) : acc[u];
+        epY[sb + u * kOwn] = __float2bfloat16_rn(x);
       }
-      if (REV) {
+      if (REV && kDecay) {
         // this chunk's total, and the part of it after this warp's 16 tokens
         float tot = 0.f, after = 0.f;
 #pragma unroll
@@ -535,10 +556,39 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
           if (it + 1 < nc) mbar_arrive(&carry_full[g ^ 1]);
         }
         float runq = cin + after;
+        if (kDiag) {
 #pragma unroll
-        for (int u = 15; u >= 0; --u) {
-          runq += term[u];
-          epG[sb + u * kOwn] = __float2bfloat16_rn(runq);
+          for (int u = 15; u >= 0; --u) {
+            runq += term[u];
+            epG[sb + u * kOwn] = __float2bfloat16_rn(runq);
+          }
+        } else {
+          // scalar form: the sum over this CTA's 32 rows (the warp's lanes) of
+          // each of the warp's 16 tokens.  A halving tree: at offset o a lane
+          // keeps the upper or lower half of its values (by bit o of its lane)
+          // and adds its partner's copy of that half, so that after offsets
+          // 16, 8, 4, 2 lane l holds token l / 2, and offset 1 adds the pair.
+          float v[16];
+#pragma unroll
+          for (int u = 15; u >= 0; --u) {
+            runq += term[u];
+            v[u] = runq;
+          }
+#pragma unroll
+          for (int o = 16, n2 = 8; o >= 2; o >>= 1, n2 >>= 1) {
+            const bool up = (lane & o) != 0;
+#pragma unroll
+            for (int u = 0; u < n2; ++u) {
+              const float send = up ? v[u] : v[u + n2];
+              const float keep = up ? v[u + n2] : v[u];
+              v[u] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+            }
+          }
+          v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
+          if ((lane & 1) == 0) {
+            const int c = (i0 + kOwn * (int)rank) / kOwn;
+            dg_part[(size_t)c * nrows + chunk_row(n) + 16 * eq + (lane >> 1)] = v[0];
+          }
         }
       }
       // the chunk's outputs leave by TMA from the stage
@@ -547,7 +597,7 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
       if (leader) {
         const int32_t r = chunk_row(n), x = i0 + kOwn * (int)rank;
         tma_store_2d(&tmOut, ep + kEpY, x, r);
-        tma_store_2d(&tmAux, ep + (REV ? kEpG : kEpQD), x, r);
+        if (kAux) tma_store_2d(&tmAux, ep + (REV ? kEpG : kEpQD), x, r);
         bulk_commit();
         if (it + 2 < nc && ok) {
           bulk_wait_read_all();  // the stores have read the stage: refill it
@@ -572,13 +622,13 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
   }
 }
 
-template <bool REV>
+template <bool REV, int FORM>
 cudaError_t launch_qk(const Dims& d, const CUtensorMap& tx, const CUtensorMap& tu,
                       const CUtensorMap& tz, const CUtensorMap& tp, const CUtensorMap& ty,
                       const CUtensorMap& tg, const CUtensorMap& tqd, const CUtensorMap& tout,
                       const CUtensorMap& taux, const float* Eb, const float* S_src,
-                      const float* carry, cudaStream_t st) {
-  auto kern = tc_bwd_qk_kernel<REV>;
+                      const float* carry, float* dg_part, cudaStream_t st) {
+  auto kern = tc_bwd_qk_kernel<REV, FORM>;
   const int smem = kSmem + 1024;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -596,7 +646,27 @@ cudaError_t launch_qk(const Dims& d, const CUtensorMap& tx, const CUtensorMap& t
   cfg.numAttrs = 1;
   prof_start(st);
   return cudaLaunchKernelEx(&cfg, kern, tx, tu, tz, tp, ty, tg, tqd, tout, taux, Eb, S_src,
-                            carry, d.T, (int)d.dk, (int)d.dv, d.P, d.L);
+                            carry, dg_part, d.T, d.B * d.H * d.T, (int)d.dk, (int)d.dv, d.P,
+                            d.L);
+}
+
+// the tensor maps of the two sweeps (tc_bwd_qk)
+enum { kMapQs, kMapKs, kMapV, kMapDo, kMapDA, kMapQp, kMapKp, kMapG, kMapQD, kMapDq, kMapDk,
+       kMapDg, kMaps };
+
+template <int FORM>
+cudaError_t launch_sweeps(const Dims& d, const CUtensorMap* m, const float* Eb,
+                          const float* S_in, const float* D, const float* carry, float* dg_part,
+                          cudaStream_t st) {
+  cudaError_t e = launch_qk<false, FORM>(d, m[kMapKs], m[kMapV], m[kMapDo], m[kMapDA], m[kMapQp],
+                                         m[kMapG], m[kMapQD], m[kMapDq], m[kMapQD], Eb, S_in,
+                                         carry, dg_part, st);
+  prof_mark("tc_bwd_dq", st);
+  if (e != cudaSuccess) return e;
+  e = launch_qk<true, FORM>(d, m[kMapQs], m[kMapDo], m[kMapV], m[kMapDA], m[kMapKp], m[kMapG],
+                            m[kMapQD], m[kMapDk], m[kMapDg], Eb, D, carry, dg_part, st);
+  prof_mark("tc_bwd_dk", st);
+  return e;
 }
 
 }  // namespace
@@ -610,27 +680,37 @@ cudaError_t tc_bwd_qk(const Dims& d, const void* Qt, const void* Kt, const void*
                       const void* g, const float* Eb, const void* dA, const float* S_in,
                       const void* d_o, void* dq, void* dk, void* dg, float* D, float* carry,
                       float* qdq, cudaStream_t st) {
-  // swizzled [64 t][64] tiles for the MMAs; plain [64 t][32 i] tiles for the epilogue
-  CUtensorMap tqs, tks, tv, tdo, tp, tqp, tkp, tgp, tqd, tdq, tdk, tdg;
+  // swizzled [64 t][64] tiles for the MMAs; plain [64 t][32 i] tiles for the
+  // epilogue.  The log-decay and its gradient by form: diagonal [rows][d_k] bf16
+  // both; scalar g [rows] bf16 (read as [rows / 64][64]) and dg the fp32
+  // partials [d_k / 32][rows]; none: neither is read or written (their maps
+  // repeat another one's).
+  CUtensorMap m[kMaps];
   const uint64_t rows = (uint64_t)(d.B * d.H * d.T);
-  if (!make_tmap_bf16(&tqs, Qt, rows, d.dk, kC) || !make_tmap_bf16(&tks, Kt, rows, d.dk, kC) ||
-      !make_tmap_bf16(&tv, v, rows, d.dv, kC) || !make_tmap_bf16(&tdo, d_o, rows, d.dv, kC) ||
-      !make_tmap_bf16(&tp, dA, rows, kC, kC) ||
-      !make_tmap_bf16_plain(&tqp, Qt, rows, d.dk, kOwn, kC) ||
-      !make_tmap_bf16_plain(&tkp, Kt, rows, d.dk, kOwn, kC) ||
-      !make_tmap_bf16_plain(&tgp, g, rows, d.dk, kOwn, kC) ||
-      !make_tmap_f32_plain(&tqd, qdq, rows, d.dk, kOwn, kC) ||
-      !make_tmap_bf16_plain(&tdq, dq, rows, d.dk, kOwn, kC) ||
-      !make_tmap_bf16_plain(&tdk, dk, rows, d.dk, kOwn, kC) ||
-      !make_tmap_bf16_plain(&tdg, dg, rows, d.dk, kOwn, kC))
-    return cudaErrorInvalidValue;
-  cudaError_t e =
-      launch_qk<false>(d, tks, tv, tdo, tp, tqp, tgp, tqd, tdq, tqd, Eb, S_in, carry, st);
-  prof_mark("tc_bwd_dq", st);
-  if (e != cudaSuccess) return e;
-  e = launch_qk<true>(d, tqs, tdo, tv, tp, tkp, tgp, tqd, tdk, tdg, Eb, D, carry, st);
-  prof_mark("tc_bwd_dk", st);
-  return e;
+  bool ok = make_tmap_bf16(&m[kMapQs], Qt, rows, d.dk, kC) &&
+            make_tmap_bf16(&m[kMapKs], Kt, rows, d.dk, kC) &&
+            make_tmap_bf16(&m[kMapV], v, rows, d.dv, kC) &&
+            make_tmap_bf16(&m[kMapDo], d_o, rows, d.dv, kC) &&
+            make_tmap_bf16(&m[kMapDA], dA, rows, kC, kC) &&
+            make_tmap_bf16_plain(&m[kMapQp], Qt, rows, d.dk, kOwn, kC) &&
+            make_tmap_bf16_plain(&m[kMapKp], Kt, rows, d.dk, kOwn, kC) &&
+            make_tmap_f32_plain(&m[kMapQD], qdq, rows, d.dk, kOwn, kC) &&
+            make_tmap_bf16_plain(&m[kMapDq], dq, rows, d.dk, kOwn, kC) &&
+            make_tmap_bf16_plain(&m[kMapDk], dk, rows, d.dk, kOwn, kC);
+  if (ok && d.decay == ZECO_DECAY_DIAG)
+    ok = make_tmap_bf16_plain(&m[kMapG], g, rows, d.dk, kOwn, kC) &&
+         make_tmap_bf16_plain(&m[kMapDg], dg, rows, d.dk, kOwn, kC);
+  else if (ok && d.decay == ZECO_DECAY_SCALAR)
+    ok = make_tmap_bf16_plain(&m[kMapG], g, rows / kC, kC, kC, 1);
+  if (!ok) return cudaErrorInvalidValue;
+  if (d.decay != ZECO_DECAY_DIAG) m[kMapDg] = m[kMapDk];
+  if (d.decay == ZECO_DECAY_NONE) m[kMapG] = m[kMapQp];
+  float* part = d.decay == ZECO_DECAY_SCALAR ? (float*)dg : nullptr;
+  if (d.decay == ZECO_DECAY_SCALAR)
+    return launch_sweeps<ZECO_DECAY_SCALAR>(d, m, Eb, S_in, D, carry, part, st);
+  if (d.decay == ZECO_DECAY_NONE)
+    return launch_sweeps<ZECO_DECAY_NONE>(d, m, Eb, S_in, D, carry, part, st);
+  return launch_sweeps<ZECO_DECAY_DIAG>(d, m, Eb, S_in, D, carry, part, st);
 }
 
 // Reads and clears this file's bounded-wait flag (nonzero: a wait gave up).

@@ -12,6 +12,10 @@
 // from the same bf16 values.  The pass is bound by HBM: each thread owns 8
 // columns of one chunk and walks its 64 tokens with 16-byte loads and stores
 // (a warp reads whole 512-byte rows when d_k = 256).
+//
+// The scalar-decay form reads its one log-decay per token ([B,H,T]; every
+// thread of a chunk reads the same value), the no-decay form reads none: b = 0,
+// Q~ = q, K~ = k, e^{b_last} = 1.
 #include "common.cuh"
 #include "launch.h"
 
@@ -37,7 +41,7 @@ __device__ __forceinline__ uint4 pack8(const float* f) {
   return w;
 }
 
-template <int DK>
+template <int DK, int FORM>
 __global__ void __launch_bounds__(256)
 decay_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
              const __nv_bfloat16* __restrict__ g, __nv_bfloat16* __restrict__ Qt,
@@ -54,11 +58,16 @@ decay_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restric
 #pragma unroll 8
   for (int u = 0; u < kC; ++u) {
     const size_t o = base + (size_t)u * DK;
-    const uint4 gw = __ldg(reinterpret_cast<const uint4*>(g + o));
     const uint4 qw = __ldg(reinterpret_cast<const uint4*>(q + o));
     const uint4 kw = __ldg(reinterpret_cast<const uint4*>(k + o));
     float gf[8], qf[8], kf[8];
-    unpack8(gw, gf);
+    if (FORM == ZECO_DECAY_DIAG) {
+      unpack8(__ldg(reinterpret_cast<const uint4*>(g + o)), gf);
+    } else {
+      const float gs = FORM == ZECO_DECAY_SCALAR ? __bfloat162float(g[chunk * kC + u]) : 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) gf[e] = gs;
+    }
     unpack8(qw, qf);
     unpack8(kw, kf);
 #pragma unroll
@@ -85,13 +94,24 @@ cudaError_t tc_decay(const Dims& d, const void* q, const void* k, const void* g,
   auto qb = (const __nv_bfloat16*)q;
   auto kb = (const __nv_bfloat16*)k;
   auto gb = (const __nv_bfloat16*)g;
+  auto Qb = (__nv_bfloat16*)Qt;
+  auto Kb = (__nv_bfloat16*)Kt;
   prof_start(st);
-  if (d.dk == 256)
-    decay_kernel<256><<<blocks, 256, 0, st>>>(qb, kb, gb, (__nv_bfloat16*)Qt,
-                                              (__nv_bfloat16*)Kt, Eb, nchunks);
-  else
-    decay_kernel<128><<<blocks, 256, 0, st>>>(qb, kb, gb, (__nv_bfloat16*)Qt,
-                                              (__nv_bfloat16*)Kt, Eb, nchunks);
+  if (d.dk == 256) {
+    if (d.decay == ZECO_DECAY_SCALAR)
+      decay_kernel<256, ZECO_DECAY_SCALAR><<<blocks, 256, 0, st>>>(qb, kb, gb, Qb, Kb, Eb, nchunks);
+    else if (d.decay == ZECO_DECAY_NONE)
+      decay_kernel<256, ZECO_DECAY_NONE><<<blocks, 256, 0, st>>>(qb, kb, gb, Qb, Kb, Eb, nchunks);
+    else
+      decay_kernel<256, ZECO_DECAY_DIAG><<<blocks, 256, 0, st>>>(qb, kb, gb, Qb, Kb, Eb, nchunks);
+  } else {
+    if (d.decay == ZECO_DECAY_SCALAR)
+      decay_kernel<128, ZECO_DECAY_SCALAR><<<blocks, 256, 0, st>>>(qb, kb, gb, Qb, Kb, Eb, nchunks);
+    else if (d.decay == ZECO_DECAY_NONE)
+      decay_kernel<128, ZECO_DECAY_NONE><<<blocks, 256, 0, st>>>(qb, kb, gb, Qb, Kb, Eb, nchunks);
+    else
+      decay_kernel<128, ZECO_DECAY_DIAG><<<blocks, 256, 0, st>>>(qb, kb, gb, Qb, Kb, Eb, nchunks);
+  }
   prof_mark("tc_decay", st);
   return cudaGetLastError();
 }

@@ -91,9 +91,12 @@ typedef enum { ZECO_PATH_AUTO = 0, ZECO_PATH_SIMT = 1, ZECO_PATH_TC = 2 } zeco_p
  *           of the per-row gradient).
  *   NONE:   alpha = 1 (plain causal linear attention); log_alpha and
  *           dlog_alpha are not used and may be NULL.
- * SCALAR and NONE run the same kernels as DIAG on a log-decay broadcast to
- * [B,H,T,dk] in the workspace (and, backward, a [B,H,T,dk] gradient that
- * SCALAR reduces over d_k). */
+ * On the tensor-core path with C = 64 the kernels that read the log-decay
+ * have each form built in: SCALAR is read once per token and its gradient is
+ * summed from fp32 partials over blocks of 32 d_k rows; NONE reads no decay
+ * and skips the dlog_alpha work.  Elsewhere SCALAR and NONE run the DIAG
+ * kernels on a log-decay broadcast to [B,H,T,dk] in the workspace (and,
+ * backward, a [B,H,T,dk] gradient that SCALAR reduces over d_k). */
 typedef enum { ZECO_DECAY_DIAG = 0, ZECO_DECAY_SCALAR = 1, ZECO_DECAY_NONE = 2 } zeco_decay;
 
 typedef struct zeco_shape {
@@ -145,10 +148,12 @@ size_t zeco_gla_saved_bytes(const zeco_shape *shape);
  * and q .* dq in fp32 [B,H,T,dk] (dlog_alpha is a long suffix sum of
  * q .* dq - k .* dk that cancels heavily, so its terms are kept in fp32).
  * On the tensor-core path the backward also holds the masked gradient of the
- * intra-chunk scores dA = do v^T [B,H,T,64] bf16.  The SCALAR and NONE decay
- * forms add the log-decay broadcast to [B,H,T,dk] (both directions) and its
- * per-row gradient (backward).  Returns 0 when no scratch is needed or the
- * shape is invalid or unsupported.
+ * intra-chunk scores dA = do v^T [B,H,T,64] bf16.  Where the kernels read the
+ * SCALAR / NONE decay forms in their own layout (see zeco_decay), SCALAR's
+ * backward adds the fp32 partial sums of its gradient [dk/32][B,H,T] and NONE
+ * adds nothing; elsewhere both forms add the log-decay broadcast to
+ * [B,H,T,dk] (both directions) and its per-row gradient (backward).  Returns
+ * 0 when no scratch is needed or the shape is invalid or unsupported.
  */
 size_t zeco_gla_workspace_bytes(const zeco_shape *shape, int bwd);
 

@@ -57,6 +57,19 @@ def test_sizes_follow_the_layout(lib):
     dA = 4 * (1 << 20) * 64 * 2
     assert z.workspace_bytes(s, True) == state + gam + qdq + dA
     assert z.workspace_bytes(s, False) == 0
+    # decay forms on the tensor-core path: read in their own layout, so no
+    # broadcast scratch; the scalar backward adds its fp32 gradient partials
+    # [dk / 32][B,H,T]
+    parts = (256 // 32) * 4 * (1 << 20) * 4
+    assert z.workspace_bytes(_shape(decay="scalar"), False) == 0
+    assert z.workspace_bytes(_shape(decay="none"), False) == 0
+    assert z.workspace_bytes(_shape(decay="scalar"), True) == state + gam + qdq + dA + parts
+    assert z.workspace_bytes(_shape(decay="none"), True) == state + gam + qdq + dA
+    # elsewhere the log-decay is broadcast to [B,H,T,dk] (and its per-row
+    # gradient too, in the backward)
+    bc = 4 * (1 << 20) * 256 * 2
+    assert z.workspace_bytes(_shape(decay="scalar", path="simt"), False) == bc
+    assert z.workspace_bytes(_shape(decay="scalar", C=128), False) == bc
     # the SIMT path keeps no decay-weighted operands
     simt = _shape(path="simt", dtype="f32", dk=64, dv=64)
     st64 = 4 * 65 * 64 * 64 * 4
@@ -95,9 +108,9 @@ def test_null_and_misaligned_pointers_are_rejected(lib):
     assert lib.zeco_gla_fwd(ctypes.byref(s), *args, None, None, None, ok, None, 0, None) == -1
     assert lib.zeco_gla_fwd(ctypes.byref(s), bad, ok, ok, ok, None, ok, None, ok, None, 0,
                             None) == -1
-    # forward with the scalar decay form (it needs scratch for the broadcast
-    # log-decay): workspace missing, then too small
-    sc = _shape(T=4096, P=4, decay="scalar")
+    # forward with the scalar decay form off the tensor-core sweeps (it needs
+    # scratch for the broadcast log-decay): workspace missing, then too small
+    sc = _shape(T=4096, P=4, decay="scalar", path="simt")
     assert lib.zeco_gla_fwd(ctypes.byref(sc), *args, None, ok, None, ok, None, 0, None) == -1
     assert lib.zeco_gla_fwd(ctypes.byref(sc), *args, None, ok, None, ok, ok, 16, None) == -3
     # workspace too small for the backward
@@ -118,16 +131,16 @@ def test_path_resolution(lib):
 
 def test_decay_forms_workspace_and_arguments(lib):
     import chunked_state_scan_gb300 as z
-    diag = _shape(T=4096, P=4)
+    diag = _shape(T=4096, P=4, path="simt")
     for name in ("scalar", "none"):
-        s = _shape(T=4096, P=4, decay=name)
+        s = _shape(T=4096, P=4, decay=name, path="simt")
         extra = 4 * 4096 * 256 * 2  # broadcast log-decay [B,H,T,dk] bf16
         assert z.workspace_bytes(s, False) == z.workspace_bytes(diag, False) + extra
         assert z.workspace_bytes(s, True) == z.workspace_bytes(diag, True) + 2 * extra
     ok = ctypes.c_void_p(4096)
     # without decay log_alpha may be NULL (the call then fails only on the tiny
     # workspace); with decay it may not
-    none = _shape(T=4096, P=4, decay="none")
+    none = _shape(T=4096, P=4, decay="none", path="simt")
     assert lib.zeco_gla_fwd(ctypes.byref(none), ok, ok, ok, None, None, ok, None, ok, ok, 16,
                             None) == -3
     assert lib.zeco_gla_fwd(ctypes.byref(diag), ok, ok, ok, None, None, ok, None, ok, ok, 16,

@@ -223,12 +223,54 @@ def test_f32_decay_forms(z, decay):
     _assert(errs, "f32", f"f32 decay form {decay}")
 
 
+@pytest.mark.parametrize("dk", [128, 256])
 @pytest.mark.parametrize("decay", [1, 2])
-def test_bf16_decay_forms_on_tensor_cores(z, decay):
-    shape = z.make_shape(1, 2, 2048, 128, 512, 2, 4, 64, "bf16", "tc", decay)
+def test_bf16_decay_forms_on_tensor_cores(z, decay, dk):
+    # the tensor-core kernels read the scalar log-decay once per token (none for
+    # the no-decay form): no [B,H,T,dk] broadcast is made, and the scalar
+    # gradient is the sum of the reverse sweep's per-32-row partials
+    shape = z.make_shape(1, 2, 2048, dk, 512, 2, 4, 64, "bf16", "tc", decay)
     assert z.resolve_path(shape) == "tc"
-    errs = _decay_case(z, decay, "bf16", 1, 2, 2048, 128, 512, 2, 4, "tc")
-    _assert(errs, "bf16", f"bf16 tc decay form {decay}")
+    names, errs = parity.kernel_names(
+        z, lambda: _decay_case(z, decay, "bf16", 1, 2, 2048, dk, 512, 2, 4, "tc"))
+    _assert(errs, "bf16", f"bf16 tc decay form {decay} dk {dk}")
+    assert "tc_decay" in names and "tc_bwd_dk" in names, names
+    assert "expand_log_alpha" not in names and "reduce_dlog_alpha" not in names, names
+    assert ("sum_dlog_alpha_parts" in names) == (decay == 1), names
+
+
+def test_bf16_scalar_decay_broadcast_on_tensor_core_path(z):
+    # C = 128: the tensor-core segment states, but the CUDA-core sweeps, which
+    # take the log-decay broadcast to [B,H,T,dk]
+    B, H, T, dk, dv, P, K, C = 1, 1, 1024, 128, 128, 2, 4, 128
+    shape = z.make_shape(B, H, T, dk, dv, P, K, C, "bf16", "tc", 1)
+    assert z.resolve_path(shape) == "tc"
+    x = workloads.make_custom(B, H, T, dk, dv, dtype="bf16", seed=41, qk_scale=1 / 16,
+                              s0_scale=0.2)
+    g = x["log_alpha"][..., 0].contiguous()
+    dev = {n: (t.cuda() if t is not None else None) for n, t in x.items()}
+
+    def run():
+        o, sf, saved = z.zeco_gla_fwd(dev["q"], dev["k"], dev["v"], g.cuda(), dev["S0"], P=P,
+                                      K=K, C=C, path="tc", decay="scalar")
+        gr = z.zeco_gla_bwd(dev["q"], dev["k"], dev["v"], g.cuda(), saved, dev["do"],
+                            dev["dS_final"], P=P, K=K, C=C, path="tc", decay="scalar")
+        torch.cuda.synchronize()
+        return o, sf, gr
+
+    names, (o, sf, gr) = parity.kernel_names(z, run)
+    assert names.count("expand_log_alpha") == 2 and "reduce_dlog_alpha" in names, names
+    assert "tc_decay" not in names, names
+    np_in = {n: (parity.to_np(t) if t is not None else None) for n, t in x.items()}
+    gn = parity.to_np(g)
+    ro, rsf = oracle.gla_fwd_decay(np_in["q"], np_in["k"], np_in["v"], gn, np_in["S0"], 1)
+    rg = oracle.gla_bwd_decay(np_in["q"], np_in["k"], np_in["v"], gn, np_in["S0"], np_in["do"],
+                              np_in["dS_final"], 1)
+    errs = {"o": parity.err(parity.to_np(o), ro, "bf16"),
+            "S_final": parity.err(parity.to_np(sf), rsf, "bf16")}
+    for n in ("dq", "dk", "dv", "dS0", "dlog_alpha"):
+        errs[n] = parity.err(parity.to_np(gr[n]), rg[n], "bf16")
+    _assert(errs, "bf16", "bf16 tc path, C = 128, scalar decay (broadcast)")
 
 
 # ------------------------------------------------------------ segment counts
