@@ -25,6 +25,7 @@ import ctypes
 import json
 import math
 import os
+import statistics
 import subprocess
 import sys
 import threading
@@ -439,17 +440,21 @@ def measure(w, args, world, rank, local, want_e2e=True, want_cpu=True, quiet=Fal
                            xx["dS_final"], P=w.P, K=w.K, C=w.C, path=args.path, grads=grads,
                            workspace=ws, stream=stream)
 
+    per_step = []  # device ms of each step of the last timed_steps call
+
     def timed_steps(n):
-        """Device time of n steps (ms), L2 flushed before each when the inputs are small."""
+        """Device time of n steps (ms), L2 flushed before each when the inputs are small;
+        each step's own time is left in per_step."""
+        per_step.clear()
         if not flush:
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            for _ in range(n):
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+            evs[0].record(stream)
+            for i in range(n):
                 step()
-            e1.record(stream)
+                evs[i + 1].record(stream)
             torch.cuda.synchronize(dev)
-            return e0.elapsed_time(e1)
-        total = 0.0
+            per_step.extend(evs[i].elapsed_time(evs[i + 1]) for i in range(n))
+            return evs[0].elapsed_time(evs[n])
         for _ in range(n):
             with torch.cuda.stream(stream):
                 flush_buf.zero_()
@@ -458,8 +463,8 @@ def measure(w, args, world, rank, local, want_e2e=True, want_cpu=True, quiet=Fal
             step()
             e1.record(stream)
             torch.cuda.synchronize(dev)
-            total += e0.elapsed_time(e1)
-        return total
+            per_step.append(e0.elapsed_time(e1))
+        return sum(per_step)
 
     torch.cuda.synchronize(dev)
     for _ in range(args.warmup):
@@ -489,6 +494,7 @@ def measure(w, args, world, rank, local, want_e2e=True, want_cpu=True, quiet=Fal
     barrier(world)
     torch.cuda.synchronize(dev)
     elapsed = timed_steps(args.steps) / 1e3
+    steps_ms = list(per_step)
     barrier(world)
     clk = clocks.stop()
     dev_status = lib.zeco_last_device_status(ctypes.c_void_p(stream.cuda_stream))
@@ -553,6 +559,10 @@ def measure(w, args, world, rank, local, want_e2e=True, want_cpu=True, quiet=Fal
         f"({w.name})",
         "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "step_ms_stats": {"mean": statistics.fmean(steps_ms),
+                          "std": statistics.stdev(steps_ms) if len(steps_ms) > 1 else 0.0,
+                          "min": min(steps_ms), "max": max(steps_ms), "n": len(steps_ms),
+                          "rank": rank},
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
         "data": "synthetic (seeded; shapes and distributions of the GLA-1B layer workload)",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "dk": w.dk, "dv": w.dv,

@@ -67,7 +67,10 @@ int check_shape(const zeco_shape* s, Dims* d) {
 }
 
 int resolve(const zeco_shape* s, const Dims& d) {
-  const bool tc = zeco::tc_supported(d);
+  // the tensor-core path runs CUDA-core kernels for the steps it has no
+  // tensor-core kernel for (C != 64): their shared memory must fit one CTA too
+  const bool tc = zeco::tc_supported(d) &&
+                  (zeco::tc_uses_dA(d) || zeco::simt_smem_bytes(d) <= 227 * 1024);
   if (s->path == ZECO_PATH_TC) return tc ? (int)ZECO_PATH_TC : (int)ZECO_ERR_UNSUPPORTED;
   if (s->path == ZECO_PATH_AUTO && tc) return ZECO_PATH_TC;
   // SIMT: shared memory must fit one CTA
@@ -75,7 +78,8 @@ int resolve(const zeco_shape* s, const Dims& d) {
   return ZECO_PATH_SIMT;
 }
 
-// Scratch layout of one call: the backward's own buffers (bwd only), then, for
+// Scratch layout of one call: the backward's own buffers (bwd only; with the
+// CUDA-core dq/dk kernel also its fp32 dA), then, for
 // the backward on the tensor-core path, the score gradient dA, then, for the
 // SCALAR / NONE decay forms, the broadcast log-decay and its per-row gradient,
 // or, where the kernels read the form in its own layout, the SCALAR gradient's
@@ -91,7 +95,7 @@ struct WsPlan {
 
 WsPlan plan_ws(const Dims& d, int path, bool bwd) {
   WsPlan w;
-  w.bwd = zeco::bwd_ws_layout(d);
+  w.bwd = zeco::bwd_ws_layout(d, path != ZECO_PATH_TC || !zeco::tc_uses_dA(d));
   size_t base = bwd ? w.bwd.total : 0;
   w.dA_off = zeco::align_up(base, 256);
   if (bwd && path == ZECO_PATH_TC && zeco::tc_uses_dA(d))
@@ -244,6 +248,7 @@ int zeco_gla_bwd(const zeco_shape* shape, const void* q, const void* k, const vo
   float* D = (float*)((char*)workspace + wl.D_off);
   float* carry = (float*)((char*)workspace + wl.carry_off);
   float* qdq = (float*)((char*)workspace + wl.qdq_off);
+  float* dAf = (float*)((char*)workspace + wl.dAf_off);  // CUDA-core dq/dk only
   cudaStream_t st = (cudaStream_t)stream;
   cudaError_t e = cudaSuccess;
   const void* g = log_alpha;
@@ -259,9 +264,9 @@ int zeco_gla_bwd(const zeco_shape* shape, const void* q, const void* k, const vo
   if (e == cudaSuccess)
     e = path == ZECO_PATH_TC
             ? zeco::tc_backward(d, q, k, v, g, S_in, gamma, d_o, dS_final, dq, dk, dv, dg, dS0, D,
-                                carry, qdq, tc_ops(sl, saved, workspace, wp.dA_off), st)
+                                carry, qdq, dAf, tc_ops(sl, saved, workspace, wp.dA_off), st)
             : zeco::simt_backward(d, q, k, v, g, S_in, gamma, d_o, dS_final, dq, dk, dv, dg,
-                                  dS0, D, carry, qdq, st);
+                                  dS0, D, carry, qdq, dAf, st);
   if (e == cudaSuccess && d.decay == ZECO_DECAY_SCALAR)
     e = wp.native ? zeco::launch_sum_dlog_alpha_parts(d, (const float*)dg, dlog_alpha, st)
                   : zeco::launch_reduce_dlog_alpha(d, dg, dlog_alpha, st);

@@ -48,7 +48,7 @@ struct SavedLayout {
   size_t total;
 };
 struct BwdWsLayout {
-  size_t D_off, carry_off, qdq_off, total;
+  size_t D_off, carry_off, qdq_off, dAf_off, total;
 };
 
 inline SavedLayout saved_layout(const Dims& d, bool ops) {
@@ -62,13 +62,16 @@ inline SavedLayout saved_layout(const Dims& d, bool ops) {
   return s;
 }
 
-inline BwdWsLayout bwd_ws_layout(const Dims& d) {
+// simt_dA: the backward runs the CUDA-core dq/dk kernel, which reads the
+// intra-chunk score gradient dA [B,H,T,C] fp32 from here (at dAf_off).
+inline BwdWsLayout bwd_ws_layout(const Dims& d, bool simt_dA) {
   BwdWsLayout w;
   const size_t bh = (size_t)d.B * d.H;
   w.D_off = 0;
   w.carry_off = align_up(bh * (d.P + 1) * d.dk * d.dv * sizeof(float), 256);
   w.qdq_off = align_up(w.carry_off + bh * d.P * d.dk * sizeof(float), 256);
-  w.total = align_up(w.qdq_off + bh * d.T * d.dk * sizeof(float), 256);
+  w.dAf_off = align_up(w.qdq_off + bh * d.T * d.dk * sizeof(float), 256);
+  w.total = simt_dA ? align_up(w.dAf_off + bh * d.T * d.C * sizeof(float), 256) : w.dAf_off;
   return w;
 }
 

@@ -62,18 +62,19 @@ cudaError_t simt_forward(const Dims& d, const void* q, const void* k, const void
 cudaError_t simt_backward(const Dims& d, const void* q, const void* k, const void* v,
                           const void* g, const float* S_in, const float* gamma, const void* d_o,
                           const float* dS_final, void* dq, void* dk, void* dv, void* dg,
-                          float* dS0, float* D, float* carry, float* qdq, cudaStream_t st);
+                          float* dS0, float* D, float* carry, float* qdq, float* dA,
+                          cudaStream_t st);
 
 cudaError_t simt_fwd_out_bf16(const Dims& d, const void* q, const void* k, const void* v,
                               const void* g, const float* S_in, void* o, cudaStream_t st);
 cudaError_t simt_bwd_main_bf16(const Dims& d, const void* q, const void* k, const void* v,
                                const void* g, const float* S_in, const void* d_o, void* dq,
                                void* dk, void* dv, void* dg, float* D, float* carry, float* qdq,
-                               cudaStream_t st);
+                               float* dA, cudaStream_t st);
 
 cudaError_t simt_bwd_dqk_bf16(const Dims& d, const void* q, const void* k, const void* v,
                               const void* g, const float* S_in, const void* d_o, void* dq,
-                              void* dk, void* dg, float* D, float* carry, float* qdq,
+                              void* dk, void* dg, float* D, float* carry, float* qdq, float* dA,
                               cudaStream_t st);
 
 // ---- tcgen05 tensor-core path (tc_*.cu) --------------------------------
@@ -135,7 +136,7 @@ cudaError_t tc_forward(const Dims& d, const void* q, const void* k, const void* 
 cudaError_t tc_backward(const Dims& d, const void* q, const void* k, const void* v,
                         const void* g, const float* S_in, const float* gamma, const void* d_o,
                         const float* dS_final, void* dq, void* dk, void* dv, void* dg,
-                        float* dS0, float* D, float* carry, float* qdq, const TcOps& ops,
-                        cudaStream_t st);
+                        float* dS0, float* D, float* carry, float* qdq, float* dAf,
+                        const TcOps& ops, cudaStream_t st);
 
 }  // namespace zeco

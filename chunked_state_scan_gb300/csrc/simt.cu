@@ -349,14 +349,69 @@ bwd_dv_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restr
   }
 }
 
+// ------------------------------------------ backward: the intra-chunk dA
+// dA[t][s] = do_t . v_s for s <= t (0 above the diagonal), fp32 [B,H,T,C]: one
+// CTA per chunk, d_v in slabs of kSlab columns; each thread owns 4 x 4 blocks of
+// (t, s) and adds each slab's partial sum into them.  Computed once here, it is
+// read by every d_k-row block of both dq/dk sweeps.
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+bwd_dA_kernel(const T* __restrict__ dO, const T* __restrict__ v, float* __restrict__ dA,
+              Dims d) {
+  extern __shared__ float sm[];
+  const int C = d.C, dv = (int)d.dv, ldA = C + 1;
+  float* Os = sm;                  // [C][kSlab]
+  float* Vs = Os + C * kSlab;      // [C][kSlab]
+  float* As = Vs + C * kSlab;      // [C][C+1]
+  const int64_t r0 = (int64_t)blockIdx.x * C;  // the chunk's first row of [B*H*T]
+  const int nb = C / 4;
+  for (int e = threadIdx.x; e < C * ldA; e += kThreads) As[e] = 0.f;
+  for (int j0 = 0; j0 < dv; j0 += kSlab) {
+    const int w = min(kSlab, dv - j0);
+    __syncthreads();
+    for (int e = threadIdx.x; e < C * kSlab; e += kThreads) {
+      const int t = e / kSlab, jj = e % kSlab;
+      const bool in = jj < w;
+      Os[e] = in ? ld(dO + (size_t)(r0 + t) * dv + j0 + jj) : 0.f;
+      Vs[e] = in ? ld(v + (size_t)(r0 + t) * dv + j0 + jj) : 0.f;
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < nb * nb; e += kThreads) {
+      const int tb = e / nb, sb = e % nb;
+      if (sb > tb) continue;
+      float a4[4][4] = {};
+      for (int jj = 0; jj < w; ++jj) {
+        float a[4], b[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) a[u] = Os[(tb * 4 + u) * kSlab + jj];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) b[u] = Vs[(sb * 4 + u) * kSlab + jj];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+          for (int x = 0; x < 4; ++x) a4[u][x] = fmaf(a[u], b[x], a4[u][x]);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int x = 0; x < 4; ++x) As[(tb * 4 + u) * ldA + sb * 4 + x] += a4[u][x];
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < C * C; e += kThreads) {
+    const int t = e / C, s2 = e % C;
+    dA[(size_t)r0 * C + e] = s2 <= t ? As[t * ldA + s2] : 0.f;
+  }
+}
+
 // ------------------------------------------------- backward: dq, dk, dg
 template <typename T>
 __global__ void __launch_bounds__(kThreads)
 bwd_dqk_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
                const T* __restrict__ g, const T* __restrict__ dO, const float* __restrict__ S_in,
                const float* __restrict__ D, const float* __restrict__ carry,
-               T* __restrict__ dq, T* __restrict__ dk_out, T* __restrict__ dg_out,
-               float* __restrict__ qdq, Dims d) {
+               const float* __restrict__ dAg, T* __restrict__ dq, T* __restrict__ dk_out,
+               T* __restrict__ dg_out, float* __restrict__ qdq, Dims d) {
   extern __shared__ float sm[];
   const int C = d.C, dk = (int)d.dk, dv = (int)d.dv, ldA = C + 1;
   float* Ss = sm;                  // state rows [kKB][dv]
@@ -380,6 +435,7 @@ bwd_dqk_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __rest
   T* dkb = dk_out + (size_t)bh * d.T * dk;
   T* dgb = dg_out + (size_t)bh * d.T * dk;
   float* qdqb = qdq + (size_t)bh * d.T * dk;
+  const float* dAb = dAg + (size_t)bh * d.T * C;
   const int nc = (int)(d.L / C);
   const int nslab = dv / kSlab + (dv % kSlab ? 1 : 0);
 
@@ -403,7 +459,9 @@ bwd_dqk_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __rest
       }
       bl[ii] = expf(b);
     }
-    for (int e = threadIdx.x; e < C * ldA; e += kThreads) As[e] = 0.f;
+    // the chunk's dA (bwd_dA_kernel)
+    for (int e = threadIdx.x; e < C * C; e += kThreads)
+      As[(e / C) * ldA + e % C] = dAb[(size_t)t0 * C + e];
     for (int e = threadIdx.x; e < C * kKB; e += kThreads) acc[e] = 0.f;
     for (int sl = 0; sl < nslab; ++sl) {
       const int j0 = sl * kSlab;
@@ -416,30 +474,6 @@ bwd_dqk_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __rest
         Vs[e] = in ? ld(vb + (size_t)(t0 + t) * dv + j0 + jj) : 0.f;
       }
       __syncthreads();
-      // dA[t][s] += do_t . v_s  (s <= t)
-      {
-        const int nb = C / 4;
-        for (int e = threadIdx.x; e < nb * nb; e += kThreads) {
-          const int tb = e / nb, sb = e % nb;
-          if (sb > tb) continue;
-          float a4[4][4] = {};
-          for (int jj = 0; jj < w; ++jj) {
-            float a[4], b[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) a[u] = Os[(tb * 4 + u) * kSlab + jj];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) b[u] = Vs[(sb * 4 + u) * kSlab + jj];
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-#pragma unroll
-              for (int x = 0; x < 4; ++x) a4[u][x] = fmaf(a[u], b[x], a4[u][x]);
-          }
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-#pragma unroll
-            for (int x = 0; x < 4; ++x) As[(tb * 4 + u) * ldA + sb * 4 + x] += a4[u][x];
-        }
-      }
       // acc[t][ii] += do_t . S[ii, slab]
       for (int e = threadIdx.x; e < C * kKB; e += kThreads) {
         const int t = e / kKB, ii = e % kKB;
@@ -491,7 +525,8 @@ bwd_dqk_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __rest
       }
       bl[ii] = expf(b);
     }
-    for (int e = threadIdx.x; e < C * ldA; e += kThreads) As[e] = 0.f;
+    for (int e = threadIdx.x; e < C * C; e += kThreads)
+      As[(e / C) * ldA + e % C] = dAb[(size_t)t0 * C + e];
     for (int e = threadIdx.x; e < C * kKB; e += kThreads) acc[e] = 0.f;
     __syncthreads();
     for (int e = threadIdx.x; e < kKB * dv; e += kThreads) Ss[e] *= bl[e / dv];
@@ -506,29 +541,6 @@ bwd_dqk_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __rest
         Vs[e] = in ? ld(vb + (size_t)(t0 + t) * dv + j0 + jj) : 0.f;
       }
       __syncthreads();
-      {
-        const int nb = C / 4;
-        for (int e = threadIdx.x; e < nb * nb; e += kThreads) {
-          const int tb = e / nb, sb = e % nb;
-          if (sb > tb) continue;
-          float a4[4][4] = {};
-          for (int jj = 0; jj < w; ++jj) {
-            float a[4], b[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) a[u] = Os[(tb * 4 + u) * kSlab + jj];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) b[u] = Vs[(sb * 4 + u) * kSlab + jj];
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-#pragma unroll
-              for (int x = 0; x < 4; ++x) a4[u][x] = fmaf(a[u], b[x], a4[u][x]);
-          }
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-#pragma unroll
-            for (int x = 0; x < 4; ++x) As[(tb * 4 + u) * ldA + sb * 4 + x] += a4[u][x];
-        }
-      }
       // acc[s][ii] += v_s . (e^{b_last} dS)[ii, slab]
       for (int e = threadIdx.x; e < C * kKB; e += kThreads) {
         const int s = e / kKB, ii = e % kKB;
@@ -578,6 +590,35 @@ size_t dqk_smem(const Dims& d) {
   const size_t C = d.C, dv = d.dv;
   return sizeof(float) * (kKB * dv + 3 * C * kKB + 2 * C * kSlab + C * (C + 1) + 2 * kKB);
 }
+size_t dA_smem(const Dims& d) {
+  const size_t C = d.C;
+  return sizeof(float) * (2 * C * kSlab + C * (C + 1));
+}
+
+// dA [B,H,T,C] fp32 (bwd_dA_kernel), then dq, dk, dg
+template <typename T>
+cudaError_t dqk_t(const Dims& d, const T* q, const T* k, const T* v, const T* g,
+                  const float* S_in, const T* dO, T* dq, T* dk, T* dg, const float* D,
+                  const float* carry, float* qdq, float* dA, cudaStream_t st) {
+  const int sm0 = (int)dA_smem(d);
+  cudaError_t e = allow_smem(bwd_dA_kernel<T>, sm0);
+  if (e != cudaSuccess) return e;
+  prof_start(st);
+  bwd_dA_kernel<T><<<(unsigned)(d.B * d.H * d.T / d.C), kThreads, sm0, st>>>(dO, v, dA, d);
+  prof_mark("simt_bwd_dA", st);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const unsigned bhp = (unsigned)(d.B * d.H * d.P);
+  const int sm2 = (int)dqk_smem(d);
+  e = allow_smem(bwd_dqk_kernel<T>, sm2);
+  if (e != cudaSuccess) return e;
+  dim3 g3((unsigned)(d.dk / kKB), bhp);
+  prof_start(st);
+  bwd_dqk_kernel<T><<<g3, kThreads, sm2, st>>>(q, k, v, g, dO, S_in, D, carry, dA, dq, dk, dg,
+                                               qdq, d);
+  prof_mark("simt_bwd_dqk", st);
+  return cudaGetLastError();
+}
 
 template <typename T>
 cudaError_t fwd_out_t(const Dims& d, const T* q, const T* k, const T* v, const T* g,
@@ -612,7 +653,7 @@ cudaError_t forward_t(const Dims& d, const T* q, const T* k, const T* v, const T
 template <typename T>
 cudaError_t bwd_main_t(const Dims& d, const T* q, const T* k, const T* v, const T* g,
                        const float* S_in, const T* dO, T* dq, T* dk, T* dv, T* dg, float* D,
-                       float* carry, float* qdq, cudaStream_t st) {
+                       float* carry, float* qdq, float* dA, cudaStream_t st) {
   const unsigned bhp = (unsigned)(d.B * d.H * d.P);
   const int sm1 = (int)fwd_smem(d);
   cudaError_t e = allow_smem(bwd_dv_kernel<T>, sm1);
@@ -623,22 +664,14 @@ cudaError_t bwd_main_t(const Dims& d, const T* q, const T* k, const T* v, const 
   prof_mark("simt_bwd_dv", st);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const int sm2 = (int)dqk_smem(d);
-  e = allow_smem(bwd_dqk_kernel<T>, sm2);
-  if (e != cudaSuccess) return e;
-  dim3 g3((unsigned)(d.dk / kKB), bhp);
-  prof_start(st);
-  bwd_dqk_kernel<T><<<g3, kThreads, sm2, st>>>(q, k, v, g, dO, S_in, D, carry, dq, dk, dg, qdq,
-                                               d);
-  prof_mark("simt_bwd_dqk", st);
-  return cudaGetLastError();
+  return dqk_t<T>(d, q, k, v, g, S_in, dO, dq, dk, dg, D, carry, qdq, dA, st);
 }
 
 template <typename T>
 cudaError_t backward_t(const Dims& d, const T* q, const T* k, const T* v, const T* g,
                        const float* S_in, const float* gamma, const T* dO,
                        const float* dS_final, T* dq, T* dk, T* dv, T* dg, float* dS0, float* D,
-                       float* carry, float* qdq, cudaStream_t st) {
+                       float* carry, float* qdq, float* dA, cudaStream_t st) {
   const unsigned bhp = (unsigned)(d.B * d.H * d.P);
   dim3 g1((unsigned)((d.dv + 63) / 64), (unsigned)((d.dk + 63) / 64), bhp);
   prof_start(st);
@@ -648,7 +681,7 @@ cudaError_t backward_t(const Dims& d, const T* q, const T* k, const T* v, const 
   if (e != cudaSuccess) return e;
   e = launch_seg_scan_rev(d, D, S_in, gamma, dS_final, dS0, carry, st);
   if (e != cudaSuccess) return e;
-  return bwd_main_t<T>(d, q, k, v, g, S_in, dO, dq, dk, dv, dg, D, carry, qdq, st);
+  return bwd_main_t<T>(d, q, k, v, g, S_in, dO, dq, dk, dv, dg, D, carry, qdq, dA, st);
 }
 
 }  // namespace
@@ -673,17 +706,18 @@ cudaError_t simt_forward(const Dims& d, const void* q, const void* k, const void
 cudaError_t simt_backward(const Dims& d, const void* q, const void* k, const void* v,
                           const void* g, const float* S_in, const float* gamma, const void* d_o,
                           const float* dS_final, void* dq, void* dk, void* dv, void* dg,
-                          float* dS0, float* D, float* carry, float* qdq, cudaStream_t st) {
+                          float* dS0, float* D, float* carry, float* qdq, float* dA,
+                          cudaStream_t st) {
   if (d.bf16) {
     using T = __nv_bfloat16;
     return backward_t<T>(d, (const T*)q, (const T*)k, (const T*)v, (const T*)g, S_in, gamma,
                          (const T*)d_o, dS_final, (T*)dq, (T*)dk, (T*)dv, (T*)dg, dS0, D, carry,
-                         qdq, st);
+                         qdq, dA, st);
   }
   using T = float;
   return backward_t<T>(d, (const T*)q, (const T*)k, (const T*)v, (const T*)g, S_in, gamma,
                        (const T*)d_o, dS_final, (T*)dq, (T*)dk, (T*)dv, (T*)dg, dS0, D, carry,
-                       qdq, st);
+                       qdq, dA, st);
 }
 
 // Single steps of the SIMT path (bf16 I/O), used by the tensor-core path for
@@ -697,28 +731,19 @@ cudaError_t simt_fwd_out_bf16(const Dims& d, const void* q, const void* k, const
 cudaError_t simt_bwd_main_bf16(const Dims& d, const void* q, const void* k, const void* v,
                                const void* g, const float* S_in, const void* d_o, void* dq,
                                void* dk, void* dv, void* dg, float* D, float* carry, float* qdq,
-                               cudaStream_t st) {
+                               float* dA, cudaStream_t st) {
   using T = __nv_bfloat16;
   return bwd_main_t<T>(d, (const T*)q, (const T*)k, (const T*)v, (const T*)g, S_in,
-                       (const T*)d_o, (T*)dq, (T*)dk, (T*)dv, (T*)dg, D, carry, qdq, st);
+                       (const T*)d_o, (T*)dq, (T*)dk, (T*)dv, (T*)dg, D, carry, qdq, dA, st);
 }
 
 cudaError_t simt_bwd_dqk_bf16(const Dims& d, const void* q, const void* k, const void* v,
                               const void* g, const float* S_in, const void* d_o, void* dq,
-                              void* dk, void* dg, float* D, float* carry, float* qdq,
+                              void* dk, void* dg, float* D, float* carry, float* qdq, float* dA,
                               cudaStream_t st) {
   using T = __nv_bfloat16;
-  const unsigned bhp = (unsigned)(d.B * d.H * d.P);
-  const int sm2 = (int)dqk_smem(d);
-  cudaError_t e = allow_smem(bwd_dqk_kernel<T>, sm2);
-  if (e != cudaSuccess) return e;
-  dim3 g3((unsigned)(d.dk / kKB), bhp);
-  prof_start(st);
-  bwd_dqk_kernel<T><<<g3, kThreads, sm2, st>>>((const T*)q, (const T*)k, (const T*)v,
-                                               (const T*)g, (const T*)d_o, S_in, D, carry,
-                                               (T*)dq, (T*)dk, (T*)dg, qdq, d);
-  prof_mark("simt_bwd_dqk", st);
-  return cudaGetLastError();
+  return dqk_t<T>(d, (const T*)q, (const T*)k, (const T*)v, (const T*)g, S_in, (const T*)d_o,
+                  (T*)dq, (T*)dk, (T*)dg, D, carry, qdq, dA, st);
 }
 
 }  // namespace zeco

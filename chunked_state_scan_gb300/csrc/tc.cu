@@ -85,14 +85,14 @@ cudaError_t tc_forward(const Dims& d, const void* q, const void* k, const void* 
 cudaError_t tc_backward(const Dims& d, const void* q, const void* k, const void* v,
                         const void* g, const float* S_in, const float* gamma, const void* d_o,
                         const float* dS_final, void* dq, void* dk, void* dv, void* dg,
-                        float* dS0, float* D, float* carry, float* qdq, const TcOps& ops,
-                        cudaStream_t st) {
+                        float* dS0, float* D, float* carry, float* qdq, float* dAf,
+                        const TcOps& ops, cudaStream_t st) {
   if (!tc_fwd_supported(d)) {
     cudaError_t e = tc_dstate_local(d, q, d_o, g, nullptr, nullptr, D, st);
     if (e != cudaSuccess) return e;
     e = launch_seg_scan_rev(d, D, S_in, gamma, dS_final, dS0, carry, st);
     if (e != cudaSuccess) return e;
-    return simt_bwd_main_bf16(d, q, k, v, g, S_in, d_o, dq, dk, dv, dg, D, carry, qdq, st);
+    return simt_bwd_main_bf16(d, q, k, v, g, S_in, d_o, dq, dk, dv, dg, D, carry, qdq, dAf, st);
   }
   const void* Qt = ops.Qt;
   const void* Kt = ops.Kt;
@@ -123,7 +123,7 @@ cudaError_t tc_backward(const Dims& d, const void* q, const void* k, const void*
   }
   if (e != cudaSuccess) return e;
   if (qk_tc) return tc_bwd_qk(d, Qt, Kt, v, g, Eb, dA, S_in, d_o, dq, dk, dg, D, carry, qdq, st);
-  return simt_bwd_dqk_bf16(d, q, k, v, g, S_in, d_o, dq, dk, dg, D, carry, qdq, st);
+  return simt_bwd_dqk_bf16(d, q, k, v, g, S_in, d_o, dq, dk, dg, D, carry, qdq, dAf, st);
 }
 
 }  // namespace zeco

@@ -148,7 +148,8 @@ size_t zeco_gla_saved_bytes(const zeco_shape *shape);
  * and q .* dq in fp32 [B,H,T,dk] (dlog_alpha is a long suffix sum of
  * q .* dq - k .* dk that cancels heavily, so its terms are kept in fp32).
  * On the tensor-core path the backward also holds the masked gradient of the
- * intra-chunk scores dA = do v^T [B,H,T,64] bf16.  Where the kernels read the
+ * intra-chunk scores dA = do v^T [B,H,T,64] bf16; where the dq/dk step runs on
+ * CUDA cores (the SIMT path, and C != 64) it holds dA [B,H,T,C] fp32 instead.  Where the kernels read the
  * SCALAR / NONE decay forms in their own layout (see zeco_decay), SCALAR's
  * backward adds the fp32 partial sums of its gradient [dk/32][B,H,T] and NONE
  * adds nothing; elsewhere both forms add the log-decay broadcast to

@@ -69,12 +69,14 @@ def test_sizes_follow_the_layout(lib):
     # gradient too, in the backward)
     bc = 4 * (1 << 20) * 256 * 2
     assert z.workspace_bytes(_shape(decay="scalar", path="simt"), False) == bc
-    assert z.workspace_bytes(_shape(decay="scalar", C=128), False) == bc
+    assert z.workspace_bytes(_shape(decay="scalar", C=128, dk=128, dv=128, K=4), False) == bc // 2
     # the SIMT path keeps no decay-weighted operands
     simt = _shape(path="simt", dtype="f32", dk=64, dv=64)
     st64 = 4 * 65 * 64 * 64 * 4
     assert z.workspace_bytes(simt, False) == 0
-    assert z.workspace_bytes(simt, True) == st64 + 4 * 64 * 64 * 4 + 4 * (1 << 20) * 64 * 4
+    # (+ the CUDA-core dq/dk kernel's intra-chunk dA [B,H,T,C] fp32)
+    assert z.workspace_bytes(simt, True) == (st64 + 4 * 64 * 64 * 4 + 4 * (1 << 20) * 64 * 4
+                                             + 4 * (1 << 20) * 64 * 4)
 
 
 @pytest.mark.parametrize("kw,code", [
@@ -127,6 +129,12 @@ def test_path_resolution(lib):
     # fp32 at full width does not fit the SIMT kernels' shared memory with C=128
     with pytest.raises(z.ZecoError):
         z.resolve_path(_shape(dtype="f32", C=128, path="simt"))
+    # nor does bf16: C = 128 takes the tensor-core segment states but the CUDA-core
+    # sweeps, so d_k = 256 fits neither path; d_k = 128, d_v = 128 fits
+    for path in ("tc", "auto"):
+        with pytest.raises(z.ZecoError):
+            z.resolve_path(_shape(C=128, path=path))
+    assert z.resolve_path(_shape(C=128, dk=128, dv=128, K=4)) == "tc"
 
 
 def test_decay_forms_workspace_and_arguments(lib):
