@@ -479,7 +479,7 @@ def measure(w, args, world, rank, local, want_e2e=True, want_cpu=True, quiet=Fal
     try:
         prof = [profile_step(lib, step, dev) for _ in range(2)]
     finally:
-        lib.zeco_set_overlap(1)
+        lib.zeco_set_overlap(z.OVERLAP_DEFAULT)
     per_kernel = {}
     for run in prof:
         for n, a, b in run:
@@ -502,32 +502,36 @@ def measure(w, args, world, rank, local, want_e2e=True, want_cpu=True, quiet=Fal
     value, ms_step = aggregate(elapsed_max, w.tokens, args.steps, world)
 
     # ---- the other schedules of the work beside the scan (zeco_set_overlap):
-    #      0 = one stream, 2 = the scan on a second stream beside the diagonal
-    #      attention (the pages' schedule); the instrument for each
+    #      0 = one stream, 1 = the score passes on a second stream, 2 = the scan on
+    #      a second stream beside the diagonal attention (the pages' schedule), 3 =
+    #      pass 2 per block of segments; the default (4) is the timed region above.
+    #      The Eq. 11 instrument for each
     overlap = None
     if path == "tc":
         modes = {}
         try:
-            for mode in (0, 2, 3, 1):
+            for mode in (0, 1, 2, 3, z.OVERLAP_DEFAULT):
                 lib.zeco_set_overlap(mode)
                 step()
                 torch.cuda.synchronize(dev)
                 modes[mode] = (timed_steps(args.steps) / args.steps, profile_step(lib, step, dev))
         finally:
-            lib.zeco_set_overlap(1)
+            lib.zeco_set_overlap(z.OVERLAP_DEFAULT)
+        names = {0: "mode0_one_stream", 1: "mode1_aux_scores", 2: "mode2_aux_scan",
+                 3: "mode3_pass2_per_segment_block", 4: "mode4_default_dqk_beside_dv"}
+        step_ms = {names[m]: modes[m][0] for m in (0, 1, 2, 3)}
+        step_ms[names[4]] = ms_step
         overlap = {
-            "step_ms": {"mode1_aux_scores": ms_step, "mode2_aux_scan": modes[2][0],
-                        "mode3_pass2_per_segment_block": modes[3][0],
-                        "mode0_one_stream": modes[0][0]},
-            "scan_not_overlapped": {"mode1_aux_scores": scan_overlap(modes[1][1]),
-                                    "mode2_aux_scan": scan_overlap(modes[2][1]),
-                                    "mode3_pass2_per_segment_block": scan_overlap(modes[3][1])},
-            "note": "mode 1 (default): scores A / dA on a second stream beside pass 1, the "
-                    "scans (and the dv sweep); mode 2: the segment scans on a second stream "
-                    "beside the A / dA pass; mode 3: the forward scan in blocks of segments, "
-                    "pass 2 of each block on the second stream as soon as its block is "
-                    "scanned; non_overlapped_frac = share of the scan's kernel time with no "
-                    "A / dA kernel running (Eq. 11 instrument)"}
+            "step_ms": step_ms,
+            "scan_not_overlapped": {names[m]: scan_overlap(modes[m][1]) for m in (1, 2, 3, 4)},
+            "note": "mode 4 (default, the timed region): mode 1, and in the backward the dq/dk "
+                    "sweeps on a high-priority stream beside the dv sweep; mode 1: scores A / "
+                    "dA on a second stream beside pass 1, the scans (and the dv sweep); mode "
+                    "2: the segment scans on a second stream beside the A / dA pass; mode 3: "
+                    "the forward scan in blocks of segments, pass 2 of each block on the "
+                    "second stream as soon as its block is scanned; non_overlapped_frac = "
+                    "share of the scan's kernel time with no A / dA kernel running (Eq. 11 "
+                    "instrument)"}
 
     # ---- roofline of the dominant kernel and of the whole step
     peaks, peak_kind = load_peaks()
@@ -738,7 +742,7 @@ def scan_sweep(args, local):
         try:
             runs = [profile_step(lib, step, dev) for _ in range(3)]
         finally:
-            lib.zeco_set_overlap(1)
+            lib.zeco_set_overlap(z.OVERLAP_DEFAULT)
         kb = kernel_bytes_per_token(w.dk, w.dv, w.L)
         res = {"P": P, "L": w.L}
         for name in ("seg_scan_fwd", "seg_scan_rev"):
@@ -803,7 +807,7 @@ def decay_forms(args, local):
         try:
             runs = [profile_step(lib, step, dev) for _ in range(3)]
         finally:
-            lib.zeco_set_overlap(1)
+            lib.zeco_set_overlap(z.OVERLAP_DEFAULT)
         kms = {}
         for r in runs:
             for n, a, b in r:

@@ -20,6 +20,7 @@ LIB_PATH = os.path.join(_HERE, "_build", "libzeco_gla.so")
 
 ZECO_OK, ZECO_ERR_ARG, ZECO_ERR_UNSUPPORTED, ZECO_ERR_WORKSPACE, ZECO_ERR_CUDA = 0, -1, -2, -3, -4
 ZECO_ERR_TIMEOUT = -5
+OVERLAP_DEFAULT = 4  # ZECO_OVERLAP_DEFAULT
 ZECO_F32, ZECO_BF16 = 0, 1
 PATH_AUTO, PATH_SIMT, PATH_TC = 0, 1, 2
 _PATHS = {"auto": PATH_AUTO, "simt": PATH_SIMT, "tc": PATH_TC}
@@ -155,9 +156,11 @@ def selftest_bounded_wait(stream=None) -> None:
 
 
 def set_overlap(mode: int) -> None:
-    """Schedule of the work beside the segment scan: 1 (default) the
-    scan-independent score passes on a second stream, 2 the segment scan on a
-    second stream beside them (the pages' schedule), 0 everything on one stream."""
+    """Schedule of the work beside the segment scan: 1 the scan-independent score
+    passes on a second stream, 2 the segment scan on a second stream beside them
+    (the pages' schedule), 3 (forward) pass 2 per block of segments as soon as the
+    scan reaches it, 4 (OVERLAP_DEFAULT) mode 1 plus the dq/dk sweeps on a
+    high-priority stream beside the dv sweep, 0 everything on one stream."""
     _check(load_library().zeco_set_overlap(int(mode)))
 
 

@@ -10,6 +10,7 @@ namespace zeco {
 // ---- auxiliary stream for the scan-independent passes (overlap.cu) -----
 struct Fork {
   cudaStream_t aux;   // where the forked kernels go (the caller's stream when off)
+  cudaStream_t hi;    // a second one at the highest priority (the caller's when off)
   cudaEvent_t ev[2];  // recorded on aux by fork_mark, waited on by fork_join
   cudaEvent_t* step;  // recorded on the caller's stream by fork_follow
   bool on;

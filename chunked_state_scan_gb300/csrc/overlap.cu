@@ -15,10 +15,14 @@
 //     caller's stream;
 //   3 (forward): pass 2 of each block of segments starts as soon as the scan has
 //     produced that block's incoming states (the scan runs block by block on the
-//     caller's stream, pass 2 of each block on the auxiliary stream).
-// The caller's stream forks to the auxiliary stream with an event and joins it
-// with another before the first kernel that needs the forked work, so the call
-// stays ordered on the caller's stream (and capturable into a CUDA graph).
+//     caller's stream, pass 2 of each block on the auxiliary stream);
+//   4 (default): mode 1, and in the backward the dq/dk sweeps on a second
+//     auxiliary stream of the highest priority while the dv sweep runs on the
+//     caller's: the two are independent, so the dv sweep's CTAs take the SMs
+//     that the dq/dk sweeps' last waves leave idle.
+// The caller's stream forks to the auxiliary streams with events and joins them
+// with others before the first kernel that needs the forked work, so the call
+// stays ordered on the caller's stream.
 //
 // The auxiliary stream and its events are created on first use, once per host
 // thread and device, and live until the thread exits.  zeco_set_overlap(0)
@@ -36,6 +40,7 @@ constexpr int kEvents = 3 + kStepEvents;
 
 struct AuxState {
   cudaStream_t stream = nullptr;
+  cudaStream_t hi = nullptr;  // the device's highest stream priority
   cudaEvent_t ev[kEvents] = {};
   bool ok = false;
   bool tried = false;
@@ -48,11 +53,12 @@ struct ThreadAux {
       if (!a.ok) continue;
       for (auto& e : a.ev) cudaEventDestroy(e);
       cudaStreamDestroy(a.stream);
+      cudaStreamDestroy(a.hi);
     }
   }
 };
 
-std::atomic<int> g_overlap{1};
+std::atomic<int> g_overlap{ZECO_OVERLAP_DEFAULT};
 thread_local ThreadAux t_aux;
 
 AuxState* aux_for_current_device() {
@@ -61,7 +67,10 @@ AuxState* aux_for_current_device() {
   AuxState& a = t_aux.dev[d];
   if (!a.tried) {
     a.tried = true;
-    bool ok = cudaStreamCreateWithFlags(&a.stream, cudaStreamNonBlocking) == cudaSuccess;
+    int lo_pri = 0, hi_pri = 0;
+    bool ok = cudaStreamCreateWithFlags(&a.stream, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaDeviceGetStreamPriorityRange(&lo_pri, &hi_pri) == cudaSuccess &&
+              cudaStreamCreateWithPriority(&a.hi, cudaStreamNonBlocking, hi_pri) == cudaSuccess;
     for (int i = 0; ok && i < kEvents; ++i)
       ok = cudaEventCreateWithFlags(&a.ev[i], cudaEventDisableTiming) == cudaSuccess;
     a.ok = ok;
@@ -76,6 +85,7 @@ int overlap_mode() { return g_overlap.load(std::memory_order_relaxed); }
 Fork fork_begin(cudaStream_t st) {
   Fork f;
   f.aux = st;
+  f.hi = st;
   f.step = nullptr;
   f.on = false;
   if (!g_overlap.load(std::memory_order_relaxed)) return f;
@@ -84,6 +94,7 @@ Fork fork_begin(cudaStream_t st) {
   if (cudaEventRecord(a->ev[0], st) != cudaSuccess) return f;
   if (cudaStreamWaitEvent(a->stream, a->ev[0], 0) != cudaSuccess) return f;
   f.aux = a->stream;
+  f.hi = a->hi;
   f.ev[0] = a->ev[1];
   f.ev[1] = a->ev[2];
   f.step = a->ev + 3;
@@ -108,7 +119,7 @@ cudaError_t fork_follow(const Fork& f, cudaStream_t st, int i) {
 }  // namespace zeco
 
 extern "C" int zeco_set_overlap(int mode) {
-  if (mode < 0 || mode > 3) return ZECO_ERR_ARG;
+  if (mode < 0 || mode > 4) return ZECO_ERR_ARG;
   zeco::g_overlap.store(mode, std::memory_order_relaxed);
   return ZECO_OK;
 }

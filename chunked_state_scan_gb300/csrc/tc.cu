@@ -101,6 +101,26 @@ cudaError_t tc_backward(const Dims& d, const void* q, const void* k, const void*
   const bool qk_tc = tc_uses_dA(d);
   void* dA = ops.dA;
   cudaError_t e = cudaSuccess;
+  if (overlap_mode() == 4 && qk_tc) {
+    // dq/dk on a high-priority stream, dv on the caller's: the dq/dk CTAs are
+    // scheduled first and the dv sweep's fill the SMs their last waves leave idle
+    const Fork f = fork_begin(st);
+    e = tc_dA(d, d_o, v, dA, f.aux);
+    if (e == cudaSuccess) e = fork_mark(f, 0);
+    if (e == cudaSuccess) e = tc_dstate_local(d, q, d_o, g, Qt, Eb, D, st);
+    if (e == cudaSuccess) e = launch_seg_scan_rev(d, D, S_in, gamma, dS_final, dS0, carry, st);
+    if (e == cudaSuccess && f.on) {
+      e = cudaEventRecord(f.step[0], st);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(f.hi, f.step[0], 0);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(f.hi, f.ev[0], 0);
+    }
+    if (e == cudaSuccess)
+      e = tc_bwd_qk(d, Qt, Kt, v, g, Eb, dA, S_in, d_o, dq, dk, dg, D, carry, qdq, f.hi);
+    if (e == cudaSuccess && f.on) e = cudaEventRecord(f.ev[1], f.hi);
+    if (e == cudaSuccess) e = tc_bwd_dv(d, Qt, Kt, d_o, A, Eb, D, dv, st);
+    if (e == cudaSuccess && f.on) e = cudaStreamWaitEvent(st, f.ev[1], 0);
+    return e;
+  }
   if (overlap_mode() == 2) {
     // the pages' schedule: the reverse scan on the second stream beside dA
     e = tc_dstate_local(d, q, d_o, g, Qt, Eb, D, st);

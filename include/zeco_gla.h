@@ -287,8 +287,8 @@ const char *zeco_profile_kernel_name(int i);
  * Eq. 11).  On the tensor-core path the passes that build the intra-chunk
  * scores A (forward) and their gradient dA (backward) do not depend on the
  * segment scan.
- *   mode 1 (default): A and dA run on an auxiliary stream as soon as their
- *     inputs exist, concurrently with the segment-state pass and the scan (and,
+ *   mode 1: A and dA run on an auxiliary stream as soon as their inputs
+ *     exist, concurrently with the segment-state pass and the scan (and,
  *     backward, the dv sweep);
  *   mode 2 (the pages' schedule): the segment scan (forward and reverse) runs
  *     on the auxiliary stream, concurrently with the A (dA) pass on `stream`;
@@ -296,14 +296,19 @@ const char *zeco_profile_kernel_name(int i);
  *     segments starts as soon as the scan has produced that block's incoming
  *     states -- the scan runs block by block on `stream`, pass 2 of each block
  *     on the auxiliary stream after the A pass and after its block's scan;
+ *   mode 4 (ZECO_OVERLAP_DEFAULT): mode 1, and in the backward the dq/dk sweeps
+ *     run on a second auxiliary stream created at the device's highest stream
+ *     priority while the dv sweep runs on `stream`: the two do not depend on
+ *     each other, and the dv sweep's CTAs take the SMs that the last waves of
+ *     the dq/dk sweeps leave idle;
  *   mode 0: everything on `stream`.
  * The call forks from and joins back into its `stream` with events, so all its
- * work stays ordered on `stream` and it can be captured into a CUDA graph.
- * Results are identical in every mode.  The auxiliary stream and eleven events
- * are created on the first such call of each host thread on each device and
- * destroyed when the thread exits.  Process-wide; returns ZECO_OK, or
- * ZECO_ERR_ARG for a mode outside 0..3.
+ * work stays ordered on `stream`.  Results are identical in every mode.  The
+ * auxiliary streams and eleven events are created on the first such call of
+ * each host thread on each device and destroyed when the thread exits.
+ * Process-wide; returns ZECO_OK, or ZECO_ERR_ARG for a mode outside 0..4.
  */
+#define ZECO_OVERLAP_DEFAULT 4
 int zeco_set_overlap(int mode);
 
 /* The path zeco_gla_fwd / zeco_gla_bwd would run for this shape

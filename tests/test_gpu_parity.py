@@ -166,12 +166,13 @@ def test_bf16_odd_chunk_counts_in_the_dq_dk_sweeps(z, B, H, T, dk, P, K):
     _assert(errs, "bf16", f"tc odd chunks B{B} H{H} T{T} dk{dk} P{P}")
 
 
-@pytest.mark.parametrize("mode", [0, 2, 3])
+@pytest.mark.parametrize("mode", [0, 1, 2, 3])
 def test_overlap_schedules_give_identical_results(z, mode):
-    # the scan-independent passes on a second stream (mode 1, the default), the
-    # scan on a second stream (mode 2), pass 2 per block of segments as soon as
-    # the scan reaches it (mode 3) or all on one stream (mode 0): the same
-    # kernels on the same inputs, so bit-identical outputs
+    # the default (mode 4: mode 1 plus the dq/dk sweeps on a high-priority
+    # stream beside the dv sweep), the scan-independent passes on a second
+    # stream (mode 1), the scan on a second stream (mode 2), pass 2 per block
+    # of segments as soon as the scan reaches it (mode 3) or all on one stream
+    # (mode 0): the same kernels on the same inputs, so bit-identical outputs
     w = workloads.LONG_FWDBWD.replace(T=16384, P=4)
     x = workloads.make_inputs(w)
     lib = z.load_library()
@@ -180,7 +181,7 @@ def test_overlap_schedules_give_identical_results(z, mode):
     try:
         b = parity.run_gpu(z, x, w.P, w.K, w.C)
     finally:
-        lib.zeco_set_overlap(1)
+        lib.zeco_set_overlap(z.OVERLAP_DEFAULT)
     for n in ("o", "S_final", "dq", "dk", "dv", "dlog_alpha", "dS0"):
         assert torch.equal(a[n], b[n]), n
 
