@@ -713,7 +713,7 @@ def measure(w, args, world, rank, local, want_e2e=True, want_cpu=True, quiet=Fal
 
 def scan_sweep(args, local):
     """The segment scans at many segments (``--scan-sweep``): the 1M-token workload's
-    inputs with P in {64, 1024, 4096, T/(2C)}; each scan's time and bytes/s."""
+    inputs with P in {64, 1024, 4096, 8192, T/C}; each scan's time and bytes/s."""
     import chunked_state_scan_gb300 as z
     lib = z.load_library()
     dev = torch.device("cuda", local)
@@ -721,8 +721,7 @@ def scan_sweep(args, local):
     base = workloads.LONG_FWDBWD
     x = workloads.make_inputs(base, device=dev)
     out = []
-    # (B*H*P is capped at 65535 by the grid; P = T/C = 16384 with 4 heads is one over)
-    for P in (64, 1024, 4096, base.T // (2 * base.C)):
+    for P in (64, 1024, 4096, 8192, base.T // base.C):
         w = base.replace(P=P, name=f"scan_sweep_P{P}")
         stream = torch.cuda.Stream(device=dev)
         shape = z.make_shape(w.B, w.H, w.T, w.dk, w.dv, w.P, w.K, w.C, w.dtype)
@@ -843,7 +842,7 @@ def main(argv=None):
                     help="one JSON line per secondary workload (GLA-1B layer fwd, "
                          "8-segment fwd, batched fwd+bwd) instead of the headline")
     ap.add_argument("--scan-sweep", action="store_true",
-                    help="time the segment scans at P in {64, 1024, 4096, T/(2C)}")
+                    help="time the segment scans at P in {64, 1024, 4096, 8192, T/C}")
     ap.add_argument("--forms", action="store_true",
                     help="time the headline step in the diagonal, scalar and no-decay forms")
     args = ap.parse_args(argv)

@@ -22,6 +22,10 @@ thread_local ProfState g_prof;
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
+// Largest B*H*P_eff: the kernels launch at most 32 blocks per (b, h, segment) along
+// grid x, whose limit is 2^31 - 1 blocks.
+constexpr int64_t kMaxBHP = ((1LL << 31) - 1) / 32;
+
 // Shape checks.  Returns ZECO_OK and fills d, or an error code.
 int check_shape(const zeco_shape* s, Dims* d) {
   if (!s) return ZECO_ERR_ARG;
@@ -37,7 +41,9 @@ int check_shape(const zeco_shape* s, Dims* d) {
   if (s->C != 16 && s->C != 32 && s->C != 64 && s->C != 128) return ZECO_ERR_UNSUPPORTED;
   if (s->dk % 16 != 0 || s->dk > 256) return ZECO_ERR_UNSUPPORTED;
   if (s->dv % 32 != 0 || s->dv > 512) return ZECO_ERR_UNSUPPORTED;
-  if (s->B * s->H * s->P > 65535LL) return ZECO_ERR_UNSUPPORTED;  // grid y/z limit
+  // grid limits: the segment scans put B*H on grid z (at most 65,535 blocks); every
+  // other kernel puts (b, h, segment) times at most 32 tiles on grid x (2^31 - 1)
+  if (s->B * s->H > 65535LL || s->B * s->H * s->P > kMaxBHP) return ZECO_ERR_UNSUPPORTED;
   d->B = s->B;
   d->H = s->H;
   d->T = s->T;
@@ -59,7 +65,7 @@ int check_shape(const zeco_shape* s, Dims* d) {
   const int64_t tiles = (s->dv + 127) / 128;
   int64_t m = 1;
   while (s->B * s->H * s->P * m * tiles < kWave && m < 64 && s->T % (s->P * m * 2 * s->C) == 0 &&
-         s->T / (s->P * m * 2) >= 4 * (int64_t)s->C && s->B * s->H * s->P * m * 2 <= 65535)
+         s->T / (s->P * m * 2) >= 4 * (int64_t)s->C && s->B * s->H * s->P * m * 2 <= kMaxBHP)
     m *= 2;
   d->P = (int)(s->P * m);
   d->L = s->T / d->P;

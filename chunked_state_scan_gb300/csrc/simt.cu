@@ -47,9 +47,13 @@ seg_state_kernel(const T* __restrict__ X, const T* __restrict__ Y, const T* __re
   __shared__ float Ys[kTB][64];
   __shared__ float run[64];
   const int tid = threadIdx.x;
-  const int64_t bh = blockIdx.z / d.P;
-  const int p = blockIdx.z % d.P;
-  const int i0 = blockIdx.y * 64, j0 = blockIdx.x * 64;
+  // block x = ((b h p) * d_k tiles + d_k tile) * d_v tiles + d_v tile
+  const int nx = (int)((d.dv + 63) / 64), ny = (int)((d.dk + 63) / 64);
+  const int bx = (int)(blockIdx.x % nx), by = (int)((blockIdx.x / nx) % ny);
+  const int64_t bhp = (int64_t)(blockIdx.x / nx) / ny;
+  const int64_t bh = bhp / d.P;
+  const int p = (int)(bhp % d.P);
+  const int i0 = by * 64, j0 = bx * 64;
   const int tx = tid % 16, ty = tid / 16;
   const int64_t seg0 = (int64_t)p * d.L;
   const T* Xb = X + (size_t)bh * d.T * d.dk;
@@ -110,7 +114,7 @@ seg_state_kernel(const T* __restrict__ X, const T* __restrict__ Y, const T* __re
       if (j < d.dv) ob[(size_t)i * d.dv + j] = acc[u][w];
     }
   }
-  if (REV && gamma && blockIdx.x == 0 && tid < 64 && i0 + tid < d.dk)
+  if (REV && gamma && bx == 0 && tid < 64 && i0 + tid < d.dk)
     gamma[((size_t)bh * d.P + p) * d.dk + i0 + tid] = expf(run[tid]);
 }
 
@@ -176,9 +180,11 @@ fwd_out_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __rest
   float* Vs = Ss + dk * kNV;   // [C][kNV]
   float* As = Vs + C * kNV;    // [C][C+1]
   float* bl = As + C * ldA;    // [dk]
-  const int64_t bh = blockIdx.y / d.P;
-  const int p = blockIdx.y % d.P;
-  const int j0 = blockIdx.x * kNV;
+  // block x = (b h p) * (d_v / kNV) + d_v tile
+  const int64_t bhp = (int64_t)(blockIdx.x / (d.dv / kNV));
+  const int64_t bh = bhp / d.P;
+  const int p = (int)(bhp % d.P);
+  const int j0 = (int)(blockIdx.x % (d.dv / kNV)) * kNV;
   const T* qb = q + (size_t)bh * d.T * dk;
   const T* kb = k + (size_t)bh * d.T * dk;
   const T* gb = g + (size_t)bh * d.T * dk;
@@ -270,9 +276,11 @@ bwd_dv_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restr
   float* Os = Ss + dk * kNV;  // do tile [C][kNV]
   float* As = Os + C * kNV;
   float* bl = As + C * ldA;
-  const int64_t bh = blockIdx.y / d.P;
-  const int p = blockIdx.y % d.P;
-  const int j0 = blockIdx.x * kNV;
+  // block x = (b h p) * (d_v / kNV) + d_v tile
+  const int64_t bhp = (int64_t)(blockIdx.x / (d.dv / kNV));
+  const int64_t bh = bhp / d.P;
+  const int p = (int)(bhp % d.P);
+  const int j0 = (int)(blockIdx.x % (d.dv / kNV)) * kNV;
   const T* qb = q + (size_t)bh * d.T * dk;
   const T* kb = k + (size_t)bh * d.T * dk;
   const T* gb = g + (size_t)bh * d.T * dk;
@@ -423,9 +431,11 @@ bwd_dqk_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __rest
   float* As = Vs + C * kSlab;      // [C][C+1]
   float* bl = As + C * ldA;        // [kKB]
   float* run = bl + kKB;           // [kKB]
-  const int64_t bh = blockIdx.y / d.P;
-  const int p = blockIdx.y % d.P;
-  const int i0 = blockIdx.x * kKB;
+  // block x = (b h p) * (d_k / kKB) + d_k tile
+  const int64_t bhp = (int64_t)(blockIdx.x / (d.dk / kKB));
+  const int64_t bh = bhp / d.P;
+  const int p = (int)(bhp % d.P);
+  const int i0 = (int)(blockIdx.x % (d.dk / kKB)) * kKB;
   const T* qb = q + (size_t)bh * d.T * dk;
   const T* kb = k + (size_t)bh * d.T * dk;
   const T* gb = g + (size_t)bh * d.T * dk;
@@ -608,11 +618,11 @@ cudaError_t dqk_t(const Dims& d, const T* q, const T* k, const T* v, const T* g,
   prof_mark("simt_bwd_dA", st);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const unsigned bhp = (unsigned)(d.B * d.H * d.P);
+  const int64_t bhp = d.B * d.H * d.P;
   const int sm2 = (int)dqk_smem(d);
   e = allow_smem(bwd_dqk_kernel<T>, sm2);
   if (e != cudaSuccess) return e;
-  dim3 g3((unsigned)(d.dk / kKB), bhp);
+  const unsigned g3 = (unsigned)(bhp * (d.dk / kKB));
   prof_start(st);
   bwd_dqk_kernel<T><<<g3, kThreads, sm2, st>>>(q, k, v, g, dO, S_in, D, carry, dA, dq, dk, dg,
                                                qdq, d);
@@ -623,11 +633,11 @@ cudaError_t dqk_t(const Dims& d, const T* q, const T* k, const T* v, const T* g,
 template <typename T>
 cudaError_t fwd_out_t(const Dims& d, const T* q, const T* k, const T* v, const T* g,
                       const float* S_in, T* o, cudaStream_t st) {
-  const unsigned bhp = (unsigned)(d.B * d.H * d.P);
+  const int64_t bhp = d.B * d.H * d.P;
   const int sm = (int)fwd_smem(d);
   cudaError_t e = allow_smem(fwd_out_kernel<T>, sm);
   if (e != cudaSuccess) return e;
-  dim3 g2((unsigned)(d.dv / kNV), bhp);
+  const unsigned g2 = (unsigned)(bhp * (d.dv / kNV));
   prof_start(st);
   fwd_out_kernel<T><<<g2, kThreads, sm, st>>>(q, k, v, g, S_in, o, d);
   prof_mark("simt_fwd_out", st);
@@ -638,8 +648,8 @@ template <typename T>
 cudaError_t forward_t(const Dims& d, const T* q, const T* k, const T* v, const T* g,
                       const float* S0, T* o, float* S_final, float* S_in, float* gamma,
                       cudaStream_t st) {
-  const unsigned bhp = (unsigned)(d.B * d.H * d.P);
-  dim3 g1((unsigned)((d.dv + 63) / 64), (unsigned)((d.dk + 63) / 64), bhp);
+  const int64_t bhp = d.B * d.H * d.P;
+  const unsigned g1 = (unsigned)(bhp * ((d.dv + 63) / 64) * ((d.dk + 63) / 64));
   prof_start(st);
   seg_state_kernel<T, true><<<g1, kThreads, 0, st>>>(k, v, g, S_in, gamma, d, 1);
   prof_mark("simt_chunk_state", st);
@@ -654,11 +664,11 @@ template <typename T>
 cudaError_t bwd_main_t(const Dims& d, const T* q, const T* k, const T* v, const T* g,
                        const float* S_in, const T* dO, T* dq, T* dk, T* dv, T* dg, float* D,
                        float* carry, float* qdq, float* dA, cudaStream_t st) {
-  const unsigned bhp = (unsigned)(d.B * d.H * d.P);
+  const int64_t bhp = d.B * d.H * d.P;
   const int sm1 = (int)fwd_smem(d);
   cudaError_t e = allow_smem(bwd_dv_kernel<T>, sm1);
   if (e != cudaSuccess) return e;
-  dim3 g2((unsigned)(d.dv / kNV), bhp);
+  const unsigned g2 = (unsigned)(bhp * (d.dv / kNV));
   prof_start(st);
   bwd_dv_kernel<T><<<g2, kThreads, sm1, st>>>(q, k, g, dO, D, dv, d);
   prof_mark("simt_bwd_dv", st);
@@ -672,8 +682,8 @@ cudaError_t backward_t(const Dims& d, const T* q, const T* k, const T* v, const 
                        const float* S_in, const float* gamma, const T* dO,
                        const float* dS_final, T* dq, T* dk, T* dv, T* dg, float* dS0, float* D,
                        float* carry, float* qdq, float* dA, cudaStream_t st) {
-  const unsigned bhp = (unsigned)(d.B * d.H * d.P);
-  dim3 g1((unsigned)((d.dv + 63) / 64), (unsigned)((d.dk + 63) / 64), bhp);
+  const int64_t bhp = d.B * d.H * d.P;
+  const unsigned g1 = (unsigned)(bhp * ((d.dv + 63) / 64) * ((d.dk + 63) / 64));
   prof_start(st);
   seg_state_kernel<T, false><<<g1, kThreads, 0, st>>>(q, dO, g, D, nullptr, d, 0);
   prof_mark("simt_dstate_local", st);

@@ -181,9 +181,13 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t rank = cluster_ctarank();   // which quarter of d_v; rows finished
-  const int64_t bh = blockIdx.y / P;
-  const int p = blockIdx.y % P;
-  const int i0 = (int)(blockIdx.x / kRanks) * kKB;
+  // block x = (b h p) * (kRanks d_k / kKB) + kRanks * d_k block + rank: a cluster is
+  // kRanks consecutive blocks of one (b, h, segment, d_k block)
+  const int nx = kRanks * dk / kKB;
+  const int64_t bhp = (int64_t)(blockIdx.x / nx);
+  const int64_t bh = bhp / P;
+  const int p = (int)(bhp % P);
+  const int i0 = (int)((blockIdx.x % nx) / kRanks) * kKB;
   const int j0 = (int)rank * kNB;
   const int64_t row0 = bh * T + (int64_t)p * L;
   const int nc = (int)(L / kC);
@@ -633,7 +637,7 @@ cudaError_t launch_qk(const Dims& d, const CUtensorMap& tx, const CUtensorMap& t
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(kRanks * d.dk / kKB), (unsigned)(d.B * d.H * d.P), 1);
+  cfg.gridDim = dim3((unsigned)(d.B * d.H * d.P * (kRanks * d.dk / kKB)), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = (size_t)smem;
   cfg.stream = st;

@@ -104,9 +104,13 @@ tc_sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   const int cq = warp >> 2;      // which quarter of the d_k columns this warp's state pass handles
   const int half = (warp >> 2) & 1;  // epilogue: which half of the 64 tokens (warps 0..7)
   // segments [p_begin, p_begin + p_count) of every (b, h)
-  const int64_t bh = blockIdx.y / p_count;
-  const int p = p_begin + (int)(blockIdx.y % p_count);
-  const int j0 = blockIdx.x * kNV;
+  // block x = ((b h) * p_count + segment - p_begin) * (d_v / kNV) + d_v tile
+  const int nx = dv / kNV;
+  const int bx = (int)(blockIdx.x % nx);
+  const int64_t by = (int64_t)(blockIdx.x / nx);
+  const int64_t bh = by / p_count;
+  const int p = p_begin + (int)(by % p_count);
+  const int j0 = bx * kNV;
   const int64_t row0 = bh * T + (int64_t)p * L;
   const int nc = (int)(L / kC);
 
@@ -179,7 +183,7 @@ tc_sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   // segment, by the first of them only)
   auto prefetch = [&](int n) {
     const int32_t r = (int32_t)(row0 + (int64_t)n * kC);
-    if (blockIdx.x == 0) {
+    if (bx == 0) {
       for (int b = 0; b < DK / 64; ++b) {
         tma_prefetch_2d(&tmQ, b * 64, r);
         tma_prefetch_2d(&tmK, b * 64, r);
@@ -391,7 +395,7 @@ cudaError_t launch_sweep(const Dims& d, const void* Qt, const void* Kt, const vo
   auto kern = tc_sweep_kernel<DK, BWD>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)(d.dv / kNV), (unsigned)(d.B * d.H * p_count));
+  const unsigned grid = (unsigned)(d.B * d.H * p_count * (d.dv / kNV));
   prof_start(st);
   kern<<<grid, kThreads, smem, st>>>(tq, tk, tv, tp, Eb, S_src, (__nv_bfloat16*)o, d.T,
                                      (int)d.dv, d.P, d.L, p_begin, p_count);

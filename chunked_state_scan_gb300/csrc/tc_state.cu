@@ -81,9 +81,14 @@ tc_seg_state_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int row = tid & (kM - 1), qd = tid >> 7;  // row within the tile, token quarter
-  const int64_t bh = blockIdx.z / P;
-  const int p = blockIdx.z % P;
-  const int i0 = blockIdx.y * kM, j0 = blockIdx.x * NT;
+  // block x = ((b h p) * (d_k / kM) + d_k tile) * (d_v / NT) + d_v tile: the CTAs of
+  // one segment are launched together and share its operand tiles in L2
+  const int nx = dv / NT, ny = dk / kM;
+  const int bx = (int)(blockIdx.x % nx), by = (int)((blockIdx.x / nx) % ny);
+  const int64_t bhp = (int64_t)(blockIdx.x / nx) / ny;
+  const int64_t bh = bhp / P;
+  const int p = (int)(bhp % P);
+  const int i0 = by * kM, j0 = bx * NT;
   const int i = i0 + row;
   const int64_t row0 = bh * T + (int64_t)p * L;  // first token row of the segment
   const int nblk = (int)(L / kTok);
@@ -253,7 +258,7 @@ tc_seg_state_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
   cbar();
   const bool ok = !wait.aborted();
   // PRE: gamma_p of every row is the product over all the segment's chunks
-  if (PRE && REV && ok && gamma && blockIdx.x == 0 && tid < 16)
+  if (PRE && REV && ok && gamma && bx == 0 && tid < 16)
 #pragma unroll
     for (int u = 0; u < 8; ++u) gamma[((size_t)bh * P + p) * dk + i0 + p_r8 + u] = run8[u];
   if (ok && warp < 4) {
@@ -271,7 +276,7 @@ tc_seg_state_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
       for (int u = 0; u < 8; ++u)
         dst[u] = make_float4(r[4 * u], r[4 * u + 1], r[4 * u + 2], r[4 * u + 3]);
     }
-    if (!PRE && REV && gamma && blockIdx.x == 0) gamma[((size_t)bh * P + p) * dk + i] = __expf(run);
+    if (!PRE && REV && gamma && bx == 0) gamma[((size_t)bh * P + p) * dk + i] = __expf(run);
     (void)lane;
   }
   if (tid == 0 && wait.aborted()) {
@@ -365,7 +370,7 @@ static cudaError_t launch_state(const Dims& d, const void* x, const void* y, con
   auto kern = tc_seg_state_kernel<NT, REV, PRE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)(d.dv / NT), (unsigned)(d.dk / kM), (unsigned)(d.B * d.H * d.P));
+  const unsigned grid = (unsigned)(d.B * d.H * d.P * (d.dk / kM) * (d.dv / NT));
   prof_start(st);
   kern<<<grid, kStateBlock, smem, st>>>(tx, tg, ty, Eb, out, gamma, d.T, (int)d.dk,
                                           (int)d.dv, d.P, d.L, slot_off);

@@ -48,7 +48,8 @@
  *     (the CUDA error is left for cudaGetLastError of the caller's choosing).
  *   - Supported shapes: B, H, T, P >= 1, T % P == 0, C in {16, 32, 64, 128}
  *     with (T/P) % C == 0, dk % K == 0, dk a multiple of 16 in [16, 256], dv a
- *     multiple of 32 in [32, 512].  The chunked form factors the decay inside a
+ *     multiple of 32 in [32, 512], B*H <= 65,535 and B*H*P <= 67,108,863 (the
+ *     grid limits of the kernels).  The chunked form factors the decay inside a
  *     chunk as exp(b_t) * exp(-b_s); this is exact in fp32 as long as the sum
  *     of log_alpha over any chunk stays above -80 (for every d_k row).
  */

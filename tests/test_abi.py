@@ -158,6 +158,18 @@ def test_decay_forms_workspace_and_arguments(lib):
     assert lib.zeco_gla_resolve_path(ctypes.byref(bad)) == -1
 
 
+def test_grid_limits(lib):
+    import chunked_state_scan_gb300 as z
+    # (b, h, segment) goes on grid x: B*H*P beyond 65,535 is supported ...
+    assert z.segments(_shape(T=1 << 20, P=16384, K=8)) == 16384          # 65,536 segments
+    assert z.segments(_shape(B=8, H=32, T=65536, P=256, K=8)) == 256      # 65,536
+    # ... up to (2^31 - 1) / 32; the scans put B*H on grid z (65,535 at most)
+    for kw in (dict(B=2048, H=16, T=2048 * 64, P=2048, K=8),             # B*H*P = 2^26
+               dict(B=256, H=256, T=64, P=1, K=8)):                     # B*H = 65,536
+        with pytest.raises(z.ZecoError):
+            z.segments(_shape(**kw))
+
+
 def test_segment_count_fills_the_gpu(lib):
     import chunked_state_scan_gb300 as z
     # the 1M-token workload already gives 1024 CTAs: no split

@@ -224,17 +224,18 @@ def test_f32_decay_forms(z, decay):
     _assert(errs, "f32", f"f32 decay form {decay}")
 
 
-@pytest.mark.parametrize("dk", [128, 256])
+@pytest.mark.parametrize("dk,dv", [(128, 512), (256, 512), (128, 256), (256, 128)])
 @pytest.mark.parametrize("decay", [1, 2])
-def test_bf16_decay_forms_on_tensor_cores(z, decay, dk):
+def test_bf16_decay_forms_on_tensor_cores(z, decay, dk, dv):
     # the tensor-core kernels read the scalar log-decay once per token (none for
     # the no-decay form): no [B,H,T,dk] broadcast is made, and the scalar
-    # gradient is the sum of the reverse sweep's per-32-row partials
-    shape = z.make_shape(1, 2, 2048, dk, 512, 2, 4, 64, "bf16", "tc", decay)
+    # gradient is the sum of the reverse sweep's per-32-row partials (d_v < 512:
+    # the dq/dk clusters' CTAs past d_v hold zero states)
+    shape = z.make_shape(1, 2, 2048, dk, dv, 2, 4, 64, "bf16", "tc", decay)
     assert z.resolve_path(shape) == "tc"
     names, errs = parity.kernel_names(
-        z, lambda: _decay_case(z, decay, "bf16", 1, 2, 2048, dk, 512, 2, 4, "tc"))
-    _assert(errs, "bf16", f"bf16 tc decay form {decay} dk {dk}")
+        z, lambda: _decay_case(z, decay, "bf16", 1, 2, 2048, dk, dv, 2, 4, "tc"))
+    _assert(errs, "bf16", f"bf16 tc decay form {decay} dk {dk} dv {dv}")
     assert "tc_decay" in names and "tc_bwd_dk" in names, names
     assert "expand_log_alpha" not in names and "reduce_dlog_alpha" not in names, names
     assert ("sum_dlog_alpha_parts" in names) == (decay == 1), names

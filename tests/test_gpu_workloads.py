@@ -31,7 +31,7 @@ def z():
     return pkg
 
 
-def _sample_check(z, w, heads, with_bwd):
+def _sample_check(z, w, heads, with_bwd, COLS=COLS, ROWS=ROWS):
     dev = "cuda"
     x = workloads.make_inputs(w, device=dev)
     o, sf, saved = z.zeco_gla_fwd(x["q"], x["k"], x["v"], x["log_alpha"], x["S0"], P=w.P,
@@ -84,3 +84,12 @@ def test_batched_fwdbwd_sampled(z):
 
 def test_long_fwdbwd_sampled(z):
     _sample_check(z, workloads.LONG_FWDBWD, [(0, 2)], with_bwd=True)
+
+
+def test_more_than_65535_segment_blocks_sampled(z):
+    # B*H*P = 65,536 (P = T/C: one chunk per segment): the (b, h, segment) index
+    # of every kernel lives on grid x, so the shape runs like any other
+    w = workloads.LONG_FWDBWD.replace(name="grid_x_H8_T524288_P8192", H=8, T=1 << 19, dk=128,
+                                      dv=128, P=8192, K=4)
+    assert z.segments(z.make_shape(w.B, w.H, w.T, w.dk, w.dv, w.P, w.K, w.C, w.dtype)) == 8192
+    _sample_check(z, w, [(0, 0), (0, 7)], with_bwd=True, COLS=[0, 77, 127], ROWS=[3, 100])
