@@ -19,13 +19,19 @@ struct Fork {
 Fork fork_begin(cudaStream_t st);
 // The schedule chosen with zeco_set_overlap: 0 one stream, 1 the scan-independent
 // passes on the auxiliary stream, 2 the segment scan on the auxiliary stream, 3 pass 2
-// per block of segments as soon as the scan has reached it.
+// per block of segments as soon as the scan has reached it, 4 (default) mode 1 with
+// the dq/dk sweeps on the high-priority stream beside the dv sweep.
 int overlap_mode();
+// Records event i (of 2) on the auxiliary stream, or on stream s (f.aux or f.hi).
 cudaError_t fork_mark(const Fork& f, int i);
+cudaError_t fork_mark_on(const Fork& f, cudaStream_t s, int i);
+// Makes st wait for event i.
 cudaError_t fork_join(const Fork& f, cudaStream_t st, int i);
-// Makes the auxiliary stream wait for st's work so far (event i of kStepEvents).
+// Makes the auxiliary stream (or stream `to`) wait for st's work so far (event i
+// of kStepEvents).
 constexpr int kStepEvents = 8;
 cudaError_t fork_follow(const Fork& f, cudaStream_t st, int i);
+cudaError_t fork_follow_to(const Fork& f, cudaStream_t st, cudaStream_t to, int i);
 
 // ---- bounded-wait flags of the tensor-core kernels: read and clear; -1 when
 //      the flag cannot be read

@@ -102,18 +102,24 @@ Fork fork_begin(cudaStream_t st) {
   return f;
 }
 
-cudaError_t fork_mark(const Fork& f, int i) {
-  return f.on ? cudaEventRecord(f.ev[i], f.aux) : cudaSuccess;
+cudaError_t fork_mark_on(const Fork& f, cudaStream_t s, int i) {
+  return f.on ? cudaEventRecord(f.ev[i], s) : cudaSuccess;
 }
+
+cudaError_t fork_mark(const Fork& f, int i) { return fork_mark_on(f, f.aux, i); }
 
 cudaError_t fork_join(const Fork& f, cudaStream_t st, int i) {
   return f.on ? cudaStreamWaitEvent(st, f.ev[i], 0) : cudaSuccess;
 }
 
-cudaError_t fork_follow(const Fork& f, cudaStream_t st, int i) {
+cudaError_t fork_follow_to(const Fork& f, cudaStream_t st, cudaStream_t to, int i) {
   if (!f.on) return cudaSuccess;
   cudaError_t e = cudaEventRecord(f.step[i], st);
-  return e == cudaSuccess ? cudaStreamWaitEvent(f.aux, f.step[i], 0) : e;
+  return e == cudaSuccess ? cudaStreamWaitEvent(to, f.step[i], 0) : e;
+}
+
+cudaError_t fork_follow(const Fork& f, cudaStream_t st, int i) {
+  return fork_follow_to(f, st, f.aux, i);
 }
 
 }  // namespace zeco

@@ -80,8 +80,9 @@ cudaError_t tc_forward(const Dims& d, const void* q, const void* k, const void* 
 
 // Backward: Q~, K~, e^{b_last} and the masked scores A are the forward's (kept in
 // `saved`); the pre-pass, the reverse scan and the dv sweep run on the caller's
-// stream while the score gradient dA runs on the auxiliary stream (overlap mode 2:
-// the reverse scan on the auxiliary stream beside dA).
+// stream while the score gradient dA runs on the auxiliary stream; in overlap mode 4
+// (the default) the dq/dk sweeps then run on the high-priority stream beside the dv
+// sweep (mode 2: the reverse scan on the auxiliary stream beside dA).
 cudaError_t tc_backward(const Dims& d, const void* q, const void* k, const void* v,
                         const void* g, const float* S_in, const float* gamma, const void* d_o,
                         const float* dS_final, void* dq, void* dk, void* dv, void* dg,
@@ -109,16 +110,13 @@ cudaError_t tc_backward(const Dims& d, const void* q, const void* k, const void*
     if (e == cudaSuccess) e = fork_mark(f, 0);
     if (e == cudaSuccess) e = tc_dstate_local(d, q, d_o, g, Qt, Eb, D, st);
     if (e == cudaSuccess) e = launch_seg_scan_rev(d, D, S_in, gamma, dS_final, dS0, carry, st);
-    if (e == cudaSuccess && f.on) {
-      e = cudaEventRecord(f.step[0], st);
-      if (e == cudaSuccess) e = cudaStreamWaitEvent(f.hi, f.step[0], 0);
-      if (e == cudaSuccess) e = cudaStreamWaitEvent(f.hi, f.ev[0], 0);
-    }
+    if (e == cudaSuccess) e = fork_follow_to(f, st, f.hi, 0);  // after the reverse scan
+    if (e == cudaSuccess) e = fork_join(f, f.hi, 0);           // and after dA
     if (e == cudaSuccess)
       e = tc_bwd_qk(d, Qt, Kt, v, g, Eb, dA, S_in, d_o, dq, dk, dg, D, carry, qdq, f.hi);
-    if (e == cudaSuccess && f.on) e = cudaEventRecord(f.ev[1], f.hi);
+    if (e == cudaSuccess) e = fork_mark_on(f, f.hi, 1);
     if (e == cudaSuccess) e = tc_bwd_dv(d, Qt, Kt, d_o, A, Eb, D, dv, st);
-    if (e == cudaSuccess && f.on) e = cudaStreamWaitEvent(st, f.ev[1], 0);
+    if (e == cudaSuccess) e = fork_join(f, st, 1);
     return e;
   }
   if (overlap_mode() == 2) {

@@ -332,34 +332,34 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
       tmem_st_wait();
     }
     // rescale this thread's 64 state entries by e (if `scale`) and write their
-    // high and low bf16 parts into copy hb
+    // high and low bf16 parts into copy hb, a quarter of 16 columns at a time, the
+    // next quarter's load in flight while this one is converted
     auto pass = [&](float e, bool scale, int hb) {
       const uint32_t hl = tmem + lane_off + kColHL + 128 * hb + 32 * h;
+      float rq[2][16];
+      tmem_ld16(sS, rq[0]);
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        float rc[32];
-        tmem_ld32(sS + 32 * c, rc);
-        tmem_ld_wait();
+      for (int qd = 0; qd < 4; ++qd) {
+        float* r = rq[qd & 1];
+        tmem_ld_wait16(r);
+        if (qd + 1 < 4) tmem_ld16(sS + 16 * (qd + 1), rq[(qd + 1) & 1]);
         if (scale) {
 #pragma unroll
-          for (int u = 0; u < 32; ++u) rc[u] *= e;
-          tmem_st32(sS + 32 * c, rc);
+          for (int u = 0; u < 16; ++u) r[u] *= e;
+          tmem_st16(sS + 16 * qd, reinterpret_cast<const uint32_t*>(r));
         }
+        uint32_t hi[8], lo[8];
 #pragma unroll
-        for (int g8 = 0; g8 < 2; ++g8) {
-          uint32_t hi[8], lo[8];
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const float x0 = rc[16 * g8 + 2 * u], x1 = rc[16 * g8 + 2 * u + 1];
-            const __nv_bfloat162 h2 = __floats2bfloat162_rn(x0, x1);
-            const float2 hf = __bfloat1622float2(h2);
-            const __nv_bfloat162 l2 = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
-            hi[u] = *reinterpret_cast<const uint32_t*>(&h2);
-            lo[u] = *reinterpret_cast<const uint32_t*>(&l2);
-          }
-          tmem_st8(hl + 16 * c + 8 * g8, hi);
-          tmem_st8(hl + 64 + 16 * c + 8 * g8, lo);
+        for (int u = 0; u < 8; ++u) {
+          const float x0 = r[2 * u], x1 = r[2 * u + 1];
+          const __nv_bfloat162 h2 = __floats2bfloat162_rn(x0, x1);
+          const float2 hf = __bfloat1622float2(h2);
+          const __nv_bfloat162 l2 = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+          hi[u] = *reinterpret_cast<const uint32_t*>(&h2);
+          lo[u] = *reinterpret_cast<const uint32_t*>(&l2);
         }
+        tmem_st8(hl + 8 * qd, hi);
+        tmem_st8(hl + 64 + 8 * qd, lo);
       }
       tmem_st_wait();
     };
