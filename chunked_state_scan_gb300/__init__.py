@@ -184,6 +184,49 @@ def _shape_of(q, v, P, K, C, path, decay="diag"):
     return make_shape(B, H, T, dk, v.shape[-1], P, K, C, q.dtype, path, decay)
 
 
+def _expect(t, name, device, shape=None, dtype=None, nbytes=None, optional=True):
+    """Raise ValueError unless ``t`` is a contiguous tensor on ``device`` with the
+    given shape and dtype (and at least ``nbytes`` bytes).  The library reads and
+    writes these buffers through raw pointers, so nothing else is safe to pass."""
+    if t is None:
+        if optional:
+            return
+        raise ValueError(f"{name}: a tensor is required")
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor, got {type(t).__name__}")
+    if t.device != device:
+        raise ValueError(f"{name}: on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name}: dtype {t.dtype}, expected {dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if nbytes is not None and t.numel() * t.element_size() < nbytes:
+        raise ValueError(f"{name}: {t.numel() * t.element_size()} bytes, needs {nbytes}")
+
+
+def _check_inputs(q, k, v, log_alpha, decay):
+    """The inputs of both directions: q, k [B,H,T,dk] and v [B,H,T,dv] of one I/O dtype
+    (fp32 or bf16) on one CUDA device; log_alpha in the layout of the decay form."""
+    if not isinstance(q, torch.Tensor) or q.dim() != 4:
+        raise ValueError("q: expected a [B, H, T, dk] tensor")
+    if q.device.type != "cuda":
+        raise ValueError(f"q: on {q.device}; the library runs on CUDA devices only")
+    if q.dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError(f"q: dtype {q.dtype}; fp32 and bf16 are supported")
+    B, H, T, dk = q.shape
+    _expect(q, "q", q.device)
+    _expect(k, "k", q.device, q.shape, q.dtype, optional=False)
+    if not isinstance(v, torch.Tensor) or v.dim() != 4 or tuple(v.shape[:3]) != (B, H, T):
+        raise ValueError("v: expected a [B, H, T, dv] tensor matching q")
+    _expect(v, "v", q.device, None, q.dtype)
+    if decay != "none" and _DECAYS.get(decay, decay) != DECAY_NONE:
+        g_shape = (B, H, T) if _DECAYS.get(decay, decay) == DECAY_SCALAR else (B, H, T, dk)
+        _expect(log_alpha, "log_alpha", q.device, g_shape, q.dtype, optional=False)
+    return (B, H, dk, v.shape[-1])
+
+
 def zeco_gla_fwd(q, k, v, log_alpha, S0=None, *, P, K, C, path="auto", o=None, S_final=None,
                  saved=None, workspace=None, stream=None, want_S_final=True, decay="diag"):
     """Forward through the C ABI.  Returns (o, S_final or None, saved).
@@ -197,9 +240,17 @@ def zeco_gla_fwd(q, k, v, log_alpha, S0=None, *, P, K, C, path="auto", o=None, S
     ``workspace``: a uint8 buffer of at least workspace_bytes(shape, False) bytes,
     allocated here when None.
     """
-    shape = _shape_of(q, v, P, K, C, path, decay)
+    B, H, dk, dv = _check_inputs(q, k, v, log_alpha, decay)
     dev = q.device
+    state = (B, H, dk, dv)
+    _expect(S0, "S0", dev, state, torch.float32)
+    _expect(o, "o", dev, v.shape, v.dtype)
+    _expect(S_final, "S_final", dev, state, torch.float32)
+    shape = _shape_of(q, v, P, K, C, path, decay)
+    nsaved = saved_bytes(shape)  # 0 for a shape the library rejects (it says why below)
+    _expect(saved, "saved", dev, nbytes=nsaved)
     nws = workspace_bytes(shape, False)
+    _expect(workspace, "workspace", dev, nbytes=nws)
     with _on(stream):
         if o is None:
             o = torch.empty(v.shape, dtype=v.dtype, device=dev)
@@ -222,9 +273,23 @@ def zeco_gla_bwd(q, k, v, log_alpha, saved, do, dS_final=None, *, P, K, C, path=
                  grads=None, workspace=None, stream=None, want_dS0=True, decay="diag"):
     """Backward through the C ABI.  Returns dict(dq, dk, dv, dlog_alpha, dS0);
     dlog_alpha has log_alpha's shape and is None without decay."""
-    shape = _shape_of(q, v, P, K, C, path, decay)
+    B, H, dk, dv = _check_inputs(q, k, v, log_alpha, decay)
     dev = q.device
+    state = (B, H, dk, dv)
+    shape = _shape_of(q, v, P, K, C, path, decay)
+    _expect(saved, "saved", dev, nbytes=saved_bytes(shape), optional=False)
+    _expect(do, "do", dev, v.shape, v.dtype, optional=False)
+    _expect(dS_final, "dS_final", dev, state, torch.float32)
+    if grads is not None:
+        _expect(grads.get("dq"), "dq", dev, q.shape, q.dtype, optional=False)
+        _expect(grads.get("dk"), "dk", dev, k.shape, k.dtype, optional=False)
+        _expect(grads.get("dv"), "dv", dev, v.shape, v.dtype, optional=False)
+        if log_alpha is not None:
+            _expect(grads.get("dlog_alpha"), "dlog_alpha", dev, log_alpha.shape,
+                    log_alpha.dtype, optional=False)
+        _expect(grads.get("dS0"), "dS0", dev, state, torch.float32)
     nws = workspace_bytes(shape, True)
+    _expect(workspace, "workspace", dev, nbytes=nws)
     with _on(stream):
         if grads is None:
             grads = dict(dq=torch.empty_like(q), dk=torch.empty_like(k),

@@ -196,3 +196,32 @@ def test_noalloc_shape_errors_match_the_workspace_backward(lib):
         rc_na = lib.zeco_gla_bwd_noalloc(ctypes.byref(shape), *([None] * 13))
         rc_ws = lib.zeco_gla_bwd(ctypes.byref(shape), *([None] * 12), None, 0, None)
         assert rc_na == rc_ws < 0, (rc_na, rc_ws)
+
+
+def test_binding_rejects_bad_tensors_before_the_library():
+    """The binding hands raw pointers to the library, so it checks every tensor
+    first: device, contiguity, dtype, shape and buffer size."""
+    import torch
+    import chunked_state_scan_gb300 as z
+    q = torch.zeros(1, 2, 128, 64)
+    with pytest.raises(ValueError, match="CUDA"):
+        z.zeco_gla_fwd(q, q, q, q, P=1, K=1, C=64)
+    with pytest.raises(ValueError, match="CUDA"):
+        z.zeco_gla_bwd(q, q, q, q, torch.zeros(16, dtype=torch.uint8), q, P=1, K=1, C=64)
+    cpu = torch.device("cpu")
+    z._expect(q, "q", cpu, q.shape, torch.float32)  # a matching tensor passes
+    z._expect(None, "S0", cpu)                       # optional tensors may be absent
+    with pytest.raises(ValueError, match="required"):
+        z._expect(None, "k", cpu, optional=False)
+    with pytest.raises(ValueError, match="contiguous"):
+        z._expect(q.transpose(2, 3), "k", cpu)
+    with pytest.raises(ValueError, match="dtype"):
+        z._expect(q.half(), "k", cpu, q.shape, torch.float32)
+    with pytest.raises(ValueError, match="shape"):
+        z._expect(q[:, :1].contiguous(), "k", cpu, q.shape, torch.float32)
+    with pytest.raises(ValueError, match="bytes"):
+        z._expect(torch.zeros(10, dtype=torch.uint8), "saved", cpu, nbytes=11)
+    with pytest.raises(ValueError, match="expected cuda"):
+        z._expect(q, "k", torch.device("cuda", 0))
+    with pytest.raises(TypeError):
+        z._expect([1, 2], "k", cpu)
