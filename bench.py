@@ -15,8 +15,9 @@ maximum over ranks.  N > 1 (torchrun) runs N independent replicas, one per GPU
 
 Other modes: `--secondary` prints one line per secondary workload (GLA-1B layer
 forward, 8-segment forward, batched forward+backward); `--scan-sweep` times the
-segment scans at many segments; `--impl reference` times the fp64 CPU oracle
-instead, on a bounded sample of the same workload, on this host's cores.
+segment scans at many segments; `--forms` times the step in each decay form;
+`--impl reference` times the fp64 CPU oracle instead, on a bounded sample of the same
+workload, on this host's cores.
 """
 from __future__ import annotations
 

@@ -3,9 +3,9 @@
 // The pages' central claim is that the state exchange between segments (the
 // All-Scan) hides behind work that does not need it (ZeCO: Pith review, "What
 // carries the argument"; Algorithm 1 runs the All-Scan and the intra-chunk
-// diagonal attention on two streams, Eq. 11).  Two schedules use an auxiliary
-// stream:
-//   1 (default): the passes that do not depend on the scan -- the intra-chunk
+// diagonal attention on two streams, Eq. 11).  The schedules that use auxiliary
+// streams:
+//   1: the passes that do not depend on the scan -- the intra-chunk
 //     scores A (forward) and their gradient dA (backward) -- go to the
 //     auxiliary stream as soon as their inputs exist, concurrently with pass 1
 //     and the scan (forward) or with the backward pre-pass, the reverse scan
