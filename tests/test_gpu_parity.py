@@ -186,6 +186,52 @@ def test_overlap_schedules_give_identical_results(z, mode):
         assert torch.equal(a[n], b[n]), n
 
 
+def test_two_host_threads_with_their_own_streams(z):
+    # the default schedule forks to auxiliary streams that belong to the calling host
+    # thread: two threads running fwd+bwd at once, each on its own stream and inputs,
+    # get exactly what one thread gets running them one after the other
+    import threading
+    ws = [workloads.LONG_FWDBWD.replace(T=8192, P=4, seed=s) for s in (11, 12)]
+    xs = [{n: (t.cuda() if t is not None else None) for n, t in workloads.make_inputs(w).items()}
+          for w in ws]
+    w = ws[0]
+
+    def run(x, stream):
+        o, sf, saved = z.zeco_gla_fwd(x["q"], x["k"], x["v"], x["log_alpha"], x["S0"], P=w.P,
+                                      K=w.K, C=w.C, stream=stream)
+        g = z.zeco_gla_bwd(x["q"], x["k"], x["v"], x["log_alpha"], saved, x["do"],
+                           x["dS_final"], P=w.P, K=w.K, C=w.C, stream=stream)
+        return dict(o=o, S_final=sf, **{k: t for k, t in g.items() if t is not None})
+
+    serial = []
+    for x in xs:
+        serial.append(run(x, torch.cuda.Stream()))
+        torch.cuda.synchronize()
+    results, errors = [None, None], []
+
+    def worker(i):
+        try:
+            st = torch.cuda.Stream()
+            with torch.cuda.stream(st):
+                for _ in range(3):
+                    results[i] = run(xs[i], st)
+            st.synchronize()
+        except Exception as e:  # reported below
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    torch.cuda.synchronize()
+    z.check_device_status()
+    for i in range(2):
+        for n, t in serial[i].items():
+            assert torch.equal(results[i][n], t), (i, n)
+
+
 # ------------------------------------------------------------ decay forms
 
 
