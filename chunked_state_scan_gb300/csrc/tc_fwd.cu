@@ -21,7 +21,8 @@
 // the V tile arrive by TMA one chunk ahead (two buffers each; later chunks are
 // prefetched into L2), so a chunk is one group of MMAs plus the
 // state pass; the output accumulator is double-buffered so that warps 0-7
-// write chunk n-1 while the tensor cores run chunk n.  Thread 256 issues the
+// write chunk n-1 while the tensor cores run chunk n (through a shared-memory
+// stage and one TMA store per chunk).  Thread 256 issues the
 // MMAs and thread 288 the copies, away from the epilogue warps.
 //
 // The same kernel, run backwards over the chunks (BWD = true), computes dv
@@ -46,6 +47,8 @@
 namespace zeco {
 bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
                     uint32_t box_rows);
+bool make_tmap_bf16_plain(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                          uint32_t box_cols, uint32_t box_rows);
 
 namespace {
 
@@ -75,15 +78,17 @@ struct FwdSmem {
   static constexpr int kV = 2 * kXBuf;       // V / do tiles, 2 buffers (chunk parity)
   static constexpr int kVBuf = kNV * kC * 2;
   static constexpr int kE = kV + 2 * kVBuf;  // backward: e^{b_last} [DK] fp32, a ring of kESlots
-  static constexpr int kBytes = kE + kESlots * DK * 4;
+  // the output tile [64 t][128 j] bf16, staged for its TMA store
+  static constexpr int kO = (kE + kESlots * DK * 4 + 1023) / 1024 * 1024;
+  static constexpr int kBytes = kO + kC * kNV * 2;
 };
 
 template <int DK, bool BWD>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmP,
-                const float* __restrict__ Eb, const float* __restrict__ S_src,
-                __nv_bfloat16* __restrict__ o, int64_t T, int dv, int P, int64_t L,
+                const __grid_constant__ CUtensorMap tmO, const float* __restrict__ Eb,
+                const float* __restrict__ S_src, int64_t T, int dv, int P, int64_t L,
                 int p_begin, int p_count) {
   using SM = FwdSmem<DK>;
   extern __shared__ __align__(1024) unsigned char smraw[];
@@ -131,6 +136,7 @@ tc_sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     prefetch_tmap(&tmK);
     prefetch_tmap(&tmV);
     prefetch_tmap(&tmP);
+    prefetch_tmap(&tmO);
   }
   if (warp == 0) tmem_alloc(&tmem_base, 512);
   tc_fence_before();
@@ -257,14 +263,25 @@ tc_sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     tmem_st_wait();
   };
 
-  // o^T of chunk n (TMEM buffer ob) -> o  (warps 0-7: lane group lg, token half)
+  // o^T of chunk n (TMEM buffer ob) -> o (warps 0-7: lane group lg, token half), through
+  // the [64 t][128 j] bf16 stage and one TMA store issued by thread 0
+  auto epi_bar = []() { asm volatile("bar.sync 1, 256;" ::: "memory"); };
   auto epilogue = [&](int n, int ob) {
     float r[32];
     tmem_ld32(tmem + lane_off + kColO + ob * 64 + half * 32, r);
     tmem_ld_wait();
-    __nv_bfloat16* op = o + (size_t)(row0 + (int64_t)n * kC + half * 32) * dv + j0 + lg * 32 + lane;
+    if (tid == 0) bulk_wait_read_all();  // the previous chunk's store has read the stage
+    epi_bar();
+    __nv_bfloat16* so =
+        reinterpret_cast<__nv_bfloat16*>(sm + SM::kO) + half * 32 * kNV + lg * 32 + lane;
 #pragma unroll
-    for (int u = 0; u < 32; ++u) op[(size_t)u * dv] = __float2bfloat16_rn(r[u]);
+    for (int u = 0; u < 32; ++u) so[u * kNV] = __float2bfloat16_rn(r[u]);
+    fence_async_smem();
+    epi_bar();
+    if (tid == 0) {
+      tma_store_2d(&tmO, sm + SM::kO, j0, (int32_t)(row0 + (int64_t)n * kC));
+      bulk_commit();
+    }
   };
 
   // backward: the adjoint entering the first chunk (the segment's last) is
@@ -377,6 +394,7 @@ tc_sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         drain_phase(&bar_e[k], n_e > k ? (n_e - k + kESlots - 1) / kESlots : 0);
     }
   }
+  if (tid == 0) bulk_wait_all();  // the output stores have read the stage and completed
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, 512);
@@ -386,10 +404,11 @@ template <int DK, bool BWD>
 cudaError_t launch_sweep(const Dims& d, const void* Qt, const void* Kt, const void* v,
                          const void* A, const float* Eb, const float* S_src, void* o,
                          cudaStream_t st, int p_begin, int p_count) {
-  CUtensorMap tq, tk, tv, tp;
+  CUtensorMap tq, tk, tv, tp, to;
   const uint64_t rows = (uint64_t)(d.B * d.H * d.T);
   if (!make_tmap_bf16(&tq, Qt, rows, DK, kC) || !make_tmap_bf16(&tk, Kt, rows, DK, kC) ||
-      !make_tmap_bf16(&tv, v, rows, d.dv, kC) || !make_tmap_bf16(&tp, A, rows, kC, kC))
+      !make_tmap_bf16(&tv, v, rows, d.dv, kC) || !make_tmap_bf16(&tp, A, rows, kC, kC) ||
+      !make_tmap_bf16_plain(&to, o, rows, d.dv, kNV, kC))
     return cudaErrorInvalidValue;
   const int smem = FwdSmem<DK>::kBytes + 1024;
   auto kern = tc_sweep_kernel<DK, BWD>;
@@ -397,7 +416,7 @@ cudaError_t launch_sweep(const Dims& d, const void* Qt, const void* Kt, const vo
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)(d.B * d.H * p_count * (d.dv / kNV));
   prof_start(st);
-  kern<<<grid, kThreads, smem, st>>>(tq, tk, tv, tp, Eb, S_src, (__nv_bfloat16*)o, d.T,
+  kern<<<grid, kThreads, smem, st>>>(tq, tk, tv, tp, to, Eb, S_src, d.T,
                                      (int)d.dv, d.P, d.L, p_begin, p_count);
   return cudaGetLastError();
 }
