@@ -267,7 +267,7 @@ const char *zeco_strerror(int code);
  * zeco_gla_bwd call made on this host thread records, for its i-th kernel
  * counted from the set call, events[2i] right before the launch and
  * events[2i + 1] right after it, both on the stream the kernel runs on (the
- * caller's, or the auxiliary stream of zeco_set_overlap), until the n events
+ * caller's, or one of the auxiliary streams of zeco_set_overlap), until the n events
  * are used; n = 0 (or events = NULL) switches it off.  So the elapsed time from
  * events[2i] to events[2i + 1] is kernel i's duration, and intervals of kernels
  * on the two streams can be compared on one timeline.  `events` are
