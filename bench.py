@@ -834,7 +834,7 @@ def main(argv=None):
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default=workloads.LONG_FWDBWD.name)
     ap.add_argument("--path", default="auto", choices=["auto", "simt", "tc"])
-    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-sample-tokens", type=int, default=16384)
     ap.add_argument("--ref-sample-tokens", type=int, default=4096)
     ap.add_argument("--no-cpu-baseline", action="store_true")
