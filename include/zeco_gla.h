@@ -304,7 +304,10 @@ const char *zeco_profile_kernel_name(int i);
  *     the dq/dk sweeps leave idle;
  *   mode 0: everything on `stream`.
  * The call forks from and joins back into its `stream` with events, so all its
- * work stays ordered on `stream`.  Results are identical in every mode.  The
+ * work stays ordered on `stream` (a zeco_gla_fwd + zeco_gla_bwd pair captured on
+ * one stream, after one eager call has created the auxiliary streams, replays as
+ * a CUDA graph with the eager results; tested).  Results are identical in every
+ * mode.  The
  * auxiliary streams and eleven events are created on the first such call of
  * each host thread on each device and destroyed when the thread exits.
  * Process-wide; returns ZECO_OK, or ZECO_ERR_ARG for a mode outside 0..4.

@@ -232,6 +232,45 @@ def test_two_host_threads_with_their_own_streams(z):
             assert torch.equal(results[i][n], t), (i, n)
 
 
+def test_forward_backward_replayed_from_a_cuda_graph(z):
+    # the calls fork to their auxiliary streams and join back with events only, so a
+    # forward+backward captured on one stream replays as a graph, bit for bit
+    w = workloads.LONG_FWDBWD.replace(T=8192, P=4, seed=21)
+    x = {n: (t.cuda() if t is not None else None) for n, t in workloads.make_inputs(w).items()}
+    shape = z.make_shape(w.B, w.H, w.T, w.dk, w.dv, w.P, w.K, w.C, w.dtype)
+    st = torch.cuda.Stream()
+    o = torch.empty_like(x["v"])
+    sf = torch.empty_like(x["S0"])
+    saved = torch.empty(z.saved_bytes(shape), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(max(z.workspace_bytes(shape, True), 16), dtype=torch.uint8, device="cuda")
+    grads = dict(dq=torch.empty_like(x["q"]), dk=torch.empty_like(x["k"]),
+                 dv=torch.empty_like(x["v"]), dlog_alpha=torch.empty_like(x["log_alpha"]),
+                 dS0=torch.empty_like(x["S0"]))
+
+    def step():
+        z.zeco_gla_fwd(x["q"], x["k"], x["v"], x["log_alpha"], x["S0"], P=w.P, K=w.K, C=w.C,
+                       o=o, S_final=sf, saved=saved, stream=st)
+        z.zeco_gla_bwd(x["q"], x["k"], x["v"], x["log_alpha"], saved, x["do"], x["dS_final"],
+                       P=w.P, K=w.K, C=w.C, grads=grads, workspace=ws, stream=st)
+
+    with torch.cuda.stream(st):
+        step()  # eager (also creates the auxiliary streams before the capture)
+    st.synchronize()
+    ref = dict(o=o.clone(), S_final=sf.clone(), **{k: t.clone() for k, t in grads.items()})
+    for t in (o, sf, *grads.values()):
+        t.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=st):
+        step()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    z.check_device_status()
+    got = dict(o=o, S_final=sf, **grads)
+    for n, t in ref.items():
+        assert torch.equal(got[n], t), n
+
+
 # ------------------------------------------------------------ decay forms
 
 
