@@ -335,24 +335,11 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
   return r;
 }
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, float c, float d) {
-  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b),
-               "f"(c), "f"(d)
-               : "memory");
-}
 // Whole-cluster barrier; release/acquire make shared::cluster writes before it
 // visible to all threads of the cluster after it.
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n"
                "barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// The two halves of cluster_sync, for a barrier whose wait comes later: every
-// thread alternates arrive and wait.
-__device__ __forceinline__ void cluster_arrive() {
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_wait() {
-  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 }  // namespace tc
 }  // namespace zeco
@@ -384,11 +371,6 @@ __device__ __forceinline__ void st_async_v4(uint32_t addr, float a, float b, flo
           addr),
       "f"(a), "f"(b), "f"(c), "f"(d), "r"(remote_bar)
       : "memory");
-}
-// Arrive (release, cluster scope) on an mbarrier of another CTA of the cluster.
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t remote_bar) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar)
-               : "memory");
 }
 }  // namespace tc
 }  // namespace zeco
