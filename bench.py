@@ -15,7 +15,8 @@ maximum over ranks.  N > 1 (torchrun) runs N independent replicas, one per GPU
 
 Other modes: `--secondary` prints one line per secondary workload (GLA-1B layer
 forward, 8-segment forward, batched forward+backward); `--scan-sweep` times the
-segment scans at many segments; `--forms` times the step in each decay form;
+segment scans at many segments; `--schedule-sweep` times the schedules of the work
+beside the scan at many segments; `--forms` times the step in each decay form;
 `--impl reference` times the fp64 CPU oracle instead, on a bounded sample of the same
 workload, on this host's cores.
 """
@@ -757,6 +758,56 @@ def scan_sweep(args, local):
             "workload": base.name + " inputs, P varied"}
 
 
+def schedule_sweep(args, local):
+    """The headline workload's inputs cut into P segments, P from 64 to T/C
+    (``--schedule-sweep``): the step time in schedules 0 (one stream), 1 (score passes
+    on a second stream) and 4 (mode 1 plus dq/dk beside dv; the default runs it from 4
+    chunks per segment up, one stream below), each set through zeco_set_overlap."""
+    import chunked_state_scan_gb300 as z
+    lib = z.load_library()
+    dev = torch.device("cuda", local)
+    base = workloads.LONG_FWDBWD
+    x = workloads.make_inputs(base, device=dev)
+    out = []
+    lib.zeco_set_overlap.argtypes = [ctypes.c_int]
+    for P in (64, 256, 1024, 4096, 8192, base.T // base.C):
+        w = base.replace(P=P)
+        shape = z.make_shape(w.B, w.H, w.T, w.dk, w.dv, w.P, w.K, w.C, w.dtype)
+        saved = torch.empty(z.saved_bytes(shape), dtype=torch.uint8, device=dev)
+        ws = torch.empty(z.workspace_bytes(shape, True), dtype=torch.uint8, device=dev)
+        stream = torch.cuda.Stream(device=dev)
+
+        def step():
+            z.zeco_gla_fwd(x["q"], x["k"], x["v"], x["log_alpha"], x["S0"], P=P, K=w.K,
+                           C=w.C, saved=saved, stream=stream)
+            z.zeco_gla_bwd(x["q"], x["k"], x["v"], x["log_alpha"], saved, x["do"],
+                           x["dS_final"], P=P, K=w.K, C=w.C, workspace=ws, stream=stream)
+
+        res = {"P": P, "chunks_per_segment": w.L // w.C}
+        try:
+            for mode in (0, 1, 4):
+                lib.zeco_set_overlap(mode)
+                for _ in range(max(2, args.warmup)):
+                    step()
+                torch.cuda.synchronize(dev)
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for _ in range(args.steps):
+                    step()
+                e1.record(stream)
+                torch.cuda.synchronize(dev)
+                key = "mode4_default_ms" if mode == 4 else f"mode{mode}_ms"
+                res[key] = e0.elapsed_time(e1) / args.steps
+        finally:
+            lib.zeco_set_overlap(z.OVERLAP_DEFAULT)
+        out.append(res)
+        del saved, ws
+        torch.cuda.empty_cache()
+    return {"schedule_sweep": out, "workload": base.name + " inputs, P varied",
+            "steps": args.steps}
+
+
 def decay_forms(args, local):
     """The headline workload's fwd+bwd step in each decay form (``--forms``): per-token
     scalar and no decay beside the diagonal form, each with its step time (L2 flushed
@@ -844,6 +895,8 @@ def main(argv=None):
                          "8-segment fwd, batched fwd+bwd) instead of the headline")
     ap.add_argument("--scan-sweep", action="store_true",
                     help="time the segment scans at P in {64, 1024, 4096, 8192, T/C}")
+    ap.add_argument("--schedule-sweep", action="store_true",
+                    help="time schedules 0, 1 and 4 at P from 64 to T/C")
     ap.add_argument("--forms", action="store_true",
                     help="time the headline step in the diagonal, scalar and no-decay forms")
     args = ap.parse_args(argv)
@@ -856,8 +909,9 @@ def main(argv=None):
 
     import chunked_state_scan_gb300 as z
     z.load_library()
-    if args.scan_sweep or args.forms:
-        res = scan_sweep(args, local) if args.scan_sweep else decay_forms(args, local)
+    if args.scan_sweep or args.forms or args.schedule_sweep:
+        res = (scan_sweep(args, local) if args.scan_sweep else
+               decay_forms(args, local) if args.forms else schedule_sweep(args, local))
         if rank == 0:
             print(json.dumps(res), flush=True)
         return 0

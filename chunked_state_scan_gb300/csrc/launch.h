@@ -15,13 +15,17 @@ struct Fork {
   cudaEvent_t* step;  // recorded on the caller's stream by fork_follow
   bool on;
 };
-// Forks from st (aux waits for st's work so far); off when overlap is disabled.
-Fork fork_begin(cudaStream_t st);
+// Forks from st (aux waits for st's work so far); off in schedule 0.
+Fork fork_begin(cudaStream_t st, int mode);
 // The schedule chosen with zeco_set_overlap: 0 one stream, 1 the scan-independent
 // passes on the auxiliary stream, 2 the segment scan on the auxiliary stream, 3 pass 2
 // per block of segments as soon as the scan has reached it, 4 (default) mode 1 with
-// the dq/dk sweeps on the high-priority stream beside the dv sweep.
-int overlap_mode();
+// the dq/dk sweeps on the high-priority stream beside the dv sweep.  The schedule
+// a call of shape d runs: the one set, except that the default (4) runs on one
+// stream (0) when the segments hold fewer than 4 chunks -- there every kernel is
+// bound by its segment-state traffic and the streams only contend (measured: at 2
+// chunks per segment 84.0 ms on one stream against 87.3 ms).
+int overlap_mode(const Dims& d);
 // Records event i (of 2) on the auxiliary stream, or on stream s (f.aux or f.hi).
 cudaError_t fork_mark(const Fork& f, int i);
 cudaError_t fork_mark_on(const Fork& f, cudaStream_t s, int i);

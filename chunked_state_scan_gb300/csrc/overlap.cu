@@ -80,15 +80,18 @@ AuxState* aux_for_current_device() {
 
 }  // namespace
 
-int overlap_mode() { return g_overlap.load(std::memory_order_relaxed); }
+int overlap_mode(const Dims& d) {
+  const int m = g_overlap.load(std::memory_order_relaxed);
+  return (m == 4 && d.L / d.C < 4) ? 0 : m;
+}
 
-Fork fork_begin(cudaStream_t st) {
+Fork fork_begin(cudaStream_t st, int mode) {
   Fork f;
   f.aux = st;
   f.hi = st;
   f.step = nullptr;
   f.on = false;
-  if (!g_overlap.load(std::memory_order_relaxed)) return f;
+  if (!mode) return f;
   AuxState* a = aux_for_current_device();
   if (!a) return f;
   if (cudaEventRecord(a->ev[0], st) != cudaSuccess) return f;

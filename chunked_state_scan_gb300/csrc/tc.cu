@@ -34,14 +34,15 @@ cudaError_t tc_forward(const Dims& d, const void* q, const void* k, const void* 
   void* Kt = ops.Kt;
   float* Eb = ops.Eb;
   void* A = ops.A;
+  const int mode = overlap_mode(d);
   cudaError_t e = tc_decay(d, q, k, g, Qt, Kt, Eb, st);
   if (e != cudaSuccess) return e;
-  if (overlap_mode() == 3) {
+  if (mode == 3) {
     // pass 2 of a block of segments starts as soon as the scan has given that block
     // its incoming states: the scan runs block by block on the caller's stream, and
     // pass 2 of each block on the auxiliary stream after the scores and after the
     // scan of its block
-    const Fork f = fork_begin(st);
+    const Fork f = fork_begin(st, mode);
     e = tc_A(d, Qt, Kt, A, f.aux);
     if (e == cudaSuccess) e = tc_chunk_state(d, k, v, g, Kt, Eb, S_in, gamma, st);
     const int nb = d.P < kStepEvents ? d.P : kStepEvents;
@@ -55,11 +56,11 @@ cudaError_t tc_forward(const Dims& d, const void* q, const void* k, const void* 
     if (e == cudaSuccess) e = fork_join(f, st, 0);
     return e;
   }
-  if (overlap_mode() == 2) {
+  if (mode == 2) {
     // the pages' schedule: the scan on the second stream beside the scores
     e = tc_chunk_state(d, k, v, g, Kt, Eb, S_in, gamma, st);
     if (e != cudaSuccess) return e;
-    const Fork f = fork_begin(st);
+    const Fork f = fork_begin(st, mode);
     e = launch_seg_scan_fwd(d, S_in, gamma, S0, S_final, f.aux);
     if (e == cudaSuccess) e = fork_mark(f, 0);
     if (e == cudaSuccess) e = tc_A(d, Qt, Kt, A, st);
@@ -67,7 +68,7 @@ cudaError_t tc_forward(const Dims& d, const void* q, const void* k, const void* 
     if (e != cudaSuccess) return e;
     return tc_fwd_out(d, Qt, Kt, v, A, Eb, S_in, o, st);
   }
-  const Fork f = fork_begin(st);
+  const Fork f = fork_begin(st, mode);
   e = tc_A(d, Qt, Kt, A, f.aux);
   if (e == cudaSuccess) e = fork_mark(f, 0);
   if (e != cudaSuccess) return e;
@@ -101,11 +102,12 @@ cudaError_t tc_backward(const Dims& d, const void* q, const void* k, const void*
   const void* A = ops.A;
   const bool qk_tc = tc_uses_dA(d);
   void* dA = ops.dA;
+  const int mode = overlap_mode(d);
   cudaError_t e = cudaSuccess;
-  if (overlap_mode() == 4 && qk_tc) {
+  if (mode == 4 && qk_tc) {
     // dq/dk on a high-priority stream, dv on the caller's: the dq/dk CTAs are
     // scheduled first and the dv sweep's fill the SMs their last waves leave idle
-    const Fork f = fork_begin(st);
+    const Fork f = fork_begin(st, mode);
     e = tc_dA(d, d_o, v, dA, f.aux);
     if (e == cudaSuccess) e = fork_mark(f, 0);
     if (e == cudaSuccess) e = tc_dstate_local(d, q, d_o, g, Qt, Eb, D, st);
@@ -119,18 +121,18 @@ cudaError_t tc_backward(const Dims& d, const void* q, const void* k, const void*
     if (e == cudaSuccess) e = fork_join(f, st, 1);
     return e;
   }
-  if (overlap_mode() == 2) {
+  if (mode == 2) {
     // the pages' schedule: the reverse scan on the second stream beside dA
     e = tc_dstate_local(d, q, d_o, g, Qt, Eb, D, st);
     if (e != cudaSuccess) return e;
-    const Fork f = fork_begin(st);
+    const Fork f = fork_begin(st, mode);
     e = launch_seg_scan_rev(d, D, S_in, gamma, dS_final, dS0, carry, f.aux);
     if (e == cudaSuccess) e = fork_mark(f, 0);
     if (e == cudaSuccess && qk_tc) e = tc_dA(d, d_o, v, dA, st);
     if (e == cudaSuccess) e = fork_join(f, st, 0);
     if (e == cudaSuccess) e = tc_bwd_dv(d, Qt, Kt, d_o, A, Eb, D, dv, st);
   } else {
-    const Fork f = fork_begin(st);
+    const Fork f = fork_begin(st, mode);
     e = qk_tc ? tc_dA(d, d_o, v, dA, f.aux) : cudaSuccess;
     if (e == cudaSuccess) e = fork_mark(f, 0);
     if (e != cudaSuccess) return e;

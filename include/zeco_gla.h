@@ -301,7 +301,9 @@ const char *zeco_profile_kernel_name(int i);
  *     run on a second auxiliary stream created at the device's highest stream
  *     priority while the dv sweep runs on `stream`: the two do not depend on
  *     each other, and the dv sweep's CTAs take the SMs that the last waves of
- *     the dq/dk sweeps leave idle;
+ *     the dq/dk sweeps leave idle.  Shapes whose segments hold fewer than 4
+ *     chunks run as mode 0 under this setting (their kernels are bound by the
+ *     segment-state traffic, and concurrent streams only contend);
  *   mode 0: everything on `stream`.
  * The call forks from and joins back into its `stream` with events, so all its
  * work stays ordered on `stream` (a zeco_gla_fwd + zeco_gla_bwd pair captured on

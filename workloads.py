@@ -87,7 +87,12 @@ WORKLOADS = [TINY_F32, GLA1B_FWD, SEG_FWD, LONG_FWDBWD, BATCHED_FWDBWD]
 # shapes per token, 1/32 of the tokens (one wave of CTAs, inputs 470 MB > L2).
 PROFILE_FWDBWD = LONG_FWDBWD.replace(name="profile_fwdbwd_T32768_P8", T=32768, P=8)
 
-BY_NAME = {w.name: w for w in WORKLOADS + [PROFILE_FWDBWD]}
+# The throughput workload cut into P = T/C segments of one chunk each: the segment
+# scans (a long chain of 16,384 states per (b, h)) then take about as long as the
+# rest of the step, the regime in which hiding them beside other work matters.
+SCAN_BOUND_FWDBWD = LONG_FWDBWD.replace(name="long_fwdbwd_T1048576_P16384", P=16384)
+
+BY_NAME = {w.name: w for w in WORKLOADS + [PROFILE_FWDBWD, SCAN_BOUND_FWDBWD]}
 
 
 def make_inputs(w: Workload, device="cpu", seed: int | None = None):
