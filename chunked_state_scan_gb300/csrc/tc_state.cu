@@ -35,6 +35,8 @@ namespace {
 using namespace tc;
 
 constexpr int kStages = 3;
+// PRE: stages of the copy ring of one CTA per SM (each ~49 KB at 256 d_v columns)
+constexpr int kStagesPre = 4;
 constexpr int kTok = 64;                // tokens per stage (MMA K)
 constexpr int kM = 128;                 // d_k rows per CTA
 constexpr int kXBytes = kTok * kM * 2;  // 16 KB: x tile, overwritten in place by A = (w .* x)
@@ -55,20 +57,22 @@ constexpr int kStateBlock = kStateThreads + 32;
 // stage loads the chunk's e^{b_last} row instead of the log_alpha tile and scales
 // the tile by a running product, with no exponential per element.
 template <int NT, bool REV, bool PRE>
-__global__ void __launch_bounds__(kStateBlock, PRE ? 2 : 1)
+__global__ void __launch_bounds__(kStateBlock, 1)
 tc_seg_state_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmG,
                     const __grid_constant__ CUtensorMap tmY, const float* __restrict__ Eb,
                     float* __restrict__ out, float* __restrict__ gamma, int64_t T, int dk, int dv,
                     int P, int64_t L, int slot_off) {
   constexpr int kBBytes = kTok * NT * 2;
-  // PRE: the log_alpha slot holds only the e^{b_last} row; two stages of ~49 KB
-  // let two CTAs share an SM (one's barriers overlap the other's MMAs)
-  constexpr int SG = PRE ? 2 : kStages;
+  // PRE: the log_alpha slot holds only the e^{b_last} row; one CTA per SM with four
+  // stages of ~49 KB (two CTAs of two stages each keep as many copies in flight, but
+  // their 1,024 CTAs at the 1M-token shape make 3.4 waves of 304 instead of 6.7 of
+  // 152: 1.24 -> 1.17 ms for pass 1)
+  constexpr int SG = PRE ? kStagesPre : kStages;
   constexpr int GB = PRE ? 1024 : kGBytes;
   constexpr int kStageBytes = kXBytes + GB + kBBytes;
   extern __shared__ __align__(1024) unsigned char smraw[];
   unsigned char* sm = align1024(smraw);
-  __shared__ uint64_t tma_bar[kStages], mma_bar[kStages], fin_bar;
+  __shared__ uint64_t tma_bar[SG], mma_bar[SG], fin_bar;
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;  // set when a bounded wait of this CTA gives up
   // After a wait of this CTA has given up, the abort word makes every later wait
@@ -366,7 +370,7 @@ static cudaError_t launch_state(const Dims& d, const void* x, const void* y, con
       !make_tmap_bf16(&tg, PRE ? x : g, rows, (uint64_t)d.dk, kTok) ||
       !make_tmap_bf16(&ty, y, rows, (uint64_t)d.dv, kTok))
     return cudaErrorInvalidValue;
-  const int smem = (PRE ? 2 : kStages) * (kXBytes + (PRE ? 1024 : kGBytes) + kTok * NT * 2) + 1024;
+  const int smem = (PRE ? kStagesPre : kStages) * (kXBytes + (PRE ? 1024 : kGBytes) + kTok * NT * 2) + 1024;
   auto kern = tc_seg_state_kernel<NT, REV, PRE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
