@@ -2,10 +2,12 @@
 //
 // dq and dk contract over all d_v columns of the state.  A cluster of four CTAs
 // owns a block of 128 d_k rows i of one (b, h, segment); CTA r of the cluster
-// holds the d_v columns [128 r, 128 r + 128).  For d_v < 512 (a multiple of 128)
-// the CTAs whose columns lie beyond d_v hold a zero state and receive zero v / do
-// tiles (the copies of boxes past the end of a tensor read zeros), so their
-// partial sums are zero and the results are those of the d_v columns that exist.
+// holds the d_v columns [128 r, 128 r + 128).  For d_v < 512 (a multiple of 64)
+// the columns beyond d_v hold a zero state and receive zero v / do tiles (the
+// copies of boxes past the end of a tensor read zeros), so their partial sums
+// are zero and the results are those of the d_v columns that exist.  Likewise a
+// d_k that is not a multiple of 128 (d_k = 64, 192) pads its last block with
+// zero rows, which are not stored.
 // Two launches sweep the segment's chunks:
 //
 //   forward sweep, state S (from S_in[p], the global state held since the
@@ -183,7 +185,9 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
   const uint32_t rank = cluster_ctarank();   // which quarter of d_v; rows finished
   // block x = (b h p) * (kRanks d_k / kKB) + kRanks * d_k block + rank: a cluster is
   // kRanks consecutive blocks of one (b, h, segment, d_k block)
-  const int nx = kRanks * dk / kKB;
+  // (a last partial block of d_k rows holds zeros past d_k: zero state rows and
+  // operand columns, no stores)
+  const int nx = kRanks * ((dk + kKB - 1) / kKB);
   const int64_t bhp = (int64_t)(blockIdx.x / nx);
   const int64_t bh = bhp / P;
   const int p = (int)(bhp % P);
@@ -310,11 +314,13 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
     const uint32_t lane_off = (uint32_t)(lg * 32) << 16;
     const uint32_t sS = tmem + lane_off + kColS + 64 * h;
     {
-      // (a CTA past d_v starts from a zero state: d_v and j0 are multiples of 128)
-      const bool live = j0 < dv;
-      const float* Sp = S_src +
-                        (((size_t)bh * (P + 1) + p + (REV ? 1 : 0)) * dk + i0 + row) * dv +
-                        (live ? j0 + 64 * h : 0);
+      // (the columns past d_v and the rows past d_k start from zero: d_v and d_k
+      // are multiples of 64)
+      const bool live = j0 + 64 * h < dv && i0 + row < dk;
+      const float* Sp =
+          live ? S_src + (((size_t)bh * (P + 1) + p + (REV ? 1 : 0)) * dk + i0 + row) * dv +
+                     j0 + 64 * h
+               : S_src;
 #pragma unroll 1
       for (int c = 0; c < 2; ++c) {
         float r[32];
@@ -365,7 +371,7 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
     };
     // e^{b_last} of row `row` for the chunk processed at iteration ie (1 past the end)
     auto e_of = [&](int ie) -> float {
-      if (ie >= nc) return 1.f;
+      if (ie >= nc || i0 + row >= dk) return 1.f;
       return __ldg(Eb + (size_t)(chunk_row(chunk_of(ie)) / kC) * dk + i0 + row);
     };
     auto ready = [&]() {
@@ -472,7 +478,7 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
       }
     }
     if (REV && kDecay && g == 0 && eq == 0)
-      sRun[er] = carry[((size_t)bh * P + p) * dk + i0 + ec];
+      sRun[er] = i0 + ec < dk ? carry[((size_t)bh * P + p) * dk + i0 + ec] : 0.f;
 #pragma unroll 1
     for (int it = g; it < nc; it += 2) {
       const int n = chunk_of(it);
@@ -589,7 +595,7 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
             }
           }
           v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
-          if ((lane & 1) == 0) {
+          if ((lane & 1) == 0 && i0 + kOwn * (int)rank < dk) {
             const int c = (i0 + kOwn * (int)rank) / kOwn;
             dg_part[(size_t)c * nrows + chunk_row(n) + 16 * eq + (lane >> 1)] = v[0];
           }
@@ -600,8 +606,10 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
       grp_bar(bar_sync);
       if (leader) {
         const int32_t r = chunk_row(n), x = i0 + kOwn * (int)rank;
-        tma_store_2d(&tmOut, ep + kEpY, x, r);
-        if (kAux) tma_store_2d(&tmAux, ep + (REV ? kEpG : kEpQD), x, r);
+        if (x < dk) {  // (rows past d_k are not stored)
+          tma_store_2d(&tmOut, ep + kEpY, x, r);
+          if (kAux) tma_store_2d(&tmAux, ep + (REV ? kEpG : kEpQD), x, r);
+        }
         bulk_commit();
         if (it + 2 < nc && ok) {
           bulk_wait_read_all();  // the stores have read the stage: refill it
@@ -637,7 +645,7 @@ cudaError_t launch_qk(const Dims& d, const CUtensorMap& tx, const CUtensorMap& t
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(d.B * d.H * d.P * (kRanks * d.dk / kKB)), 1, 1);
+  cfg.gridDim = dim3((unsigned)(d.B * d.H * d.P * (kRanks * ((d.dk + kKB - 1) / kKB))), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = (size_t)smem;
   cfg.stream = st;
@@ -676,7 +684,7 @@ cudaError_t launch_sweeps(const Dims& d, const CUtensorMap* m, const float* Eb,
 }  // namespace
 
 bool tc_bwd_qk_supported(const Dims& d) {
-  return d.bf16 && d.dk % kKB == 0 && d.dv % kNB == 0 && d.dv <= kDVMax && d.C == kC &&
+  return d.bf16 && d.dk % 64 == 0 && d.dv % 64 == 0 && d.dv <= kDVMax && d.C == kC &&
          d.L % kC == 0;
 }
 

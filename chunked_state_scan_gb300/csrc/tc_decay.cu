@@ -11,7 +11,7 @@
 // intra-chunk scores, so every kernel that builds or consumes a state works
 // from the same bf16 values.  The pass is bound by HBM: each thread owns 8
 // columns of one chunk and walks its 64 tokens with 16-byte loads and stores
-// (a warp reads whole 512-byte rows when d_k = 256).
+// (a warp reads whole 512-byte rows when d_k = 256; d_k = 64, 128 or 256).
 //
 // The scalar-decay form reads its one log-decay per token ([B,H,T]; every
 // thread of a chunk reads the same value), the no-decay form reads none: b = 0,
@@ -86,6 +86,18 @@ decay_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restric
 
 }  // namespace
 
+template <int DK>
+static void launch_decay(const Dims& d, const __nv_bfloat16* q, const __nv_bfloat16* k,
+                         const __nv_bfloat16* g, __nv_bfloat16* Qt, __nv_bfloat16* Kt, float* Eb,
+                         int64_t nchunks, unsigned blocks, cudaStream_t st) {
+  if (d.decay == ZECO_DECAY_SCALAR)
+    decay_kernel<DK, ZECO_DECAY_SCALAR><<<blocks, 256, 0, st>>>(q, k, g, Qt, Kt, Eb, nchunks);
+  else if (d.decay == ZECO_DECAY_NONE)
+    decay_kernel<DK, ZECO_DECAY_NONE><<<blocks, 256, 0, st>>>(q, k, g, Qt, Kt, Eb, nchunks);
+  else
+    decay_kernel<DK, ZECO_DECAY_DIAG><<<blocks, 256, 0, st>>>(q, k, g, Qt, Kt, Eb, nchunks);
+}
+
 cudaError_t tc_decay(const Dims& d, const void* q, const void* k, const void* g, void* Qt,
                      void* Kt, float* Eb, cudaStream_t st) {
   const int64_t nchunks = d.B * d.H * d.T / kC;
@@ -96,22 +108,14 @@ cudaError_t tc_decay(const Dims& d, const void* q, const void* k, const void* g,
   auto gb = (const __nv_bfloat16*)g;
   auto Qb = (__nv_bfloat16*)Qt;
   auto Kb = (__nv_bfloat16*)Kt;
+  if (d.dk != 64 && d.dk != 128 && d.dk != 256) return cudaErrorInvalidValue;
   prof_start(st);
-  if (d.dk == 256) {
-    if (d.decay == ZECO_DECAY_SCALAR)
-      decay_kernel<256, ZECO_DECAY_SCALAR><<<blocks, 256, 0, st>>>(qb, kb, gb, Qb, Kb, Eb, nchunks);
-    else if (d.decay == ZECO_DECAY_NONE)
-      decay_kernel<256, ZECO_DECAY_NONE><<<blocks, 256, 0, st>>>(qb, kb, gb, Qb, Kb, Eb, nchunks);
-    else
-      decay_kernel<256, ZECO_DECAY_DIAG><<<blocks, 256, 0, st>>>(qb, kb, gb, Qb, Kb, Eb, nchunks);
-  } else {
-    if (d.decay == ZECO_DECAY_SCALAR)
-      decay_kernel<128, ZECO_DECAY_SCALAR><<<blocks, 256, 0, st>>>(qb, kb, gb, Qb, Kb, Eb, nchunks);
-    else if (d.decay == ZECO_DECAY_NONE)
-      decay_kernel<128, ZECO_DECAY_NONE><<<blocks, 256, 0, st>>>(qb, kb, gb, Qb, Kb, Eb, nchunks);
-    else
-      decay_kernel<128, ZECO_DECAY_DIAG><<<blocks, 256, 0, st>>>(qb, kb, gb, Qb, Kb, Eb, nchunks);
-  }
+  if (d.dk == 256)
+    launch_decay<256>(d, qb, kb, gb, Qb, Kb, Eb, nchunks, blocks, st);
+  else if (d.dk == 128)
+    launch_decay<128>(d, qb, kb, gb, Qb, Kb, Eb, nchunks, blocks, st);
+  else
+    launch_decay<64>(d, qb, kb, gb, Qb, Kb, Eb, nchunks, blocks, st);
   prof_mark("tc_decay", st);
   return cudaGetLastError();
 }

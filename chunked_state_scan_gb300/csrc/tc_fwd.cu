@@ -83,6 +83,26 @@ struct FwdSmem {
   static constexpr int kBytes = kO + kC * kNV * 2;
 };
 
+// A warp's W consecutive fp32 columns of its 32 lanes (W = 32 or 16), and their
+// bf16 pairs packed into W / 2 columns
+template <int W>
+__device__ __forceinline__ void st_cols(uint32_t taddr, const float* r) {
+  if constexpr (W == 32)
+    tmem_st32(taddr, r);
+  else
+    tmem_st16(taddr, reinterpret_cast<const uint32_t*>(r));
+}
+template <int W>
+__device__ __forceinline__ void st_half(uint32_t taddr, const float* r) {
+  uint32_t h[W / 2];
+#pragma unroll
+  for (int u = 0; u < W / 2; ++u) h[u] = pack_bf16(r[2 * u], r[2 * u + 1]);
+  if constexpr (W == 32)
+    tmem_st16(taddr, h);
+  else
+    tmem_st8(taddr, h);
+}
+
 template <int DK, bool BWD>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -110,7 +130,9 @@ tc_sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   const int half = (warp >> 2) & 1;  // epilogue: which half of the 64 tokens (warps 0..7)
   // segments [p_begin, p_begin + p_count) of every (b, h)
   // block x = ((b h) * p_count + segment - p_begin) * (d_v / kNV) + d_v tile
-  const int nx = dv / kNV;
+  // (a last partial tile of d_v columns starts from a zero state, reads zeros
+  // past the end of V and stores only the columns that exist)
+  const int nx = (dv + kNV - 1) / kNV;
   const int bx = (int)(blockIdx.x % nx);
   const int64_t by = (int64_t)(blockIdx.x / nx);
   const int64_t bh = by / p_count;
@@ -197,7 +219,8 @@ tc_sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       tma_prefetch_2d(&tmP, 0, r);
       bulk_prefetch(Eb + (size_t)(r / kC) * DK, DK * 4);
     }
-    for (int b = 0; b < kNV / 64; ++b) tma_prefetch_2d(&tmV, j0 + b * 64, r);
+    for (int b = 0; b < kNV / 64; ++b)
+      if (j0 + b * 64 < dv) tma_prefetch_2d(&tmV, j0 + b * 64, r);
   };
   if (tid == kTmaTid) {
     issue_x(BWD ? nc - 1 : 0, 0);
@@ -210,20 +233,19 @@ tc_sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   // ---- initial state: S^T fp32 (and, forward, its bf16 copy) from the state
   //      entering the segment (forward: S_in[p]) or the adjoint at its end
   //      (backward: D[p+1]).
+  constexpr int kQ = DK / 4;            // TMEM columns of one warp's quarter
+  constexpr int kW = kQ < 32 ? kQ : 32;  // columns per tensor-memory load / store
   {
+    const int jl = j0 + lg * 32 + lane;  // this thread's d_v column
+    const bool live = jl < dv;
     const float* Sp =
-        S_src + ((size_t)bh * (P + 1) + p + (BWD ? 1 : 0)) * DK * dv + j0 + lg * 32 + lane;
-    for (int c = cq * (DK / 4); c < (cq + 1) * (DK / 4); c += 32) {
-      float r[32];
+        S_src + ((size_t)bh * (P + 1) + p + (BWD ? 1 : 0)) * DK * dv + (live ? jl : 0);
+    for (int c = cq * kQ; c < (cq + 1) * kQ; c += kW) {
+      float r[kW];
 #pragma unroll
-      for (int u = 0; u < 32; ++u) r[u] = Sp[(size_t)(c + u) * dv];
-      tmem_st32(tmem + lane_off + c, r);
-      if (!BWD) {
-        uint32_t h[16];
-#pragma unroll
-        for (int u = 0; u < 16; ++u) h[u] = pack_bf16(r[2 * u], r[2 * u + 1]);
-        tmem_st16(tmem + lane_off + kColS16 + c / 2, h);
-      }
+      for (int u = 0; u < kW; ++u) r[u] = live ? Sp[(size_t)(c + u) * dv] : 0.f;
+      st_cols<kW>(tmem + lane_off + c, r);
+      if (!BWD) st_half<kW>(tmem + lane_off + kColS16 + c / 2, r);
     }
     tmem_st_wait();
   }
@@ -233,12 +255,16 @@ tc_sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   // state update.  Part 2: the bf16 copy of the scaled state (the A operand of
   // the next chunk's output MMAs); it waits until this chunk's output MMAs have
   // read the old copy.
-  constexpr int kQ = DK / 4;  // TMEM columns of one warp's quarter
   auto scale_part = [&](const float* sE, float* r) {
     const int c0 = cq * kQ;
+    if constexpr (kW == 32) {
 #pragma unroll
-    for (int c = 0; c < kQ; c += 32) tmem_ld32(tmem + lane_off + c0 + c, r + c);
-    tmem_ld_wait();
+      for (int c = 0; c < kQ; c += 32) tmem_ld32(tmem + lane_off + c0 + c, r + c);
+      tmem_ld_wait();
+    } else {
+      tmem_ld16(tmem + lane_off + c0, r);
+      tmem_ld_wait16(r);
+    }
     const float4* e4 = reinterpret_cast<const float4*>(sE + c0);
 #pragma unroll
     for (int u = 0; u < kQ / 4; ++u) {
@@ -249,17 +275,12 @@ tc_sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       r[4 * u + 3] *= e.w;
     }
 #pragma unroll
-    for (int c = 0; c < kQ; c += 32) tmem_st32(tmem + lane_off + c0 + c, r + c);
+    for (int c = 0; c < kQ; c += kW) st_cols<kW>(tmem + lane_off + c0 + c, r + c);
   };
   auto copy_part = [&](const float* r) {
     const int c0 = cq * kQ;
 #pragma unroll
-    for (int c = 0; c < kQ; c += 32) {
-      uint32_t h[16];
-#pragma unroll
-      for (int u = 0; u < 16; ++u) h[u] = pack_bf16(r[c + 2 * u], r[c + 2 * u + 1]);
-      tmem_st16(tmem + lane_off + kColS16 + (c0 + c) / 2, h);
-    }
+    for (int c = 0; c < kQ; c += kW) st_half<kW>(tmem + lane_off + kColS16 + (c0 + c) / 2, r + c);
     tmem_st_wait();
   };
 
@@ -414,7 +435,7 @@ cudaError_t launch_sweep(const Dims& d, const void* Qt, const void* Kt, const vo
   auto kern = tc_sweep_kernel<DK, BWD>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const unsigned grid = (unsigned)(d.B * d.H * p_count * (d.dv / kNV));
+  const unsigned grid = (unsigned)(d.B * d.H * p_count * ((d.dv + kNV - 1) / kNV));
   prof_start(st);
   kern<<<grid, kThreads, smem, st>>>(tq, tk, tv, tp, to, Eb, S_src, d.T,
                                      (int)d.dv, d.P, d.L, p_begin, p_count);
@@ -424,8 +445,8 @@ cudaError_t launch_sweep(const Dims& d, const void* Qt, const void* Kt, const vo
 }  // namespace
 
 bool tc_fwd_supported(const Dims& d) {
-  return d.bf16 && (d.dk == 128 || d.dk == 256) && d.dv % kNV == 0 && d.C == kC &&
-         d.L % kC == 0;
+  return d.bf16 && (d.dk == 64 || d.dk == 128 || d.dk == 256) && d.dv % 64 == 0 &&
+         d.C == kC && d.L % kC == 0;
 }
 
 cudaError_t tc_fwd_out(const Dims& d, const void* Qt, const void* Kt, const void* v,
@@ -433,8 +454,9 @@ cudaError_t tc_fwd_out(const Dims& d, const void* Qt, const void* Kt, const void
                        cudaStream_t st, int p_begin, int p_count) {
   if (p_count < 0) p_count = d.P - p_begin;
   cudaError_t e =
-      d.dk == 256 ? launch_sweep<256, false>(d, Qt, Kt, v, A, Eb, S_in, o, st, p_begin, p_count)
-                  : launch_sweep<128, false>(d, Qt, Kt, v, A, Eb, S_in, o, st, p_begin, p_count);
+      d.dk == 256   ? launch_sweep<256, false>(d, Qt, Kt, v, A, Eb, S_in, o, st, p_begin, p_count)
+      : d.dk == 128 ? launch_sweep<128, false>(d, Qt, Kt, v, A, Eb, S_in, o, st, p_begin, p_count)
+                    : launch_sweep<64, false>(d, Qt, Kt, v, A, Eb, S_in, o, st, p_begin, p_count);
   prof_mark("tc_fwd_out", st);
   return e;
 }
@@ -442,8 +464,9 @@ cudaError_t tc_fwd_out(const Dims& d, const void* Qt, const void* Kt, const void
 cudaError_t tc_bwd_dv(const Dims& d, const void* Qt, const void* Kt, const void* d_o,
                       const void* A, const float* Eb, const float* D, void* dv,
                       cudaStream_t st) {
-  cudaError_t e = d.dk == 256 ? launch_sweep<256, true>(d, Qt, Kt, d_o, A, Eb, D, dv, st, 0, d.P)
-                              : launch_sweep<128, true>(d, Qt, Kt, d_o, A, Eb, D, dv, st, 0, d.P);
+  cudaError_t e = d.dk == 256   ? launch_sweep<256, true>(d, Qt, Kt, d_o, A, Eb, D, dv, st, 0, d.P)
+                  : d.dk == 128 ? launch_sweep<128, true>(d, Qt, Kt, d_o, A, Eb, D, dv, st, 0, d.P)
+                                : launch_sweep<64, true>(d, Qt, Kt, d_o, A, Eb, D, dv, st, 0, d.P);
   prof_mark("tc_bwd_dv", st);
   return e;
 }

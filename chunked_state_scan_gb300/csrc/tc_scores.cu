@@ -48,7 +48,9 @@ tc_masked_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
   __shared__ int abort_word;  // set when a bounded wait of this CTA gives up
   const Waits wait{smem_u32(&abort_word), &g_scores_status};
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int nq = K / kQ;
+  // K slices of kQ columns; a last partial slice reads zeros past column K (the
+  // copy of a box past the end of a tensor fills it with zeros)
+  const int nq = (K + kQ - 1) / kQ;
   int64_t gi = 0;  // producer: (chunk, K slice) stages issued
 
   if (tid == 0) {
@@ -172,8 +174,8 @@ tc_masked_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
 
 }  // namespace
 
-bool tc_dA_supported(const Dims& d) { return d.bf16 && d.C == kC && d.dv % kQ == 0; }
-bool tc_A_supported(const Dims& d) { return d.bf16 && d.C == kC && d.dk % kQ == 0; }
+bool tc_dA_supported(const Dims& d) { return d.bf16 && d.C == kC && d.dv % 64 == 0; }
+bool tc_A_supported(const Dims& d) { return d.bf16 && d.C == kC && d.dk % 64 == 0; }
 
 namespace {
 cudaError_t launch_masked(const Dims& d, const void* X, const void* Y, int K, void* P,

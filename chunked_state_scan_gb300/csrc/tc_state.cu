@@ -87,13 +87,16 @@ tc_seg_state_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
   const int row = tid & (kM - 1), qd = tid >> 7;  // row within the tile, token quarter
   // block x = ((b h p) * (d_k / kM) + d_k tile) * (d_v / NT) + d_v tile: the CTAs of
   // one segment are launched together and share its operand tiles in L2
-  const int nx = dv / NT, ny = dk / kM;
+  // (a last partial tile of d_k rows or d_v columns reads zeros past the end of
+  // its operands and stores only the rows and columns that exist)
+  const int nx = (dv + NT - 1) / NT, ny = (dk + kM - 1) / kM;
   const int bx = (int)(blockIdx.x % nx), by = (int)((blockIdx.x / nx) % ny);
   const int64_t bhp = (int64_t)(blockIdx.x / nx) / ny;
   const int64_t bh = bhp / P;
   const int p = (int)(bhp % P);
   const int i0 = by * kM, j0 = bx * NT;
   const int i = i0 + row;
+  const int nE = dk - i0 < kM ? dk - i0 : kM;  // rows of this tile that exist
   const int64_t row0 = bh * T + (int64_t)p * L;  // first token row of the segment
   const int nblk = (int)(L / kTok);
 
@@ -123,12 +126,12 @@ tc_seg_state_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
     const int s = it % SG;
     unsigned char* base = sm + s * kStageBytes;
     const int32_t r = blk_row(it);
-    mbar_expect_tx(&tma_bar[s], PRE ? kXBytes + kM * 4 + kBBytes : kStageBytes);
+    mbar_expect_tx(&tma_bar[s], PRE ? kXBytes + nE * 4 + kBBytes : kStageBytes);
     for (int mb = 0; mb < kM / 64; ++mb) {
       tma_load_2d(base + mb * 8192, &tmX, i0 + mb * 64, r, &tma_bar[s]);
       if (!PRE) tma_load_2d(base + kXBytes + mb * 8192, &tmG, i0 + mb * 64, r, &tma_bar[s]);
     }
-    if (PRE) bulk_load(base + kXBytes, Eb + (size_t)(r / kTok) * dk + i0, kM * 4, &tma_bar[s]);
+    if (PRE) bulk_load(base + kXBytes, Eb + (size_t)(r / kTok) * dk + i0, nE * 4, &tma_bar[s]);
     for (int nb = 0; nb < NT / 64; ++nb)
       tma_load_2d(base + kXBytes + GB + nb * 8192, &tmY, j0 + nb * 64, r, &tma_bar[s]);
   };
@@ -175,30 +178,33 @@ tc_seg_state_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
     if (PRE) {
       // every 16-byte group of 8 rows of the tile scaled in place (2 per thread, the
       // same 8 rows in every stage): this stage's factor of each of those rows from
-      // the running products this thread carries
-      const float4* e4 = reinterpret_cast<const float4*>(xbuf + kXBytes + 4 * p_r8);
-      const float4 ea = e4[0], eb = e4[1];
-      const float ev[8] = {ea.x, ea.y, ea.z, ea.w, eb.x, eb.y, eb.z, eb.w};
-      float f[8];
+      // the running products this thread carries (rows past d_k are zeros and stay
+      // so; their factors were not loaded)
+      if (p_r8 < nE) {
+        const float4* e4 = reinterpret_cast<const float4*>(xbuf + kXBytes + 4 * p_r8);
+        const float4 ea = e4[0], eb = e4[1];
+        const float ev[8] = {ea.x, ea.y, ea.z, ea.w, eb.x, eb.y, eb.z, eb.w};
+        float f[8];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        if (REV) run8[u] *= ev[u];
-        f[u] = run8[u];
-        if (!REV) run8[u] *= ev[u];
-      }
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int c = tid + h * kStateThreads;  // 64 tokens x 2 row blocks x 8 groups
-        const int t = c >> 4, mb = (c >> 3) & 1, c8 = c & 7;
-        uint4* ptr = reinterpret_cast<uint4*>(xbuf + mb * 8192 + sw128((uint32_t)t, (uint32_t)c8));
-        uint4 wv = *ptr;
-        __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(&wv);
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const float2 x2 = __bfloat1622float2(h2[u]);
-          h2[u] = __floats2bfloat162_rn(x2.x * f[2 * u], x2.y * f[2 * u + 1]);
+        for (int u = 0; u < 8; ++u) {
+          if (REV) run8[u] *= ev[u];
+          f[u] = run8[u];
+          if (!REV) run8[u] *= ev[u];
         }
-        *ptr = wv;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int c = tid + h * kStateThreads;  // 64 tokens x 2 row blocks x 8 groups
+          const int t = c >> 4, mb = (c >> 3) & 1, c8 = c & 7;
+          uint4* ptr = reinterpret_cast<uint4*>(xbuf + mb * 8192 + sw128((uint32_t)t, (uint32_t)c8));
+          uint4 wv = *ptr;
+          __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(&wv);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const float2 x2 = __bfloat1622float2(h2[u]);
+            h2[u] = __floats2bfloat162_rn(x2.x * f[2 * u], x2.y * f[2 * u + 1]);
+          }
+          *ptr = wv;
+        }
       }
     } else
     // A = (w .* x) written over x; this thread: row i, tokens 16 qd .. 16 qd + 15
@@ -262,16 +268,16 @@ tc_seg_state_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
   cbar();
   const bool ok = !wait.aborted();
   // PRE: gamma_p of every row is the product over all the segment's chunks
-  if (PRE && REV && ok && gamma && bx == 0 && tid < 16)
+  if (PRE && REV && ok && gamma && bx == 0 && tid < 16 && p_r8 < nE)
 #pragma unroll
     for (int u = 0; u < 8; ++u) gamma[((size_t)bh * P + p) * dk + i0 + p_r8 + u] = run8[u];
-  if (ok && warp < 4) {
+  if (ok && warp < 4 && warp * 32 < nE) {
     const int last = nblk - 1;
     wt(&mma_bar[last % SG], (last / SG) & 1);
     tc_fence_after();
     float* orow = out + (((size_t)bh * (P + 1) + p + slot_off) * dk + i) * dv + j0;
 #pragma unroll 1
-    for (int c = 0; c < NT; c += 32) {
+    for (int c = 0; c < NT && j0 + c < dv; c += 32) {
       float r[32];
       tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + c, r);
       tmem_ld_wait();
@@ -374,7 +380,8 @@ static cudaError_t launch_state(const Dims& d, const void* x, const void* y, con
   auto kern = tc_seg_state_kernel<NT, REV, PRE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const unsigned grid = (unsigned)(d.B * d.H * d.P * (d.dk / kM) * (d.dv / NT));
+  const unsigned grid =
+      (unsigned)(d.B * d.H * d.P * ((d.dk + kM - 1) / kM) * ((d.dv + NT - 1) / NT));
   prof_start(st);
   kern<<<grid, kStateBlock, smem, st>>>(tx, tg, ty, Eb, out, gamma, d.T, (int)d.dk,
                                           (int)d.dv, d.P, d.L, slot_off);
@@ -393,7 +400,7 @@ static cudaError_t launch_state_any(const Dims& d, const void* x, const void* y,
 }
 
 bool tc_state_supported(const Dims& d) {
-  return d.bf16 && d.dk % kM == 0 && d.dv % 128 == 0 && d.L % kTok == 0;
+  return d.bf16 && d.dk % 64 == 0 && d.dv % 64 == 0 && d.L % kTok == 0;
 }
 
 cudaError_t tc_chunk_state(const Dims& d, const void* k, const void* v, const void* g,

@@ -80,7 +80,11 @@ typedef enum { ZECO_F32 = 0, ZECO_BF16 = 1 } zeco_dtype;
 
 /* Kernel path.  AUTO picks the tcgen05 tensor-core kernels for bf16 shapes they
  * support and the fp32 SIMT kernels otherwise; SIMT and TC force one path
- * (TC on an unsupported shape returns ZECO_ERR_UNSUPPORTED). */
+ * (TC on an unsupported shape returns ZECO_ERR_UNSUPPORTED).  The tensor-core
+ * path takes bf16 shapes whose d_k and d_v are multiples of 64: with C = 64 and
+ * d_k in {64, 128, 256} every step of the forward and backward runs on tensor
+ * cores; otherwise (d_k = 192, or C != 64) the segment states do, and the chunk
+ * sweeps run on CUDA cores. */
 typedef enum { ZECO_PATH_AUTO = 0, ZECO_PATH_SIMT = 1, ZECO_PATH_TC = 2 } zeco_path;
 
 /* Form of the decay (the ZeCO pages study the diagonal, per-d_k-row decay of
@@ -128,8 +132,8 @@ int64_t zeco_gla_segments(const zeco_shape *shape);
  * zeco_gla_bwd: the incoming global state of every segment, S_in
  * [B,H,P_eff+1,dk,dv] fp32 (S_in[0] = S0, S_in[P_eff] = S_final), then the
  * segment decays gamma [B,H,P_eff,dk] fp32.  When the shape resolves to the
- * tensor-core path with its decay pass (d_k in {128, 256}, d_v a multiple of
- * 128, C = 64), `saved` also keeps the operands the forward computes once
+ * tensor-core path with its decay pass (d_k in {64, 128, 256}, d_v a multiple
+ * of 64, C = 64), `saved` also keeps the operands the forward computes once
  * and the backward reads again instead of recomputing them: the
  * decay-weighted Q~ = q .* e^{b} and K~ = k .* e^{-b} [B,H,T,dk] bf16 (Pith
  * review of ZeCO, minor comment 4; b the cumulative log-decay from the chunk

@@ -137,6 +137,25 @@ def test_path_resolution(lib):
     assert z.resolve_path(_shape(C=128, dk=128, dv=128, K=4)) == "tc"
 
 
+@pytest.mark.parametrize("dk,dv", [(64, 64), (64, 512), (128, 192), (256, 320), (64, 448),
+                                   (192, 512), (256, 512)])
+def test_bf16_shapes_resolve_to_the_tensor_core_path(lib, dk, dv):
+    """Every bf16 shape with C = 64 and d_k, d_v multiples of 64 runs on the
+    tensor-core path (d_k = 192 with its sweeps on CUDA cores); others on the
+    CUDA-core path."""
+    import chunked_state_scan_gb300 as z
+    assert z.resolve_path(_shape(T=4096, P=4, K=1, dk=dk, dv=dv)) == "tc"
+    assert z.resolve_path(_shape(T=4096, P=4, K=1, dk=dk, dv=dv, path="simt")) == "simt"
+
+
+@pytest.mark.parametrize("dk,dv", [(96, 128), (128, 96), (32, 32)])
+def test_bf16_shapes_off_the_64_grid_take_the_cuda_core_path(lib, dk, dv):
+    import chunked_state_scan_gb300 as z
+    assert z.resolve_path(_shape(T=4096, P=4, K=1, dk=dk, dv=dv)) == "simt"
+    with pytest.raises(z.ZecoError):
+        z.resolve_path(_shape(T=4096, P=4, K=1, dk=dk, dv=dv, path="tc"))
+
+
 def test_decay_forms_workspace_and_arguments(lib):
     import chunked_state_scan_gb300 as z
     diag = _shape(T=4096, P=4, path="simt")

@@ -134,11 +134,18 @@ def test_bf16_slow_decay_carry_dominated(z, path):
                                              (1, 1, 4096, 128, 384, 2, 1),
                                              (1, 1, 256, 256, 512, 4, 8),
                                              (1, 2, 2048, 256, 128, 4, 2),
-                                             (1, 1, 2048, 256, 384, 2, 4)])
+                                             (1, 1, 2048, 256, 384, 2, 4),
+                                             (1, 2, 1024, 64, 64, 4, 2),
+                                             (1, 1, 2048, 64, 512, 2, 1),
+                                             (2, 1, 1024, 128, 192, 4, 2),
+                                             (1, 1, 1024, 256, 320, 2, 4),
+                                             (1, 1, 1024, 64, 448, 2, 2)])
 def test_bf16_tensor_core_path_shapes(z, B, H, T, dk, dv, P, K):
     """The tcgen05 path on several tilings: one token block per segment (L = 64),
     d_v tiles of 128 and 256, one and several d_k tiles, several batches.  Every
-    d_v (128, 256, 384, 512) runs dq, dk and dlog_alpha on the tensor-core kernel."""
+    d_v (128, 256, 384, 512) runs dq, dk and dlog_alpha on the tensor-core kernel.
+    d_k = 64 and d_v not a multiple of 128 (64, 192, 320, 448): partial tiles that
+    read zeros past the end of the operands and store only what exists."""
     shape = z.make_shape(B, H, T, dk, dv, P, K, 64, "bf16", "tc")
     assert z.resolve_path(shape) == "tc"
     x = workloads.make_custom(B, H, T, dk, dv, dtype="bf16", seed=T + dk + dv,
@@ -148,6 +155,20 @@ def test_bf16_tensor_core_path_shapes(z, B, H, T, dk, dv, P, K):
     assert not any(n.startswith("simt") for n in names), names
     errs = parity.compare_full(z, x, P, K, 64, "bf16", path="tc")
     _assert(errs, "bf16", f"tc B{B} H{H} T{T} dk{dk} dv{dv} P{P}")
+
+
+@pytest.mark.parametrize("dk,dv,C", [(192, 512, 64), (64, 128, 128)])
+def test_bf16_tensor_core_segment_states_with_cuda_core_sweeps(z, dk, dv, C):
+    """Shapes whose segment states run on tensor cores (a partial d_k tile of 64
+    rows: d_k = 192, or d_k = 64 with C = 128) while the sweeps run on CUDA cores."""
+    shape = z.make_shape(1, 2, 2048, dk, dv, 2, 1, C, "bf16", "tc")
+    assert z.resolve_path(shape) == "tc"
+    x = workloads.make_custom(1, 2, 2048, dk, dv, dtype="bf16", seed=dk + dv + C,
+                              qk_scale=1 / 16, s0_scale=0.2)
+    names, _ = parity.kernel_names(z, lambda: parity.run_gpu(z, x, 2, 1, C, path="tc"))
+    assert "tc_chunk_state" in names and "tc_dstate_local" in names, names
+    errs = parity.compare_full(z, x, 2, 1, C, "bf16", path="tc")
+    _assert(errs, "bf16", f"tc states, simt sweeps dk{dk} dv{dv} C{C}")
 
 
 @pytest.mark.parametrize("B,H,T,dk,P,K", [(1, 1, 384, 256, 2, 8),    # 3 chunks per segment
@@ -309,7 +330,8 @@ def test_f32_decay_forms(z, decay):
     _assert(errs, "f32", f"f32 decay form {decay}")
 
 
-@pytest.mark.parametrize("dk,dv", [(128, 512), (256, 512), (128, 256), (256, 128)])
+@pytest.mark.parametrize("dk,dv", [(128, 512), (256, 512), (128, 256), (256, 128), (64, 64),
+                                   (64, 192)])
 @pytest.mark.parametrize("decay", [1, 2])
 def test_bf16_decay_forms_on_tensor_cores(z, decay, dk, dv):
     # the tensor-core kernels read the scalar log-decay once per token (none for

@@ -67,12 +67,13 @@ def _fill_array_with_other_data(z, stream):
     torch.cuda.synchronize()
 
 
-# fp32 and bf16 on the CUDA-core path (d_k = d_v = 64), and a bf16 shape on the
+# fp32 and bf16 on the CUDA-core path (d_k = 64; d_v = 64, and for bf16 d_v = 96,
+# off the tensor-core kernels' 64-column grid), and a bf16 shape on the
 # tensor-core path, whose backward also keeps the score gradient dA in the array
 # and writes it from a second stream
 CASES = {
     "f32_simt": (workloads.TINY_F32.replace(dtype="f32", s0_scale=0.2), "simt"),
-    "bf16_simt": (workloads.TINY_F32.replace(dtype="bf16", s0_scale=0.2), "simt"),
+    "bf16_simt": (workloads.TINY_F32.replace(dtype="bf16", s0_scale=0.2, dv=96), "simt"),
     "bf16_tc": (workloads.Workload("tc", B=1, H=1, T=2048, dk=128, dv=512, P=2, K=4, C=64,
                                    dtype="bf16", seed=12, qk_scale=1 / 16, v_scale=1.0,
                                    x_mean=0.0, s0_scale=0.2, bwd=True), "tc"),
