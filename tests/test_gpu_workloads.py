@@ -93,3 +93,12 @@ def test_more_than_65535_segment_blocks_sampled(z):
                                       dv=128, P=8192, K=4)
     assert z.segments(z.make_shape(w.B, w.H, w.T, w.dk, w.dv, w.P, w.K, w.C, w.dtype)) == 8192
     _sample_check(z, w, [(0, 0), (0, 7)], with_bwd=True, COLS=[0, 77, 127], ROWS=[3, 100])
+
+
+def test_small_head_fwdbwd_sampled(z):
+    # d_k = 64, d_v = 128 at the 1M-token size: partial 128-row tiles in the
+    # segment-state and dq/dk kernels, native d_k = 64 sweeps
+    w = workloads.SMALL_HEAD_FWDBWD
+    assert z.resolve_path(z.make_shape(w.B, w.H, w.T, w.dk, w.dv, w.P, w.K, w.C,
+                                       w.dtype)) == "tc"
+    _sample_check(z, w, [(0, 1)], with_bwd=True, COLS=[0, 63, 64, 127], ROWS=[0, 31, 63])

@@ -92,7 +92,13 @@ PROFILE_FWDBWD = LONG_FWDBWD.replace(name="profile_fwdbwd_T32768_P8", T=32768, P
 # rest of the step, the regime in which hiding them beside other work matters.
 SCAN_BOUND_FWDBWD = LONG_FWDBWD.replace(name="long_fwdbwd_T1048576_P16384", P=16384)
 
-BY_NAME = {w.name: w for w in WORKLOADS + [PROFILE_FWDBWD, SCAN_BOUND_FWDBWD]}
+# The throughput workload with small heads (d_k = 64, d_v = 128): the tensor-core
+# kernels' partial tiles of 128 d_k rows and the native d_k = 64 sweeps.
+SMALL_HEAD_FWDBWD = LONG_FWDBWD.replace(name="small_head_fwdbwd_T1048576_dk64_dv128", dk=64,
+                                        dv=128, K=2)
+
+BY_NAME = {w.name: w for w in WORKLOADS + [PROFILE_FWDBWD, SCAN_BOUND_FWDBWD,
+                                            SMALL_HEAD_FWDBWD]}
 
 
 def make_inputs(w: Workload, device="cpu", seed: int | None = None):
