@@ -608,8 +608,10 @@ def measure(w, args, world, rank, local, want_e2e=True, want_cpu=True, quiet=Fal
     # are pipelined the way a caller would run them: uploads and downloads have
     # their own streams, inputs and outputs are double-buffered on the device, so
     # step i+1's upload and step i-1's download overlap step i's kernels.  Each
-    # tensor's copy is cut into kCopyStreams contiguous pieces on as many streams
-    # per direction, so that several copy engines share the transfer.
+    # tensor's copy may be cut into kCopyStreams contiguous pieces on as many
+    # streams per direction (--e2e-copy-streams; default one: the host link, not
+    # the copy engines, bounds the copies, and 1, 2, 4 or 8 streams measured
+    # within 3% of each other, one the fastest).
     if want_e2e and w.bwd:
         names_in = ["q", "k", "v", "log_alpha", "do", "dS_final", "S0"]
         host_in = {n: x[n].cpu().pin_memory() for n in names_in}
@@ -623,7 +625,7 @@ def measure(w, args, world, rank, local, want_e2e=True, want_cpu=True, quiet=Fal
         del x
         bi = sum(t.numel() * t.element_size() for t in host_in.values())
         bo = sum(t.numel() * t.element_size() for t in host_out.values())
-        kCopyStreams = 4
+        kCopyStreams = args.e2e_copy_streams
         s_up = [torch.cuda.Stream(device=dev) for _ in range(kCopyStreams)]
         s_down = [torch.cuda.Stream(device=dev) for _ in range(kCopyStreams)]
         ev_up = [[torch.cuda.Event() for _ in range(kCopyStreams)] for _ in range(2)]
@@ -697,7 +699,8 @@ def measure(w, args, world, rank, local, want_e2e=True, want_cpu=True, quiet=Fal
                        "copy_bound": {**cb, "t_copy_ms": t_copy * 1e3, "bound_tokens_s": bound,
                                       "frac": ev / bound},
                        "note": "uploads, kernels and downloads of consecutive steps pipelined "
-                               "(each tensor's copy in 4 pieces on 4 streams per direction); "
+                               f"(each tensor's copy in {kCopyStreams} pieces on "
+                               f"{kCopyStreams} streams per direction); "
                                "every step's copies inside the timed region; copy_bound: plain "
                                "pinned copies of 2 GiB on this box"}
 
@@ -886,6 +889,8 @@ def main(argv=None):
     ap.add_argument("--workload", default=workloads.LONG_FWDBWD.name)
     ap.add_argument("--path", default="auto", choices=["auto", "simt", "tc"])
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--e2e-copy-streams", type=int, default=1,
+                    help="streams (and pieces of each tensor's copy) per direction in e2e")
     ap.add_argument("--cpu-sample-tokens", type=int, default=16384)
     ap.add_argument("--ref-sample-tokens", type=int, default=4096)
     ap.add_argument("--no-cpu-baseline", action="store_true")
