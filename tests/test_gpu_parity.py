@@ -414,8 +414,8 @@ def test_low_parallelism_shape_is_split_and_unchanged(z):
 # ------------------------------------- edge cases on the tensor-core dq/dk kernel
 
 
-def _tc_edge_inputs(case, device="cpu"):
-    kw = dict(B=1, H=2, T=2048, dk=128, dv=512, dtype="bf16", seed=31, qk_scale=1 / 12,
+def _tc_edge_inputs(case, dk=128, dv=512, device="cpu"):
+    kw = dict(B=1, H=2, T=2048, dk=dk, dv=dv, dtype="bf16", seed=31, qk_scale=1 / 12,
               s0_scale=0.3, device=device)
     if case == "slow_decay":
         kw.update(x_mean=8.0, s0_scale=0.5)   # log_alpha ~ -2e-5: the carry dominates
@@ -426,18 +426,20 @@ def _tc_edge_inputs(case, device="cpu"):
     return workloads.make_custom(**kw)
 
 
+@pytest.mark.parametrize("dk,dv", [(128, 512), (64, 64)])
 @pytest.mark.parametrize("case", ["slow_decay", "fast_decay", "no_decay"])
-def test_bf16_tc_dq_dk_kernel_edge_cases(z, case):
+def test_bf16_tc_dq_dk_kernel_edge_cases(z, case, dk, dv):
     """The decay regimes the method has, on the tensor-core dq/dk/dlog_alpha
-    kernel (d_v = 512): the carry-dominated slow decay, a fast decay whose chunk
-    log-decay sums reach about -72 (the chunk factorisation's range ends at -80),
-    and exactly no decay.  Besides every full tensor, the first and last two
-    chunks of every segment are checked on their own: there the states carried
-    across segments (forward) and back (adjoint) weigh most."""
-    B, H, T, dk, dv, P, K = 1, 2, 2048, 128, 512, 8, 2
+    kernel (d_v = 512, and d_k = d_v = 64 with its partial tiles): the
+    carry-dominated slow decay, a fast decay whose chunk log-decay sums reach
+    about -72 (the chunk factorisation's range ends at -80), and exactly no
+    decay.  Besides every full tensor, the first and last two chunks of every
+    segment are checked on their own: there the states carried across segments
+    (forward) and back (adjoint) weigh most."""
+    B, H, T, P, K = 1, 2, 2048, 8, 2
     shape = z.make_shape(B, H, T, dk, dv, P, K, 64, "bf16", "tc")
     assert z.resolve_path(shape) == "tc"
-    x = _tc_edge_inputs(case)
+    x = _tc_edge_inputs(case, dk, dv)
     csum = x["log_alpha"].float().view(B, H, T // 64, 64, dk).sum(3)
     if case == "fast_decay":
         assert -80.0 < float(csum.min()) and float(csum.max()) < -60.0
@@ -455,7 +457,7 @@ def test_bf16_tc_dq_dk_kernel_edge_cases(z, case):
                  ("dlog_alpha", rg["dlog_alpha"])):
         errs[n + "[segment ends]"] = parity.rel_l2(parity.to_np(res[n])[:, :, idx],
                                                    r[:, :, idx])
-    _assert(errs, "bf16", f"tc {case}")
+    _assert(errs, "bf16", f"tc {case} dk {dk} dv {dv}")
 
 
 @pytest.mark.parametrize("x_mean", [0.0, 8.0])
