@@ -54,6 +54,25 @@ def test_f32_invariance_to_P_K_C(z, P, K, C):
     _assert(errs, "f32", f"P={P} K={K} C={C}")
 
 
+def test_bf16_tensor_core_results_do_not_depend_on_K(z):
+    """The segment scans run on K blocks of d_k rows (the pages' pipelined All-Scan
+    granularity); every row's scan is the same arithmetic whatever the block, so
+    the tensor-core path gives bit-identical outputs for every K."""
+    B, H, T, dk, dv, P = 1, 2, 2048, 128, 256, 4
+    x = workloads.make_custom(B, H, T, dk, dv, dtype="bf16", seed=41, qk_scale=1 / 16,
+                              s0_scale=0.3)
+    ref = None
+    for K in (1, 2, 4, 8):
+        assert z.resolve_path(z.make_shape(B, H, T, dk, dv, P, K, 64, "bf16", "tc")) == "tc"
+        res = parity.run_gpu(z, x, P, K, 64, path="tc")
+        res.pop("saved")
+        if ref is None:
+            ref = res
+            continue
+        for n, t in res.items():
+            assert torch.equal(t, ref[n]), f"K={K}: {n} differs from K=1"
+
+
 @pytest.mark.parametrize("case", ["no_decay", "slow_decay", "fast_decay", "single_chunk",
                                   "ragged_tiles", "min_width", "no_init_no_dsf"])
 def test_f32_edge_cases(z, case):
