@@ -176,6 +176,36 @@ def test_bf16_tensor_core_path_shapes(z, B, H, T, dk, dv, P, K):
     _assert(errs, "bf16", f"tc B{B} H{H} T{T} dk{dk} dv{dv} P{P}")
 
 
+def _random_tc_shapes(n, seed=2026):
+    """Seeded shapes on the tensor-core path's grid: d_k in {64, 128, 256}, d_v a
+    multiple of 64, a few segments of a few chunks, K dividing d_k."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(n):
+        dk = int(rng.choice([64, 128, 256]))
+        dv = int(64 * rng.integers(1, 9))
+        P = int(rng.choice([1, 2, 4]))
+        L = int(64 * rng.integers(1, 5))
+        K = int(rng.choice([k for k in (1, 2, 4, 8) if dk % k == 0]))
+        out.append((int(rng.integers(1, 3)), int(rng.integers(1, 3)), P * L, dk, dv, P, K))
+    return out
+
+
+@pytest.mark.parametrize("B,H,T,dk,dv,P,K", _random_tc_shapes(10))
+def test_bf16_tensor_core_random_shapes(z, B, H, T, dk, dv, P, K):
+    """Seeded random shapes across the tensor-core grid (full and partial d_k and
+    d_v tiles, 1-4 chunks per segment, several batches and heads) against the
+    oracle, every output and state."""
+    shape = z.make_shape(B, H, T, dk, dv, P, K, 64, "bf16", "tc")
+    assert z.resolve_path(shape) == "tc"
+    x = workloads.make_custom(B, H, T, dk, dv, dtype="bf16", seed=T + dk + dv + P,
+                              qk_scale=1 / 16, s0_scale=0.2)
+    names, _ = parity.kernel_names(z, lambda: parity.run_gpu(z, x, P, K, 64, path="tc"))
+    assert not any(n.startswith("simt") for n in names), names
+    errs = parity.compare_full(z, x, P, K, 64, "bf16", path="tc")
+    _assert(errs, "bf16", f"tc random B{B} H{H} T{T} dk{dk} dv{dv} P{P} K{K}")
+
+
 @pytest.mark.parametrize("dk,dv,C", [(192, 512, 64), (64, 128, 128)])
 def test_bf16_tensor_core_segment_states_with_cuda_core_sweeps(z, dk, dv, C):
     """Shapes whose segment states run on tensor cores (a partial d_k tile of 64
