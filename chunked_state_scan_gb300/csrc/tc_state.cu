@@ -18,7 +18,9 @@
 // writes gamma_p[i] = exp(sum_{t in segment} g_t[i]).
 //
 // Tiling: one CTA = 128 d_k rows (M) x NT d_v columns (N, 256 or 128) of one
-// (b, h, segment); K = 64 tokens per stage, 3 stages.  A = (w .* x)^T is
+// (b, h, segment); K = 64 tokens per stage, 3 stages (4 with the decay pass's
+// operands, one CTA per SM).  A last tile of d_k = 64 or 192 rows, or of d_v not
+// a multiple of NT, is partial.  A = (w .* x)^T is
 // written by the threads straight into the 128B-swizzled MN-major operand
 // layout (row i contiguous over tokens' rows); B = y arrives by TMA in the
 // same layout.  The accumulator lives in TMEM (NT fp32 columns); one thread
