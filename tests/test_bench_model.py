@@ -47,3 +47,24 @@ def test_implementation_bytes_of_the_tensor_core_step():
     total = sum(kb[k] for k in tc)
     assert total == 26832
     assert abs(total / bench.zeco_operator_bytes_per_token(DK, DV, L) - 1.9014) < 1e-4
+
+
+def test_scan_overlap_instrument_on_synthetic_intervals():
+    # the pages' Eq. 11 instrument: the share of the scan's kernel time during which
+    # no diagonal-attention kernel (A forward, dA backward) runs
+    iv = [("tc_A", 0.0, 1.0), ("seg_scan_fwd", 0.5, 1.5),      # half of the scan overlapped
+          ("tc_dA", 2.0, 3.0), ("seg_scan_rev", 2.0, 2.5)]     # all of it overlapped
+    out = bench.scan_overlap(iv)
+    assert abs(out["fwd"]["non_overlapped_frac"] - 0.5) < 1e-12
+    assert abs(out["bwd"]["non_overlapped_frac"] - 0.0) < 1e-12
+    assert abs(out["fwd"]["scan_ms"] - 1.0) < 1e-12
+    # no diagonal-attention kernel in the run: no figure for that direction
+    assert "fwd" not in bench.scan_overlap([("seg_scan_fwd", 0.0, 1.0)])
+
+
+def test_kernel_names_map_to_their_byte_counts():
+    kb = bench.kernel_bytes_per_token(DK, DV, L)
+    for name in ("tc_decay", "tc_A", "tc_chunk_state", "seg_scan_fwd", "tc_fwd_out", "tc_dA",
+                 "tc_dstate_local", "seg_scan_rev", "tc_bwd_dv", "tc_bwd_dq", "tc_bwd_dk"):
+        assert bench.canonical_kernel(name) in kb, name
+    assert bench.canonical_kernel("tc_dA") == "dA" and bench.canonical_kernel("tc_A") == "A"
