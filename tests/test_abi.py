@@ -244,3 +244,22 @@ def test_binding_rejects_bad_tensors_before_the_library():
         z._expect(q, "k", torch.device("cuda", 0))
     with pytest.raises(TypeError):
         z._expect([1, 2], "k", cpu)
+
+
+def test_schedule_and_profiling_switches_on_the_host(lib):
+    """zeco_set_overlap takes the modes 0-4 only; the profiling switch records
+    nothing while it is off (no GPU work: no call is enqueued)."""
+    import chunked_state_scan_gb300 as z
+    try:
+        for bad in (-1, 5, 1 << 20):
+            assert lib.zeco_set_overlap(bad) == z.ZECO_ERR_ARG
+        for mode in range(5):
+            assert lib.zeco_set_overlap(mode) == z.ZECO_OK
+    finally:
+        assert lib.zeco_set_overlap(z.OVERLAP_DEFAULT) == z.ZECO_OK
+    lib.zeco_set_profile_events.argtypes = [ctypes.c_void_p, ctypes.c_int]
+    lib.zeco_profile_kernel_name.restype = ctypes.c_char_p
+    assert lib.zeco_set_profile_events(None, 0) == z.ZECO_OK
+    assert lib.zeco_profile_event_count() == 0
+    assert lib.zeco_profile_kernel_name(0) is None
+    assert lib.zeco_profile_kernel_name(-1) is None
