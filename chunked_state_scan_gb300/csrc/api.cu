@@ -55,6 +55,14 @@ int check_shape(const zeco_shape* s, Dims* d) {
   d->L = L;
   d->bf16 = s->dtype == ZECO_BF16;
   d->decay = s->decay;
+  // Chunk length.  The chunked form is exact for any chunk length (results are
+  // the token recurrence's, up to rounding), and a 128-token chunk's decay range
+  // (the sum of log_alpha over a chunk above -80) implies that of its 64-token
+  // halves, so a bf16 call asking for C = 128 that does not force the CUDA-core
+  // path is evaluated with C = 64: the tensor-core kernels' chunk, and one the
+  // CUDA-core kernels' shared memory holds at every width.  (Shorter chunks are
+  // kept: their range may be what the caller needs.)
+  if (d->bf16 && s->path != ZECO_PATH_SIMT && s->C == 128) d->C = 64;
   // Segments on one GPU.  The P segments of the method exchange their states
   // through the segment scan; the decomposition is exact for any split, so when
   // B*H*P is too small to give the chunk sweeps a wave of CTAs (one per 128 d_v
@@ -63,9 +71,10 @@ int check_shape(const zeco_shape* s, Dims* d) {
   // below, the `saved` layout included, uses the effective count.
   constexpr int64_t kWave = 152;
   const int64_t tiles = (s->dv + 127) / 128;
+  const int64_t C = d->C;
   int64_t m = 1;
-  while (s->B * s->H * s->P * m * tiles < kWave && m < 64 && s->T % (s->P * m * 2 * s->C) == 0 &&
-         s->T / (s->P * m * 2) >= 4 * (int64_t)s->C && s->B * s->H * s->P * m * 2 <= kMaxBHP)
+  while (s->B * s->H * s->P * m * tiles < kWave && m < 64 && s->T % (s->P * m * 2 * C) == 0 &&
+         s->T / (s->P * m * 2) >= 4 * C && s->B * s->H * s->P * m * 2 <= kMaxBHP)
     m *= 2;
   d->P = (int)(s->P * m);
   d->L = s->T / d->P;

@@ -69,7 +69,8 @@ def test_sizes_follow_the_layout(lib):
     # gradient too, in the backward)
     bc = 4 * (1 << 20) * 256 * 2
     assert z.workspace_bytes(_shape(decay="scalar", path="simt"), False) == bc
-    assert z.workspace_bytes(_shape(decay="scalar", C=128, dk=128, dv=128, K=4), False) == bc // 2
+    # (C = 32: the tensor-core segment states, the CUDA-core sweeps)
+    assert z.workspace_bytes(_shape(decay="scalar", C=32, dk=128, dv=128, K=4), False) == bc // 2
     # the SIMT path keeps no decay-weighted operands
     simt = _shape(path="simt", dtype="f32", dk=64, dv=64)
     st64 = 4 * 65 * 64 * 64 * 4
@@ -129,12 +130,22 @@ def test_path_resolution(lib):
     # fp32 at full width does not fit the SIMT kernels' shared memory with C=128
     with pytest.raises(z.ZecoError):
         z.resolve_path(_shape(dtype="f32", C=128, path="simt"))
-    # nor does bf16: C = 128 takes the tensor-core segment states but the CUDA-core
-    # sweeps, so d_k = 256 fits neither path; d_k = 128, d_v = 128 fits
+    # nor does bf16 on the CUDA-core path; on the tensor-core path a bf16 call with
+    # C = 128 is evaluated at the kernels' C = 64 (results do not depend on C), with
+    # the same scratch sizes and segment count
+    with pytest.raises(z.ZecoError):
+        z.resolve_path(_shape(C=128, path="simt"))
     for path in ("tc", "auto"):
-        with pytest.raises(z.ZecoError):
-            z.resolve_path(_shape(C=128, path=path))
+        s128, s64 = _shape(C=128, path=path), _shape(C=64, path=path)
+        assert z.resolve_path(s128) == "tc"
+        assert z.saved_bytes(s128) == z.saved_bytes(s64)
+        assert z.workspace_bytes(s128, True) == z.workspace_bytes(s64, True)
+        assert z.segments(s128) == z.segments(s64)
     assert z.resolve_path(_shape(C=128, dk=128, dv=128, K=4)) == "tc"
+    # shorter chunks are kept as asked (their decay range may be what the caller
+    # needs): C = 32 takes the tensor-core segment states and the CUDA-core sweeps
+    # (GPU tests check which kernels run)
+    assert z.resolve_path(_shape(C=32, dk=128, dv=128, K=4)) == "tc"
 
 
 @pytest.mark.parametrize("dk,dv", [(64, 64), (64, 512), (128, 192), (256, 320), (64, 448),
@@ -263,3 +274,21 @@ def test_schedule_and_profiling_switches_on_the_host(lib):
     assert lib.zeco_profile_event_count() == 0
     assert lib.zeco_profile_kernel_name(0) is None
     assert lib.zeco_profile_kernel_name(-1) is None
+
+
+def test_every_accepted_bf16_shape_runs_under_auto(lib):
+    """With path AUTO every bf16 width and chunk length the boundary accepts
+    resolves to a path (C = 128 runs at C = 64); fp32 at C = 128 with d_k above
+    128 does not fit the CUDA-core kernels' shared memory and is refused."""
+    import chunked_state_scan_gb300 as z
+    refused = []
+    for dtype in ("bf16", "f32"):
+        for dk in range(16, 257, 16):
+            for dv in range(32, 513, 32):
+                for C in (16, 32, 64, 128):
+                    try:
+                        z.resolve_path(_shape(dtype=dtype, T=16384, P=4, K=1, dk=dk, dv=dv, C=C))
+                    except z.ZecoError:
+                        refused.append((dtype, dk, C))
+    assert not [r for r in refused if r[0] == "bf16"], refused[:5]
+    assert sorted(set(refused)) == [("f32", dk, 128) for dk in range(144, 257, 16)]

@@ -206,10 +206,44 @@ def test_bf16_tensor_core_random_shapes(z, B, H, T, dk, dv, P, K):
     _assert(errs, "bf16", f"tc random B{B} H{H} T{T} dk{dk} dv{dv} P{P} K{K}")
 
 
-@pytest.mark.parametrize("dk,dv,C", [(192, 512, 64), (64, 128, 128)])
+@pytest.mark.parametrize("dk,dv", [(256, 512), (64, 128)])
+def test_bf16_chunk_128_runs_as_chunk_64_on_tensor_cores(z, dk, dv):
+    """A bf16 call asking for C = 128 is evaluated with the tensor-core kernels'
+    C = 64 (exact for any chunk length; a 128-token chunk's decay range implies
+    that of its halves): every kernel is a tensor-core one and every output is
+    bit-identical to the C = 64 call's, which the oracle checks."""
+    B, H, T, P, K = 1, 2, 2048, 2, 4
+    assert z.resolve_path(z.make_shape(B, H, T, dk, dv, P, K, 128, "bf16", "tc")) == "tc"
+    x = workloads.make_custom(B, H, T, dk, dv, dtype="bf16", seed=dk + dv, qk_scale=1 / 16,
+                              s0_scale=0.2)
+    names, r128 = parity.kernel_names(z, lambda: parity.run_gpu(z, x, P, K, 128))
+    assert "tc_bwd_dq" in names and not any(n.startswith("simt") for n in names), names
+    r64 = parity.run_gpu(z, x, P, K, 64)
+    for n in ("o", "S_final", "dq", "dk", "dv", "dlog_alpha", "dS0"):
+        assert torch.equal(r128[n], r64[n]), n
+    errs = parity.compare_full(z, x, P, K, 128, "bf16")
+    _assert(errs, "bf16", f"C = 128 as 64, dk {dk} dv {dv}")
+
+
+def test_bf16_chunk_128_off_the_tensor_core_grid_runs_as_chunk_64(z):
+    """d_k = 192, d_v = 96 at C = 128: the CUDA-core steps run at C = 64 too (a
+    128-token chunk would not fit their shared memory at this width): identical to
+    the C = 64 call and to the oracle."""
+    B, H, T, dk, dv, P, K = 1, 1, 1024, 192, 96, 2, 2
+    x = workloads.make_custom(B, H, T, dk, dv, dtype="bf16", seed=5, qk_scale=1 / 16,
+                              s0_scale=0.2)
+    r128 = parity.run_gpu(z, x, P, K, 128)
+    r64 = parity.run_gpu(z, x, P, K, 64)
+    for n in ("o", "S_final", "dq", "dk", "dv", "dlog_alpha", "dS0"):
+        assert torch.equal(r128[n], r64[n]), n
+    errs = parity.compare_full(z, x, P, K, 128, "bf16")
+    _assert(errs, "bf16", "C = 128 as 64, dk 192 dv 96")
+
+
+@pytest.mark.parametrize("dk,dv,C", [(192, 512, 64), (64, 128, 32)])
 def test_bf16_tensor_core_segment_states_with_cuda_core_sweeps(z, dk, dv, C):
     """Shapes whose segment states run on tensor cores (a partial d_k tile of 64
-    rows: d_k = 192, or d_k = 64 with C = 128) while the sweeps run on CUDA cores."""
+    rows: d_k = 192, or d_k = 64 with C = 32) while the sweeps run on CUDA cores."""
     shape = z.make_shape(1, 2, 2048, dk, dv, 2, 1, C, "bf16", "tc")
     assert z.resolve_path(shape) == "tc"
     x = workloads.make_custom(1, 2, 2048, dk, dv, dtype="bf16", seed=dk + dv + C,
@@ -398,9 +432,9 @@ def test_bf16_decay_forms_on_tensor_cores(z, decay, dk, dv):
 
 
 def test_bf16_scalar_decay_broadcast_on_tensor_core_path(z):
-    # C = 128: the tensor-core segment states, but the CUDA-core sweeps, which
+    # C = 32: the tensor-core segment states, but the CUDA-core sweeps, which
     # take the log-decay broadcast to [B,H,T,dk]
-    B, H, T, dk, dv, P, K, C = 1, 1, 1024, 128, 128, 2, 4, 128
+    B, H, T, dk, dv, P, K, C = 1, 1, 1024, 128, 128, 2, 4, 32
     shape = z.make_shape(B, H, T, dk, dv, P, K, C, "bf16", "tc", 1)
     assert z.resolve_path(shape) == "tc"
     x = workloads.make_custom(B, H, T, dk, dv, dtype="bf16", seed=41, qk_scale=1 / 16,
@@ -428,7 +462,7 @@ def test_bf16_scalar_decay_broadcast_on_tensor_core_path(z):
             "S_final": parity.err(parity.to_np(sf), rsf, "bf16")}
     for n in ("dq", "dk", "dv", "dS0", "dlog_alpha"):
         errs[n] = parity.err(parity.to_np(gr[n]), rg[n], "bf16")
-    _assert(errs, "bf16", "bf16 tc path, C = 128, scalar decay (broadcast)")
+    _assert(errs, "bf16", "bf16 tc path, C = 32, scalar decay (broadcast)")
 
 
 # ------------------------------------------------------------ segment counts
