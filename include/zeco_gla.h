@@ -40,9 +40,10 @@
  *     bf16 tensor-core products accumulate in fp32).
  *   - Every pointer is DEVICE memory owned by the caller and must be 16-byte
  *     aligned.  The library never allocates, never frees, never synchronises
- *     (except zeco_last_device_status, whose job it is) and never prints.  Work is enqueued on `stream` (NULL: the legacy default
- *     stream) and is asynchronous; outputs are valid once the stream reaches
- *     that point.  Calls that share `saved` or `workspace` must be ordered.
+ *     (except zeco_last_device_status, whose job it is) and never prints.
+ *     Work is enqueued on `stream` (NULL: the legacy default stream) and is
+ *     asynchronous; outputs are valid once the stream reaches that point.
+ *     Calls that share `saved` or `workspace` must be ordered.
  *   - Return value: ZECO_OK (0) or a negative ZECO_ERR_* code; nothing is
  *     enqueued when argument checks fail.  ZECO_ERR_CUDA means a launch failed
  *     (the CUDA error is left for cudaGetLastError of the caller's choosing).
@@ -157,8 +158,9 @@ size_t zeco_gla_saved_bytes(const zeco_shape *shape);
  * q .* dq - k .* dk that cancels heavily, so its terms are kept in fp32).
  * On the tensor-core path the backward also holds the masked gradient of the
  * intra-chunk scores dA = do v^T [B,H,T,64] bf16; where the dq/dk step runs on
- * CUDA cores (the SIMT path, and C != 64) it holds dA [B,H,T,C] fp32 instead.  Where the kernels read the
- * SCALAR / NONE decay forms in their own layout (see zeco_decay), SCALAR's
+ * CUDA cores (the SIMT path, and the tensor-core path's shapes whose sweeps run
+ * there: d_k = 192, C = 16 or 32) it holds dA [B,H,T,C] fp32 instead.  Where the kernels read the SCALAR / NONE decay forms in their own
+ * layout (see zeco_decay), SCALAR's
  * backward adds the fp32 partial sums of its gradient [dk/32][B,H,T] and NONE
  * adds nothing; elsewhere both forms add the log-decay broadcast to
  * [B,H,T,dk] (both directions) and its per-row gradient (backward).  Returns
