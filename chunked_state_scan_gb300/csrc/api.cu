@@ -58,11 +58,14 @@ int check_shape(const zeco_shape* s, Dims* d) {
   // Chunk length.  The chunked form is exact for any chunk length (results are
   // the token recurrence's, up to rounding), and a 128-token chunk's decay range
   // (the sum of log_alpha over a chunk above -80) implies that of its 64-token
-  // halves, so a bf16 call asking for C = 128 that does not force the CUDA-core
-  // path is evaluated with C = 64: the tensor-core kernels' chunk, and one the
-  // CUDA-core kernels' shared memory holds at every width.  (Shorter chunks are
-  // kept: their range may be what the caller needs.)
-  if (d->bf16 && s->path != ZECO_PATH_SIMT && s->C == 128) d->C = 64;
+  // halves, so a call asking for C = 128 that does not force the CUDA-core path
+  // is evaluated with C = 64 where that is what runs it: bf16 (the tensor-core
+  // kernels' chunk), and fp32 where a 128-token chunk does not fit the CUDA-core
+  // kernels' shared memory (d_k above 128).  (Shorter chunks are kept: their
+  // range may be what the caller needs.)
+  if (s->path != ZECO_PATH_SIMT && s->C == 128 &&
+      (d->bf16 || zeco::simt_smem_bytes(*d) > 227 * 1024))
+    d->C = 64;
   // Segments on one GPU.  The P segments of the method exchange their states
   // through the segment scan; the decomposition is exact for any split, so when
   // B*H*P is too small to give the chunk sweeps a wave of CTAs (one per 128 d_v

@@ -85,10 +85,11 @@ typedef enum { ZECO_F32 = 0, ZECO_BF16 = 1 } zeco_dtype;
  * path takes bf16 shapes whose d_k and d_v are multiples of 64: with C = 64 and
  * d_k in {64, 128, 256} every step of the forward and backward runs on tensor
  * cores; otherwise (d_k = 192, or C = 16 or 32) the segment states do, and the
- * chunk sweeps run on CUDA cores.  A bf16 call with C = 128 that is not forced
- * onto the SIMT path is evaluated with C = 64: results do not depend on C, and
- * the decay range of a 128-token chunk implies that of its halves (shorter
- * chunks are kept as asked). */
+ * chunk sweeps run on CUDA cores.  A call with C = 128 that is not forced onto
+ * the SIMT path is evaluated with C = 64 where that is what runs it (bf16; fp32
+ * with d_k above 128, where a 128-token chunk does not fit the SIMT kernels):
+ * results do not depend on C, and the decay range of a 128-token chunk implies
+ * that of its halves (shorter chunks are kept as asked). */
 typedef enum { ZECO_PATH_AUTO = 0, ZECO_PATH_SIMT = 1, ZECO_PATH_TC = 2 } zeco_path;
 
 /* Form of the decay (the ZeCO pages study the diagonal, per-d_k-row decay of

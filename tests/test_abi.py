@@ -276,19 +276,22 @@ def test_schedule_and_profiling_switches_on_the_host(lib):
     assert lib.zeco_profile_kernel_name(-1) is None
 
 
-def test_every_accepted_bf16_shape_runs_under_auto(lib):
-    """With path AUTO every bf16 width and chunk length the boundary accepts
-    resolves to a path (C = 128 runs at C = 64); fp32 at C = 128 with d_k above
-    128 does not fit the CUDA-core kernels' shared memory and is refused."""
+def test_every_accepted_shape_runs_under_auto(lib):
+    """With path AUTO every width and chunk length the boundary accepts resolves
+    to a path (C = 128 runs at C = 64 where that is what runs it); forcing the
+    CUDA-core path keeps C = 128, which its shared memory holds up to d_k = 128."""
     import chunked_state_scan_gb300 as z
-    refused = []
+    refused_auto, refused_simt = [], []
     for dtype in ("bf16", "f32"):
         for dk in range(16, 257, 16):
             for dv in range(32, 513, 32):
                 for C in (16, 32, 64, 128):
-                    try:
-                        z.resolve_path(_shape(dtype=dtype, T=16384, P=4, K=1, dk=dk, dv=dv, C=C))
-                    except z.ZecoError:
-                        refused.append((dtype, dk, C))
-    assert not [r for r in refused if r[0] == "bf16"], refused[:5]
-    assert sorted(set(refused)) == [("f32", dk, 128) for dk in range(144, 257, 16)]
+                    for path, out in (("auto", refused_auto), ("simt", refused_simt)):
+                        try:
+                            z.resolve_path(_shape(dtype=dtype, T=16384, P=4, K=1, dk=dk, dv=dv,
+                                                  C=C, path=path))
+                        except z.ZecoError:
+                            out.append((dtype, dk, C))
+    assert not refused_auto, refused_auto[:5]
+    assert sorted(set(refused_simt)) == sorted(
+        (dt, dk, 128) for dt in ("bf16", "f32") for dk in range(144, 257, 16))

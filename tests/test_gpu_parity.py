@@ -225,6 +225,23 @@ def test_bf16_chunk_128_runs_as_chunk_64_on_tensor_cores(z, dk, dv):
     _assert(errs, "bf16", f"C = 128 as 64, dk {dk} dv {dv}")
 
 
+def test_f32_chunk_128_beyond_the_cuda_core_width_runs_as_chunk_64(z):
+    """fp32 at d_k = 256 with C = 128: a 128-token chunk does not fit the CUDA-core
+    kernels' shared memory at this width, so the call runs at C = 64 (forcing the
+    SIMT path keeps C = 128 and is refused): identical to the C = 64 call and
+    within the fp32 tolerance of the oracle."""
+    B, H, T, dk, dv, P, K = 1, 1, 512, 256, 64, 2, 4
+    with pytest.raises(z.ZecoError):
+        z.resolve_path(z.make_shape(B, H, T, dk, dv, P, K, 128, "f32", "simt"))
+    x = workloads.make_custom(B, H, T, dk, dv, dtype="f32", seed=6, s0_scale=0.3)
+    r128 = parity.run_gpu(z, x, P, K, 128)
+    r64 = parity.run_gpu(z, x, P, K, 64)
+    for n in ("o", "S_final", "dq", "dk", "dv", "dlog_alpha", "dS0"):
+        assert torch.equal(r128[n], r64[n]), n
+    errs = parity.compare_full(z, x, P, K, 128, "f32")
+    _assert(errs, "f32", "f32 C = 128 as 64, dk 256")
+
+
 def test_bf16_chunk_128_off_the_tensor_core_grid_runs_as_chunk_64(z):
     """d_k = 192, d_v = 96 at C = 128: the CUDA-core steps run at C = 64 too (a
     128-token chunk would not fit their shared memory at this width): identical to
