@@ -11,7 +11,7 @@ L2 flush before every timed step).
 Timing: W untimed warm-up steps, then K timed steps bracketed by a barrier and
 torch.cuda.synchronize() on both sides, CUDA events on the library's stream,
 maximum over ranks.  N > 1 (torchrun) runs N independent replicas, one per GPU
-(weak scaling; the path has no cross-GPU exchange in this build).
+(weak scaling; the library has no cross-GPU exchange).
 
 Other modes: `--secondary` prints one line per secondary workload (GLA-1B layer
 forward, 8-segment forward, batched forward+backward); `--scan-sweep` times the
@@ -687,7 +687,7 @@ def measure(w, args, world, rank, local, want_e2e=True, want_cpu=True, quiet=Fal
         barrier(world)
         el = max_over_ranks(t1 - t0, world)
         ev, _ = aggregate(el, w.tokens, args.e2e_steps, world)
-        # the copy bound: a step cannot beat moving its bytes at the box's pinned
+        # the copy bound: a step cannot beat moving its bytes at this machine's pinned
         # copy rates (both directions at once), nor its own device time
         del dev_in, dev_out, out1, up_pieces, down_pieces
         torch.cuda.empty_cache()
