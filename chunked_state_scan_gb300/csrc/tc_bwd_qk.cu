@@ -43,7 +43,8 @@
 // products are accurate to ~2^-17; (2) the terms use the rounded operands that
 // the state itself was built from (the stored bf16 Q~ and K~ times the raw
 // accumulators), so that the identity's telescoping holds for the rounded model
-// instead of breaking on the rounding.
+// instead of breaking on the rounding.  The no-decay form has no dlog_alpha:
+// it writes and multiplies only the high part (9 MMAs per chunk instead of 17).
 //
 // Tensor memory (512 columns): the CTA's state block S[i][j] in fp32 (lane i,
 // column j) | two bf16 hi/lo copies of it (lane i; 64 columns of packed pairs
@@ -157,6 +158,9 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
                  int64_t L) {
   constexpr bool kDiag = FORM == ZECO_DECAY_DIAG, kScalar = FORM == ZECO_DECAY_SCALAR;
   constexpr bool kDecay = FORM != ZECO_DECAY_NONE;
+  // the low bf16 part of the state copy serves dlog_alpha's long suffix sums; the
+  // no-decay form has none, and its dq / dk need only the high part
+  constexpr int kParts = kDecay ? 2 : 1;
   // the second output of the sweep, stored by TMA: q.dq (forward, both decaying
   // forms), dlog_alpha (reverse, diagonal form)
   constexpr bool kAux = REV ? kDiag : kDecay;
@@ -296,7 +300,7 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
         umma_bf16(acc, sdesc_sw128(x0 + rank * 2048, kTile, 1024), pd, idP, 0u);
         const uint32_t hl = tmem + kColHL + 128 * b;
 #pragma unroll
-        for (int part = 0; part < 2; ++part)
+        for (int part = 0; part < kParts; ++part)
 #pragma unroll
           for (int m = 0; m < kNB / 16; ++m)
             umma_bf16_ta(acc, hl + 64 * part + 8 * m,
@@ -365,7 +369,7 @@ tc_bwd_qk_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
           lo[u] = *reinterpret_cast<const uint32_t*>(&l2);
         }
         tmem_st8(hl + 8 * qd, hi);
-        tmem_st8(hl + 64 + 8 * qd, lo);
+        if (kParts == 2) tmem_st8(hl + 64 + 8 * qd, lo);
       }
       tmem_st_wait();
     };
